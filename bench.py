@@ -1,0 +1,446 @@
+#!/usr/bin/env python
+"""Benchmark of the MSA hot path on GB300; prints ONE JSON line (rank 0).
+
+A step is one pass of the whole hot path over one batch of synthetic input:
+  prefill at N = 131072 tokens (index block scores -> per-group top-k selection -> sparse main
+  branch; H_q=32, H_kv=4, d_h=128, d_idx=64, block 64, k=16, 8 hot blocks), then
+  decode of 32 sequences with cache lengths ~ U[65536, 262144] (same head layout).
+`value` is prefill tokens/s (N / prefill device time); decode tokens/s is reported beside it.
+Inputs stay resident in HBM; every timed input (M alone is 4.3 GB, the decode caches 11.5 GB)
+is larger than the 129 MB L2, so no flush is needed.
+
+--impl reference times the CPU oracle (the plain fp64 restatement of the formulas) on bounded
+samples of the same prefill workload, on this host's cores.
+Multi-process (torchrun): every rank runs its own replica of the workload on its own GPU
+(weak scaling, no collective on the data path); times are max-reduced.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import gen  # noqa: E402
+
+METRIC = ("MSA prefill tokens/s and decode tokens/s at 128K ctx; % of bf16 TC / HBM roofline")
+LAUNCHES_PER_STEP = 7       # scores, select, attention; decode: scores, select, attention, merge
+KERNEL_FILES = {"k_index_block_scores": "k_score.cu", "k_select_prefill": "k_select.cu",
+                "k_sparse_attn": "k_attn.cu", "decode": "k_decode.cu"}
+
+
+# ------------------------------------------------------------------------ helpers --
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        p = json.load(open(path))
+        return dict(hbm=p["hbm_gbs"], bf16=p["bf16_tflops"],
+                    bf16_sust=p.get("bf16_tflops_sustained", p["bf16_tflops"]), src="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sust=1700.0, src="fallback")
+
+
+def kernel_source_hash(fname):
+    return hashlib.sha256(open(os.path.join(ROOT, "block_sparse_gqa_scores_gb300", "csrc",
+                                            fname), "rb").read()).hexdigest()[:16]
+
+
+def ncu_traffic(kernel):
+    """DRAM bytes per launch of a kernel from the last ncu capture, if the kernel source is
+    unchanged since (profiles/traffic.json records the source hash it was taken on)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    rec = json.load(open(path)).get(kernel)
+    if not rec or rec.get("source_sha") != kernel_source_hash(KERNEL_FILES[kernel]):
+        return None
+    return rec.get("bytes_per_launch")
+
+
+class Clocks:
+    """nvidia-smi samples (200 ms) of this GPU's clocks and throttle reasons."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.proc = None
+        self.path = None
+        self.gpu = gpu_index
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        self.proc.wait()
+        rows = []
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) == 7:
+                rows.append(f)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[0]) for r in rows if r[0].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for r in rows for k in range(4) if r[3 + k] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": float(rows[0][1]) if rows[0][1].replace(".", "").isdigit() else None,
+                "samples": len(rows), "reasons": reasons}
+
+
+# ----------------------------------------------------------------------- workload --
+
+def workload_sizes(pcfg, dcfg, lens):
+    N, Hq, Hkv, dh, di, k = pcfg.N, pcfg.H_q, pcfg.H_kv, pcfg.d_h, pcfg.d_idx, pcfg.k
+    i = np.arange(N, dtype=np.float64)
+    T = np.minimum(i + 1, (k - 1) * 64 + (i % 64) + 1)                # |T_i|
+    nvis = np.minimum(i // 64, np.inf)                                  # blocks b < l read
+    out = dict(
+        F_idx=2.0 * di * Hkv * N * (N + 1) / 2,
+        F_main=4.0 * dh * Hq * T.sum(),
+        select_bytes=4.0 * Hkv * nvis.sum() + 4.0 * Hkv * N * k,
+    )
+    # decode algorithmic bytes: the index-key stream + selected visible K/V + small vectors
+    dbytes = 0.0
+    for L in lens:
+        ii = L - 1
+        Tt = min(ii + 1, (dcfg.k - 1) * 64 + (ii % 64) + 1)
+        dbytes += 2.0 * dcfg.d_idx * L + 2.0 * 2 * dcfg.H_kv * dcfg.d_h * Tt
+        dbytes += 2.0 * (2 * dcfg.H_q * dcfg.d_h + dcfg.H_kv * dcfg.d_idx) + 4.0 * dcfg.H_q
+    out["decode_bytes"] = dbytes
+    return out
+
+
+def setup(pcfg, dcfg, seed=0):
+    msa = __import__("block_sparse_gqa_scores_gb300")
+    x = gen.prefill_inputs(pcfg, seed=seed, device="cuda")
+    N = pcfg.N
+    nblk = -(-N // 64)
+    bufs = dict(
+        M=torch.empty((pcfg.H_kv, N, nblk), dtype=torch.float32, device="cuda"),
+        idx=torch.empty((pcfg.H_kv, N, pcfg.k), dtype=torch.int32, device="cuda"),
+        o=torch.empty_like(x["q"]),
+        lse=torch.empty((pcfg.H_q, N), dtype=torch.float32, device="cuda"),
+    )
+    d = gen.decode_inputs(dcfg, seed=seed, device="cuda")
+    max_len = dcfg.len_hi
+    nws = msa.msa_sparse_decode_workspace(dcfg.S, max_len, dcfg.H_q, dcfg.H_kv, dcfg.d_h,
+                                          dcfg.d_idx, dcfg.k)
+    dbufs = dict(o=torch.empty_like(d["q"]),
+                 lse=torch.empty((dcfg.S, dcfg.H_q), dtype=torch.float32, device="cuda"),
+                 idx=torch.empty((dcfg.S, dcfg.H_kv, dcfg.k), dtype=torch.int32, device="cuda"),
+                 ws=torch.empty(nws, dtype=torch.uint8, device="cuda"), max_len=max_len)
+    return msa, x, bufs, d, dbufs
+
+
+def run_msa(args, world, rank, local):
+    pcfg, dcfg = gen.CONFIGS[args.prefill], gen.CONFIGS[args.decode]
+    msa, x, bufs, d, dbufs = setup(pcfg, dcfg, seed=args.seed + rank)
+    stream = torch.cuda.current_stream()
+    N = pcfg.N
+
+    def prefill():
+        msa.msa_index_block_scores(x["q_idx"], x["k_idx"], M=bufs["M"])
+        ev[1].record(stream)
+        msa.msa_select_blocks(bufs["M"], N, pcfg.k, idx=bufs["idx"])
+        ev[2].record(stream)
+        msa.msa_sparse_attn_fwd(x["q"], x["k"], x["v"], bufs["idx"], o=bufs["o"], lse=bufs["lse"])
+
+    def decode():
+        msa.msa_sparse_decode(d["q"], d["q_idx"], d["k_cache"], d["v_cache"], d["k_idx_cache"],
+                              d["cu_seqlens"], dbufs["max_len"], dcfg.k, o=dbufs["o"],
+                              lse=dbufs["lse"], idx_out=dbufs["idx"], ws=dbufs["ws"])
+
+    K, W = args.steps, args.warmup
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+    for _ in range(W):
+        ev[0].record(stream)
+        prefill()
+        ev[3].record(stream)
+        decode()
+        ev[4].record(stream)
+    torch.cuda.synchronize()
+    msa.msa_device_status()
+
+    clocks = Clocks(local)
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for s in range(K):
+        ev = evs[s]
+        ev[0].record(stream)
+        prefill()
+        ev[3].record(stream)
+        decode()
+        ev[4].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    barrier(world)
+    msa.msa_device_status()
+
+    per = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(4)] for e in evs])   # ms
+    t_score, t_select, t_attn, t_decode = per.mean(axis=0)
+    t_prefill_total = max_over_ranks(float(per[:, :3].sum()), world)   # ms over K steps
+    t_decode_total = max_over_ranks(float(per[:, 3].sum()), world)
+    t_all = max_over_ranks(t_start.elapsed_time(t_end), world)
+
+    sizes = workload_sizes(pcfg, dcfg, d["meta"]["lens"])
+    pk = peaks()
+    kern = []
+
+    def add(name, ms, bound, work, unit, peak, traffic=None):
+        achieved = work / (ms * 1e-3) / (1e12 if unit == "TFLOP/s" else 1e9)
+        kern.append({"kernel": name, "ms": round(ms, 4), "bound": bound,
+                     "achieved": round(achieved, 2), "peak": peak, "unit": unit,
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "algorithmic": work})
+
+    add("k_index_block_scores", t_score, "tensor", sizes["F_idx"], "TFLOP/s", pk["bf16_sust"],
+        ncu_traffic("k_index_block_scores"))
+    add("k_select_prefill", t_select, "hbm", sizes["select_bytes"], "GB/s", pk["hbm"],
+        ncu_traffic("k_select_prefill"))
+    add("k_sparse_attn", t_attn, "tensor", sizes["F_main"], "TFLOP/s", pk["bf16_sust"],
+        ncu_traffic("k_sparse_attn"))
+    add("decode (4 kernels)", t_decode, "hbm", sizes["decode_bytes"], "GB/s", pk["hbm"],
+        ncu_traffic("decode"))
+    dom = max(kern, key=lambda r: r["ms"])
+
+    value = world * N * K / (t_prefill_total * 1e-3)
+    dec_value = world * dcfg.S * K / (t_decode_total * 1e-3)
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
+        "steps": K, "warmup": W, "ms_per_step": round(t_all / K, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {
+            "workload": "prefill N=%d + decode %d seqs L~U[%d,%d]" % (N, dcfg.S, dcfg.len_lo,
+                                                                     dcfg.len_hi),
+            "prefill": {"N": N, "H_q": pcfg.H_q, "H_kv": pcfg.H_kv, "d_h": pcfg.d_h,
+                        "d_idx": pcfg.d_idx, "block": 64, "k": pcfg.k,
+                        "hot_blocks": pcfg.hot_blocks, "block_offset_std": pcfg.block_offset_std},
+            "decode": {"S": dcfg.S, "len_lo": dcfg.len_lo, "len_hi": dcfg.len_hi,
+                       "mean_len": float(np.mean(d["meta"]["lens"])), "k": dcfg.k},
+            "l2": "no flush: every timed input exceeds the 129 MB L2 (M 4.3 GB, caches 11.5 GB)",
+            "parallelism": "replicas" if world > 1 else "single",
+        },
+        "ms_prefill": round(t_prefill_total / K, 4),
+        "ms_decode": round(t_decode_total / K, 4),
+        "decode": {"value": round(dec_value, 1), "unit": "tokens/s",
+                   "ms": round(t_decode_total / K, 4)},
+        "kernels": kern,
+        "roofline": {"kernel": dom["kernel"], "bound": dom["bound"], "achieved": dom["achieved"],
+                     "peak": dom["peak"], "unit": dom["unit"], "frac": dom["frac"],
+                     "traffic": dom["traffic"],
+                     "peak_source": "%s (%s)" % (pk["src"], "bf16 sustained" if dom["unit"] ==
+                                                 "TFLOP/s" else "HBM copy")},
+        "clocks": clk,
+        "gpu_launches": LAUNCHES_PER_STEP * K,
+    }
+    if not args.no_e2e:
+        line["e2e"] = e2e_prefill(msa, pcfg, x, bufs, K, W, world)
+    if not args.no_cpu_baseline and rank == 0 and world == 1:
+        line["cpu_baseline"] = cpu_baseline(pcfg, x, args.cpu_seconds, args.seed)
+    return line
+
+
+def e2e_prefill(msa, pcfg, x, bufs, K, W, world):
+    """Prefill through the public calls with host (pinned) inputs and outputs: H2D of
+    Q, K, V, Q_idx, K_idx, the three calls, D2H of O and LSE -- all inside the timed region."""
+    names = ["q", "k", "v", "q_idx", "k_idx"]
+    host = {n: torch.empty(x[n].shape, dtype=x[n].dtype, pin_memory=True) for n in names}
+    for n in names:
+        host[n].copy_(x[n])
+    dev = {n: torch.empty_like(x[n]) for n in names}
+    o_h = torch.empty(bufs["o"].shape, dtype=bufs["o"].dtype, pin_memory=True)
+    l_h = torch.empty(bufs["lse"].shape, dtype=bufs["lse"].dtype, pin_memory=True)
+    N = pcfg.N
+
+    def step():
+        for n in names:
+            dev[n].copy_(host[n], non_blocking=True)
+        M = msa.msa_index_block_scores(dev["q_idx"], dev["k_idx"], M=bufs["M"])
+        idx = msa.msa_select_blocks(M, N, pcfg.k, idx=bufs["idx"])
+        msa.msa_sparse_attn_fwd(dev["q"], dev["k"], dev["v"], idx, o=bufs["o"], lse=bufs["lse"])
+        o_h.copy_(bufs["o"], non_blocking=True)
+        l_h.copy_(bufs["lse"], non_blocking=True)
+
+    for _ in range(W):
+        step()
+    torch.cuda.synchronize()
+    barrier(world)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(K):
+        step()
+    b.record()
+    torch.cuda.synchronize()
+    t = max_over_ranks(a.elapsed_time(b), world)
+    h2d = sum(host[n].numel() * host[n].element_size() for n in names)
+    d2h = o_h.numel() * o_h.element_size() + l_h.numel() * l_h.element_size()
+    del dev, host
+    return {"value": round(world * N * K / (t * 1e-3), 1), "unit": "tokens/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": round(t / K, 4)}
+
+
+def cpu_sample_rows(N, n, seed):
+    rng = np.random.default_rng(seed)
+    return np.sort(rng.choice(N, size=n, replace=False)).astype(np.int64)
+
+
+def oracle_rows_rate(pcfg, xh, seconds, seed, max_rows=4096, batch=16):
+    """Times the oracle's whole prefill path on uniformly sampled query rows until about
+    `seconds` of CPU work; returns (rows/s, rows, threads)."""
+    import oracle
+    oracle.build()
+    rows_all = cpu_sample_rows(pcfg.N, max_rows, seed)
+    done, t = 0, 0.0
+    while t < seconds and done < max_rows:
+        rows = rows_all[done:done + batch]
+        qr = np.ascontiguousarray(xh["q"][rows])
+        qir = np.ascontiguousarray(xh["q_idx"][rows])
+        t0 = time.perf_counter()
+        oracle.prefill(qr, xh["k"], xh["v"], qir, xh["k_idx"], pcfg.k, rows=rows, compact=True)
+        t += time.perf_counter() - t0
+        done += len(rows)
+    return done / t, done, oracle.get_threads()
+
+
+def host_bits(x, names=("k", "v", "k_idx")):
+    out = {n: gen.to_bits(x[n]) for n in names}
+    return out
+
+
+def cpu_baseline(pcfg, x, seconds, seed):
+    xh = host_bits(x)
+    xh["q"] = gen.to_bits(x["q"])
+    xh["q_idx"] = gen.to_bits(x["q_idx"])
+    rate, rows, cores = oracle_rows_rate(pcfg, xh, seconds, seed)
+    return {"value": round(rate, 3), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": "%d uniformly sampled query rows of the N=%d prefill workload, whole path "
+                      "(causal index scores, selection, main branch), fp64" % (rows, pcfg.N)}
+
+
+def run_reference(args, world, rank):
+    """The CPU oracle as the reference arm, on bounded samples of the prefill workload."""
+    if rank != 0:
+        return None
+    pcfg = gen.CONFIGS[args.prefill]
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    x = gen.prefill_inputs(pcfg, seed=args.seed, device=dev)
+    xh = host_bits(x, ("q", "k", "v", "q_idx", "k_idx"))
+    del x
+    per_step = max(1.0, args.cpu_seconds / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        oracle_rows_rate(pcfg, xh, per_step / 4, args.seed, batch=8)
+    rates, total_rows = [], 0
+    t0 = time.perf_counter()
+    for s in range(args.steps):
+        rate, rows, cores = oracle_rows_rate(pcfg, xh, per_step, args.seed + 1 + s, batch=8)
+        rates.append(rate)
+        total_rows += rows
+    elapsed = time.perf_counter() - t0
+    value = float(np.mean(rates))
+    return {"metric": METRIC, "impl": "reference", "value": round(value, 3), "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 * elapsed / args.steps, 2), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "prefill N=%d (sampled query rows)" % pcfg.N},
+            "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": cores,
+                             "kind": "oracle",
+                             "sample": "%d uniformly sampled query rows per run of the N=%d "
+                                       "prefill workload, whole path, fp64" % (total_rows //
+                                                                              args.steps, pcfg.N)},
+            "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["msa", "reference"], default="msa")
+    ap.add_argument("--prefill", default="p128k")
+    ap.add_argument("--decode", default="decode")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "msa":
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        line = run_reference(args, world, rank)
+    else:
+        line = run_msa(args, world, rank, local)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

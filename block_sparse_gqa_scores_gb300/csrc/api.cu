@@ -1,0 +1,191 @@
+// C ABI of libmsa: host-side validation, workspace layout and dispatch to the kernels.
+// Nothing here allocates device memory or synchronises, except msa_device_status().
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "../../include/msa.h"
+#include "msa_internal.h"
+
+#define MSA_API extern "C" __attribute__((visibility("default")))
+
+namespace msa {
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+cudaError_t make_tma_2d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                             int box_inner, int box_outer, int swizzle_bytes) {
+  auto fn = encode_fn();
+  if (!fn) return cudaErrorNotSupported;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {inner * 2};
+  cuuint32_t box[2] = {(cuuint32_t)box_inner, (cuuint32_t)box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  const CUtensorMapSwizzle sw = swizzle_bytes == 128  ? CU_TENSOR_MAP_SWIZZLE_128B
+                                : swizzle_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                                      : CU_TENSOR_MAP_SWIZZLE_NONE;
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+}  // namespace msa
+
+namespace {
+
+constexpr int64_t kMaxRows = (int64_t)1 << 31;   // TMA coordinates and grid.x are 32-bit
+
+bool aligned16(const void* p) { return p && ((uintptr_t)p & 15u) == 0; }
+bool aligned4(const void* p) { return p && ((uintptr_t)p & 3u) == 0; }
+bool pow2_upto(int x, int hi) { return x >= 1 && x <= hi && (x & (x - 1)) == 0; }
+
+msa_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? MSA_OK : MSA_ERR_CUDA; }
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct DecodeWs {
+  size_t off_m, off_idx, off_po, off_pl, total;
+  int nsplit;
+};
+
+DecodeWs decode_layout(int S, int64_t max_len, int H_q, int H_kv, int d_h, int k) {
+  DecodeWs w{};
+  const int64_t nblk = (max_len + 63) / 64;
+  const int G = H_q / H_kv;
+  w.nsplit = k < 4 ? k : 4;
+  size_t off = 0;
+  w.off_m = off;
+  off = align256(off + sizeof(float) * (size_t)S * H_kv * nblk);
+  w.off_idx = off;
+  off = align256(off + sizeof(int32_t) * (size_t)S * H_kv * k);
+  w.off_po = off;
+  off = align256(off + sizeof(float) * (size_t)S * H_kv * w.nsplit * G * d_h);
+  w.off_pl = off;
+  off = align256(off + sizeof(float) * (size_t)S * H_kv * w.nsplit * G);
+  w.total = off;
+  return w;
+}
+
+}  // namespace
+
+MSA_API const char* msa_status_string(msa_status_t s) {
+  switch (s) {
+    case MSA_OK: return "MSA_OK";
+    case MSA_ERR_INVALID_ARGUMENT: return "MSA_ERR_INVALID_ARGUMENT";
+    case MSA_ERR_UNSUPPORTED: return "MSA_ERR_UNSUPPORTED";
+    case MSA_ERR_WORKSPACE: return "MSA_ERR_WORKSPACE";
+    case MSA_ERR_CUDA: return "MSA_ERR_CUDA";
+    case MSA_ERR_TIMEOUT: return "MSA_ERR_TIMEOUT";
+  }
+  return "MSA_ERR_UNKNOWN";
+}
+
+MSA_API msa_status_t msa_index_block_scores(const void* q_idx, const void* k_idx, float* M,
+                                            int64_t N, int H_kv, int d_idx, int block_size,
+                                            int64_t q_start, int64_t q_count, void* stream) {
+  if (!aligned16(q_idx) || !aligned16(k_idx) || !aligned16(M)) return MSA_ERR_INVALID_ARGUMENT;
+  if (N < 1 || H_kv < 1 || d_idx < 1 || block_size != 64) return MSA_ERR_INVALID_ARGUMENT;
+  if (q_start < 0 || q_count < 1 || q_start + q_count > N) return MSA_ERR_INVALID_ARGUMENT;
+  if (!pow2_upto(H_kv, 8) || (d_idx != 32 && d_idx != 64)) return MSA_ERR_UNSUPPORTED;
+  if (N * H_kv >= kMaxRows) return MSA_ERR_UNSUPPORTED;
+  return from_cuda(msa::launch_index_block_scores(q_idx, k_idx, M, N, H_kv, d_idx, q_start,
+                                                  q_count, (cudaStream_t)stream));
+}
+
+MSA_API msa_status_t msa_select_blocks(const float* M, int32_t* idx, int64_t N, int H_kv,
+                                       int block_size, int k, int64_t q_start, int64_t q_count,
+                                       void* stream) {
+  if (!aligned16(M) || !aligned4(idx)) return MSA_ERR_INVALID_ARGUMENT;
+  if (N < 1 || H_kv < 1 || block_size != 64 || k < 1 || k > 64) return MSA_ERR_INVALID_ARGUMENT;
+  if (q_start < 0 || q_count < 1 || q_start + q_count > N) return MSA_ERR_INVALID_ARGUMENT;
+  if (!pow2_upto(H_kv, 8)) return MSA_ERR_UNSUPPORTED;
+  if (N * H_kv >= kMaxRows) return MSA_ERR_UNSUPPORTED;
+  return from_cuda(
+      msa::launch_select_prefill(M, idx, N, H_kv, k, q_start, q_count, (cudaStream_t)stream));
+}
+
+MSA_API size_t msa_sparse_attn_fwd_workspace(int64_t N, int H_q, int H_kv, int d_h, int k) {
+  (void)N, (void)H_q, (void)H_kv, (void)d_h, (void)k;
+  return 0;
+}
+
+MSA_API msa_status_t msa_sparse_attn_fwd(const void* q, const void* k, const void* v,
+                                         const int32_t* idx, void* o, float* lse, int64_t N,
+                                         int H_q, int H_kv, int d_h, int block_size, int k_blocks,
+                                         void* ws, size_t ws_bytes, void* stream) {
+  (void)ws;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned4(idx) || !aligned16(o) ||
+      !aligned4(lse))
+    return MSA_ERR_INVALID_ARGUMENT;
+  if (N < 1 || H_q < 1 || H_kv < 1 || H_q % H_kv != 0 || d_h < 1 || block_size != 64 ||
+      k_blocks < 1 || k_blocks > 64)
+    return MSA_ERR_INVALID_ARGUMENT;
+  if (!pow2_upto(H_kv, 8) || !pow2_upto(H_q / H_kv, 8) || (d_h != 64 && d_h != 128))
+    return MSA_ERR_UNSUPPORTED;
+  if (N * H_kv >= kMaxRows) return MSA_ERR_UNSUPPORTED;
+  if (ws_bytes < msa_sparse_attn_fwd_workspace(N, H_q, H_kv, d_h, k_blocks))
+    return MSA_ERR_WORKSPACE;
+  return from_cuda(msa::launch_sparse_attn_prefill(q, k, v, idx, o, lse, N, H_q, H_kv, d_h,
+                                                   k_blocks, (cudaStream_t)stream));
+}
+
+MSA_API size_t msa_sparse_decode_workspace(int S, int64_t max_len, int H_q, int H_kv, int d_h,
+                                           int d_idx, int k) {
+  (void)d_idx;
+  if (S < 1 || max_len < 1 || H_kv < 1 || H_q < H_kv || k < 1) return 0;
+  return decode_layout(S, max_len, H_q, H_kv, d_h, k).total;
+}
+
+MSA_API msa_status_t msa_sparse_decode(const void* q, const void* q_idx, const void* k_cache,
+                                       const void* v_cache, const void* k_idx_cache,
+                                       const int64_t* cu_seqlens, int S, int64_t max_len, int H_q,
+                                       int H_kv, int d_h, int d_idx, int block_size, int k,
+                                       void* o, float* lse, int32_t* idx_out, void* ws,
+                                       size_t ws_bytes, void* stream) {
+  if (!aligned16(q) || !aligned16(q_idx) || !aligned16(k_cache) || !aligned16(v_cache) ||
+      !aligned16(k_idx_cache) || !cu_seqlens || ((uintptr_t)cu_seqlens & 7u) || !aligned16(o) ||
+      !aligned4(lse) || (idx_out && !aligned4(idx_out)) || !aligned16(ws))
+    return MSA_ERR_INVALID_ARGUMENT;
+  if (S < 1 || S > 65535 || max_len < 1 || H_q < 1 || H_kv < 1 || H_q % H_kv != 0 ||
+      block_size != 64 || k < 1 || k > 64 || d_h < 1 || d_idx < 1)
+    return MSA_ERR_INVALID_ARGUMENT;
+  if (!pow2_upto(H_kv, 8) || !pow2_upto(H_q / H_kv, 8) || (d_h != 64 && d_h != 128) ||
+      (d_idx != 32 && d_idx != 64))
+    return MSA_ERR_UNSUPPORTED;
+  const DecodeWs w = decode_layout(S, max_len, H_q, H_kv, d_h, k);
+  if (ws_bytes < w.total) return MSA_ERR_WORKSPACE;
+  cudaStream_t st = (cudaStream_t)stream;
+  char* base = static_cast<char*>(ws);
+  float* Mdec = reinterpret_cast<float*>(base + w.off_m);
+  int32_t* idx = idx_out ? idx_out : reinterpret_cast<int32_t*>(base + w.off_idx);
+  float* part_o = reinterpret_cast<float*>(base + w.off_po);
+  float* part_lse = reinterpret_cast<float*>(base + w.off_pl);
+  const int64_t nblk = (max_len + 63) / 64;
+  cudaError_t e = msa::launch_decode_block_scores(q_idx, k_idx_cache, cu_seqlens, Mdec, S, H_kv,
+                                                  d_idx, max_len, nblk, st);
+  if (e != cudaSuccess) return MSA_ERR_CUDA;
+  e = msa::launch_select_decode(Mdec, idx, cu_seqlens, S, H_kv, k, max_len, nblk, st);
+  if (e != cudaSuccess) return MSA_ERR_CUDA;
+  e = msa::launch_sparse_attn_decode(q, k_cache, v_cache, idx, cu_seqlens, S, max_len, H_q, H_kv,
+                                     d_h, k, w.nsplit, part_o, part_lse, o, lse, st);
+  return from_cuda(e);
+}
+
+MSA_API msa_status_t msa_device_status(void) {
+  unsigned v = 0;
+  if (msa::read_reset_score_status(&v) != cudaSuccess) return MSA_ERR_CUDA;
+  return v ? MSA_ERR_TIMEOUT : MSA_OK;
+}

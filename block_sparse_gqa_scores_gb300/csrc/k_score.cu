@@ -1,0 +1,303 @@
+// Index branch of MSA on sm_103a: causal token scores Q_idx . K_idx^T / sqrt(d_idx) with the
+// per-block max-pool fused into the epilogue («MiniMax-M3：MSA 技术报告速读», section 索引分支,
+// eqs. S^idx and M^idx).
+//
+// One dense GEMM  [N*H_kv x d_idx] . [d_idx x N]  restricted to the causal triangle:
+//   * rows are (query i, group r) pairs, i.e. Q_idx viewed as [N*H_kv, d_idx]; 128 consecutive
+//     rows (128/H_kv queries x H_kv groups) form one UMMA M=128 sub-tile, and SUB sub-tiles
+//     share every K_idx tile, so the shared index key is read once for all groups.
+//   * K_idx tiles of 128 keys (two 64-token blocks) stream through a 4-deep TMA ring.
+//   * one thread issues tcgen05.mma (bf16 x bf16 -> fp32) into a double-buffered TMEM
+//     accumulator; the next tile's MMA overlaps the epilogue of the previous one.
+//   * epilogue warps tcgen05.ld 64 columns (= one block) per row, mask j > i on the
+//     diagonal block, max-reduce with 3-input max, scale once, and stage 32 blocks per row
+//     in shared memory before one coalesced 128-byte store per row.
+//   * blocks after a row's own block are written as -inf.
+// Warp roles: warp 0 = TMA producer, warp 1 = TMEM allocator + MMA issuer,
+// warps 2.. = 4*SUB epilogue warps (warp w reads TMEM lanes 32*(w%4) .. +31).
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <mutex>
+
+#include "msa_device.cuh"
+#include "msa_internal.h"
+
+namespace msa {
+namespace {
+
+__device__ unsigned g_score_status = 0;
+
+constexpr int kRows = 128;     // UMMA M: rows per sub-tile
+constexpr int kKeys = 128;     // UMMA N: keys per tile
+constexpr int kStages = 4;     // K_idx ring depth
+constexpr int kGroupBlocks = 32;   // blocks staged per row before a store
+constexpr int kTilesPerGroup = kGroupBlocks / (kKeys / kBlock);
+
+template <int D_IDX, int SUB>
+struct ScoreSmem {
+  static constexpr int kABytes = kRows * D_IDX * 2;
+  static constexpr int kBBytes = kKeys * D_IDX * 2;
+  static constexpr int kEpiWarps = 4 * SUB;
+  static constexpr int kStageFloats = 32 * 33;        // 32 rows x 32 blocks, padded
+  static constexpr int kOffA = 0;
+  static constexpr int kOffB = kOffA + SUB * kABytes;
+  static constexpr int kOffStage = kOffB + kStages * kBBytes;
+  static constexpr int kOffBar = kOffStage + kEpiWarps * kStageFloats * 4;
+  // barriers: full_a, full_b[kStages], empty_b[kStages], tfull[2], tempty[2], done
+  static constexpr int kNumBars = 1 + 2 * kStages + 4 + 1;
+  static constexpr int kOffTmem = kOffBar + kNumBars * 8;
+  static constexpr int kBytes = kOffTmem + 16;
+  static constexpr int kAlloc = kBytes + 1024;
+  static constexpr int kThreads = 64 + 32 * kEpiWarps;
+  static constexpr uint32_t kTmemCols = 2 * SUB * kKeys;
+  static_assert(kTmemCols <= 512, "TMEM has 512 columns");
+  static_assert(kOffB % 1024 == 0 && kOffStage % 1024 == 0, "1024-B aligned swizzle atoms");
+};
+
+__device__ __forceinline__ float max64(const uint32_t* v) {
+  float m0 = fmax3(__uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]));
+  float m1 = fmax3(__uint_as_float(v[3]), __uint_as_float(v[4]), __uint_as_float(v[5]));
+  float m2 = fmax3(__uint_as_float(v[6]), __uint_as_float(v[7]), __uint_as_float(v[8]));
+  float m3 = fmax3(__uint_as_float(v[9]), __uint_as_float(v[10]), __uint_as_float(v[11]));
+#pragma unroll
+  for (int c = 12; c < 60; c += 8) {
+    m0 = fmax3(m0, __uint_as_float(v[c + 0]), __uint_as_float(v[c + 1]));
+    m1 = fmax3(m1, __uint_as_float(v[c + 2]), __uint_as_float(v[c + 3]));
+    m2 = fmax3(m2, __uint_as_float(v[c + 4]), __uint_as_float(v[c + 5]));
+    m3 = fmax3(m3, __uint_as_float(v[c + 6]), __uint_as_float(v[c + 7]));
+  }
+  m0 = fmax3(m0, __uint_as_float(v[60]), __uint_as_float(v[61]));
+  m1 = fmax3(m1, __uint_as_float(v[62]), __uint_as_float(v[63]));
+  return fmax3(m0, m1, fmaxf(m2, m3));
+}
+
+template <int D_IDX, int SUB>
+__global__ void __launch_bounds__(ScoreSmem<D_IDX, SUB>::kThreads, 1)
+    k_index_block_scores(const __grid_constant__ CUtensorMap tm_q,
+                         const __grid_constant__ CUtensorMap tm_k, float* __restrict__ M,
+                         int log2_hkv, int64_t q_start, int64_t q_count, int64_t nblk,
+                         float scale) {
+  using L = ScoreSmem<D_IDX, SUB>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+  const uint32_t sbase = smem_u32(smem);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int H_kv = 1 << log2_hkv;
+  const int QT = kRows >> log2_hkv;                      // queries per sub-tile
+  const int64_t per_cta = (int64_t)SUB * QT;
+  const int64_t n_super = (q_count + per_cta - 1) / per_cta;
+  const int64_t st = n_super - 1 - blockIdx.x;           // heaviest (latest) tiles first
+  const int64_t i0 = q_start + st * per_cta;
+  const int64_t i_end = min(i0 + per_cta, q_start + q_count);
+  const int nkt = (int)((i_end - 1) / kKeys) + 1;         // key tiles covering [0, i_end)
+  const int64_t R0 = i0 << log2_hkv;                      // first (query, group) row
+
+  const uint32_t bar0 = sbase + L::kOffBar;
+  const uint32_t full_a = bar0;
+  auto full_b = [&](int s) { return bar0 + 8u * (1 + s); };
+  auto empty_b = [&](int s) { return bar0 + 8u * (1 + kStages + s); };
+  auto tfull = [&](int a) { return bar0 + 8u * (1 + 2 * kStages + a); };
+  auto tempty = [&](int a) { return bar0 + 8u * (3 + 2 * kStages + a); };
+  const uint32_t done_bar = bar0 + 8u * (5 + 2 * kStages);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffTmem);
+
+  if (threadIdx.x == 0) {
+    mbar_init(full_a, 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(full_b(s), 1);
+      mbar_init(empty_b(s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull(a), 1);
+      mbar_init(tempty(a), L::kEpiWarps);
+    }
+    mbar_init(done_bar, 1);
+    fence_barrier_init();
+  }
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), L::kTmemCols);
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      prefetch_tensormap(&tm_q);
+      prefetch_tensormap(&tm_k);
+      mbar_expect_tx(full_a, SUB * L::kABytes);
+      for (int s = 0; s < SUB; ++s)
+        tma_load_2d(sbase + L::kOffA + s * L::kABytes, &tm_q, full_a, 0, (int)(R0 + s * kRows));
+      int last_round[kStages];
+      for (int s = 0; s < kStages; ++s) last_round[s] = -1;
+      for (int kt = 0; kt < nkt; ++kt) {
+        const int stg = kt % kStages, round = kt / kStages;
+        if (!mbar_wait(empty_b(stg), (round & 1) ^ 1, &g_score_status)) break;
+        mbar_expect_tx(full_b(stg), L::kBBytes);
+        tma_load_2d(sbase + L::kOffB + stg * L::kBBytes, &tm_k, full_b(stg), 0, kt * kKeys);
+        last_round[stg] = round;
+      }
+      // never leave the CTA with a copy in flight
+      mbar_wait(full_a, 0, &g_score_status);
+      for (int s = 0; s < kStages; ++s)
+        if (last_round[s] >= 0) mbar_wait(full_b(s), last_round[s] & 1, &g_score_status);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = umma_idesc_bf16(kRows, kKeys);
+      constexpr uint32_t sbo = 8 * D_IDX * 2;            // 8 rows of one swizzle atom
+      constexpr int swz = D_IDX * 2;                     // 128-B or 64-B swizzle rows
+      if (mbar_wait(full_a, 0, &g_score_status)) {
+        tc_fence_after();
+        for (int kt = 0; kt < nkt; ++kt) {
+          const int stg = kt % kStages, round = kt / kStages;
+          const int acc = kt & 1, use = kt >> 1;
+          if (!mbar_wait(tempty(acc), (use & 1) ^ 1, &g_score_status)) break;
+          if (!mbar_wait(full_b(stg), round & 1, &g_score_status)) break;
+          tc_fence_after();
+          const uint32_t b_addr = sbase + L::kOffB + stg * L::kBBytes;
+#pragma unroll
+          for (int s = 0; s < SUB; ++s) {
+            const uint32_t d = tmem_base + (uint32_t)((acc * SUB + s) * kKeys);
+            const uint32_t a_addr = sbase + L::kOffA + s * L::kABytes;
+#pragma unroll
+            for (int ks = 0; ks < D_IDX / 16; ++ks)
+              umma_bf16(d, umma_desc_kmajor(a_addr + ks * 32, sbo, swz),
+                        umma_desc_kmajor(b_addr + ks * 32, sbo, swz), idesc, ks > 0 ? 1u : 0u);
+          }
+          umma_commit(empty_b(stg));
+          umma_commit(tfull(acc));
+        }
+      }
+      umma_commit(done_bar);                           // every MMA issued has completed
+      mbar_wait(done_bar, 0, &g_score_status);
+    }
+  } else {
+    // --------------------------------------------------------------- epilogue
+    const int e = warp - 2;
+    const int s = e >> 2;                                 // sub-tile
+    const int q = warp & 3;                               // TMEM lane quarter
+    float* stage = reinterpret_cast<float*>(smem + L::kOffStage) + e * L::kStageFloats;
+    const int64_t Rw = R0 + (int64_t)s * kRows + 32 * q;  // first row of this warp
+    const int64_t R = Rw + lane;
+    const int64_t i = R >> log2_hkv;
+    const int64_t l = i >> 6;                             // local block of this row
+    const float ninf = -INFINITY;
+
+    auto flush = [&](int g, int ncols) {
+      __syncwarp();
+      for (int rho = 0; rho < 32; ++rho) {
+        const int64_t Rr = Rw + rho;
+        const int64_t ir = Rr >> log2_hkv;
+        if (ir >= i_end) break;
+        const int rr = (int)(Rr & (H_kv - 1));
+        const int64_t b = (int64_t)g * kGroupBlocks + lane;
+        if (b < nblk) {
+          const float val = lane < ncols ? stage[rho * 33 + lane] : ninf;
+          M[((int64_t)rr * q_count + (ir - q_start)) * nblk + b] = val;
+        }
+      }
+      __syncwarp();
+    };
+
+    bool ok = true;
+    for (int kt = 0; kt < nkt; ++kt) {
+      const int acc = kt & 1, use = kt >> 1;
+      if (!mbar_wait(tfull(acc), use & 1, &g_score_status)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int64_t b = 2 * (int64_t)kt + h;
+        uint32_t v[64];
+        const uint32_t taddr = tmem_base + ((uint32_t)(32 * q) << 16) +
+                               (uint32_t)((acc * SUB + s) * kKeys + 64 * h);
+        MSA_TMEM_LD64(taddr, v);
+        tmem_ld_wait();
+        float m = ninf;
+        if (b < l) {
+          m = max64(v) * scale;
+        } else if (b == l) {                              // diagonal block: keys j <= i only
+          const int lim = (int)(i - 64 * b);
+#pragma unroll
+          for (int c = 0; c < 64; ++c)
+            if (c > lim) v[c] = __float_as_uint(ninf);
+          m = max64(v) * scale;
+        }
+        stage[lane * 33 + (int)(b & (kGroupBlocks - 1))] = m;
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty(acc));
+      const int kt_in_group = kt % kTilesPerGroup;
+      if (kt_in_group == kTilesPerGroup - 1 || kt == nkt - 1)
+        flush(kt / kTilesPerGroup, 2 * (kt_in_group + 1));
+    }
+    if (ok) {
+      // blocks after the last key tile are in every row's future
+      const int64_t b_first = ((int64_t)(nkt - 1) / kTilesPerGroup + 1) * kGroupBlocks;
+      for (int rho = 0; rho < 32; ++rho) {
+        const int64_t Rr = Rw + rho;
+        const int64_t ir = Rr >> log2_hkv;
+        if (ir >= i_end) break;
+        const int rr = (int)(Rr & (H_kv - 1));
+        float* row = M + ((int64_t)rr * q_count + (ir - q_start)) * nblk;
+        for (int64_t b = b_first + lane; b < nblk; b += 32) row[b] = ninf;
+      }
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, L::kTmemCols);
+  }
+}
+
+template <int D_IDX, int SUB>
+cudaError_t launch_scores(const CUtensorMap& tq, const CUtensorMap& tk, float* M, int H_kv,
+                          int64_t q_start, int64_t q_count, int64_t nblk, cudaStream_t stream) {
+  using L = ScoreSmem<D_IDX, SUB>;
+  auto kern = k_index_block_scores<D_IDX, SUB>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+  if (e != cudaSuccess) return e;
+  int log2_hkv = 0;
+  while ((1 << log2_hkv) < H_kv) ++log2_hkv;
+  const int64_t per_cta = (int64_t)SUB * (kRows / H_kv);
+  const int64_t grid = (q_count + per_cta - 1) / per_cta;
+  const float scale = (float)(1.0 / std::sqrt((double)D_IDX));
+  kern<<<(unsigned)grid, L::kThreads, L::kAlloc, stream>>>(tq, tk, M, log2_hkv, q_start, q_count,
+                                                           nblk, scale);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_index_block_scores(const void* q_idx, const void* k_idx, float* M, int64_t N,
+                                      int H_kv, int d_idx, int64_t q_start, int64_t q_count,
+                                      cudaStream_t stream) {
+  CUtensorMap tq, tk;
+  const int swz = d_idx * 2;   // one swizzle row per index vector
+  cudaError_t e = make_tma_2d_bf16(&tq, q_idx, (uint64_t)d_idx, (uint64_t)N * H_kv, d_idx, kRows, swz);
+  if (e != cudaSuccess) return e;
+  e = make_tma_2d_bf16(&tk, k_idx, (uint64_t)d_idx, (uint64_t)N, d_idx, kKeys, swz);
+  if (e != cudaSuccess) return e;
+  const int64_t nblk = (N + kBlock - 1) / kBlock;
+  if (d_idx == 64) return launch_scores<64, 2>(tq, tk, M, H_kv, q_start, q_count, nblk, stream);
+  return launch_scores<32, 2>(tq, tk, M, H_kv, q_start, q_count, nblk, stream);
+}
+
+cudaError_t read_reset_score_status(unsigned* out) {
+  unsigned zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(out, g_score_status, sizeof(unsigned));
+  if (e != cudaSuccess) return e;
+  return cudaMemcpyToSymbol(g_score_status, &zero, sizeof(unsigned));
+}
+
+}  // namespace msa

@@ -1,0 +1,39 @@
+// Internal launchers shared between the kernel translation units and the C ABI layer.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace msa {
+
+// 2-D bf16 TMA descriptor over a row-major [outer, inner] tensor; box = box_inner x box_outer,
+// swizzle_bytes in {0, 64, 128}.
+cudaError_t make_tma_2d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                             int box_inner, int box_outer, int swizzle_bytes);
+
+cudaError_t launch_index_block_scores(const void* q_idx, const void* k_idx, float* M, int64_t N,
+                                      int H_kv, int d_idx, int64_t q_start, int64_t q_count,
+                                      cudaStream_t stream);
+cudaError_t read_reset_score_status(unsigned* out);
+
+cudaError_t launch_select_prefill(const float* M, int32_t* idx, int64_t N, int H_kv, int k,
+                                  int64_t q_start, int64_t q_count, cudaStream_t stream);
+cudaError_t launch_select_decode(const float* Mdec, int32_t* idx, const int64_t* cu, int S,
+                                 int H_kv, int k, int64_t max_len, int64_t nblk_max,
+                                 cudaStream_t stream);
+
+cudaError_t launch_sparse_attn_prefill(const void* q, const void* k, const void* v,
+                                       const int32_t* idx, void* o, float* lse, int64_t N, int H_q,
+                                       int H_kv, int d_h, int kk, cudaStream_t stream);
+cudaError_t launch_sparse_attn_decode(const void* q, const void* k_cache, const void* v_cache,
+                                      const int32_t* idx, const int64_t* cu, int S,
+                                      int64_t max_len, int H_q, int H_kv, int d_h, int kk,
+                                      int nsplit, float* part_o, float* part_lse, void* o,
+                                      float* lse, cudaStream_t stream);
+
+cudaError_t launch_decode_block_scores(const void* q_idx, const void* k_idx_cache,
+                                       const int64_t* cu, float* Mdec, int S, int H_kv, int d_idx,
+                                       int64_t max_len, int64_t nblk_max, cudaStream_t stream);
+
+}  // namespace msa

@@ -1,0 +1,167 @@
+"""Thin ctypes binding of libmsa.so: argument marshalling only.
+
+Every function has the name of the C entry point it calls (include/msa.h), takes torch
+tensors that already live on the GPU (bf16 for activations, fp32 for M/LSE, int32 for block
+indices, int64 for cu_seqlens), checks dtypes/shapes/contiguity, and passes data pointers,
+sizes and the current CUDA stream.  All arithmetic happens in the CUDA kernels; there is no
+fallback of any kind: if the library is missing, importing this module raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmsa.so")
+
+STATUS = {0: "MSA_OK", 1: "MSA_ERR_INVALID_ARGUMENT", 2: "MSA_ERR_UNSUPPORTED",
+          3: "MSA_ERR_WORKSPACE", 4: "MSA_ERR_CUDA", 5: "MSA_ERR_TIMEOUT"}
+
+
+class MSAError(RuntimeError):
+    def __init__(self, fn, code):
+        super().__init__("%s returned %s" % (fn, STATUS.get(code, code)))
+        self.code = code
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError("libmsa.so not built (run __graft_entry__.build() or "
+                          "python block_sparse_gqa_scores_gb300/_build.py)")
+    L = ctypes.CDLL(LIB_PATH)
+    P, i64, i32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
+    L.msa_status_string.argtypes = [i32]
+    L.msa_status_string.restype = ctypes.c_char_p
+    L.msa_index_block_scores.argtypes = [P, P, P, i64, i32, i32, i32, i64, i64, P]
+    L.msa_select_blocks.argtypes = [P, P, i64, i32, i32, i32, i64, i64, P]
+    L.msa_sparse_attn_fwd_workspace.argtypes = [i64, i32, i32, i32, i32]
+    L.msa_sparse_attn_fwd_workspace.restype = sz
+    L.msa_sparse_attn_fwd.argtypes = [P, P, P, P, P, P, i64, i32, i32, i32, i32, i32, P, sz, P]
+    L.msa_sparse_decode_workspace.argtypes = [i32, i64, i32, i32, i32, i32, i32]
+    L.msa_sparse_decode_workspace.restype = sz
+    L.msa_sparse_decode.argtypes = [P, P, P, P, P, P, i32, i64, i32, i32, i32, i32, i32, i32, P, P,
+                                    P, P, sz, P]
+    for fn in ("msa_index_block_scores", "msa_select_blocks", "msa_sparse_attn_fwd",
+               "msa_sparse_decode", "msa_device_status"):
+        getattr(L, fn).restype = i32
+    return L
+
+
+lib = _load()
+
+BLOCK = 64
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(fn, code):
+    if code != 0:
+        raise MSAError(fn, code)
+
+
+def _req(t, dtype, ndim, name):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch.Tensor" % name)
+    if t.dtype != dtype or t.dim() != ndim or not t.is_contiguous() or not t.is_cuda:
+        raise ValueError("%s must be a contiguous %dD %s CUDA tensor, got %s %s %s" % (
+            name, ndim, dtype, tuple(t.shape), t.dtype, t.device))
+
+
+def msa_index_block_scores(q_idx, k_idx, M=None, q_start=0, q_count=None, block_size=BLOCK,
+                           stream=None):
+    """Block scores M [H_kv, q_count, ceil(N/64)] fp32 of rows [q_start, q_start+q_count)."""
+    _req(q_idx, torch.bfloat16, 3, "q_idx")
+    _req(k_idx, torch.bfloat16, 2, "k_idx")
+    N, H_kv, d_idx = q_idx.shape
+    q_count = N - q_start if q_count is None else q_count
+    nblk = -(-N // block_size)
+    if M is None:
+        M = torch.empty((H_kv, q_count, nblk), dtype=torch.float32, device=q_idx.device)
+    _req(M, torch.float32, 3, "M")
+    _check("msa_index_block_scores", lib.msa_index_block_scores(
+        _ptr(q_idx), _ptr(k_idx), _ptr(M), N, H_kv, d_idx, block_size, q_start, q_count,
+        _stream(stream)))
+    return M
+
+
+def msa_select_blocks(M, N, k, idx=None, q_start=0, block_size=BLOCK, stream=None):
+    """Selected blocks idx [H_kv, N, k] int32 (rows q_start..q_start+q_count-1 written)."""
+    _req(M, torch.float32, 3, "M")
+    H_kv, q_count, _ = M.shape
+    if idx is None:
+        idx = torch.full((H_kv, N, k), -2, dtype=torch.int32, device=M.device)
+    _req(idx, torch.int32, 3, "idx")
+    _check("msa_select_blocks", lib.msa_select_blocks(
+        _ptr(M), _ptr(idx), N, H_kv, block_size, k, q_start, q_count, _stream(stream)))
+    return idx
+
+
+def msa_sparse_attn_fwd_workspace(N, H_q, H_kv, d_h, k):
+    return int(lib.msa_sparse_attn_fwd_workspace(N, H_q, H_kv, d_h, k))
+
+
+def msa_sparse_attn_fwd(q, k, v, idx, o=None, lse=None, ws=None, block_size=BLOCK, stream=None):
+    """Main branch: O [N, H_q, d_h] bf16 and LSE [H_q, N] fp32 over the selected blocks."""
+    _req(q, torch.bfloat16, 3, "q")
+    _req(k, torch.bfloat16, 3, "k")
+    _req(v, torch.bfloat16, 3, "v")
+    _req(idx, torch.int32, 3, "idx")
+    N, H_q, d_h = q.shape
+    H_kv = k.shape[1]
+    kk = idx.shape[2]
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((H_q, N), dtype=torch.float32, device=q.device)
+    nws = msa_sparse_attn_fwd_workspace(N, H_q, H_kv, d_h, kk)
+    if ws is None and nws:
+        ws = torch.empty(nws, dtype=torch.uint8, device=q.device)
+    _check("msa_sparse_attn_fwd", lib.msa_sparse_attn_fwd(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(idx), _ptr(o), _ptr(lse), N, H_q, H_kv, d_h, block_size,
+        kk, _ptr(ws), 0 if ws is None else ws.numel(), _stream(stream)))
+    return o, lse
+
+
+def msa_sparse_decode_workspace(S, max_len, H_q, H_kv, d_h, d_idx, k):
+    return int(lib.msa_sparse_decode_workspace(S, max_len, H_q, H_kv, d_h, d_idx, k))
+
+
+def msa_sparse_decode(q, q_idx, k_cache, v_cache, k_idx_cache, cu_seqlens, max_len, k,
+                      o=None, lse=None, idx_out=None, ws=None, block_size=BLOCK, stream=None):
+    """Decode one new query per sequence -> (O [S,H_q,d_h] bf16, LSE [S,H_q] fp32, idx)."""
+    _req(q, torch.bfloat16, 3, "q")
+    _req(q_idx, torch.bfloat16, 3, "q_idx")
+    _req(k_cache, torch.bfloat16, 3, "k_cache")
+    _req(v_cache, torch.bfloat16, 3, "v_cache")
+    _req(k_idx_cache, torch.bfloat16, 2, "k_idx_cache")
+    _req(cu_seqlens, torch.int64, 1, "cu_seqlens")
+    S, H_q, d_h = q.shape
+    H_kv, d_idx = q_idx.shape[1], q_idx.shape[2]
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((S, H_q), dtype=torch.float32, device=q.device)
+    if idx_out is None:
+        idx_out = torch.empty((S, H_kv, k), dtype=torch.int32, device=q.device)
+    nws = msa_sparse_decode_workspace(S, max_len, H_q, H_kv, d_h, d_idx, k)
+    if ws is None:
+        ws = torch.empty(max(nws, 16), dtype=torch.uint8, device=q.device)
+    _check("msa_sparse_decode", lib.msa_sparse_decode(
+        _ptr(q), _ptr(q_idx), _ptr(k_cache), _ptr(v_cache), _ptr(k_idx_cache), _ptr(cu_seqlens),
+        S, max_len, H_q, H_kv, d_h, d_idx, block_size, k, _ptr(o), _ptr(lse), _ptr(idx_out),
+        _ptr(ws), ws.numel(), _stream(stream)))
+    return o, lse, idx_out
+
+
+def msa_device_status():
+    """Reads and clears the device status words; raises on a recorded timeout."""
+    _check("msa_device_status", lib.msa_device_status())

@@ -1,0 +1,131 @@
+/*
+ * msa.h -- C ABI of the GB300 (sm_103a) MSA block-sparse GQA attention library
+ * (libmsa.so).
+ *
+ * MSA (MiniMax Sparse Attention) as described in «MiniMax-M3：MSA 技术报告速读»
+ * (MSA tech-report digest), section 核心机制：两个分支，先选后算:
+ *   index branch:  S^{idx,(r)}_{i,j} = Q^idx(r)_i . K^idx_j / sqrt(d_idx)           (eq. S^idx)
+ *                  M^{idx,(r)}_{i,b} = max_{j in block b, j <= i} S^{idx,(r)}_{i,j}   (eq. M^idx)
+ *                  I^{(r)}_i = TopK_b(M^{idx,(r)}_{i,.}, k), local block always kept (eq. I^(r)_i)
+ *   main branch:   O^{(h)}_i = softmax(Q^(h)_i K^(r)[I]^T / sqrt(d_h)) V^(r)[I]       (eq. O^(h)_i)
+ *                  over the visible tokens (j <= i) of the selected blocks, shared by the
+ *                  G = H_q/H_kv query heads of group r = h / G; the forward also emits the
+ *                  per-row log-sum-exp (section Kernel).
+ *
+ * Conventions (every entry point):
+ *   - Pointers are DEVICE pointers owned by the caller; the library never allocates or
+ *     frees memory and never synchronises.  Work is enqueued on `stream` (a cudaStream_t
+ *     passed as void*; NULL = legacy default stream).
+ *   - bf16 tensors are passed as `const void*` / `void*` (IEEE bfloat16 bit patterns),
+ *     contiguous, row-major, 16-byte aligned base.
+ *   - block_size must be 64.  Scales are fixed by the formulas (1/sqrt(d_idx), 1/sqrt(d_h)).
+ *   - Supported shapes: H_kv in {1,2,4,8,16}; G = H_q/H_kv in {1,2,4,8}; d_h in {64,128};
+ *     d_idx in {32,64}; 1 <= k <= 64.  Other valid shapes return MSA_ERR_UNSUPPORTED.
+ *   - Inputs must be finite (no inf/NaN).
+ *   - Host-side validation happens before any launch: a bad argument returns
+ *     MSA_ERR_INVALID_ARGUMENT and enqueues nothing.  A launch failure returns
+ *     MSA_ERR_CUDA.  Kernel-side waits are bounded; a wait that gives up records
+ *     MSA_ERR_TIMEOUT in a device status word that msa_device_status() reports.
+ *   - Selection ties go to the lower block index; selected indices are stored ascending
+ *     and padded with -1 when fewer than k blocks are visible.
+ *   - All functions are thread-safe (no mutable host state besides a lazily resolved
+ *     driver entry point).
+ */
+#ifndef MSA_H_
+#define MSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MSA_OK = 0,
+    MSA_ERR_INVALID_ARGUMENT = 1, /* null/misaligned pointer, bad size, range outside [0,N) */
+    MSA_ERR_UNSUPPORTED = 2,      /* valid shape this build has no kernel for            */
+    MSA_ERR_WORKSPACE = 3,        /* ws_bytes smaller than the *_workspace() size         */
+    MSA_ERR_CUDA = 4,             /* CUDA runtime/driver error at launch                  */
+    MSA_ERR_TIMEOUT = 5           /* a bounded device-side wait gave up                   */
+} msa_status_t;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *msa_status_string(msa_status_t status);
+
+/* Index branch: causal token scores max-pooled into block scores (eqs. S^idx and M^idx of
+ * the digest's section 索引分支).  For query rows i in [q_start, q_start+q_count):
+ *   M[r, i-q_start, b] = max_{j in [64b, min(64b+63, i)]} (q_idx[i,r,:] . k_idx[j,:]) / sqrt(d_idx)
+ * and M = -inf for blocks b > floor(i/64) (max over an empty set).
+ *   q_idx  bf16 [N, H_kv, d_idx]   one index query head per KV group
+ *   k_idx  bf16 [N, d_idx]          one index key shared by all groups
+ *   M      fp32 [H_kv, q_count, ceil(N/64)]  (written in full)
+ * fp32 accumulation of bf16 products; on inputs whose products and sums are exact in
+ * fp32 (small integers) M equals the exact value scaled and rounded once. */
+msa_status_t msa_index_block_scores(const void *q_idx, const void *k_idx, float *M, int64_t N,
+                                    int H_kv, int d_idx, int block_size, int64_t q_start,
+                                    int64_t q_count, void *stream);
+
+/* Per-group top-k block selection with the forced local block (eq. I^(r)_i and the local-
+ * block rule of section 索引分支).  For each group r and row i in [q_start, q_start+q_count),
+ * with l = floor(i/64):
+ *   idx[r, i, :] = ascending( {l} U the k-1 blocks b < l with the largest M[r, i-q_start, b] )
+ * ties broken toward the lower b; when l+1 <= k every visible block 0..l is selected and the
+ * remaining k-(l+1) entries are -1.  Comparisons only (no exponentials).
+ *   M    fp32 [H_kv, q_count, ceil(N/64)]  as written by msa_index_block_scores
+ *   idx  int32 [H_kv, N, k]  only rows q_start..q_start+q_count-1 are written */
+msa_status_t msa_select_blocks(const float *M, int32_t *idx, int64_t N, int H_kv, int block_size,
+                               int k, int64_t q_start, int64_t q_count, void *stream);
+
+/* Workspace bytes msa_sparse_attn_fwd needs for these sizes (may be 0). */
+size_t msa_sparse_attn_fwd_workspace(int64_t N, int H_q, int H_kv, int d_h, int k);
+
+/* Sparse main branch (eq. O^(h)_i of section 主分支, LSE of section Kernel).  For every row i
+ * and query head h (group r = h / (H_q/H_kv)), over T = {j : floor(j/64) in idx[r,i,:], j <= i}:
+ *   s_j = q[i,h,:] . k[j,r,:] / sqrt(d_h),   lse[h,i] = ln sum_{j in T} exp(s_j),
+ *   o[i,h,:] = sum_{j in T} exp(s_j - lse[h,i]) v[j,r,:]
+ *   q    bf16 [N, H_q, d_h];  k, v bf16 [N, H_kv, d_h];  idx int32 [H_kv, N, k]
+ *        (entries -1 are skipped; entries must be distinct blocks <= floor(i/64) and must
+ *        include floor(i/64), as msa_select_blocks writes them)
+ *   o    bf16 [N, H_q, d_h] (fp32 accumulation, rounded to nearest even)
+ *   lse  fp32 [H_q, N] (natural log)
+ *   ws   device workspace of msa_sparse_attn_fwd_workspace() bytes (NULL if 0). */
+msa_status_t msa_sparse_attn_fwd(const void *q, const void *k, const void *v, const int32_t *idx,
+                                 void *o, float *lse, int64_t N, int H_q, int H_kv, int d_h,
+                                 int block_size, int k_blocks, void *ws, size_t ws_bytes,
+                                 void *stream);
+
+/* Workspace bytes msa_sparse_decode needs (block scores, selections, split partials). */
+size_t msa_sparse_decode_workspace(int S, int64_t max_len, int H_q, int H_kv, int d_h, int d_idx,
+                                   int k);
+
+/* Decode: the whole path (index scores, selection, main branch) for one new query per
+ * sequence.  Sequence s occupies cache rows cu_seqlens[s] .. cu_seqlens[s+1]-1 (length
+ * L_s >= 1, L_s <= max_len); its newest token, already appended, is the query at position
+ * i = L_s - 1, so its local block is floor((L_s-1)/64).  Same formulas as the prefill calls
+ * for that one row.
+ *   q            bf16 [S, H_q, d_h]        q_idx  bf16 [S, H_kv, d_idx]
+ *   k_cache      bf16 [sum L, H_kv, d_h]   v_cache bf16 [sum L, H_kv, d_h]
+ *   k_idx_cache  bf16 [sum L, d_idx]       cu_seqlens int64 [S+1], cu_seqlens[0] = 0
+ *   o            bf16 [S, H_q, d_h]        lse fp32 [S, H_q]
+ *   idx_out      int32 [S, H_kv, k] or NULL (selected blocks, as msa_select_blocks)
+ *   ws           device workspace of msa_sparse_decode_workspace() bytes.
+ * cu_seqlens is read on the device only (the call never synchronises); lengths outside
+ * [1, max_len] are a caller error that the kernels clamp rather than trust. */
+msa_status_t msa_sparse_decode(const void *q, const void *q_idx, const void *k_cache,
+                               const void *v_cache, const void *k_idx_cache,
+                               const int64_t *cu_seqlens, int S, int64_t max_len, int H_q,
+                               int H_kv, int d_h, int d_idx, int block_size, int k, void *o,
+                               float *lse, int32_t *idx_out, void *ws, size_t ws_bytes,
+                               void *stream);
+
+/* Reads and clears the device status words of the current device (synchronising call).
+ * Returns MSA_ERR_TIMEOUT if any kernel since the last call gave up a bounded wait,
+ * MSA_ERR_CUDA if the read itself failed, MSA_OK otherwise. */
+msa_status_t msa_device_status(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MSA_H_ */

@@ -133,14 +133,18 @@ def sparse_attn(q, k, v, I, block_size=64, rows=None):
     return O64, O16, LSE
 
 
-def prefill(q, k, v, q_idx, k_idx, kk, block_size=64, rows=None, want_m=False):
+def prefill(q, k, v, q_idx, k_idx, kk, block_size=64, rows=None, want_m=False, compact=False):
     """Whole prefill path on the given rows (None: all) ->
-    dict(I [n,H_kv,kk], O64, O16, LSE [n,H_q], M32 [n,H_kv,nblk] if want_m)."""
+    dict(I [n,H_kv,kk], O64, O16, LSE [n,H_q], M32 [n,H_kv,nblk] if want_m).
+    compact=True: q and q_idx hold only the listed rows ([n,H_q,d_h], [n,H_kv,d_idx])."""
     q, k, v, q_idx, k_idx = map(_u16, (q, k, v, q_idx, k_idx))
-    N, H_q, d_h = q.shape
-    H_kv, d_idx = q_idx.shape[1], q_idx.shape[2]
+    N, H_kv, d_h = k.shape
+    H_q, d_idx = q.shape[1], q_idx.shape[2]
     rows_a = np.arange(N, dtype=np.int64) if rows is None else np.ascontiguousarray(rows, np.int64)
     n = len(rows_a)
+    if not compact:
+        q, q_idx = np.ascontiguousarray(q[rows_a]), np.ascontiguousarray(q_idx[rows_a])
+    assert q.shape[0] == n and q_idx.shape[0] == n
     nblk = -(-N // block_size)
     I = np.empty((n, H_kv, kk), np.int32)
     M32 = np.empty((n, H_kv, nblk), np.float32) if want_m else None

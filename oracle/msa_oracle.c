@@ -278,9 +278,11 @@ void msa_oracle_sparse_attn(const uint16_t *q, const uint16_t *k, const uint16_t
 }
 
 /* The whole prefill path (scores -> selection -> main branch) for the given rows only.
+ * q_rows [n_rows,H_q,d_h] and q_idx_rows [n_rows,H_kv,d_idx] hold the projections of the
+ * listed rows only (row t is query position rows[t]); K, V, K_idx are the full sequence.
  * I_out [n_rows,H_kv,kk]; M32_out (nullable) [n_rows,H_kv,nblk]; O64/O16/LSE as above. */
-void msa_oracle_prefill_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v,
-                             const uint16_t *q_idx, const uint16_t *k_idx, int64_t N, int H_q,
+void msa_oracle_prefill_rows(const uint16_t *q_rows, const uint16_t *k, const uint16_t *v,
+                             const uint16_t *q_idx_rows, const uint16_t *k_idx, int64_t N, int H_q,
                              int H_kv, int d_h, int d_idx, int B, int kk, const int64_t *rows,
                              int64_t n_rows, int32_t *I_out, float *M32_out, double *O64,
                              uint16_t *O16, double *LSE)
@@ -298,14 +300,15 @@ void msa_oracle_prefill_rows(const uint16_t *q, const uint16_t *k, const uint16_
             const int64_t i = rows[t];
             const int64_t l = i / B;
             for (int r = 0; r < H_kv; ++r) {
-                row_block_scores(q_idx + (i * H_kv + r) * (int64_t)d_idx, k_idx, i, d_idx, B, m64);
+                row_block_scores(q_idx_rows + (t * H_kv + r) * (int64_t)d_idx, k_idx, i, d_idx, B,
+                                 m64);
                 for (int64_t b = 0; b < nblk; ++b) m32[b] = b <= l ? (float)m64[b] : -INFINITY;
                 if (M32_out) memcpy(M32_out + (t * H_kv + r) * nblk, m32, (size_t)nblk * sizeof(float));
                 row_select(m32, l, kk, sel + r * kk);
             }
             memcpy(I_out + t * H_kv * (int64_t)kk, sel, (size_t)H_kv * kk * sizeof(int32_t));
             double *o = O64 + t * H_q * (int64_t)d_h;
-            row_attend(q + i * H_q * (int64_t)d_h, k, v, i, H_q, H_kv, d_h, B, sel, kk, o,
+            row_attend(q_rows + t * H_q * (int64_t)d_h, k, v, i, H_q, H_kv, d_h, B, sel, kk, o,
                        LSE + t * H_q, s_buf, j_buf);
             if (O16)
                 for (int64_t e = 0; e < (int64_t)H_q * d_h; ++e)

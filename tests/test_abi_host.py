@@ -1,0 +1,129 @@
+"""Host-side checks of the C ABI (no GPU needed): the library builds for sm_103a, loads,
+exports every entry point include/msa.h declares, and rejects bad arguments before any
+CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from block_sparse_gqa_scores_gb300 import _build
+    path = _build.build()
+    return ctypes.CDLL(path)
+
+
+def declared_symbols():
+    text = open(os.path.join(ROOT, "include", "msa.h")).read()
+    return sorted(set(re.findall(r"^\w[\w\s\*]*?\b(msa_\w+)\s*\(", text, re.M)))
+
+
+def test_header_declares_the_api():
+    syms = declared_symbols()
+    for name in ("msa_index_block_scores", "msa_select_blocks", "msa_sparse_attn_fwd",
+                 "msa_sparse_attn_fwd_workspace", "msa_sparse_decode",
+                 "msa_sparse_decode_workspace", "msa_status_string", "msa_device_status"):
+        assert name in syms
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    lib.msa_status_string.restype = ctypes.c_char_p
+    names = [lib.msa_status_string(i).decode() for i in range(6)]
+    assert names == ["MSA_OK", "MSA_ERR_INVALID_ARGUMENT", "MSA_ERR_UNSUPPORTED",
+                     "MSA_ERR_WORKSPACE", "MSA_ERR_CUDA", "MSA_ERR_TIMEOUT"]
+    assert lib.msa_status_string(99) == b"MSA_ERR_UNKNOWN"
+
+
+# Fake, 16-byte aligned pointer values: every call below must return before touching them.
+P = ctypes.c_void_p(0x10000)
+MIS = ctypes.c_void_p(0x10002)
+NUL = ctypes.c_void_p(0)
+i64 = ctypes.c_int64
+
+
+def scores(lib, q=P, k=P, M=P, N=1024, H_kv=4, d_idx=64, B=64, qs=0, qc=1024):
+    return lib.msa_index_block_scores(q, k, M, i64(N), H_kv, d_idx, B, i64(qs), i64(qc), NUL)
+
+
+def select(lib, M=P, idx=P, N=1024, H_kv=4, B=64, k=16, qs=0, qc=1024):
+    return lib.msa_select_blocks(M, idx, i64(N), H_kv, B, k, i64(qs), i64(qc), NUL)
+
+
+def attn(lib, q=P, k=P, v=P, idx=P, o=P, lse=P, N=1024, H_q=32, H_kv=4, d_h=128, B=64, kk=16,
+         ws=NUL, wsb=0):
+    return lib.msa_sparse_attn_fwd(q, k, v, idx, o, lse, i64(N), H_q, H_kv, d_h, B, kk, ws,
+                                   ctypes.c_size_t(wsb), NUL)
+
+
+def decode(lib, q=P, S=4, max_len=1000, H_q=32, H_kv=4, d_h=128, d_idx=64, B=64, k=16, ws=P,
+           wsb=1 << 40, cu=P, idx_out=NUL):
+    return lib.msa_sparse_decode(q, P, P, P, P, cu, S, i64(max_len), H_q, H_kv, d_h, d_idx, B, k,
+                                 P, P, idx_out, ws, ctypes.c_size_t(wsb), NUL)
+
+
+INVALID, UNSUPPORTED, WORKSPACE = 1, 2, 3
+
+
+@pytest.mark.parametrize("kw", [dict(q=NUL), dict(k=MIS), dict(M=NUL), dict(N=0), dict(B=32),
+                                dict(qs=-1), dict(qc=0), dict(qs=1000, qc=100), dict(H_kv=0)])
+def test_scores_invalid(lib, kw):
+    assert scores(lib, **kw) == INVALID
+
+
+@pytest.mark.parametrize("kw", [dict(H_kv=3), dict(H_kv=16), dict(d_idx=48), dict(d_idx=128)])
+def test_scores_unsupported(lib, kw):
+    assert scores(lib, **kw) == UNSUPPORTED
+
+
+@pytest.mark.parametrize("kw", [dict(M=NUL), dict(idx=NUL), dict(k=0), dict(k=65), dict(B=128),
+                                dict(qs=1024, qc=1), dict(N=-5)])
+def test_select_invalid(lib, kw):
+    assert select(lib, **kw) == INVALID
+
+
+@pytest.mark.parametrize("kw", [dict(q=NUL), dict(o=MIS), dict(N=0), dict(H_q=30), dict(kk=0),
+                                dict(kk=100), dict(B=16)])
+def test_attn_invalid(lib, kw):
+    assert attn(lib, **kw) == INVALID
+
+
+@pytest.mark.parametrize("kw", [dict(d_h=96), dict(d_h=256), dict(H_q=64, H_kv=4),
+                                dict(H_q=12, H_kv=4)])
+def test_attn_unsupported(lib, kw):
+    assert attn(lib, **kw) == UNSUPPORTED
+
+
+@pytest.mark.parametrize("kw", [dict(q=NUL), dict(S=0), dict(max_len=0), dict(cu=NUL),
+                                dict(cu=ctypes.c_void_p(0x10004)), dict(k=0), dict(ws=NUL),
+                                dict(idx_out=MIS)])
+def test_decode_invalid(lib, kw):
+    assert decode(lib, **kw) == INVALID
+
+
+def test_decode_workspace_checked(lib):
+    lib.msa_sparse_decode_workspace.restype = ctypes.c_size_t
+    need = lib.msa_sparse_decode_workspace(4, i64(1000), 32, 4, 128, 64, 16)
+    assert need > 0
+    assert decode(lib, wsb=need - 1) == WORKSPACE
+    assert decode(lib, d_h=80) == UNSUPPORTED
+
+
+def test_workspace_sizes(lib):
+    lib.msa_sparse_decode_workspace.restype = ctypes.c_size_t
+    lib.msa_sparse_attn_fwd_workspace.restype = ctypes.c_size_t
+    S, L, H_q, H_kv, d_h, k = 32, 262144, 32, 4, 128, 16
+    need = lib.msa_sparse_decode_workspace(S, i64(L), H_q, H_kv, d_h, 64, k)
+    # block scores + selections + 4 split partials per (sequence, group)
+    nblk = L // 64
+    floor = 4 * S * H_kv * nblk + 4 * S * H_kv * k + 4 * S * H_kv * 4 * (H_q // H_kv) * (d_h + 1)
+    assert floor <= need <= floor + 4 * 256
+    assert lib.msa_sparse_attn_fwd_workspace(i64(1024), 8, 2, 64, 4) == 0

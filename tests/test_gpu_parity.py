@@ -1,0 +1,284 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle on the same seeded
+inputs, at sizes that span several tiles plus ragged tails, and on the degenerate cases.
+
+Bars:  block scores -- exact on small-integer inputs at d_idx=64 (fp32 dot products exact,
+       scale 1/8 exact), <= 1 ulp at d_idx=32 (scale rounded once), fp32-accumulation
+       tolerance on Gaussian inputs;  selection -- bit-exact when both sides see the same
+       fp32 block scores; end to end, exact on integer inputs and exact up to near-ties
+       (< 1e-3 relative) on Gaussian inputs;  O max-abs <= 2e-2, LSE abs <= 1e-3 against the
+       oracle evaluated on the GPU's own selection."""
+import numpy as np
+import pytest
+import torch
+
+import gen
+import oracle
+from msa_testutil import (LSE_TOL, O_TOL, bits, cuda, max_abs, selection_mismatches)
+
+pytestmark = pytest.mark.gpu
+
+msa = pytest.importorskip("block_sparse_gqa_scores_gb300")
+
+
+def cfg_of(name, **kw):
+    base = gen.CONFIGS[name]
+    return gen.PrefillConfig(**{**base.__dict__, **kw}) if kw else base
+
+
+def fresh(cfg, N=None, seed=0, variant="gauss"):
+    x = gen.prefill_inputs(cfg, seed=seed, device="cuda", variant=variant, N=N)
+    return x, bits(x)
+
+
+def sync_ok():
+    torch.cuda.synchronize()
+    msa.msa_device_status()
+
+
+# ---------------------------------------------------------------- block scores --
+
+SCORE_CASES = [
+    ("tiny", 1024, "gauss", 0), ("tiny", 1024, "gauss", 1), ("tiny", 1024, "gauss", 2),
+    ("tiny", 1024, "int", 0), ("tiny", 777, "int", 3),
+    ("p32k", 1, "gauss", 0), ("p32k", 63, "gauss", 0), ("p32k", 64, "gauss", 0),
+    ("p32k", 65, "int", 0), ("p32k", 1000, "gauss", 0), ("p32k", 3000, "int", 1),
+    ("p32k", 4099, "gauss", 2),
+]
+
+
+@pytest.mark.parametrize("name,N,variant,seed", SCORE_CASES)
+def test_block_scores(name, N, variant, seed):
+    cfg = cfg_of(name)
+    x, b = fresh(cfg, N, seed, variant)
+    M = msa.msa_index_block_scores(x["q_idx"], x["k_idx"])
+    sync_ok()
+    M = M.cpu().numpy()
+    _, ref = oracle.block_scores(b["q_idx"], b["k_idx"])
+    assert np.array_equal(np.isneginf(M), np.isneginf(ref))
+    fin = np.isfinite(ref)
+    if variant == "int":
+        if cfg.d_idx == 64:
+            assert np.array_equal(M[fin], ref[fin])
+        else:
+            ulp = np.abs(M[fin].view(np.int32).astype(np.int64) - ref[fin].view(np.int32))
+            assert ulp.max() <= 1
+    else:
+        np.testing.assert_allclose(M[fin], ref[fin], rtol=1e-5, atol=1e-4)
+
+
+@pytest.mark.parametrize("q_start,q_count", [(0, 1), (100, 333), (2999, 1), (64, 1000), (1, 2998)])
+def test_block_scores_query_range(q_start, q_count):
+    cfg = cfg_of("p32k")
+    x, b = fresh(cfg, 3000, 5, "int")
+    M = msa.msa_index_block_scores(x["q_idx"], x["k_idx"], q_start=q_start, q_count=q_count)
+    sync_ok()
+    _, ref = oracle.block_scores(b["q_idx"], b["k_idx"], q_start=q_start, q_count=q_count)
+    assert np.array_equal(M.cpu().numpy(), ref)
+
+
+# ------------------------------------------------------------------- selection --
+
+def synthetic_scores(H_kv, N, q_start, q_count, kind, seed):
+    """Block-score tensors with -inf after each row's own block: Gaussian, small integers
+    (many ties) or all equal (ties everywhere)."""
+    rng = np.random.default_rng(seed)
+    nblk = -(-N // 64)
+    if kind == "gauss":
+        M = rng.standard_normal((H_kv, q_count, nblk)).astype(np.float32)
+    elif kind == "intM":
+        M = rng.integers(0, 4, (H_kv, q_count, nblk)).astype(np.float32)
+    else:
+        M = np.zeros((H_kv, q_count, nblk), np.float32)
+    l = (np.arange(q_start, q_start + q_count) // 64)[None, :, None]
+    M[np.arange(nblk)[None, None, :] > l] = -np.inf
+    return M
+
+
+SELECT_CASES = [
+    (2, 1024, 0, 1024, 4, "gauss"), (2, 1024, 0, 1024, 4, "intM"), (4, 5000, 0, 5000, 16, "gauss"),
+    (4, 5000, 0, 5000, 16, "intM"), (4, 5000, 0, 5000, 16, "const"), (4, 5000, 0, 5000, 1, "gauss"),
+    (4, 5000, 0, 5000, 2, "intM"), (4, 5000, 0, 5000, 33, "gauss"), (4, 5000, 0, 5000, 64, "intM"),
+    (4, 70000, 60000, 2000, 16, "gauss"), (4, 70000, 60000, 2000, 16, "intM"),
+    (4, 70000, 65000, 300, 64, "const"), (8, 20000, 19000, 1000, 16, "gauss"),
+    (1, 300000, 299000, 1000, 16, "gauss"),
+]
+
+
+@pytest.mark.parametrize("H_kv,N,q_start,q_count,k,kind", SELECT_CASES)
+def test_select_bit_exact(H_kv, N, q_start, q_count, k, kind):
+    M = synthetic_scores(H_kv, N, q_start, q_count, kind, seed=N + k)
+    ref = oracle.select_blocks(M, N, k, q_start=q_start)
+    idx = msa.msa_select_blocks(torch.from_numpy(M).cuda(), N, k, q_start=q_start)
+    sync_ok()
+    assert np.array_equal(idx.cpu().numpy(), ref)
+
+
+# ------------------------------------------------------------------ main branch --
+
+ATTN_CASES = [
+    ("tiny", {}, 1024, 4), ("tiny", {}, 1024, 1), ("tiny", {}, 1024, 64),
+    ("p32k", {}, 1, 16), ("p32k", {}, 63, 16), ("p32k", {}, 64, 16), ("p32k", {}, 65, 16),
+    ("p32k", {}, 1000, 16), ("p32k", {}, 1000, 64), ("p32k", {}, 2500, 16),
+    ("p32k", dict(H_q=4, H_kv=4), 700, 8), ("p32k", dict(H_q=8, H_kv=4), 700, 8),
+    ("p32k", dict(H_q=16, H_kv=4), 700, 8), ("p32k", dict(H_q=8, H_kv=1), 700, 5),
+    ("p32k", dict(d_h=64), 900, 16), ("tiny", dict(d_h=128), 900, 4),
+]
+
+
+@pytest.mark.parametrize("name,over,N,k", ATTN_CASES)
+def test_sparse_attention(name, over, N, k):
+    cfg = cfg_of(name, k=k, **over)
+    x, b = fresh(cfg, N, seed=11)
+    _, M32 = oracle.block_scores(b["q_idx"], b["k_idx"])
+    I = oracle.select_blocks(M32, N, k)
+    O64, _, L = oracle.sparse_attn(b["q"], b["k"], b["v"], I)
+    o, lse = msa.msa_sparse_attn_fwd(x["q"], x["k"], x["v"], torch.from_numpy(I).cuda())
+    sync_ok()
+    assert max_abs(o.float().cpu().numpy(), O64) <= O_TOL
+    assert max_abs(lse.cpu().numpy().T, L) <= LSE_TOL
+
+
+def test_sparse_attention_zero_query_closed_form():
+    """Q = 0: LSE = ln|T| and O = mean of V over T, on the GPU."""
+    cfg = cfg_of("p32k")
+    x, b = fresh(cfg, 1500, seed=3, variant="zero_q")
+    _, M32 = oracle.block_scores(b["q_idx"], b["k_idx"])
+    I = oracle.select_blocks(M32, 1500, 16)
+    _, lse = msa.msa_sparse_attn_fwd(x["q"], x["k"], x["v"], torch.from_numpy(I).cuda())
+    sync_ok()
+    i = np.arange(1500)
+    T = np.minimum(i + 1, 15 * 64 + i % 64 + 1)
+    assert np.abs(lse.cpu().numpy() - np.log(T)[None, :]).max() <= 1e-4
+
+
+# ------------------------------------------------------------------- end to end --
+
+@pytest.mark.parametrize("name,N,variant,seed", [("tiny", 1024, "gauss", 0), ("tiny", 1024, "gauss", 1),
+                                                 ("tiny", 1024, "gauss", 2), ("tiny", 1024, "int", 0),
+                                                 ("p32k", 3000, "gauss", 0), ("p32k", 3000, "int", 0),
+                                                 ("p128k", 4500, "gauss", 0)])
+def test_prefill_chain(name, N, variant, seed):
+    cfg = cfg_of(name)
+    x, b = fresh(cfg, N, seed, variant)
+    M = msa.msa_index_block_scores(x["q_idx"], x["k_idx"])
+    idx = msa.msa_select_blocks(M, N, cfg.k)
+    o, lse = msa.msa_sparse_attn_fwd(x["q"], x["k"], x["v"], idx)
+    sync_ok()
+    _, M_ref = oracle.block_scores(b["q_idx"], b["k_idx"])
+    I_ref = oracle.select_blocks(M_ref, N, cfg.k)
+    I_gpu = idx.cpu().numpy()
+    if variant == "int":
+        assert np.array_equal(I_gpu, I_ref)
+    else:
+        differ, bad = selection_mismatches(I_gpu, I_ref, M_ref, cfg.k)
+        assert not bad, bad[:5]
+        assert differ <= max(2, I_ref.shape[0] * N // 200)
+    O64, _, L = oracle.sparse_attn(b["q"], b["k"], b["v"], I_gpu)
+    assert max_abs(o.float().cpu().numpy(), O64) <= O_TOL
+    assert max_abs(lse.cpu().numpy().T, L) <= LSE_TOL
+
+
+# ------------------------------------------------------------------------ decode --
+
+def decode_case(cfg, lens, seed, variant="gauss"):
+    d = gen.decode_inputs(cfg, seed=seed, device="cuda", S=len(lens), len_lo=1, len_hi=1,
+                          variant=variant)
+    # replace the drawn lengths with the requested ones (same generator for the payload)
+    cu = torch.zeros(len(lens) + 1, dtype=torch.int64)
+    cu[1:] = torch.cumsum(torch.tensor(lens), 0)
+    total = int(cu[-1])
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed + 17)
+    draw = (lambda shape: torch.randint(-3, 4, shape, generator=g, device="cuda").float()) \
+        if variant == "int" else (lambda shape: torch.randn(*shape, generator=g, device="cuda"))
+    bf = torch.bfloat16
+    d["k_cache"] = draw((total, cfg.H_kv, cfg.d_h)).to(bf)
+    d["v_cache"] = draw((total, cfg.H_kv, cfg.d_h)).to(bf)
+    d["k_idx_cache"] = draw((total, cfg.d_idx)).to(bf)
+    d["cu_seqlens"] = cu.cuda()
+    return d
+
+
+def check_decode(cfg, d, max_len, exact_idx):
+    o, lse, idx = msa.msa_sparse_decode(d["q"], d["q_idx"], d["k_cache"], d["v_cache"],
+                                        d["k_idx_cache"], d["cu_seqlens"], max_len, cfg.k)
+    sync_ok()
+    b = bits(d)
+    cu = d["cu_seqlens"].cpu().numpy()
+    ref = oracle.decode(b["q"], b["q_idx"], b["k_cache"], b["v_cache"], b["k_idx_cache"], cu,
+                        cfg.k, want_m=True)
+    I_gpu = idx.cpu().numpy()                       # [S, H_kv, k]
+    if exact_idx:
+        assert np.array_equal(I_gpu, ref["I"])
+    else:
+        differ, bad = selection_mismatches(I_gpu.transpose(1, 0, 2), ref["I"].transpose(1, 0, 2),
+                                           ref["M32"].transpose(1, 0, 2), cfg.k,
+                                           rows=(cu[1:] - cu[:-1] - 1))
+        assert not bad, bad
+    # main branch on the GPU's own selection, one sequence at a time
+    o_np, lse_np = o.float().cpu().numpy(), lse.cpu().numpy()
+    for s in range(len(cu) - 1):
+        L = int(cu[s + 1] - cu[s])
+        sl = slice(int(cu[s]), int(cu[s + 1]))
+        q = np.zeros((L, cfg.H_q, cfg.d_h), np.uint16)
+        q[L - 1] = b["q"][s]
+        I = np.full((cfg.H_kv, L, cfg.k), -1, np.int32)
+        I[:, L - 1] = I_gpu[s]
+        O64, _, Lr = oracle.sparse_attn(q, b["k_cache"][sl], b["v_cache"][sl], I, rows=[L - 1])
+        assert max_abs(o_np[s], O64[0]) <= O_TOL
+        assert max_abs(lse_np[s], Lr[0]) <= LSE_TOL
+
+
+@pytest.mark.parametrize("name,lens,variant", [
+    ("p32k", [1, 2, 63, 64, 65, 128, 1000, 1025, 5000, 4097], "gauss"),
+    ("p32k", [70, 3000, 129, 64 * 17, 2049], "int"),
+    ("tiny", [1, 100, 900, 1024, 333], "gauss"),
+    ("tiny", [5, 700, 64, 2000], "int"),
+])
+def test_decode(name, lens, variant):
+    cfg = cfg_of(name)
+    dcfg = gen.DecodeConfig("t", len(lens), 1, 1, cfg.H_q, cfg.H_kv, cfg.d_h, cfg.d_idx, cfg.k)
+    d = decode_case(dcfg, lens, seed=len(lens), variant=variant)
+    check_decode(dcfg, d, max(lens) + 37, exact_idx=(variant == "int"))
+
+
+def test_decode_equals_prefill_last_row():
+    cfg = cfg_of("p32k")
+    x, _ = fresh(cfg, 2000, seed=4)
+    lens = [2000, 1500, 64, 1]
+    cu = torch.zeros(len(lens) + 1, dtype=torch.int64)
+    cu[1:] = torch.cumsum(torch.tensor(lens), 0)
+    cat = lambda t: torch.cat([t[:L] for L in lens])
+    last = torch.tensor([L - 1 for L in lens], device="cuda")
+    o_d, lse_d, idx_d = msa.msa_sparse_decode(
+        x["q"][last].contiguous(), x["q_idx"][last].contiguous(), cat(x["k"]), cat(x["v"]),
+        cat(x["k_idx"]), cu.cuda(), 2000, cfg.k)
+    M = msa.msa_index_block_scores(x["q_idx"], x["k_idx"])
+    idx = msa.msa_select_blocks(M, 2000, cfg.k)
+    o, lse = msa.msa_sparse_attn_fwd(x["q"], x["k"], x["v"], idx)
+    sync_ok()
+    assert torch.equal(idx_d.cpu(), idx[:, last].permute(1, 0, 2).cpu())
+    assert (o_d.float() - o[last].float()).abs().max().item() <= 1e-2
+    assert (lse_d - lse[:, last].T).abs().max().item() <= 1e-4
+
+
+# ---------------------------------------------------------------- error handling --
+
+def test_errors_are_reported():
+    cfg = cfg_of("tiny")
+    x, _ = fresh(cfg, 128)
+    with pytest.raises(msa.MSAError) as e:
+        msa.msa_index_block_scores(x["q_idx"], x["k_idx"], q_start=100, q_count=100)
+    assert e.value.code == 1
+    with pytest.raises(msa.MSAError) as e:
+        msa.msa_sparse_attn_fwd(x["q"][:, :, :48].contiguous(), x["k"][:, :, :48].contiguous(),
+                                x["v"][:, :, :48].contiguous(),
+                                torch.zeros((2, 128, 4), dtype=torch.int32, device="cuda"))
+    assert e.value.code == 2
+    d = gen.decode_inputs(gen.CONFIGS["decode"], S=2, len_lo=100, len_hi=200, device="cuda")
+    with pytest.raises(msa.MSAError) as e:
+        msa.msa_sparse_decode(d["q"], d["q_idx"], d["k_cache"], d["v_cache"], d["k_idx_cache"],
+                              d["cu_seqlens"], 200, 16, ws=torch.empty(64, dtype=torch.uint8,
+                                                                       device="cuda"))
+    assert e.value.code == 3
+    sync_ok()
