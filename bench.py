@@ -157,7 +157,7 @@ def workload_sizes(pcfg, dcfg, lens):
     )
     # decode algorithmic bytes: the index-key stream + selected visible K/V + small vectors
     dbytes = 0.0
-    for L in lens:
+    for L in (lens if dcfg is not None else []):
         ii = L - 1
         Tt = min(ii + 1, (dcfg.k - 1) * 64 + (ii % 64) + 1)
         dbytes += 2.0 * dcfg.d_idx * L + 2.0 * 2 * dcfg.H_kv * dcfg.d_h * Tt
@@ -177,6 +177,8 @@ def setup(pcfg, dcfg, seed=0):
         o=torch.empty_like(x["q"]),
         lse=torch.empty((pcfg.H_q, N), dtype=torch.float32, device="cuda"),
     )
+    if dcfg is None:
+        return msa, x, bufs, None, None
     d = gen.decode_inputs(dcfg, seed=seed, device="cuda")
     max_len = dcfg.len_hi
     nws = msa.msa_sparse_decode_workspace(dcfg.S, max_len, dcfg.H_q, dcfg.H_kv, dcfg.d_h,
@@ -189,7 +191,10 @@ def setup(pcfg, dcfg, seed=0):
 
 
 def run_msa(args, world, rank, local):
-    pcfg, dcfg = gen.CONFIGS[args.prefill], gen.CONFIGS[args.decode]
+    pcfg = gen.CONFIGS[args.prefill]
+    if args.prefill_n:
+        pcfg = gen.PrefillConfig(**{**pcfg.__dict__, "N": args.prefill_n})
+    dcfg = None if args.decode == "none" else gen.CONFIGS[args.decode]
     msa, x, bufs, d, dbufs = setup(pcfg, dcfg, seed=args.seed + rank)
     stream = torch.cuda.current_stream()
     N = pcfg.N
@@ -202,6 +207,8 @@ def run_msa(args, world, rank, local):
         msa.msa_sparse_attn_fwd(x["q"], x["k"], x["v"], bufs["idx"], o=bufs["o"], lse=bufs["lse"])
 
     def decode():
+        if d is None:
+            return
         msa.msa_sparse_decode(d["q"], d["q_idx"], d["k_cache"], d["v_cache"], d["k_idx_cache"],
                               d["cu_seqlens"], dbufs["max_len"], dcfg.k, o=dbufs["o"],
                               lse=dbufs["lse"], idx_out=dbufs["idx"], ws=dbufs["ws"])
@@ -245,7 +252,7 @@ def run_msa(args, world, rank, local):
     t_decode_total = max_over_ranks(float(per[:, 3].sum()), world)
     t_all = max_over_ranks(t_start.elapsed_time(t_end), world)
 
-    sizes = workload_sizes(pcfg, dcfg, d["meta"]["lens"])
+    sizes = workload_sizes(pcfg, dcfg, d["meta"]["lens"] if d else [])
     pk = peaks()
     kern = []
 
@@ -262,31 +269,33 @@ def run_msa(args, world, rank, local):
         ncu_traffic("k_select_prefill"))
     add("k_sparse_attn", t_attn, "tensor", sizes["F_main"], "TFLOP/s", pk["bf16_sust"],
         ncu_traffic("k_sparse_attn"))
-    add("decode (4 kernels)", t_decode, "hbm", sizes["decode_bytes"], "GB/s", pk["hbm"],
-        ncu_traffic("decode"))
+    if d is not None:
+        add("decode (4 kernels)", t_decode, "hbm", sizes["decode_bytes"], "GB/s", pk["hbm"],
+            ncu_traffic("decode"))
     dom = max(kern, key=lambda r: r["ms"])
 
     value = world * N * K / (t_prefill_total * 1e-3)
-    dec_value = world * dcfg.S * K / (t_decode_total * 1e-3)
+    dec_value = world * dcfg.S * K / (t_decode_total * 1e-3) if d is not None else None
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
         "steps": K, "warmup": W, "ms_per_step": round(t_all / K, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {
-            "workload": "prefill N=%d + decode %d seqs L~U[%d,%d]" % (N, dcfg.S, dcfg.len_lo,
-                                                                     dcfg.len_hi),
+            "workload": "prefill N=%d" % N + (" + decode %d seqs L~U[%d,%d]" % (
+                dcfg.S, dcfg.len_lo, dcfg.len_hi) if d is not None else ""),
             "prefill": {"N": N, "H_q": pcfg.H_q, "H_kv": pcfg.H_kv, "d_h": pcfg.d_h,
                         "d_idx": pcfg.d_idx, "block": 64, "k": pcfg.k,
                         "hot_blocks": pcfg.hot_blocks, "block_offset_std": pcfg.block_offset_std},
             "decode": {"S": dcfg.S, "len_lo": dcfg.len_lo, "len_hi": dcfg.len_hi,
-                       "mean_len": float(np.mean(d["meta"]["lens"])), "k": dcfg.k},
+                       "mean_len": float(np.mean(d["meta"]["lens"])), "k": dcfg.k}
+            if d is not None else None,
             "l2": "no flush: every timed input exceeds the 129 MB L2 (M 4.3 GB, caches 11.5 GB)",
             "parallelism": "replicas" if world > 1 else "single",
         },
         "ms_prefill": round(t_prefill_total / K, 4),
         "ms_decode": round(t_decode_total / K, 4),
         "decode": {"value": round(dec_value, 1), "unit": "tokens/s",
-                   "ms": round(t_decode_total / K, 4)},
+                   "ms": round(t_decode_total / K, 4)} if d is not None else None,
         "kernels": kern,
         "roofline": {"kernel": dom["kernel"], "bound": dom["bound"], "achieved": dom["achieved"],
                      "peak": dom["peak"], "unit": dom["unit"], "frac": dom["frac"],
@@ -294,7 +303,7 @@ def run_msa(args, world, rank, local):
                      "peak_source": "%s (%s)" % (pk["src"], "bf16 sustained" if dom["unit"] ==
                                                  "TFLOP/s" else "HBM copy")},
         "clocks": clk,
-        "gpu_launches": LAUNCHES_PER_STEP * K,
+        "gpu_launches": (LAUNCHES_PER_STEP if d is not None else 3) * K,
     }
     if not args.no_e2e:
         line["e2e"] = e2e_prefill(msa, pcfg, x, bufs, K, W, world)
@@ -422,7 +431,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["msa", "reference"], default="msa")
     ap.add_argument("--prefill", default="p128k")
-    ap.add_argument("--decode", default="decode")
+    ap.add_argument("--prefill-n", type=int, default=None,
+                    help="override the prefill length (same head layout and structure)")
+    ap.add_argument("--decode", default="decode", help="decode workload, or 'none'")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-e2e", action="store_true")

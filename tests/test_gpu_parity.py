@@ -90,7 +90,7 @@ def synthetic_scores(H_kv, N, q_start, q_count, kind, seed):
     else:
         M = np.zeros((H_kv, q_count, nblk), np.float32)
     l = (np.arange(q_start, q_start + q_count) // 64)[None, :, None]
-    M[np.arange(nblk)[None, None, :] > l] = -np.inf
+    M[np.broadcast_to(np.arange(nblk)[None, None, :] > l, M.shape)] = -np.inf
     return M
 
 
@@ -244,7 +244,7 @@ def test_decode(name, lens, variant):
 
 def test_decode_equals_prefill_last_row():
     cfg = cfg_of("p32k")
-    x, _ = fresh(cfg, 2000, seed=4)
+    x, _ = fresh(cfg, 2000, seed=4, variant="int")      # exact scores on both index paths
     lens = [2000, 1500, 64, 1]
     cu = torch.zeros(len(lens) + 1, dtype=torch.int64)
     cu[1:] = torch.cumsum(torch.tensor(lens), 0)
@@ -258,7 +258,7 @@ def test_decode_equals_prefill_last_row():
     o, lse = msa.msa_sparse_attn_fwd(x["q"], x["k"], x["v"], idx)
     sync_ok()
     assert torch.equal(idx_d.cpu(), idx[:, last].permute(1, 0, 2).cpu())
-    assert (o_d.float() - o[last].float()).abs().max().item() <= 1e-2
+    assert (o_d.float() - o[last].float()).abs().max().item() <= O_TOL   # 1 bf16 ulp at |O|~3
     assert (lse_d - lse[:, last].T).abs().max().item() <= 1e-4
 
 
