@@ -42,6 +42,23 @@ cudaError_t make_tma_2d_bf16(CUtensorMap* map, const void* base, uint64_t inner,
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+cudaError_t make_tma_3d_bf16(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1,
+                             uint64_t d2, int box0, int box1, int box2, int swizzle_bytes) {
+  auto fn = encode_fn();
+  if (!fn) return cudaErrorNotSupported;
+  cuuint64_t dims[3] = {d0, d1, d2};
+  cuuint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
+  cuuint32_t box[3] = {(cuuint32_t)box0, (cuuint32_t)box1, (cuuint32_t)box2};
+  cuuint32_t estr[3] = {1, 1, 1};
+  const CUtensorMapSwizzle sw = swizzle_bytes == 128  ? CU_TENSOR_MAP_SWIZZLE_128B
+                                : swizzle_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                                      : CU_TENSOR_MAP_SWIZZLE_NONE;
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 }  // namespace msa
 
 namespace {
@@ -138,8 +155,8 @@ MSA_API msa_status_t msa_sparse_attn_fwd(const void* q, const void* k, const voi
   if (N * H_kv >= kMaxRows) return MSA_ERR_UNSUPPORTED;
   if (ws_bytes < msa_sparse_attn_fwd_workspace(N, H_q, H_kv, d_h, k_blocks))
     return MSA_ERR_WORKSPACE;
-  return from_cuda(msa::launch_sparse_attn_prefill(q, k, v, idx, o, lse, N, H_q, H_kv, d_h,
-                                                   k_blocks, (cudaStream_t)stream));
+  return from_cuda(msa::launch_sparse_attn_tiled(q, k, v, idx, o, lse, N, H_q, H_kv, d_h,
+                                                 k_blocks, (cudaStream_t)stream));
 }
 
 MSA_API size_t msa_sparse_decode_workspace(int S, int64_t max_len, int H_q, int H_kv, int d_h,
@@ -185,7 +202,8 @@ MSA_API msa_status_t msa_sparse_decode(const void* q, const void* q_idx, const v
 }
 
 MSA_API msa_status_t msa_device_status(void) {
-  unsigned v = 0;
+  unsigned v = 0, w = 0;
   if (msa::read_reset_score_status(&v) != cudaSuccess) return MSA_ERR_CUDA;
-  return v ? MSA_ERR_TIMEOUT : MSA_OK;
+  if (msa::read_reset_attn_status(&w) != cudaSuccess) return MSA_ERR_CUDA;
+  return (v | w) ? MSA_ERR_TIMEOUT : MSA_OK;
 }

@@ -12,6 +12,16 @@ namespace msa {
 cudaError_t make_tma_2d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
                              int box_inner, int box_outer, int swizzle_bytes);
 
+// 3-D bf16 TMA descriptor over a row-major [d2, d1, d0] tensor (d0 innermost); box
+// box0 x box1 x box2, swizzle_bytes in {0, 64, 128}.
+cudaError_t make_tma_3d_bf16(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1,
+                             uint64_t d2, int box0, int box1, int box2, int swizzle_bytes);
+
+cudaError_t launch_sparse_attn_tiled(const void* q, const void* k, const void* v,
+                                     const int32_t* idx, void* o, float* lse, int64_t N, int H_q,
+                                     int H_kv, int d_h, int kk, cudaStream_t stream);
+cudaError_t read_reset_attn_status(unsigned* out);
+
 cudaError_t launch_index_block_scores(const void* q_idx, const void* k_idx, float* M, int64_t N,
                                       int H_kv, int d_idx, int64_t q_start, int64_t q_count,
                                       cudaStream_t stream);
