@@ -73,10 +73,9 @@ msa_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? MSA_OK : MSA_E
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-struct DecodeWs {
-  size_t off_m, off_idx, off_po, off_pl, total;
-  int nsplit;
-};
+}  // namespace
+
+namespace msa {
 
 DecodeWs decode_layout(int S, int64_t max_len, int H_q, int H_kv, int d_h, int k) {
   DecodeWs w{};
@@ -96,7 +95,10 @@ DecodeWs decode_layout(int S, int64_t max_len, int H_q, int H_kv, int d_h, int k
   return w;
 }
 
-}  // namespace
+}  // namespace msa
+
+using msa::DecodeWs;
+using msa::decode_layout;
 
 MSA_API const char* msa_status_string(msa_status_t s) {
   switch (s) {

@@ -7,6 +7,15 @@
 
 namespace msa {
 
+// Byte offsets of the decode workspace: block scores [S, H_kv, ceil(max_len/64)] fp32,
+// selections [S, H_kv, k] int32, split partials O [S*H_kv*nsplit, G, d_h] and LSE
+// [S*H_kv*nsplit, G] fp32, each 256-byte aligned.
+struct DecodeWs {
+  size_t off_m, off_idx, off_po, off_pl, total;
+  int nsplit;
+};
+DecodeWs decode_layout(int S, int64_t max_len, int H_q, int H_kv, int d_h, int k);
+
 // 2-D bf16 TMA descriptor over a row-major [outer, inner] tensor; box = box_inner x box_outer,
 // swizzle_bytes in {0, 64, 128}.
 cudaError_t make_tma_2d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,

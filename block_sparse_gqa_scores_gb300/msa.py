@@ -43,8 +43,10 @@ def _load():
     L.msa_sparse_decode_workspace.restype = sz
     L.msa_sparse_decode.argtypes = [P, P, P, P, P, P, i32, i64, i32, i32, i32, i32, i32, i32, P, P,
                                     P, P, sz, P]
+    L.msa_sparse_decode_noalloc.argtypes = [P, P, P, P, P, P, i32, i64, i32, i32, i32, i32, i32,
+                                            i32, P, P, P, P]
     for fn in ("msa_index_block_scores", "msa_select_blocks", "msa_sparse_attn_fwd",
-               "msa_sparse_decode", "msa_device_status"):
+               "msa_sparse_decode", "msa_sparse_decode_noalloc", "msa_device_status"):
         getattr(L, fn).restype = i32
     return L
 
@@ -159,6 +161,29 @@ def msa_sparse_decode(q, q_idx, k_cache, v_cache, k_idx_cache, cu_seqlens, max_l
         _ptr(q), _ptr(q_idx), _ptr(k_cache), _ptr(v_cache), _ptr(k_idx_cache), _ptr(cu_seqlens),
         S, max_len, H_q, H_kv, d_h, d_idx, block_size, k, _ptr(o), _ptr(lse), _ptr(idx_out),
         _ptr(ws), ws.numel(), _stream(stream)))
+    return o, lse, idx_out
+
+
+def msa_sparse_decode_noalloc(q, q_idx, k_cache, v_cache, k_idx_cache, cu_seqlens, max_len, k,
+                              o, lse, idx_out=None, block_size=BLOCK, stream=None):
+    """msa_sparse_decode for callers that cannot allocate where they decode: the library's fixed
+    device scratch replaces the workspace, and the outputs o [S,H_q,d_h] bf16 and
+    lse [S,H_q] fp32 (and optionally idx_out [S,H_kv,k] int32) must be passed in.  Calls that
+    overlap on the GPU share that scratch and must be serialised."""
+    _req(q, torch.bfloat16, 3, "q")
+    _req(q_idx, torch.bfloat16, 3, "q_idx")
+    _req(k_cache, torch.bfloat16, 3, "k_cache")
+    _req(v_cache, torch.bfloat16, 3, "v_cache")
+    _req(k_idx_cache, torch.bfloat16, 2, "k_idx_cache")
+    _req(cu_seqlens, torch.int64, 1, "cu_seqlens")
+    _req(o, torch.bfloat16, 3, "o")
+    _req(lse, torch.float32, 2, "lse")
+    S, H_q, d_h = q.shape
+    H_kv, d_idx = q_idx.shape[1], q_idx.shape[2]
+    _check("msa_sparse_decode_noalloc", lib.msa_sparse_decode_noalloc(
+        _ptr(q), _ptr(q_idx), _ptr(k_cache), _ptr(v_cache), _ptr(k_idx_cache), _ptr(cu_seqlens),
+        S, max_len, H_q, H_kv, d_h, d_idx, block_size, k, _ptr(o), _ptr(lse), _ptr(idx_out),
+        _stream(stream)))
     return o, lse, idx_out
 
 

@@ -119,6 +119,30 @@ msa_status_t msa_sparse_decode(const void *q, const void *q_idx, const void *k_c
                                float *lse, int32_t *idx_out, void *ws, size_t ws_bytes,
                                void *stream);
 
+/* Size of the fixed device scratch used by msa_sparse_decode_noalloc (8 MiB). */
+#define MSA_DECODE_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+/* Decode exactly as msa_sparse_decode, for callers that cannot allocate device memory where they
+ * decode (a runtime that reserved all device memory for its own pool, or a latency-critical loop
+ * that must not call cudaMalloc/cudaFree, which can block or synchronise).  The paper has no
+ * counterpart to this entry point; it changes where the scratch lives, not what is computed.
+ *   - Arguments and results are those of msa_sparse_decode without ws/ws_bytes; the caller still
+ *     owns and passes every input and output.  Nothing is allocated by the call.
+ *   - The temporaries (block scores, selections, split partials) live in a fixed device array of
+ *     MSA_DECODE_NOALLOC_SCRATCH_BYTES inside libmsa.so, held by every GPU that loads the library
+ *     until the process exits.  Sizes whose msa_sparse_decode_workspace() exceeds it return
+ *     MSA_ERR_WORKSPACE before any launch.
+ *   - The first call on each device looks up the array's device address (cudaGetSymbolAddress)
+ *     with that device current; make that first call before capturing any stream.
+ *   - All calls share the array and it keeps the last call's contents (nothing in it needs to
+ *     start at zero).  Calls whose GPU work overlaps -- on different streams or from different
+ *     host threads on one device -- race on it and must be serialised by the caller. */
+msa_status_t msa_sparse_decode_noalloc(const void *q, const void *q_idx, const void *k_cache,
+                                       const void *v_cache, const void *k_idx_cache,
+                                       const int64_t *cu_seqlens, int S, int64_t max_len, int H_q,
+                                       int H_kv, int d_h, int d_idx, int block_size, int k,
+                                       void *o, float *lse, int32_t *idx_out, void *stream);
+
 /* Reads and clears the device status words of the current device (synchronising call).
  * Returns MSA_ERR_TIMEOUT if any kernel since the last call gave up a bounded wait,
  * MSA_ERR_CUDA if the read itself failed, MSA_OK otherwise. */
