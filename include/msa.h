@@ -19,7 +19,7 @@
  *   - bf16 tensors are passed as `const void*` / `void*` (IEEE bfloat16 bit patterns),
  *     contiguous, row-major, 16-byte aligned base.
  *   - block_size must be 64.  Scales are fixed by the formulas (1/sqrt(d_idx), 1/sqrt(d_h)).
- *   - Supported shapes: H_kv in {1,2,4,8,16}; G = H_q/H_kv in {1,2,4,8}; d_h in {64,128};
+ *   - Supported shapes: H_kv in {1,2,4,8}; G = H_q/H_kv in {1,2,4,8}; d_h in {64,128};
  *     d_idx in {32,64}; 1 <= k <= 64.  Other valid shapes return MSA_ERR_UNSUPPORTED.
  *   - Inputs must be finite (no inf/NaN).
  *   - Host-side validation happens before any launch: a bad argument returns
