@@ -35,9 +35,14 @@ sys.path.insert(0, ROOT)
 import gen  # noqa: E402
 
 METRIC = ("MSA prefill tokens/s and decode tokens/s at 128K ctx; % of bf16 TC / HBM roofline")
-LAUNCHES_PER_STEP = 7       # scores, select, attention; decode: scores, select, attention, merge
-KERNEL_FILES = {"k_index_block_scores": "k_score.cu", "k_select_prefill": "k_select.cu",
-                "k_sparse_attn": "k_attn.cu", "decode": "k_decode.cu"}
+# kernels per step: scores, select; attention per 16384-row chunk: plan, scan, plan, block-major
+# pass, shared-block pass, merge (+ one memset); decode: scores, select, attention, merge
+ATTN_LAUNCHES_PER_CHUNK = 6
+DECODE_LAUNCHES = 4
+KERNEL_FILES = {"k_index_block_scores": ["k_score.cu"], "k_select_prefill": ["k_select.cu"],
+                "main_branch": ["k_attn_tiled.cu", "k_attn_kvouter.cu", "k_attn_plan.cu",
+                                "attn_tile.cuh"],
+                "decode": ["k_decode.cu", "k_select.cu", "k_attn.cu"]}
 
 
 # ------------------------------------------------------------------------ helpers --
@@ -82,9 +87,11 @@ def peaks():
     return dict(hbm=6800.0, bf16=1900.0, bf16_sust=1700.0, src="fallback")
 
 
-def kernel_source_hash(fname):
-    return hashlib.sha256(open(os.path.join(ROOT, "block_sparse_gqa_scores_gb300", "csrc",
-                                            fname), "rb").read()).hexdigest()[:16]
+def kernel_source_hash(fnames):
+    h = hashlib.sha256()
+    for f in fnames:
+        h.update(open(os.path.join(ROOT, "block_sparse_gqa_scores_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
 
 
 def ncu_traffic(kernel):
@@ -176,6 +183,9 @@ def setup(pcfg, dcfg, seed=0):
         idx=torch.empty((pcfg.H_kv, N, pcfg.k), dtype=torch.int32, device="cuda"),
         o=torch.empty_like(x["q"]),
         lse=torch.empty((pcfg.H_q, N), dtype=torch.float32, device="cuda"),
+        ws=torch.empty(max(16, msa.msa_sparse_attn_fwd_workspace(N, pcfg.H_q, pcfg.H_kv, pcfg.d_h,
+                                                                   pcfg.k)),
+                       dtype=torch.uint8, device="cuda"),
     )
     if dcfg is None:
         return msa, x, bufs, None, None
@@ -204,7 +214,8 @@ def run_msa(args, world, rank, local):
         ev[1].record(stream)
         msa.msa_select_blocks(bufs["M"], N, pcfg.k, idx=bufs["idx"])
         ev[2].record(stream)
-        msa.msa_sparse_attn_fwd(x["q"], x["k"], x["v"], bufs["idx"], o=bufs["o"], lse=bufs["lse"])
+        msa.msa_sparse_attn_fwd(x["q"], x["k"], x["v"], bufs["idx"], o=bufs["o"], lse=bufs["lse"],
+                                ws=bufs["ws"])
 
     def decode():
         if d is None:
@@ -267,8 +278,8 @@ def run_msa(args, world, rank, local):
         ncu_traffic("k_index_block_scores"))
     add("k_select_prefill", t_select, "hbm", sizes["select_bytes"], "GB/s", pk["hbm"],
         ncu_traffic("k_select_prefill"))
-    add("k_sparse_attn", t_attn, "tensor", sizes["F_main"], "TFLOP/s", pk["bf16_sust"],
-        ncu_traffic("k_sparse_attn"))
+    add("main_branch", t_attn, "tensor", sizes["F_main"], "TFLOP/s", pk["bf16_sust"],
+        ncu_traffic("main_branch"))
     if d is not None:
         add("decode (4 kernels)", t_decode, "hbm", sizes["decode_bytes"], "GB/s", pk["hbm"],
             ncu_traffic("decode"))
@@ -303,7 +314,8 @@ def run_msa(args, world, rank, local):
                      "peak_source": "%s (%s)" % (pk["src"], "bf16 sustained" if dom["unit"] ==
                                                  "TFLOP/s" else "HBM copy")},
         "clocks": clk,
-        "gpu_launches": (LAUNCHES_PER_STEP if d is not None else 3) * K,
+        "gpu_launches": (2 + ATTN_LAUNCHES_PER_CHUNK * (-(-N // 16384)) +
+                         (DECODE_LAUNCHES if d is not None else 0)) * K,
     }
     if not args.no_e2e:
         line["e2e"] = e2e_prefill(msa, pcfg, x, bufs, K, W, world)
@@ -329,7 +341,8 @@ def e2e_prefill(msa, pcfg, x, bufs, K, W, world):
             dev[n].copy_(host[n], non_blocking=True)
         M = msa.msa_index_block_scores(dev["q_idx"], dev["k_idx"], M=bufs["M"])
         idx = msa.msa_select_blocks(M, N, pcfg.k, idx=bufs["idx"])
-        msa.msa_sparse_attn_fwd(dev["q"], dev["k"], dev["v"], idx, o=bufs["o"], lse=bufs["lse"])
+        msa.msa_sparse_attn_fwd(dev["q"], dev["k"], dev["v"], idx, o=bufs["o"], lse=bufs["lse"],
+                                ws=bufs["ws"])
         o_h.copy_(bufs["o"], non_blocking=True)
         l_h.copy_(bufs["lse"], non_blocking=True)
 

@@ -137,17 +137,16 @@ MSA_API msa_status_t msa_select_blocks(const float* M, int32_t* idx, int64_t N, 
 }
 
 MSA_API size_t msa_sparse_attn_fwd_workspace(int64_t N, int H_q, int H_kv, int d_h, int k) {
-  (void)N, (void)H_q, (void)H_kv, (void)d_h, (void)k;
-  return 0;
+  if (N < 1 || H_kv < 1 || H_q < H_kv || H_q % H_kv != 0 || k < 1 || k > 64 || d_h < 1) return 0;
+  return msa::sparse_attn_ws_bytes(N, H_q, H_kv, d_h, k);
 }
 
 MSA_API msa_status_t msa_sparse_attn_fwd(const void* q, const void* k, const void* v,
                                          const int32_t* idx, void* o, float* lse, int64_t N,
                                          int H_q, int H_kv, int d_h, int block_size, int k_blocks,
                                          void* ws, size_t ws_bytes, void* stream) {
-  (void)ws;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned4(idx) || !aligned16(o) ||
-      !aligned4(lse))
+      !aligned4(lse) || !aligned16(ws))
     return MSA_ERR_INVALID_ARGUMENT;
   if (N < 1 || H_q < 1 || H_kv < 1 || H_q % H_kv != 0 || d_h < 1 || block_size != 64 ||
       k_blocks < 1 || k_blocks > 64)
@@ -157,8 +156,8 @@ MSA_API msa_status_t msa_sparse_attn_fwd(const void* q, const void* k, const voi
   if (N * H_kv >= kMaxRows) return MSA_ERR_UNSUPPORTED;
   if (ws_bytes < msa_sparse_attn_fwd_workspace(N, H_q, H_kv, d_h, k_blocks))
     return MSA_ERR_WORKSPACE;
-  return from_cuda(msa::launch_sparse_attn_tiled(q, k, v, idx, o, lse, N, H_q, H_kv, d_h,
-                                                 k_blocks, (cudaStream_t)stream));
+  return from_cuda(msa::launch_sparse_attn_fwd(q, k, v, idx, o, lse, N, H_q, H_kv, d_h, k_blocks,
+                                               ws, (cudaStream_t)stream));
 }
 
 MSA_API size_t msa_sparse_decode_workspace(int S, int64_t max_len, int H_q, int H_kv, int d_h,
@@ -204,8 +203,9 @@ MSA_API msa_status_t msa_sparse_decode(const void* q, const void* q_idx, const v
 }
 
 MSA_API msa_status_t msa_device_status(void) {
-  unsigned v = 0, w = 0;
+  unsigned v = 0, w = 0, x = 0;
   if (msa::read_reset_score_status(&v) != cudaSuccess) return MSA_ERR_CUDA;
   if (msa::read_reset_attn_status(&w) != cudaSuccess) return MSA_ERR_CUDA;
-  return (v | w) ? MSA_ERR_TIMEOUT : MSA_OK;
+  if (msa::read_reset_kvo_status(&x) != cudaSuccess) return MSA_ERR_CUDA;
+  return (v | w | x) ? MSA_ERR_TIMEOUT : MSA_OK;
 }

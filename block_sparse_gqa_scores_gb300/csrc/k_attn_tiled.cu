@@ -1,31 +1,30 @@
-// Sparse main branch of MSA for prefill («MiniMax-M3：MSA 技术报告速读», section 主分支, eq.
-// O^(h)_i, and the LSE of section Kernel), organised so that a KV block selected by several
-// nearby queries is read from L2 once.
+// Shared-block pass of the sparse main branch («MiniMax-M3：MSA 技术报告速读», section 主分支,
+// eq. O^(h)_i, and the LSE of section Kernel): the KV blocks that two or more queries of an
+// 8-query tile selected are read from L2 once for the tile.  Blocks only one query selected go
+// to the block-major pass (k_attn_kvouter.cu); k_attn_merge combines both kinds of partial.
 //
 // One CTA = 8 consecutive queries of one KV group r: 8 consumer warps (warp w owns query
 // i0+w and its G <= 8 heads) and one TMA producer warp.
-//   1. The producer warp forms the union of the 8 queries' selected blocks (ascending) and,
-//      per block, a bit mask of the queries that selected it: one warp-wide bitonic sort of
-//      (block << 3 | query) keys.  Blocks shared by nearby queries -- the local block, and
-//      blocks that many queries pick -- therefore enter shared memory once.
-//   2. The producer streams the union as 32-token half blocks (K and V of group r, a 3-D
-//      tensor map over [N, H_kv, d_h] with 128-byte swizzle) through a 6-stage ring.  When it
-//      fills a stage it arrives on the stage's "empty" barrier on behalf of every warp whose
-//      query did not select the block, so each consumer touches only its own stages and the
-//      warps run independently.  Because a consumer may skip whole ring turns, it first waits
-//      for the producer's count of issued stages to pass its stage: the previous turn of that
-//      slot has then landed and been released, and the next turn cannot be issued before this
-//      consumer releases it, so the slot's "full" parity names exactly one turn.
+//   1. The producer warp forms the union of the 8 queries' selected blocks with a per-block mask
+//      of the queries that selected it (attn_tile.cuh) and keeps the blocks with >= 2 users.
+//   2. It streams them as 32-token half blocks (K and V of group r, a 3-D tensor map over
+//      [N, H_kv, d_h] with 128-byte swizzle) through a 6-stage ring.  When it fills a stage it
+//      arrives on the stage's "empty" barrier on behalf of every warp whose query did not
+//      select the block, so each consumer touches only its own stages.  Because a consumer may
+//      skip whole ring turns, it first waits for the producer's count of issued stages to pass
+//      its stage: the previous turn of that slot has then landed and been released, and the
+//      next turn cannot be issued before this consumer releases it, so the slot's "full"
+//      parity names exactly one turn.
 //   3. A consumer computes on the blocks its query selected: S^T = K Q^T and O^T += V^T P^T
 //      as m16n8k16 MMAs with the group's heads on N = 8, operands by ldmatrix /
 //      ldmatrix.trans from the swizzled tiles, online softmax in the log2 domain.
-//   4. Each warp normalises its own query's state and writes O (8x8 tiles transposed back with
-//      movmatrix) and LSE.  Results are independent of the tile's other queries.
+//   4. Each warp writes its query's partial: O normalised by its own sum (bf16, [G, d_h]) and
+//      the log2-domain LSE (-inf when the query shares no block with its tile).
 // All mbarrier waits are bounded; a timeout sets the device status word and ends the loop.
 #include <climits>
 #include <cmath>
 
-#include "msa_device.cuh"
+#include "attn_tile.cuh"
 #include "msa_internal.h"
 
 namespace msa {
@@ -54,85 +53,12 @@ struct TiledSmem {
   static constexpr int kAlloc = kBytes + 1024;
 };
 
-// Ascending bitonic sort of the 32*EPL keys a warp holds lane-major (element EPL*lane + j).
 template <int EPL>
-__device__ __forceinline__ void warp_sort(int (&x)[EPL]) {
-  const int lane = threadIdx.x & 31;
-#pragma unroll
-  for (int size = 2; size <= 32 * EPL; size <<= 1) {
-#pragma unroll
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      int nx[EPL];
-#pragma unroll
-      for (int j = 0; j < EPL; ++j) {
-        const int e = EPL * lane + j;
-        const int other = stride < EPL ? x[j ^ stride] : __shfl_xor_sync(kFull, x[j], stride / EPL);
-        const bool lower = (e & stride) == 0, asc = (e & size) == 0;
-        nx[j] = (lower == asc) ? min(x[j], other) : max(x[j], other);
-      }
-#pragma unroll
-      for (int j = 0; j < EPL; ++j) x[j] = nx[j];
-    }
-  }
-}
-
-// Union of the tile's selections (called by one whole warp): s_U[0..nU) ascending distinct
-// visible blocks, s_mask[u] = bit w set when query i0+w selected s_U[u].  Returns nU.
-template <int EPL>
-__device__ __forceinline__ int build_union(const int32_t* __restrict__ idx, int r, int64_t i0,
-                                           int64_t N, int kk, int* s_U, unsigned* s_mask) {
-  const int lane = threadIdx.x & 31;
-  const int n = kQT * kk;
-  int x[EPL];
-#pragma unroll
-  for (int j = 0; j < EPL; ++j) {
-    const int e = EPL * lane + j;
-    int key = INT_MAX;
-    if (e < n) {
-      const int w = e / kk;
-      const int64_t i = i0 + w;
-      if (i < N) {
-        const int b = __ldg(idx + ((int64_t)r * N + i) * kk + (e - w * kk));
-        if (b >= 0 && (int64_t)b <= (i >> 6)) key = (b << 3) | w;   // visible blocks only
-      }
-    }
-    x[j] = key;
-  }
-  warp_sort<EPL>(x);
-  // run heads (first key of each distinct block) and their ranks
-  int prev = __shfl_up_sync(kFull, x[EPL - 1], 1);
-  if (lane == 0) prev = INT_MIN;
-  int head[EPL], cnt = 0;
-#pragma unroll
-  for (int j = 0; j < EPL; ++j) {
-    const int pk = j ? x[j - 1] : prev;
-    head[j] = (x[j] != INT_MAX) && (j == 0 ? (prev == INT_MIN || (pk >> 3) != (x[j] >> 3))
-                                           : ((pk >> 3) != (x[j] >> 3)));
-    cnt += head[j];
-  }
-  int incl = cnt;                                   // inclusive scan of head counts
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int t = __shfl_up_sync(kFull, incl, o);
-    if (lane >= o) incl += t;
-  }
-  const int nU = __shfl_sync(kFull, incl, 31);
-  int rank[EPL], run = incl - cnt;
-#pragma unroll
-  for (int j = 0; j < EPL; ++j) {
-    run += head[j];
-    rank[j] = run - 1;                              // union slot of this key's block
-    if (head[j]) {
-      s_U[rank[j]] = x[j] >> 3;
-      s_mask[rank[j]] = 0u;
-    }
-  }
-  __syncwarp();
-#pragma unroll
-  for (int j = 0; j < EPL; ++j)
-    if (x[j] != INT_MAX) atomicOr(&s_mask[rank[j]], 1u << (x[j] & 7));
-  __syncwarp();
-  return nU;
+__device__ __forceinline__ int union_of(const int32_t* __restrict__ idx, int r, int64_t i0,
+                                       int64_t i_end, int64_t N, int kk, int* s_U,
+                                       unsigned* s_mask) {
+  int x[EPL], rank[EPL];
+  return tile_union<EPL>(idx, r, i0, i_end, N, kk, x, rank, s_U, s_mask);
 }
 
 template <int D_H>
@@ -140,8 +66,9 @@ __global__ void __launch_bounds__(kThreads, 2)
     k_sparse_attn_tiled(const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v,
                         const __nv_bfloat16* __restrict__ q, const int32_t* __restrict__ idx,
-                        __nv_bfloat16* __restrict__ o, float* __restrict__ lse, int64_t N, int H_q,
-                        int G, int kk, int64_t ntiles, float scale_log2) {
+                        __nv_bfloat16* __restrict__ tp_o, float* __restrict__ tp_lse, int64_t N,
+                        int64_t q0, int64_t q1, int H_q, int G, int kk, int64_t ntiles,
+                        float scale_log2) {
   using L = TiledSmem<D_H>;
   constexpr int KS = D_H / 16;
   extern __shared__ uint8_t smem_raw[];
@@ -158,18 +85,34 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t bid = blockIdx.x;
   const int r = (int)(bid / ntiles);
-  const int64_t i0 = (bid - (int64_t)r * ntiles) * kQT;
+  const int64_t i0 = q0 + (bid - (int64_t)r * ntiles) * kQT;
 
-  // ---- 1. union of the tile's selections (producer warp), barrier init
+  // ---- 1. the tile's shared blocks (producer warp), barrier init
   if (warp == kQT) {
     int nU;
-    if (kk <= 4) nU = build_union<1>(idx, r, i0, N, kk, s_U, s_mask);
-    else if (kk <= 8) nU = build_union<2>(idx, r, i0, N, kk, s_U, s_mask);
-    else if (kk <= 16) nU = build_union<4>(idx, r, i0, N, kk, s_U, s_mask);
-    else if (kk <= 32) nU = build_union<8>(idx, r, i0, N, kk, s_U, s_mask);
-    else nU = build_union<16>(idx, r, i0, N, kk, s_U, s_mask);
+    if (kk <= 4) nU = union_of<1>(idx, r, i0, q1, N, kk, s_U, s_mask);
+    else if (kk <= 8) nU = union_of<2>(idx, r, i0, q1, N, kk, s_U, s_mask);
+    else if (kk <= 16) nU = union_of<4>(idx, r, i0, q1, N, kk, s_U, s_mask);
+    else if (kk <= 32) nU = union_of<8>(idx, r, i0, q1, N, kk, s_U, s_mask);
+    else nU = union_of<16>(idx, r, i0, q1, N, kk, s_U, s_mask);
+    int nS = 0;                                       // keep blocks with two or more users
+    for (int base = 0; base < nU; base += 32) {
+      const int u = base + lane;
+      const int bu = u < nU ? s_U[u] : 0;
+      const unsigned mu = u < nU ? s_mask[u] : 0u;
+      const bool keep = __popc(mu) >= 2;
+      const unsigned kb = __ballot_sync(kAllLanes, keep);
+      __syncwarp();
+      if (keep) {
+        const int pos = nS + __popc(kb & ((1u << lane) - 1u));
+        s_U[pos] = bu;
+        s_mask[pos] = mu;
+      }
+      nS += __popc(kb);
+      __syncwarp();
+    }
     if (lane == 0) {
-      *s_nU = nU;
+      *s_nU = nS;
       *s_issued = 0;
       for (int s = 0; s < kStages; ++s) {
         mbar_init(full(s), 1);
@@ -215,7 +158,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   // ------------------------------------------------------------------ consumers
   const int c = lane & 3, r4 = lane >> 2;
   const int64_t i = i0 + warp;
-  const bool valid = i < N;
+  const bool valid = i < q1;
   const int hq0 = r * G;
 
   uint32_t qf[KS][2];
@@ -342,16 +285,15 @@ __global__ void __launch_bounds__(kThreads, 2)
     inv[hh] = t > 0.f ? 1.f / t : 0.f;
   }
   if (valid) {
+    const int64_t unit = (int64_t)r * (q1 - q0) + (i - q0);   // partial row of this query
     if (r4 == 0) {
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         const int h = 2 * c + hh;
-        if (h < G)
-          lse[(int64_t)(hq0 + h) * N + i] =
-              lsum[hh] > 0.f ? (m_run[hh] + __log2f(lsum[hh])) * 0.69314718055994531f : -INFINITY;
+        if (h < G) tp_lse[unit * G + h] = lsum[hh] > 0.f ? m_run[hh] + __log2f(lsum[hh]) : -INFINITY;
       }
     }
-    uint32_t* orow = reinterpret_cast<uint32_t*>(o + (i * H_q + hq0 + (r4 < G ? r4 : 0)) * D_H);
+    uint32_t* orow = reinterpret_cast<uint32_t*>(tp_o + (unit * G + (r4 < G ? r4 : 0)) * D_H);
 #pragma unroll
     for (int mtd = 0; mtd < KS; ++mtd) {
       const uint32_t lo = movmatrix_trans(pack_bf16x2(oacc[mtd][0] * inv[0], oacc[mtd][1] * inv[1]));
@@ -366,32 +308,105 @@ __global__ void __launch_bounds__(kThreads, 2)
 
 template <int D_H>
 cudaError_t launch_tiled(const CUtensorMap& tk, const CUtensorMap& tv, const void* q,
-                         const int32_t* idx, void* o, float* lse, int64_t N, int H_q, int H_kv,
-                         int kk, cudaStream_t stream) {
+                         const int32_t* idx, void* tp_o, float* tp_lse, int64_t N, int64_t q0,
+                         int64_t q1, int H_q, int H_kv, int kk, cudaStream_t stream) {
   using L = TiledSmem<D_H>;
   auto kern = k_sparse_attn_tiled<D_H>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
   if (e != cudaSuccess) return e;
-  const int64_t ntiles = (N + kQT - 1) / kQT;
+  const int64_t ntiles = (q1 - q0 + kQT - 1) / kQT;
   const float scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D_H));
   kern<<<(unsigned)(ntiles * H_kv), kThreads, L::kAlloc, stream>>>(
-      tk, tv, static_cast<const __nv_bfloat16*>(q), idx, static_cast<__nv_bfloat16*>(o), lse, N,
-      H_q, H_q / H_kv, kk, ntiles, scale_log2);
+      tk, tv, static_cast<const __nv_bfloat16*>(q), idx, static_cast<__nv_bfloat16*>(tp_o), tp_lse,
+      N, q0, q1, H_q, H_q / H_kv, kk, ntiles, scale_log2);
   return cudaGetLastError();
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+constexpr int64_t kChunkRows = 16384;     // query rows per pass (bounds the workspace)
+
+struct AttnWs {
+  size_t count, offset, tile_off, cursor, entries, slotmap, part_o, part_lse, tp_o, tp_lse, total;
+  int64_t qc;
+  int nb;
+};
+
+AttnWs attn_layout(int64_t N, int H_q, int H_kv, int d_h, int kk) {
+  AttnWs w{};
+  const int G = H_q / H_kv;
+  w.qc = ((N < kChunkRows ? N : kChunkRows) + kQT - 1) / kQT * kQT;
+  const int64_t nblk = (N + kBlock - 1) / kBlock;
+  w.nb = (int)(H_kv * nblk);
+  const size_t sel = (size_t)H_kv * w.qc * kk;            // selections of one chunk
+  size_t off = 0;
+  auto take = [&](size_t bytes) { const size_t o = off; off = align256(off + bytes); return o; };
+  w.count = take(4 * (size_t)(w.nb + 1));
+  w.offset = take(4 * (size_t)(w.nb + 1));
+  w.tile_off = take(4 * (size_t)(w.nb + 1));
+  w.cursor = take(4 * (size_t)(w.nb + 1));
+  w.entries = take(4 * sel);
+  w.slotmap = take(4 * sel);
+  w.part_o = take(2 * sel * G * d_h);
+  w.part_lse = take(4 * sel * G);
+  w.tp_o = take(2 * (size_t)H_kv * w.qc * G * d_h);
+  w.tp_lse = take(4 * (size_t)H_kv * w.qc * G);
+  w.total = off;
+  return w;
 }
 
 }  // namespace
 
-cudaError_t launch_sparse_attn_tiled(const void* q, const void* k, const void* v,
-                                     const int32_t* idx, void* o, float* lse, int64_t N, int H_q,
-                                     int H_kv, int d_h, int kk, cudaStream_t stream) {
+size_t sparse_attn_ws_bytes(int64_t N, int H_q, int H_kv, int d_h, int kk) {
+  return attn_layout(N, H_q, H_kv, d_h, kk).total;
+}
+
+// The main branch over query chunks: plan (count) -> scan -> plan (scatter) -> block-major pass
+// over private selections -> shared-block pass -> merge.  Everything is enqueued on `stream`.
+cudaError_t launch_sparse_attn_fwd(const void* q, const void* k, const void* v, const int32_t* idx,
+                                   void* o, float* lse, int64_t N, int H_q, int H_kv, int d_h,
+                                   int kk, void* ws, cudaStream_t stream) {
+  const AttnWs w = attn_layout(N, H_q, H_kv, d_h, kk);
+  char* base = static_cast<char*>(ws);
+  int* count = reinterpret_cast<int*>(base + w.count);
+  int* offset = reinterpret_cast<int*>(base + w.offset);
+  int* tile_off = reinterpret_cast<int*>(base + w.tile_off);
+  int* cursor = reinterpret_cast<int*>(base + w.cursor);
+  int* entries = reinterpret_cast<int*>(base + w.entries);
+  int* slotmap = reinterpret_cast<int*>(base + w.slotmap);
+  void* part_o = base + w.part_o;
+  float* part_lse = reinterpret_cast<float*>(base + w.part_lse);
+  void* tp_o = base + w.tp_o;
+  float* tp_lse = reinterpret_cast<float*>(base + w.tp_lse);
+
   CUtensorMap tk, tv;
   cudaError_t e = make_tma_3d_bf16(&tk, k, (uint64_t)d_h, (uint64_t)H_kv, (uint64_t)N, 64, 1, kHalf, 128);
   if (e != cudaSuccess) return e;
   e = make_tma_3d_bf16(&tv, v, (uint64_t)d_h, (uint64_t)H_kv, (uint64_t)N, 64, 1, kHalf, 128);
   if (e != cudaSuccess) return e;
-  if (d_h == 128) return launch_tiled<128>(tk, tv, q, idx, o, lse, N, H_q, H_kv, kk, stream);
-  return launch_tiled<64>(tk, tv, q, idx, o, lse, N, H_q, H_kv, kk, stream);
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess)
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t nblk = (N + kBlock - 1) / kBlock;
+  const int G = H_q / H_kv;
+  for (int64_t q0 = 0; q0 < N; q0 += w.qc) {
+    const int64_t q1 = q0 + w.qc < N ? q0 + w.qc : N;
+    if ((e = cudaMemsetAsync(count, 0, 4 * (size_t)w.nb, stream)) != cudaSuccess) return e;
+    if ((e = launch_attn_plan(idx, N, H_kv, kk, q0, q1, q1 - q0, nblk, 0, count, offset, cursor,
+                              entries, slotmap, stream)) != cudaSuccess) return e;
+    if ((e = launch_attn_scan(count, offset, tile_off, cursor, w.nb, 128 / G, stream)) != cudaSuccess)
+      return e;
+    if ((e = launch_attn_plan(idx, N, H_kv, kk, q0, q1, q1 - q0, nblk, 1, count, offset, cursor,
+                              entries, slotmap, stream)) != cudaSuccess) return e;
+    if ((e = launch_attn_kvouter(q, k, v, entries, offset, tile_off, w.nb, nblk, N, q0, H_q, H_kv,
+                                 d_h, 2 * sms, part_o, part_lse, stream)) != cudaSuccess) return e;
+    e = d_h == 128 ? launch_tiled<128>(tk, tv, q, idx, tp_o, tp_lse, N, q0, q1, H_q, H_kv, kk, stream)
+                   : launch_tiled<64>(tk, tv, q, idx, tp_o, tp_lse, N, q0, q1, H_q, H_kv, kk, stream);
+    if (e != cudaSuccess) return e;
+    if ((e = launch_attn_merge(tp_o, tp_lse, slotmap, part_o, part_lse, o, lse, N, H_q, H_kv, d_h,
+                               kk, q0, q1, stream)) != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 cudaError_t read_reset_attn_status(unsigned* out) {

@@ -59,7 +59,7 @@ def select(lib, M=P, idx=P, N=1024, H_kv=4, B=64, k=16, qs=0, qc=1024):
 
 
 def attn(lib, q=P, k=P, v=P, idx=P, o=P, lse=P, N=1024, H_q=32, H_kv=4, d_h=128, B=64, kk=16,
-         ws=NUL, wsb=0):
+         ws=P, wsb=1 << 40):
     return lib.msa_sparse_attn_fwd(q, k, v, idx, o, lse, i64(N), H_q, H_kv, d_h, B, kk, ws,
                                    ctypes.c_size_t(wsb), NUL)
 
@@ -91,7 +91,7 @@ def test_select_invalid(lib, kw):
 
 
 @pytest.mark.parametrize("kw", [dict(q=NUL), dict(o=MIS), dict(N=0), dict(H_q=30), dict(kk=0),
-                                dict(kk=100), dict(B=16)])
+                                dict(kk=100), dict(B=16), dict(ws=NUL), dict(ws=MIS)])
 def test_attn_invalid(lib, kw):
     assert attn(lib, **kw) == INVALID
 
@@ -126,4 +126,10 @@ def test_workspace_sizes(lib):
     nblk = L // 64
     floor = 4 * S * H_kv * nblk + 4 * S * H_kv * k + 4 * S * H_kv * 4 * (H_q // H_kv) * (d_h + 1)
     assert floor <= need <= floor + 4 * 256
-    assert lib.msa_sparse_attn_fwd_workspace(i64(1024), 8, 2, 64, 4) == 0
+    # main branch: per query chunk (<= 16384 rows) the bucket arrays, entries, slot map, the
+    # private partials (bf16 O + fp32 LSE per selection) and the shared-block partials
+    need = lib.msa_sparse_attn_fwd_workspace(i64(1024), 8, 2, 64, 4)
+    sel = 2 * 1024 * 4
+    floor = 4 * 2 * sel + sel * 4 * (64 * 2 + 4) + 2 * 1024 * 4 * (64 * 2 + 4) + 4 * 4 * (2 * 16 + 1)
+    assert floor <= need <= floor + 10 * 256
+    assert attn(lib, N=1024, H_q=8, H_kv=2, d_h=64, kk=4, wsb=need - 1) == WORKSPACE
