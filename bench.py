@@ -36,12 +36,12 @@ import gen  # noqa: E402
 
 METRIC = ("MSA prefill tokens/s and decode tokens/s at 128K ctx; % of bf16 TC / HBM roofline")
 # kernels per step: scores, select; attention per 16384-row chunk: plan, scan, plan, block-major
-# pass, shared-block pass, merge (+ one memset); decode: scores, select, attention, merge
-ATTN_LAUNCHES_PER_CHUNK = 6
+# pass, shared-block pass with the merge (+ one memset); decode: scores, select, attention, merge
+ATTN_LAUNCHES_PER_CHUNK = 5
 DECODE_LAUNCHES = 4
 KERNEL_FILES = {"k_index_block_scores": ["k_score.cu"], "k_select_prefill": ["k_select.cu"],
-                "main_branch": ["k_attn_tiled.cu", "k_attn_kvouter.cu", "k_attn_plan.cu",
-                                "attn_tile.cuh"],
+                "main_branch": ["attn_fwd.cu", "k_attn_shared.cu", "k_attn_kvouter.cu",
+                                "k_attn_plan.cu", "attn_tile.cuh"],
                 "decode": ["k_decode.cu", "k_select.cu", "k_attn.cu"]}
 
 

@@ -153,7 +153,7 @@ MSA_API msa_status_t msa_sparse_attn_fwd(const void* q, const void* k, const voi
     return MSA_ERR_INVALID_ARGUMENT;
   if (!pow2_upto(H_kv, 8) || !pow2_upto(H_q / H_kv, 8) || (d_h != 64 && d_h != 128))
     return MSA_ERR_UNSUPPORTED;
-  if (N * H_kv >= kMaxRows) return MSA_ERR_UNSUPPORTED;
+  if (N * H_kv >= kMaxRows || N > ((int64_t)1 << 21)) return MSA_ERR_UNSUPPORTED;
   if (ws_bytes < msa_sparse_attn_fwd_workspace(N, H_q, H_kv, d_h, k_blocks))
     return MSA_ERR_WORKSPACE;
   return from_cuda(msa::launch_sparse_attn_fwd(q, k, v, idx, o, lse, N, H_q, H_kv, d_h, k_blocks,
@@ -205,7 +205,7 @@ MSA_API msa_status_t msa_sparse_decode(const void* q, const void* q_idx, const v
 MSA_API msa_status_t msa_device_status(void) {
   unsigned v = 0, w = 0, x = 0;
   if (msa::read_reset_score_status(&v) != cudaSuccess) return MSA_ERR_CUDA;
-  if (msa::read_reset_attn_status(&w) != cudaSuccess) return MSA_ERR_CUDA;
+  if (msa::read_reset_shared_status(&w) != cudaSuccess) return MSA_ERR_CUDA;
   if (msa::read_reset_kvo_status(&x) != cudaSuccess) return MSA_ERR_CUDA;
   return (v | w | x) ? MSA_ERR_TIMEOUT : MSA_OK;
 }

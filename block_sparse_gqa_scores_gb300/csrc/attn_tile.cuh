@@ -1,20 +1,34 @@
-// The 8-query tile of the main branch: union of the tile's block selections.
+// The 16-query tile of the main branch: union of the tile's block selections.
 //
-// A tile is 8 consecutive queries of one KV group (they always fall in the same 64-token block).
-// Its selections are sorted as (block, query, slot) keys by one warp; the distinct blocks form
-// the tile's union and each gets a mask of the queries that selected it.  A block selected by
-// two or more of the tile's queries is "shared" and is read once for the tile; a block selected
-// by exactly one query is "private" and goes to the block-major (KV-outer) pass.
+// A tile is 16 consecutive queries of one KV group (they always fall in the same 64-token
+// block); with G <= 8 heads their rows fill one 128-row UMMA tile.  The tile's selections are
+// sorted as (block, query, slot) keys by one warp; the distinct blocks form the tile's union and
+// each gets a mask of the queries that selected it.  A block selected by two or more of the
+// tile's queries is "shared" and is processed once for the tile; a block selected by exactly one
+// query is "private" and goes to the block-major (KV-outer) pass.
 #pragma once
 
 #include <climits>
+#include <type_traits>
 
 #include "msa_device.cuh"
 
 namespace msa {
 
-constexpr int kTileQ = 8;          // queries per tile
+constexpr int kTileQ = 16;         // queries per tile
 constexpr int kMaxSel = 64;        // largest k supported
+constexpr int kMaxKeys = kTileQ * kMaxSel;
+
+// Keys per lane for a tile's 16*k selections (a power of two, 32*EPL >= 16*k).
+template <typename F>
+__device__ __forceinline__ auto with_epl(int kk, F&& f) {
+  if (kk <= 2) return f(std::integral_constant<int, 1>());
+  if (kk <= 4) return f(std::integral_constant<int, 2>());
+  if (kk <= 8) return f(std::integral_constant<int, 4>());
+  if (kk <= 16) return f(std::integral_constant<int, 8>());
+  if (kk <= 32) return f(std::integral_constant<int, 16>());
+  return f(std::integral_constant<int, 32>());
+}
 constexpr unsigned kAllLanes = 0xffffffffu;
 
 // Ascending bitonic sort of the 32*EPL keys a warp holds lane-major (element EPL*lane + j).
@@ -40,12 +54,12 @@ __device__ __forceinline__ void warp_sort(int (&x)[EPL]) {
   }
 }
 
-// Sorted selection keys of one tile: key = block << 9 | query-in-tile << 6 | slot, INT_MAX for
-// padding, -1 entries and blocks after the query's own block.  Queries at or after i_end are
-// not part of the tile.
+// Sorted selection keys of one tile: key = block << 10 | query-in-tile << 6 | slot, INT_MAX for
+// padding, -1 entries and blocks after the query's own block (block < 2^21).  Queries at or
+// after i_end are not part of the tile.
 struct TileKeys {
-  __device__ static int block(int key) { return key >> 9; }
-  __device__ static int query(int key) { return (key >> 6) & 7; }
+  __device__ static int block(int key) { return key >> 10; }
+  __device__ static int query(int key) { return (key >> 6) & 15; }
   __device__ static int slot(int key) { return key & 63; }
 };
 
@@ -66,7 +80,7 @@ __device__ __forceinline__ int tile_union(const int32_t* __restrict__ idx, int r
       const int64_t i = i0 + w;
       if (i < i_end) {
         const int b = __ldg(idx + ((int64_t)r * N + i) * kk + t);
-        if (b >= 0 && (int64_t)b <= (i >> 6)) key = (b << 9) | (w << 6) | t;
+        if (b >= 0 && (int64_t)b <= (i >> 6)) key = (b << 10) | (w << 6) | t;
       }
     }
     x[j] = key;
@@ -78,7 +92,7 @@ __device__ __forceinline__ int tile_union(const int32_t* __restrict__ idx, int r
 #pragma unroll
   for (int j = 0; j < EPL; ++j) {
     const int pk = j ? x[j - 1] : prev;
-    head[j] = x[j] != INT_MAX && (pk == INT_MIN || (pk >> 9) != (x[j] >> 9));
+    head[j] = x[j] != INT_MAX && (pk == INT_MIN || (pk >> 10) != (x[j] >> 10));
     cnt += head[j];
   }
   int incl = cnt;
@@ -94,14 +108,14 @@ __device__ __forceinline__ int tile_union(const int32_t* __restrict__ idx, int r
     run += head[j];
     rank[j] = run - 1;
     if (head[j]) {
-      s_U[rank[j]] = x[j] >> 9;
+      s_U[rank[j]] = x[j] >> 10;
       s_mask[rank[j]] = 0u;
     }
   }
   __syncwarp();
 #pragma unroll
   for (int j = 0; j < EPL; ++j)
-    if (x[j] != INT_MAX) atomicOr(&s_mask[rank[j]], 1u << ((x[j] >> 6) & 7));
+    if (x[j] != INT_MAX) atomicOr(&s_mask[rank[j]], 1u << ((x[j] >> 6) & 15));
   __syncwarp();
   return nU;
 }

@@ -12,7 +12,9 @@
 // A partial covers exactly one block, so no rescaling is needed; the merge kernel combines
 // the partials of a row with the shared-block partial in a fixed order.
 // Q rows, K_b and V_b are gathered with cp.async into 128-byte-swizzled tiles (the canonical
-// K-major / MN-major SW128 layouts).  Persistent grid; each tile finds its bucket by binary
+// K-major / MN-major SW128 layouts).  P reuses Q's shared memory and O reuses S's TMEM
+// columns, so three CTAs fit on an SM.  Persistent grid; each CTA takes a contiguous range of
+// work tiles (consecutive tiles often share K_b, V_b) and finds each tile's bucket by binary
 // search over the per-bucket tile offsets.
 #include <cmath>
 
@@ -33,14 +35,14 @@ struct KvoSmem {
   static constexpr int kQHalf = kRowsT * 128;     // 128 rows x 64 dims
   static constexpr int kKHalf = 64 * 128;         // 64 keys x 64 dims
   static constexpr int kOffQ = 0;
+  static constexpr int kOffP = 0;                 // P (128 rows x 64 keys) reuses Q's first half
   static constexpr int kOffK = kOffQ + kHalves * kQHalf;
   static constexpr int kOffV = kOffK + kHalves * kKHalf;
-  static constexpr int kOffP = kOffV + kHalves * kKHalf;   // 128 rows x 64 keys
-  static constexpr int kOffBar = kOffP + kRowsT * 128;
+  static constexpr int kOffBar = kOffV + kHalves * kKHalf;
   static constexpr int kOffMisc = kOffBar + 16;
   static constexpr int kBytes = kOffMisc + 16;
   static constexpr int kAlloc = kBytes + 1024;
-  static constexpr uint32_t kTmemCols = 256;      // S: 64 columns, O: d_h columns at 64
+  static constexpr uint32_t kTmemCols = D_H;      // S (64 columns), then O over the same columns
 };
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
@@ -73,7 +75,7 @@ __device__ __forceinline__ float rowmax64(const uint32_t* v) {
 }
 
 template <int D_H>
-__global__ void __launch_bounds__(kThreadsKvo, 2)
+__global__ void __launch_bounds__(kThreadsKvo, 3)
     k_attn_kvouter(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
                    const __nv_bfloat16* __restrict__ v, const int* __restrict__ entries,
                    const int* __restrict__ offset, const int* __restrict__ tile_off, int nbuckets,
@@ -100,7 +102,8 @@ __global__ void __launch_bounds__(kThreadsKvo, 2)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tmem_s = tmem, tmem_o = tmem + 64;
+  // S lives in columns [0, 64); O overwrites columns [0, d_h) once S has been read
+  const uint32_t tmem_s = tmem, tmem_o = tmem;
 
   const int total_tiles = tile_off[nbuckets];
   const int64_t kv_stride = (int64_t)H_kv * D_H;             // elements between tokens
@@ -108,7 +111,11 @@ __global__ void __launch_bounds__(kThreadsKvo, 2)
   int loaded_bucket = -1;
   bool ok = true;
 
-  for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
+  // a contiguous range of work tiles per CTA: consecutive tiles often share a bucket (K_b, V_b)
+  const int per = (total_tiles + gridDim.x - 1) / gridDim.x;
+  const int t_beg = blockIdx.x * per;
+  const int t_end = min(total_tiles, t_beg + per);
+  for (int tile = t_beg; tile < t_end && ok; ++tile) {
     // ---- which bucket: last b with tile_off[b] <= tile
     int lo = 0, hi = nbuckets;                               // tile_off[lo] <= tile < tile_off[hi]
     while (hi - lo > 1) {
