@@ -40,7 +40,8 @@ struct KvoSmem {
   static constexpr int kOffV = kOffK + kHalves * kKHalf;
   static constexpr int kOffBar = kOffV + kHalves * kKHalf;
   static constexpr int kOffMisc = kOffBar + 16;
-  static constexpr int kBytes = kOffMisc + 16;
+  static constexpr int kOffEnt = kOffMisc + 16;   // entries of the current tile (<= 128)
+  static constexpr int kBytes = kOffEnt + kRowsT * 4;
   static constexpr int kAlloc = kBytes + 1024;
   static constexpr uint32_t kTmemCols = D_H;      // S (64 columns), then O over the same columns
 };
@@ -88,6 +89,7 @@ __global__ void __launch_bounds__(kThreadsKvo, 3)
   const uint32_t sb = smem_u32(smem);
   const uint32_t mma_bar = sb + L::kOffBar;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffMisc);
+  int* s_ent = reinterpret_cast<int*>(smem + L::kOffEnt);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tid = threadIdx.x;
 
@@ -149,11 +151,12 @@ __global__ void __launch_bounds__(kThreadsKvo, 3)
       }
       loaded_bucket = bucket;
     }
+    if (tid < n_e) s_ent[tid] = __ldg(entries + e0 + tid);   // the tile's (row, slot) entries
+    __syncthreads();
     for (int x = tid; x < rows * kChunks; x += kThreadsKvo) {
       const int R = x / kChunks, c = x - R * kChunks;
       const int e = R / G, h = R - e * G;
-      const int ent = __ldg(entries + e0 + e);
-      const int64_t i = q0 + (ent >> 6);
+      const int64_t i = q0 + (s_ent[e] >> 6);
       const uint32_t off = (c >> 3) * L::kQHalf + R * 128 + (((c & 7) ^ (R & 7)) << 4);
       cp_async16(sb + L::kOffQ + off, q + (i * H_q + (int64_t)r * G + h) * D_H + c * 8);
     }
@@ -193,7 +196,7 @@ __global__ void __launch_bounds__(kThreadsKvo, 3)
         const int e = R / G;
         h = R - e * G;
         ent_pos = e0 + e;
-        i = q0 + (__ldg(entries + ent_pos) >> 6);
+        i = q0 + (s_ent[e] >> 6);
         if (b == (i >> 6)) {                                // local block: keys j <= i only
           const int lim = (int)(i - b * kBlock);
 #pragma unroll

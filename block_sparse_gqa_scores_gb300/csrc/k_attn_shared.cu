@@ -44,16 +44,27 @@ struct ShSmem {
   static constexpr int kStage = 2 * kKBytes;        // K boxes, then V boxes
   static constexpr int kOffQ = 0;
   static constexpr int kOffRing = kOffQ + kHalves * kQHalf;
-  static constexpr int kOffP = kOffRing + kRing * kStage;      // 128 rows x 32 keys, SW64
-  static constexpr int kOffList = kOffP + 128 * 64;
+  static constexpr int kOffP = kOffRing + kRing * kStage;      // 2 x (128 rows x 32 keys), SW64
+  static constexpr int kPBytes = 128 * 64;
+  static constexpr int kOffList = kOffP + 2 * kPBytes;
   static constexpr int kOffBar = kOffList + kMaxShared * 4;
-  // kv_full[kRing], kv_empty[kRing], s_full[2], s_free[2], p_full, p_free, q_ready, done
-  static constexpr int kNumBars = 2 * kRing + 8;
+  // kv_full[kRing], kv_empty[kRing], s_full[2], s_free[2], p_full[2], p_free[2], o_done,
+  // q_ready, done
+  static constexpr int kNumBars = 2 * kRing + 11;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kBytes = kOffMisc + 16;
   static constexpr int kAlloc = kBytes + 1024;
   static constexpr uint32_t kTmemCols = 256;        // S[0] 0..31, S[1] 32..63, O from 128
   static_assert(kRing * kStage >= kMaxKeys * 8, "the union is built in the ring");
+  // epilogue, over Q / ring / P once every MMA has completed: the rows' shared-block O (fp32,
+  // already weighted), per-row max and 1/sum of the merge, per query its private partials
+  static constexpr int kOsStride = D_H + 4;          // floats; 16-byte pad against conflicts
+  static constexpr int kOffOs = 0;
+  static constexpr int kOffMx = kOffOs + 128 * kOsStride * 4;
+  static constexpr int kOffInv = kOffMx + 128 * 4;
+  static constexpr int kOffPos = kOffInv + 128 * 4;
+  static constexpr int kOffNp = kOffPos + kTileQ * kMaxSel * 4;
+  static_assert(kOffNp + kTileQ * 4 <= kOffList, "epilogue staging fits below the block list");
 };
 
 #define MSA_TMEM_LD32(taddr, r)                                                                 \
@@ -100,6 +111,13 @@ __device__ __forceinline__ uint64_t desc_mn_sw128(uint32_t a, uint32_t lbo, uint
          ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
 
+__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p) : "memory");
+}
+
 template <int EPL>
 __device__ __forceinline__ int shared_blocks(const int32_t* __restrict__ idx, int r, int64_t i0,
                                              int64_t q1, int64_t N, int kk, int* tmpU,
@@ -140,8 +158,10 @@ __global__ void __launch_bounds__(kShThreads, 2)
   auto kv_empty = [&](int s) { return bar + 8u * (kRing + s); };
   auto s_full = [&](int b) { return bar + 8u * (2 * kRing + b); };
   auto s_free = [&](int b) { return bar + 8u * (2 * kRing + 2 + b); };
-  const uint32_t p_full = bar + 8u * (2 * kRing + 4), p_free = bar + 8u * (2 * kRing + 5);
-  const uint32_t q_ready = bar + 8u * (2 * kRing + 6), done = bar + 8u * (2 * kRing + 7);
+  auto p_full = [&](int b) { return bar + 8u * (2 * kRing + 4 + b); };
+  auto p_free = [&](int b) { return bar + 8u * (2 * kRing + 6 + b); };
+  const uint32_t o_done = bar + 8u * (2 * kRing + 8);
+  const uint32_t q_ready = bar + 8u * (2 * kRing + 9), done = bar + 8u * (2 * kRing + 10);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t bid = blockIdx.x;
@@ -165,8 +185,11 @@ __global__ void __launch_bounds__(kShThreads, 2)
         mbar_init(s_full(b), 1);
         mbar_init(s_free(b), 4);
       }
-      mbar_init(p_full, 4);
-      mbar_init(p_free, 1);
+      for (int b = 0; b < 2; ++b) {
+        mbar_init(p_full(b), 4);
+        mbar_init(p_free(b), 1);
+      }
+      mbar_init(o_done, 1);
       mbar_init(q_ready, 4);
       mbar_init(done, 1);
       fence_barrier_init();
@@ -241,15 +264,18 @@ __global__ void __launch_bounds__(kShThreads, 2)
       if (ok && nH > 0) ok = issue_s(0);
       for (int hb = 0; hb < nH && ok; ++hb) {
         if (hb + 1 < nH && !(ok = issue_s(hb + 1))) break;
-        if (!(ok = mbar_wait(p_full, hb & 1, &g_shared_status))) break;
+        const int pb = hb & 1;
+        if (!(ok = mbar_wait(p_full(pb), (hb >> 1) & 1, &g_shared_status))) break;
         tc_fence_after();
         const uint32_t vbase = sb + L::kOffRing + (hb % kRing) * L::kStage + L::kKBytes;
+        const uint32_t pbase = sb + L::kOffP + pb * L::kPBytes;
 #pragma unroll
         for (int ks = 0; ks < kHalfTok / 16; ++ks)
-          umma_bf16(tmem + 128, umma_desc_kmajor(sb + L::kOffP + ks * 32, 512, 64),
+          umma_bf16(tmem + 128, umma_desc_kmajor(pbase + ks * 32, 512, 64),
                     desc_mn_sw128(vbase + ks * 2048, L::kBox, 1024), idesc_o,
                     (hb > 0 || ks > 0) ? 1u : 0u);
-        umma_commit(p_free);
+        umma_commit(p_free(pb));
+        umma_commit(o_done);
         umma_commit(kv_empty(hb % kRing));
       }
       umma_commit(done);
@@ -265,6 +291,17 @@ __global__ void __launch_bounds__(kShThreads, 2)
     const uint32_t lanes = (uint32_t)(32 * qd) << 16;
     __syncwarp();
     if (lane == 0) mbar_arrive(q_ready);
+    const int* sm = slotmap + ((int64_t)r * (q1 - q0) + (i - q0)) * kk;
+    if (valid) {
+      // the row's query pulls its private partials toward L2 while the shared blocks run
+      for (int t = h; t < kk; t += G) {
+        const int pos = __ldg(sm + t);
+        if (pos >= 0) {
+          prefetch_l2_bulk(part_o + (int64_t)pos * G * D_H, (uint32_t)(G * D_H * 2));
+          prefetch_l2(part_lse + (int64_t)pos * G);
+        }
+      }
+    }
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
     for (int hb = 0; hb < nH && ok; ++hb) {
@@ -285,14 +322,17 @@ __global__ void __launch_bounds__(kShThreads, 2)
       float alpha = 1.f;
       uint32_t pk[16];
       if (sel) {
-        const int64_t j0 = b * kBlock + (hb & 1) * kHalfTok;
-        float bm = -INFINITY;
+        if (b == (i >> 6)) {                          // local block: keys j <= i only
+          const int lim = (int)(i - (b * kBlock + (hb & 1) * kHalfTok));
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          if (j0 + c > i) sv[c] = __float_as_uint(-INFINITY);
-          bm = fmaxf(bm, __uint_as_float(sv[c]));
+          for (int c = 0; c < 32; ++c)
+            if (c > lim) sv[c] = __float_as_uint(-INFINITY);
         }
-        bm *= scale_log2;
+        float bm = fmax3(__uint_as_float(sv[0]), __uint_as_float(sv[1]), __uint_as_float(sv[2]));
+#pragma unroll
+        for (int c = 3; c < 31; c += 2)
+          bm = fmax3(bm, __uint_as_float(sv[c]), __uint_as_float(sv[c + 1]));
+        bm = fmaxf(bm, __uint_as_float(sv[31])) * scale_log2;
         if (m_ref == -INFINITY) {
           m_ref = bm;                                 // this row's O and l are still zero
         } else if (bm > m_ref + 8.f) {
@@ -312,11 +352,15 @@ __global__ void __launch_bounds__(kShThreads, 2)
 #pragma unroll
         for (int c = 0; c < 16; ++c) pk[c] = 0u;
       }
-      // P and O may be touched once the previous half block's O += P V has completed
-      if (hb > 0 &&
-          !(ok = __all_sync(kAllLanes, mbar_wait(p_free, (hb - 1) & 1, &g_shared_status))))
+      // P buffer hb&1 is free once O += P V of half block hb-2 has completed
+      if (hb > 1 &&
+          !(ok = __all_sync(kAllLanes, mbar_wait(p_free(buf), ((hb >> 1) & 1) ^ 1, &g_shared_status))))
         break;
       if (__any_sync(kAllLanes, alpha != 1.f)) {
+        // O itself may be rescaled only once O += P V of half block hb-1 has completed
+        if (hb > 0 &&
+            !(ok = __all_sync(kAllLanes, mbar_wait(o_done, (hb - 1) & 1, &g_shared_status))))
+          break;
         tc_fence_after();
 #pragma unroll
         for (int part = 0; part < D_H / 64; ++part) {
@@ -331,7 +375,7 @@ __global__ void __launch_bounds__(kShThreads, 2)
       }
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        const uint32_t addr = sb + L::kOffP + R * 64 + ((c ^ ((R >> 1) & 3)) << 4);
+        const uint32_t addr = sb + L::kOffP + buf * L::kPBytes + R * 64 + ((c ^ ((R >> 1) & 3)) << 4);
         asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(pk[4 * c]),
                      "r"(pk[4 * c + 1]), "r"(pk[4 * c + 2]), "r"(pk[4 * c + 3])
                      : "memory");
@@ -339,29 +383,53 @@ __global__ void __launch_bounds__(kShThreads, 2)
       fence_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(p_full);
+      if (lane == 0) mbar_arrive(p_full(buf));
     }
-    // ---- epilogue: shared-block state + private partials of this row, in slot order
+    // ---- epilogue: shared-block state + private partials of each row, in slot order
     if (ok) ok = __all_sync(kAllLanes, mbar_wait(done, 0, &g_shared_status));
     tc_fence_after();
     const bool have_o = nH > 0 && ok;               // warp-uniform
-    const int* sm = slotmap + ((int64_t)r * (q1 - q0) + (i - q0)) * kk;
+    float* s_os = reinterpret_cast<float*>(smem + L::kOffOs);
+    float* s_mx = reinterpret_cast<float*>(smem + L::kOffMx);
+    float* s_inv = reinterpret_cast<float*>(smem + L::kOffInv);
+    int* s_pos = reinterpret_cast<int*>(smem + L::kOffPos);
+    int* s_np = reinterpret_cast<int*>(smem + L::kOffNp);
+    // (a) one thread per row: merge max and sum over the shared state and the private LSEs
+    //     (online, 16 slots at a time); the query's head-0 row lists its private partials
     const float lse_s = l > 0.f ? m_ref + __log2f(l) : -INFINITY;
-    float mx = lse_s;
-    if (valid)
-      for (int t = 0; t < kk; ++t) {
-        const int pos = __ldg(sm + t);
-        if (pos >= 0) mx = fmaxf(mx, __ldg(part_lse + (int64_t)pos * G + h));
+    float mx = lse_s, wsum = lse_s == -INFINITY ? 0.f : 1.f;
+    int np = 0;
+    for (int t0 = 0; t0 < kk; t0 += 16) {
+      int pos[16];
+      float lv[16];
+#pragma unroll
+      for (int d = 0; d < 16; ++d) pos[d] = (valid && t0 + d < kk) ? __ldg(sm + t0 + d) : -1;
+#pragma unroll
+      for (int d = 0; d < 16; ++d)
+        lv[d] = pos[d] >= 0 ? __ldg(part_lse + (int64_t)pos[d] * G + h) : -INFINITY;
+      float cm = mx;
+#pragma unroll
+      for (int d = 0; d < 16; ++d) cm = fmaxf(cm, lv[d]);
+      if (cm != -INFINITY) {
+        if (mx != -INFINITY) wsum *= ex2(mx - cm);
+        mx = cm;
+#pragma unroll
+        for (int d = 0; d < 16; ++d)
+          if (pos[d] >= 0) wsum += ex2(lv[d] - mx);
       }
-    const float w_s = lse_s == -INFINITY ? 0.f : ex2(lse_s - mx);
-    float wsum = w_s;
-    if (valid)
-      for (int t = 0; t < kk; ++t) {
-        const int pos = __ldg(sm + t);
-        if (pos >= 0) wsum += ex2(__ldg(part_lse + (int64_t)pos * G + h) - mx);
+      if (valid && h == 0) {
+#pragma unroll
+        for (int d = 0; d < 16; ++d)
+          if (pos[d] >= 0) s_pos[w * kk + np++] = pos[d];
       }
+    }
     const float inv_w = wsum > 0.f ? 1.f / wsum : 0.f;
-    const float c_s = l > 0.f ? w_s / l : 0.f;      // weight of the TMEM accumulator
+    const float c_o = l > 0.f ? ex2(lse_s - mx) * inv_w / l : 0.f;
+    if (valid) lse[((int64_t)r * G + h) * N + i] = (mx + __log2f(wsum)) * 0.69314718055994531f;
+    s_mx[R] = mx;
+    s_inv[R] = inv_w;
+    if (valid && h == 0) s_np[w] = np;
+    // (b) the shared-block O of the row, weighted, into shared memory
 #pragma unroll
     for (int part = 0; part < D_H / 64; ++part) {
       uint32_t ov[64];
@@ -369,41 +437,92 @@ __global__ void __launch_bounds__(kShThreads, 2)
         MSA_TMEM_LD64(tmem + lanes + 128 + 64 * part, ov);
         tmem_ld_wait();
       }
-      if (valid) {
-        float acc[64];
+      float4* dst = reinterpret_cast<float4*>(s_os + R * L::kOsStride + 64 * part);
 #pragma unroll
-        for (int c = 0; c < 64; ++c) acc[c] = have_o ? __uint_as_float(ov[c]) * c_s : 0.f;
-        for (int t = 0; t < kk; ++t) {
-          const int pos = __ldg(sm + t);
-          if (pos < 0) continue;
-          const float wp = ex2(__ldg(part_lse + (int64_t)pos * G + h) - mx);
-          const uint4* src =
-              reinterpret_cast<const uint4*>(part_o + ((int64_t)pos * G + h) * D_H + 64 * part);
+      for (int c = 0; c < 16; ++c)
+        dst[c] = have_o ? make_float4(__uint_as_float(ov[4 * c]) * c_o,
+                                      __uint_as_float(ov[4 * c + 1]) * c_o,
+                                      __uint_as_float(ov[4 * c + 2]) * c_o,
+                                      __uint_as_float(ov[4 * c + 3]) * c_o)
+                        : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    __syncwarp();
+    // (c) the warp's queries, whole: a query's partial for all G heads is G*d_h contiguous bf16,
+    //     as is its output row, so lanes split it in 16-byte pieces (coalesced) and add the
+    //     private partials to the staged shared-block O in slot order
+    {
+      const int U = G * D_H / 8;                      // 16-byte pieces per query
+      const int lpq = U < 32 ? U : 32, qpp = 32 / lpq, ipl = U / lpq;
+      const int wq0 = (32 * qd) / G;
+      const int nwq = wq0 < kTileQ ? min(32 / G, kTileQ - wq0) : 0;
+      const int sub = lane % lpq;
+      constexpr int kIpl = D_H / 32;                  // most pieces per lane (G <= 8)
+      constexpr int kNb = 4;                          // partials in flight per lane
+      for (int p = 0; p < nwq; p += qpp) {
+        const int wl = p + lane / lpq, wq = wq0 + wl;
+        const bool qv = wl < nwq && i0 + wq < q1;
+        float acc[kIpl][8], pm[kIpl], pi[kIpl];
+        int pe[kIpl], ph[kIpl];
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            const uint4 u = __ldg(src + c);
-            const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-            for (int k2 = 0; k2 < 4; ++k2) {
-              const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wd[k2]));
-              acc[8 * c + 2 * k2] += wp * f.x;
-              acc[8 * c + 2 * k2 + 1] += wp * f.y;
-            }
-          }
+        for (int c = 0; c < kIpl; ++c) {
+          pe[c] = 8 * (c * lpq + sub);                // element within the query's G*d_h
+          ph[c] = pe[c] / D_H;
+          const int RR = min(wq * G + ph[c], 127);
+          pm[c] = s_mx[RR];
+          pi[c] = s_inv[RR];
+          const float4* src =
+              reinterpret_cast<const float4*>(s_os + RR * L::kOsStride + (pe[c] - ph[c] * D_H));
+          const float4 a0 = src[0], a1 = src[1];
+          acc[c][0] = a0.x; acc[c][1] = a0.y; acc[c][2] = a0.z; acc[c][3] = a0.w;
+          acc[c][4] = a1.x; acc[c][5] = a1.y; acc[c][6] = a1.z; acc[c][7] = a1.w;
         }
-        uint4* dst = reinterpret_cast<uint4*>(o + (i * H_q + (int64_t)r * G + h) * D_H + 64 * part);
+        const int npq = qv ? s_np[wq] : 0;
+        for (int j = 0; j < npq; j += kNb) {
+          int pos[kNb];
+          uint4 u[kNb][kIpl];
+          float lv[kNb][kIpl];
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          uint4 v4;
-          v4.x = pack_bf16x2(acc[8 * c + 0] * inv_w, acc[8 * c + 1] * inv_w);
-          v4.y = pack_bf16x2(acc[8 * c + 2] * inv_w, acc[8 * c + 3] * inv_w);
-          v4.z = pack_bf16x2(acc[8 * c + 4] * inv_w, acc[8 * c + 5] * inv_w);
-          v4.w = pack_bf16x2(acc[8 * c + 6] * inv_w, acc[8 * c + 7] * inv_w);
-          dst[c] = v4;
+          for (int d = 0; d < kNb; ++d) pos[d] = j + d < npq ? s_pos[wq * kk + j + d] : -1;
+#pragma unroll
+          for (int d = 0; d < kNb; ++d)
+#pragma unroll
+            for (int c = 0; c < kIpl; ++c)
+              if (pos[d] >= 0 && c < ipl) {
+                u[d][c] = __ldg(reinterpret_cast<const uint4*>(part_o + (int64_t)pos[d] * G * D_H +
+                                                               pe[c]));
+                lv[d][c] = __ldg(part_lse + (int64_t)pos[d] * G + ph[c]);
+              }
+#pragma unroll
+          for (int d = 0; d < kNb; ++d)
+#pragma unroll
+            for (int c = 0; c < kIpl; ++c)
+              if (pos[d] >= 0 && c < ipl) {
+                const float wt = ex2(lv[d][c] - pm[c]) * pi[c];
+                const uint32_t wd[4] = {u[d][c].x, u[d][c].y, u[d][c].z, u[d][c].w};
+#pragma unroll
+                for (int k2 = 0; k2 < 4; ++k2) {
+                  const float2 f =
+                      __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wd[k2]));
+                  acc[c][2 * k2] += wt * f.x;
+                  acc[c][2 * k2 + 1] += wt * f.y;
+                }
+              }
+        }
+        if (qv) {
+          __nv_bfloat16* orow = o + ((i0 + wq) * H_q + (int64_t)r * G) * D_H;
+#pragma unroll
+          for (int c = 0; c < kIpl; ++c)
+            if (c < ipl) {
+              uint4 v;
+              v.x = pack_bf16x2(acc[c][0], acc[c][1]);
+              v.y = pack_bf16x2(acc[c][2], acc[c][3]);
+              v.z = pack_bf16x2(acc[c][4], acc[c][5]);
+              v.w = pack_bf16x2(acc[c][6], acc[c][7]);
+              *reinterpret_cast<uint4*>(orow + pe[c]) = v;
+            }
         }
       }
     }
-    if (valid) lse[((int64_t)r * G + h) * N + i] = (mx + __log2f(wsum)) * 0.69314718055994531f;
     tc_fence_before();
   }
 

@@ -60,14 +60,29 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// As mbar_try_wait, but the thread may sleep (up to `suspend_ns`) until the phase completes
+// instead of returning at once, so waiting threads do not take issue slots from working ones.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity,
+                                                    uint32_t suspend_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(suspend_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Waits until the phase with the given parity has completed.  Gives up after kWaitNs,
 // records kErrTimeout in *err and returns false; the caller then stops its loop.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned* err) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer_ns();
   while (true) {
-    for (int it = 0; it < 256; ++it)
-      if (mbar_try_wait(bar, parity)) return true;
+    for (int it = 0; it < 16; ++it)
+      if (mbar_try_wait_sleep(bar, parity, 100000u)) return true;
     if (globaltimer_ns() - t0 > kWaitNs) {
       atomicOr(err, kErrTimeout);
       return false;
