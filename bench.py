@@ -94,16 +94,55 @@ def kernel_source_hash(fnames):
     return h.hexdigest()[:16]
 
 
+# ncu kernel name -> the bench row it belongs to (a row is one call of the C ABI per step)
+NCU_ROWS = {"k_index_block_scores": "k_index_block_scores", "k_select_prefill": "k_select_prefill",
+            "k_attn_plan": "main_branch", "k_attn_scan": "main_branch",
+            "k_attn_kvouter": "main_branch", "k_attn_shared": "main_branch",
+            "k_decode_block_scores": "decode", "k_select_decode": "decode",
+            "k_sparse_attn": "decode", "k_decode_merge": "decode"}
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.txt")
+
+
 def ncu_traffic(kernel):
-    """DRAM bytes per launch of a kernel from the last ncu capture, if the kernel source is
-    unchanged since (profiles/traffic.json records the source hash it was taken on)."""
-    path = os.path.join(ROOT, "profiles", "traffic.json")
-    if not os.path.exists(path):
+    """DRAM bytes per call of a bench row from the last full-size ncu capture, if the row's
+    kernel sources are unchanged since (profiles/traffic.txt records the source hash)."""
+    if not os.path.exists(TRAFFIC_FILE):
         return None
-    rec = json.load(open(path)).get(kernel)
-    if not rec or rec.get("source_sha") != kernel_source_hash(KERNEL_FILES[kernel]):
-        return None
-    return rec.get("bytes_per_launch")
+    for line in open(TRAFFIC_FILE):
+        f = line.split()
+        if len(f) >= 3 and not line.startswith("#") and f[0] == kernel:
+            return int(float(f[1])) if f[2] == kernel_source_hash(KERNEL_FILES[kernel]) else None
+    return None
+
+
+def write_traffic(csv_path, command):
+    """profiles/traffic.txt from an ncu CSV of gpu__time_duration.sum, dram__bytes_read.sum and
+    dram__bytes_write.sum over whole bench steps: bytes per step of each row (one call each)."""
+    import csv
+    import collections
+    rows = list(csv.reader(l for l in open(csv_path) if not l.startswith("==")))
+    hdr = rows[0]
+    ki, mi, vi, ui = (hdr.index(c) for c in ("Kernel Name", "Metric Name", "Metric Value",
+                                              "Metric Unit"))
+    scale = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9}
+    tot = collections.defaultdict(float)
+    steps = 0
+    for r in rows[1:]:
+        name = r[ki].split("(")[0].split("<")[0].split("::")[-1].strip()
+        if name not in NCU_ROWS:
+            continue
+        if r[mi] == "gpu__time_duration.sum" and name == "k_index_block_scores":
+            steps += 1
+        if r[mi] in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
+            tot[NCU_ROWS[name]] += float(r[vi].replace(",", "")) * scale[r[ui]]
+    with open(TRAFFIC_FILE, "w") as f:
+        f.write("# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per call of each bench\n"
+                "# row, averaged over %d whole steps of one ncu capture (1 pass, cold cache):\n"
+                "#   %s\n# row  bytes_per_call  source_sha\n" % (steps, command))
+        for k in ("k_index_block_scores", "k_select_prefill", "main_branch", "decode"):
+            if k in tot:
+                f.write("%s %d %s\n" % (k, tot[k] / max(steps, 1),
+                                         kernel_source_hash(KERNEL_FILES[k])))
 
 
 class Clocks:
@@ -451,7 +490,14 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--write-traffic", metavar="NCU_CSV",
+                    help="write profiles/traffic.txt from an ncu CSV of whole steps and exit")
+    ap.add_argument("--traffic-command", default="",
+                    help="the command the ncu CSV was captured on (recorded in the file)")
     args = ap.parse_args()
+    if args.write_traffic:
+        write_traffic(args.write_traffic, args.traffic_command)
+        return
     if args.warmup < 3 and args.impl == "msa":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
     world, rank, local = dist_setup()

@@ -1,14 +1,15 @@
-// Sparse main branch of MSA («MiniMax-M3：MSA 技术报告速读», section 主分支, eq. O^(h)_i, and
-// the LSE of section Kernel): exact softmax attention of the G query heads of group r over the
-// visible tokens of the blocks selected for (i, r).
+// Decode attention of MSA («MiniMax-M3：MSA 技术报告速读», section 主分支, eq. O^(h)_i, and
+// the LSE of section Kernel): exact softmax attention of the G query heads of group r of one new
+// token over the visible tokens of its selected blocks, split into block ranges whose partials
+// are merged in a fixed order (the kernel section's pre-scheduled splits with a two-stage merge
+// and no atomics).
 //
-// Layout of the work: one CTA = 4 warps per (row, group) -- or per (sequence, group, split)
-// for decode.  Warp w owns keys [16w, 16w+16) of every selected block, so a block is read by
-// the 4 warps side by side.  The G <= 8 heads of the group are the N=8 side of the legacy
-// m16n8k16 MMA with the keys (S^T = K Q^T) or the head dims (O^T += V^T P^T) as its M side,
-// which wastes no MMA lane on a single query; P goes from the S^T accumulator to the P^T
-// operand with one movmatrix transpose per 8x8 tile.  K and V rows are loaded from global
-// memory directly into MMA fragments as 16-byte vectors:
+// Layout of the work: one CTA = 4 warps per (sequence, group, split).  Warp w owns keys
+// [16w, 16w+16) of every selected block, so a block is read by the 4 warps side by side.  The
+// G <= 8 heads of the group are the N=8 side of the m16n8k16 MMA with the keys (S^T = K Q^T) or
+// the head dims (O^T += V^T P^T) as its M side, which wastes no MMA lane on the single query; P
+// goes from the S^T accumulator to the P^T operand with one movmatrix transpose per 8x8 tile.
+// K and V rows are loaded from global memory directly into MMA fragments as 16-byte vectors:
 //   * S^T: the contracted head dim is permuted identically in K (A operand) and Q^T (B), so a
 //     thread's A fragment words are whole 16-byte chunks of a K row;
 //   * O^T: a thread owns 8 (d_h=64) or 16 (d_h=128) head dims of V for 4 keys and pairs keys
@@ -38,18 +39,15 @@ struct AttnParams {
   const __nv_bfloat16* k;
   const __nv_bfloat16* v;
   const int32_t* idx;
-  __nv_bfloat16* o;
-  float* lse;
   float* part_o;      // decode split partials [S*H_kv*nsplit, G, D_H] (normalised)
   float* part_lse;    // decode split partials [S*H_kv*nsplit, G] (log2 units)
-  const int64_t* cu;  // decode: cumulative sequence lengths
-  int64_t N;          // prefill: tokens
-  int64_t max_len;    // decode: length bound
+  const int64_t* cu;  // cumulative sequence lengths
+  int64_t max_len;    // length bound
   int H_q, H_kv, G, kk, nsplit, S;
   float scale_log2;   // log2(e) / sqrt(d_h)
 };
 
-template <int D_H, bool DECODE>
+template <int D_H>
 __global__ void __launch_bounds__(32 * kWarps) k_sparse_attn(const AttnParams p) {
   constexpr int KS = D_H / 16;             // k-steps of S^T, m-tiles of O^T
   constexpr int KCH = D_H / 32;            // 16-B K chunks per thread per key row
@@ -60,38 +58,20 @@ __global__ void __launch_bounds__(32 * kWarps) k_sparse_attn(const AttnParams p)
   const int c = lane & 3, r4 = lane >> 2;
 
   // ---------------------------------------------------------------- the problem
-  int64_t i, tok0;                          // query position, first cache row of the sequence
-  int r, t0, t1;
-  const int32_t* sel;
-  const __nv_bfloat16* qrow;
-  int64_t unit;                             // output unit (decode: (s, r, split))
-  if (!DECODE) {
-    const int64_t bid = blockIdx.x;
-    r = (int)(bid / p.N);
-    i = bid - (int64_t)r * p.N;
-    tok0 = 0;
-    sel = p.idx + ((int64_t)r * p.N + i) * p.kk;
-    qrow = p.q + i * (int64_t)p.H_q * D_H;
-    t0 = 0;
-    t1 = p.kk;
-    unit = 0;
-  } else {
-    unit = blockIdx.x;
-    const int split = (int)(unit % p.nsplit);
-    const int64_t sr = unit / p.nsplit;
-    const int64_t s = sr / p.H_kv;
-    r = (int)(sr - s * p.H_kv);
-    tok0 = p.cu[s];
-    int64_t L = p.cu[s + 1] - tok0;
-    L = L < 1 ? 1 : (L > p.max_len ? p.max_len : L);
-    i = L - 1;
-    sel = p.idx + sr * p.kk;
-    qrow = p.q + s * (int64_t)p.H_q * D_H;
-    const int per = (p.kk + p.nsplit - 1) / p.nsplit;
-    t0 = split * per;
-    t1 = min(p.kk, t0 + per);
-  }
-  const int64_t l_blk = i >> 6;
+  const int64_t unit = blockIdx.x;          // (sequence, group, split)
+  const int split = (int)(unit % p.nsplit);
+  const int64_t sr = unit / p.nsplit;
+  const int64_t s = sr / p.H_kv;
+  const int r = (int)(sr - s * p.H_kv);
+  const int64_t tok0 = p.cu[s];             // first cache row of the sequence
+  int64_t L = p.cu[s + 1] - tok0;
+  L = L < 1 ? 1 : (L > p.max_len ? p.max_len : L);
+  const int64_t i = L - 1;                  // the new token's position
+  const int32_t* sel = p.idx + sr * p.kk;
+  const __nv_bfloat16* qrow = p.q + s * (int64_t)p.H_q * D_H;
+  const int per = (p.kk + p.nsplit - 1) / p.nsplit;
+  const int t0 = split * per;
+  const int t1 = min(p.kk, t0 + per);
 
   // Q^T fragments (B operand of S^T = K Q^T): head n = r4, dims permuted as the K loads.
   uint32_t qf[KS][2];
@@ -267,21 +247,10 @@ __global__ void __launch_bounds__(32 * kWarps) k_sparse_attn(const AttnParams p)
       ov[e] = acc * inv;
     }
     const float lse2 = L > 0.f ? mx + __log2f(L) : -INFINITY;
-    const int hq = r * p.G + h;
-    if (!DECODE) {
-      uint4 pk;
-      pk.x = pack_bf16x2(ov[0], ov[1]);
-      pk.y = pack_bf16x2(ov[2], ov[3]);
-      pk.z = pack_bf16x2(ov[4], ov[5]);
-      pk.w = pack_bf16x2(ov[6], ov[7]);
-      *reinterpret_cast<uint4*>(p.o + (i * p.H_q + hq) * D_H + d0) = pk;
-      if (d0 == 0) p.lse[(int64_t)hq * p.N + i] = lse2 * 0.69314718055994531f;
-    } else {
-      float* po = p.part_o + (unit * p.G + h) * D_H + d0;
+    float* po = p.part_o + (unit * p.G + h) * D_H + d0;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) po[e] = ov[e];
-      if (d0 == 0) p.part_lse[unit * p.G + h] = lse2;
-    }
+    for (int e = 0; e < 8; ++e) po[e] = ov[e];
+    if (d0 == 0) p.part_lse[unit * p.G + h] = lse2;
   }
 }
 
@@ -323,31 +292,6 @@ __global__ void __launch_bounds__(128) k_decode_merge(const float* __restrict__ 
 
 }  // namespace
 
-cudaError_t launch_sparse_attn_prefill(const void* q, const void* k, const void* v,
-                                       const int32_t* idx, void* o, float* lse, int64_t N, int H_q,
-                                       int H_kv, int d_h, int kk, cudaStream_t stream) {
-  AttnParams p{};
-  p.q = static_cast<const __nv_bfloat16*>(q);
-  p.k = static_cast<const __nv_bfloat16*>(k);
-  p.v = static_cast<const __nv_bfloat16*>(v);
-  p.idx = idx;
-  p.o = static_cast<__nv_bfloat16*>(o);
-  p.lse = lse;
-  p.N = N;
-  p.H_q = H_q;
-  p.H_kv = H_kv;
-  p.G = H_q / H_kv;
-  p.kk = kk;
-  p.nsplit = 1;
-  p.scale_log2 = (float)(1.4426950408889634 / sqrt((double)d_h));
-  const int64_t grid = N * H_kv;
-  if (d_h == 128)
-    k_sparse_attn<128, false><<<(unsigned)grid, 32 * kWarps, 0, stream>>>(p);
-  else
-    k_sparse_attn<64, false><<<(unsigned)grid, 32 * kWarps, 0, stream>>>(p);
-  return cudaGetLastError();
-}
-
 cudaError_t launch_sparse_attn_decode(const void* q, const void* k_cache, const void* v_cache,
                                       const int32_t* idx, const int64_t* cu, int S,
                                       int64_t max_len, int H_q, int H_kv, int d_h, int kk,
@@ -372,11 +316,11 @@ cudaError_t launch_sparse_attn_decode(const void* q, const void* k_cache, const 
   const int64_t grid = (int64_t)S * H_kv * nsplit;
   const int64_t mgrid = (int64_t)S * H_kv;
   if (d_h == 128) {
-    k_sparse_attn<128, true><<<(unsigned)grid, 32 * kWarps, 0, stream>>>(p);
+    k_sparse_attn<128><<<(unsigned)grid, 32 * kWarps, 0, stream>>>(p);
     k_decode_merge<128><<<(unsigned)mgrid, 128, 0, stream>>>(
         part_o, part_lse, static_cast<__nv_bfloat16*>(o), lse, H_q, H_kv, p.G, nsplit);
   } else {
-    k_sparse_attn<64, true><<<(unsigned)grid, 32 * kWarps, 0, stream>>>(p);
+    k_sparse_attn<64><<<(unsigned)grid, 32 * kWarps, 0, stream>>>(p);
     k_decode_merge<64><<<(unsigned)mgrid, 128, 0, stream>>>(
         part_o, part_lse, static_cast<__nv_bfloat16*>(o), lse, H_q, H_kv, p.G, nsplit);
   }

@@ -3,14 +3,15 @@
 // gathers the queries that chose it and stacks them to fill tensor-core MMAs).
 //
 // Input: the private selections of a query chunk -- (query, slot) pairs whose block no other
-// query of the same 8-query tile selected -- bucketed by (group r, block b).  A work tile is up
+// query of the same 16-query tile selected -- bucketed by (group r, block b).  A work tile is up
 // to 128/G entries of one bucket; their G heads stack into the 128 rows of one UMMA tile:
 //   S = Q_stack [128 x d_h] . K_b^T [d_h x 64]       tcgen05, bf16 -> fp32 in TMEM
 //   row-wise softmax over the block's visible keys   one thread per row (TMEM lane)
 //   O = P [128 x 64] . V_b [64 x d_h]                tcgen05, V as an MN-major operand
 // and every row writes a partial: O normalised by its own sum (bf16) and its log2-domain LSE.
-// A partial covers exactly one block, so no rescaling is needed; the merge kernel combines
-// the partials of a row with the shared-block partial in a fixed order.
+// A partial covers exactly one block, so no rescaling is needed; the epilogue of the
+// shared-block pass (k_attn_shared.cu) combines a row's partials with its shared-block state in
+// slot order.
 // Q rows, K_b and V_b are gathered with cp.async into 128-byte-swizzled tiles (the canonical
 // K-major / MN-major SW128 layouts).  P reuses Q's shared memory and O reuses S's TMEM
 // columns, so three CTAs fit on an SM.  Persistent grid; each CTA takes a contiguous range of

@@ -2,7 +2,7 @@
 // eq. O^(h)_i; the kernel section's pre-scheduled work with a two-stage merge and no atomic
 // updates of results).
 //
-//   k_attn_plan (pass 0)  per 8-query tile: count each private selection in its (group, block)
+//   k_attn_plan (pass 0)  per 16-query tile: count each private selection in its (group, block)
 //                         bucket (a block that only one of the tile's queries selected)
 //   k_attn_scan           exclusive scans: entry offsets and work-tile offsets per bucket
 //   k_attn_plan (pass 1)  scatter private selections into their buckets; record, per (row,

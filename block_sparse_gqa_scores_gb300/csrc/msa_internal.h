@@ -59,9 +59,6 @@ cudaError_t launch_select_decode(const float* Mdec, int32_t* idx, const int64_t*
                                  int H_kv, int k, int64_t max_len, int64_t nblk_max,
                                  cudaStream_t stream);
 
-cudaError_t launch_sparse_attn_prefill(const void* q, const void* k, const void* v,
-                                       const int32_t* idx, void* o, float* lse, int64_t N, int H_q,
-                                       int H_kv, int d_h, int kk, cudaStream_t stream);
 cudaError_t launch_sparse_attn_decode(const void* q, const void* k_cache, const void* v_cache,
                                       const int32_t* idx, const int64_t* cu, int S,
                                       int64_t max_len, int H_q, int H_kv, int d_h, int kk,

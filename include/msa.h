@@ -77,7 +77,9 @@ msa_status_t msa_index_block_scores(const void *q_idx, const void *k_idx, float 
 msa_status_t msa_select_blocks(const float *M, int32_t *idx, int64_t N, int H_kv, int block_size,
                                int k, int64_t q_start, int64_t q_count, void *stream);
 
-/* Workspace bytes msa_sparse_attn_fwd needs for these sizes (may be 0). */
+/* Workspace bytes msa_sparse_attn_fwd needs for these sizes (0 for invalid sizes).  It grows
+ * with min(N, 16384) * H_q * k * d_h (the private-block partials of one 16384-row query chunk):
+ * 2.19 GB at H_q=32, k=16, d_h=128 for any N >= 16384. */
 size_t msa_sparse_attn_fwd_workspace(int64_t N, int H_q, int H_kv, int d_h, int k);
 
 /* Sparse main branch (eq. O^(h)_i of section 主分支, LSE of section Kernel).  For every row i
@@ -89,7 +91,11 @@ size_t msa_sparse_attn_fwd_workspace(int64_t N, int H_q, int H_kv, int d_h, int 
  *        include floor(i/64), as msa_select_blocks writes them)
  *   o    bf16 [N, H_q, d_h] (fp32 accumulation, rounded to nearest even)
  *   lse  fp32 [H_q, N] (natural log)
- *   ws   device workspace of msa_sparse_attn_fwd_workspace() bytes (NULL if 0). */
+ *   ws   device workspace, 16-byte aligned, of at least msa_sparse_attn_fwd_workspace() bytes
+ *        (caller-owned; contents ignored on entry, unspecified on return; one call at a time
+ *        per workspace).  Smaller: MSA_ERR_WORKSPACE.  N > 2^21: MSA_ERR_UNSUPPORTED.
+ * Results do not depend on the launch order of work inside the call: the private-block
+ * partials are merged per row in slot order, with no atomic updates of results. */
 msa_status_t msa_sparse_attn_fwd(const void *q, const void *k, const void *v, const int32_t *idx,
                                  void *o, float *lse, int64_t N, int H_q, int H_kv, int d_h,
                                  int block_size, int k_blocks, void *ws, size_t ws_bytes,
