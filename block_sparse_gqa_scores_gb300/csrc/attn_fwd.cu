@@ -19,7 +19,7 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 constexpr int64_t kChunkRows = 16384;     // query rows per pass (bounds the workspace)
 
 struct AttnWs {
-  size_t count, offset, tile_off, cursor, entries, slotmap, part_o, part_lse, total;
+  size_t count, offset, tile_off, cursor, entries, part_o, part_lse, total;
   int64_t qc;
   int nb;
 };
@@ -38,7 +38,6 @@ AttnWs attn_layout(int64_t N, int H_q, int H_kv, int d_h, int kk) {
   w.tile_off = take(4 * (size_t)(w.nb + 1));
   w.cursor = take(4 * (size_t)(w.nb + 1));
   w.entries = take(4 * sel);
-  w.slotmap = take(4 * sel);
   w.part_o = take(2 * sel * G * d_h);
   w.part_lse = take(4 * sel * G);
   w.total = off;
@@ -64,7 +63,6 @@ cudaError_t launch_sparse_attn_fwd(const void* q, const void* k, const void* v, 
   int* tile_off = reinterpret_cast<int*>(base + w.tile_off);
   int* cursor = reinterpret_cast<int*>(base + w.cursor);
   int* entries = reinterpret_cast<int*>(base + w.entries);
-  int* slotmap = reinterpret_cast<int*>(base + w.slotmap);
   void* part_o = base + w.part_o;
   float* part_lse = reinterpret_cast<float*>(base + w.part_lse);
 
@@ -81,15 +79,16 @@ cudaError_t launch_sparse_attn_fwd(const void* q, const void* k, const void* v, 
   for (int64_t q0 = 0; q0 < N; q0 += w.qc) {
     const int64_t q1 = q0 + w.qc < N ? q0 + w.qc : N;
     if ((e = cudaMemsetAsync(count, 0, 4 * (size_t)w.nb, stream)) != cudaSuccess) return e;
-    if ((e = launch_attn_plan(idx, N, H_kv, kk, q0, q1, q1 - q0, nblk, 0, count, offset, cursor,
-                              entries, slotmap, stream)) != cudaSuccess) return e;
+    if ((e = launch_attn_plan(idx, N, H_kv, kk, q0, q1, nblk, 0, count, offset, cursor, entries,
+                              stream)) != cudaSuccess) return e;
     if ((e = launch_attn_scan(count, offset, tile_off, cursor, w.nb, 128 / G, stream)) != cudaSuccess)
       return e;
-    if ((e = launch_attn_plan(idx, N, H_kv, kk, q0, q1, q1 - q0, nblk, 1, count, offset, cursor,
-                              entries, slotmap, stream)) != cudaSuccess) return e;
-    if ((e = launch_attn_kvouter(q, k, v, entries, offset, tile_off, w.nb, nblk, N, q0, H_q, H_kv,
-                                 d_h, 3 * sms, part_o, part_lse, stream)) != cudaSuccess) return e;
-    if ((e = launch_attn_shared(tk, tv, q, idx, slotmap, part_o, part_lse, o, lse, N, q0, q1, H_q,
+    if ((e = launch_attn_plan(idx, N, H_kv, kk, q0, q1, nblk, 1, count, offset, cursor, entries,
+                              stream)) != cudaSuccess) return e;
+    if ((e = launch_attn_kvouter(q, k, v, entries, offset, tile_off, w.nb, nblk, N, q0, q1, H_q,
+                                 H_kv, d_h, kk, 3 * sms, part_o, part_lse, stream)) != cudaSuccess)
+      return e;
+    if ((e = launch_attn_shared(tk, tv, q, idx, part_o, part_lse, o, lse, N, q0, q1, H_q,
                                 H_kv, d_h, kk, stream)) != cudaSuccess) return e;
   }
   return cudaSuccess;

@@ -8,7 +8,9 @@
 //   S = Q_stack [128 x d_h] . K_b^T [d_h x 64]       tcgen05, bf16 -> fp32 in TMEM
 //   row-wise softmax over the block's visible keys   one thread per row (TMEM lane)
 //   O = P [128 x 64] . V_b [64 x d_h]                tcgen05, V as an MN-major operand
-// and every row writes a partial: O normalised by its own sum (bf16) and its log2-domain LSE.
+// and every row writes a partial: O normalised by its own sum (bf16) and its log2-domain LSE,
+// at the fixed position of its (group, query, slot) -- a query's partials are contiguous, so the
+// merge reads them in order without an index.
 // A partial covers exactly one block, so no rescaling is needed; the epilogue of the
 // shared-block pass (k_attn_shared.cu) combines a row's partials with its shared-block state in
 // slot order.
@@ -81,7 +83,8 @@ __global__ void __launch_bounds__(kThreadsKvo, 3)
     k_attn_kvouter(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
                    const __nv_bfloat16* __restrict__ v, const int* __restrict__ entries,
                    const int* __restrict__ offset, const int* __restrict__ tile_off, int nbuckets,
-                   int64_t nblk, int64_t N, int64_t q0, int H_q, int H_kv, int G, int ept,
+                   int64_t nblk, int64_t N, int64_t q0, int64_t nq, int H_q, int H_kv, int G,
+                   int kk, int ept,
                    __nv_bfloat16* __restrict__ part_o, float* __restrict__ part_lse,
                    float scale_log2) {
   using L = KvoSmem<D_H>;
@@ -186,8 +189,8 @@ __global__ void __launch_bounds__(kThreadsKvo, 3)
     // ---- softmax of row R = 32*warp + lane over the block's visible keys
     const int R = 32 * warp + lane;
     const bool rv = R < rows;
-    int64_t i = 0;
-    int h = 0, ent_pos = 0;
+    int64_t i = 0, slot_pos = 0;
+    int h = 0;
     float mx = 0.f, l = 0.f;
     {
       uint32_t s[64];
@@ -196,8 +199,9 @@ __global__ void __launch_bounds__(kThreadsKvo, 3)
       if (rv) {
         const int e = R / G;
         h = R - e * G;
-        ent_pos = e0 + e;
-        i = q0 + (s_ent[e] >> 6);
+        const int ent = s_ent[e];
+        slot_pos = ((int64_t)r * nq + (ent >> 6)) * kk + (ent & 63);
+        i = q0 + (ent >> 6);
         if (b == (i >> 6)) {                                // local block: keys j <= i only
           const int lim = (int)(i - b * kBlock);
 #pragma unroll
@@ -253,7 +257,7 @@ __global__ void __launch_bounds__(kThreadsKvo, 3)
         MSA_TMEM_LD64(tmem_o + ((uint32_t)(32 * warp) << 16) + 64 * half, o);
         tmem_ld_wait();
         if (rv) {
-          uint4* dst = reinterpret_cast<uint4*>(part_o + ((int64_t)ent_pos * G + h) * D_H + 64 * half);
+          uint4* dst = reinterpret_cast<uint4*>(part_o + (slot_pos * G + h) * D_H + 64 * half);
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
             uint4 w;
@@ -265,7 +269,7 @@ __global__ void __launch_bounds__(kThreadsKvo, 3)
           }
         }
       }
-      if (rv) part_lse[(int64_t)ent_pos * G + h] = mx + __log2f(l);
+      if (rv) part_lse[slot_pos * G + h] = mx + __log2f(l);
     }
     tc_fence_before();
     __syncthreads();
@@ -286,12 +290,13 @@ int kvouter_smem_bytes(int d_h) {
 
 cudaError_t launch_attn_kvouter(const void* q, const void* k, const void* v, const int* entries,
                                 const int* offset, const int* tile_off, int nbuckets, int64_t nblk,
-                                int64_t N, int64_t q0, int H_q, int H_kv, int d_h, int grid, void* part_o,
-                                float* part_lse, cudaStream_t stream) {
+                                int64_t N, int64_t q0, int64_t q1, int H_q, int H_kv, int d_h,
+                                int kk, int grid, void* part_o, float* part_lse,
+                                cudaStream_t stream) {
   const int G = H_q / H_kv;
   const float scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)d_h));
   const auto* qq = static_cast<const __nv_bfloat16*>(q);
-  const auto* kk = static_cast<const __nv_bfloat16*>(k);
+  const auto* kp = static_cast<const __nv_bfloat16*>(k);
   const auto* vv = static_cast<const __nv_bfloat16*>(v);
   auto* po = static_cast<__nv_bfloat16*>(part_o);
   if (d_h == 128) {
@@ -299,17 +304,17 @@ cudaError_t launch_attn_kvouter(const void* q, const void* k, const void* v, con
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          KvoSmem<128>::kAlloc);
     if (e != cudaSuccess) return e;
-    kern<<<grid, kThreadsKvo, KvoSmem<128>::kAlloc, stream>>>(qq, kk, vv, entries, offset, tile_off,
-                                                             nbuckets, nblk, N, q0, H_q, H_kv, G,
-                                                             kRowsT / G, po, part_lse, scale_log2);
+    kern<<<grid, kThreadsKvo, KvoSmem<128>::kAlloc, stream>>>(qq, kp, vv, entries, offset, tile_off,
+                                                             nbuckets, nblk, N, q0, q1 - q0, H_q, H_kv, G,
+                                                             kk, kRowsT / G, po, part_lse, scale_log2);
   } else {
     auto kern = k_attn_kvouter<64>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          KvoSmem<64>::kAlloc);
     if (e != cudaSuccess) return e;
-    kern<<<grid, kThreadsKvo, KvoSmem<64>::kAlloc, stream>>>(qq, kk, vv, entries, offset, tile_off,
-                                                            nbuckets, nblk, N, q0, H_q, H_kv, G,
-                                                            kRowsT / G, po, part_lse, scale_log2);
+    kern<<<grid, kThreadsKvo, KvoSmem<64>::kAlloc, stream>>>(qq, kp, vv, entries, offset, tile_off,
+                                                            nbuckets, nblk, N, q0, q1 - q0, H_q, H_kv, G,
+                                                            kk, kRowsT / G, po, part_lse, scale_log2);
   }
   return cudaGetLastError();
 }

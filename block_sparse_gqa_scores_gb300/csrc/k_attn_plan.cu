@@ -5,12 +5,12 @@
 //   k_attn_plan (pass 0)  per 16-query tile: count each private selection in its (group, block)
 //                         bucket (a block that only one of the tile's queries selected)
 //   k_attn_scan           exclusive scans: entry offsets and work-tile offsets per bucket
-//   k_attn_plan (pass 1)  scatter private selections into their buckets; record, per (row,
-//                         slot), where the block-major pass writes that slot's partial (-1 if the
-//                         slot is empty or shared)
-// The merge itself is the epilogue of k_attn_shared.  Bucket order is decided by integer atomics
-// and does not affect any result: every partial is computed independently and the merge visits
-// partials in slot order.
+//   k_attn_plan (pass 1)  scatter private selections into their buckets
+// The block-major pass writes the partial of (row, slot) at a fixed position of that row and
+// slot; the merge itself is the epilogue of k_attn_shared, which finds a row's private slots
+// from its own union of the tile.  Bucket order is decided by integer atomics and does not
+// affect any result: every partial is computed independently and the merge visits partials in
+// slot order.
 #include <cmath>
 
 #include "attn_tile.cuh"
@@ -23,19 +23,13 @@ constexpr int kPlanWarps = 4;
 
 template <int EPL>
 __device__ __forceinline__ void plan_tile(const int32_t* __restrict__ idx, int r, int64_t i0,
-                                          int64_t q0, int64_t q1, int64_t N, int kk, int64_t qc,
+                                          int64_t q0, int64_t q1, int64_t N, int kk,
                                           int64_t nblk, int pass, int* s_U, unsigned* s_mask,
-                                          int* count, const int* offset, int* cursor, int* entries,
-                                          int* slotmap) {
+                                          int* count, const int* offset, int* cursor,
+                                          int* entries) {
   const int lane = threadIdx.x & 31;
   int x[EPL], rank[EPL];
   tile_union<EPL>(idx, r, i0, q1, N, kk, x, rank, s_U, s_mask);
-  if (pass == 1) {
-    const int nq = (int)min((int64_t)kTileQ, q1 - i0);
-    for (int e = lane; e < nq * kk; e += 32)
-      slotmap[((int64_t)r * qc + (i0 - q0)) * kk + e] = -1;
-    __syncwarp();
-  }
 #pragma unroll
   for (int j = 0; j < EPL; ++j) {
     const int key = x[j];
@@ -48,15 +42,14 @@ __device__ __forceinline__ void plan_tile(const int32_t* __restrict__ idx, int r
       const int pos = offset[bucket] + atomicAdd(cursor + bucket, 1);
       const int64_t li = i0 - q0 + w;
       entries[pos] = (int)((li << 6) | t);
-      slotmap[((int64_t)r * qc + li) * kk + t] = pos;
     }
   }
 }
 
 __global__ void __launch_bounds__(32 * kPlanWarps)
     k_attn_plan(const int32_t* __restrict__ idx, int64_t N, int kk, int64_t q0, int64_t q1,
-                int64_t qc, int64_t nblk, int pass, int* count, const int* offset, int* cursor,
-                int* entries, int* slotmap) {
+                int64_t nblk, int pass, int* count, const int* offset, int* cursor,
+                int* entries) {
   __shared__ int s_U[kPlanWarps][kMaxKeys];
   __shared__ unsigned s_mask[kPlanWarps][kMaxKeys];
   const int warp = threadIdx.x >> 5;
@@ -66,8 +59,8 @@ __global__ void __launch_bounds__(32 * kPlanWarps)
   int* U = s_U[warp];
   unsigned* Mk = s_mask[warp];
   with_epl(kk, [&](auto e) {
-    plan_tile<decltype(e)::value>(idx, r, i0, q0, q1, N, kk, qc, nblk, pass, U, Mk, count, offset,
-                                  cursor, entries, slotmap);
+    plan_tile<decltype(e)::value>(idx, r, i0, q0, q1, N, kk, nblk, pass, U, Mk, count, offset,
+                                  cursor, entries);
     return 0;
   });
 }
@@ -118,13 +111,12 @@ __global__ void __launch_bounds__(kScanThreads)
 }  // namespace
 
 cudaError_t launch_attn_plan(const int32_t* idx, int64_t N, int H_kv, int kk, int64_t q0,
-                             int64_t q1, int64_t qc_stride, int64_t nblk, int pass, int* count,
-                             const int* offset, int* cursor, int* entries, int* slotmap,
-                             cudaStream_t st) {
+                             int64_t q1, int64_t nblk, int pass, int* count, const int* offset,
+                             int* cursor, int* entries, cudaStream_t st) {
   const int64_t tiles = (q1 - q0 + kTileQ - 1) / kTileQ;
   const dim3 grid((unsigned)((tiles + kPlanWarps - 1) / kPlanWarps), (unsigned)H_kv);
-  k_attn_plan<<<grid, 32 * kPlanWarps, 0, st>>>(idx, N, kk, q0, q1, qc_stride, nblk, pass, count,
-                                                offset, cursor, entries, slotmap);
+  k_attn_plan<<<grid, 32 * kPlanWarps, 0, st>>>(idx, N, kk, q0, q1, nblk, pass, count, offset,
+                                                cursor, entries);
   return cudaGetLastError();
 }
 

@@ -8,16 +8,17 @@
 //            as 32-token half blocks (K and V, 3-D tensor maps over [N, H_kv, d_h], 128-byte
 //            swizzle) through a 3-stage TMA ring;
 //   warp 1   allocates TMEM and issues  S[buf] = Q K^T  (M=128, N=32) and  O += P V  (M=128,
-//            N=d_h, V as an MN-major operand); S is double-buffered so the next half block's
-//            QK^T runs while the softmax of this one is computed;
+//            N=d_h, P read from TMEM, V as an MN-major operand); S and P are double-buffered
+//            so the next half block's QK^T runs while the softmax of this one is computed;
 //   warps 2-5 own one row each (TMEM lane): they load Q, read S rows, mask queries that did not
-//            select the block and keys after the query, and write P (bf16, 64-byte swizzle).
+//            select the block and keys after the query, and write P (bf16) back to TMEM.
 // Online softmax with a lazily moved reference max: a row's reference m moves only when a block
 // max exceeds it by more than 2^8, so P <= 2^8 and O (in TMEM) is rescaled only then.  The
 // result is exact either way -- O/l and m + log2 l use the same reference.
 // The epilogue finishes each row: it combines the row's shared-block state (O in TMEM, fp32)
 // with the row's private-block partials written by the block-major pass (k_attn_kvouter.cu, run
-// before this kernel) in slot order, and writes O (bf16) and the natural-log LSE.
+// before this kernel) at the row's own slot positions, in slot order, and writes O (bf16) and
+// the natural-log LSE.
 // Every wait is bounded; a timeout sets the device status word and the roles stop.
 #include <climits>
 #include <cmath>
@@ -44,19 +45,21 @@ struct ShSmem {
   static constexpr int kStage = 2 * kKBytes;        // K boxes, then V boxes
   static constexpr int kOffQ = 0;
   static constexpr int kOffRing = kOffQ + kHalves * kQHalf;
-  static constexpr int kOffP = kOffRing + kRing * kStage;      // 2 x (128 rows x 32 keys), SW64
-  static constexpr int kPBytes = 128 * 64;
-  static constexpr int kOffList = kOffP + 2 * kPBytes;
+  static constexpr int kOffList = kOffRing + kRing * kStage;
   static constexpr int kOffBar = kOffList + kMaxShared * 4;
   // kv_full[kRing], kv_empty[kRing], s_full[2], s_free[2], p_full[2], p_free[2], o_done,
   // q_ready, done
   static constexpr int kNumBars = 2 * kRing + 11;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
-  static constexpr int kBytes = kOffMisc + 16;
+  static constexpr int kOffPriv = kOffMisc + 16;    // per query: its private slots (bit t)
+  static constexpr int kBytes = kOffPriv + kTileQ * 8;
   static constexpr int kAlloc = kBytes + 1024;
-  static constexpr uint32_t kTmemCols = 256;        // S[0] 0..31, S[1] 32..63, O from 128
+  // TMEM columns: S[0] 0..31, S[1] 32..63 (fp32); P[0] 64..79, P[1] 80..95 (bf16 pairs);
+  // O 128..128+d_h (fp32)
+  static constexpr uint32_t kTmemCols = 256;
+  static constexpr uint32_t kColP = 64, kColO = 128;
   static_assert(kRing * kStage >= kMaxKeys * 8, "the union is built in the ring");
-  // epilogue, over Q / ring / P once every MMA has completed: the rows' shared-block O (fp32,
+  // epilogue, over Q / ring once every MMA has completed: the rows' shared-block O (fp32,
   // already weighted), per-row max and 1/sum of the merge, per query its private partials
   static constexpr int kOsStride = D_H + 4;          // floats; 16-byte pad against conflicts
   static constexpr int kOffOs = 0;
@@ -78,6 +81,15 @@ struct ShSmem {
         "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),           \
         "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])            \
       : "r"(taddr))
+
+#define MSA_TMEM_ST16(taddr, r)                                                                 \
+  asm volatile(                                                                                 \
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "                                           \
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),                 \
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),   \
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),         \
+      "r"(r[15])                                                                                \
+      : "memory")
 
 #define MSA_TMEM_ST64(taddr, r)                                                                 \
   asm volatile(                                                                                 \
@@ -111,20 +123,28 @@ __device__ __forceinline__ uint64_t desc_mn_sw128(uint32_t a, uint32_t lbo, uint
          ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
 
-__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ void prefetch_l2(const void* p) {
-  asm volatile("prefetch.global.L2 [%0];" ::"l"(p) : "memory");
+// Warp 0: the tile's union; keeps the shared blocks (selected by >= 2 of the tile's queries) in
+// s_list as (block << 16 | query mask) and marks, per query, the slots whose block is private
+// (selected by that query alone: the block-major pass wrote their partials).
+__device__ __forceinline__ float ldg_nc_f32(const float* p) {
+  float v;
+  asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(v) : "l"(p));
+  return v;
 }
 
 template <int EPL>
 __device__ __forceinline__ int shared_blocks(const int32_t* __restrict__ idx, int r, int64_t i0,
                                              int64_t q1, int64_t N, int kk, int* tmpU,
-                                             unsigned* tmpM, int* s_list) {
+                                             unsigned* tmpM, int* s_list,
+                                             unsigned long long* s_priv) {
   const int lane = threadIdx.x & 31;
+  if (lane < kTileQ) s_priv[lane] = 0ull;
   int x[EPL], rank[EPL];
   const int nU = tile_union<EPL>(idx, r, i0, q1, N, kk, x, rank, tmpU, tmpM);
+#pragma unroll
+  for (int j = 0; j < EPL; ++j)
+    if (x[j] != INT_MAX && __popc(tmpM[rank[j]]) == 1)
+      atomicOr(&s_priv[TileKeys::query(x[j])], 1ull << TileKeys::slot(x[j]));
   int nS = 0;
   for (int base = 0; base < nU; base += 32) {
     const int u = base + lane;
@@ -142,7 +162,7 @@ template <int D_H>
 __global__ void __launch_bounds__(kShThreads, 2)
     k_attn_shared(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                   const __nv_bfloat16* __restrict__ q, const int32_t* __restrict__ idx,
-                  const int* __restrict__ slotmap, const __nv_bfloat16* __restrict__ part_o,
+                  const __nv_bfloat16* __restrict__ part_o,
                   const float* __restrict__ part_lse, __nv_bfloat16* __restrict__ o,
                   float* __restrict__ lse, int64_t N, int64_t q0, int64_t q1, int H_q, int G,
                   int kk, int64_t ntiles, float scale_log2) {
@@ -153,6 +173,7 @@ __global__ void __launch_bounds__(kShThreads, 2)
   int* s_list = reinterpret_cast<int*>(smem + L::kOffList);
   int* s_nS = reinterpret_cast<int*>(smem + L::kOffMisc);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffMisc + 4);
+  unsigned long long* s_priv = reinterpret_cast<unsigned long long*>(smem + L::kOffPriv);
   const uint32_t bar = sb + L::kOffBar;
   auto kv_full = [&](int s) { return bar + 8u * s; };
   auto kv_empty = [&](int s) { return bar + 8u * (kRing + s); };
@@ -173,7 +194,7 @@ __global__ void __launch_bounds__(kShThreads, 2)
     int* tmpU = reinterpret_cast<int*>(smem + L::kOffRing);
     unsigned* tmpM = reinterpret_cast<unsigned*>(smem + L::kOffRing + kMaxKeys * 4);
     const int nS = with_epl(kk, [&](auto e) {
-      return shared_blocks<decltype(e)::value>(idx, r, i0, q1, N, kk, tmpU, tmpM, s_list);
+      return shared_blocks<decltype(e)::value>(idx, r, i0, q1, N, kk, tmpU, tmpM, s_list, s_priv);
     });
     if (lane == 0) {
       *s_nS = nS;
@@ -268,12 +289,11 @@ __global__ void __launch_bounds__(kShThreads, 2)
         if (!(ok = mbar_wait(p_full(pb), (hb >> 1) & 1, &g_shared_status))) break;
         tc_fence_after();
         const uint32_t vbase = sb + L::kOffRing + (hb % kRing) * L::kStage + L::kKBytes;
-        const uint32_t pbase = sb + L::kOffP + pb * L::kPBytes;
 #pragma unroll
         for (int ks = 0; ks < kHalfTok / 16; ++ks)
-          umma_bf16(tmem + 128, umma_desc_kmajor(pbase + ks * 32, 512, 64),
-                    desc_mn_sw128(vbase + ks * 2048, L::kBox, 1024), idesc_o,
-                    (hb > 0 || ks > 0) ? 1u : 0u);
+          umma_bf16_ta(tmem + L::kColO, tmem + L::kColP + 16 * pb + 8 * ks,
+                       desc_mn_sw128(vbase + ks * 2048, L::kBox, 1024), idesc_o,
+                       (hb > 0 || ks > 0) ? 1u : 0u);
         umma_commit(p_free(pb));
         umma_commit(o_done);
         umma_commit(kv_empty(hb % kRing));
@@ -291,17 +311,6 @@ __global__ void __launch_bounds__(kShThreads, 2)
     const uint32_t lanes = (uint32_t)(32 * qd) << 16;
     __syncwarp();
     if (lane == 0) mbar_arrive(q_ready);
-    const int* sm = slotmap + ((int64_t)r * (q1 - q0) + (i - q0)) * kk;
-    if (valid) {
-      // the row's query pulls its private partials toward L2 while the shared blocks run
-      for (int t = h; t < kk; t += G) {
-        const int pos = __ldg(sm + t);
-        if (pos >= 0) {
-          prefetch_l2_bulk(part_o + (int64_t)pos * G * D_H, (uint32_t)(G * D_H * 2));
-          prefetch_l2(part_lse + (int64_t)pos * G);
-        }
-      }
-    }
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
     for (int hb = 0; hb < nH && ok; ++hb) {
@@ -356,6 +365,7 @@ __global__ void __launch_bounds__(kShThreads, 2)
       if (hb > 1 &&
           !(ok = __all_sync(kAllLanes, mbar_wait(p_free(buf), ((hb >> 1) & 1) ^ 1, &g_shared_status))))
         break;
+      tc_fence_after();
       if (__any_sync(kAllLanes, alpha != 1.f)) {
         // O itself may be rescaled only once O += P V of half block hb-1 has completed
         if (hb > 0 &&
@@ -365,22 +375,15 @@ __global__ void __launch_bounds__(kShThreads, 2)
 #pragma unroll
         for (int part = 0; part < D_H / 64; ++part) {
           uint32_t ov[64];
-          MSA_TMEM_LD64(tmem + lanes + 128 + 64 * part, ov);
+          MSA_TMEM_LD64(tmem + lanes + L::kColO + 64 * part, ov);
           tmem_ld_wait();
 #pragma unroll
           for (int c = 0; c < 64; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * alpha);
-          MSA_TMEM_ST64(tmem + lanes + 128 + 64 * part, ov);
+          MSA_TMEM_ST64(tmem + lanes + L::kColO + 64 * part, ov);
         }
-        tmem_st_wait();
       }
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const uint32_t addr = sb + L::kOffP + buf * L::kPBytes + R * 64 + ((c ^ ((R >> 1) & 3)) << 4);
-        asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(pk[4 * c]),
-                     "r"(pk[4 * c + 1]), "r"(pk[4 * c + 2]), "r"(pk[4 * c + 3])
-                     : "memory");
-      }
-      fence_async_smem();
+      MSA_TMEM_ST16(tmem + lanes + L::kColP + 16 * buf, pk);
+      tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(p_full(buf));
@@ -395,7 +398,10 @@ __global__ void __launch_bounds__(kShThreads, 2)
     int* s_pos = reinterpret_cast<int*>(smem + L::kOffPos);
     int* s_np = reinterpret_cast<int*>(smem + L::kOffNp);
     // (a) one thread per row: merge max and sum over the shared state and the private LSEs
-    //     (online, 16 slots at a time); the query's head-0 row lists its private partials
+    //     (online, 16 slots at a time); the query's head-0 row lists its private partials, which
+    //     the block-major pass wrote at the row's own slot positions
+    const unsigned long long priv = valid ? s_priv[w] : 0ull;
+    const int64_t row_pos = ((int64_t)r * (q1 - q0) + (i - q0)) * kk;
     const float lse_s = l > 0.f ? m_ref + __log2f(l) : -INFINITY;
     float mx = lse_s, wsum = lse_s == -INFINITY ? 0.f : 1.f;
     int np = 0;
@@ -403,7 +409,8 @@ __global__ void __launch_bounds__(kShThreads, 2)
       int pos[16];
       float lv[16];
 #pragma unroll
-      for (int d = 0; d < 16; ++d) pos[d] = (valid && t0 + d < kk) ? __ldg(sm + t0 + d) : -1;
+      for (int d = 0; d < 16; ++d)
+        pos[d] = (valid && t0 + d < kk && ((priv >> (t0 + d)) & 1ull)) ? (int)(row_pos + t0 + d) : -1;
 #pragma unroll
       for (int d = 0; d < 16; ++d)
         lv[d] = pos[d] >= 0 ? __ldg(part_lse + (int64_t)pos[d] * G + h) : -INFINITY;
@@ -434,7 +441,7 @@ __global__ void __launch_bounds__(kShThreads, 2)
     for (int part = 0; part < D_H / 64; ++part) {
       uint32_t ov[64];
       if (have_o) {
-        MSA_TMEM_LD64(tmem + lanes + 128 + 64 * part, ov);
+        MSA_TMEM_LD64(tmem + lanes + L::kColO + 64 * part, ov);
         tmem_ld_wait();
       }
       float4* dst = reinterpret_cast<float4*>(s_os + R * L::kOsStride + 64 * part);
@@ -483,14 +490,14 @@ __global__ void __launch_bounds__(kShThreads, 2)
           float lv[kNb][kIpl];
 #pragma unroll
           for (int d = 0; d < kNb; ++d) pos[d] = j + d < npq ? s_pos[wq * kk + j + d] : -1;
+          // every load of the batch is issued before any is used (ordered volatile loads)
 #pragma unroll
           for (int d = 0; d < kNb; ++d)
 #pragma unroll
             for (int c = 0; c < kIpl; ++c)
               if (pos[d] >= 0 && c < ipl) {
-                u[d][c] = __ldg(reinterpret_cast<const uint4*>(part_o + (int64_t)pos[d] * G * D_H +
-                                                               pe[c]));
-                lv[d][c] = __ldg(part_lse + (int64_t)pos[d] * G + ph[c]);
+                u[d][c] = ldg_nc_v4(part_o + (int64_t)pos[d] * G * D_H + pe[c]);
+                lv[d][c] = ldg_nc_f32(part_lse + (int64_t)pos[d] * G + ph[c]);
               }
 #pragma unroll
           for (int d = 0; d < kNb; ++d)
@@ -537,7 +544,7 @@ __global__ void __launch_bounds__(kShThreads, 2)
 
 template <int D_H>
 static cudaError_t launch_shared_t(const CUtensorMap& tk, const CUtensorMap& tv, const void* q,
-                                   const int32_t* idx, const int* slotmap, const void* part_o,
+                                   const int32_t* idx, const void* part_o,
                                    const float* part_lse, void* o, float* lse, int64_t N,
                                    int64_t q0, int64_t q1, int H_q, int H_kv, int kk,
                                    cudaStream_t st) {
@@ -548,20 +555,20 @@ static cudaError_t launch_shared_t(const CUtensorMap& tk, const CUtensorMap& tv,
   const int64_t ntiles = (q1 - q0 + kTileQ - 1) / kTileQ;
   const float scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D_H));
   kern<<<(unsigned)(ntiles * H_kv), kShThreads, L::kAlloc, st>>>(
-      tk, tv, static_cast<const __nv_bfloat16*>(q), idx, slotmap,
+      tk, tv, static_cast<const __nv_bfloat16*>(q), idx,
       static_cast<const __nv_bfloat16*>(part_o), part_lse, static_cast<__nv_bfloat16*>(o), lse, N,
       q0, q1, H_q, H_q / H_kv, kk, ntiles, scale_log2);
   return cudaGetLastError();
 }
 
 cudaError_t launch_attn_shared(const CUtensorMap& tk, const CUtensorMap& tv, const void* q,
-                               const int32_t* idx, const int* slotmap, const void* part_o,
+                               const int32_t* idx, const void* part_o,
                                const float* part_lse, void* o, float* lse, int64_t N, int64_t q0,
                                int64_t q1, int H_q, int H_kv, int d_h, int kk, cudaStream_t st) {
   if (d_h == 128)
-    return launch_shared_t<128>(tk, tv, q, idx, slotmap, part_o, part_lse, o, lse, N, q0, q1, H_q,
+    return launch_shared_t<128>(tk, tv, q, idx, part_o, part_lse, o, lse, N, q0, q1, H_q,
                                 H_kv, kk, st);
-  return launch_shared_t<64>(tk, tv, q, idx, slotmap, part_o, part_lse, o, lse, N, q0, q1, H_q,
+  return launch_shared_t<64>(tk, tv, q, idx, part_o, part_lse, o, lse, N, q0, q1, H_q,
                              H_kv, kk, st);
 }
 

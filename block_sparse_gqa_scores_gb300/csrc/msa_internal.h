@@ -34,20 +34,20 @@ cudaError_t launch_sparse_attn_fwd(const void* q, const void* k, const void* v, 
 cudaError_t read_reset_shared_status(unsigned* out);
 cudaError_t read_reset_kvo_status(unsigned* out);
 cudaError_t launch_attn_shared(const CUtensorMap& tk, const CUtensorMap& tv, const void* q,
-                               const int32_t* idx, const int* slotmap, const void* part_o,
+                               const int32_t* idx, const void* part_o,
                                const float* part_lse, void* o, float* lse, int64_t N, int64_t q0,
                                int64_t q1, int H_q, int H_kv, int d_h, int kk, cudaStream_t st);
 
 cudaError_t launch_attn_plan(const int32_t* idx, int64_t N, int H_kv, int kk, int64_t q0,
-                             int64_t q1, int64_t qc_stride, int64_t nblk, int pass, int* count,
-                             const int* offset, int* cursor, int* entries, int* slotmap,
-                             cudaStream_t st);
+                             int64_t q1, int64_t nblk, int pass, int* count, const int* offset,
+                             int* cursor, int* entries, cudaStream_t st);
 cudaError_t launch_attn_scan(const int* count, int* offset, int* tile_off, int* cursor, int nb,
                              int ept, cudaStream_t st);
 cudaError_t launch_attn_kvouter(const void* q, const void* k, const void* v, const int* entries,
                                 const int* offset, const int* tile_off, int nbuckets, int64_t nblk,
-                                int64_t N, int64_t q0, int H_q, int H_kv, int d_h, int grid,
-                                void* part_o, float* part_lse, cudaStream_t stream);
+                                int64_t N, int64_t q0, int64_t q1, int H_q, int H_kv, int d_h,
+                                int kk, int grid, void* part_o, float* part_lse,
+                                cudaStream_t stream);
 cudaError_t launch_index_block_scores(const void* q_idx, const void* k_idx, float* M, int64_t N,
                                       int H_kv, int d_idx, int64_t q_start, int64_t q_count,
                                       cudaStream_t stream);
