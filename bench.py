@@ -35,11 +35,12 @@ sys.path.insert(0, ROOT)
 import gen  # noqa: E402
 
 METRIC = ("MSA prefill tokens/s and decode tokens/s at 128K ctx; % of bf16 TC / HBM roofline")
-# kernels per step: scores, select; attention per 16384-row chunk: plan, scan, plan, block-major
-# pass, shared-block pass with the merge (+ one memset); decode: scores, select, attention, merge
+# kernels per step: the fused index branch (block scores + top-k); attention per 16384-row chunk:
+# plan, scan, plan, block-major pass, shared-block pass with the merge (+ one memset); decode:
+# scores, select, attention, merge
 ATTN_LAUNCHES_PER_CHUNK = 5
 DECODE_LAUNCHES = 4
-KERNEL_FILES = {"k_index_block_scores": ["k_score.cu"], "k_select_prefill": ["k_select.cu"],
+KERNEL_FILES = {"index_branch": ["k_score.cu"],
                 "main_branch": ["attn_fwd.cu", "k_attn_shared.cu", "k_attn_kvouter.cu",
                                 "k_attn_plan.cu", "attn_tile.cuh"],
                 "decode": ["k_decode.cu", "k_select.cu", "k_attn.cu"]}
@@ -95,7 +96,7 @@ def kernel_source_hash(fnames):
 
 
 # ncu kernel name -> the bench row it belongs to (a row is one call of the C ABI per step)
-NCU_ROWS = {"k_index_block_scores": "k_index_block_scores", "k_select_prefill": "k_select_prefill",
+NCU_ROWS = {"k_index_block_scores": "index_branch",
             "k_attn_plan": "main_branch", "k_attn_scan": "main_branch",
             "k_attn_kvouter": "main_branch", "k_attn_shared": "main_branch",
             "k_decode_block_scores": "decode", "k_select_decode": "decode",
@@ -131,7 +132,7 @@ def write_traffic(csv_path, command):
         name = r[ki].split("(")[0].split("<")[0].split("::")[-1].strip()
         if name not in NCU_ROWS:
             continue
-        if r[mi] == "gpu__time_duration.sum" and name == "k_index_block_scores":
+        if r[mi] == "gpu__time_duration.sum" and name == "k_index_block_scores":   # 1 per step
             steps += 1
         if r[mi] in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
             tot[NCU_ROWS[name]] += float(r[vi].replace(",", "")) * scale[r[ui]]
@@ -139,7 +140,7 @@ def write_traffic(csv_path, command):
         f.write("# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per call of each bench\n"
                 "# row, averaged over %d whole steps of one ncu capture (1 pass, cold cache):\n"
                 "#   %s\n# row  bytes_per_call  source_sha\n" % (steps, command))
-        for k in ("k_index_block_scores", "k_select_prefill", "main_branch", "decode"):
+        for k in ("index_branch", "main_branch", "decode"):
             if k in tot:
                 f.write("%s %d %s\n" % (k, tot[k] / max(steps, 1),
                                          kernel_source_hash(KERNEL_FILES[k])))
@@ -195,11 +196,9 @@ def workload_sizes(pcfg, dcfg, lens):
     N, Hq, Hkv, dh, di, k = pcfg.N, pcfg.H_q, pcfg.H_kv, pcfg.d_h, pcfg.d_idx, pcfg.k
     i = np.arange(N, dtype=np.float64)
     T = np.minimum(i + 1, (k - 1) * 64 + (i % 64) + 1)                # |T_i|
-    nvis = np.minimum(i // 64, np.inf)                                  # blocks b < l read
     out = dict(
         F_idx=2.0 * di * Hkv * N * (N + 1) / 2,
         F_main=4.0 * dh * Hq * T.sum(),
-        select_bytes=4.0 * Hkv * nvis.sum() + 4.0 * Hkv * N * k,
     )
     # decode algorithmic bytes: the index-key stream + selected visible K/V + small vectors
     dbytes = 0.0
@@ -216,9 +215,7 @@ def setup(pcfg, dcfg, seed=0):
     msa = __import__("block_sparse_gqa_scores_gb300")
     x = gen.prefill_inputs(pcfg, seed=seed, device="cuda")
     N = pcfg.N
-    nblk = -(-N // 64)
     bufs = dict(
-        M=torch.empty((pcfg.H_kv, N, nblk), dtype=torch.float32, device="cuda"),
         idx=torch.empty((pcfg.H_kv, N, pcfg.k), dtype=torch.int32, device="cuda"),
         o=torch.empty_like(x["q"]),
         lse=torch.empty((pcfg.H_q, N), dtype=torch.float32, device="cuda"),
@@ -249,10 +246,9 @@ def run_msa(args, world, rank, local):
     N = pcfg.N
 
     def prefill():
-        msa.msa_index_block_scores(x["q_idx"], x["k_idx"], M=bufs["M"])
+        # the index branch fused (block scores + top-k, no M), then the main branch
+        msa.msa_index_select(x["q_idx"], x["k_idx"], pcfg.k, idx=bufs["idx"])
         ev[1].record(stream)
-        msa.msa_select_blocks(bufs["M"], N, pcfg.k, idx=bufs["idx"])
-        ev[2].record(stream)
         msa.msa_sparse_attn_fwd(x["q"], x["k"], x["v"], bufs["idx"], o=bufs["o"], lse=bufs["lse"],
                                 ws=bufs["ws"])
 
@@ -264,14 +260,14 @@ def run_msa(args, world, rank, local):
                               lse=dbufs["lse"], idx_out=dbufs["idx"], ws=dbufs["ws"])
 
     K, W = args.steps, args.warmup
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
     for _ in range(W):
         ev[0].record(stream)
         prefill()
-        ev[3].record(stream)
+        ev[2].record(stream)
         decode()
-        ev[4].record(stream)
+        ev[3].record(stream)
     torch.cuda.synchronize()
     msa.msa_device_status()
 
@@ -287,19 +283,19 @@ def run_msa(args, world, rank, local):
         ev = evs[s]
         ev[0].record(stream)
         prefill()
-        ev[3].record(stream)
+        ev[2].record(stream)
         decode()
-        ev[4].record(stream)
+        ev[3].record(stream)
     t_end.record(stream)
     torch.cuda.synchronize()
     clk = clocks.stop()
     barrier(world)
     msa.msa_device_status()
 
-    per = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(4)] for e in evs])   # ms
-    t_score, t_select, t_attn, t_decode = per.mean(axis=0)
-    t_prefill_total = max_over_ranks(float(per[:, :3].sum()), world)   # ms over K steps
-    t_decode_total = max_over_ranks(float(per[:, 3].sum()), world)
+    per = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(3)] for e in evs])   # ms
+    t_index, t_attn, t_decode = per.mean(axis=0)
+    t_prefill_total = max_over_ranks(float(per[:, :2].sum()), world)   # ms over K steps
+    t_decode_total = max_over_ranks(float(per[:, 2].sum()), world)
     t_all = max_over_ranks(t_start.elapsed_time(t_end), world)
 
     sizes = workload_sizes(pcfg, dcfg, d["meta"]["lens"] if d else [])
@@ -313,10 +309,8 @@ def run_msa(args, world, rank, local):
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "algorithmic": work})
 
-    add("k_index_block_scores", t_score, "tensor", sizes["F_idx"], "TFLOP/s", pk["bf16_sust"],
-        ncu_traffic("k_index_block_scores"))
-    add("k_select_prefill", t_select, "hbm", sizes["select_bytes"], "GB/s", pk["hbm"],
-        ncu_traffic("k_select_prefill"))
+    add("index_branch", t_index, "tensor", sizes["F_idx"], "TFLOP/s", pk["bf16_sust"],
+        ncu_traffic("index_branch"))
     add("main_branch", t_attn, "tensor", sizes["F_main"], "TFLOP/s", pk["bf16_sust"],
         ncu_traffic("main_branch"))
     if d is not None:
@@ -353,7 +347,7 @@ def run_msa(args, world, rank, local):
                      "peak_source": "%s (%s)" % (pk["src"], "bf16 sustained" if dom["unit"] ==
                                                  "TFLOP/s" else "HBM copy")},
         "clocks": clk,
-        "gpu_launches": (2 + ATTN_LAUNCHES_PER_CHUNK * (-(-N // 16384)) +
+        "gpu_launches": (1 + ATTN_LAUNCHES_PER_CHUNK * (-(-N // 16384)) +
                          (DECODE_LAUNCHES if d is not None else 0)) * K,
     }
     if not args.no_e2e:
@@ -365,7 +359,7 @@ def run_msa(args, world, rank, local):
 
 def e2e_prefill(msa, pcfg, x, bufs, K, W, world):
     """Prefill through the public calls with host (pinned) inputs and outputs: H2D of
-    Q, K, V, Q_idx, K_idx, the three calls, D2H of O and LSE -- all inside the timed region."""
+    Q, K, V, Q_idx, K_idx, the two calls, D2H of O and LSE -- all inside the timed region."""
     names = ["q", "k", "v", "q_idx", "k_idx"]
     host = {n: torch.empty(x[n].shape, dtype=x[n].dtype, pin_memory=True) for n in names}
     for n in names:
@@ -378,8 +372,7 @@ def e2e_prefill(msa, pcfg, x, bufs, K, W, world):
     def step():
         for n in names:
             dev[n].copy_(host[n], non_blocking=True)
-        M = msa.msa_index_block_scores(dev["q_idx"], dev["k_idx"], M=bufs["M"])
-        idx = msa.msa_select_blocks(M, N, pcfg.k, idx=bufs["idx"])
+        idx = msa.msa_index_select(dev["q_idx"], dev["k_idx"], pcfg.k, idx=bufs["idx"])
         msa.msa_sparse_attn_fwd(dev["q"], dev["k"], dev["v"], idx, o=bufs["o"], lse=bufs["lse"],
                                 ws=bufs["ws"])
         o_h.copy_(bufs["o"], non_blocking=True)

@@ -2,5 +2,5 @@
 top-k block selection with the forced local block, sparse main-branch attention (O, LSE),
 and the decode path, behind the C ABI of libmsa.so (include/msa.h)."""
 from .msa import (MSAError, msa_device_status, msa_index_block_scores,  # noqa: F401
-                  msa_select_blocks, msa_sparse_attn_fwd, msa_sparse_attn_fwd_workspace,
+                  msa_index_select, msa_select_blocks, msa_sparse_attn_fwd, msa_sparse_attn_fwd_workspace,
                   msa_sparse_decode, msa_sparse_decode_workspace)

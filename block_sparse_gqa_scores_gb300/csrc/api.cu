@@ -136,6 +136,20 @@ MSA_API msa_status_t msa_select_blocks(const float* M, int32_t* idx, int64_t N, 
       msa::launch_select_prefill(M, idx, N, H_kv, k, q_start, q_count, (cudaStream_t)stream));
 }
 
+MSA_API msa_status_t msa_index_select(const void* q_idx, const void* k_idx, int32_t* idx,
+                                      int64_t N, int H_kv, int d_idx, int block_size, int k,
+                                      int64_t q_start, int64_t q_count, void* stream) {
+  if (!aligned16(q_idx) || !aligned16(k_idx) || !aligned4(idx)) return MSA_ERR_INVALID_ARGUMENT;
+  if (N < 1 || H_kv < 1 || d_idx < 1 || block_size != 64 || k < 1 || k > 64)
+    return MSA_ERR_INVALID_ARGUMENT;
+  if (q_start < 0 || q_count < 1 || q_start + q_count > N) return MSA_ERR_INVALID_ARGUMENT;
+  if (!pow2_upto(H_kv, 8) || (d_idx != 32 && d_idx != 64) || k > MSA_INDEX_SELECT_MAX_K)
+    return MSA_ERR_UNSUPPORTED;
+  if (N * H_kv >= kMaxRows) return MSA_ERR_UNSUPPORTED;
+  return from_cuda(msa::launch_index_select(q_idx, k_idx, idx, N, H_kv, d_idx, k, q_start,
+                                            q_count, (cudaStream_t)stream));
+}
+
 MSA_API size_t msa_sparse_attn_fwd_workspace(int64_t N, int H_q, int H_kv, int d_h, int k) {
   if (N < 1 || H_kv < 1 || H_q < H_kv || H_q % H_kv != 0 || k < 1 || k > 64 || d_h < 1) return 0;
   return msa::sparse_attn_ws_bytes(N, H_q, H_kv, d_h, k);

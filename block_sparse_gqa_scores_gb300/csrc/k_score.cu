@@ -15,9 +15,20 @@
 //   * blocks after a row's own block are written as -inf.
 // Warp roles: warp 0 = TMA producer, warp 1 = TMEM allocator + MMA issuer,
 // warps 2.. = 4*SUB epilogue warps (warp w reads TMEM lanes 32*(w%4) .. +31).
+//
+// The SELECT variant fuses the per-group top-k of the same section (eq. I^(r)_i) into the
+// epilogue and never writes M: the thread that owns a (query, group) row sees the row's block
+// maxima in ascending block order, and keeps every block b < l(i) whose score is strictly
+// above tau, the (k-1)-th best score among the blocks kept so far, in a per-row buffer in
+// shared memory.  When a buffer is about to overflow, the warp compacts (all lanes at once) to
+// each row's best k-1 under (score desc, block asc) and raises tau.  A block with a score equal
+// to tau ranks below the k-1 earlier (lower-indexed) blocks that hold tau or more, so the
+// strict test loses nothing.  At the end each row writes its kept blocks ascending, then l(i),
+// then -1 padding: exactly what msa_select_blocks writes from the same fp32 block scores.
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <climits>
 #include <cmath>
 #include <mutex>
 
@@ -34,9 +45,12 @@ constexpr int kKeys = 128;     // UMMA N: keys per tile
 constexpr int kStages = 4;     // K_idx ring depth
 constexpr int kGroupBlocks = 32;   // blocks staged per row before a store
 constexpr int kTilesPerGroup = kGroupBlocks / (kKeys / kBlock);
-
-template <int D_IDX, int SUB>
+// SELECT: candidate slots per row, CAP = 32 for k <= 16 and 56 for k <= 32 (k - 1 kept after
+// each compaction); the row stride CAP + 1 is odd, so the 32 lanes' rows fall in distinct banks.
+template <int D_IDX, int SUB, int CAP = 0>
 struct ScoreSmem {
+  static constexpr bool SELECT = CAP > 0;
+  static constexpr int kCapStride = CAP + 1;
   static constexpr int kABytes = kRows * D_IDX * 2;
   static constexpr int kBBytes = kKeys * D_IDX * 2;
   static constexpr int kEpiWarps = 4 * SUB;
@@ -44,7 +58,10 @@ struct ScoreSmem {
   static constexpr int kOffA = 0;
   static constexpr int kOffB = kOffA + SUB * kABytes;
   static constexpr int kOffStage = kOffB + kStages * kBBytes;
-  static constexpr int kOffBar = kOffStage + kEpiWarps * kStageFloats * 4;
+  // SELECT: candidate scores of every epilogue row (row stride kCapStride), then their blocks
+  static constexpr int kStageBytes =
+      SELECT ? kEpiWarps * 32 * kCapStride * 8 : kEpiWarps * kStageFloats * 4;
+  static constexpr int kOffBar = kOffStage + kStageBytes;
   // barriers: full_a, full_b[kStages], empty_b[kStages], tfull[2], tempty[2], done
   static constexpr int kNumBars = 1 + 2 * kStages + 4 + 1;
   static constexpr int kOffTmem = kOffBar + kNumBars * 8;
@@ -53,6 +70,7 @@ struct ScoreSmem {
   static constexpr int kThreads = 64 + 32 * kEpiWarps;
   static constexpr uint32_t kTmemCols = 2 * SUB * kKeys;
   static_assert(kTmemCols <= 512, "TMEM has 512 columns");
+  static_assert(kAlloc <= 227 * 1024, "shared memory per CTA");
   static_assert(kOffB % 1024 == 0 && kOffStage % 1024 == 0, "1024-B aligned swizzle atoms");
 };
 
@@ -73,13 +91,66 @@ __device__ __forceinline__ float max64(const uint32_t* v) {
   return fmax3(m0, m1, fmaxf(m2, m3));
 }
 
-template <int D_IDX, int SUB>
-__global__ void __launch_bounds__(ScoreSmem<D_IDX, SUB>::kThreads, 1)
+// SELECT: keeps a row's best min(cnt, km1) candidates, in rank order (score desc, block asc),
+// at the front of its buffer; returns the new tau (the km1-th best score, -inf if fewer, +inf
+// for k = 1).  The buffer is always in ascending block order among equal scores (a sorted
+// prefix, then blocks appended in increasing order), so an entry's rank is the number of
+// earlier entries with a score >= its own plus later ones with a score > its own: independent
+// comparisons in registers, no dependent chain.
+template <int CAP>
+__device__ __forceinline__ float compact_row(float* sc, int* bl, int& cnt, int km1) {
+  float sv[CAP];
+  int bv[CAP], rk[CAP];
+#pragma unroll
+  for (int t = 0; t < CAP; ++t) {
+    sv[t] = t < cnt ? sc[t] : -INFINITY;
+    bv[t] = bl[t];
+    rk[t] = 0;
+  }
+#pragma unroll
+  for (int e = 1; e < CAP; ++e)
+#pragma unroll
+    for (int t = 0; t < e; ++t) {
+      const int above = sv[t] >= sv[e];       // the earlier entry ranks first on a tie
+      rk[e] += above;
+      rk[t] += 1 - above;
+    }
+  int kept = 0;
+#pragma unroll
+  for (int e = 0; e < CAP; ++e)
+    if (e < cnt && rk[e] < km1) {
+      sc[rk[e]] = sv[e];
+      bl[rk[e]] = bv[e];
+      ++kept;
+    }
+  cnt = kept;
+  if (km1 == 0) return INFINITY;                   // k = 1: only the local block
+  return kept == km1 ? sc[km1 - 1] : -INFINITY;
+}
+
+// SELECT: writes the row's kept blocks (distinct) in ascending order, each at its rank.
+template <int CAP>
+__device__ __forceinline__ void write_ascending(const int* bl, int cnt, int32_t* out) {
+  int bv[CAP];
+#pragma unroll
+  for (int t = 0; t < CAP; ++t) bv[t] = t < cnt ? bl[t] : INT_MAX;
+#pragma unroll
+  for (int e = 0; e < CAP; ++e) {
+    if (e >= cnt) break;
+    int pos = 0;
+#pragma unroll
+    for (int t = 0; t < CAP; ++t) pos += bv[t] < bv[e];
+    out[pos] = bv[e];
+  }
+}
+
+template <int D_IDX, int SUB, int CAP>
+__global__ void __launch_bounds__(ScoreSmem<D_IDX, SUB, CAP>::kThreads, 1)
     k_index_block_scores(const __grid_constant__ CUtensorMap tm_q,
                          const __grid_constant__ CUtensorMap tm_k, float* __restrict__ M,
-                         int log2_hkv, int64_t q_start, int64_t q_count, int64_t nblk,
-                         float scale) {
-  using L = ScoreSmem<D_IDX, SUB>;
+                         int32_t* __restrict__ idx, int kk, int64_t N, int log2_hkv,
+                         int64_t q_start, int64_t q_count, int64_t nblk, float scale) {
+  using L = ScoreSmem<D_IDX, SUB, CAP>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -181,74 +252,128 @@ __global__ void __launch_bounds__(ScoreSmem<D_IDX, SUB>::kThreads, 1)
     const int e = warp - 2;
     const int s = e >> 2;                                 // sub-tile
     const int q = warp & 3;                               // TMEM lane quarter
-    float* stage = reinterpret_cast<float*>(smem + L::kOffStage) + e * L::kStageFloats;
-    const int64_t Rw = R0 + (int64_t)s * kRows + 32 * q;  // first row of this warp
-    const int64_t R = Rw + lane;
-    const int64_t i = R >> log2_hkv;
-    const int64_t l = i >> 6;                             // local block of this row
-    const float ninf = -INFINITY;
-
-    auto flush = [&](int g, int ncols) {
-      __syncwarp();
-      for (int rho = 0; rho < 32; ++rho) {
-        const int64_t Rr = Rw + rho;
-        const int64_t ir = Rr >> log2_hkv;
-        if (ir >= i_end) break;
-        const int rr = (int)(Rr & (H_kv - 1));
-        const int64_t b = (int64_t)g * kGroupBlocks + lane;
-        if (b < nblk) {
-          const float val = lane < ncols ? stage[rho * 33 + lane] : ninf;
-          M[((int64_t)rr * q_count + (ir - q_start)) * nblk + b] = val;
+    if constexpr (L::SELECT) {
+      const int64_t R = R0 + (int64_t)s * kRows + 32 * q + lane;
+      const int64_t i = R >> log2_hkv;
+      const int64_t l = i >> 6;                           // local block of this row
+      float* sc = reinterpret_cast<float*>(smem + L::kOffStage) + (e * 32 + lane) * L::kCapStride;
+      int* bl = reinterpret_cast<int*>(smem + L::kOffStage) +
+                (L::kEpiWarps + e) * 32 * L::kCapStride + lane * L::kCapStride;
+      const int km1 = kk - 1;
+      int cnt = 0;
+      float tau = km1 > 0 ? -INFINITY : INFINITY;
+      bool ok = true;
+      for (int kt = 0; kt < nkt; ++kt) {
+        const int acc = kt & 1, use = kt >> 1;
+        if (!mbar_wait(tfull(acc), use & 1, &g_score_status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int64_t b = 2 * (int64_t)kt + h;
+          if (!__any_sync(0xffffffffu, b < l)) continue;   // no row of the warp needs it
+          uint32_t v[64];
+          const uint32_t taddr = tmem_base + ((uint32_t)(32 * q) << 16) +
+                                 (uint32_t)((acc * SUB + s) * kKeys + 64 * h);
+          MSA_TMEM_LD64(taddr, v);
+          tmem_ld_wait();
+          if (b < l) {
+            const float m = max64(v) * scale;
+            if (m > tau) {
+              sc[cnt] = m;
+              bl[cnt] = (int)b;
+              ++cnt;
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tempty(acc));
+        if (__any_sync(0xffffffffu, cnt > CAP - 2)) tau = compact_row<CAP>(sc, bl, cnt, km1);
+      }
+      if (ok) {
+        compact_row<CAP>(sc, bl, cnt, km1);      // whole warp: the compaction is unrolled
+        if (i < i_end) {
+          // kept blocks ascending, then l, then -1
+          const int rr = (int)(R & ((1 << log2_hkv) - 1));
+          int32_t* out = idx + ((int64_t)rr * N + i) * kk;
+          write_ascending<CAP>(bl, cnt, out);
+          out[cnt] = (int32_t)l;
+          for (int j = cnt + 1; j < kk; ++j) out[j] = -1;
         }
       }
-      __syncwarp();
-    };
+    } else {
+      float* stage = reinterpret_cast<float*>(smem + L::kOffStage) + e * L::kStageFloats;
+      const int64_t Rw = R0 + (int64_t)s * kRows + 32 * q;  // first row of this warp
+      const int64_t R = Rw + lane;
+      const int64_t i = R >> log2_hkv;
+      const int64_t l = i >> 6;                             // local block of this row
+      const float ninf = -INFINITY;
 
-    bool ok = true;
-    for (int kt = 0; kt < nkt; ++kt) {
-      const int acc = kt & 1, use = kt >> 1;
-      if (!mbar_wait(tfull(acc), use & 1, &g_score_status)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int64_t b = 2 * (int64_t)kt + h;
-        uint32_t v[64];
-        const uint32_t taddr = tmem_base + ((uint32_t)(32 * q) << 16) +
-                               (uint32_t)((acc * SUB + s) * kKeys + 64 * h);
-        MSA_TMEM_LD64(taddr, v);
-        tmem_ld_wait();
-        float m = ninf;
-        if (b < l) {
-          m = max64(v) * scale;
-        } else if (b == l) {                              // diagonal block: keys j <= i only
-          const int lim = (int)(i - 64 * b);
-#pragma unroll
-          for (int c = 0; c < 64; ++c)
-            if (c > lim) v[c] = __float_as_uint(ninf);
-          m = max64(v) * scale;
+      auto flush = [&](int g, int ncols) {
+        __syncwarp();
+        for (int rho = 0; rho < 32; ++rho) {
+          const int64_t Rr = Rw + rho;
+          const int64_t ir = Rr >> log2_hkv;
+          if (ir >= i_end) break;
+          const int rr = (int)(Rr & (H_kv - 1));
+          const int64_t b = (int64_t)g * kGroupBlocks + lane;
+          if (b < nblk) {
+            const float val = lane < ncols ? stage[rho * 33 + lane] : ninf;
+            M[((int64_t)rr * q_count + (ir - q_start)) * nblk + b] = val;
+          }
         }
-        stage[lane * 33 + (int)(b & (kGroupBlocks - 1))] = m;
+        __syncwarp();
+      };
+
+      bool ok = true;
+      for (int kt = 0; kt < nkt; ++kt) {
+        const int acc = kt & 1, use = kt >> 1;
+        if (!mbar_wait(tfull(acc), use & 1, &g_score_status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+  #pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int64_t b = 2 * (int64_t)kt + h;
+          uint32_t v[64];
+          const uint32_t taddr = tmem_base + ((uint32_t)(32 * q) << 16) +
+                                 (uint32_t)((acc * SUB + s) * kKeys + 64 * h);
+          MSA_TMEM_LD64(taddr, v);
+          tmem_ld_wait();
+          float m = ninf;
+          if (b < l) {
+            m = max64(v) * scale;
+          } else if (b == l) {                              // diagonal block: keys j <= i only
+            const int lim = (int)(i - 64 * b);
+  #pragma unroll
+            for (int c = 0; c < 64; ++c)
+              if (c > lim) v[c] = __float_as_uint(ninf);
+            m = max64(v) * scale;
+          }
+          stage[lane * 33 + (int)(b & (kGroupBlocks - 1))] = m;
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tempty(acc));
+        const int kt_in_group = kt % kTilesPerGroup;
+        if (kt_in_group == kTilesPerGroup - 1 || kt == nkt - 1)
+          flush(kt / kTilesPerGroup, 2 * (kt_in_group + 1));
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(tempty(acc));
-      const int kt_in_group = kt % kTilesPerGroup;
-      if (kt_in_group == kTilesPerGroup - 1 || kt == nkt - 1)
-        flush(kt / kTilesPerGroup, 2 * (kt_in_group + 1));
-    }
-    if (ok) {
-      // blocks after the last key tile are in every row's future
-      const int64_t b_first = ((int64_t)(nkt - 1) / kTilesPerGroup + 1) * kGroupBlocks;
-      for (int rho = 0; rho < 32; ++rho) {
-        const int64_t Rr = Rw + rho;
-        const int64_t ir = Rr >> log2_hkv;
-        if (ir >= i_end) break;
-        const int rr = (int)(Rr & (H_kv - 1));
-        float* row = M + ((int64_t)rr * q_count + (ir - q_start)) * nblk;
-        for (int64_t b = b_first + lane; b < nblk; b += 32) row[b] = ninf;
+      if (ok) {
+        // blocks after the last key tile are in every row's future
+        const int64_t b_first = ((int64_t)(nkt - 1) / kTilesPerGroup + 1) * kGroupBlocks;
+        for (int rho = 0; rho < 32; ++rho) {
+          const int64_t Rr = Rw + rho;
+          const int64_t ir = Rr >> log2_hkv;
+          if (ir >= i_end) break;
+          const int rr = (int)(Rr & (H_kv - 1));
+          float* row = M + ((int64_t)rr * q_count + (ir - q_start)) * nblk;
+          for (int64_t b = b_first + lane; b < nblk; b += 32) row[b] = ninf;
+        }
       }
     }
   }
@@ -260,11 +385,12 @@ __global__ void __launch_bounds__(ScoreSmem<D_IDX, SUB>::kThreads, 1)
   }
 }
 
-template <int D_IDX, int SUB>
-cudaError_t launch_scores(const CUtensorMap& tq, const CUtensorMap& tk, float* M, int H_kv,
-                          int64_t q_start, int64_t q_count, int64_t nblk, cudaStream_t stream) {
-  using L = ScoreSmem<D_IDX, SUB>;
-  auto kern = k_index_block_scores<D_IDX, SUB>;
+template <int D_IDX, int SUB, int CAP>
+cudaError_t launch_scores(const CUtensorMap& tq, const CUtensorMap& tk, float* M, int32_t* idx,
+                          int kk, int64_t N, int H_kv, int64_t q_start, int64_t q_count,
+                          int64_t nblk, cudaStream_t stream) {
+  using L = ScoreSmem<D_IDX, SUB, CAP>;
+  auto kern = k_index_block_scores<D_IDX, SUB, CAP>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
   if (e != cudaSuccess) return e;
   int log2_hkv = 0;
@@ -272,16 +398,16 @@ cudaError_t launch_scores(const CUtensorMap& tq, const CUtensorMap& tk, float* M
   const int64_t per_cta = (int64_t)SUB * (kRows / H_kv);
   const int64_t grid = (q_count + per_cta - 1) / per_cta;
   const float scale = (float)(1.0 / std::sqrt((double)D_IDX));
-  kern<<<(unsigned)grid, L::kThreads, L::kAlloc, stream>>>(tq, tk, M, log2_hkv, q_start, q_count,
-                                                           nblk, scale);
+  kern<<<(unsigned)grid, L::kThreads, L::kAlloc, stream>>>(tq, tk, M, idx, kk, N, log2_hkv,
+                                                           q_start, q_count, nblk, scale);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_index_block_scores(const void* q_idx, const void* k_idx, float* M, int64_t N,
-                                      int H_kv, int d_idx, int64_t q_start, int64_t q_count,
-                                      cudaStream_t stream) {
+static cudaError_t launch_index(const void* q_idx, const void* k_idx, float* M, int32_t* idx,
+                               int kk, int64_t N, int H_kv, int d_idx, int64_t q_start,
+                               int64_t q_count, cudaStream_t stream) {
   CUtensorMap tq, tk;
   const int swz = d_idx * 2;   // one swizzle row per index vector
   cudaError_t e = make_tma_2d_bf16(&tq, q_idx, (uint64_t)d_idx, (uint64_t)N * H_kv, d_idx, kRows, swz);
@@ -289,8 +415,24 @@ cudaError_t launch_index_block_scores(const void* q_idx, const void* k_idx, floa
   e = make_tma_2d_bf16(&tk, k_idx, (uint64_t)d_idx, (uint64_t)N, d_idx, kKeys, swz);
   if (e != cudaSuccess) return e;
   const int64_t nblk = (N + kBlock - 1) / kBlock;
-  if (d_idx == 64) return launch_scores<64, 2>(tq, tk, M, H_kv, q_start, q_count, nblk, stream);
-  return launch_scores<32, 2>(tq, tk, M, H_kv, q_start, q_count, nblk, stream);
+#define MSA_SCORES(D, CAP) \
+  launch_scores<D, 2, CAP>(tq, tk, M, idx, kk, N, H_kv, q_start, q_count, nblk, stream)
+  if (idx != nullptr && kk <= 16) return d_idx == 64 ? MSA_SCORES(64, 32) : MSA_SCORES(32, 32);
+  if (idx != nullptr) return d_idx == 64 ? MSA_SCORES(64, 56) : MSA_SCORES(32, 56);
+  return d_idx == 64 ? MSA_SCORES(64, 0) : MSA_SCORES(32, 0);
+#undef MSA_SCORES
+}
+
+cudaError_t launch_index_block_scores(const void* q_idx, const void* k_idx, float* M, int64_t N,
+                                      int H_kv, int d_idx, int64_t q_start, int64_t q_count,
+                                      cudaStream_t stream) {
+  return launch_index(q_idx, k_idx, M, nullptr, 0, N, H_kv, d_idx, q_start, q_count, stream);
+}
+
+cudaError_t launch_index_select(const void* q_idx, const void* k_idx, int32_t* idx, int64_t N,
+                                int H_kv, int d_idx, int k, int64_t q_start, int64_t q_count,
+                                cudaStream_t stream) {
+  return launch_index(q_idx, k_idx, nullptr, idx, k, N, H_kv, d_idx, q_start, q_count, stream);
 }
 
 cudaError_t read_reset_score_status(unsigned* out) {

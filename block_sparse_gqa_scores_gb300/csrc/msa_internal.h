@@ -51,6 +51,9 @@ cudaError_t launch_attn_kvouter(const void* q, const void* k, const void* v, con
 cudaError_t launch_index_block_scores(const void* q_idx, const void* k_idx, float* M, int64_t N,
                                       int H_kv, int d_idx, int64_t q_start, int64_t q_count,
                                       cudaStream_t stream);
+cudaError_t launch_index_select(const void* q_idx, const void* k_idx, int32_t* idx, int64_t N,
+                                int H_kv, int d_idx, int k, int64_t q_start, int64_t q_count,
+                                cudaStream_t stream);
 cudaError_t read_reset_score_status(unsigned* out);
 
 cudaError_t launch_select_prefill(const float* M, int32_t* idx, int64_t N, int H_kv, int k,

@@ -36,6 +36,7 @@ def _load():
     L.msa_status_string.restype = ctypes.c_char_p
     L.msa_index_block_scores.argtypes = [P, P, P, i64, i32, i32, i32, i64, i64, P]
     L.msa_select_blocks.argtypes = [P, P, i64, i32, i32, i32, i64, i64, P]
+    L.msa_index_select.argtypes = [P, P, P, i64, i32, i32, i32, i32, i64, i64, P]
     L.msa_sparse_attn_fwd_workspace.argtypes = [i64, i32, i32, i32, i32]
     L.msa_sparse_attn_fwd_workspace.restype = sz
     L.msa_sparse_attn_fwd.argtypes = [P, P, P, P, P, P, i64, i32, i32, i32, i32, i32, P, sz, P]
@@ -45,7 +46,7 @@ def _load():
                                     P, P, sz, P]
     L.msa_sparse_decode_noalloc.argtypes = [P, P, P, P, P, P, i32, i64, i32, i32, i32, i32, i32,
                                             i32, P, P, P, P]
-    for fn in ("msa_index_block_scores", "msa_select_blocks", "msa_sparse_attn_fwd",
+    for fn in ("msa_index_block_scores", "msa_select_blocks", "msa_index_select", "msa_sparse_attn_fwd",
                "msa_sparse_decode", "msa_sparse_decode_noalloc", "msa_device_status"):
         getattr(L, fn).restype = i32
     return L
@@ -104,6 +105,23 @@ def msa_select_blocks(M, N, k, idx=None, q_start=0, block_size=BLOCK, stream=Non
     _req(idx, torch.int32, 3, "idx")
     _check("msa_select_blocks", lib.msa_select_blocks(
         _ptr(M), _ptr(idx), N, H_kv, block_size, k, q_start, q_count, _stream(stream)))
+    return idx
+
+
+def msa_index_select(q_idx, k_idx, k, idx=None, q_start=0, q_count=None, block_size=BLOCK,
+                     stream=None):
+    """Selected blocks idx [H_kv, N, k] int32 straight from Q_idx, K_idx (no M); rows
+    q_start..q_start+q_count-1 written."""
+    _req(q_idx, torch.bfloat16, 3, "q_idx")
+    _req(k_idx, torch.bfloat16, 2, "k_idx")
+    N, H_kv, d_idx = q_idx.shape
+    q_count = N - q_start if q_count is None else q_count
+    if idx is None:
+        idx = torch.full((H_kv, N, k), -2, dtype=torch.int32, device=q_idx.device)
+    _req(idx, torch.int32, 3, "idx")
+    _check("msa_index_select", lib.msa_index_select(
+        _ptr(q_idx), _ptr(k_idx), _ptr(idx), N, H_kv, d_idx, block_size, k, q_start, q_count,
+        _stream(stream)))
     return idx
 
 

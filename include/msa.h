@@ -77,6 +77,23 @@ msa_status_t msa_index_block_scores(const void *q_idx, const void *k_idx, float 
 msa_status_t msa_select_blocks(const float *M, int32_t *idx, int64_t N, int H_kv, int block_size,
                                int k, int64_t q_start, int64_t q_count, void *stream);
 
+/* Largest k msa_index_select supports (larger k: MSA_ERR_UNSUPPORTED; use
+ * msa_index_block_scores + msa_select_blocks). */
+#define MSA_INDEX_SELECT_MAX_K 32
+
+/* The index branch in one pass: the block scores of msa_index_block_scores and the selection of
+ * msa_select_blocks (eqs. S^idx, M^idx and I^(r)_i of section 索引分支), without writing M.
+ * For each group r and row i in [q_start, q_start+q_count) it writes idx[r, i, :] exactly as
+ * msa_select_blocks would from the M that msa_index_block_scores computes for the same inputs
+ * (same fp32 block scores, same ordering (score desc, block asc), ascending, -1 padded).
+ *   q_idx  bf16 [N, H_kv, d_idx];  k_idx bf16 [N, d_idx]
+ *   idx    int32 [H_kv, N, k]  only rows q_start..q_start+q_count-1 are written
+ * Needs no workspace.  k in [1, MSA_INDEX_SELECT_MAX_K]; other argument errors as
+ * msa_index_block_scores and msa_select_blocks. */
+msa_status_t msa_index_select(const void *q_idx, const void *k_idx, int32_t *idx, int64_t N,
+                              int H_kv, int d_idx, int block_size, int k, int64_t q_start,
+                              int64_t q_count, void *stream);
+
 /* Workspace bytes msa_sparse_attn_fwd needs for these sizes (0 for invalid sizes).  It grows
  * with min(N, 16384) * H_q * k * d_h (the private-block partials of one 16384-row query chunk):
  * 2.19 GB at H_q=32, k=16, d_h=128 for any N >= 16384. */

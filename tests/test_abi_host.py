@@ -24,8 +24,8 @@ def declared_symbols():
 
 def test_header_declares_the_api():
     syms = declared_symbols()
-    for name in ("msa_index_block_scores", "msa_select_blocks", "msa_sparse_attn_fwd",
-                 "msa_sparse_attn_fwd_workspace", "msa_sparse_decode",
+    for name in ("msa_index_block_scores", "msa_select_blocks", "msa_index_select",
+                 "msa_sparse_attn_fwd", "msa_sparse_attn_fwd_workspace", "msa_sparse_decode",
                  "msa_sparse_decode_workspace", "msa_status_string", "msa_device_status"):
         assert name in syms
 
@@ -58,6 +58,10 @@ def select(lib, M=P, idx=P, N=1024, H_kv=4, B=64, k=16, qs=0, qc=1024):
     return lib.msa_select_blocks(M, idx, i64(N), H_kv, B, k, i64(qs), i64(qc), NUL)
 
 
+def index_select(lib, q=P, k=P, idx=P, N=1024, H_kv=4, d_idx=64, B=64, kk=16, qs=0, qc=1024):
+    return lib.msa_index_select(q, k, idx, i64(N), H_kv, d_idx, B, kk, i64(qs), i64(qc), NUL)
+
+
 def attn(lib, q=P, k=P, v=P, idx=P, o=P, lse=P, N=1024, H_q=32, H_kv=4, d_h=128, B=64, kk=16,
          ws=P, wsb=1 << 40):
     return lib.msa_sparse_attn_fwd(q, k, v, idx, o, lse, i64(N), H_q, H_kv, d_h, B, kk, ws,
@@ -88,6 +92,19 @@ def test_scores_unsupported(lib, kw):
                                 dict(qs=1024, qc=1), dict(N=-5)])
 def test_select_invalid(lib, kw):
     assert select(lib, **kw) == INVALID
+
+
+@pytest.mark.parametrize("kw", [dict(q=NUL), dict(k=MIS), dict(idx=NUL), dict(N=0), dict(B=32),
+                                dict(kk=0), dict(kk=65), dict(qs=-1), dict(qc=0),
+                                dict(qs=1000, qc=100), dict(H_kv=0)])
+def test_index_select_invalid(lib, kw):
+    assert index_select(lib, **kw) == INVALID
+
+
+@pytest.mark.parametrize("kw", [dict(H_kv=3), dict(H_kv=16), dict(d_idx=48), dict(kk=33),
+                                dict(kk=64)])
+def test_index_select_unsupported(lib, kw):
+    assert index_select(lib, **kw) == UNSUPPORTED
 
 
 @pytest.mark.parametrize("kw", [dict(q=NUL), dict(o=MIS), dict(N=0), dict(H_q=30), dict(kk=0),

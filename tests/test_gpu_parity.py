@@ -151,6 +151,67 @@ def test_sparse_attention_zero_query_closed_form():
     assert np.abs(lse.cpu().numpy() - np.log(T)[None, :]).max() <= 1e-4
 
 
+# ---------------------------------------------------------- fused index branch --
+# msa_index_select must write exactly what msa_select_blocks writes from the block scores of
+# msa_index_block_scores (same fp32 scores, same ordering), and so match the oracle wherever
+# the unfused path does.
+
+FUSED_CASES = [
+    ("tiny", {}, 1024, "gauss", 0, 4, 0, None), ("tiny", {}, 1024, "int", 0, 4, 0, None),
+    ("tiny", {}, 777, "int", 3, 2, 0, None), ("tiny", {}, 1024, "gauss", 1, 1, 0, None),
+    ("tiny", {"H_kv": 1}, 1000, "gauss", 0, 4, 0, None),
+    ("tiny", {"H_kv": 8}, 1000, "int", 0, 5, 0, None),
+    ("tiny", {"d_idx": 64}, 1024, "gauss", 2, 4, 0, None),
+    ("p32k", {}, 1, "gauss", 0, 16, 0, None), ("p32k", {}, 63, "gauss", 0, 16, 0, None),
+    ("p32k", {}, 65, "int", 0, 16, 0, None), ("p32k", {}, 3000, "gauss", 0, 16, 0, None),
+    ("p32k", {}, 4099, "int", 1, 32, 0, None), ("p32k", {}, 4099, "gauss", 2, 16, 0, None),
+    ("p32k", {}, 4099, "gauss", 0, 16, 1000, 2000), ("p32k", {}, 3000, "int", 0, 16, 2999, 1),
+    ("p128k", {}, 4500, "gauss", 0, 16, 0, None), ("p32k", {}, 32768, "gauss", 0, 16, 0, None),
+]
+
+
+@pytest.mark.parametrize("name,over,N,variant,seed,k,q_start,q_count", FUSED_CASES)
+def test_index_select_equals_scores_then_select(name, over, N, variant, seed, k, q_start, q_count):
+    if "H_kv" in over:
+        over = {**over, "H_q": 8 * over["H_kv"]}
+    cfg = cfg_of(name, **over)
+    x, b = fresh(cfg, N, seed, variant)
+    qc = N - q_start if q_count is None else q_count
+    fused = msa.msa_index_select(x["q_idx"], x["k_idx"], k, q_start=q_start, q_count=qc)
+    M = msa.msa_index_block_scores(x["q_idx"], x["k_idx"], q_start=q_start, q_count=qc)
+    ref = msa.msa_select_blocks(M, N, k, q_start=q_start)
+    sync_ok()
+    assert torch.equal(fused, ref)
+    if variant == "int" and N <= 4099:
+        _, M_ref = oracle.block_scores(b["q_idx"], b["k_idx"], q_start=q_start, q_count=qc)
+        I_ref = oracle.select_blocks(M_ref, N, k, q_start=q_start)
+        assert np.array_equal(fused.cpu().numpy(), I_ref)
+
+
+@pytest.mark.parametrize("trend,k", [("rising", 32), ("rising", 2), ("falling", 16), ("flat", 16)])
+def test_index_select_score_trends(trend, k):
+    """Block scores that rise with the block index make every block a candidate (the most
+    compactions); falling scores fill the buffer once; flat scores tie everywhere, where the
+    closed form is I = {0, ..., k-2} U {l}."""
+    N, H_kv, d_idx = 8192, 4, 64
+    j = torch.arange(N, device="cuda")
+    val = {"rising": (j // 64) % 200, "falling": 199 - (j // 64) % 200, "flat": 0 * j}[trend]
+    k_idx = (val.float()[:, None] / 8).expand(N, d_idx).to(torch.bfloat16).contiguous()
+    q_idx = torch.ones((N, H_kv, d_idx), dtype=torch.bfloat16, device="cuda")
+    fused = msa.msa_index_select(q_idx, k_idx, k)
+    M = msa.msa_index_block_scores(q_idx, k_idx)
+    ref = msa.msa_select_blocks(M, N, k)
+    sync_ok()
+    assert torch.equal(fused, ref)
+    if trend == "flat":
+        I = fused.cpu().numpy()
+        for i in (0, 63, 64, 1000, N - 1):
+            l = i // 64
+            want = list(range(min(l, k - 1))) + [l]
+            want += [-1] * (k - len(want))
+            assert I[:, i].tolist() == [want] * H_kv
+
+
 # ------------------------------------------------------------------- end to end --
 
 @pytest.mark.parametrize("name,N,variant,seed", [("tiny", 1024, "gauss", 0), ("tiny", 1024, "gauss", 1),
