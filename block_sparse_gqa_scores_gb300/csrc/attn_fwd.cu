@@ -7,7 +7,16 @@
 //   k_attn_shared                            16-query tiles over their shared blocks; its
 //                                            epilogue merges the private partials in slot
 //                                            order and writes O and LSE
-// Nothing here allocates or synchronises; the caller provides the workspace.
+// The two passes stress different units (the block-major pass moves the partials and the
+// gathered query rows through HBM; the shared-block pass is bound by its softmax chain), so
+// chunks are pipelined over two streams: the plan and block-major pass of chunk c+1 run on a
+// library-owned side stream while the shared-block pass of chunk c runs on the caller's
+// stream, with two workspace sets used alternately and events ordering each hand-over.  All
+// work of the call is complete when the caller's stream reaches the end of it.
+// Nothing here allocates device memory or synchronises the host; the caller provides the
+// workspace.
+#include <mutex>
+
 #include "attn_tile.cuh"
 #include "msa_internal.h"
 
@@ -17,13 +26,15 @@ namespace {
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 constexpr int64_t kChunkRows = 16384;     // query rows per pass (bounds the workspace)
+constexpr int kKvoCtasPerSm = 3;         // block-major pass: 3 resident CTAs hide its gathers
 
 struct AttnWs {
-  size_t count, offset, tile_off, cursor, entries, part_o, part_lse, total;
+  size_t count, offset, tile_off, cursor, entries, part_o, part_lse, set_bytes;
   int64_t qc;
-  int nb;
+  int nb, sets;
 };
 
+// One workspace set per chunk in flight: two when there is more than one chunk.
 AttnWs attn_layout(int64_t N, int H_q, int H_kv, int d_h, int kk) {
   AttnWs w{};
   const int G = H_q / H_kv;
@@ -40,32 +51,60 @@ AttnWs attn_layout(int64_t N, int H_q, int H_kv, int d_h, int kk) {
   w.entries = take(4 * sel);
   w.part_o = take(2 * sel * G * d_h);
   w.part_lse = take(4 * sel * G);
-  w.total = off;
+  w.set_bytes = off;
+  w.sets = N > w.qc ? 2 : 1;
   return w;
 }
+
+// The side stream of each device, created on first use.
+std::mutex g_side_mutex;
+cudaStream_t g_side[64] = {};
+
+cudaError_t side_stream(cudaStream_t* out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_side_mutex);
+  if (!g_side[dev] && (e = cudaStreamCreateWithFlags(&g_side[dev], cudaStreamNonBlocking)) != cudaSuccess)
+    return e;
+  *out = g_side[dev];
+  return cudaSuccess;
+}
+
+// Events of one call (released once the device has passed them).
+struct CallEvents {
+  cudaEvent_t start = nullptr, ready[2] = {nullptr, nullptr}, freed[2] = {nullptr, nullptr};
+  cudaError_t create() {
+    cudaError_t e = cudaEventCreateWithFlags(&start, cudaEventDisableTiming);
+    for (int s = 0; s < 2 && e == cudaSuccess; ++s) {
+      e = cudaEventCreateWithFlags(&ready[s], cudaEventDisableTiming);
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&freed[s], cudaEventDisableTiming);
+    }
+    return e;
+  }
+  ~CallEvents() {
+    if (start) cudaEventDestroy(start);
+    for (int s = 0; s < 2; ++s) {
+      if (ready[s]) cudaEventDestroy(ready[s]);
+      if (freed[s]) cudaEventDestroy(freed[s]);
+    }
+  }
+};
 
 }  // namespace
 
 size_t sparse_attn_ws_bytes(int64_t N, int H_q, int H_kv, int d_h, int kk) {
-  return attn_layout(N, H_q, H_kv, d_h, kk).total;
+  const AttnWs w = attn_layout(N, H_q, H_kv, d_h, kk);
+  return w.set_bytes * w.sets;
 }
 
 // The main branch over query chunks: plan (count) -> scan -> plan (scatter) -> block-major pass
-// over private selections -> shared-block pass (which also merges).  Everything is enqueued on
-// `stream`.
+// over private selections, then the shared-block pass (which also merges), pipelined as above.
 cudaError_t launch_sparse_attn_fwd(const void* q, const void* k, const void* v, const int32_t* idx,
                                    void* o, float* lse, int64_t N, int H_q, int H_kv, int d_h,
                                    int kk, void* ws, cudaStream_t stream) {
   const AttnWs w = attn_layout(N, H_q, H_kv, d_h, kk);
-  char* base = static_cast<char*>(ws);
-  int* count = reinterpret_cast<int*>(base + w.count);
-  int* offset = reinterpret_cast<int*>(base + w.offset);
-  int* tile_off = reinterpret_cast<int*>(base + w.tile_off);
-  int* cursor = reinterpret_cast<int*>(base + w.cursor);
-  int* entries = reinterpret_cast<int*>(base + w.entries);
-  void* part_o = base + w.part_o;
-  float* part_lse = reinterpret_cast<float*>(base + w.part_lse);
-
   CUtensorMap tk, tv;
   cudaError_t e = make_tma_3d_bf16(&tk, k, (uint64_t)d_h, (uint64_t)H_kv, (uint64_t)N, 64, 1, 32, 128);
   if (e != cudaSuccess) return e;
@@ -76,21 +115,52 @@ cudaError_t launch_sparse_attn_fwd(const void* q, const void* k, const void* v, 
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int64_t nblk = (N + kBlock - 1) / kBlock;
   const int G = H_q / H_kv;
-  for (int64_t q0 = 0; q0 < N; q0 += w.qc) {
+
+  // one chunk: everything on the caller's stream
+  cudaStream_t side = stream;
+  CallEvents ev;
+  if (w.sets == 2) {
+    if ((e = side_stream(&side)) != cudaSuccess) return e;
+    if ((e = ev.create()) != cudaSuccess) return e;
+    if ((e = cudaEventRecord(ev.start, stream)) != cudaSuccess) return e;     // inputs ready
+    if ((e = cudaStreamWaitEvent(side, ev.start, 0)) != cudaSuccess) return e;
+  }
+  int64_t c = 0;
+  for (int64_t q0 = 0; q0 < N; q0 += w.qc, ++c) {
     const int64_t q1 = q0 + w.qc < N ? q0 + w.qc : N;
-    if ((e = cudaMemsetAsync(count, 0, 4 * (size_t)w.nb, stream)) != cudaSuccess) return e;
+    const int s = (int)(c & 1) % w.sets;
+    char* base = static_cast<char*>(ws) + (size_t)s * w.set_bytes;
+    int* count = reinterpret_cast<int*>(base + w.count);
+    int* offset = reinterpret_cast<int*>(base + w.offset);
+    int* tile_off = reinterpret_cast<int*>(base + w.tile_off);
+    int* cursor = reinterpret_cast<int*>(base + w.cursor);
+    int* entries = reinterpret_cast<int*>(base + w.entries);
+    void* part_o = base + w.part_o;
+    float* part_lse = reinterpret_cast<float*>(base + w.part_lse);
+    // the block-major half of chunk c, once the shared-block pass of chunk c-2 has read set s
+    if (w.sets == 2 && c >= 2 && (e = cudaStreamWaitEvent(side, ev.freed[s], 0)) != cudaSuccess)
+      return e;
+    if ((e = cudaMemsetAsync(count, 0, 4 * (size_t)w.nb, side)) != cudaSuccess) return e;
     if ((e = launch_attn_plan(idx, N, H_kv, kk, q0, q1, nblk, 0, count, offset, cursor, entries,
-                              stream)) != cudaSuccess) return e;
-    if ((e = launch_attn_scan(count, offset, tile_off, cursor, w.nb, 128 / G, stream)) != cudaSuccess)
+                              side)) != cudaSuccess) return e;
+    if ((e = launch_attn_scan(count, offset, tile_off, cursor, w.nb, 128 / G, side)) != cudaSuccess)
       return e;
     if ((e = launch_attn_plan(idx, N, H_kv, kk, q0, q1, nblk, 1, count, offset, cursor, entries,
-                              stream)) != cudaSuccess) return e;
+                              side)) != cudaSuccess) return e;
     if ((e = launch_attn_kvouter(q, k, v, entries, offset, tile_off, w.nb, nblk, N, q0, q1, H_q,
-                                 H_kv, d_h, kk, 3 * sms, part_o, part_lse, stream)) != cudaSuccess)
+                                 H_kv, d_h, kk, kKvoCtasPerSm * sms, part_o, part_lse, side)) != cudaSuccess)
       return e;
+    // the shared-block half (and the merge) of chunk c on the caller's stream
+    if (w.sets == 2) {
+      if ((e = cudaEventRecord(ev.ready[s], side)) != cudaSuccess) return e;
+      if ((e = cudaStreamWaitEvent(stream, ev.ready[s], 0)) != cudaSuccess) return e;
+    }
     if ((e = launch_attn_shared(tk, tv, q, idx, part_o, part_lse, o, lse, N, q0, q1, H_q,
                                 H_kv, d_h, kk, stream)) != cudaSuccess) return e;
+    if (w.sets == 2 && (e = cudaEventRecord(ev.freed[s], stream)) != cudaSuccess) return e;
   }
+  // every side-stream launch precedes a shared-block pass that waited for it, so the caller's
+  // stream finishing the last pass means the whole call is done
   return cudaSuccess;
 }
 
