@@ -333,7 +333,9 @@ def run_msa(args, world, rank, local):
             "decode": {"S": dcfg.S, "len_lo": dcfg.len_lo, "len_hi": dcfg.len_hi,
                        "mean_len": float(np.mean(d["meta"]["lens"])), "k": dcfg.k}
             if d is not None else None,
-            "l2": "no flush: every timed input exceeds the 129 MB L2 (M 4.3 GB, caches 11.5 GB)",
+            "l2": "no explicit flush: each step streams Q (1.07 GB), K/V (134 MB each), the "
+                  "4.4 GB main-branch workspace and the 11.5 GB decode caches, so nothing the "
+                  "next step reads is still in the 129 MB L2",
             "parallelism": "replicas" if world > 1 else "single",
         },
         "ms_prefill": round(t_prefill_total / K, 4),
