@@ -23,8 +23,9 @@
 // shared memory.  When a buffer is about to overflow, the warp compacts (all lanes at once) to
 // each row's best k-1 under (score desc, block asc) and raises tau.  A block with a score equal
 // to tau ranks below the k-1 earlier (lower-indexed) blocks that hold tau or more, so the
-// strict test loses nothing.  At the end each row writes its kept blocks ascending, then l(i),
-// then -1 padding: exactly what msa_select_blocks writes from the same fp32 block scores.
+// strict test loses nothing.  Compaction is stable, so the buffer stays in ascending block
+// order; at the end each row writes its kept blocks, then l(i), then -1 padding: exactly what
+// msa_select_blocks writes from the same fp32 block scores.
 #include <cudaTypedefs.h>
 
 #include <algorithm>
@@ -91,57 +92,77 @@ __device__ __forceinline__ float max64(const uint32_t* v) {
   return fmax3(m0, m1, fmaxf(m2, m3));
 }
 
-// SELECT: keeps a row's best min(cnt, km1) candidates, in rank order (score desc, block asc),
-// at the front of its buffer; returns the new tau (the km1-th best score, -inf if fewer, +inf
-// for k = 1).  The buffer is always in ascending block order among equal scores (a sorted
-// prefix, then blocks appended in increasing order), so an entry's rank is the number of
-// earlier entries with a score >= its own plus later ones with a score > its own: independent
-// comparisons in registers, no dependent chain.
-template <int CAP>
-__device__ __forceinline__ float compact_row(float* sc, int* bl, int& cnt, int km1) {
-  float sv[CAP];
-  int bv[CAP], rk[CAP];
+// Bitonic sorting network over P2 registers, every index a compile-time constant: merge stage
+// (K2, J) compares t with t ^ J, descending where bit K2 of t is clear.
+template <int P2, int K2, int J>
+__device__ __forceinline__ void bitonic_stage(float (&v)[P2]) {
 #pragma unroll
-  for (int t = 0; t < CAP; ++t) {
-    sv[t] = t < cnt ? sc[t] : -INFINITY;
-    bv[t] = bl[t];
-    rk[t] = 0;
+  for (int t = 0; t < P2; ++t) {
+    constexpr int kJ = J;
+    const int u = t ^ kJ;
+    if (u > t) {
+      const float hi = fmaxf(v[t], v[u]), lo = fminf(v[t], v[u]);
+      const bool desc = (t & K2) == 0;
+      v[t] = desc ? hi : lo;
+      v[u] = desc ? lo : hi;
+    }
   }
-#pragma unroll
-  for (int e = 1; e < CAP; ++e)
-#pragma unroll
-    for (int t = 0; t < e; ++t) {
-      const int above = sv[t] >= sv[e];       // the earlier entry ranks first on a tie
-      rk[e] += above;
-      rk[t] += 1 - above;
-    }
-  int kept = 0;
-#pragma unroll
-  for (int e = 0; e < CAP; ++e)
-    if (e < cnt && rk[e] < km1) {
-      sc[rk[e]] = sv[e];
-      bl[rk[e]] = bv[e];
-      ++kept;
-    }
-  cnt = kept;
-  if (km1 == 0) return INFINITY;                   // k = 1: only the local block
-  return kept == km1 ? sc[km1 - 1] : -INFINITY;
+  if constexpr (J > 1) bitonic_stage<P2, K2, J / 2>(v);
+}
+template <int P2, int K2>
+__device__ __forceinline__ void bitonic_pass(float (&v)[P2]) {
+  bitonic_stage<P2, K2, K2 / 2>(v);
+  if constexpr (K2 < P2) bitonic_pass<P2, K2 * 2>(v);
 }
 
-// SELECT: writes the row's kept blocks (distinct) in ascending order, each at its rank.
+// SELECT: a row's buffer always holds its candidates in ascending block order (blocks are
+// appended in increasing order and compaction is stable), which is also the order that breaks
+// score ties.  Compaction keeps the row's best min(cnt, km1) candidates: it finds the km1-th best
+// score t (a bitonic sort of the scores, unrolled in registers), then keeps, in buffer order,
+// every entry above t and the first entries equal to t until km1 are kept.  Returns the new tau:
+// t once km1 entries are held, -inf while fewer, +inf for k = 1 (only the local block).
 template <int CAP>
-__device__ __forceinline__ void write_ascending(const int* bl, int cnt, int32_t* out) {
+__device__ __forceinline__ float compact_row(float* sc, int* bl, int& cnt, int km1) {
+  if (km1 == 0) {
+    cnt = 0;
+    return INFINITY;
+  }
+  constexpr int P2 = CAP <= 32 ? 32 : 64;
+  float v[P2];
+#pragma unroll
+  for (int t = 0; t < P2; ++t) v[t] = t < cnt && t < CAP ? sc[t] : -INFINITY;
+  bitonic_pass<P2, 2>(v);                        // descending overall
+  // the km1-th best is the least of the first km1 sorted scores (a running min keeps every
+  // index a constant, so v stays in registers)
+  float th = INFINITY;
+  int above = 0;
+#pragma unroll
+  for (int j = 0; j < P2; ++j)
+    if (j < km1) th = fminf(th, v[j]);
+#pragma unroll
+  for (int j = 0; j < P2; ++j) above += v[j] > th;
+  int eq_left = km1 - above, kept = 0;
+  float sv[CAP];
   int bv[CAP];
 #pragma unroll
-  for (int t = 0; t < CAP; ++t) bv[t] = t < cnt ? bl[t] : INT_MAX;
-#pragma unroll
-  for (int e = 0; e < CAP; ++e) {
-    if (e >= cnt) break;
-    int pos = 0;
-#pragma unroll
-    for (int t = 0; t < CAP; ++t) pos += bv[t] < bv[e];
-    out[pos] = bv[e];
+  for (int t = 0; t < CAP; ++t) {
+    sv[t] = sc[t];
+    bv[t] = bl[t];
   }
+#pragma unroll
+  for (int t = 0; t < CAP; ++t) {
+    if (t < cnt) {
+      const bool eq = sv[t] == th;
+      if (sv[t] > th || (eq && eq_left > 0)) {
+        eq_left -= eq;
+        sc[kept] = sv[t];
+        bl[kept] = bv[t];
+        ++kept;
+      }
+    }
+  }
+  cnt = kept;
+  return kept == km1 ? th : -INFINITY;
 }
 
 template <int D_IDX, int SUB, int CAP>
@@ -296,10 +317,10 @@ __global__ void __launch_bounds__(ScoreSmem<D_IDX, SUB, CAP>::kThreads, 1)
       if (ok) {
         compact_row<CAP>(sc, bl, cnt, km1);      // whole warp: the compaction is unrolled
         if (i < i_end) {
-          // kept blocks ascending, then l, then -1
+          // kept blocks (already ascending), then l, then -1
           const int rr = (int)(R & ((1 << log2_hkv) - 1));
           int32_t* out = idx + ((int64_t)rr * N + i) * kk;
-          write_ascending<CAP>(bl, cnt, out);
+          for (int j = 0; j < cnt; ++j) out[j] = bl[j];
           out[cnt] = (int32_t)l;
           for (int j = cnt + 1; j < kk; ++j) out[j] = -1;
         }
