@@ -121,14 +121,23 @@ __global__ void __launch_bounds__(kThreadsKvo, 3)
   const int per = (total_tiles + gridDim.x - 1) / gridDim.x;
   const int t_beg = blockIdx.x * per;
   const int t_end = min(total_tiles, t_beg + per);
-  for (int tile = t_beg; tile < t_end && ok; ++tile) {
-    // ---- which bucket: last b with tile_off[b] <= tile
-    int lo = 0, hi = nbuckets;                               // tile_off[lo] <= tile < tile_off[hi]
+  // bucket of the first tile: last b with tile_off[b] <= t_beg (binary search, once per CTA);
+  // later tiles advance it, since a CTA's tiles are consecutive
+  int bucket = 0;
+  if (t_beg < t_end) {
+    int lo = 0, hi = nbuckets;                               // tile_off[lo] <= t_beg < tile_off[hi]
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
-      if (__ldg(tile_off + mid) <= tile) lo = mid; else hi = mid;
+      if (__ldg(tile_off + mid) <= t_beg) lo = mid; else hi = mid;
     }
-    const int bucket = lo;
+    bucket = lo;
+  }
+  int next_off = t_beg < t_end ? __ldg(tile_off + bucket + 1) : 0;   // first tile of bucket + 1
+  for (int tile = t_beg; tile < t_end && ok; ++tile) {
+    while (next_off <= tile) {                               // skip to the tile's bucket
+      ++bucket;
+      next_off = __ldg(tile_off + bucket + 1);
+    }
     const int r = (int)(bucket / nblk);
     const int64_t b = bucket - (int64_t)r * nblk;
     const int e0 = __ldg(offset + bucket) + (tile - __ldg(tile_off + bucket)) * ept;
