@@ -26,7 +26,7 @@ namespace {
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 constexpr int64_t kChunkRows = 16384;     // query rows per pass (bounds the workspace)
-constexpr int kKvoCtasPerSm = 3;         // block-major pass: 3 resident CTAs hide its gathers
+constexpr int kKvoCtasPerSm = 3;         // block-major pass: resident CTAs per SM (shared memory)
 
 struct AttnWs {
   size_t count, offset, tile_off, cursor, entries, part_o, part_lse, set_bytes;

@@ -16,7 +16,9 @@
 // slot order.
 // Q rows, K_b and V_b are gathered with cp.async into 128-byte-swizzled tiles (the canonical
 // K-major / MN-major SW128 layouts).  P reuses Q's shared memory and O reuses S's TMEM
-// columns, so three CTAs fit on an SM.  Persistent grid; each CTA takes a contiguous range of
+// columns, so three CTAs fit on an SM.  The next tile's K_b (if its bucket differs) is loaded
+// as soon as S = Q K^T has completed, and its query rows and V_b once O = P V has completed,
+// so those loads run under the softmax and the epilogue.  Persistent grid; each CTA takes a contiguous range of
 // work tiles (consecutive tiles often share K_b, V_b) and finds each tile's bucket by binary
 // search over the per-bucket tile offsets.
 #include <cmath>
@@ -43,8 +45,8 @@ struct KvoSmem {
   static constexpr int kOffV = kOffK + kHalves * kKHalf;
   static constexpr int kOffBar = kOffV + kHalves * kKHalf;
   static constexpr int kOffMisc = kOffBar + 16;
-  static constexpr int kOffEnt = kOffMisc + 16;   // entries of the current tile (<= 128)
-  static constexpr int kBytes = kOffEnt + kRowsT * 4;
+  static constexpr int kOffEnt = kOffMisc + 16;   // entries of this tile and the next (<= 128 each)
+  static constexpr int kBytes = kOffEnt + 2 * kRowsT * 4;
   static constexpr int kAlloc = kBytes + 1024;
   static constexpr uint32_t kTmemCols = D_H;      // S (64 columns), then O over the same columns
 };
@@ -113,8 +115,8 @@ __global__ void __launch_bounds__(kThreadsKvo, 3)
 
   const int total_tiles = tile_off[nbuckets];
   const int64_t kv_stride = (int64_t)H_kv * D_H;             // elements between tokens
+  constexpr int kChunks = D_H / 8;                           // 16-B chunks per row
   uint32_t phase = 0;
-  int loaded_bucket = -1;
   bool ok = true;
 
   // a contiguous range of work tiles per CTA: consecutive tiles often share a bucket (K_b, V_b)
@@ -133,47 +135,64 @@ __global__ void __launch_bounds__(kThreadsKvo, 3)
     bucket = lo;
   }
   int next_off = t_beg < t_end ? __ldg(tile_off + bucket + 1) : 0;   // first tile of bucket + 1
-  for (int tile = t_beg; tile < t_end && ok; ++tile) {
-    while (next_off <= tile) {                               // skip to the tile's bucket
-      ++bucket;
-      next_off = __ldg(tile_off + bucket + 1);
+  // tile -> (bucket, first entry, entries), advancing (bkt, nxt) from the previous tile's
+  auto describe = [&](int tile, int& bkt, int& nxt, int& e0, int& n_e) {
+    while (nxt <= tile) {
+      ++bkt;
+      nxt = __ldg(tile_off + bkt + 1);
     }
-    const int r = (int)(bucket / nblk);
-    const int64_t b = bucket - (int64_t)r * nblk;
-    const int e0 = __ldg(offset + bucket) + (tile - __ldg(tile_off + bucket)) * ept;
-    const int n_e = min(ept, __ldg(offset + bucket + 1) - e0);
-    const int rows = n_e * G;
-
-    // ---- gather: K_b, V_b (when the bucket changes) and the stacked query rows
-    constexpr int kChunks = D_H / 8;                         // 16-B chunks per row
-    if (bucket != loaded_bucket) {
-      const __nv_bfloat16* kb = k + (b * kBlock * H_kv + r) * (int64_t)D_H;
-      const __nv_bfloat16* vb = v + (b * kBlock * H_kv + r) * (int64_t)D_H;
-      for (int x = tid; x < kBlock * kChunks; x += kThreadsKvo) {
-        const int j = x / kChunks, c = x - j * kChunks;
-        const uint32_t off = (c >> 3) * L::kKHalf + j * 128 + (((c & 7) ^ (j & 7)) << 4);
-        if (b * kBlock + j < N) {
-          cp_async16(sb + L::kOffK + off, kb + j * kv_stride + c * 8);
-          cp_async16(sb + L::kOffV + off, vb + j * kv_stride + c * 8);
-        } else {                                  // past the sequence: finite zeros (p = 0 there)
+    e0 = __ldg(offset + bkt) + (tile - __ldg(tile_off + bkt)) * ept;
+    n_e = min(ept, __ldg(offset + bkt + 1) - e0);
+  };
+  // K_b and/or V_b of a bucket into their buffers (rows past the sequence: zeros, so p = 0)
+  auto load_kv = [&](int bkt, bool do_k, bool do_v) {
+    const int rb = (int)(bkt / nblk);
+    const int64_t bb = bkt - (int64_t)rb * nblk;
+    const __nv_bfloat16* kb = k + (bb * kBlock * H_kv + rb) * (int64_t)D_H;
+    const __nv_bfloat16* vb = v + (bb * kBlock * H_kv + rb) * (int64_t)D_H;
+    for (int x = tid; x < kBlock * kChunks; x += kThreadsKvo) {
+      const int j = x / kChunks, c = x - j * kChunks;
+      const uint32_t off = (c >> 3) * L::kKHalf + j * 128 + (((c & 7) ^ (j & 7)) << 4);
+      if (bb * kBlock + j < N) {
+        if (do_k) cp_async16(sb + L::kOffK + off, kb + j * kv_stride + c * 8);
+        if (do_v) cp_async16(sb + L::kOffV + off, vb + j * kv_stride + c * 8);
+      } else {
+        if (do_k)
           asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};" ::"r"(sb + L::kOffK + off), "r"(0u)
                        : "memory");
+        if (do_v)
           asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};" ::"r"(sb + L::kOffV + off), "r"(0u)
                        : "memory");
-        }
       }
-      loaded_bucket = bucket;
     }
-    if (tid < n_e) s_ent[tid] = __ldg(entries + e0 + tid);   // the tile's (row, slot) entries
-    __syncthreads();
+  };
+  // the stacked query rows of a tile (entry e's G heads are rows e*G .. e*G+G-1)
+  auto gather_q = [&](int bkt, const int* ent, int rows) {
+    const int rb = (int)(bkt / nblk);
     for (int x = tid; x < rows * kChunks; x += kThreadsKvo) {
       const int R = x / kChunks, c = x - R * kChunks;
       const int e = R / G, h = R - e * G;
-      const int64_t i = q0 + (s_ent[e] >> 6);
+      const int64_t i = q0 + (ent[e] >> 6);
       const uint32_t off = (c >> 3) * L::kQHalf + R * 128 + (((c & 7) ^ (R & 7)) << 4);
-      cp_async16(sb + L::kOffQ + off, q + (i * H_q + (int64_t)r * G + h) * D_H + c * 8);
+      cp_async16(sb + L::kOffQ + off, q + (i * H_q + (int64_t)rb * G + h) * D_H + c * 8);
     }
-    cp_async_wait_all();
+  };
+
+  int e0 = 0, n_e = 0;
+  if (t_beg < t_end) {
+    describe(t_beg, bucket, next_off, e0, n_e);
+    load_kv(bucket, true, true);
+    if (tid < n_e) s_ent[tid] = __ldg(entries + e0 + tid);
+    __syncthreads();
+    gather_q(bucket, s_ent, n_e * G);
+  }
+  for (int tile = t_beg; tile < t_end && ok; ++tile) {
+    const int cur = (tile - t_beg) & 1;
+    const int* ent_cur = s_ent + cur * kRowsT;
+    const int r = (int)(bucket / nblk);
+    const int64_t b = bucket - (int64_t)r * nblk;
+    const int rows = n_e * G;
+    cp_async_wait_all();                                     // this tile's Q (and K_b, V_b)
     fence_async_smem();
     __syncthreads();
 
@@ -195,6 +214,17 @@ __global__ void __launch_bounds__(kThreadsKvo, 3)
     phase ^= 1u;
     tc_fence_after();
 
+    // ---- K_b is free: the next tile's entries and, for a new bucket, its K_b
+    const bool has_next = tile + 1 < t_end;
+    int n_bucket = bucket, n_next = next_off, n_e0 = 0, n_ne = 0;
+    if (has_next) {
+      describe(tile + 1, n_bucket, n_next, n_e0, n_ne);
+      if (tid < n_ne) s_ent[(cur ^ 1) * kRowsT + tid] = __ldg(entries + n_e0 + tid);
+    }
+    const bool new_bucket = has_next && n_bucket != bucket;
+    if (new_bucket) load_kv(n_bucket, true, false);
+    asm volatile("cp.async.commit_group;" ::: "memory");
+
     // ---- softmax of row R = 32*warp + lane over the block's visible keys
     const int R = 32 * warp + lane;
     const bool rv = R < rows;
@@ -208,7 +238,7 @@ __global__ void __launch_bounds__(kThreadsKvo, 3)
       if (rv) {
         const int e = R / G;
         h = R - e * G;
-        const int ent = s_ent[e];
+        const int ent = ent_cur[e];
         slot_pos = ((int64_t)r * nq + (ent >> 6)) * kk + (ent & 63);
         i = q0 + (ent >> 6);
         if (b == (i >> 6)) {                                // local block: keys j <= i only
@@ -257,6 +287,11 @@ __global__ void __launch_bounds__(kThreadsKvo, 3)
     phase ^= 1u;
     tc_fence_after();
 
+    // ---- Q (holding P) and V_b are free once O = P V is done: the next tile's rows, V_b
+    if (new_bucket) load_kv(n_bucket, false, true);
+    if (has_next) gather_q(n_bucket, s_ent + (cur ^ 1) * kRowsT, n_ne * G);
+    asm volatile("cp.async.commit_group;" ::: "memory");
+
     // ---- epilogue: normalised partial (bf16) and log2-domain LSE of each row
     {
       const float inv = l > 0.f ? 1.f / l : 0.f;
@@ -282,7 +317,12 @@ __global__ void __launch_bounds__(kThreadsKvo, 3)
     }
     tc_fence_before();
     __syncthreads();
+    bucket = n_bucket;
+    next_off = n_next;
+    e0 = n_e0;
+    n_e = n_ne;
   }
+  cp_async_wait_all();                                       // no copy left in flight
 
   __syncthreads();
   if (warp == 0) {
