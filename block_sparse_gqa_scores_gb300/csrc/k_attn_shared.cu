@@ -126,6 +126,13 @@ __device__ __forceinline__ uint64_t desc_mn_sw128(uint32_t a, uint32_t lbo, uint
 // Warp 0: the tile's union; keeps the shared blocks (selected by >= 2 of the tile's queries) in
 // s_list as (block << 16 | query mask) and marks, per query, the slots whose block is private
 // (selected by that query alone: the block-major pass wrote their partials).
+__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p) : "memory");
+}
+
 __device__ __forceinline__ float ldg_nc_f32(const float* p) {
   float v;
   asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(v) : "l"(p));
@@ -389,6 +396,15 @@ __global__ void __launch_bounds__(kShThreads, 2)
       if (lane == 0) mbar_arrive(p_full(buf));
     }
     // ---- epilogue: shared-block state + private partials of each row, in slot order
+    // the query's private partials start toward L2 now, while the last MMAs drain
+    if (valid && h == 0) {
+      const unsigned long long pv = s_priv[w];
+      const int64_t rp = ((int64_t)r * (q1 - q0) + (i - q0)) * kk;
+      for (int t = 0; t < kk; ++t)
+        if ((pv >> t) & 1ull) prefetch_l2_bulk(part_o + (rp + t) * G * D_H, (uint32_t)(G * D_H * 2));
+      const float* lp = part_lse + rp * G;
+      for (int x = 0; x < kk * G; x += 32) prefetch_l2(lp + x);
+    }
     if (ok) ok = __all_sync(kAllLanes, mbar_wait(done, 0, &g_shared_status));
     tc_fence_after();
     const bool have_o = nH > 0 && ok;               // warp-uniform
@@ -453,21 +469,31 @@ __global__ void __launch_bounds__(kShThreads, 2)
                                       __uint_as_float(ov[4 * c + 3]) * c_o)
                         : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    __syncwarp();
-    // (c) the warp's queries, whole: a query's partial for all G heads is G*d_h contiguous bf16,
-    //     as is its output row, so lanes split it in 16-byte pieces (coalesced) and add the
-    //     private partials to the staged shared-block O in slot order
+    tc_fence_before();
+  }
+
+  __syncthreads();                                    // (b) of every row is in shared memory
+  // (c) every warp (the producer and MMA warps are idle by now) takes whole queries: a query's
+  //     partial for all G heads is G*d_h contiguous bf16, as is its output row, so lanes split
+  //     it in 16-byte pieces (coalesced) and add the private partials to the staged shared-block
+  //     O in slot order
+  {
+    const float* s_os = reinterpret_cast<const float*>(smem + L::kOffOs);
+    const float* s_mx = reinterpret_cast<const float*>(smem + L::kOffMx);
+    const float* s_inv = reinterpret_cast<const float*>(smem + L::kOffInv);
+    const int* s_pos = reinterpret_cast<const int*>(smem + L::kOffPos);
+    const int* s_np = reinterpret_cast<const int*>(smem + L::kOffNp);
     {
       const int U = G * D_H / 8;                      // 16-byte pieces per query
       const int lpq = U < 32 ? U : 32, qpp = 32 / lpq, ipl = U / lpq;
-      const int wq0 = (32 * qd) / G;
-      const int nwq = wq0 < kTileQ ? min(32 / G, kTileQ - wq0) : 0;
       const int sub = lane % lpq;
+      const int npass = (kTileQ + qpp - 1) / qpp;
+      const int wslot = (warp + kShThreads / 32 - 2) % (kShThreads / 32);   // warps 2.. first
       constexpr int kIpl = D_H / 32;                  // most pieces per lane (G <= 8)
       constexpr int kNb = 4;                          // partials in flight per lane
-      for (int p = 0; p < nwq; p += qpp) {
-        const int wl = p + lane / lpq, wq = wq0 + wl;
-        const bool qv = wl < nwq && i0 + wq < q1;
+      for (int ps = wslot; ps < npass; ps += kShThreads / 32) {
+        const int wq = ps * qpp + lane / lpq;
+        const bool qv = wq < kTileQ && i0 + wq < q1;
         float acc[kIpl][8], pm[kIpl], pi[kIpl];
         int pe[kIpl], ph[kIpl];
 #pragma unroll
@@ -530,10 +556,7 @@ __global__ void __launch_bounds__(kShThreads, 2)
         }
       }
     }
-    tc_fence_before();
   }
-
-  __syncthreads();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, L::kTmemCols);
