@@ -2,7 +2,8 @@
 // launch sequence over query chunks and its workspace.
 //
 // Per chunk of at most 16384 query rows:
-//   plan (count) -> scan -> plan (scatter)   bucket the private selections (attn_tile.cuh)
+//   plan (count) -> scan -> plan (scatter)   bucket the private selections (attn_tile.cuh) and
+//                                            record each tile's shared blocks
 //   k_attn_kvouter                           block-major tcgen05 pass over private selections
 //   k_attn_shared                            16-query tiles over their shared blocks; its
 //                                            epilogue merges the private partials in slot
@@ -29,7 +30,8 @@ constexpr int64_t kChunkRows = 16384;     // query rows per pass (bounds the wor
 constexpr int kKvoCtasPerSm = 3;         // block-major pass: resident CTAs per SM (shared memory)
 
 struct AttnWs {
-  size_t count, offset, tile_off, cursor, entries, part_o, part_lse, set_bytes;
+  size_t count, offset, tile_off, cursor, entries, tile_list, tile_priv, part_o, part_lse,
+      set_bytes;
   int64_t qc;
   int nb, sets;
 };
@@ -49,6 +51,9 @@ AttnWs attn_layout(int64_t N, int H_q, int H_kv, int d_h, int kk) {
   w.tile_off = take(4 * (size_t)(w.nb + 1));
   w.cursor = take(4 * (size_t)(w.nb + 1));
   w.entries = take(4 * sel);
+  const size_t tiles = (size_t)H_kv * (w.qc / kTileQ);            // 16-query tiles of a chunk
+  w.tile_list = take(4 * tiles * (kMaxShared + 1));
+  w.tile_priv = take(8 * tiles * kTileQ);
   w.part_o = take(2 * sel * G * d_h);
   w.part_lse = take(4 * sel * G);
   w.set_bytes = off;
@@ -135,6 +140,8 @@ cudaError_t launch_sparse_attn_fwd(const void* q, const void* k, const void* v, 
     int* tile_off = reinterpret_cast<int*>(base + w.tile_off);
     int* cursor = reinterpret_cast<int*>(base + w.cursor);
     int* entries = reinterpret_cast<int*>(base + w.entries);
+    int* tile_list = reinterpret_cast<int*>(base + w.tile_list);
+    auto* tile_priv = reinterpret_cast<unsigned long long*>(base + w.tile_priv);
     void* part_o = base + w.part_o;
     float* part_lse = reinterpret_cast<float*>(base + w.part_lse);
     // the block-major half of chunk c, once the shared-block pass of chunk c-2 has read set s
@@ -142,11 +149,11 @@ cudaError_t launch_sparse_attn_fwd(const void* q, const void* k, const void* v, 
       return e;
     if ((e = cudaMemsetAsync(count, 0, 4 * (size_t)w.nb, side)) != cudaSuccess) return e;
     if ((e = launch_attn_plan(idx, N, H_kv, kk, q0, q1, nblk, 0, count, offset, cursor, entries,
-                              side)) != cudaSuccess) return e;
+                              tile_list, tile_priv, side)) != cudaSuccess) return e;
     if ((e = launch_attn_scan(count, offset, tile_off, cursor, w.nb, 128 / G, side)) != cudaSuccess)
       return e;
     if ((e = launch_attn_plan(idx, N, H_kv, kk, q0, q1, nblk, 1, count, offset, cursor, entries,
-                              side)) != cudaSuccess) return e;
+                              tile_list, tile_priv, side)) != cudaSuccess) return e;
     if ((e = launch_attn_kvouter(q, k, v, entries, offset, tile_off, w.nb, nblk, N, q0, q1, H_q,
                                  H_kv, d_h, kk, kKvoCtasPerSm * sms, part_o, part_lse, side)) != cudaSuccess)
       return e;
@@ -155,7 +162,7 @@ cudaError_t launch_sparse_attn_fwd(const void* q, const void* k, const void* v, 
       if ((e = cudaEventRecord(ev.ready[s], side)) != cudaSuccess) return e;
       if ((e = cudaStreamWaitEvent(stream, ev.ready[s], 0)) != cudaSuccess) return e;
     }
-    if ((e = launch_attn_shared(tk, tv, q, idx, part_o, part_lse, o, lse, N, q0, q1, H_q,
+    if ((e = launch_attn_shared(tk, tv, q, tile_list, tile_priv, part_o, part_lse, o, lse, N, q0, q1, H_q,
                                 H_kv, d_h, kk, stream)) != cudaSuccess) return e;
     if (w.sets == 2 && (e = cudaEventRecord(ev.freed[s], stream)) != cudaSuccess) return e;
   }

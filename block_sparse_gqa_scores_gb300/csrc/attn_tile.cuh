@@ -18,6 +18,7 @@ namespace msa {
 constexpr int kTileQ = 16;         // queries per tile
 constexpr int kMaxSel = 64;        // largest k supported
 constexpr int kMaxKeys = kTileQ * kMaxSel;
+constexpr int kMaxShared = kMaxKeys / 2;   // a shared block holds at least two selections
 
 // Keys per lane for a tile's 16*k selections (a power of two, 32*EPL >= 16*k).
 template <typename F>

@@ -5,7 +5,9 @@
 //   k_attn_plan (pass 0)  per 16-query tile: count each private selection in its (group, block)
 //                         bucket (a block that only one of the tile's queries selected)
 //   k_attn_scan           exclusive scans: entry offsets and work-tile offsets per bucket
-//   k_attn_plan (pass 1)  scatter private selections into their buckets
+//   k_attn_plan (pass 1)  scatter private selections into their buckets, and record per tile its
+//                         shared blocks (block << 16 | query mask) and per query its private
+//                         slots, which the shared-block pass reads instead of rebuilding them
 // The block-major pass writes the partial of (row, slot) at a fixed position of that row and
 // slot; the merge itself is the epilogue of k_attn_shared, which finds a row's private slots
 // from its own union of the tile.  Bucket order is decided by integer atomics and does not
@@ -25,11 +27,33 @@ template <int EPL>
 __device__ __forceinline__ void plan_tile(const int32_t* __restrict__ idx, int r, int64_t i0,
                                           int64_t q0, int64_t q1, int64_t N, int kk,
                                           int64_t nblk, int pass, int* s_U, unsigned* s_mask,
-                                          int* count, const int* offset, int* cursor,
-                                          int* entries) {
+                                          unsigned long long* s_pm, int* count, const int* offset,
+                                          int* cursor, int* entries, int* tile_list,
+                                          unsigned long long* tile_priv) {
   const int lane = threadIdx.x & 31;
   int x[EPL], rank[EPL];
-  tile_union<EPL>(idx, r, i0, q1, N, kk, x, rank, s_U, s_mask);
+  if (pass == 1 && lane < kTileQ) s_pm[lane] = 0ull;
+  const int nU = tile_union<EPL>(idx, r, i0, q1, N, kk, x, rank, s_U, s_mask);
+  if (pass == 1) {
+    const int64_t tix = (int64_t)r * ((q1 - q0 + kTileQ - 1) / kTileQ) + (i0 - q0) / kTileQ;
+    int* lst = tile_list + tix * (kMaxShared + 1);
+    int nS = 0;
+    for (int base = 0; base < nU; base += 32) {
+      const int u = base + lane;
+      const unsigned m = u < nU ? s_mask[u] : 0u;
+      const bool keep = __popc(m) >= 2;
+      const unsigned kb = __ballot_sync(kAllLanes, keep);
+      if (keep) lst[1 + nS + __popc(kb & ((1u << lane) - 1u))] = (s_U[u] << 16) | (int)m;
+      nS += __popc(kb);
+    }
+    if (lane == 0) lst[0] = nS;
+#pragma unroll
+    for (int j = 0; j < EPL; ++j)
+      if (x[j] != INT_MAX && __popc(s_mask[rank[j]]) == 1)
+        atomicOr(&s_pm[TileKeys::query(x[j])], 1ull << TileKeys::slot(x[j]));
+    __syncwarp();
+    if (lane < kTileQ) tile_priv[tix * kTileQ + lane] = s_pm[lane];
+  }
 #pragma unroll
   for (int j = 0; j < EPL; ++j) {
     const int key = x[j];
@@ -49,9 +73,10 @@ __device__ __forceinline__ void plan_tile(const int32_t* __restrict__ idx, int r
 __global__ void __launch_bounds__(32 * kPlanWarps)
     k_attn_plan(const int32_t* __restrict__ idx, int64_t N, int kk, int64_t q0, int64_t q1,
                 int64_t nblk, int pass, int* count, const int* offset, int* cursor,
-                int* entries) {
+                int* entries, int* tile_list, unsigned long long* tile_priv) {
   __shared__ int s_U[kPlanWarps][kMaxKeys];
   __shared__ unsigned s_mask[kPlanWarps][kMaxKeys];
+  __shared__ unsigned long long s_pm[kPlanWarps][kTileQ];
   const int warp = threadIdx.x >> 5;
   const int r = blockIdx.y;
   const int64_t i0 = q0 + ((int64_t)blockIdx.x * kPlanWarps + warp) * kTileQ;
@@ -59,8 +84,8 @@ __global__ void __launch_bounds__(32 * kPlanWarps)
   int* U = s_U[warp];
   unsigned* Mk = s_mask[warp];
   with_epl(kk, [&](auto e) {
-    plan_tile<decltype(e)::value>(idx, r, i0, q0, q1, N, kk, nblk, pass, U, Mk, count, offset,
-                                  cursor, entries);
+    plan_tile<decltype(e)::value>(idx, r, i0, q0, q1, N, kk, nblk, pass, U, Mk, s_pm[warp], count,
+                                  offset, cursor, entries, tile_list, tile_priv);
     return 0;
   });
 }
@@ -112,11 +137,12 @@ __global__ void __launch_bounds__(kScanThreads)
 
 cudaError_t launch_attn_plan(const int32_t* idx, int64_t N, int H_kv, int kk, int64_t q0,
                              int64_t q1, int64_t nblk, int pass, int* count, const int* offset,
-                             int* cursor, int* entries, cudaStream_t st) {
+                             int* cursor, int* entries, int* tile_list,
+                             unsigned long long* tile_priv, cudaStream_t st) {
   const int64_t tiles = (q1 - q0 + kTileQ - 1) / kTileQ;
   const dim3 grid((unsigned)((tiles + kPlanWarps - 1) / kPlanWarps), (unsigned)H_kv);
   k_attn_plan<<<grid, 32 * kPlanWarps, 0, st>>>(idx, N, kk, q0, q1, nblk, pass, count, offset,
-                                                cursor, entries);
+                                                cursor, entries, tile_list, tile_priv);
   return cudaGetLastError();
 }
 

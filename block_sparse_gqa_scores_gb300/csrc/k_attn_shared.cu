@@ -4,7 +4,7 @@
 //
 // One CTA = one tile (16 consecutive queries of KV group r).  Its 16*G <= 128 (query, head)
 // rows are the M side of every UMMA:
-//   warp 0   builds the tile's union of selections, keeps the shared blocks, then streams them
+//   warp 0   loads the tile's shared blocks (recorded by the plan pass), then streams them
 //            as 32-token half blocks (K and V, 3-D tensor maps over [N, H_kv, d_h], 128-byte
 //            swizzle) through a 3-stage TMA ring;
 //   warp 1   allocates TMEM and issues  S[buf] = Q K^T  (M=128, N=32) and  O += P V  (M=128,
@@ -34,7 +34,6 @@ __device__ unsigned g_shared_status = 0;
 constexpr int kRing = 3;                 // half-block stages
 constexpr int kHalfTok = 32;             // tokens per stage
 constexpr int kShThreads = 192;          // producer, MMA, 4 softmax/epilogue warps
-constexpr int kMaxShared = kMaxKeys / 2; // a shared block holds at least two selections
 
 template <int D_H>
 struct ShSmem {
@@ -58,7 +57,6 @@ struct ShSmem {
   // O 128..128+d_h (fp32)
   static constexpr uint32_t kTmemCols = 256;
   static constexpr uint32_t kColP = 64, kColO = 128;
-  static_assert(kRing * kStage >= kMaxKeys * 8, "the union is built in the ring");
   // epilogue, over Q / ring once every MMA has completed: the rows' shared-block O (fp32,
   // already weighted), per-row max and 1/sum of the merge, per query its private partials
   static constexpr int kOsStride = D_H + 4;          // floats; 16-byte pad against conflicts
@@ -123,52 +121,23 @@ __device__ __forceinline__ uint64_t desc_mn_sw128(uint32_t a, uint32_t lbo, uint
          ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
 
-// Warp 0: the tile's union; keeps the shared blocks (selected by >= 2 of the tile's queries) in
-// s_list as (block << 16 | query mask) and marks, per query, the slots whose block is private
-// (selected by that query alone: the block-major pass wrote their partials).
 __device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 __device__ __forceinline__ void prefetch_l2(const void* p) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(p) : "memory");
 }
-
 __device__ __forceinline__ float ldg_nc_f32(const float* p) {
   float v;
   asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(v) : "l"(p));
   return v;
 }
 
-template <int EPL>
-__device__ __forceinline__ int shared_blocks(const int32_t* __restrict__ idx, int r, int64_t i0,
-                                             int64_t q1, int64_t N, int kk, int* tmpU,
-                                             unsigned* tmpM, int* s_list,
-                                             unsigned long long* s_priv) {
-  const int lane = threadIdx.x & 31;
-  if (lane < kTileQ) s_priv[lane] = 0ull;
-  int x[EPL], rank[EPL];
-  const int nU = tile_union<EPL>(idx, r, i0, q1, N, kk, x, rank, tmpU, tmpM);
-#pragma unroll
-  for (int j = 0; j < EPL; ++j)
-    if (x[j] != INT_MAX && __popc(tmpM[rank[j]]) == 1)
-      atomicOr(&s_priv[TileKeys::query(x[j])], 1ull << TileKeys::slot(x[j]));
-  int nS = 0;
-  for (int base = 0; base < nU; base += 32) {
-    const int u = base + lane;
-    const unsigned m = u < nU ? tmpM[u] : 0u;
-    const bool keep = __popc(m) >= 2;
-    const unsigned kb = __ballot_sync(kAllLanes, keep);
-    if (keep) s_list[nS + __popc(kb & ((1u << lane) - 1u))] = (tmpU[u] << 16) | (int)m;
-    nS += __popc(kb);
-  }
-  __syncwarp();
-  return nS;
-}
-
 template <int D_H>
 __global__ void __launch_bounds__(kShThreads, 2)
     k_attn_shared(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                  const __nv_bfloat16* __restrict__ q, const int32_t* __restrict__ idx,
+                  const __nv_bfloat16* __restrict__ q, const int* __restrict__ tile_list,
+                  const unsigned long long* __restrict__ tile_priv,
                   const __nv_bfloat16* __restrict__ part_o,
                   const float* __restrict__ part_lse, __nv_bfloat16* __restrict__ o,
                   float* __restrict__ lse, int64_t N, int64_t q0, int64_t q1, int H_q, int G,
@@ -198,11 +167,11 @@ __global__ void __launch_bounds__(kShThreads, 2)
   const int rows = kTileQ * G;                       // 16 G <= 128 rows in use
 
   if (warp == 0) {
-    int* tmpU = reinterpret_cast<int*>(smem + L::kOffRing);
-    unsigned* tmpM = reinterpret_cast<unsigned*>(smem + L::kOffRing + kMaxKeys * 4);
-    const int nS = with_epl(kk, [&](auto e) {
-      return shared_blocks<decltype(e)::value>(idx, r, i0, q1, N, kk, tmpU, tmpM, s_list, s_priv);
-    });
+    // the tile's shared blocks (block << 16 | query mask) and its queries' private slots
+    const int* lst = tile_list + bid * (kMaxShared + 1);
+    const int nS = __ldg(lst);
+    for (int x = lane; x < nS; x += 32) s_list[x] = __ldg(lst + 1 + x);
+    if (lane < kTileQ) s_priv[lane] = __ldg(tile_priv + bid * kTileQ + lane);
     if (lane == 0) {
       *s_nS = nS;
       for (int s = 0; s < kRing; ++s) {
@@ -567,7 +536,8 @@ __global__ void __launch_bounds__(kShThreads, 2)
 
 template <int D_H>
 static cudaError_t launch_shared_t(const CUtensorMap& tk, const CUtensorMap& tv, const void* q,
-                                   const int32_t* idx, const void* part_o,
+                                   const int* tile_list, const unsigned long long* tile_priv,
+                                   const void* part_o,
                                    const float* part_lse, void* o, float* lse, int64_t N,
                                    int64_t q0, int64_t q1, int H_q, int H_kv, int kk,
                                    cudaStream_t st) {
@@ -578,20 +548,21 @@ static cudaError_t launch_shared_t(const CUtensorMap& tk, const CUtensorMap& tv,
   const int64_t ntiles = (q1 - q0 + kTileQ - 1) / kTileQ;
   const float scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D_H));
   kern<<<(unsigned)(ntiles * H_kv), kShThreads, L::kAlloc, st>>>(
-      tk, tv, static_cast<const __nv_bfloat16*>(q), idx,
+      tk, tv, static_cast<const __nv_bfloat16*>(q), tile_list, tile_priv,
       static_cast<const __nv_bfloat16*>(part_o), part_lse, static_cast<__nv_bfloat16*>(o), lse, N,
       q0, q1, H_q, H_q / H_kv, kk, ntiles, scale_log2);
   return cudaGetLastError();
 }
 
 cudaError_t launch_attn_shared(const CUtensorMap& tk, const CUtensorMap& tv, const void* q,
-                               const int32_t* idx, const void* part_o,
+                               const int* tile_list, const unsigned long long* tile_priv,
+                               const void* part_o,
                                const float* part_lse, void* o, float* lse, int64_t N, int64_t q0,
                                int64_t q1, int H_q, int H_kv, int d_h, int kk, cudaStream_t st) {
   if (d_h == 128)
-    return launch_shared_t<128>(tk, tv, q, idx, part_o, part_lse, o, lse, N, q0, q1, H_q,
+    return launch_shared_t<128>(tk, tv, q, tile_list, tile_priv, part_o, part_lse, o, lse, N, q0, q1, H_q,
                                 H_kv, kk, st);
-  return launch_shared_t<64>(tk, tv, q, idx, part_o, part_lse, o, lse, N, q0, q1, H_q,
+  return launch_shared_t<64>(tk, tv, q, tile_list, tile_priv, part_o, part_lse, o, lse, N, q0, q1, H_q,
                              H_kv, kk, st);
 }
 

@@ -34,13 +34,15 @@ cudaError_t launch_sparse_attn_fwd(const void* q, const void* k, const void* v, 
 cudaError_t read_reset_shared_status(unsigned* out);
 cudaError_t read_reset_kvo_status(unsigned* out);
 cudaError_t launch_attn_shared(const CUtensorMap& tk, const CUtensorMap& tv, const void* q,
-                               const int32_t* idx, const void* part_o,
+                               const int* tile_list, const unsigned long long* tile_priv,
+                               const void* part_o,
                                const float* part_lse, void* o, float* lse, int64_t N, int64_t q0,
                                int64_t q1, int H_q, int H_kv, int d_h, int kk, cudaStream_t st);
 
 cudaError_t launch_attn_plan(const int32_t* idx, int64_t N, int H_kv, int kk, int64_t q0,
                              int64_t q1, int64_t nblk, int pass, int* count, const int* offset,
-                             int* cursor, int* entries, cudaStream_t st);
+                             int* cursor, int* entries, int* tile_list,
+                             unsigned long long* tile_priv, cudaStream_t st);
 cudaError_t launch_attn_scan(const int* count, int* offset, int* tile_off, int* cursor, int nb,
                              int ept, cudaStream_t st);
 cudaError_t launch_attn_kvouter(const void* q, const void* k, const void* v, const int* entries,
