@@ -110,8 +110,11 @@ cudaError_t launch_sparse_attn_fwd(const void* q, const void* k, const void* v, 
                                    void* o, float* lse, int64_t N, int H_q, int H_kv, int d_h,
                                    int kk, void* ws, cudaStream_t stream) {
   const AttnWs w = attn_layout(N, H_q, H_kv, d_h, kk);
-  CUtensorMap tk, tv;
-  cudaError_t e = make_tma_3d_bf16(&tk, k, (uint64_t)d_h, (uint64_t)H_kv, (uint64_t)N, 64, 1, 32, 128);
+  const int G = H_q / H_kv;
+  CUtensorMap tq, tk, tv;
+  cudaError_t e = make_tma_3d_bf16(&tq, q, (uint64_t)d_h, (uint64_t)H_q, (uint64_t)N, 64, G, kTileQ, 128);
+  if (e != cudaSuccess) return e;
+  e = make_tma_3d_bf16(&tk, k, (uint64_t)d_h, (uint64_t)H_kv, (uint64_t)N, 64, 1, 32, 128);
   if (e != cudaSuccess) return e;
   e = make_tma_3d_bf16(&tv, v, (uint64_t)d_h, (uint64_t)H_kv, (uint64_t)N, 64, 1, 32, 128);
   if (e != cudaSuccess) return e;
@@ -119,7 +122,6 @@ cudaError_t launch_sparse_attn_fwd(const void* q, const void* k, const void* v, 
   if (cudaGetDevice(&dev) == cudaSuccess)
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int64_t nblk = (N + kBlock - 1) / kBlock;
-  const int G = H_q / H_kv;
 
   // one chunk: everything on the caller's stream
   cudaStream_t side = stream;
@@ -162,7 +164,7 @@ cudaError_t launch_sparse_attn_fwd(const void* q, const void* k, const void* v, 
       if ((e = cudaEventRecord(ev.ready[s], side)) != cudaSuccess) return e;
       if ((e = cudaStreamWaitEvent(stream, ev.ready[s], 0)) != cudaSuccess) return e;
     }
-    if ((e = launch_attn_shared(tk, tv, q, tile_list, tile_priv, part_o, part_lse, o, lse, N, q0, q1, H_q,
+    if ((e = launch_attn_shared(tq, tk, tv, q, tile_list, tile_priv, part_o, part_lse, o, lse, N, q0, q1, H_q,
                                 H_kv, d_h, kk, stream)) != cudaSuccess) return e;
     if (w.sets == 2 && (e = cudaEventRecord(ev.freed[s], stream)) != cudaSuccess) return e;
   }

@@ -3,7 +3,7 @@
 // tile selected, processed once for the tile on the 5th-generation tensor cores.
 //
 // One CTA = one tile (16 consecutive queries of KV group r).  Its 16*G <= 128 (query, head)
-// rows are the M side of every UMMA:
+// rows are the M side of every UMMA; they arrive by TMA (a 3-D map over [N, H_q, d_h]):
 //   warp 0   loads the tile's shared blocks (recorded by the plan pass), then streams them
 //            as 32-token half blocks (K and V, 3-D tensor maps over [N, H_kv, d_h], 128-byte
 //            swizzle) through a 3-stage TMA ring;
@@ -110,12 +110,6 @@ struct ShSmem {
 __device__ __forceinline__ void tmem_st_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void fence_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
 __device__ __forceinline__ uint64_t desc_mn_sw128(uint32_t a, uint32_t lbo, uint32_t sbo) {
   return (uint64_t)((a & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
          ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
@@ -135,7 +129,8 @@ __device__ __forceinline__ float ldg_nc_f32(const float* p) {
 
 template <int D_H>
 __global__ void __launch_bounds__(kShThreads, 2)
-    k_attn_shared(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+    k_attn_shared(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v,
                   const __nv_bfloat16* __restrict__ q, const int* __restrict__ tile_list,
                   const unsigned long long* __restrict__ tile_priv,
                   const __nv_bfloat16* __restrict__ part_o,
@@ -187,26 +182,13 @@ __global__ void __launch_bounds__(kShThreads, 2)
         mbar_init(p_free(b), 1);
       }
       mbar_init(o_done, 1);
-      mbar_init(q_ready, 4);
+      mbar_init(q_ready, 1);
       mbar_init(done, 1);
       fence_barrier_init();
     }
   } else if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), L::kTmemCols);
     tc_fence_before();
-  } else {
-    // softmax warps: gather the tile's Q rows (row R = query w * G + head h) into SW128 halves
-    constexpr int kChunks = D_H / 8;
-    for (int x = threadIdx.x - 64; x < rows * kChunks; x += 128) {
-      const int R = x / kChunks, c = x - R * kChunks;
-      const int w = R / G;
-      const int64_t i = i0 + w;
-      if (i >= q1) continue;
-      const uint32_t off = (c >> 3) * L::kQHalf + R * 128 + (((c & 7) ^ (R & 7)) << 4);
-      cp_async16(sb + L::kOffQ + off, q + (i * H_q + (int64_t)r * G + (R - w * G)) * D_H + c * 8);
-    }
-    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
-    fence_async_smem();
   }
   __syncthreads();
   tc_fence_after();
@@ -217,6 +199,13 @@ __global__ void __launch_bounds__(kShThreads, 2)
   if (warp == 0) {
     // ------------------------------------------------------------------ producer
     if (lane == 0) {
+      // the tile's Q rows (row R = query w * G + head h): one box of G heads x 16 queries per
+      // 64-dim half, 128-byte swizzle
+      prefetch_tensormap(&tm_q);
+      mbar_expect_tx(q_ready, (uint32_t)(L::kHalves * rows * 128));
+#pragma unroll
+      for (int bx = 0; bx < L::kHalves; ++bx)
+        tma_load_3d(sb + L::kOffQ + bx * L::kQHalf, &tm_q, q_ready, 64 * bx, r * G, (int)i0);
       prefetch_tensormap(&tm_k);
       prefetch_tensormap(&tm_v);
       int last[kRing];
@@ -236,6 +225,7 @@ __global__ void __launch_bounds__(kShThreads, 2)
       }
       for (int s = 0; s < kRing; ++s)
         if (last[s] >= 0) mbar_wait(kv_full(s), last[s] & 1, &g_shared_status);
+      mbar_wait(q_ready, 0, &g_shared_status);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
@@ -285,8 +275,6 @@ __global__ void __launch_bounds__(kShThreads, 2)
     const int64_t i = i0 + w;
     const bool valid = R < rows && i < q1;
     const uint32_t lanes = (uint32_t)(32 * qd) << 16;
-    __syncwarp();
-    if (lane == 0) mbar_arrive(q_ready);
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
     for (int hb = 0; hb < nH && ok; ++hb) {
@@ -535,7 +523,8 @@ __global__ void __launch_bounds__(kShThreads, 2)
 }  // namespace
 
 template <int D_H>
-static cudaError_t launch_shared_t(const CUtensorMap& tk, const CUtensorMap& tv, const void* q,
+static cudaError_t launch_shared_t(const CUtensorMap& tq, const CUtensorMap& tk,
+                                   const CUtensorMap& tv, const void* q,
                                    const int* tile_list, const unsigned long long* tile_priv,
                                    const void* part_o,
                                    const float* part_lse, void* o, float* lse, int64_t N,
@@ -548,21 +537,22 @@ static cudaError_t launch_shared_t(const CUtensorMap& tk, const CUtensorMap& tv,
   const int64_t ntiles = (q1 - q0 + kTileQ - 1) / kTileQ;
   const float scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D_H));
   kern<<<(unsigned)(ntiles * H_kv), kShThreads, L::kAlloc, st>>>(
-      tk, tv, static_cast<const __nv_bfloat16*>(q), tile_list, tile_priv,
+      tq, tk, tv, static_cast<const __nv_bfloat16*>(q), tile_list, tile_priv,
       static_cast<const __nv_bfloat16*>(part_o), part_lse, static_cast<__nv_bfloat16*>(o), lse, N,
       q0, q1, H_q, H_q / H_kv, kk, ntiles, scale_log2);
   return cudaGetLastError();
 }
 
-cudaError_t launch_attn_shared(const CUtensorMap& tk, const CUtensorMap& tv, const void* q,
+cudaError_t launch_attn_shared(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                               const void* q,
                                const int* tile_list, const unsigned long long* tile_priv,
                                const void* part_o,
                                const float* part_lse, void* o, float* lse, int64_t N, int64_t q0,
                                int64_t q1, int H_q, int H_kv, int d_h, int kk, cudaStream_t st) {
   if (d_h == 128)
-    return launch_shared_t<128>(tk, tv, q, tile_list, tile_priv, part_o, part_lse, o, lse, N, q0, q1, H_q,
+    return launch_shared_t<128>(tq, tk, tv, q, tile_list, tile_priv, part_o, part_lse, o, lse, N, q0, q1, H_q,
                                 H_kv, kk, st);
-  return launch_shared_t<64>(tk, tv, q, tile_list, tile_priv, part_o, part_lse, o, lse, N, q0, q1, H_q,
+  return launch_shared_t<64>(tq, tk, tv, q, tile_list, tile_priv, part_o, part_lse, o, lse, N, q0, q1, H_q,
                              H_kv, kk, st);
 }
 

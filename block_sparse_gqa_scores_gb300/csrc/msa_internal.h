@@ -33,7 +33,8 @@ cudaError_t launch_sparse_attn_fwd(const void* q, const void* k, const void* v, 
                                    int kk, void* ws, cudaStream_t stream);
 cudaError_t read_reset_shared_status(unsigned* out);
 cudaError_t read_reset_kvo_status(unsigned* out);
-cudaError_t launch_attn_shared(const CUtensorMap& tk, const CUtensorMap& tv, const void* q,
+cudaError_t launch_attn_shared(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                               const void* q,
                                const int* tile_list, const unsigned long long* tile_priv,
                                const void* part_o,
                                const float* part_lse, void* o, float* lse, int64_t N, int64_t q0,
