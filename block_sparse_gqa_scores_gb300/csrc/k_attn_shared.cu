@@ -6,10 +6,10 @@
 // rows are the M side of every UMMA; they arrive by TMA (a 3-D map over [N, H_q, d_h]):
 //   warp 0   loads the tile's shared blocks (recorded by the plan pass), then streams them
 //            as 32-token half blocks (K and V, 3-D tensor maps over [N, H_kv, d_h], 128-byte
-//            swizzle) through a 3-stage TMA ring;
-//   warp 1   allocates TMEM and issues  S[buf] = Q K^T  (M=128, N=32) and  O += P V  (M=128,
-//            N=d_h, P read from TMEM, V as an MN-major operand); S and P are double-buffered
-//            so the next half block's QK^T runs while the softmax of this one is computed;
+//            swizzle) through a 4-stage TMA ring;
+//   warp 1   allocates TMEM and issues  S[b] = Q K^T  (M=128, N=32) and  O += P V  (M=128,
+//            N=d_h, P read from TMEM, V as an MN-major operand); S is triple- and P
+//            double-buffered, so QK^T runs two half blocks ahead of the softmax;
 //   warps 2-5 own one row each (TMEM lane): they load Q, read S rows, mask queries that did not
 //            select the block and keys after the query, and write P (bf16) back to TMEM.
 // Online softmax with a lazily moved reference max: a row's reference m moves only when a block
@@ -31,7 +31,8 @@ namespace {
 
 __device__ unsigned g_shared_status = 0;
 
-constexpr int kRing = 3;                 // half-block stages
+constexpr int kRing = 4;                 // half-block stages
+constexpr int kSBufs = 3;                // S buffers in TMEM: QK^T runs two half blocks ahead
 constexpr int kHalfTok = 32;             // tokens per stage
 constexpr int kShThreads = 192;          // producer, MMA, 4 softmax/epilogue warps
 
@@ -46,17 +47,18 @@ struct ShSmem {
   static constexpr int kOffRing = kOffQ + kHalves * kQHalf;
   static constexpr int kOffList = kOffRing + kRing * kStage;
   static constexpr int kOffBar = kOffList + kMaxShared * 4;
-  // kv_full[kRing], kv_empty[kRing], s_full[2], s_free[2], p_full[2], p_free[2], o_done,
+  // kv_full[kRing], kv_empty[kRing], s_full[kSBufs], s_free[kSBufs], p_full[2], p_free[2],
   // q_ready, done
-  static constexpr int kNumBars = 2 * kRing + 11;
+  static constexpr int kNumBars = 2 * kRing + 2 * kSBufs + 6;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kOffPriv = kOffMisc + 16;    // per query: its private slots (bit t)
   static constexpr int kBytes = kOffPriv + kTileQ * 8;
   static constexpr int kAlloc = kBytes + 1024;
-  // TMEM columns: S[0] 0..31, S[1] 32..63 (fp32); P[0] 64..79, P[1] 80..95 (bf16 pairs);
-  // O 128..128+d_h (fp32)
+  // TMEM columns: S[b] 32b..32b+31 for b < 3 (fp32); P[0] 96..111, P[1] 112..127 (bf16
+  // pairs); O 128..128+d_h (fp32)
   static constexpr uint32_t kTmemCols = 256;
-  static constexpr uint32_t kColP = 64, kColO = 128;
+  static constexpr uint32_t kColP = 32 * kSBufs, kColO = 128;
+  static_assert(kColP + 32 <= kColO, "S and P buffers below O");
   // epilogue, over Q / ring once every MMA has completed: the rows' shared-block O (fp32,
   // already weighted), per-row max and 1/sum of the merge, per query its private partials
   static constexpr int kOsStride = D_H + 4;          // floats; 16-byte pad against conflicts
@@ -149,11 +151,11 @@ __global__ void __launch_bounds__(kShThreads, 2)
   auto kv_full = [&](int s) { return bar + 8u * s; };
   auto kv_empty = [&](int s) { return bar + 8u * (kRing + s); };
   auto s_full = [&](int b) { return bar + 8u * (2 * kRing + b); };
-  auto s_free = [&](int b) { return bar + 8u * (2 * kRing + 2 + b); };
-  auto p_full = [&](int b) { return bar + 8u * (2 * kRing + 4 + b); };
-  auto p_free = [&](int b) { return bar + 8u * (2 * kRing + 6 + b); };
-  const uint32_t o_done = bar + 8u * (2 * kRing + 8);
-  const uint32_t q_ready = bar + 8u * (2 * kRing + 9), done = bar + 8u * (2 * kRing + 10);
+  auto s_free = [&](int b) { return bar + 8u * (2 * kRing + kSBufs + b); };
+  auto p_full = [&](int b) { return bar + 8u * (2 * kRing + 2 * kSBufs + b); };
+  auto p_free = [&](int b) { return bar + 8u * (2 * kRing + 2 * kSBufs + 2 + b); };
+  const uint32_t q_ready = bar + 8u * (2 * kRing + 2 * kSBufs + 4);
+  const uint32_t done = bar + 8u * (2 * kRing + 2 * kSBufs + 5);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t bid = blockIdx.x;
@@ -173,7 +175,7 @@ __global__ void __launch_bounds__(kShThreads, 2)
         mbar_init(kv_full(s), 1);
         mbar_init(kv_empty(s), 1);
       }
-      for (int b = 0; b < 2; ++b) {
+      for (int b = 0; b < kSBufs; ++b) {
         mbar_init(s_full(b), 1);
         mbar_init(s_free(b), 4);
       }
@@ -181,7 +183,6 @@ __global__ void __launch_bounds__(kShThreads, 2)
         mbar_init(p_full(b), 4);
         mbar_init(p_free(b), 1);
       }
-      mbar_init(o_done, 1);
       mbar_init(q_ready, 1);
       mbar_init(done, 1);
       fence_barrier_init();
@@ -234,9 +235,9 @@ __global__ void __launch_bounds__(kShThreads, 2)
       constexpr uint32_t idesc_o = umma_idesc_bf16(128, D_H) | (1u << 16);   // B MN-major
       bool ok = mbar_wait(q_ready, 0, &g_shared_status);
       auto issue_s = [&](int hb) -> bool {
-        const int s = hb % kRing, b = hb & 1;
+        const int s = hb % kRing, b = hb % kSBufs;
         if (!mbar_wait(kv_full(s), (hb / kRing) & 1, &g_shared_status)) return false;
-        if (!mbar_wait(s_free(b), ((hb >> 1) & 1) ^ 1, &g_shared_status)) return false;
+        if (!mbar_wait(s_free(b), ((hb / kSBufs) & 1) ^ 1, &g_shared_status)) return false;
         tc_fence_after();
         const uint32_t kbase = sb + L::kOffRing + s * L::kStage;
 #pragma unroll
@@ -249,8 +250,9 @@ __global__ void __launch_bounds__(kShThreads, 2)
         return true;
       };
       if (ok && nH > 0) ok = issue_s(0);
+      if (ok && nH > 1) ok = issue_s(1);
       for (int hb = 0; hb < nH && ok; ++hb) {
-        if (hb + 1 < nH && !(ok = issue_s(hb + 1))) break;
+        if (hb + 2 < nH && !(ok = issue_s(hb + 2))) break;
         const int pb = hb & 1;
         if (!(ok = mbar_wait(p_full(pb), (hb >> 1) & 1, &g_shared_status))) break;
         tc_fence_after();
@@ -261,7 +263,6 @@ __global__ void __launch_bounds__(kShThreads, 2)
                        desc_mn_sw128(vbase + ks * 2048, L::kBox, 1024), idesc_o,
                        (hb > 0 || ks > 0) ? 1u : 0u);
         umma_commit(p_free(pb));
-        umma_commit(o_done);
         umma_commit(kv_empty(hb % kRing));
       }
       umma_commit(done);
@@ -281,16 +282,16 @@ __global__ void __launch_bounds__(kShThreads, 2)
       const int ent = s_list[hb >> 1];
       const int64_t b = ent >> 16;
       const bool sel = valid && ((ent >> w) & 1);
-      const int buf = hb & 1;
-      if (!(ok = __all_sync(kAllLanes, mbar_wait(s_full(buf), (hb >> 1) & 1, &g_shared_status))))
+      const int buf = hb & 1, sbuf = hb % kSBufs;          // P buffer, S buffer
+      if (!(ok = __all_sync(kAllLanes, mbar_wait(s_full(sbuf), (hb / kSBufs) & 1, &g_shared_status))))
         break;
       tc_fence_after();
       uint32_t sv[32];
-      MSA_TMEM_LD32(tmem + lanes + 32 * buf, sv);
+      MSA_TMEM_LD32(tmem + lanes + 32 * sbuf, sv);
       tmem_ld_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(s_free(buf));
+      if (lane == 0) mbar_arrive(s_free(sbuf));
 
       float alpha = 1.f;
       uint32_t pk[16];
@@ -331,9 +332,13 @@ __global__ void __launch_bounds__(kShThreads, 2)
         break;
       tc_fence_after();
       if (__any_sync(kAllLanes, alpha != 1.f)) {
-        // O itself may be rescaled only once O += P V of half block hb-1 has completed
+        // O itself may be rescaled only once O += P V of half block hb-1 (and so of every
+        // earlier one) has completed: the (hb-1)/2-th phase of P buffer (hb-1)&1's "free"
+        // barrier.  S of this half block was issued after O += P V of hb-3, so no later phase
+        // of that barrier can be pending and the parity is unambiguous.
         if (hb > 0 &&
-            !(ok = __all_sync(kAllLanes, mbar_wait(o_done, (hb - 1) & 1, &g_shared_status))))
+            !(ok = __all_sync(kAllLanes, mbar_wait(p_free((hb - 1) & 1), ((hb - 1) >> 1) & 1,
+                                                   &g_shared_status))))
           break;
         tc_fence_after();
 #pragma unroll
