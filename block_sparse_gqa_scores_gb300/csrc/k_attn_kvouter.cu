@@ -14,8 +14,8 @@
 // A partial covers exactly one block, so no rescaling is needed; the epilogue of the
 // shared-block pass (k_attn_shared.cu) combines a row's partials with its shared-block state in
 // slot order.
-// Q rows, K_b and V_b are gathered with cp.async into 128-byte-swizzled tiles (the canonical
-// K-major / MN-major SW128 layouts).  P reuses Q's shared memory and O reuses S's TMEM
+// Q rows (by TMA, one box per query, at G = 8; by cp.async otherwise), K_b and V_b (cp.async)
+// land in 128-byte-swizzled tiles (the canonical K-major / MN-major SW128 layouts).  P reuses Q's shared memory and O reuses S's TMEM
 // columns, so three CTAs fit on an SM.  The next tile's K_b (if its bucket differs) is loaded
 // as soon as S = Q K^T has completed, and its query rows and V_b once O = P V has completed,
 // so those loads run under the softmax and the epilogue.  Persistent grid; each CTA takes a contiguous range of
@@ -82,7 +82,8 @@ __device__ __forceinline__ float rowmax64(const uint32_t* v) {
 
 template <int D_H>
 __global__ void __launch_bounds__(kThreadsKvo, 3)
-    k_attn_kvouter(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
+    k_attn_kvouter(const __grid_constant__ CUtensorMap tm_q,
+                   const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
                    const __nv_bfloat16* __restrict__ v, const int* __restrict__ entries,
                    const int* __restrict__ offset, const int* __restrict__ tile_off, int nbuckets,
                    int64_t nblk, int64_t N, int64_t q0, int64_t nq, int H_q, int H_kv, int G,
@@ -93,7 +94,7 @@ __global__ void __launch_bounds__(kThreadsKvo, 3)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sb = smem_u32(smem);
-  const uint32_t mma_bar = sb + L::kOffBar;
+  const uint32_t mma_bar = sb + L::kOffBar, q_bar = sb + L::kOffBar + 8;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffMisc);
   int* s_ent = reinterpret_cast<int*>(smem + L::kOffEnt);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -101,6 +102,7 @@ __global__ void __launch_bounds__(kThreadsKvo, 3)
 
   if (tid == 0) {
     mbar_init(mma_bar, 1);
+    mbar_init(q_bar, 1);
     fence_barrier_init();
   }
   if (warp == 0) {
@@ -166,9 +168,24 @@ __global__ void __launch_bounds__(kThreadsKvo, 3)
       }
     }
   };
-  // the stacked query rows of a tile (entry e's G heads are rows e*G .. e*G+G-1)
-  auto gather_q = [&](int bkt, const int* ent, int rows) {
+  // the stacked query rows of a tile (entry e's G heads are rows e*G .. e*G+G-1): at G = 8 an
+  // entry is one 1-KB swizzle atom per 64-dim half, a single TMA box issued by thread 0 and
+  // counted on q_bar; otherwise every thread gathers 16-byte pieces with cp.async
+  auto gather_q = [&](int bkt, const int* ent, int n_ent) {
     const int rb = (int)(bkt / nblk);
+    if (G == 8) {
+      if (tid == 0) {
+        mbar_expect_tx(q_bar, (uint32_t)(n_ent * 8 * 128 * L::kHalves));
+        for (int e = 0; e < n_ent; ++e) {
+          const int i = (int)(q0 + (ent[e] >> 6));
+#pragma unroll
+          for (int bx = 0; bx < L::kHalves; ++bx)
+            tma_load_3d(sb + L::kOffQ + bx * L::kQHalf + e * 1024, &tm_q, q_bar, 64 * bx, rb * 8, i);
+        }
+      }
+      return;
+    }
+    const int rows = n_ent * G;
     for (int x = tid; x < rows * kChunks; x += kThreadsKvo) {
       const int R = x / kChunks, c = x - R * kChunks;
       const int e = R / G, h = R - e * G;
@@ -184,8 +201,9 @@ __global__ void __launch_bounds__(kThreadsKvo, 3)
     load_kv(bucket, true, true);
     if (tid < n_e) s_ent[tid] = __ldg(entries + e0 + tid);
     __syncthreads();
-    gather_q(bucket, s_ent, n_e * G);
+    gather_q(bucket, s_ent, n_e);
   }
+  uint32_t qphase = 0;
   for (int tile = t_beg; tile < t_end && ok; ++tile) {
     const int cur = (tile - t_beg) & 1;
     const int* ent_cur = s_ent + cur * kRowsT;
@@ -194,7 +212,11 @@ __global__ void __launch_bounds__(kThreadsKvo, 3)
     const int rows = n_e * G;
     cp_async_wait_all();                                     // this tile's Q (and K_b, V_b)
     fence_async_smem();
-    __syncthreads();
+    bool qok = true;
+    if (G == 8 && tid == 0) qok = mbar_wait(q_bar, qphase, &g_kvo_status);   // Q by TMA
+    qphase ^= 1u;
+    ok = __syncthreads_and(qok);
+    if (!ok) break;
 
     // ---- S = Q_stack K_b^T
     if (tid == 0) {
@@ -289,7 +311,7 @@ __global__ void __launch_bounds__(kThreadsKvo, 3)
 
     // ---- Q (holding P) and V_b are free once O = P V is done: the next tile's rows, V_b
     if (new_bucket) load_kv(n_bucket, false, true);
-    if (has_next) gather_q(n_bucket, s_ent + (cur ^ 1) * kRowsT, n_ne * G);
+    if (has_next) gather_q(n_bucket, s_ent + (cur ^ 1) * kRowsT, n_ne);
     asm volatile("cp.async.commit_group;" ::: "memory");
 
     // ---- epilogue: normalised partial (bf16) and log2-domain LSE of each row
@@ -345,6 +367,10 @@ cudaError_t launch_attn_kvouter(const void* q, const void* k, const void* v, con
   const int G = H_q / H_kv;
   const float scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)d_h));
   const auto* qq = static_cast<const __nv_bfloat16*>(q);
+  // Q as [N, H_q, d_h]: one box = one query's G heads x 64 dims, 128-byte swizzle
+  CUtensorMap tq;
+  cudaError_t me = make_tma_3d_bf16(&tq, q, (uint64_t)d_h, (uint64_t)H_q, (uint64_t)N, 64, G, 1, 128);
+  if (me != cudaSuccess) return me;
   const auto* kp = static_cast<const __nv_bfloat16*>(k);
   const auto* vv = static_cast<const __nv_bfloat16*>(v);
   auto* po = static_cast<__nv_bfloat16*>(part_o);
@@ -353,7 +379,7 @@ cudaError_t launch_attn_kvouter(const void* q, const void* k, const void* v, con
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          KvoSmem<128>::kAlloc);
     if (e != cudaSuccess) return e;
-    kern<<<grid, kThreadsKvo, KvoSmem<128>::kAlloc, stream>>>(qq, kp, vv, entries, offset, tile_off,
+    kern<<<grid, kThreadsKvo, KvoSmem<128>::kAlloc, stream>>>(tq, qq, kp, vv, entries, offset, tile_off,
                                                              nbuckets, nblk, N, q0, q1 - q0, H_q, H_kv, G,
                                                              kk, kRowsT / G, po, part_lse, scale_log2);
   } else {
@@ -361,7 +387,7 @@ cudaError_t launch_attn_kvouter(const void* q, const void* k, const void* v, con
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          KvoSmem<64>::kAlloc);
     if (e != cudaSuccess) return e;
-    kern<<<grid, kThreadsKvo, KvoSmem<64>::kAlloc, stream>>>(qq, kp, vv, entries, offset, tile_off,
+    kern<<<grid, kThreadsKvo, KvoSmem<64>::kAlloc, stream>>>(tq, qq, kp, vv, entries, offset, tile_off,
                                                             nbuckets, nblk, N, q0, q1 - q0, H_q, H_kv, G,
                                                             kk, kRowsT / G, po, part_lse, scale_log2);
   }
