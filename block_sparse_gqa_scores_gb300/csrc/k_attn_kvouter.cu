@@ -272,13 +272,18 @@ __global__ void __launch_bounds__(kThreadsKvo, 3)
         mx = rowmax64(s) * scale_log2;
       }
       uint32_t pk[32];
+      float l0 = 0.f, l1 = 0.f;
 #pragma unroll
       for (int c = 0; c < 32; ++c) {
-        const float p0 = rv ? ex2(__uint_as_float(s[2 * c]) * scale_log2 - mx) : 0.f;
-        const float p1 = rv ? ex2(__uint_as_float(s[2 * c + 1]) * scale_log2 - mx) : 0.f;
-        l += p0 + p1;
+        float x0, x1;
+        ffma2(x0, x1, __uint_as_float(s[2 * c]), __uint_as_float(s[2 * c + 1]), scale_log2,
+              scale_log2, -mx, -mx);
+        const float p0 = rv ? ex2(x0) : 0.f;
+        const float p1 = rv ? ex2(x1) : 0.f;
+        fadd2(l0, l1, l0, l1, p0, p1);
         pk[c] = pack_bf16x2(p0, p1);
       }
+      l = l0 + l1;
 #pragma unroll
       for (int cc = 0; cc < 8; ++cc) {
         const uint32_t addr = sb + L::kOffP + R * 128 + ((cc ^ (R & 7)) << 4);

@@ -313,15 +313,17 @@ __global__ void __launch_bounds__(kShThreads, 2)
           alpha = ex2(m_ref - bm);
           m_ref = bm;
         }
-        float ps = 0.f;
+        float ps0 = 0.f, ps1 = 0.f;
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
-          const float p0 = ex2(__uint_as_float(sv[2 * c]) * scale_log2 - m_ref);
-          const float p1 = ex2(__uint_as_float(sv[2 * c + 1]) * scale_log2 - m_ref);
-          ps += p0 + p1;
+          float x0, x1;
+          ffma2(x0, x1, __uint_as_float(sv[2 * c]), __uint_as_float(sv[2 * c + 1]), scale_log2,
+                scale_log2, -m_ref, -m_ref);
+          const float p0 = ex2(x0), p1 = ex2(x1);
+          fadd2(ps0, ps1, ps0, ps1, p0, p1);
           pk[c] = pack_bf16x2(p0, p1);
         }
-        l = l * alpha + ps;
+        l = l * alpha + (ps0 + ps1);
       } else {
 #pragma unroll
         for (int c = 0; c < 16; ++c) pk[c] = 0u;
