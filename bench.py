@@ -35,10 +35,11 @@ sys.path.insert(0, ROOT)
 import gen  # noqa: E402
 
 METRIC = ("MSA prefill tokens/s and decode tokens/s at 128K ctx; % of bf16 TC / HBM roofline")
-# kernels per step: the fused index branch (block scores + top-k); attention per 16384-row chunk:
+# kernels per step: the fused index branch (block scores + top-k); attention per 32768-row chunk:
 # plan, scan, plan, block-major pass, shared-block pass with the merge (+ one memset); decode:
 # scores, select, attention, merge
 ATTN_LAUNCHES_PER_CHUNK = 5
+ATTN_CHUNK_ROWS = 32768
 DECODE_LAUNCHES = 4
 KERNEL_FILES = {"index_branch": ["k_score.cu"],
                 "main_branch": ["attn_fwd.cu", "k_attn_shared.cu", "k_attn_kvouter.cu",
@@ -334,7 +335,7 @@ def run_msa(args, world, rank, local):
                        "mean_len": float(np.mean(d["meta"]["lens"])), "k": dcfg.k}
             if d is not None else None,
             "l2": "no explicit flush: each step streams Q (1.07 GB), K/V (134 MB each), the "
-                  "4.4 GB main-branch workspace and the 11.5 GB decode caches, so nothing the "
+                  "8.8 GB main-branch workspace and the 11.5 GB decode caches, so nothing the "
                   "next step reads is still in the 129 MB L2",
             "parallelism": "replicas" if world > 1 else "single",
         },
@@ -349,7 +350,7 @@ def run_msa(args, world, rank, local):
                      "peak_source": "%s (%s)" % (pk["src"], "bf16 sustained" if dom["unit"] ==
                                                  "TFLOP/s" else "HBM copy")},
         "clocks": clk,
-        "gpu_launches": (1 + ATTN_LAUNCHES_PER_CHUNK * (-(-N // 16384)) +
+        "gpu_launches": (1 + ATTN_LAUNCHES_PER_CHUNK * (-(-N // ATTN_CHUNK_ROWS)) +
                          (DECODE_LAUNCHES if d is not None else 0)) * K,
     }
     if not args.no_e2e:

@@ -1,7 +1,7 @@
 // Main branch of prefill («MiniMax-M3：MSA 技术报告速读», section 主分支, eq. O^(h)_i): the
 // launch sequence over query chunks and its workspace.
 //
-// Per chunk of at most 16384 query rows:
+// Per chunk of at most 32768 query rows:
 //   plan (count) -> scan -> plan (scatter)   bucket the private selections (attn_tile.cuh) and
 //                                            record each tile's shared blocks
 //   k_attn_kvouter                           block-major tcgen05 pass over private selections
@@ -26,7 +26,9 @@ namespace {
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-constexpr int64_t kChunkRows = 16384;     // query rows per pass (bounds the workspace)
+// query rows per pass: bounds the workspace; larger chunks fill the (group, block) buckets of
+// the block-major pass better (32768 rows: 9.59 ms at 128K against 10.01 ms with 16384)
+constexpr int64_t kChunkRows = 32768;
 constexpr int kKvoCtasPerSm = 3;         // block-major pass: resident CTAs per SM (shared memory)
 
 struct AttnWs {

@@ -500,8 +500,8 @@ __global__ void __launch_bounds__(kShThreads, 2)
                 for (int k2 = 0; k2 < 4; ++k2) {
                   const float2 f =
                       __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wd[k2]));
-                  acc[c][2 * k2] += wt * f.x;
-                  acc[c][2 * k2 + 1] += wt * f.y;
+                  ffma2(acc[c][2 * k2], acc[c][2 * k2 + 1], wt, wt, f.x, f.y, acc[c][2 * k2],
+                        acc[c][2 * k2 + 1]);
                 }
               }
         }
