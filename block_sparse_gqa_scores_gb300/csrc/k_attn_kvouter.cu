@@ -2,8 +2,8 @@
 // section 主分支 eq. O^(h)_i; the kernel section's organisation in which a selected KV block
 // gathers the queries that chose it and stacks them to fill tensor-core MMAs).
 //
-// Input: the private selections of a query chunk -- (query, slot) pairs whose block no other
-// query of the same 16-query tile selected -- bucketed by (group r, block b).  A work tile is up
+// Input: the private selections of a query chunk -- (query, slot) pairs whose block fewer than
+// kSharedMin queries of the same 16-query tile selected -- bucketed by (group r, block b).  A work tile is up
 // to 128/G entries of one bucket; their G heads stack into the 128 rows of one UMMA tile:
 //   S = Q_stack [128 x d_h] . K_b^T [d_h x 64]       tcgen05, bf16 -> fp32 in TMEM
 //   row-wise softmax over the block's visible keys   one thread per row (TMEM lane)

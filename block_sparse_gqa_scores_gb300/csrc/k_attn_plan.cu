@@ -3,7 +3,8 @@
 // updates of results).
 //
 //   k_attn_plan (pass 0)  per 16-query tile: count each private selection in its (group, block)
-//                         bucket (a block that only one of the tile's queries selected)
+//                         bucket (a block that fewer than kSharedMin of the tile's queries
+//                         selected)
 //   k_attn_scan           exclusive scans: entry offsets and work-tile offsets per bucket
 //   k_attn_plan (pass 1)  scatter private selections into their buckets, and record per tile its
 //                         shared blocks (block << 16 | query mask) and per query its private
@@ -41,7 +42,7 @@ __device__ __forceinline__ void plan_tile(const int32_t* __restrict__ idx, int r
     for (int base = 0; base < nU; base += 32) {
       const int u = base + lane;
       const unsigned m = u < nU ? s_mask[u] : 0u;
-      const bool keep = __popc(m) >= 2;
+      const bool keep = __popc(m) >= kSharedMin;
       const unsigned kb = __ballot_sync(kAllLanes, keep);
       if (keep) lst[1 + nS + __popc(kb & ((1u << lane) - 1u))] = (s_U[u] << 16) | (int)m;
       nS += __popc(kb);
@@ -49,7 +50,7 @@ __device__ __forceinline__ void plan_tile(const int32_t* __restrict__ idx, int r
     if (lane == 0) lst[0] = nS;
 #pragma unroll
     for (int j = 0; j < EPL; ++j)
-      if (x[j] != INT_MAX && __popc(s_mask[rank[j]]) == 1)
+      if (x[j] != INT_MAX && __popc(s_mask[rank[j]]) < kSharedMin)
         atomicOr(&s_pm[TileKeys::query(x[j])], 1ull << TileKeys::slot(x[j]));
     __syncwarp();
     if (lane < kTileQ) tile_priv[tix * kTileQ + lane] = s_pm[lane];
@@ -57,7 +58,7 @@ __device__ __forceinline__ void plan_tile(const int32_t* __restrict__ idx, int r
 #pragma unroll
   for (int j = 0; j < EPL; ++j) {
     const int key = x[j];
-    if (key == INT_MAX || __popc(s_mask[rank[j]]) != 1) continue;
+    if (key == INT_MAX || __popc(s_mask[rank[j]]) >= kSharedMin) continue;
     const int b = TileKeys::block(key), w = TileKeys::query(key), t = TileKeys::slot(key);
     const int64_t bucket = (int64_t)r * nblk + b;
     if (pass == 0) {

@@ -1,6 +1,6 @@
 // Shared-block pass of the sparse main branch («MiniMax-M3：MSA 技术报告速读», section 主分支,
-// eq. O^(h)_i; LSE from section Kernel): the KV blocks that two or more queries of a 16-query
-// tile selected, processed once for the tile on the 5th-generation tensor cores.
+// eq. O^(h)_i; LSE from section Kernel): the KV blocks that at least kSharedMin (3) queries of a
+// 16-query tile selected, processed once for the tile on the 5th-generation tensor cores.
 //
 // One CTA = one tile (16 consecutive queries of KV group r).  Its 16*G <= 128 (query, head)
 // rows are the M side of every UMMA; they arrive by TMA (a 3-D map over [N, H_q, d_h]):
