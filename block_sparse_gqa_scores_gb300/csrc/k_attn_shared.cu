@@ -34,7 +34,7 @@ __device__ unsigned g_shared_status = 0;
 constexpr int kRing = 4;                 // half-block stages
 constexpr int kSBufs = 3;                // S buffers in TMEM: QK^T runs two half blocks ahead
 constexpr int kHalfTok = 32;             // tokens per stage
-constexpr int kShThreads = 192;          // producer, MMA, 4 softmax/epilogue warps
+constexpr int kShThreads = 320;          // producer, MMA, 8 softmax/epilogue warps (2 per quarter)
 
 template <int D_H>
 struct ShSmem {
@@ -52,7 +52,12 @@ struct ShSmem {
   static constexpr int kNumBars = 2 * kRing + 2 * kSBufs + 6;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kOffPriv = kOffMisc + 16;    // per query: its private slots (bit t)
-  static constexpr int kBytes = kOffPriv + kTileQ * 8;
+  // the two softmax warps of a lane quarter exchange per-row values: half-block maxima
+  // (double-buffered by half-block parity), the halves of the row sum, the O weight
+  static constexpr int kOffXm = kOffPriv + kTileQ * 8;
+  static constexpr int kOffLh = kOffXm + 2 * 2 * 128 * 4;
+  static constexpr int kOffCo = kOffLh + 2 * 128 * 4;
+  static constexpr int kBytes = kOffCo + 128 * 4;
   static constexpr int kAlloc = kBytes + 1024;
   // TMEM columns: S[b] 32b..32b+31 for b < 3 (fp32); P[0] 96..111, P[1] 112..127 (bf16
   // pairs); O 128..128+d_h (fp32)
@@ -81,6 +86,34 @@ struct ShSmem {
         "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),           \
         "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])            \
       : "r"(taddr))
+
+#define MSA_TMEM_LD16(taddr, r)                                                                 \
+  asm volatile(                                                                                 \
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "                                                 \
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"                         \
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),     \
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), \
+        "=r"(r[14]), "=r"(r[15])                                                                \
+      : "r"(taddr))
+
+#define MSA_TMEM_ST8(taddr, r)                                                                  \
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"( \
+                   taddr),                                                                      \
+               "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]),     \
+               "r"(r[7])                                                                        \
+               : "memory")
+
+#define MSA_TMEM_ST32(taddr, r)                                                                 \
+  asm volatile(                                                                                 \
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "                                           \
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"                                \
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),         \
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),   \
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),         \
+      "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),       \
+      "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),       \
+      "r"(r[29]), "r"(r[30]), "r"(r[31])                                                        \
+      : "memory")
 
 #define MSA_TMEM_ST16(taddr, r)                                                                 \
   asm volatile(                                                                                 \
@@ -115,6 +148,22 @@ __device__ __forceinline__ void tmem_st_wait() {
 __device__ __forceinline__ uint64_t desc_mn_sw128(uint32_t a, uint32_t lbo, uint32_t sbo) {
   return (uint64_t)((a & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
          ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+// Named barrier of the two softmax warps of one TMEM lane quarter (64 threads); the reducing
+// form returns the AND of every thread's flag, so both warps take the same branch after it.
+__device__ __forceinline__ bool pair_and(int id, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, %2, 64, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)v), "r"(id)
+      : "memory");
+  return r != 0;
+}
+__device__ __forceinline__ void pair_sync(int id) {
+  asm volatile("bar.sync %0, 64;" ::"r"(id) : "memory");
 }
 
 __device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
@@ -177,10 +226,10 @@ __global__ void __launch_bounds__(kShThreads, 2)
       }
       for (int b = 0; b < kSBufs; ++b) {
         mbar_init(s_full(b), 1);
-        mbar_init(s_free(b), 4);
+        mbar_init(s_free(b), 8);
       }
       for (int b = 0; b < 2; ++b) {
-        mbar_init(p_full(b), 4);
+        mbar_init(p_full(b), 8);
         mbar_init(p_free(b), 1);
       }
       mbar_init(q_ready, 1);
@@ -270,43 +319,62 @@ __global__ void __launch_bounds__(kShThreads, 2)
     }
   } else {
     // ------------------------------------------------------ softmax and epilogue
+    // warps 2..9, two per TMEM lane quarter: half ch takes keys [16 ch, 16 ch + 16) of every
+    // half block and columns [ch d_h / 2, (ch + 1) d_h / 2) of O; the pair exchanges row maxima
+    // and sums through shared memory at its own named barrier
     const int qd = warp & 3;                          // TMEM lane quarter
+    const int ch = (warp - 2) >> 2;
+    const int pair = 1 + qd;                          // named barrier id of the quarter's pair
     const int R = 32 * qd + lane;
     const int w = R / G, h = R - (R / G) * G;
     const int64_t i = i0 + w;
     const bool valid = R < rows && i < q1;
     const uint32_t lanes = (uint32_t)(32 * qd) << 16;
-    float m_ref = -INFINITY, l = 0.f;
+    float* s_xm = reinterpret_cast<float*>(smem + L::kOffXm);
+    float* s_lh = reinterpret_cast<float*>(smem + L::kOffLh);
+    float* s_co = reinterpret_cast<float*>(smem + L::kOffCo);
+    float m_ref = -INFINITY, l = 0.f;                 // l: this half's share of the row sum
     bool ok = true;
-    for (int hb = 0; hb < nH && ok; ++hb) {
+    // No warp leaves the loop except at the pair barrier, which both reach every half block:
+    // a failed wait is carried in `ok` to the next one, where both see it.
+    for (int hb = 0; hb < nH; ++hb) {
       const int ent = s_list[hb >> 1];
       const int64_t b = ent >> 16;
       const bool sel = valid && ((ent >> w) & 1);
       const int buf = hb & 1, sbuf = hb % kSBufs;          // P buffer, S buffer
-      if (!(ok = __all_sync(kAllLanes, mbar_wait(s_full(sbuf), (hb / kSBufs) & 1, &g_shared_status))))
-        break;
-      tc_fence_after();
-      uint32_t sv[32];
-      MSA_TMEM_LD32(tmem + lanes + 32 * sbuf, sv);
-      tmem_ld_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(s_free(sbuf));
-
-      float alpha = 1.f;
-      uint32_t pk[16];
-      if (sel) {
-        if (b == (i >> 6)) {                          // local block: keys j <= i only
-          const int lim = (int)(i - (b * kBlock + (hb & 1) * kHalfTok));
+      const bool okw =
+          ok && __all_sync(kAllLanes, mbar_wait(s_full(sbuf), (hb / kSBufs) & 1, &g_shared_status));
+      uint32_t sv[16];
+      float pmx = -INFINITY;
+      if (okw) {
+        tc_fence_after();
+        MSA_TMEM_LD16(tmem + lanes + 32 * sbuf + 16 * ch, sv);
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(s_free(sbuf));
+        if (sel) {
+          if (b == (i >> 6)) {                        // local block: keys j <= i only
+            const int lim = (int)(i - (b * kBlock + (hb & 1) * kHalfTok)) - 16 * ch;
 #pragma unroll
-          for (int c = 0; c < 32; ++c)
-            if (c > lim) sv[c] = __float_as_uint(-INFINITY);
+            for (int c = 0; c < 16; ++c)
+              if (c > lim) sv[c] = __float_as_uint(-INFINITY);
+          }
+          pmx = fmax3(__uint_as_float(sv[0]), __uint_as_float(sv[1]), __uint_as_float(sv[2]));
+#pragma unroll
+          for (int c = 3; c < 15; c += 2)
+            pmx = fmax3(pmx, __uint_as_float(sv[c]), __uint_as_float(sv[c + 1]));
+          pmx = fmaxf(pmx, __uint_as_float(sv[15]));
         }
-        float bm = fmax3(__uint_as_float(sv[0]), __uint_as_float(sv[1]), __uint_as_float(sv[2]));
-#pragma unroll
-        for (int c = 3; c < 31; c += 2)
-          bm = fmax3(bm, __uint_as_float(sv[c]), __uint_as_float(sv[c + 1]));
-        bm = fmaxf(bm, __uint_as_float(sv[31])) * scale_log2;
+      }
+      s_xm[((hb & 1) * 2 + ch) * 128 + R] = pmx;
+      ok = pair_and(pair, okw);
+      if (!ok) break;
+      float alpha = 1.f;
+      uint32_t pk[8];
+      if (sel) {
+        const float bm =
+            fmaxf(s_xm[(hb & 1) * 256 + R], s_xm[(hb & 1) * 256 + 128 + R]) * scale_log2;
         if (m_ref == -INFINITY) {
           m_ref = bm;                                 // this row's O and l are still zero
         } else if (bm > m_ref + 8.f) {
@@ -315,7 +383,7 @@ __global__ void __launch_bounds__(kShThreads, 2)
         }
         float ps0 = 0.f, ps1 = 0.f;
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
+        for (int c = 0; c < 8; ++c) {
           float x0, x1;
           ffma2(x0, x1, __uint_as_float(sv[2 * c]), __uint_as_float(sv[2 * c + 1]), scale_log2,
                 scale_log2, -m_ref, -m_ref);
@@ -326,42 +394,52 @@ __global__ void __launch_bounds__(kShThreads, 2)
         l = l * alpha + (ps0 + ps1);
       } else {
 #pragma unroll
-        for (int c = 0; c < 16; ++c) pk[c] = 0u;
+        for (int c = 0; c < 8; ++c) pk[c] = 0u;
       }
       // P buffer hb&1 is free once O += P V of half block hb-2 has completed
-      if (hb > 1 &&
-          !(ok = __all_sync(kAllLanes, mbar_wait(p_free(buf), ((hb >> 1) & 1) ^ 1, &g_shared_status))))
-        break;
+      bool okp = true;
+      if (hb > 1)
+        okp = __all_sync(kAllLanes, mbar_wait(p_free(buf), ((hb >> 1) & 1) ^ 1, &g_shared_status));
       tc_fence_after();
-      if (__any_sync(kAllLanes, alpha != 1.f)) {
+      if (okp && __any_sync(kAllLanes, alpha != 1.f)) {
         // O itself may be rescaled only once O += P V of half block hb-1 (and so of every
         // earlier one) has completed: the (hb-1)/2-th phase of P buffer (hb-1)&1's "free"
         // barrier.  S of this half block was issued after O += P V of hb-3, so no later phase
-        // of that barrier can be pending and the parity is unambiguous.
-        if (hb > 0 &&
-            !(ok = __all_sync(kAllLanes, mbar_wait(p_free((hb - 1) & 1), ((hb - 1) >> 1) & 1,
-                                                   &g_shared_status))))
-          break;
+        // of that barrier can be pending and the parity is unambiguous.  Both warps of the
+        // pair decide alike (same rows, same maxima) and each rescales its half of O.
+        if (hb > 0)
+          okp = __all_sync(kAllLanes, mbar_wait(p_free((hb - 1) & 1), ((hb - 1) >> 1) & 1,
+                                                &g_shared_status));
         tc_fence_after();
-#pragma unroll
-        for (int part = 0; part < D_H / 64; ++part) {
-          uint32_t ov[64];
-          MSA_TMEM_LD64(tmem + lanes + L::kColO + 64 * part, ov);
+        if (okp) {
+          uint32_t ov[D_H / 2];
+          if constexpr (D_H == 128) {
+            MSA_TMEM_LD64(tmem + lanes + L::kColO + 64 * ch, ov);
+          } else {
+            MSA_TMEM_LD32(tmem + lanes + L::kColO + 32 * ch, ov);
+          }
           tmem_ld_wait();
 #pragma unroll
-          for (int c = 0; c < 64; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * alpha);
-          MSA_TMEM_ST64(tmem + lanes + L::kColO + 64 * part, ov);
+          for (int c = 0; c < D_H / 2; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * alpha);
+          if constexpr (D_H == 128) {
+            MSA_TMEM_ST64(tmem + lanes + L::kColO + 64 * ch, ov);
+          } else {
+            MSA_TMEM_ST32(tmem + lanes + L::kColO + 32 * ch, ov);
+          }
         }
       }
-      MSA_TMEM_ST16(tmem + lanes + L::kColP + 16 * buf, pk);
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(p_full(buf));
+      if (okp) {
+        MSA_TMEM_ST8(tmem + lanes + L::kColP + 16 * buf + 8 * ch, pk);
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(p_full(buf));
+      }
+      ok = okp;
     }
     // ---- epilogue: shared-block state + private partials of each row, in slot order
     // the query's private partials start toward L2 now, while the last MMAs drain
-    if (valid && h == 0) {
+    if (ch == 0 && valid && h == 0) {
       const unsigned long long pv = s_priv[w];
       const int64_t rp = ((int64_t)r * (q1 - q0) + (i - q0)) * kk;
       for (int t = 0; t < kk; ++t)
@@ -369,64 +447,76 @@ __global__ void __launch_bounds__(kShThreads, 2)
       const float* lp = part_lse + rp * G;
       for (int x = 0; x < kk * G; x += 32) prefetch_l2(lp + x);
     }
-    if (ok) ok = __all_sync(kAllLanes, mbar_wait(done, 0, &g_shared_status));
+    const bool okd = pair_and(
+        pair, ok && __all_sync(kAllLanes, mbar_wait(done, 0, &g_shared_status)));
     tc_fence_after();
-    const bool have_o = nH > 0 && ok;               // warp-uniform
+    const bool have_o = nH > 0 && okd;               // the same in both warps of the pair
     float* s_os = reinterpret_cast<float*>(smem + L::kOffOs);
     float* s_mx = reinterpret_cast<float*>(smem + L::kOffMx);
     float* s_inv = reinterpret_cast<float*>(smem + L::kOffInv);
     int* s_pos = reinterpret_cast<int*>(smem + L::kOffPos);
     int* s_np = reinterpret_cast<int*>(smem + L::kOffNp);
-    // (a) one thread per row: merge max and sum over the shared state and the private LSEs
-    //     (online, 16 slots at a time); the query's head-0 row lists its private partials, which
-    //     the block-major pass wrote at the row's own slot positions
-    const unsigned long long priv = valid ? s_priv[w] : 0ull;
-    const int64_t row_pos = ((int64_t)r * (q1 - q0) + (i - q0)) * kk;
-    const float lse_s = l > 0.f ? m_ref + __log2f(l) : -INFINITY;
-    float mx = lse_s, wsum = lse_s == -INFINITY ? 0.f : 1.f;
-    int np = 0;
-    for (int t0 = 0; t0 < kk; t0 += 16) {
-      int pos[16];
-      float lv[16];
-#pragma unroll
-      for (int d = 0; d < 16; ++d)
-        pos[d] = (valid && t0 + d < kk && ((priv >> (t0 + d)) & 1ull)) ? (int)(row_pos + t0 + d) : -1;
-#pragma unroll
-      for (int d = 0; d < 16; ++d)
-        lv[d] = pos[d] >= 0 ? __ldg(part_lse + (int64_t)pos[d] * G + h) : -INFINITY;
-      float cm = mx;
-#pragma unroll
-      for (int d = 0; d < 16; ++d) cm = fmaxf(cm, lv[d]);
-      if (cm != -INFINITY) {
-        if (mx != -INFINITY) wsum *= ex2(mx - cm);
-        mx = cm;
+    s_lh[ch * 128 + R] = l;
+    pair_sync(pair);
+    const float lrow = s_lh[R] + s_lh[128 + R];      // the row sum over both halves
+    if (ch == 0) {
+      // (a) one thread per row: merge max and sum over the shared state and the private LSEs
+      //     (online, 16 slots at a time); the query's head-0 row lists its private partials, which
+      //     the block-major pass wrote at the row's own slot positions
+      const unsigned long long priv = valid ? s_priv[w] : 0ull;
+      const int64_t row_pos = ((int64_t)r * (q1 - q0) + (i - q0)) * kk;
+      const float lse_s = lrow > 0.f ? m_ref + __log2f(lrow) : -INFINITY;
+      float mx = lse_s, wsum = lse_s == -INFINITY ? 0.f : 1.f;
+      int np = 0;
+      for (int t0 = 0; t0 < kk; t0 += 16) {
+        int pos[16];
+        float lv[16];
 #pragma unroll
         for (int d = 0; d < 16; ++d)
-          if (pos[d] >= 0) wsum += ex2(lv[d] - mx);
-      }
-      if (valid && h == 0) {
+          pos[d] = (valid && t0 + d < kk && ((priv >> (t0 + d)) & 1ull)) ? (int)(row_pos + t0 + d) : -1;
 #pragma unroll
         for (int d = 0; d < 16; ++d)
-          if (pos[d] >= 0) s_pos[w * kk + np++] = pos[d];
+          lv[d] = pos[d] >= 0 ? __ldg(part_lse + (int64_t)pos[d] * G + h) : -INFINITY;
+        float cm = mx;
+#pragma unroll
+        for (int d = 0; d < 16; ++d) cm = fmaxf(cm, lv[d]);
+        if (cm != -INFINITY) {
+          if (mx != -INFINITY) wsum *= ex2(mx - cm);
+          mx = cm;
+#pragma unroll
+          for (int d = 0; d < 16; ++d)
+            if (pos[d] >= 0) wsum += ex2(lv[d] - mx);
+        }
+        if (valid && h == 0) {
+#pragma unroll
+          for (int d = 0; d < 16; ++d)
+            if (pos[d] >= 0) s_pos[w * kk + np++] = pos[d];
+        }
       }
+      const float inv_w = wsum > 0.f ? 1.f / wsum : 0.f;
+      const float c_o = lrow > 0.f ? ex2(lse_s - mx) * inv_w / lrow : 0.f;
+      if (valid) lse[((int64_t)r * G + h) * N + i] = (mx + __log2f(wsum)) * 0.69314718055994531f;
+      s_mx[R] = mx;
+      s_inv[R] = inv_w;
+      if (valid && h == 0) s_np[w] = np;
+      s_co[R] = c_o;
     }
-    const float inv_w = wsum > 0.f ? 1.f / wsum : 0.f;
-    const float c_o = l > 0.f ? ex2(lse_s - mx) * inv_w / l : 0.f;
-    if (valid) lse[((int64_t)r * G + h) * N + i] = (mx + __log2f(wsum)) * 0.69314718055994531f;
-    s_mx[R] = mx;
-    s_inv[R] = inv_w;
-    if (valid && h == 0) s_np[w] = np;
-    // (b) the shared-block O of the row, weighted, into shared memory
-#pragma unroll
-    for (int part = 0; part < D_H / 64; ++part) {
-      uint32_t ov[64];
+    pair_sync(pair);
+    // (b) this half of the row's shared-block O, weighted, into shared memory
+    {
+      const float c_o = s_co[R];
+      uint32_t ov[D_H / 2];
       if (have_o) {
-        MSA_TMEM_LD64(tmem + lanes + L::kColO + 64 * part, ov);
+        if constexpr (D_H == 128) {
+          MSA_TMEM_LD64(tmem + lanes + L::kColO + 64 * ch, ov);
+        } else {
+          MSA_TMEM_LD32(tmem + lanes + L::kColO + 32 * ch, ov);
+        }
         tmem_ld_wait();
       }
-      float4* dst = reinterpret_cast<float4*>(s_os + R * L::kOsStride + 64 * part);
+      float4* dst = reinterpret_cast<float4*>(s_os + R * L::kOsStride + ch * (D_H / 2));
 #pragma unroll
-      for (int c = 0; c < 16; ++c)
+      for (int c = 0; c < D_H / 8; ++c)
         dst[c] = have_o ? make_float4(__uint_as_float(ov[4 * c]) * c_o,
                                       __uint_as_float(ov[4 * c + 1]) * c_o,
                                       __uint_as_float(ov[4 * c + 2]) * c_o,
@@ -437,10 +527,10 @@ __global__ void __launch_bounds__(kShThreads, 2)
   }
 
   __syncthreads();                                    // (b) of every row is in shared memory
-  // (c) every warp (the producer and MMA warps are idle by now) takes whole queries: a query's
-  //     partial for all G heads is G*d_h contiguous bf16, as is its output row, so lanes split
-  //     it in 16-byte pieces (coalesced) and add the private partials to the staged shared-block
-  //     O in slot order
+  // (c) every warp (the producer and MMA warps are idle by now) takes units of a query: a
+  //     query's partial for all G heads is G*d_h contiguous bf16, as is its output row, split in
+  //     16-byte pieces (coalesced) and in units of at most 64 pieces; lanes add the private
+  //     partials to the staged shared-block O in slot order
   {
     const float* s_os = reinterpret_cast<const float*>(smem + L::kOffOs);
     const float* s_mx = reinterpret_cast<const float*>(smem + L::kOffMx);
@@ -449,22 +539,28 @@ __global__ void __launch_bounds__(kShThreads, 2)
     const int* s_np = reinterpret_cast<const int*>(smem + L::kOffNp);
     {
       const int U = G * D_H / 8;                      // 16-byte pieces per query
-      const int lpq = U < 32 ? U : 32, qpp = 32 / lpq, ipl = U / lpq;
-      const int sub = lane % lpq;
-      const int npass = (kTileQ + qpp - 1) / qpp;
-      const int wslot = (warp + kShThreads / 32 - 2) % (kShThreads / 32);   // warps 2.. first
-      constexpr int kIpl = D_H / 32;                  // most pieces per lane (G <= 8)
+      const int UP = U > 64 ? 64 : U;                 // pieces per unit
+      const int upq = U / UP;                         // units per query (1 or 2)
+      const int lpu = UP < 32 ? UP : 32;              // lanes per unit
+      const int upp = 32 / lpu, ipl = UP / lpu;       // units per pass, pieces per lane
+      const int sub = lane % lpu;
+      const int nunits = kTileQ * upq;
+      const int npass = (nunits + upp - 1) / upp;
+      constexpr int kWarps = kShThreads / 32;
+      const int wslot = (warp + kWarps - 2) % kWarps;  // softmax warps first
+      constexpr int kIpl = 2;                         // most pieces per lane
       constexpr int kNb = 4;                          // partials in flight per lane
-      for (int ps = wslot; ps < npass; ps += kShThreads / 32) {
-        const int wq = ps * qpp + lane / lpq;
-        const bool qv = wq < kTileQ && i0 + wq < q1;
+      for (int ps = wslot; ps < npass; ps += kWarps) {
+        const int unit = ps * upp + lane / lpu;
+        const int wq = unit / upq, uh = unit - wq * upq;
+        const bool qv = unit < nunits && i0 + wq < q1;
         float acc[kIpl][8], pm[kIpl], pi[kIpl];
         int pe[kIpl], ph[kIpl];
 #pragma unroll
         for (int c = 0; c < kIpl; ++c) {
-          pe[c] = 8 * (c * lpq + sub);                // element within the query's G*d_h
+          pe[c] = 8 * (uh * UP + c * lpu + sub);      // element within the query's G*d_h
           ph[c] = pe[c] / D_H;
-          const int RR = min(wq * G + ph[c], 127);
+          const int RR = min(min(wq, kTileQ - 1) * G + ph[c], 127);
           pm[c] = s_mx[RR];
           pi[c] = s_inv[RR];
           const float4* src =
