@@ -237,6 +237,23 @@ def setup(pcfg, dcfg, seed=0):
     return msa, x, bufs, d, dbufs
 
 
+def bench_config(pcfg, dcfg, world):
+    """The workload a bench line measures; both arms report the same object."""
+    return {
+        "workload": "prefill N=%d" % pcfg.N + (" + decode %d seqs L~U[%d,%d]" % (
+            dcfg.S, dcfg.len_lo, dcfg.len_hi) if dcfg is not None else ""),
+        "prefill": {"N": pcfg.N, "H_q": pcfg.H_q, "H_kv": pcfg.H_kv, "d_h": pcfg.d_h,
+                    "d_idx": pcfg.d_idx, "block": 64, "k": pcfg.k,
+                    "hot_blocks": pcfg.hot_blocks, "block_offset_std": pcfg.block_offset_std},
+        "decode": {"S": dcfg.S, "len_lo": dcfg.len_lo, "len_hi": dcfg.len_hi, "k": dcfg.k}
+        if dcfg is not None else None,
+        "l2": "no explicit flush: each step streams Q (1.07 GB), K/V (134 MB each), the "
+              "8.8 GB main-branch workspace and the 11.5 GB decode caches, so nothing the "
+              "next step reads is still in the 129 MB L2",
+        "parallelism": "replicas" if world > 1 else "single",
+    }
+
+
 def run_msa(args, world, rank, local):
     pcfg = gen.CONFIGS[args.prefill]
     if args.prefill_n:
@@ -325,24 +342,12 @@ def run_msa(args, world, rank, local):
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
         "steps": K, "warmup": W, "ms_per_step": round(t_all / K, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {
-            "workload": "prefill N=%d" % N + (" + decode %d seqs L~U[%d,%d]" % (
-                dcfg.S, dcfg.len_lo, dcfg.len_hi) if d is not None else ""),
-            "prefill": {"N": N, "H_q": pcfg.H_q, "H_kv": pcfg.H_kv, "d_h": pcfg.d_h,
-                        "d_idx": pcfg.d_idx, "block": 64, "k": pcfg.k,
-                        "hot_blocks": pcfg.hot_blocks, "block_offset_std": pcfg.block_offset_std},
-            "decode": {"S": dcfg.S, "len_lo": dcfg.len_lo, "len_hi": dcfg.len_hi,
-                       "mean_len": float(np.mean(d["meta"]["lens"])), "k": dcfg.k}
-            if d is not None else None,
-            "l2": "no explicit flush: each step streams Q (1.07 GB), K/V (134 MB each), the "
-                  "8.8 GB main-branch workspace and the 11.5 GB decode caches, so nothing the "
-                  "next step reads is still in the 129 MB L2",
-            "parallelism": "replicas" if world > 1 else "single",
-        },
+        "config": bench_config(pcfg, dcfg, world),
         "ms_prefill": round(t_prefill_total / K, 4),
         "ms_decode": round(t_decode_total / K, 4),
         "decode": {"value": round(dec_value, 1), "unit": "tokens/s",
-                   "ms": round(t_decode_total / K, 4)} if d is not None else None,
+                   "ms": round(t_decode_total / K, 4),
+                   "mean_len": float(np.mean(d["meta"]["lens"]))} if d is not None else None,
         "kernels": kern,
         "roofline": {"kernel": dom["kernel"], "bound": dom["bound"], "achieved": dom["achieved"],
                      "peak": dom["peak"], "unit": dom["unit"], "frac": dom["frac"],
@@ -443,6 +448,9 @@ def run_reference(args, world, rank):
     if rank != 0:
         return None
     pcfg = gen.CONFIGS[args.prefill]
+    if args.prefill_n:
+        pcfg = gen.PrefillConfig(**{**pcfg.__dict__, "N": args.prefill_n})
+    dcfg = None if args.decode == "none" else gen.CONFIGS[args.decode]
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     x = gen.prefill_inputs(pcfg, seed=args.seed, device=dev)
     xh = host_bits(x, ("q", "k", "v", "q_idx", "k_idx"))
@@ -462,12 +470,13 @@ def run_reference(args, world, rank):
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(1e3 * elapsed / args.steps, 2), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": "prefill N=%d (sampled query rows)" % pcfg.N},
+            "config": bench_config(pcfg, dcfg, world),
             "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": cores,
                              "kind": "oracle",
                              "sample": "%d uniformly sampled query rows per run of the N=%d "
-                                       "prefill workload, whole path, fp64" % (total_rows //
-                                                                              args.steps, pcfg.N)},
+                                       "prefill workload, whole prefill path, fp64 (the metric "
+                                       "is prefill tokens/s; decode is not timed on this arm)" % (
+                                           total_rows // args.steps, pcfg.N)},
             "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
 

@@ -143,7 +143,7 @@ def test_workspace_sizes(lib):
     nblk = L // 64
     floor = 4 * S * H_kv * nblk + 4 * S * H_kv * k + 4 * S * H_kv * 4 * (H_q // H_kv) * (d_h + 1)
     assert floor <= need <= floor + 4 * 256
-    # main branch: per query chunk (<= 16384 rows) the bucket arrays, the entries, each tile's
+    # main branch: per query chunk (<= 32768 rows) the bucket arrays, the entries, each tile's
     # shared-block list and private-slot masks, and the private partials (bf16 O + fp32 LSE per
     # selection, at fixed (row, slot) positions)
     need = lib.msa_sparse_attn_fwd_workspace(i64(1024), 8, 2, 64, 4)
