@@ -2,7 +2,8 @@
 
 A plain C (OpenMP, fp64) restatement of the formulas in «MiniMax-M3：MSA 技术报告速读»,
 section 核心机制 (index branch eq. S^idx / M^idx, TopK eq. I^(r)_i with the forced local
-block, main branch eq. O^(h)_i, LSE from section Kernel).  Only tests, the smoke check
+block, main branch eq. O^(h)_i, LSE from section Kernel; the KL alignment loss of section
+训练, eq. P^idx / P / L_KL).  Only tests, the smoke check
 and the bench's CPU-baseline leg import this package; the CUDA library never does, and
 the two share no code.
 
@@ -17,6 +18,10 @@ Pins (what this oracle is checked against, in tests/test_oracle_pins.py):
                    torch.nn.functional.scaled_dot_product_attention (causal, fp64);
                    Q = 0 closed form (LSE = ln|T|, O = mean of V over T).
   decode        -- equals the prefill row L-1 on the same tokens.
+  KL loss       -- k >= #blocks equals scipy.stats.entropy of torch.softmax distributions
+                   (causal); sparse selections equal the same library routines on a mask
+                   built by brute force; uniform-teacher and uniform-student closed forms;
+                   KL = 0 when the student's scores equal the teacher's; KL >= 0.
   bf16 rounding -- exhaustive agreement with torch's fp32->bf16 RNE on fp32-representable
                    values plus hand-picked tie cases.
 """
@@ -59,6 +64,8 @@ def lib():
                                               P, i64, P, P, P, P, P]
         L.msa_oracle_decode.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32, P,
                                         i32, P, P, i64, P, P, P]
+        L.msa_oracle_kl_loss.argtypes = [P, P, P, P, P, i64, i32, i32, i32, i32, i32, i32, P,
+                                          i64, P]
         L.msa_oracle_set_threads.argtypes = [i32]
         L.msa_oracle_get_threads.restype = i32
         L.msa_oracle_f64_to_bf16.argtypes = [ctypes.c_double]
@@ -184,3 +191,19 @@ def decode(q, q_idx, k_cache, v_cache, k_idx_cache, cu_seqlens, kk, block_size=6
     if want_m:
         out["M32"] = M32
     return out
+
+
+def kl_loss(q, k, q_idx, k_idx, I, block_size=64, rows=None):
+    """KL alignment loss over a given selection I [H_kv, N, kk] -> KL [n, H_kv] float64
+    (row t is query rows[t], or t when rows is None)."""
+    q, k, q_idx, k_idx = map(_u16, (q, k, q_idx, k_idx))
+    I = np.ascontiguousarray(I, dtype=np.int32)
+    N, H_q, d_h = q.shape
+    H_kv, d_idx = k.shape[1], q_idx.shape[2]
+    kk = I.shape[2]
+    rows_a = None if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
+    n = N if rows_a is None else len(rows_a)
+    KL = np.empty((n, H_kv), np.float64)
+    lib().msa_oracle_kl_loss(_p(q), _p(k), _p(q_idx), _p(k_idx), _p(I), N, H_q, H_kv, d_h, d_idx,
+                             block_size, kk, _p(rows_a), n, _p(KL))
+    return KL

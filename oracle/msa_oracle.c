@@ -16,6 +16,9 @@
  *     the visible tokens of the selected blocks; all query heads of group r share I^(r)_i
  *     (eq. O^(h)_i).
  *   - section Kernel: the forward also emits the per-row log-sum-exp (LSE).
+ * and the section 训练：top-k 不可导怎么办 (training), eq. P^idx / P / L_KL: the KL alignment
+ *   loss of a row and group over its selected token set, the main branch's group-averaged
+ *   attention (teacher) against the index branch's softmax (student).
  *
  * Readings where the page is silent (each is listed with its reason in the design notes):
  *   - k counts the forced local block: I = {l} U top-(k-1) of the blocks b < l.
@@ -29,6 +32,9 @@
  *   - the selection compares block scores rounded once to fp32 (the precision the
  *     CUDA path decides in); everything else is fp64 from exactly-widened bf16 inputs.
  *   - decode: the query is the last cache row i = L-1 of its sequence.
+ *   - KL loss: the selected token set is the main branch's T (visible tokens of the selected
+ *     blocks); both softmaxes normalise over T; the teacher's scores are the main branch's
+ *     scaled scores; the result is one value per (row, group), no reduction over rows.
  *
  * Layouts (row-major, bf16 passed as uint16 bit patterns):
  *   Q [N,H_q,d_h], K,V [N,H_kv,d_h], Q_idx [N,H_kv,d_idx], K_idx [N,d_idx],
@@ -180,6 +186,65 @@ static void row_attend(const uint16_t *q_i, const uint16_t *K, const uint16_t *V
             for (int d = 0; d < d_h; ++d) oh[d] += p * bf16_to_f64(vj[d]);
         }
     }
+}
+
+/* ------------------------------------------------ KL alignment loss (L4) -- */
+
+/* KL alignment loss of row i, group r over the selected token set T (the visible tokens of
+ * the blocks sel[0..kk), entries < 0 skipped):
+ *   student  P^idx_j = exp(S^idx_j) / sum_{u in T} exp(S^idx_u),
+ *            S^idx_j = Q_idx[i,r] . K_idx[j] / sqrt(d_idx)
+ *   teacher  P_j = (1/G) sum over the G heads h of group r of exp(s^h_j) / sum_{u in T} exp(s^h_u),
+ *            s^h_j = Q[i,h] . K[j,r] / sqrt(d_h)
+ *   KL = sum_{j in T} P_j (ln P_j - ln P^idx_j)      (a term with P_j = 0 contributes 0)
+ * q_i points at Q[i,0,0], qidx_ir at Q_idx[i,r,0]; K, K_idx at token 0 of the sequence. */
+static double row_kl(const uint16_t *q_i, const uint16_t *qidx_ir, const uint16_t *K,
+                     const uint16_t *K_idx, int64_t i, int r, int H_q, int H_kv, int d_h,
+                     int d_idx, int B, const int32_t *sel, int kk, double *s_buf, double *p_buf,
+                     int64_t *j_buf)
+{
+    const int G = H_q / H_kv;
+    int64_t nt = 0;
+    for (int t = 0; t < kk; ++t) {
+        const int64_t b = sel[t];
+        if (b < 0) continue;
+        const int64_t j1 = imin64(b * B + B - 1, i);
+        for (int64_t j = b * B; j <= j1; ++j) j_buf[nt++] = j;
+    }
+    /* teacher: the mean over the group's heads of each head's softmax over T */
+    const double scale_h = 1.0 / sqrt((double)d_h);
+    for (int64_t t = 0; t < nt; ++t) p_buf[t] = 0.0;
+    for (int h = r * G; h < (r + 1) * G; ++h) {
+        const uint16_t *qh = q_i + (int64_t)h * d_h;
+        double m = -INFINITY;
+        for (int64_t t = 0; t < nt; ++t) {
+            const uint16_t *kj = K + (j_buf[t] * H_kv + r) * (int64_t)d_h;
+            double dot = 0.0;
+            for (int d = 0; d < d_h; ++d) dot += bf16_to_f64(qh[d]) * bf16_to_f64(kj[d]);
+            s_buf[t] = dot * scale_h;
+            if (s_buf[t] > m) m = s_buf[t];
+        }
+        double z = 0.0;
+        for (int64_t t = 0; t < nt; ++t) z += exp(s_buf[t] - m);
+        for (int64_t t = 0; t < nt; ++t) p_buf[t] += exp(s_buf[t] - m) / z / G;
+    }
+    /* student: the index branch's softmax over T, kept as log-probabilities */
+    const double scale_idx = 1.0 / sqrt((double)d_idx);
+    double m = -INFINITY;
+    for (int64_t t = 0; t < nt; ++t) {
+        const uint16_t *kj = K_idx + j_buf[t] * (int64_t)d_idx;
+        double dot = 0.0;
+        for (int d = 0; d < d_idx; ++d) dot += bf16_to_f64(qidx_ir[d]) * bf16_to_f64(kj[d]);
+        s_buf[t] = dot * scale_idx;
+        if (s_buf[t] > m) m = s_buf[t];
+    }
+    double z = 0.0;
+    for (int64_t t = 0; t < nt; ++t) z += exp(s_buf[t] - m);
+    const double lse_idx = m + log(z);
+    double kl = 0.0;
+    for (int64_t t = 0; t < nt; ++t)
+        if (p_buf[t] > 0.0) kl += p_buf[t] * (log(p_buf[t]) - (s_buf[t] - lse_idx));
+    return kl;
 }
 
 /* ------------------------------------------------------------- exports ----- */
@@ -367,6 +432,34 @@ void msa_oracle_decode(const uint16_t *q, const uint16_t *q_idx, const uint16_t 
         free(m64);
         free(m32);
         free(s_buf);
+        free(j_buf);
+    }
+}
+
+/* KL alignment loss for the given rows (rows == NULL: all N rows) with a given selection
+ * I [H_kv, N, kk].  KL [n_rows, H_kv], fp64. */
+void msa_oracle_kl_loss(const uint16_t *q, const uint16_t *k, const uint16_t *q_idx,
+                        const uint16_t *k_idx, const int32_t *I, int64_t N, int H_q, int H_kv,
+                        int d_h, int d_idx, int B, int kk, const int64_t *rows, int64_t n_rows,
+                        double *KL)
+{
+    if (!rows) n_rows = N;
+#pragma omp parallel
+    {
+        double *s_buf = (double *)malloc((size_t)kk * B * sizeof(double));
+        double *p_buf = (double *)malloc((size_t)kk * B * sizeof(double));
+        int64_t *j_buf = (int64_t *)malloc((size_t)kk * B * sizeof(int64_t));
+#pragma omp for schedule(dynamic, 8)
+        for (int64_t t = 0; t < n_rows; ++t) {
+            const int64_t i = rows ? rows[t] : t;
+            for (int r = 0; r < H_kv; ++r)
+                KL[t * H_kv + r] = row_kl(q + i * H_q * (int64_t)d_h,
+                                          q_idx + (i * H_kv + r) * (int64_t)d_idx, k, k_idx, i, r,
+                                          H_q, H_kv, d_h, d_idx, B, I + ((int64_t)r * N + i) * kk,
+                                          kk, s_buf, p_buf, j_buf);
+        }
+        free(s_buf);
+        free(p_buf);
         free(j_buf);
     }
 }

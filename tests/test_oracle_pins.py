@@ -284,3 +284,150 @@ def test_flop_ratio_closed_form():
     ratio = lambda T: (4 * hq_dh * N / 2) / (4 * hq_dh * T + 2 * hidx_didx * N / 2)
     assert round(ratio(2048), 1) == 28.4
     assert round(ratio(1024), 1) == 30.1
+
+
+# ------------------------------------------------------ KL alignment loss --
+
+def selected_token_mask(I, N, B):
+    """Brute force: mask[r, i, j] = token j is visible from i and its block is in I[r, i]."""
+    H_kv = I.shape[0]
+    blk = np.arange(N) // B
+    mask = np.zeros((H_kv, N, N), bool)
+    for r in range(H_kv):
+        for i in range(N):
+            chosen = [int(b) for b in I[r, i] if b >= 0]
+            mask[r, i] = np.isin(blk, chosen) & (np.arange(N) <= i)
+    return mask
+
+
+def library_kl(x, mask):
+    """Teacher and student from torch.softmax over the masked fp64 scores; the KL from
+    scipy.stats.entropy (sum p log(p/q)) row by row -> [N, H_kv]."""
+    from scipy.stats import entropy
+    Q, K = torch.from_numpy(f64(x["q"])), torch.from_numpy(f64(x["k"]))
+    Qi, Ki = torch.from_numpy(f64(x["q_idx"])), torch.from_numpy(f64(x["k_idx"]))
+    N, H_q, d_h = Q.shape
+    H_kv, d_idx = K.shape[1], Qi.shape[2]
+    G = H_q // H_kv
+    m = torch.from_numpy(np.array(mask))
+    out = np.zeros((N, H_kv))
+    for r in range(H_kv):
+        S = torch.einsum("nhd,md->hnm", Q[:, r * G:(r + 1) * G], K[:, r]) / math.sqrt(d_h)
+        teacher = torch.softmax(S.masked_fill(~m[r], float("-inf")), dim=-1).mean(dim=0)
+        Si = (Qi[:, r] @ Ki.T) / math.sqrt(d_idx)
+        student = torch.softmax(Si.masked_fill(~m[r], float("-inf")), dim=-1)
+        for i in range(N):
+            sel = m[r, i]
+            out[i, r] = entropy(teacher[i, sel].numpy(), student[i, sel].numpy())
+    return out
+
+
+def test_kl_full_k_equals_library_entropy():
+    """k >= number of blocks: T is the whole causal prefix, so the loss is the KL of two
+    plain causal softmaxes (torch.softmax), computed by scipy.stats.entropy."""
+    cfg = small_cfg(N=96, H_q=8, H_kv=2, d_h=16, d_idx=8, k=12)
+    x = bits(gen.prefill_inputs(cfg, seed=11))
+    B = 8
+    _, M32 = oracle.block_scores(x["q_idx"], x["k_idx"], block_size=B)
+    I = oracle.select_blocks(M32, 96, 12, block_size=B)
+    KL = oracle.kl_loss(x["q"], x["k"], x["q_idx"], x["k_idx"], I, block_size=B)
+    causal = np.broadcast_to(np.tril(np.ones((96, 96), bool)), (2, 96, 96))
+    np.testing.assert_allclose(KL, library_kl(x, causal), rtol=1e-10, atol=1e-12)
+
+
+@pytest.mark.parametrize("variant,seed", [("gauss", 12), ("int", 13)])
+def test_kl_sparse_matches_library_on_bruteforce_mask(variant, seed):
+    cfg = small_cfg(N=120, H_q=8, H_kv=2, d_h=16, d_idx=8, k=3)
+    x = bits(gen.prefill_inputs(cfg, seed=seed, variant=variant))
+    B = 8
+    _, M32 = oracle.block_scores(x["q_idx"], x["k_idx"], block_size=B)
+    I = oracle.select_blocks(M32, 120, 3, block_size=B)
+    KL = oracle.kl_loss(x["q"], x["k"], x["q_idx"], x["k_idx"], I, block_size=B)
+    np.testing.assert_allclose(KL, library_kl(x, selected_token_mask(I, 120, B)), rtol=1e-10,
+                               atol=1e-12)
+    rows = np.array([0, 7, 8, 63, 119])
+    sub = oracle.kl_loss(x["q"], x["k"], x["q_idx"], x["k_idx"], I, block_size=B, rows=rows)
+    assert np.array_equal(sub, KL[rows])
+
+
+def test_kl_uniform_teacher_closed_form():
+    """Q = 0: every head's softmax over T is uniform, so the teacher is 1/|T| and
+    KL(U || softmax(x)) = logsumexp_T(x) - mean_T(x) - ln|T|, x the index scores over T,
+    with |T| = min(i+1, (k-1)B + (i mod B) + 1)."""
+    from scipy.special import logsumexp
+    cfg = small_cfg(N=140, k=3)
+    x = bits(gen.prefill_inputs(cfg, seed=14, variant="zero_q"))
+    B = 8
+    _, M32 = oracle.block_scores(x["q_idx"], x["k_idx"], block_size=B)
+    I = oracle.select_blocks(M32, 140, 3, block_size=B)
+    KL = oracle.kl_loss(x["q"], x["k"], x["q_idx"], x["k_idx"], I, block_size=B)
+    Qi, Ki = f64(x["q_idx"]), f64(x["k_idx"])
+    for r in range(2):
+        for i in range(140):
+            toks = [j for b in I[r, i] if b >= 0 for j in range(b * B, min(b * B + B, i + 1))]
+            assert len(toks) == min(i + 1, 2 * B + (i % B) + 1)
+            s = Ki[toks] @ Qi[i, r] / math.sqrt(8)
+            want = logsumexp(s) - s.mean() - math.log(len(toks))
+            assert KL[i, r] == pytest.approx(want, abs=1e-12)
+
+
+def test_kl_uniform_student_closed_form():
+    """Q_idx = 0: the student is 1/|T|, so KL(P || U) = ln|T| - H(P), H the entropy of the
+    teacher (the mean of the group's per-head causal softmaxes over T)."""
+    from scipy.stats import entropy
+    cfg = small_cfg(N=100, H_q=8, H_kv=2, d_h=16, d_idx=8, k=4)
+    x = bits(gen.prefill_inputs(cfg, seed=15))
+    B = 8
+    _, M32 = oracle.block_scores(x["q_idx"], x["k_idx"], block_size=B)
+    I = oracle.select_blocks(M32, 100, 4, block_size=B)
+    x["q_idx"] = np.zeros_like(x["q_idx"])
+    KL = oracle.kl_loss(x["q"], x["k"], x["q_idx"], x["k_idx"], I, block_size=B)
+    Q, K = f64(x["q"]), f64(x["k"])
+    for r in range(2):
+        for i in range(100):
+            toks = [j for b in I[r, i] if b >= 0 for j in range(b * B, min(b * B + B, i + 1))]
+            P = np.zeros(len(toks))
+            for h in range(4 * r, 4 * r + 4):
+                s = K[toks, r] @ Q[i, h] / 4.0
+                e = np.exp(s - s.max())
+                P += e / e.sum() / 4
+            want = math.log(len(toks)) - entropy(P)
+            assert KL[i, r] == pytest.approx(want, abs=1e-12)
+
+
+def test_kl_zero_when_student_scores_equal_teacher():
+    """d_idx = d_h, one KV head, both query heads equal to the index query and K_idx = K:
+    the student's scores are the teacher's, so the loss is 0 on every row; a perturbed
+    index query gives a strictly positive loss (Gibbs' inequality)."""
+    cfg = small_cfg(N=130, H_q=2, H_kv=1, d_h=16, d_idx=16, k=3)
+    x = bits(gen.prefill_inputs(cfg, seed=16))
+    B = 8
+    x["q"][:, 1] = x["q"][:, 0]
+    x["q_idx"] = np.ascontiguousarray(x["q"][:, :1])
+    x["k_idx"] = np.ascontiguousarray(x["k"][:, 0])
+    _, M32 = oracle.block_scores(x["q_idx"], x["k_idx"], block_size=B)
+    I = oracle.select_blocks(M32, 130, 3, block_size=B)
+    KL = oracle.kl_loss(x["q"], x["k"], x["q_idx"], x["k_idx"], I, block_size=B)
+    assert np.abs(KL).max() < 1e-13
+    x["q_idx"] = gen.to_bits(gen.from_bits(x["q_idx"]) * 2)
+    KL2 = oracle.kl_loss(x["q"], x["k"], x["q_idx"], x["k_idx"], I, block_size=B)
+    assert (KL2[1:] > 0).all() and KL2[0, 0] == pytest.approx(0, abs=1e-15)   # |T| = 1 at i = 0
+
+
+def test_kl_nonnegative_and_group_specific():
+    """KL >= 0 on every row; swapping the two groups' query heads changes the loss (the
+    teacher of group r averages heads r*G .. r*G+G-1 only)."""
+    cfg = small_cfg(N=90, H_q=8, H_kv=2, d_h=16, d_idx=8, k=3)
+    x = bits(gen.prefill_inputs(cfg, seed=17))
+    B = 8
+    _, M32 = oracle.block_scores(x["q_idx"], x["k_idx"], block_size=B)
+    I = oracle.select_blocks(M32, 90, 3, block_size=B)
+    KL = oracle.kl_loss(x["q"], x["k"], x["q_idx"], x["k_idx"], I, block_size=B)
+    assert (KL >= -1e-15).all() and KL.max() > 0.01
+    y = dict(x)
+    y["q"] = np.ascontiguousarray(x["q"][:, [4, 5, 6, 7, 0, 1, 2, 3]])
+    KL_sw = oracle.kl_loss(y["q"], y["k"], y["q_idx"], y["k_idx"], I, block_size=B)
+    assert np.abs(KL_sw - KL).max() > 1e-3
+    y["q"] = np.ascontiguousarray(x["q"][:, [3, 2, 1, 0, 7, 6, 5, 4]])  # within-group order
+    KL_perm = oracle.kl_loss(y["q"], y["k"], y["q_idx"], y["k_idx"], I, block_size=B)
+    np.testing.assert_allclose(KL_perm, KL, rtol=1e-12, atol=1e-14)
