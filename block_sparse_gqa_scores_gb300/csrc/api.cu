@@ -216,10 +216,36 @@ MSA_API msa_status_t msa_sparse_decode(const void* q, const void* q_idx, const v
   return from_cuda(e);
 }
 
+MSA_API size_t msa_kl_loss_fwd_workspace(int64_t N, int H_kv, int k) {
+  if (N < 1 || H_kv < 1 || k < 1 || k > 64) return 0;
+  return msa::kl_ws_bytes(N, H_kv, k);
+}
+
+MSA_API msa_status_t msa_kl_loss_fwd(const void* q, const void* k, const void* q_idx,
+                                     const void* k_idx, const int32_t* idx, const float* lse,
+                                     float* kl, int64_t N, int H_q, int H_kv, int d_h, int d_idx,
+                                     int block_size, int k_blocks, void* ws, size_t ws_bytes,
+                                     void* stream) {
+  if (!aligned16(q) || !aligned16(k) || !aligned16(q_idx) || !aligned16(k_idx) ||
+      !aligned4(idx) || !aligned4(lse) || !aligned4(kl) || !aligned16(ws))
+    return MSA_ERR_INVALID_ARGUMENT;
+  if (N < 1 || H_q < 1 || H_kv < 1 || H_q % H_kv != 0 || d_h < 1 || d_idx < 1 ||
+      block_size != 64 || k_blocks < 1 || k_blocks > 64)
+    return MSA_ERR_INVALID_ARGUMENT;
+  if (!pow2_upto(H_kv, 8) || !pow2_upto(H_q / H_kv, 8) || (d_h != 64 && d_h != 128) ||
+      (d_idx != 32 && d_idx != 64))
+    return MSA_ERR_UNSUPPORTED;
+  if (N > ((int64_t)1 << 21) || N * H_kv * k_blocks >= kMaxRows) return MSA_ERR_UNSUPPORTED;
+  if (ws_bytes < msa::kl_ws_bytes(N, H_kv, k_blocks)) return MSA_ERR_WORKSPACE;
+  return from_cuda(msa::launch_kl_loss_fwd(q, k, q_idx, k_idx, idx, lse, kl, N, H_q, H_kv, d_h,
+                                           d_idx, k_blocks, ws, (cudaStream_t)stream));
+}
+
 MSA_API msa_status_t msa_device_status(void) {
-  unsigned v = 0, w = 0, x = 0;
+  unsigned v = 0, w = 0, x = 0, y = 0;
   if (msa::read_reset_score_status(&v) != cudaSuccess) return MSA_ERR_CUDA;
   if (msa::read_reset_shared_status(&w) != cudaSuccess) return MSA_ERR_CUDA;
   if (msa::read_reset_kvo_status(&x) != cudaSuccess) return MSA_ERR_CUDA;
-  return (v | w | x) ? MSA_ERR_TIMEOUT : MSA_OK;
+  if (msa::read_reset_kl_status(&y) != cudaSuccess) return MSA_ERR_CUDA;
+  return (v | w | x | y) ? MSA_ERR_TIMEOUT : MSA_OK;
 }

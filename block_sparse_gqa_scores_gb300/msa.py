@@ -46,8 +46,12 @@ def _load():
                                     P, P, sz, P]
     L.msa_sparse_decode_noalloc.argtypes = [P, P, P, P, P, P, i32, i64, i32, i32, i32, i32, i32,
                                             i32, P, P, P, P]
+    L.msa_kl_loss_fwd_workspace.argtypes = [i64, i32, i32]
+    L.msa_kl_loss_fwd_workspace.restype = sz
+    L.msa_kl_loss_fwd.argtypes = [P, P, P, P, P, P, P, i64, i32, i32, i32, i32, i32, i32, P, sz, P]
     for fn in ("msa_index_block_scores", "msa_select_blocks", "msa_index_select", "msa_sparse_attn_fwd",
-               "msa_sparse_decode", "msa_sparse_decode_noalloc", "msa_device_status"):
+               "msa_sparse_decode", "msa_sparse_decode_noalloc", "msa_kl_loss_fwd",
+               "msa_device_status"):
         getattr(L, fn).restype = i32
     return L
 
@@ -203,6 +207,33 @@ def msa_sparse_decode_noalloc(q, q_idx, k_cache, v_cache, k_idx_cache, cu_seqlen
         S, max_len, H_q, H_kv, d_h, d_idx, block_size, k, _ptr(o), _ptr(lse), _ptr(idx_out),
         _stream(stream)))
     return o, lse, idx_out
+
+
+def msa_kl_loss_fwd_workspace(N, H_kv, k):
+    return int(lib.msa_kl_loss_fwd_workspace(N, H_kv, k))
+
+
+def msa_kl_loss_fwd(q, k, q_idx, k_idx, idx, lse, kl=None, ws=None, block_size=BLOCK,
+                    stream=None):
+    """KL alignment loss per (group, row): KL [H_kv, N] fp32, teacher from the forward's LSE."""
+    _req(q, torch.bfloat16, 3, "q")
+    _req(k, torch.bfloat16, 3, "k")
+    _req(q_idx, torch.bfloat16, 3, "q_idx")
+    _req(k_idx, torch.bfloat16, 2, "k_idx")
+    _req(idx, torch.int32, 3, "idx")
+    _req(lse, torch.float32, 2, "lse")
+    N, H_q, d_h = q.shape
+    H_kv, d_idx = k.shape[1], q_idx.shape[2]
+    kk = idx.shape[2]
+    if kl is None:
+        kl = torch.empty((H_kv, N), dtype=torch.float32, device=q.device)
+    nws = msa_kl_loss_fwd_workspace(N, H_kv, kk)
+    if ws is None and nws:
+        ws = torch.empty(nws, dtype=torch.uint8, device=q.device)
+    _check("msa_kl_loss_fwd", lib.msa_kl_loss_fwd(
+        _ptr(q), _ptr(k), _ptr(q_idx), _ptr(k_idx), _ptr(idx), _ptr(lse), _ptr(kl), N, H_q, H_kv,
+        d_h, d_idx, block_size, kk, _ptr(ws), 0 if ws is None else ws.numel(), _stream(stream)))
+    return kl
 
 
 def msa_device_status():

@@ -11,6 +11,8 @@
  *                  over the visible tokens (j <= i) of the selected blocks, shared by the
  *                  G = H_q/H_kv query heads of group r = h / G; the forward also emits the
  *                  per-row log-sum-exp (section Kernel).
+ *   training:      the KL alignment loss between the main branch's group-averaged attention and
+ *                  the index branch's softmax over the selected tokens (section 训练, eq. L_KL).
  *
  * Conventions (every entry point):
  *   - Pointers are DEVICE pointers owned by the caller; the library never allocates or
@@ -169,6 +171,34 @@ msa_status_t msa_sparse_decode_noalloc(const void *q, const void *q_idx, const v
                                        const int64_t *cu_seqlens, int S, int64_t max_len, int H_q,
                                        int H_kv, int d_h, int d_idx, int block_size, int k,
                                        void *o, float *lse, int32_t *idx_out, void *stream);
+
+/* Workspace bytes msa_kl_loss_fwd needs (0 for invalid sizes): per (group, block) bucket counts
+ * and offsets, and per selection an entry and a 16-byte partial -- 20 * H_kv * N * k bytes plus
+ * 16 * H_kv * ceil(N/64) (168 MB at N = 131072, H_kv = 4, k = 16). */
+size_t msa_kl_loss_fwd_workspace(int64_t N, int H_kv, int k);
+
+/* Forward of the KL alignment loss that trains the index branch (section 训练：top-k 不可导怎么办
+ * of the digest, eqs. P^idx, P and L_KL; the LSE it needs is the main branch's, section Kernel).
+ * For every group r and row i, over the selected token set T = {j : floor(j/64) in idx[r,i,:],
+ * j <= i} (the main branch's T):
+ *   teacher  P_j     = (1/G) sum_{h = rG .. rG+G-1} exp(q[i,h,:] . k[j,r,:] / sqrt(d_h) - lse[h,i])
+ *   student  P^idx_j = exp(S^idx_j) / sum_{u in T} exp(S^idx_u),  S^idx_j = q_idx[i,r,:] . k_idx[j,:] / sqrt(d_idx)
+ *   kl[r, i] = sum_{j in T} P_j (ln P_j - ln P^idx_j)      (terms with P_j = 0 count 0)
+ * No reduction over rows or groups is applied (the caller averages as its training step needs).
+ *   q    bf16 [N, H_q, d_h];  k bf16 [N, H_kv, d_h];  q_idx bf16 [N, H_kv, d_idx];
+ *   k_idx bf16 [N, d_idx];  idx int32 [H_kv, N, k] (as msa_sparse_attn_fwd requires it);
+ *   lse  fp32 [H_q, N], the natural-log LSE msa_sparse_attn_fwd wrote for the same q, k, idx
+ *        (with another lse the teacher rows do not sum to 1 and the result is not a KL);
+ *   kl   fp32 [H_kv, N];
+ *   ws   device workspace of at least msa_kl_loss_fwd_workspace() bytes, 16-byte aligned
+ *        (contents ignored on entry, unspecified on return; one call at a time per workspace).
+ * fp32 arithmetic from bf16 inputs.  Each selection's contribution is computed independently
+ * and a row's contributions are combined in slot order, with no atomic update of any result.
+ * Errors as msa_sparse_attn_fwd; N > 2^21 or H_kv * N * k >= 2^31: MSA_ERR_UNSUPPORTED. */
+msa_status_t msa_kl_loss_fwd(const void *q, const void *k, const void *q_idx, const void *k_idx,
+                             const int32_t *idx, const float *lse, float *kl, int64_t N, int H_q,
+                             int H_kv, int d_h, int d_idx, int block_size, int k_blocks, void *ws,
+                             size_t ws_bytes, void *stream);
 
 /* Reads and clears the device status words of the current device (synchronising call).
  * Returns MSA_ERR_TIMEOUT if any kernel since the last call gave up a bounded wait,

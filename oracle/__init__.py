@@ -64,8 +64,7 @@ def lib():
                                               P, i64, P, P, P, P, P]
         L.msa_oracle_decode.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32, P,
                                         i32, P, P, i64, P, P, P]
-        L.msa_oracle_kl_loss.argtypes = [P, P, P, P, P, i64, i32, i32, i32, i32, i32, i32, P,
-                                          i64, P]
+        L.msa_oracle_kl_loss.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, i32, P, i64, P]
         L.msa_oracle_set_threads.argtypes = [i32]
         L.msa_oracle_get_threads.restype = i32
         L.msa_oracle_f64_to_bf16.argtypes = [ctypes.c_double]
@@ -193,17 +192,22 @@ def decode(q, q_idx, k_cache, v_cache, k_idx_cache, cu_seqlens, kk, block_size=6
     return out
 
 
-def kl_loss(q, k, q_idx, k_idx, I, block_size=64, rows=None):
-    """KL alignment loss over a given selection I [H_kv, N, kk] -> KL [n, H_kv] float64
-    (row t is query rows[t], or t when rows is None)."""
+def kl_loss(q, k, q_idx, k_idx, I, block_size=64, rows=None, compact=False):
+    """KL alignment loss over a given selection -> KL [n, H_kv] float64, row t = query rows[t]
+    (all N rows when rows is None).  I is [H_kv, N, kk]; compact=True: q, q_idx and I hold only
+    the listed rows ([n,H_q,d_h], [n,H_kv,d_idx], [H_kv,n,kk])."""
     q, k, q_idx, k_idx = map(_u16, (q, k, q_idx, k_idx))
-    I = np.ascontiguousarray(I, dtype=np.int32)
-    N, H_q, d_h = q.shape
-    H_kv, d_idx = k.shape[1], q_idx.shape[2]
-    kk = I.shape[2]
-    rows_a = None if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
-    n = N if rows_a is None else len(rows_a)
+    N, H_kv, d_h = k.shape
+    H_q, d_idx = q.shape[1], q_idx.shape[2]
+    rows_a = np.arange(N, dtype=np.int64) if rows is None else np.ascontiguousarray(rows, np.int64)
+    I = np.asarray(I, dtype=np.int32)
+    if not compact:
+        q, q_idx, I = q[rows_a], q_idx[rows_a], I[:, rows_a]
+    q, q_idx = np.ascontiguousarray(q), np.ascontiguousarray(q_idx)
+    I_rows = np.ascontiguousarray(I.transpose(1, 0, 2))
+    n = len(rows_a)
+    assert q.shape[0] == n and q_idx.shape[0] == n and I_rows.shape[:2] == (n, H_kv)
     KL = np.empty((n, H_kv), np.float64)
-    lib().msa_oracle_kl_loss(_p(q), _p(k), _p(q_idx), _p(k_idx), _p(I), N, H_q, H_kv, d_h, d_idx,
-                             block_size, kk, _p(rows_a), n, _p(KL))
+    lib().msa_oracle_kl_loss(_p(q), _p(k), _p(q_idx), _p(k_idx), _p(I_rows), H_q, H_kv, d_h,
+                             d_idx, block_size, I_rows.shape[2], _p(rows_a), n, _p(KL))
     return KL

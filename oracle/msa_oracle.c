@@ -436,28 +436,26 @@ void msa_oracle_decode(const uint16_t *q, const uint16_t *q_idx, const uint16_t 
     }
 }
 
-/* KL alignment loss for the given rows (rows == NULL: all N rows) with a given selection
- * I [H_kv, N, kk].  KL [n_rows, H_kv], fp64. */
-void msa_oracle_kl_loss(const uint16_t *q, const uint16_t *k, const uint16_t *q_idx,
-                        const uint16_t *k_idx, const int32_t *I, int64_t N, int H_q, int H_kv,
-                        int d_h, int d_idx, int B, int kk, const int64_t *rows, int64_t n_rows,
-                        double *KL)
+/* KL alignment loss for the listed rows: row t is query position rows[t]; q_rows [n,H_q,d_h],
+ * q_idx_rows [n,H_kv,d_idx] and I_rows [n,H_kv,kk] hold that row's projections and selection;
+ * K, K_idx are the full sequence.  KL [n, H_kv], fp64. */
+void msa_oracle_kl_loss(const uint16_t *q_rows, const uint16_t *k, const uint16_t *q_idx_rows,
+                        const uint16_t *k_idx, const int32_t *I_rows, int H_q, int H_kv, int d_h,
+                        int d_idx, int B, int kk, const int64_t *rows, int64_t n_rows, double *KL)
 {
-    if (!rows) n_rows = N;
 #pragma omp parallel
     {
         double *s_buf = (double *)malloc((size_t)kk * B * sizeof(double));
         double *p_buf = (double *)malloc((size_t)kk * B * sizeof(double));
         int64_t *j_buf = (int64_t *)malloc((size_t)kk * B * sizeof(int64_t));
 #pragma omp for schedule(dynamic, 8)
-        for (int64_t t = 0; t < n_rows; ++t) {
-            const int64_t i = rows ? rows[t] : t;
+        for (int64_t t = 0; t < n_rows; ++t)
             for (int r = 0; r < H_kv; ++r)
-                KL[t * H_kv + r] = row_kl(q + i * H_q * (int64_t)d_h,
-                                          q_idx + (i * H_kv + r) * (int64_t)d_idx, k, k_idx, i, r,
-                                          H_q, H_kv, d_h, d_idx, B, I + ((int64_t)r * N + i) * kk,
-                                          kk, s_buf, p_buf, j_buf);
-        }
+                KL[t * H_kv + r] = row_kl(q_rows + t * H_q * (int64_t)d_h,
+                                          q_idx_rows + (t * H_kv + r) * (int64_t)d_idx, k, k_idx,
+                                          rows[t], r, H_q, H_kv, d_h, d_idx, B,
+                                          I_rows + (t * H_kv + r) * (int64_t)kk, kk, s_buf, p_buf,
+                                          j_buf);
         free(s_buf);
         free(p_buf);
         free(j_buf);

@@ -26,7 +26,8 @@ def test_header_declares_the_api():
     syms = declared_symbols()
     for name in ("msa_index_block_scores", "msa_select_blocks", "msa_index_select",
                  "msa_sparse_attn_fwd", "msa_sparse_attn_fwd_workspace", "msa_sparse_decode",
-                 "msa_sparse_decode_workspace", "msa_status_string", "msa_device_status"):
+                 "msa_sparse_decode_workspace", "msa_kl_loss_fwd", "msa_kl_loss_fwd_workspace",
+                 "msa_status_string", "msa_device_status"):
         assert name in syms
 
 
@@ -72,6 +73,12 @@ def decode(lib, q=P, S=4, max_len=1000, H_q=32, H_kv=4, d_h=128, d_idx=64, B=64,
            wsb=1 << 40, cu=P, idx_out=NUL):
     return lib.msa_sparse_decode(q, P, P, P, P, cu, S, i64(max_len), H_q, H_kv, d_h, d_idx, B, k,
                                  P, P, idx_out, ws, ctypes.c_size_t(wsb), NUL)
+
+
+def kl(lib, q=P, k=P, qi=P, ki=P, idx=P, lse=P, out=P, N=1024, H_q=32, H_kv=4, d_h=128, d_idx=64,
+       B=64, kk=16, ws=P, wsb=1 << 40):
+    return lib.msa_kl_loss_fwd(q, k, qi, ki, idx, lse, out, i64(N), H_q, H_kv, d_h, d_idx, B, kk,
+                               ws, ctypes.c_size_t(wsb), NUL)
 
 
 INVALID, UNSUPPORTED, WORKSPACE = 1, 2, 3
@@ -153,3 +160,27 @@ def test_workspace_sizes(lib):
              8 * tiles * 16)
     assert floor <= need <= floor + 8 * 256
     assert attn(lib, N=1024, H_q=8, H_kv=2, d_h=64, kk=4, wsb=need - 1) == WORKSPACE
+
+
+@pytest.mark.parametrize("kw", [dict(q=NUL), dict(qi=MIS), dict(ki=NUL), dict(idx=NUL),
+                                dict(lse=ctypes.c_void_p(0x10001)), dict(out=NUL), dict(N=0),
+                                dict(H_q=30), dict(kk=0), dict(kk=65), dict(B=32), dict(ws=NUL),
+                                dict(ws=MIS)])
+def test_kl_invalid(lib, kw):
+    assert kl(lib, **kw) == INVALID
+
+
+@pytest.mark.parametrize("kw", [dict(d_h=96), dict(d_idx=128), dict(H_q=64, H_kv=4),
+                                dict(H_q=12, H_kv=4), dict(N=(1 << 21) + 1)])
+def test_kl_unsupported(lib, kw):
+    assert kl(lib, **kw) == UNSUPPORTED
+
+
+def test_kl_workspace(lib):
+    lib.msa_kl_loss_fwd_workspace.restype = ctypes.c_size_t
+    need = lib.msa_kl_loss_fwd_workspace(i64(131072), 4, 16)
+    sel = 4 * 131072 * 16
+    floor = 20 * sel + 4 * 4 * (4 * 2048 + 1)           # entries + partials, four bucket arrays
+    assert floor <= need <= floor + 6 * 256
+    assert lib.msa_kl_loss_fwd_workspace(i64(0), 4, 16) == 0
+    assert kl(lib, N=1000, wsb=lib.msa_kl_loss_fwd_workspace(i64(1000), 4, 16) - 1) == WORKSPACE

@@ -78,6 +78,25 @@ def test_fullsize_prefill(name, n_rows):
     check_rows(x, cfg, idx, o, lse, sample_rows(cfg.N, n_rows, seed=1))
 
 
+def test_fullsize_kl_loss():
+    """The KL alignment loss at 128K, in the benchmark's launch sequence (fused index branch,
+    main branch, KL forward), on sampled rows the oracle recomputes on the GPU's selection."""
+    cfg = gen.CONFIGS["p128k"]
+    x = gen.prefill_inputs(cfg, seed=0, device="cuda")
+    idx, _, lse = run_prefill(x, cfg)
+    kl = msa.msa_kl_loss_fwd(x["q"], x["k"], x["q_idx"], x["k_idx"], idx, lse)
+    torch.cuda.synchronize()
+    msa.msa_device_status()
+    rows = sample_rows(cfg.N, 40, seed=3)
+    rows_t = torch.from_numpy(rows).cuda()
+    ref = oracle.kl_loss(gen.to_bits(x["q"][rows_t]), gen.to_bits(x["k"]),
+                         gen.to_bits(x["q_idx"][rows_t]), gen.to_bits(x["k_idx"]),
+                         idx[:, rows_t].cpu().numpy(), rows=rows, compact=True)
+    got = kl[:, rows_t].cpu().numpy().T.astype(np.float64)
+    assert np.isfinite(kl.cpu().numpy()).all() and float(kl.min()) >= -1e-3
+    assert (np.abs(got - ref) <= 5e-4 + 1e-3 * np.abs(ref)).all(), float(np.abs(got - ref).max())
+
+
 def test_fullsize_prefill_1m():
     cfg = gen.CONFIGS["p1m"]
     x = gen.prefill_inputs(cfg, seed=0, device="cuda")

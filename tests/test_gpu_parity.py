@@ -239,6 +239,75 @@ def test_prefill_chain(name, N, variant, seed):
     assert max_abs(lse.cpu().numpy().T, L) <= LSE_TOL
 
 
+# ---------------------------------------------------------------- KL alignment loss --
+# The GPU loss (teacher normalised by the GPU forward's LSE) against the oracle evaluated on the
+# GPU's own selection.  Tolerance: fp32 dot products of bf16 inputs and the forward's fp32 LSE
+# leave ~1e-5 in each exponent; ex2/lg2 approximations ~2^-22 relative; fp32 sums of <= 1024
+# terms of magnitude <= ~30 in C = sum P (ln P - S^idx) and in LSE^idx * sum P, which cancel
+# down to the KL: a few 1e-5 typical, so 5e-4 + 1e-3 |KL| leaves a wide margin.
+KL_ATOL, KL_RTOL = 5e-4, 1e-3
+
+KL_CASES = [
+    ("tiny", {}, 1024, 4), ("tiny", {}, 1000, 4), ("tiny", {}, 1024, 1), ("tiny", {}, 1024, 64),
+    ("p32k", {}, 1, 16), ("p32k", {}, 65, 16), ("p32k", {}, 3000, 16), ("p32k", {}, 2500, 64),
+    ("p32k", dict(H_q=4, H_kv=4), 700, 8), ("p32k", dict(H_q=8, H_kv=4), 700, 8),
+    ("p32k", dict(H_q=16, H_kv=4), 700, 8), ("p32k", dict(H_q=8, H_kv=1), 700, 5),
+    ("p32k", dict(d_h=64), 900, 16), ("tiny", dict(d_h=128), 900, 4),
+    ("p32k", dict(d_idx=32), 900, 16),
+]
+
+
+def gpu_index(x, cfg, N):
+    if cfg.k <= 32:
+        return msa.msa_index_select(x["q_idx"], x["k_idx"], cfg.k)
+    return msa.msa_select_blocks(msa.msa_index_block_scores(x["q_idx"], x["k_idx"]), N, cfg.k)
+
+
+def check_kl(kl, ref):
+    got = kl.cpu().numpy().T                                   # [N, H_kv]
+    err = np.abs(got.astype(np.float64) - ref)
+    assert np.isfinite(got).all()
+    assert (err <= KL_ATOL + KL_RTOL * np.abs(ref)).all(), float(err.max())
+
+
+@pytest.mark.parametrize("name,over,N,k", KL_CASES)
+def test_kl_loss(name, over, N, k):
+    cfg = cfg_of(name, k=k, **over)
+    x, b = fresh(cfg, N, seed=21)
+    idx = gpu_index(x, cfg, N)
+    _, lse = msa.msa_sparse_attn_fwd(x["q"], x["k"], x["v"], idx)
+    kl = msa.msa_kl_loss_fwd(x["q"], x["k"], x["q_idx"], x["k_idx"], idx, lse)
+    sync_ok()
+    ref = oracle.kl_loss(b["q"], b["k"], b["q_idx"], b["k_idx"], idx.cpu().numpy())
+    check_kl(kl, ref)
+    assert ref.max() > 0.05 or N == 1                            # a loss that is not trivially 0
+
+
+def test_kl_loss_zero_when_student_equals_teacher():
+    """One head per group, d_idx = d_h = 64, q_idx = q and k_idx = k: the student's scores are
+    the teacher's, so the loss is 0 up to the forward LSE's rounding."""
+    cfg = cfg_of("p32k", H_q=1, H_kv=1, d_h=64, d_idx=64, k=8)
+    x, _ = fresh(cfg, 2000, seed=22)
+    x["q_idx"] = x["q"].clone()
+    x["k_idx"] = x["k"][:, 0].contiguous()
+    idx = msa.msa_index_select(x["q_idx"], x["k_idx"], 8)
+    _, lse = msa.msa_sparse_attn_fwd(x["q"], x["k"], x["v"], idx)
+    kl = msa.msa_kl_loss_fwd(x["q"], x["k"], x["q_idx"], x["k_idx"], idx, lse)
+    sync_ok()
+    assert float(kl.abs().max()) <= 1e-4
+
+
+def test_kl_loss_uniform_teacher():
+    """Q = 0: the teacher is uniform over T, the oracle's closed-form case, on the GPU."""
+    cfg = cfg_of("p32k")
+    x, b = fresh(cfg, 1500, seed=23, variant="zero_q")
+    idx = msa.msa_index_select(x["q_idx"], x["k_idx"], 16)
+    _, lse = msa.msa_sparse_attn_fwd(x["q"], x["k"], x["v"], idx)
+    kl = msa.msa_kl_loss_fwd(x["q"], x["k"], x["q_idx"], x["k_idx"], idx, lse)
+    sync_ok()
+    check_kl(kl, oracle.kl_loss(b["q"], b["k"], b["q_idx"], b["k_idx"], idx.cpu().numpy()))
+
+
 # ------------------------------------------------------------------------ decode --
 
 def decode_case(cfg, lens, seed, variant="gauss"):
