@@ -5,7 +5,9 @@ A step is one pass of the whole hot path over one batch of synthetic input:
   prefill at N = 131072 tokens (index block scores -> per-group top-k selection -> sparse main
   branch; H_q=32, H_kv=4, d_h=128, d_idx=64, block 64, k=16, 8 hot blocks), then
   decode of 32 sequences with cache lengths ~ U[65536, 262144] (same head layout).
-`value` is prefill tokens/s (N / prefill device time); decode tokens/s is reported beside it.
+`value` is prefill tokens/s (N / prefill device time); decode tokens/s is reported beside it, and
+the forward of the KL alignment loss (on the step's selection and LSE) is timed after the steps,
+outside `value`.
 Inputs stay resident in HBM; every timed input (M alone is 4.3 GB, the decode caches 11.5 GB)
 is larger than the 129 MB L2, so no flush is needed.
 
@@ -44,7 +46,11 @@ DECODE_LAUNCHES = 4
 KERNEL_FILES = {"index_branch": ["k_score.cu"],
                 "main_branch": ["attn_fwd.cu", "k_attn_shared.cu", "k_attn_kvouter.cu",
                                 "k_attn_plan.cu", "attn_tile.cuh"],
-                "decode": ["k_decode.cu", "k_select.cu", "k_attn.cu"]}
+                "decode": ["k_decode.cu", "k_select.cu", "k_attn.cu"],
+                "kl_loss_fwd": ["k_kl.cu", "k_attn_plan.cu", "attn_tile.cuh"]}
+# the KL alignment loss forward, timed apart from the step: plan, scan, plan, block-major pass,
+# merge (+ one memset)
+KL_LAUNCHES = 5
 
 
 # ------------------------------------------------------------------------ helpers --
@@ -101,7 +107,8 @@ NCU_ROWS = {"k_index_block_scores": "index_branch",
             "k_attn_plan": "main_branch", "k_attn_scan": "main_branch",
             "k_attn_kvouter": "main_branch", "k_attn_shared": "main_branch",
             "k_decode_block_scores": "decode", "k_select_decode": "decode",
-            "k_sparse_attn": "decode", "k_decode_merge": "decode"}
+            "k_sparse_attn": "decode", "k_decode_merge": "decode",
+            "k_kl_plan": "kl_loss_fwd", "k_kl_kvouter": "kl_loss_fwd", "k_kl_merge": "kl_loss_fwd"}
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.txt")
 
 
@@ -141,7 +148,7 @@ def write_traffic(csv_path, command):
         f.write("# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per call of each bench\n"
                 "# row, averaged over %d whole steps of one ncu capture (1 pass, cold cache):\n"
                 "#   %s\n# row  bytes_per_call  source_sha\n" % (steps, command))
-        for k in ("index_branch", "main_branch", "decode"):
+        for k in ("index_branch", "main_branch", "decode", "kl_loss_fwd"):
             if k in tot:
                 f.write("%s %d %s\n" % (k, tot[k] / max(steps, 1),
                                          kernel_source_hash(KERNEL_FILES[k])))
@@ -200,6 +207,8 @@ def workload_sizes(pcfg, dcfg, lens):
     out = dict(
         F_idx=2.0 * di * Hkv * N * (N + 1) / 2,
         F_main=4.0 * dh * Hq * T.sum(),
+        # KL loss: the teacher's scores of the G heads and the student's score per visible token
+        F_kl=(2.0 * dh * Hq + 2.0 * di * Hkv) * T.sum(),
     )
     # decode algorithmic bytes: the index-key stream + selected visible K/V + small vectors
     dbytes = 0.0
@@ -358,11 +367,45 @@ def run_msa(args, world, rank, local):
         "gpu_launches": (1 + ATTN_LAUNCHES_PER_CHUNK * (-(-N // ATTN_CHUNK_ROWS)) +
                          (DECODE_LAUNCHES if d is not None else 0)) * K,
     }
+    if not args.no_kl:
+        line["kl_loss_fwd"] = time_kl(msa, pcfg, x, bufs, K, sizes, pk, world)
     if not args.no_e2e:
         line["e2e"] = e2e_prefill(msa, pcfg, x, bufs, K, W, world)
     if not args.no_cpu_baseline and rank == 0 and world == 1:
         line["cpu_baseline"] = cpu_baseline(pcfg, x, args.cpu_seconds, args.seed)
     return line
+
+
+def time_kl(msa, pcfg, x, bufs, K, sizes, pk, world):
+    """The KL alignment loss forward (the training-side consumer of the forward's LSE) on the
+    last step's selection and LSE, timed apart from the step: K calls after 3 warm-up calls."""
+    N = pcfg.N
+    kl = torch.empty((pcfg.H_kv, N), dtype=torch.float32, device="cuda")
+    ws = torch.empty(msa.msa_kl_loss_fwd_workspace(N, pcfg.H_kv, pcfg.k), dtype=torch.uint8,
+                     device="cuda")
+
+    def call():
+        msa.msa_kl_loss_fwd(x["q"], x["k"], x["q_idx"], x["k_idx"], bufs["idx"], bufs["lse"],
+                            kl=kl, ws=ws)
+
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(K + 1)]
+    evs[0].record(stream)
+    for s in range(K):
+        call()
+        evs[s + 1].record(stream)
+    torch.cuda.synchronize()
+    msa.msa_device_status()
+    ms = max_over_ranks(float(np.mean([evs[s].elapsed_time(evs[s + 1]) for s in range(K)])), world)
+    achieved = sizes["F_kl"] / (ms * 1e-3) / 1e12
+    return {"ms": round(ms, 4), "value": round(world * N / (ms * 1e-3), 1), "unit": "tokens/s",
+            "mean_kl": round(float(kl.mean()), 6), "gpu_launches_per_call": KL_LAUNCHES,
+            "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": pk["bf16_sust"],
+                         "unit": "TFLOP/s", "frac": round(achieved / pk["bf16_sust"], 4),
+                         "traffic": ncu_traffic("kl_loss_fwd"), "algorithmic": sizes["F_kl"]}}
 
 
 def e2e_prefill(msa, pcfg, x, bufs, K, W, world):
@@ -494,6 +537,7 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-kl", action="store_true", help="skip the KL loss forward measurement")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--write-traffic", metavar="NCU_CSV",
                     help="write profiles/traffic.txt from an ncu CSV of whole steps and exit")

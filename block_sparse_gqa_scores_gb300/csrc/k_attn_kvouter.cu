@@ -169,18 +169,21 @@ __global__ void __launch_bounds__(kThreadsKvo, 3)
     }
   };
   // the stacked query rows of a tile (entry e's G heads are rows e*G .. e*G+G-1): at G = 8 an
-  // entry is one 1-KB swizzle atom per 64-dim half, a single TMA box issued by thread 0 and
-  // counted on q_bar; otherwise every thread gathers 16-byte pieces with cp.async
+  // entry is one 1-KB swizzle atom per 64-dim half, a single TMA box issued by lane e of warp 0
+  // and counted on q_bar; otherwise every thread gathers 16-byte pieces with cp.async
   auto gather_q = [&](int bkt, const int* ent, int n_ent) {
     const int rb = (int)(bkt / nblk);
     if (G == 8) {
-      if (tid == 0) {
-        mbar_expect_tx(q_bar, (uint32_t)(n_ent * 8 * 128 * L::kHalves));
-        for (int e = 0; e < n_ent; ++e) {
-          const int i = (int)(q0 + (ent[e] >> 6));
+      // one lane of warp 0 per entry: the boxes are issued in parallel, not one after another
+      if (warp == 0) {
+        if (lane == 0) mbar_expect_tx(q_bar, (uint32_t)(n_ent * 8 * 128 * L::kHalves));
+        __syncwarp();
+        if (lane < n_ent) {
+          const int i = (int)(q0 + (ent[lane] >> 6));
 #pragma unroll
           for (int bx = 0; bx < L::kHalves; ++bx)
-            tma_load_3d(sb + L::kOffQ + bx * L::kQHalf + e * 1024, &tm_q, q_bar, 64 * bx, rb * 8, i);
+            tma_load_3d(sb + L::kOffQ + bx * L::kQHalf + lane * 1024, &tm_q, q_bar, 64 * bx,
+                        rb * 8, i);
         }
       }
       return;

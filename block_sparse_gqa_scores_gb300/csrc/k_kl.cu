@@ -224,13 +224,16 @@ __global__ void __launch_bounds__(kKlThreads, kKlCtasPerSm)
   auto gather_q = [&](int bkt, const int* ent, int n_ent) {
     const int rb = (int)(bkt / nblk);
     if (G == 8) {
-      if (tid == 0) {
-        mbar_expect_tx(q_bar, (uint32_t)(n_ent * 8 * 128 * L::kHalves));
-        for (int e = 0; e < n_ent; ++e) {
-          const int i = ent[e] >> 6;
+      // one lane of warp 0 per entry: the boxes are issued in parallel, not one after another
+      if (warp == 0) {
+        if (lane == 0) mbar_expect_tx(q_bar, (uint32_t)(n_ent * 8 * 128 * L::kHalves));
+        __syncwarp();
+        if (lane < n_ent) {
+          const int i = ent[lane] >> 6;
 #pragma unroll
           for (int bx = 0; bx < L::kHalves; ++bx)
-            tma_load_3d(sb + L::kOffQ + bx * L::kQHalf + e * 1024, &tm_q, q_bar, 64 * bx, rb * 8, i);
+            tma_load_3d(sb + L::kOffQ + bx * L::kQHalf + lane * 1024, &tm_q, q_bar, 64 * bx,
+                        rb * 8, i);
         }
       }
     } else {
