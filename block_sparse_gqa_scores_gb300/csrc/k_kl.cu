@@ -31,29 +31,45 @@ namespace {
 __device__ unsigned g_kl_status = 0;
 
 constexpr int kKlRows = 128;                 // UMMA M
-constexpr int kKlThreads = 128;              // 4 warps: TMEM lane quarters
 constexpr int kKlPlanWarps = 4;
 constexpr float kLn2 = 0.693147180559945309f;
 constexpr float kLog2e = 1.442695040888963407f;
 
-template <int D_H>
+// One persistent CTA per SM (its TMEM stages take all 512 columns).  Shared memory holds a ring
+// of query stages -- the tile's stacked query rows and its entries' index queries, one row per
+// entry -- a ring of two key stages (K_b and K_idx_b of one bucket) and, per epilogue group, the
+// tile's student scores transposed to (entry, token).  TMEM holds kTStages accumulator stages:
+// S (128 rows x 64 tokens) and the student scores (64 tokens on the lanes x the tile's entries).
+template <int D_H, int G>
 struct KlSmem {
+  static constexpr int kEpt = kKlRows / G;        // entries per work tile
   static constexpr int kHalves = D_H / 64;
   static constexpr int kQHalf = kKlRows * 128;    // 128 rows x 64 dims, bf16, SW128
   static constexpr int kKHalf = 64 * 128;         // 64 keys x 64 dims
+  static constexpr int kQiBytes = kEpt * 128 < 1024 ? 1024 : kEpt * 128;
+  static constexpr int kQStages = G == 8 ? 4 : (G == 4 ? 3 : 2);
+  static constexpr int kKStages = 2;
+  static constexpr int kTCols = 64 + kEpt <= 128 ? 128 : 256;
+  static constexpr int kTStages = 512 / kTCols;
+  static constexpr int kQStage = kHalves * kQHalf + kQiBytes;
+  static constexpr int kKStage = kHalves * kKHalf + kKHalf;
   static constexpr int kOffQ = 0;
-  static constexpr int kOffQi = kOffQ + kHalves * kQHalf;   // stacked index queries (<= 64 dims)
-  static constexpr int kOffK = kOffQi + kQHalf;
-  static constexpr int kOffKi = kOffK + kHalves * kKHalf;   // the block's index keys
-  static constexpr int kOffBar = kOffKi + kKHalf;
-  static constexpr int kOffMisc = kOffBar + 16;
-  static constexpr int kOffEnt = kOffMisc + 16;   // entries of this tile and the next
-  static constexpr int kBytes = kOffEnt + 2 * kKlRows * 4;
-  static constexpr int kAlloc = kBytes + 1024;
-  static constexpr uint32_t kTmemCols = 128;      // S, then S^idx
+  static constexpr int kOffK = kOffQ + kQStages * kQStage;
+  // the student MMA reads 128 rows of K_idx_b, the last 64 of them past the stage (ignored
+  // lanes): the transposed-score buffers (>= 8 KB) follow the key stages
+  static constexpr int kOffSi = kOffK + kKStages * kKStage;
+  static constexpr int kSiBytes = kEpt * 64 * 4;  // per epilogue group
+  static constexpr int kOffBar = kOffSi + 2 * kSiBytes;
+  static constexpr int kNumBars = 2 * kQStages + 2 * kKStages + 2 * kTStages;
+  static constexpr int kOffMisc = kOffBar + 8 * kNumBars;
+  static constexpr int kOffPEnt = kOffMisc + 16;  // each producer warp's copy of a tile's entries
+  static constexpr int kBytes = kOffPEnt + 2 * 4 * kKlRows;
+  // more than half of the SM's shared memory: one CTA per SM
+  static constexpr int kAlloc = kBytes + 1024 > 116 * 1024 ? kBytes + 1024 : 116 * 1024;
+  static_assert(kQStage % 1024 == 0 && kKStage % 1024 == 0, "swizzle atoms");
+  static_assert(2 * kSiBytes >= 8 * 1024, "rows 64..127 of the student A operand stay in bounds");
+  static_assert(kAlloc <= 227 * 1024, "shared memory");
 };
-constexpr int kKlCtasPerSm = 3;
-static_assert(kKlCtasPerSm * (KlSmem<128>::kAlloc + 1024) <= 228 * 1024, "3 CTAs per SM");
 
 __device__ __forceinline__ void kl_cp_async16(uint32_t dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
@@ -136,62 +152,120 @@ __device__ __forceinline__ void lane_split(float (&a)[64], int h) {
   }
 }
 
+#define KL_TMEM_LD16(taddr, r)                                                                  \
+  asm volatile(                                                                                 \
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "                                                 \
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"                         \
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),     \
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), \
+        "=r"(r[14]), "=r"(r[15])                                                                \
+      : "r"(taddr))
+
+__device__ __forceinline__ void kl_group_sync(int id) {
+  asm volatile("bar.sync %0, 128;" ::"r"(id) : "memory");
+}
+// Barrier of one epilogue group (four warps) that also ANDs a predicate over its 128 threads:
+// the only place where a group may leave its loop, so all four warps leave together.
+__device__ __forceinline__ bool kl_group_and(int id, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.and.pred q, %2, 128, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)v), "r"(id)
+      : "memory");
+  return r != 0;
+}
+
+// Q as [N, H_q, d_h] with boxes of 64 dims x G heads x 2^m consecutive tokens (m = 0..4): a run
+// of consecutive query rows among a tile's entries (the queries of one 16-query tile that chose
+// the same block land next to each other in its bucket) loads with a few large boxes instead of
+// one box per row.
+struct KlQMaps {
+  CUtensorMap m[5];
+};
+
+// Warp roles: warps 0 and 10 load (warp 0 the query rows, warp 10 the keys and index queries),
+// warp 1 issues the MMAs, warps 2..9 are two epilogue groups of four (one warp per TMEM lane
+// quarter) that take alternate work tiles.
+constexpr int kKlWarps = 11;
+constexpr int kKlWsThreads = 32 * kKlWarps;
+
 template <int D_H, int G>
-__global__ void __launch_bounds__(kKlThreads, kKlCtasPerSm)
-    k_kl_kvouter(const __grid_constant__ CUtensorMap tm_q, const __nv_bfloat16* __restrict__ q,
+__global__ void __launch_bounds__(kKlWsThreads, 1)
+    k_kl_kvouter(const __grid_constant__ KlQMaps tm_q, const __nv_bfloat16* __restrict__ q,
                  const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ q_idx,
                  const __nv_bfloat16* __restrict__ k_idx, const float* __restrict__ lse,
                  const int* __restrict__ entries, const int* __restrict__ offset,
                  const int* __restrict__ tile_off, int nbuckets, int64_t nblk, int64_t N,
                  int H_kv, int d_idx, int kk, float4* __restrict__ part, float scale_log2,
                  float idx_scale) {
-  using L = KlSmem<D_H>;
-  constexpr int kEpt = kKlRows / G;          // entries per work tile
+  using L = KlSmem<D_H, G>;
+  constexpr int kEpt = L::kEpt;
+  constexpr int kQStages = L::kQStages, kKStages = L::kKStages, kTStages = L::kTStages;
   constexpr int kCpl = 64 / G;               // columns a lane owns after the reduce-scatter
   constexpr int kChunks = D_H / 8;           // 16-byte chunks per K / Q row
+  constexpr int kEntPerLane = kEpt > 32 ? kEpt / 32 : 1;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sb = smem_u32(smem);
-  const uint32_t mma_bar = sb + L::kOffBar, q_bar = sb + L::kOffBar + 8;
+  const uint32_t bar0 = sb + L::kOffBar;
+  auto q_full = [&](int s) { return bar0 + 8u * s; };
+  auto q_empty = [&](int s) { return bar0 + 8u * (kQStages + s); };
+  auto k_full = [&](int s) { return bar0 + 8u * (2 * kQStages + s); };
+  auto k_empty = [&](int s) { return bar0 + 8u * (2 * kQStages + kKStages + s); };
+  auto t_full = [&](int s) { return bar0 + 8u * (2 * kQStages + 2 * kKStages + s); };
+  auto t_empty = [&](int s) { return bar0 + 8u * (2 * kQStages + 2 * kKStages + kTStages + s); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffMisc);
-  int* s_ent = reinterpret_cast<int*>(smem + L::kOffEnt);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + L::kOffMisc + 4);
+  int* s_pent = reinterpret_cast<int*>(smem + L::kOffPEnt);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int tid = threadIdx.x;
   const int H_q = H_kv * G;
   const int ichunks = d_idx / 8;             // 16-byte chunks per index row
 
-  if (tid == 0) {
-    mbar_init(mma_bar, 1);
-    mbar_init(q_bar, 1);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kQStages; ++s) {
+      // warp 0's arrive (with the TMA transaction bytes at G = 8), warp 10's 32 lanes' copies,
+      // and warp 0's 32 lanes' copies when the query rows also come by cp.async
+      mbar_init(q_full(s), G == 8 ? 33 : 65);
+      mbar_init(q_empty(s), 1);              // MMA commit
+    }
+    for (int s = 0; s < kKStages; ++s) {
+      mbar_init(k_full(s), 32);
+      mbar_init(k_empty(s), 1);
+    }
+    for (int s = 0; s < kTStages; ++s) {
+      mbar_init(t_full(s), 1);
+      mbar_init(t_empty(s), 4 * 32);         // the 128 threads of one epilogue group
+    }
+    *s_abort = 0;
     fence_barrier_init();
   }
-  if (warp == 0) {
-    tmem_alloc(smem_u32(tmem_slot), L::kTmemCols);
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
     tc_fence_before();
   }
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  const int total_tiles = tile_off[nbuckets];
-  const int64_t kv_stride = (int64_t)H_kv * D_H;
-  uint32_t phase = 0, qphase = 0;
-  bool ok = true;
-
   // a contiguous range of work tiles per CTA (consecutive tiles often share a bucket)
+  const int total_tiles = tile_off[nbuckets];
   const int per = (total_tiles + gridDim.x - 1) / gridDim.x;
   const int t_beg = blockIdx.x * per;
   const int t_end = min(total_tiles, t_beg + per);
-  int bucket = 0;
-  if (t_beg < t_end) {
+  const int ntiles = max(0, t_end - t_beg);
+  int bucket0 = 0;
+  if (ntiles > 0) {
     int lo = 0, hi = nbuckets;                             // tile_off[lo] <= t_beg < tile_off[hi]
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
       if (__ldg(tile_off + mid) <= t_beg) lo = mid; else hi = mid;
     }
-    bucket = lo;
+    bucket0 = lo;
   }
-  int next_off = t_beg < t_end ? __ldg(tile_off + bucket + 1) : 0;
+  const int next0 = ntiles > 0 ? __ldg(tile_off + bucket0 + 1) : 0;
+  // tile -> (bucket, first entry, entries), advancing a cursor (bkt, nxt) over increasing tiles
   auto describe = [&](int tile, int& bkt, int& nxt, int& e0, int& n_e) {
     while (nxt <= tile) {
       ++bkt;
@@ -200,206 +274,305 @@ __global__ void __launch_bounds__(kKlThreads, kKlCtasPerSm)
     e0 = __ldg(offset + bkt) + (tile - __ldg(tile_off + bkt)) * kEpt;
     n_e = min(kEpt, __ldg(offset + bkt + 1) - e0);
   };
-  // K_b and K_idx_b of a bucket (rows past the sequence: zeros; they are masked anyway)
-  auto load_k = [&](int bkt) {
-    const int rb = (int)(bkt / nblk);
-    const int64_t bb = bkt - (int64_t)rb * nblk;
-    const __nv_bfloat16* kb = k + (bb * kBlock * H_kv + rb) * (int64_t)D_H;
-    for (int x = tid; x < kBlock * kChunks; x += kKlThreads) {
-      const int j = x / kChunks, c = x - j * kChunks;
-      const uint32_t off = (c >> 3) * L::kKHalf + j * 128 + (((c & 7) ^ (j & 7)) << 4);
-      if (bb * kBlock + j < N) kl_cp_async16(sb + L::kOffK + off, kb + j * kv_stride + c * 8);
-      else kl_zero16(sb + L::kOffK + off);
-    }
-    const __nv_bfloat16* kib = k_idx + bb * kBlock * (int64_t)d_idx;
-    for (int x = tid; x < kBlock * ichunks; x += kKlThreads) {
-      const int j = x / ichunks, c = x - j * ichunks;
-      const uint32_t off = j * 128 + ((c ^ (j & 7)) << 4);
-      if (bb * kBlock + j < N) kl_cp_async16(sb + L::kOffKi + off, kib + (int64_t)j * d_idx + c * 8);
-      else kl_zero16(sb + L::kOffKi + off);
-    }
-  };
-  // the stacked query rows (entry e's heads are rows e*G .. e*G+G-1) and the stacked index
-  // queries (entry e's index query on each of its G rows); ent: the tile's entries in smem
-  auto gather_q = [&](int bkt, const int* ent, int n_ent) {
-    const int rb = (int)(bkt / nblk);
-    if (G == 8) {
-      // one lane of warp 0 per entry: the boxes are issued in parallel, not one after another
-      if (warp == 0) {
-        if (lane == 0) mbar_expect_tx(q_bar, (uint32_t)(n_ent * 8 * 128 * L::kHalves));
-        __syncwarp();
-        if (lane < n_ent) {
-          const int i = ent[lane] >> 6;
+  auto fail = [&]() { *s_abort = 1; };
+
+  if (warp == 0 || warp == kKlWarps - 1) {
+    // ------------------------------------------------------------ producers (two warps)
+    const bool pq = warp == 0;                             // query rows; else keys, index queries
+    int* s_pw = s_pent + (pq ? 0 : kKlRows);
+    int bkt = bucket0, nxt = next0;
+    int last_bkt = -1, kfill = 0, issued = 0;
+    // entries of the next tile, loaded one iteration ahead into registers
+    int pb = bkt, pn = nxt, p_e0 = 0, p_ne = 0;
+    int pre[kEntPerLane];
+    auto load_ents = [&](int j) {
+      describe(t_beg + j, pb, pn, p_e0, p_ne);
 #pragma unroll
-          for (int bx = 0; bx < L::kHalves; ++bx)
-            tma_load_3d(sb + L::kOffQ + bx * L::kQHalf + lane * 1024, &tm_q, q_bar, 64 * bx,
-                        rb * 8, i);
+      for (int m = 0; m < kEntPerLane; ++m) {
+        const int x = lane + 32 * m;
+        pre[m] = x < p_ne ? __ldg(entries + p_e0 + x) : 0;
+      }
+    };
+    if (ntiles > 0) load_ents(0);
+    for (int j = 0; j < ntiles; ++j) {
+      if (__any_sync(0xffffffffu, *s_abort != 0)) break;  // warp-uniform exits only
+      int e0, n_e;
+      describe(t_beg + j, bkt, nxt, e0, n_e);
+      const int rb = (int)(bkt / nblk);
+      const int64_t bb = bkt - (int64_t)rb * nblk;
+      if (!pq && bkt != last_bkt) {                        // K_b and K_idx_b of a new bucket
+        const int ks = kfill % kKStages;
+        if (!__all_sync(0xffffffffu,
+                        mbar_wait(k_empty(ks), ((kfill / kKStages) & 1) ^ 1, &g_kl_status))) {
+          fail();
+          break;
+        }
+        const uint32_t kbase = sb + L::kOffK + ks * L::kKStage;
+        const __nv_bfloat16* kb = k + (bb * kBlock * H_kv + rb) * (int64_t)D_H;
+        for (int x = lane; x < kBlock * kChunks; x += 32) {
+          const int jj = x / kChunks, c = x - jj * kChunks;
+          const uint32_t off = (c >> 3) * L::kKHalf + jj * 128 + (((c & 7) ^ (jj & 7)) << 4);
+          if (bb * kBlock + jj < N)
+            kl_cp_async16(kbase + off, kb + jj * (int64_t)H_kv * D_H + c * 8);
+          else
+            kl_zero16(kbase + off);
+        }
+        const __nv_bfloat16* kib = k_idx + bb * kBlock * (int64_t)d_idx;
+        for (int x = lane; x < kBlock * ichunks; x += 32) {
+          const int jj = x / ichunks, c = x - jj * ichunks;
+          const uint32_t off = L::kHalves * L::kKHalf + jj * 128 + ((c ^ (jj & 7)) << 4);
+          if (bb * kBlock + jj < N)
+            kl_cp_async16(kbase + off, kib + (int64_t)jj * d_idx + c * 8);
+          else
+            kl_zero16(kbase + off);
+        }
+        asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        mbar_arrive(k_full(ks));
+        last_bkt = bkt;
+        ++kfill;
+      }
+      const int s = j % kQStages;
+      if (!__all_sync(0xffffffffu,
+                      mbar_wait(q_empty(s), ((j / kQStages) & 1) ^ 1, &g_kl_status))) {
+        fail();
+        break;
+      }
+      const uint32_t qbase = sb + L::kOffQ + s * L::kQStage;
+      __syncwarp();                                        // the previous tile's reads are done
+#pragma unroll
+      for (int m = 0; m < kEntPerLane; ++m)
+        if (lane + 32 * m < kEpt) s_pw[lane + 32 * m] = pre[m];
+      __syncwarp();
+      if (j + 1 < ntiles) load_ents(j + 1);                // lands while this tile is issued
+      if (pq && G == 8) {
+        // runs of consecutive query rows: the lane at the start of a run issues its boxes
+        if (lane == 0) mbar_expect_tx(q_full(s), (uint32_t)(n_e * 8 * 128 * L::kHalves));
+        __syncwarp();
+        const int row = lane < n_e ? (s_pw[lane] >> 6) : -2;
+        const int prev = __shfl_up_sync(0xffffffffu, row, 1);
+        const bool start = lane < n_e && (lane == 0 || prev != row - 1);
+        const unsigned starts = __ballot_sync(0xffffffffu, start);
+        if (start) {
+          const unsigned later = starts & ~((2u << lane) - 1u);
+          const int stop = later ? __ffs(later) - 1 : n_e;
+          int off = 0;
+          while (off < stop - lane) {
+            const int rem = stop - lane - off;
+            const int m = rem >= 16 ? 4 : rem >= 8 ? 3 : rem >= 4 ? 2 : rem >= 2 ? 1 : 0;
+#pragma unroll
+            for (int bx = 0; bx < L::kHalves; ++bx)
+              tma_load_3d(qbase + bx * L::kQHalf + (lane + off) * 1024, &tm_q.m[m], q_full(s),
+                          64 * bx, rb * 8, row + off);
+            off += 1 << m;
+          }
+        }
+      } else if (pq) {
+        if (lane == 0) mbar_arrive(q_full(s));             // no transaction bytes
+        for (int x = lane; x < n_e * G * kChunks; x += 32) {
+          const int R = x / kChunks, c = x - R * kChunks;
+          const int e = R / G, h = R - e * G;
+          const int64_t i = s_pw[e] >> 6;
+          const uint32_t off = (c >> 3) * L::kQHalf + R * 128 + (((c & 7) ^ (R & 7)) << 4);
+          kl_cp_async16(qbase + off, q + (i * H_q + (int64_t)rb * G + h) * D_H + c * 8);
+        }
+      } else {
+        for (int x = lane; x < n_e * ichunks; x += 32) {   // index queries, one row per entry
+          const int e = x / ichunks, c = x - e * ichunks;
+          const int64_t i = s_pw[e] >> 6;
+          const uint32_t off = L::kHalves * L::kQHalf + e * 128 + ((c ^ (e & 7)) << 4);
+          kl_cp_async16(qbase + off, q_idx + (i * H_kv + rb) * d_idx + c * 8);
         }
       }
-    } else {
-      for (int x = tid; x < n_ent * G * kChunks; x += kKlThreads) {
-        const int R = x / kChunks, c = x - R * kChunks;
-        const int e = R / G, h = R - e * G;
-        const int64_t i = ent[e] >> 6;
-        const uint32_t off = (c >> 3) * L::kQHalf + R * 128 + (((c & 7) ^ (R & 7)) << 4);
-        kl_cp_async16(sb + L::kOffQ + off, q + (i * H_q + (int64_t)rb * G + h) * D_H + c * 8);
+      // each lane's copies arrive on the stage's barrier when they land (the MMA issuer then
+      // makes them visible to the tensor core with a proxy fence)
+      if (!pq || G != 8)
+        asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(q_full(s))
+                     : "memory");
+      ++issued;
+    }
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    // every tile issued has its arrivals; wait until the copies of the last stages have landed
+    for (int j = max(0, issued - kQStages); j < issued; ++j)
+      mbar_wait(q_full(j % kQStages), (j / kQStages) & 1, &g_kl_status);
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer (one lane)
+    if (lane == 0) {
+      int bkt = bucket0, nxt = next0;
+      int last_bkt = -1, kfill = -1, issued = 0;
+      constexpr uint32_t idesc_s = umma_idesc_bf16(kKlRows, 64);
+      constexpr uint32_t idesc_i = umma_idesc_bf16(kKlRows, kEpt);
+      for (int j = 0; j < ntiles; ++j) {
+        if (*s_abort) break;
+        int e0, n_e;
+        describe(t_beg + j, bkt, nxt, e0, n_e);
+        if (bkt != last_bkt) {
+          if (kfill >= 0) umma_commit(k_empty(kfill % kKStages));   // its MMAs are all issued
+          ++kfill;
+          if (!mbar_wait(k_full(kfill % kKStages), (kfill / kKStages) & 1, &g_kl_status)) {
+            fail();
+            break;
+          }
+          last_bkt = bkt;
+        }
+        const int s = j % kQStages, t = j % kTStages;
+        if (!mbar_wait(q_full(s), (j / kQStages) & 1, &g_kl_status)) { fail(); break; }
+        if (!mbar_wait(t_empty(t), ((j / kTStages) & 1) ^ 1, &g_kl_status)) { fail(); break; }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // cp.async data -> MMA
+        tc_fence_after();
+        const uint32_t qbase = sb + L::kOffQ + s * L::kQStage;
+        const uint32_t kbase = sb + L::kOffK + (kfill % kKStages) * L::kKStage;
+        const uint32_t d = tmem + (uint32_t)(L::kTCols * t);
+        // teacher scores: S = Q_stack K_b^T, 128 rows x 64 tokens
+#pragma unroll
+        for (int ks = 0; ks < D_H / 16; ++ks) {
+          const uint32_t a = qbase + (ks >> 2) * L::kQHalf + (ks & 3) * 32;
+          const uint32_t bk = kbase + (ks >> 2) * L::kKHalf + (ks & 3) * 32;
+          umma_bf16(d, umma_desc_kmajor(a, 1024, 128), umma_desc_kmajor(bk, 1024, 128), idesc_s,
+                    ks > 0 ? 1u : 0u);
+        }
+        // student scores, transposed: K_idx_b [tokens on M] . Qi^T [the tile's entries on N]
+        for (int ks = 0; ks < d_idx / 16; ++ks) {
+          const uint32_t a = kbase + L::kHalves * L::kKHalf + ks * 32;
+          const uint32_t bq = qbase + L::kHalves * L::kQHalf + ks * 32;
+          umma_bf16(d + 64, umma_desc_kmajor(a, 1024, 128), umma_desc_kmajor(bq, 1024, 128),
+                    idesc_i, ks > 0 ? 1u : 0u);
+        }
+        umma_commit(t_full(t));
+        umma_commit(q_empty(s));
+        issued = j + 1;
       }
+      // the MMAs in flight complete before TMEM is released
+      if (issued > 0)
+        mbar_wait(t_full((issued - 1) % kTStages), ((issued - 1) / kTStages) & 1, &g_kl_status);
     }
-    for (int x = tid; x < n_ent * G * ichunks; x += kKlThreads) {
-      const int R = x / ichunks, c = x - R * ichunks;
-      const int64_t i = ent[R / G] >> 6;
-      const uint32_t off = R * 128 + ((c ^ (R & 7)) << 4);
-      kl_cp_async16(sb + L::kOffQi + off, q_idx + (i * H_kv + rb) * d_idx + c * 8);
-    }
-  };
-
-  int e0 = 0, n_e = 0;
-  if (t_beg < t_end) {
-    describe(t_beg, bucket, next_off, e0, n_e);
-    load_k(bucket);
-    if (tid < n_e) s_ent[tid] = __ldg(entries + e0 + tid);
-    __syncthreads();
-    gather_q(bucket, s_ent, n_e);
-  }
-  const int R = 32 * warp + lane;                          // this thread's row (TMEM lane)
-  for (int tile = t_beg; tile < t_end && ok; ++tile) {
-    const int cur = (tile - t_beg) & 1;
-    const int* ent_cur = s_ent + cur * kKlRows;
-    const int r = (int)(bucket / nblk);
-    const int64_t b = bucket - (int64_t)r * nblk;
-    const int rows = n_e * G;
-    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    bool qok = true;
-    if (G == 8 && tid == 0) qok = mbar_wait(q_bar, qphase, &g_kl_status);
-    qphase ^= 1u;
-    ok = __syncthreads_and(qok);
-    if (!ok) break;
-    // this row's entry and its head's forward LSE, loaded under the MMAs
-    const bool rv = R < rows;
+  } else {
+    // ------------------------------------------------------------ epilogue groups
+    const int grp = (warp - 2) >> 2;
+    const int qd = warp & 3;                               // TMEM lane quarter of this warp
+    const int R = 32 * qd + lane;                          // row (TMEM lane) of this thread
     const int e = R / G, h = R - e * G;
-    const int ent = rv ? ent_cur[e] : 0;
-    const float lse_raw = rv ? __ldg(lse + (int64_t)(r * G + h) * N + (ent >> 6)) : 0.f;
-
-    // ---- S = Q_stack K_b^T (columns 0..63) and S^idx = Qi_stack K_idx_b^T (columns 64..127)
-    if (tid == 0) {
+    float* s_si = reinterpret_cast<float*>(smem + L::kOffSi + grp * L::kSiBytes);
+    int bkt = bucket0, nxt = next0;
+    // this row's entry and forward LSE, fetched one group-tile ahead
+    int c_e0 = 0, c_ne = 0, c_bkt = 0;
+    int ent = 0;
+    float lse_raw = 0.f;
+    if (grp < ntiles) {
+      describe(t_beg + grp, bkt, nxt, c_e0, c_ne);
+      c_bkt = bkt;
+      const int r0 = (int)(bkt / nblk);
+      if (R < c_ne * G) {
+        ent = __ldg(entries + c_e0 + e);
+        lse_raw = __ldg(lse + (int64_t)(r0 * G + h) * N + (ent >> 6));
+      }
+    }
+    for (int j = grp; j < ntiles; j += 2) {
+      const int r = (int)(c_bkt / nblk);
+      const int64_t b = c_bkt - (int64_t)r * nblk;
+      const bool rv = R < c_ne * G;
+      const int cur_ent = ent;
+      const float cur_lse = lse_raw;
+      // the group's next tile: its entry now, its LSE (which needs the entry) after this tile
+      int n_e0 = 0, n_ne = 0, n_bkt = c_bkt;
+      const bool has_next = j + 2 < ntiles;
+      if (has_next) {
+        describe(t_beg + j + 2, bkt, nxt, n_e0, n_ne);
+        n_bkt = bkt;
+        ent = R < n_ne * G ? __ldg(entries + n_e0 + e) : 0;
+      }
+      const int t = j % kTStages;
+      const bool okw = *s_abort == 0 && mbar_wait(t_full(t), (j / kTStages) & 1, &g_kl_status);
+      if (!kl_group_and(1 + grp, okw)) { fail(); break; }
       tc_fence_after();
-      constexpr uint32_t idesc = umma_idesc_bf16(kKlRows, 64);
+      const uint32_t tbase = tmem + ((uint32_t)(32 * qd) << 16) + (uint32_t)(L::kTCols * t);
+      // student scores of tokens 32*qd .. 32*qd+31 (lanes 0..63 only) -> s_si[entry][token]
+      if (qd < 2) {
 #pragma unroll
-      for (int ks = 0; ks < D_H / 16; ++ks) {
-        const uint32_t a = sb + L::kOffQ + (ks >> 2) * L::kQHalf + (ks & 3) * 32;
-        const uint32_t bk = sb + L::kOffK + (ks >> 2) * L::kKHalf + (ks & 3) * 32;
-        umma_bf16(tmem, umma_desc_kmajor(a, 1024, 128), umma_desc_kmajor(bk, 1024, 128), idesc,
-                  ks > 0 ? 1u : 0u);
+        for (int cc = 0; cc < kEpt; cc += 16) {
+          uint32_t v[16];
+          KL_TMEM_LD16(tbase + 64 + cc, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int c = 0; c < 16; ++c) s_si[(cc + c) * 64 + R] = __uint_as_float(v[c]);
+        }
       }
-      for (int ks = 0; ks < d_idx / 16; ++ks) {
-        const uint32_t a = sb + L::kOffQi + ks * 32;
-        const uint32_t bk = sb + L::kOffKi + ks * 32;
-        umma_bf16(tmem + 64, umma_desc_kmajor(a, 1024, 128), umma_desc_kmajor(bk, 1024, 128),
-                  idesc, ks > 0 ? 1u : 0u);
+      int cmax = -1;                                       // last visible column, -1: none
+      if (rv) {
+        const int64_t i = cur_ent >> 6;
+        cmax = b == (i >> 6) ? (int)(i - b * kBlock) : kBlock - 1;
       }
-      umma_commit(mma_bar);
-    }
-    // the next tile's entries, also under the MMAs
-    const bool has_next = tile + 1 < t_end;
-    int n_bucket = bucket, n_next = next_off, n_e0 = 0, n_ne = 0;
-    if (has_next) {
-      describe(tile + 1, n_bucket, n_next, n_e0, n_ne);
-      if (tid < n_ne) s_ent[(cur ^ 1) * kKlRows + tid] = __ldg(entries + n_e0 + tid);
-    }
-    ok = __syncthreads_and(mbar_wait(mma_bar, phase, &g_kl_status));
-    if (!ok) break;
-    phase ^= 1u;
-    tc_fence_after();
+      const float lse2 = cur_lse * kLog2e;
+      float a[64];
+      {
+        uint32_t sv[64];
+        MSA_TMEM_LD64(tbase, sv);
+        tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < 64; c += 2) {
+          float x0, x1;
+          ffma2(x0, x1, __uint_as_float(sv[c]), __uint_as_float(sv[c + 1]), scale_log2,
+                scale_log2, -lse2, -lse2);
+          a[c] = c <= cmax ? ex2(x0) : 0.f;
+          a[c + 1] = c + 1 <= cmax ? ex2(x1) : 0.f;
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(t_empty(t));                             // this TMEM stage may be reused
+      lane_split<G, true>(a, h);                           // a[c]: G * P of column kCpl*h + c
+      kl_group_sync(1 + grp);                              // s_si is complete
+      const int cb = kCpl * h;
+      float si[kCpl];
+#pragma unroll
+      for (int c = 0; c < kCpl; c += 4) {
+        const float4 v = *reinterpret_cast<const float4*>(s_si + e * 64 + cb + c);
+        si[c] = v.x;
+        si[c + 1] = v.y;
+        si[c + 2] = v.z;
+        si[c + 3] = v.w;
+      }
+      kl_group_sync(1 + grp);                              // s_si may be overwritten
+      if (has_next && R < n_ne * G)                        // the next tile's LSE, under this one
+        lse_raw = __ldg(lse + (int64_t)((int)(n_bkt / nblk) * G + h) * N + (ent >> 6));
 
-    // ---- shared memory is free: the next tile's rows (and its keys for a new bucket)
-    if (has_next) {
-      if (n_bucket != bucket) load_k(n_bucket);
-      gather_q(n_bucket, s_ent + (cur ^ 1) * kKlRows, n_ne);
-    }
-    asm volatile("cp.async.commit_group;" ::: "memory");
-
-    // ---- row R = (entry e, head h): teacher probabilities of the block's tokens
-    int cmax = -1;                                         // last visible column, -1: none
-    if (rv) {
-      const int64_t i = ent >> 6;
-      cmax = b == (i >> 6) ? (int)(i - b * kBlock) : kBlock - 1;
-    }
-    const float lse2 = lse_raw * kLog2e;
-    float a[64];
-    {
-      uint32_t s[64];
-      MSA_TMEM_LD64(tmem + ((uint32_t)(32 * warp) << 16), s);
-      tmem_ld_wait();
+      // this lane's columns: sum P (ln P - S^idx), sum P, student max / sum (log2 domain)
+      const float invG = 1.f / (float)G, log2G = __log2f((float)G);
+      float C = 0.f, W = 0.f, mx = -1e30f, l = 0.f;
 #pragma unroll
-      for (int c = 0; c < 64; c += 2) {
-        float x0, x1;
-        ffma2(x0, x1, __uint_as_float(s[c]), __uint_as_float(s[c + 1]), scale_log2, scale_log2,
-              -lse2, -lse2);
-        a[c] = c <= cmax ? ex2(x0) : 0.f;
-        a[c + 1] = c + 1 <= cmax ? ex2(x1) : 0.f;
+      for (int c = 0; c < kCpl; ++c)
+        if (cb + c <= cmax) mx = fmaxf(mx, si[c] * idx_scale * kLog2e);
+#pragma unroll
+      for (int c = 0; c < kCpl; ++c) {
+        if (cb + c <= cmax) {
+          const float x2 = si[c] * idx_scale * kLog2e;
+          l += ex2(x2 - mx);
+          const float P = a[c] * invG;
+          if (P > 0.f) C += P * ((__log2f(a[c]) - log2G) * kLn2 - si[c] * idx_scale);
+          W += P;
+        }
       }
-    }
-    lane_split<G, true>(a, h);                             // a[c]: G * P of column kCpl*h + c
-    float si[64];
-    {
-      uint32_t s[64];
-      MSA_TMEM_LD64(tmem + ((uint32_t)(32 * warp) << 16) + 64, s);
-      tmem_ld_wait();
+      // combine the entry's G lanes; its first lane writes the partial
 #pragma unroll
-      for (int c = 0; c < 64; ++c) si[c] = __uint_as_float(s[c]);
-    }
-    lane_split<G, false>(si, h);                           // si[c]: raw S^idx of the same column
-    tc_fence_before();
-
-    // ---- this lane's columns: sum P (ln P - S^idx), sum P, student max / sum (log2 domain)
-    const int cb = kCpl * h;
-    const float invG = 1.f / (float)G, log2G = __log2f((float)G);
-    float C = 0.f, W = 0.f, mx = -1e30f, l = 0.f;
-#pragma unroll
-    for (int c = 0; c < kCpl; ++c)
-      if (cb + c <= cmax) mx = fmaxf(mx, si[c] * idx_scale * kLog2e);
-#pragma unroll
-    for (int c = 0; c < kCpl; ++c) {
-      if (cb + c <= cmax) {
-        const float x2 = si[c] * idx_scale * kLog2e;
-        l += ex2(x2 - mx);
-        const float P = a[c] * invG;
-        if (P > 0.f) C += P * ((__log2f(a[c]) - log2G) * kLn2 - si[c] * idx_scale);
-        W += P;
+      for (int m = 1; m < G; m <<= 1) {
+        C += __shfl_xor_sync(0xffffffffu, C, m);
+        W += __shfl_xor_sync(0xffffffffu, W, m);
+        const float mo = __shfl_xor_sync(0xffffffffu, mx, m);
+        const float lo = __shfl_xor_sync(0xffffffffu, l, m);
+        const float nm = fmaxf(mx, mo);
+        l = l * ex2(mx - nm) + lo * ex2(mo - nm);
+        mx = nm;
       }
+      if (rv && h == 0)
+        part[((int64_t)r * N + (cur_ent >> 6)) * kk + (cur_ent & 63)] = make_float4(C, W, mx, l);
+      c_bkt = n_bkt;
+      c_e0 = n_e0;
+      c_ne = n_ne;
     }
-    // ---- combine the entry's G lanes; its first lane writes the partial
-#pragma unroll
-    for (int m = 1; m < G; m <<= 1) {
-      C += __shfl_xor_sync(0xffffffffu, C, m);
-      W += __shfl_xor_sync(0xffffffffu, W, m);
-      const float mo = __shfl_xor_sync(0xffffffffu, mx, m);
-      const float lo = __shfl_xor_sync(0xffffffffu, l, m);
-      const float nm = fmaxf(mx, mo);
-      l = l * ex2(mx - nm) + lo * ex2(mo - nm);
-      mx = nm;
-    }
-    if (rv && h == 0) {
-      const int64_t i = ent >> 6;
-      part[((int64_t)r * N + i) * kk + (ent & 63)] = make_float4(C, W, mx, l);
-    }
-    __syncthreads();                                       // TMEM read before the next MMA
-    bucket = n_bucket;
-    next_off = n_next;
-    e0 = n_e0;
-    n_e = n_ne;
-  }
-  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
-  if (G == 8 && !ok && tid == 0) {
-    // a wait gave up: let this tile's Q copies land before the CTA exits (the phase of the
-    // last wait on q_bar; it returns at once if that wait had succeeded)
-    mbar_wait(q_bar, qphase ^ 1u, &g_kl_status);
   }
   __syncthreads();
-  if (warp == 0) {
+  if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, L::kTmemCols);
+    tmem_dealloc(tmem, 512);
   }
 }
 
@@ -467,9 +640,12 @@ cudaError_t launch_kl_loss_fwd(const void* q, const void* k, const void* q_idx, 
                                                  entries);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
-  CUtensorMap tq;
-  e = make_tma_3d_bf16(&tq, q, (uint64_t)d_h, (uint64_t)H_q, (uint64_t)N, 64, G, 1, 128);
-  if (e != cudaSuccess) return e;
+  KlQMaps tq;
+  for (int m = 0; m < 5; ++m) {
+    e = make_tma_3d_bf16(&tq.m[m], q, (uint64_t)d_h, (uint64_t)H_q, (uint64_t)N, 64, G, 1 << m,
+                         128);
+    if (e != cudaSuccess) return e;
+  }
   int dev = 0, sms = 0;
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
@@ -483,19 +659,18 @@ cudaError_t launch_kl_loss_fwd(const void* q, const void* k, const void* q_idx, 
   auto run = [&](auto kern, int smem) -> cudaError_t {
     cudaError_t x = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (x != cudaSuccess) return x;
-    const int grid = kKlCtasPerSm * sms;                   // persistent: 3 CTAs per SM
-    kern<<<grid, kKlThreads, smem, st>>>(tq, qq, kp, qi, ki, lse, entries, offset, tile_off, nb,
+    const int grid = sms;                                  // persistent: one CTA per SM
+    kern<<<grid, kKlWsThreads, smem, st>>>(tq, qq, kp, qi, ki, lse, entries, offset, tile_off, nb,
                                          nblk, N, H_kv, d_idx, kk, part, scale_log2, idx_scale);
     return cudaGetLastError();
   };
   auto dispatch_g = [&](auto dh) -> cudaError_t {
     constexpr int D = decltype(dh)::value;
-    const int smem = KlSmem<D>::kAlloc;
     switch (G) {
-      case 1: return run(k_kl_kvouter<D, 1>, smem);
-      case 2: return run(k_kl_kvouter<D, 2>, smem);
-      case 4: return run(k_kl_kvouter<D, 4>, smem);
-      default: return run(k_kl_kvouter<D, 8>, smem);
+      case 1: return run(k_kl_kvouter<D, 1>, KlSmem<D, 1>::kAlloc);
+      case 2: return run(k_kl_kvouter<D, 2>, KlSmem<D, 2>::kAlloc);
+      case 4: return run(k_kl_kvouter<D, 4>, KlSmem<D, 4>::kAlloc);
+      default: return run(k_kl_kvouter<D, 8>, KlSmem<D, 8>::kAlloc);
     }
   };
   e = d_h == 128 ? dispatch_g(std::integral_constant<int, 128>())
