@@ -185,10 +185,12 @@ struct KlQMaps {
   CUtensorMap m[5];
 };
 
-// Warp roles: warps 0 and 10 load (warp 0 the query rows, warp 10 the keys and index queries),
-// warp 1 issues the MMAs, warps 2..9 are two epilogue groups of four (one warp per TMEM lane
-// quarter) that take alternate work tiles.
-constexpr int kKlWarps = 11;
+// Warp roles: warps 0 and 11.. load the query rows (their TMA boxes dealt round-robin: a warp
+// issues one box at a time, so several warps keep more of them in flight), warp 10 loads the
+// keys and index queries, warp 1 issues the MMAs, warps 2..9 are two epilogue groups of four
+// (one warp per TMEM lane quarter) that take alternate work tiles.
+constexpr int kKlQWarps = 4;
+constexpr int kKlWarps = 10 + 1 + (kKlQWarps - 1);
 constexpr int kKlWsThreads = 32 * kKlWarps;
 
 template <int D_H, int G>
@@ -276,9 +278,12 @@ __global__ void __launch_bounds__(kKlWsThreads, 1)
   };
   auto fail = [&]() { *s_abort = 1; };
 
-  if (warp == 0 || warp == kKlWarps - 1) {
-    // ------------------------------------------------------------ producers (two warps)
-    const bool pq = warp == 0;                             // query rows; else keys, index queries
+  if (warp == 0 || warp == 10 || (warp >= 11 && G == 8)) {
+    // ------------------------------------------------------------ producers
+    const bool pq = warp != 10;                            // query rows; else keys, index queries
+    const int qw = warp == 0 ? 0 : warp - 10;              // index among the query-row warps
+    // each producer warp keeps its own copy of the tile's entries (in registers, or in shared
+    // memory for the index-query warp)
     int* s_pw = s_pent + (pq ? 0 : kKlRows);
     int bkt = bucket0, nxt = next0;
     int last_bkt = -1, kfill = 0, issued = 0;
@@ -339,17 +344,21 @@ __global__ void __launch_bounds__(kKlWsThreads, 1)
         break;
       }
       const uint32_t qbase = sb + L::kOffQ + s * L::kQStage;
-      __syncwarp();                                        // the previous tile's reads are done
+      const int my_ent = pre[0];                           // entry `lane` (G = 8: <= 16 entries)
+      if (!(pq && G == 8)) {                               // cp.async paths read them from smem
+        __syncwarp();                                      // the previous tile's reads are done
 #pragma unroll
-      for (int m = 0; m < kEntPerLane; ++m)
-        if (lane + 32 * m < kEpt) s_pw[lane + 32 * m] = pre[m];
-      __syncwarp();
+        for (int m = 0; m < kEntPerLane; ++m)
+          if (lane + 32 * m < kEpt) s_pw[lane + 32 * m] = pre[m];
+        __syncwarp();
+      }
       if (j + 1 < ntiles) load_ents(j + 1);                // lands while this tile is issued
       if (pq && G == 8) {
         // runs of consecutive query rows: the lane at the start of a run issues its boxes
-        if (lane == 0) mbar_expect_tx(q_full(s), (uint32_t)(n_e * 8 * 128 * L::kHalves));
+        if (warp == 0 && lane == 0)
+          mbar_expect_tx(q_full(s), (uint32_t)(n_e * 8 * 128 * L::kHalves));
         __syncwarp();
-        const int row = lane < n_e ? (s_pw[lane] >> 6) : -2;
+        const int row = lane < n_e ? (my_ent >> 6) : -2;
         const int prev = __shfl_up_sync(0xffffffffu, row, 1);
         const bool start = lane < n_e && (lane == 0 || prev != row - 1);
         const unsigned starts = __ballot_sync(0xffffffffu, start);
@@ -360,10 +369,13 @@ __global__ void __launch_bounds__(kKlWsThreads, 1)
           while (off < stop - lane) {
             const int rem = stop - lane - off;
             const int m = rem >= 16 ? 4 : rem >= 8 ? 3 : rem >= 4 ? 2 : rem >= 2 ? 1 : 0;
+            // the boxes are dealt round-robin over the query-row warps by (first entry, half);
+            // every such warp computes the same decomposition
 #pragma unroll
             for (int bx = 0; bx < L::kHalves; ++bx)
-              tma_load_3d(qbase + bx * L::kQHalf + (lane + off) * 1024, &tm_q.m[m], q_full(s),
-                          64 * bx, rb * 8, row + off);
+              if (((lane + off) * L::kHalves + bx) % kKlQWarps == qw)
+                tma_load_3d(qbase + bx * L::kQHalf + (lane + off) * 1024, &tm_q.m[m], q_full(s),
+                            64 * bx, rb * 8, row + off);
             off += 1 << m;
           }
         }
@@ -446,7 +458,7 @@ __global__ void __launch_bounds__(kKlWsThreads, 1)
       if (issued > 0)
         mbar_wait(t_full((issued - 1) % kTStages), ((issued - 1) / kTStages) & 1, &g_kl_status);
     }
-  } else {
+  } else if (warp >= 2 && warp <= 9) {
     // ------------------------------------------------------------ epilogue groups
     const int grp = (warp - 2) >> 2;
     const int qd = warp & 3;                               // TMEM lane quarter of this warp
