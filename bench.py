@@ -112,10 +112,14 @@ NCU_ROWS = {"k_index_block_scores": "index_branch",
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.txt")
 
 
+DEFAULT_WORKLOAD = True   # cleared by run_msa for any other prefill/decode workload
+
+
 def ncu_traffic(kernel):
     """DRAM bytes per call of a bench row from the last full-size ncu capture, if the row's
-    kernel sources are unchanged since (profiles/traffic.txt records the source hash)."""
-    if not os.path.exists(TRAFFIC_FILE):
+    kernel sources are unchanged since (profiles/traffic.txt records the source hash) and the
+    bench runs the workload that capture was taken on."""
+    if not DEFAULT_WORKLOAD or not os.path.exists(TRAFFIC_FILE):
         return None
     for line in open(TRAFFIC_FILE):
         f = line.split()
@@ -264,6 +268,8 @@ def bench_config(pcfg, dcfg, world):
 
 
 def run_msa(args, world, rank, local):
+    global DEFAULT_WORKLOAD
+    DEFAULT_WORKLOAD = args.prefill == "p128k" and not args.prefill_n and args.decode == "decode"
     pcfg = gen.CONFIGS[args.prefill]
     if args.prefill_n:
         pcfg = gen.PrefillConfig(**{**pcfg.__dict__, "N": args.prefill_n})

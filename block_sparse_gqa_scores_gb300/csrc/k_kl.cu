@@ -228,8 +228,9 @@ __global__ void __launch_bounds__(kKlWsThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kQStages; ++s) {
       // warp 0's arrive (with the TMA transaction bytes at G = 8), warp 10's 32 lanes' copies,
-      // and warp 0's 32 lanes' copies when the query rows also come by cp.async
-      mbar_init(q_full(s), G == 8 ? 33 : 65);
+      // and at G = 8 one arrive of each other query-row warp (so that none of them can fall a
+      // full phase behind when a tile gives it no box), else warp 0's 32 lanes' copies
+      mbar_init(q_full(s), G == 8 ? 33 + (kKlQWarps - 1) : 65);
       mbar_init(q_empty(s), 1);              // MMA commit
     }
     for (int s = 0; s < kKStages; ++s) {
@@ -379,6 +380,8 @@ __global__ void __launch_bounds__(kKlWsThreads, 1)
             off += 1 << m;
           }
         }
+        __syncwarp();
+        if (warp != 0 && lane == 0) mbar_arrive(q_full(s));   // after this warp's boxes
       } else if (pq) {
         if (lane == 0) mbar_arrive(q_full(s));             // no transaction bytes
         for (int x = lane; x < n_e * G * kChunks; x += 32) {
