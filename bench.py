@@ -6,8 +6,8 @@ A step is one pass of the whole hot path over one batch of synthetic input:
   branch; H_q=32, H_kv=4, d_h=128, d_idx=64, block 64, k=16, 8 hot blocks), then
   decode of 32 sequences with cache lengths ~ U[65536, 262144] (same head layout).
 `value` is prefill tokens/s (N / prefill device time); decode tokens/s is reported beside it, and
-the forward of the KL alignment loss (on the step's selection and LSE) is timed after the steps,
-outside `value`.
+the forward of the KL alignment loss (on the step's selection and LSE) and the decode of the same
+batch from a paged KV cache are timed after the steps, outside `value`.
 Inputs stay resident in HBM; every timed input (M alone is 4.3 GB, the decode caches 11.5 GB)
 is larger than the 129 MB L2, so no flush is needed.
 
@@ -375,6 +375,8 @@ def run_msa(args, world, rank, local):
     }
     if not args.no_kl:
         line["kl_loss_fwd"] = time_kl(msa, pcfg, x, bufs, K, sizes, pk, world)
+    if d is not None and not args.no_paged:
+        line["decode_paged"] = time_decode_paged(msa, dcfg, d, dbufs, K, sizes, pk, world)
     if not args.no_e2e:
         line["e2e"] = e2e_prefill(msa, pcfg, x, bufs, K, W, world)
     if not args.no_cpu_baseline and rank == 0 and world == 1:
@@ -412,6 +414,40 @@ def time_kl(msa, pcfg, x, bufs, K, sizes, pk, world):
             "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": pk["bf16_sust"],
                          "unit": "TFLOP/s", "frac": round(achieved / pk["bf16_sust"], 4),
                          "traffic": ncu_traffic("kl_loss_fwd"), "algorithmic": sizes["F_kl"]}}
+
+
+def time_decode_paged(msa, dcfg, d, dbufs, K, sizes, pk, world):
+    """Decode of the same batch from a paged cache (the tokens in shuffled 64-token pages),
+    timed apart from the step: K calls after 3 warm-up calls."""
+    kp, vp, kip, pt, sl = gen.to_pages(d, seed=1)
+    max_len = min(dbufs["max_len"], 64 * pt.shape[1])
+    o, lse = torch.empty_like(dbufs["o"]), torch.empty_like(dbufs["lse"])
+    idx = torch.empty_like(dbufs["idx"])
+
+    def call():
+        msa.msa_sparse_decode_paged(d["q"], d["q_idx"], kp, vp, kip, pt, sl, max_len, dcfg.k,
+                                    o=o, lse=lse, idx_out=idx, ws=dbufs["ws"])
+
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(K + 1)]
+    evs[0].record(stream)
+    for s in range(K):
+        call()
+        evs[s + 1].record(stream)
+    torch.cuda.synchronize()
+    msa.msa_device_status()
+    same = bool(torch.equal(o, dbufs["o"]) and torch.equal(idx, dbufs["idx"]))
+    del kp, vp, kip
+    ms = max_over_ranks(float(np.mean([evs[s].elapsed_time(evs[s + 1]) for s in range(K)])), world)
+    achieved = sizes["decode_bytes"] / (ms * 1e-3) / 1e9
+    return {"ms": round(ms, 4), "value": round(world * dcfg.S / (ms * 1e-3), 1),
+            "unit": "tokens/s", "equals_packed": same, "gpu_launches_per_call": DECODE_LAUNCHES,
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": pk["hbm"],
+                         "unit": "GB/s", "frac": round(achieved / pk["hbm"], 4),
+                         "algorithmic": sizes["decode_bytes"]}}
 
 
 def e2e_prefill(msa, pcfg, x, bufs, K, W, world):
@@ -544,6 +580,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-kl", action="store_true", help="skip the KL loss forward measurement")
+    ap.add_argument("--no-paged", action="store_true",
+                    help="skip the paged-cache decode measurement")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--write-traffic", metavar="NCU_CSV",
                     help="write profiles/traffic.txt from an ncu CSV of whole steps and exit")

@@ -206,13 +206,52 @@ MSA_API msa_status_t msa_sparse_decode(const void* q, const void* q_idx, const v
   float* part_o = reinterpret_cast<float*>(base + w.off_po);
   float* part_lse = reinterpret_cast<float*>(base + w.off_pl);
   const int64_t nblk = (max_len + 63) / 64;
-  cudaError_t e = msa::launch_decode_block_scores(q_idx, k_idx_cache, cu_seqlens, Mdec, S, H_kv,
+  const msa::CacheMap cm{cu_seqlens, nullptr, nullptr, 0, 0};
+  cudaError_t e = msa::launch_decode_block_scores(q_idx, k_idx_cache, cm, Mdec, S, H_kv,
                                                   d_idx, max_len, nblk, st);
   if (e != cudaSuccess) return MSA_ERR_CUDA;
-  e = msa::launch_select_decode(Mdec, idx, cu_seqlens, S, H_kv, k, max_len, nblk, st);
+  e = msa::launch_select_decode(Mdec, idx, cm, S, H_kv, k, max_len, nblk, st);
   if (e != cudaSuccess) return MSA_ERR_CUDA;
-  e = msa::launch_sparse_attn_decode(q, k_cache, v_cache, idx, cu_seqlens, S, max_len, H_q, H_kv,
+  e = msa::launch_sparse_attn_decode(q, k_cache, v_cache, idx, cm, S, max_len, H_q, H_kv,
                                      d_h, k, w.nsplit, part_o, part_lse, o, lse, st);
+  return from_cuda(e);
+}
+
+MSA_API msa_status_t msa_sparse_decode_paged(
+    const void* q, const void* q_idx, const void* k_pages, const void* v_pages,
+    const void* k_idx_pages, const int32_t* page_table, const int64_t* seq_lens, int S,
+    int64_t max_pages, int64_t num_pages, int64_t max_len, int H_q, int H_kv, int d_h, int d_idx,
+    int block_size, int k, void* o, float* lse, int32_t* idx_out, void* ws, size_t ws_bytes,
+    void* stream) {
+  if (!aligned16(q) || !aligned16(q_idx) || !aligned16(k_pages) || !aligned16(v_pages) ||
+      !aligned16(k_idx_pages) || !aligned4(page_table) || !seq_lens ||
+      ((uintptr_t)seq_lens & 7u) || !aligned16(o) || !aligned4(lse) ||
+      (idx_out && !aligned4(idx_out)) || !aligned16(ws))
+    return MSA_ERR_INVALID_ARGUMENT;
+  if (S < 1 || S > 65535 || max_len < 1 || H_q < 1 || H_kv < 1 || H_q % H_kv != 0 ||
+      block_size != 64 || k < 1 || k > 64 || d_h < 1 || d_idx < 1 || num_pages < 1 ||
+      max_pages < 1 || max_pages * 64 < max_len)
+    return MSA_ERR_INVALID_ARGUMENT;
+  if (!pow2_upto(H_kv, 8) || !pow2_upto(H_q / H_kv, 8) || (d_h != 64 && d_h != 128) ||
+      (d_idx != 32 && d_idx != 64))
+    return MSA_ERR_UNSUPPORTED;
+  const DecodeWs w = decode_layout(S, max_len, H_q, H_kv, d_h, k);
+  if (ws_bytes < w.total) return MSA_ERR_WORKSPACE;
+  cudaStream_t st = (cudaStream_t)stream;
+  char* base = static_cast<char*>(ws);
+  float* Mdec = reinterpret_cast<float*>(base + w.off_m);
+  int32_t* idx = idx_out ? idx_out : reinterpret_cast<int32_t*>(base + w.off_idx);
+  float* part_o = reinterpret_cast<float*>(base + w.off_po);
+  float* part_lse = reinterpret_cast<float*>(base + w.off_pl);
+  const int64_t nblk = (max_len + 63) / 64;
+  const msa::CacheMap cm{nullptr, page_table, seq_lens, max_pages, num_pages};
+  cudaError_t e = msa::launch_decode_block_scores(q_idx, k_idx_pages, cm, Mdec, S, H_kv, d_idx,
+                                                  max_len, nblk, st);
+  if (e != cudaSuccess) return MSA_ERR_CUDA;
+  e = msa::launch_select_decode(Mdec, idx, cm, S, H_kv, k, max_len, nblk, st);
+  if (e != cudaSuccess) return MSA_ERR_CUDA;
+  e = msa::launch_sparse_attn_decode(q, k_pages, v_pages, idx, cm, S, max_len, H_q, H_kv, d_h, k,
+                                     w.nsplit, part_o, part_lse, o, lse, st);
   return from_cuda(e);
 }
 

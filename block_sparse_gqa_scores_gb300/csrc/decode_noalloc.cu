@@ -78,12 +78,13 @@ extern "C" __attribute__((visibility("default"))) msa_status_t msa_sparse_decode
   float* part_o = reinterpret_cast<float*>(base + w.off_po);
   float* part_lse = reinterpret_cast<float*>(base + w.off_pl);
   const int64_t nblk = (max_len + 63) / 64;
-  cudaError_t e = msa::launch_decode_block_scores(q_idx, k_idx_cache, cu_seqlens, Mdec, S, H_kv,
+  const msa::CacheMap cm{cu_seqlens, nullptr, nullptr, 0, 0};
+  cudaError_t e = msa::launch_decode_block_scores(q_idx, k_idx_cache, cm, Mdec, S, H_kv,
                                                   d_idx, max_len, nblk, st);
   if (e != cudaSuccess) return MSA_ERR_CUDA;
-  e = msa::launch_select_decode(Mdec, idx, cu_seqlens, S, H_kv, k, max_len, nblk, st);
+  e = msa::launch_select_decode(Mdec, idx, cm, S, H_kv, k, max_len, nblk, st);
   if (e != cudaSuccess) return MSA_ERR_CUDA;
-  e = msa::launch_sparse_attn_decode(q, k_cache, v_cache, idx, cu_seqlens, S, max_len, H_q, H_kv,
+  e = msa::launch_sparse_attn_decode(q, k_cache, v_cache, idx, cm, S, max_len, H_q, H_kv,
                                      d_h, k, w.nsplit, part_o, part_lse, o, lse, st);
   return e == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
 }

@@ -41,13 +41,13 @@ struct AttnParams {
   const int32_t* idx;
   float* part_o;      // decode split partials [S*H_kv*nsplit, G, D_H] (normalised)
   float* part_lse;    // decode split partials [S*H_kv*nsplit, G] (log2 units)
-  const int64_t* cu;  // cumulative sequence lengths
+  CacheMap cm;        // where each sequence's cache rows are (packed or paged)
   int64_t max_len;    // length bound
   int H_q, H_kv, G, kk, nsplit, S;
   float scale_log2;   // log2(e) / sqrt(d_h)
 };
 
-template <int D_H>
+template <int D_H, bool PAGED>
 __global__ void __launch_bounds__(32 * kWarps) k_sparse_attn(const AttnParams p) {
   constexpr int KS = D_H / 16;             // k-steps of S^T, m-tiles of O^T
   constexpr int KCH = D_H / 32;            // 16-B K chunks per thread per key row
@@ -63,9 +63,11 @@ __global__ void __launch_bounds__(32 * kWarps) k_sparse_attn(const AttnParams p)
   const int64_t sr = unit / p.nsplit;
   const int64_t s = sr / p.H_kv;
   const int r = (int)(sr - s * p.H_kv);
-  const int64_t tok0 = p.cu[s];             // first cache row of the sequence
-  int64_t L = p.cu[s + 1] - tok0;
-  L = L < 1 ? 1 : (L > p.max_len ? p.max_len : L);
+  const int64_t L = p.cm.len<PAGED>(s, p.max_len);
+  const int64_t srow = p.cm.seq_row<PAGED>(s);
+  const int64_t kv_stride = (int64_t)p.H_kv * D_H;          // elements between tokens
+  const __nv_bfloat16* kseq = p.k + (srow * p.H_kv + r) * D_H;   // packed: the sequence's rows
+  const __nv_bfloat16* vseq = p.v + (srow * p.H_kv + r) * D_H;
   const int64_t i = L - 1;                  // the new token's position
   const int32_t* sel = p.idx + sr * p.kk;
   const __nv_bfloat16* qrow = p.q + s * (int64_t)p.H_q * D_H;
@@ -97,13 +99,18 @@ __global__ void __launch_bounds__(32 * kWarps) k_sparse_attn(const AttnParams p)
   float m_run[2] = {-INFINITY, -INFINITY};
   float l_run[2] = {0.f, 0.f};
 
-  const int64_t kv_stride = (int64_t)p.H_kv * D_H;          // elements between tokens
-  const __nv_bfloat16* kbase = p.k + (tok0 * p.H_kv + r) * D_H;
-  const __nv_bfloat16* vbase = p.v + (tok0 * p.H_kv + r) * D_H;
 
   for (int t = t0; t < t1; ++t) {
     const int b = __ldg(sel + t);
     if (b < 0) continue;
+    // keys are indexed by position; a paged block's rows are shifted to its page
+    const __nv_bfloat16* kbase = kseq;
+    const __nv_bfloat16* vbase = vseq;
+    if (PAGED) {
+      const int64_t shift = (p.cm.block_row<true>(s, b, 0) - (int64_t)b * kBlock) * p.H_kv * D_H;
+      kbase = p.k + shift + r * D_H;
+      vbase = p.v + shift + r * D_H;
+    }
     const int64_t j0 = (int64_t)b * kBlock + 16 * warp;     // first key of this warp's slice
     const int64_t jlo = j0 + r4, jhi = j0 + r4 + 8;
     const bool vlo = jlo <= i, vhi = jhi <= i;
@@ -293,7 +300,7 @@ __global__ void __launch_bounds__(128) k_decode_merge(const float* __restrict__ 
 }  // namespace
 
 cudaError_t launch_sparse_attn_decode(const void* q, const void* k_cache, const void* v_cache,
-                                      const int32_t* idx, const int64_t* cu, int S,
+                                      const int32_t* idx, const CacheMap& cm, int S,
                                       int64_t max_len, int H_q, int H_kv, int d_h, int kk,
                                       int nsplit, float* part_o, float* part_lse, void* o,
                                       float* lse, cudaStream_t stream) {
@@ -302,7 +309,7 @@ cudaError_t launch_sparse_attn_decode(const void* q, const void* k_cache, const 
   p.k = static_cast<const __nv_bfloat16*>(k_cache);
   p.v = static_cast<const __nv_bfloat16*>(v_cache);
   p.idx = idx;
-  p.cu = cu;
+  p.cm = cm;
   p.part_o = part_o;
   p.part_lse = part_lse;
   p.max_len = max_len;
@@ -316,11 +323,17 @@ cudaError_t launch_sparse_attn_decode(const void* q, const void* k_cache, const 
   const int64_t grid = (int64_t)S * H_kv * nsplit;
   const int64_t mgrid = (int64_t)S * H_kv;
   if (d_h == 128) {
-    k_sparse_attn<128><<<(unsigned)grid, 32 * kWarps, 0, stream>>>(p);
+    if (cm.pages)
+      k_sparse_attn<128, true><<<(unsigned)grid, 32 * kWarps, 0, stream>>>(p);
+    else
+      k_sparse_attn<128, false><<<(unsigned)grid, 32 * kWarps, 0, stream>>>(p);
     k_decode_merge<128><<<(unsigned)mgrid, 128, 0, stream>>>(
         part_o, part_lse, static_cast<__nv_bfloat16*>(o), lse, H_q, H_kv, p.G, nsplit);
   } else {
-    k_sparse_attn<64><<<(unsigned)grid, 32 * kWarps, 0, stream>>>(p);
+    if (cm.pages)
+      k_sparse_attn<64, true><<<(unsigned)grid, 32 * kWarps, 0, stream>>>(p);
+    else
+      k_sparse_attn<64, false><<<(unsigned)grid, 32 * kWarps, 0, stream>>>(p);
     k_decode_merge<64><<<(unsigned)mgrid, 128, 0, stream>>>(
         part_o, part_lse, static_cast<__nv_bfloat16*>(o), lse, H_q, H_kv, p.G, nsplit);
   }

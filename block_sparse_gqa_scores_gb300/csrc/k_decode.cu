@@ -7,7 +7,9 @@
 // 16 tokens with the H_kv <= 8 index heads are one m16n8k16 MMA per 16 dims (tokens on M,
 // heads on N), with the index-key rows loaded from global memory straight into A fragments
 // as 16-byte vectors (the contracted dim is permuted the same way in the q_idx fragment).
-// Every token of the cache is visible to the last row, so only the cache end is masked.
+// Every token of the cache is visible to the last row, so only the cache end is masked.  The
+// cache is packed or paged (CacheMap): a 64-token block is contiguous either way, so a warp finds
+// the cache row of its block once and reads the block's rows from there.
 #include <math.h>
 
 #include "msa_device.cuh"
@@ -20,10 +22,10 @@ constexpr int kDecWarps = 4;
 constexpr int kChunkTokens = 1024;
 constexpr unsigned kFull = 0xffffffffu;
 
-template <int D_IDX>
+template <int D_IDX, bool PAGED>
 __global__ void __launch_bounds__(32 * kDecWarps)
     k_decode_block_scores(const __nv_bfloat16* __restrict__ q_idx,
-                          const __nv_bfloat16* __restrict__ k_idx, const int64_t* __restrict__ cu,
+                          const __nv_bfloat16* __restrict__ k_idx, const CacheMap cm,
                           float* __restrict__ Mdec, int H_kv, int64_t max_len, int64_t nblk_max,
                           float scale) {
   constexpr int KS = D_IDX / 16;           // k-steps
@@ -31,9 +33,8 @@ __global__ void __launch_bounds__(32 * kDecWarps)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int c = lane & 3, r4 = lane >> 2;
   const int64_t s = blockIdx.y;
-  const int64_t tok0 = cu[s];
-  int64_t L = cu[s + 1] - tok0;
-  L = L < 1 ? 1 : (L > max_len ? max_len : L);
+  const int64_t L = cm.len<PAGED>(s, max_len);
+  const __nv_bfloat16* kseq = k_idx + cm.seq_row<PAGED>(s) * D_IDX;   // packed: the sequence
   const int64_t first = (int64_t)blockIdx.x * kChunkTokens;
   if (first >= L) return;
   const int64_t last_blk = (L - 1) >> 6;
@@ -52,11 +53,12 @@ __global__ void __launch_bounds__(32 * kDecWarps)
         qf[ks][hl] = valid ? qh[d >> 1] : 0u;
       }
   }
-  const __nv_bfloat16* kb = k_idx + tok0 * D_IDX;
-
   for (int64_t b = (first >> 6) + warp; b <= last_blk && b < ((first + kChunkTokens) >> 6);
        b += kDecWarps) {
     float best[2] = {-INFINITY, -INFINITY};          // heads 2c, 2c+1
+    // token rows: packed, from the sequence's first row; paged, from the block's page
+    const __nv_bfloat16* kb =
+        PAGED ? k_idx + (cm.block_row<true>(s, b, 0) - b * kBlock) * D_IDX : kseq;
 #pragma unroll
     for (int mt = 0; mt < 4; ++mt) {
       const int64_t jlo = b * kBlock + 16 * mt + r4, jhi = jlo + 8;
@@ -102,18 +104,20 @@ __global__ void __launch_bounds__(32 * kDecWarps)
 }  // namespace
 
 cudaError_t launch_decode_block_scores(const void* q_idx, const void* k_idx_cache,
-                                       const int64_t* cu, float* Mdec, int S, int H_kv, int d_idx,
+                                       const CacheMap& cm, float* Mdec, int S, int H_kv, int d_idx,
                                        int64_t max_len, int64_t nblk_max, cudaStream_t stream) {
   const dim3 grid((unsigned)((max_len + kChunkTokens - 1) / kChunkTokens), (unsigned)S);
   const float scale = (float)(1.0 / sqrt((double)d_idx));
   const auto* q = static_cast<const __nv_bfloat16*>(q_idx);
   const auto* kc = static_cast<const __nv_bfloat16*>(k_idx_cache);
-  if (d_idx == 64)
-    k_decode_block_scores<64><<<grid, 32 * kDecWarps, 0, stream>>>(q, kc, cu, Mdec, H_kv, max_len,
-                                                                  nblk_max, scale);
-  else
-    k_decode_block_scores<32><<<grid, 32 * kDecWarps, 0, stream>>>(q, kc, cu, Mdec, H_kv, max_len,
-                                                                  nblk_max, scale);
+  auto run = [&](auto kern) {
+    kern<<<grid, 32 * kDecWarps, 0, stream>>>(q, kc, cm, Mdec, H_kv, max_len, nblk_max, scale);
+  };
+  if (cm.pages) {
+    if (d_idx == 64) run(k_decode_block_scores<64, true>); else run(k_decode_block_scores<32, true>);
+  } else {
+    if (d_idx == 64) run(k_decode_block_scores<64, false>); else run(k_decode_block_scores<32, false>);
+  }
   return cudaGetLastError();
 }
 

@@ -160,15 +160,14 @@ __global__ void __launch_bounds__(32 * kSelWarps)
 
 __global__ void __launch_bounds__(32 * kSelWarps)
     k_select_decode(const float* __restrict__ Mdec, int32_t* __restrict__ idx,
-                    const int64_t* __restrict__ cu, int S, int H_kv, int k, int64_t max_len,
+                    const CacheMap cm, int S, int H_kv, int k, int64_t max_len,
                     int64_t nblk_max) {
   __shared__ SelScratch sc[kSelWarps];
   const int warp = threadIdx.x >> 5;
   const int64_t row = (int64_t)blockIdx.x * kSelWarps + warp;   // row = s*H_kv + r
   if (row >= (int64_t)S * H_kv) return;
   const int64_t s = row / H_kv;
-  int64_t L = cu[s + 1] - cu[s];
-  L = L < 1 ? 1 : (L > max_len ? max_len : L);
+  const int64_t L = cm.pages ? cm.len<true>(s, max_len) : cm.len<false>(s, max_len);
   select_row(Mdec + row * nblk_max, (L - 1) >> 6, k, idx + row * k, sc[warp]);
 }
 
@@ -184,12 +183,12 @@ cudaError_t launch_select_prefill(const float* M, int32_t* idx, int64_t N, int H
   return cudaGetLastError();
 }
 
-cudaError_t launch_select_decode(const float* Mdec, int32_t* idx, const int64_t* cu, int S,
+cudaError_t launch_select_decode(const float* Mdec, int32_t* idx, const CacheMap& cm, int S,
                                  int H_kv, int k, int64_t max_len, int64_t nblk_max,
                                  cudaStream_t stream) {
   const int64_t nrows = (int64_t)S * H_kv;
   const int64_t grid = (nrows + kSelWarps - 1) / kSelWarps;
-  k_select_decode<<<(unsigned)grid, 32 * kSelWarps, 0, stream>>>(Mdec, idx, cu, S, H_kv, k, max_len,
+  k_select_decode<<<(unsigned)grid, 32 * kSelWarps, 0, stream>>>(Mdec, idx, cm, S, H_kv, k, max_len,
                                                                  nblk_max);
   return cudaGetLastError();
 }

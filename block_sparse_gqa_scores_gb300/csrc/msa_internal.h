@@ -69,18 +69,50 @@ cudaError_t read_reset_kl_status(unsigned* out);
 
 cudaError_t launch_select_prefill(const float* M, int32_t* idx, int64_t N, int H_kv, int k,
                                   int64_t q_start, int64_t q_count, cudaStream_t stream);
-cudaError_t launch_select_decode(const float* Mdec, int32_t* idx, const int64_t* cu, int S,
+// Where a decode sequence's cache rows live.  Packed: sequence s is rows cu[s] .. cu[s+1]-1 of the
+// cache.  Paged: the cache is 64-token pages (one page per MSA block); token j of sequence s is
+// row j % 64 of page pages[s * max_pages + j / 64], and the sequence is lens[s] tokens long.
+// Lengths are clamped to [1, max_len] and page ids to [0, num_pages): a caller's bad value gives
+// wrong results, never an access outside the cache.
+struct CacheMap {
+  const int64_t* cu;        // packed (nullptr when paged)
+  const int32_t* pages;     // paged: [S, max_pages]
+  const int64_t* lens;      // paged: [S]
+  int64_t max_pages;
+  int64_t num_pages;
+#ifdef __CUDACC__
+  // The kernels are instantiated per layout (PAGED), so the packed path carries no paged code.
+  template <bool PAGED>
+  __device__ __forceinline__ int64_t len(int64_t s, int64_t max_len) const {
+    const int64_t L = PAGED ? __ldg(lens + s) : __ldg(cu + s + 1) - __ldg(cu + s);
+    return L < 1 ? 1 : (L > max_len ? max_len : L);
+  }
+  // first cache row of sequence s when packed (0 when paged); read once per sequence
+  template <bool PAGED>
+  __device__ __forceinline__ int64_t seq_row(int64_t s) const { return PAGED ? 0 : __ldg(cu + s); }
+  // cache row of token 64 * b of sequence s (the first token of its block b); row0 = seq_row(s)
+  template <bool PAGED>
+  __device__ __forceinline__ int64_t block_row(int64_t s, int64_t b, int64_t row0) const {
+    if (!PAGED) return row0 + b * 64;
+    int64_t pg = __ldg(pages + s * max_pages + b);
+    pg = pg < 0 ? 0 : (pg >= num_pages ? num_pages - 1 : pg);
+    return pg * 64;
+  }
+#endif
+};
+
+cudaError_t launch_select_decode(const float* Mdec, int32_t* idx, const CacheMap& cm, int S,
                                  int H_kv, int k, int64_t max_len, int64_t nblk_max,
                                  cudaStream_t stream);
 
 cudaError_t launch_sparse_attn_decode(const void* q, const void* k_cache, const void* v_cache,
-                                      const int32_t* idx, const int64_t* cu, int S,
+                                      const int32_t* idx, const CacheMap& cm, int S,
                                       int64_t max_len, int H_q, int H_kv, int d_h, int kk,
                                       int nsplit, float* part_o, float* part_lse, void* o,
                                       float* lse, cudaStream_t stream);
 
 cudaError_t launch_decode_block_scores(const void* q_idx, const void* k_idx_cache,
-                                       const int64_t* cu, float* Mdec, int S, int H_kv, int d_idx,
+                                       const CacheMap& cm, float* Mdec, int S, int H_kv, int d_idx,
                                        int64_t max_len, int64_t nblk_max, cudaStream_t stream);
 
 }  // namespace msa

@@ -46,11 +46,14 @@ def _load():
                                     P, P, sz, P]
     L.msa_sparse_decode_noalloc.argtypes = [P, P, P, P, P, P, i32, i64, i32, i32, i32, i32, i32,
                                             i32, P, P, P, P]
+    L.msa_sparse_decode_paged.argtypes = [P, P, P, P, P, P, P, i32, i64, i64, i64, i32, i32, i32,
+                                          i32, i32, i32, P, P, P, P, sz, P]
     L.msa_kl_loss_fwd_workspace.argtypes = [i64, i32, i32]
     L.msa_kl_loss_fwd_workspace.restype = sz
     L.msa_kl_loss_fwd.argtypes = [P, P, P, P, P, P, P, i64, i32, i32, i32, i32, i32, i32, P, sz, P]
     for fn in ("msa_index_block_scores", "msa_select_blocks", "msa_index_select", "msa_sparse_attn_fwd",
-               "msa_sparse_decode", "msa_sparse_decode_noalloc", "msa_kl_loss_fwd",
+               "msa_sparse_decode", "msa_sparse_decode_noalloc", "msa_sparse_decode_paged",
+               "msa_kl_loss_fwd",
                "msa_device_status"):
         getattr(L, fn).restype = i32
     return L
@@ -206,6 +209,36 @@ def msa_sparse_decode_noalloc(q, q_idx, k_cache, v_cache, k_idx_cache, cu_seqlen
         _ptr(q), _ptr(q_idx), _ptr(k_cache), _ptr(v_cache), _ptr(k_idx_cache), _ptr(cu_seqlens),
         S, max_len, H_q, H_kv, d_h, d_idx, block_size, k, _ptr(o), _ptr(lse), _ptr(idx_out),
         _stream(stream)))
+    return o, lse, idx_out
+
+
+def msa_sparse_decode_paged(q, q_idx, k_pages, v_pages, k_idx_pages, page_table, seq_lens,
+                            max_len, k, o=None, lse=None, idx_out=None, ws=None, block_size=BLOCK,
+                            stream=None):
+    """Decode from 64-token pages -> (O [S,H_q,d_h] bf16, LSE [S,H_q] fp32, idx [S,H_kv,k])."""
+    _req(q, torch.bfloat16, 3, "q")
+    _req(q_idx, torch.bfloat16, 3, "q_idx")
+    _req(k_pages, torch.bfloat16, 4, "k_pages")
+    _req(v_pages, torch.bfloat16, 4, "v_pages")
+    _req(k_idx_pages, torch.bfloat16, 3, "k_idx_pages")
+    _req(page_table, torch.int32, 2, "page_table")
+    _req(seq_lens, torch.int64, 1, "seq_lens")
+    S, H_q, d_h = q.shape
+    H_kv, d_idx = q_idx.shape[1], q_idx.shape[2]
+    num_pages, max_pages = k_pages.shape[0], page_table.shape[1]
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((S, H_q), dtype=torch.float32, device=q.device)
+    if idx_out is None:
+        idx_out = torch.empty((S, H_kv, k), dtype=torch.int32, device=q.device)
+    nws = msa_sparse_decode_workspace(S, max_len, H_q, H_kv, d_h, d_idx, k)
+    if ws is None:
+        ws = torch.empty(max(nws, 16), dtype=torch.uint8, device=q.device)
+    _check("msa_sparse_decode_paged", lib.msa_sparse_decode_paged(
+        _ptr(q), _ptr(q_idx), _ptr(k_pages), _ptr(v_pages), _ptr(k_idx_pages), _ptr(page_table),
+        _ptr(seq_lens), S, max_pages, num_pages, max_len, H_q, H_kv, d_h, d_idx, block_size, k,
+        _ptr(o), _ptr(lse), _ptr(idx_out), _ptr(ws), ws.numel(), _stream(stream)))
     return o, lse, idx_out
 
 

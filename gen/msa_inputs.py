@@ -27,7 +27,7 @@ import numpy as np
 import torch
 
 __all__ = [
-    "PrefillConfig", "DecodeConfig", "CONFIGS", "prefill_inputs", "decode_inputs",
+    "PrefillConfig", "DecodeConfig", "CONFIGS", "prefill_inputs", "decode_inputs", "to_pages",
     "to_bits", "from_bits", "bf16_bits_to_f64", "nblocks", "ceil_div", "BLOCK",
 ]
 
@@ -189,3 +189,38 @@ def nblocks(n: int, block: int = BLOCK) -> int:
 def ceil_div(a: int, b: int) -> int:
     return -(-a // b)
 
+
+def to_pages(d, seed, extra=3):
+    """Scatter a packed decode cache (rows cu_seqlens[s] .. cu_seqlens[s+1]-1 per sequence) into
+    64-token pages in a random order: `extra` unused pages, noise in the rows of a last page
+    past the sequence's end, and page-table entries past a sequence's last block set to an id
+    far out of range (they must never be read).  Layout only, no arithmetic of the method.
+    Returns (k_pages, v_pages, k_idx_pages, page_table [S, max_pages] int32, seq_lens int64)."""
+    cu = d["cu_seqlens"].cpu().numpy()
+    lens = cu[1:] - cu[:-1]
+    nb = (lens + 63) // 64
+    npages = int(nb.sum()) + extra
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed)
+    perm = torch.randperm(npages, generator=g, device="cuda").cpu().numpy()
+    kc, vc, kic = d["k_cache"], d["v_cache"], d["k_idx_cache"]
+    kp = torch.randn((npages * 64,) + tuple(kc.shape[1:]), generator=g, device="cuda").to(kc.dtype)
+    vp = torch.randn((npages * 64,) + tuple(vc.shape[1:]), generator=g, device="cuda").to(vc.dtype)
+    kip = torch.randn((npages * 64,) + tuple(kic.shape[1:]), generator=g, device="cuda").to(kic.dtype)
+    S, max_pages = len(lens), int(nb.max())
+    pt = np.full((S, max_pages), 1 << 30, np.int32)
+    dst, src, nxt = [], [], 0
+    for s in range(S):
+        for b in range(int(nb[s])):
+            pg = int(perm[nxt])
+            nxt += 1
+            pt[s, b] = pg
+            n = min(64, int(lens[s]) - 64 * b)
+            dst.append(pg * 64 + np.arange(n))
+            src.append(int(cu[s]) + 64 * b + np.arange(n))
+    dst = torch.from_numpy(np.concatenate(dst)).cuda()
+    src = torch.from_numpy(np.concatenate(src)).cuda()
+    kp[dst], vp[dst], kip[dst] = kc[src], vc[src], kic[src]
+    shape = lambda t: t.view((npages, 64) + tuple(t.shape[1:]))
+    return (shape(kp), shape(vp), shape(kip), torch.from_numpy(pt).cuda(),
+            torch.from_numpy(lens.astype(np.int64)).cuda())

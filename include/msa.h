@@ -148,6 +148,28 @@ msa_status_t msa_sparse_decode(const void *q, const void *q_idx, const void *k_c
                                float *lse, int32_t *idx_out, void *ws, size_t ws_bytes,
                                void *stream);
 
+/* Decode from a paged KV cache: the same computation as msa_sparse_decode, with each sequence's
+ * cache held in 64-token pages -- one page per MSA block, so a selected block is one page.
+ * Token j of sequence s is row j % 64 of page page_table[s * max_pages + j / 64]; the sequence
+ * is seq_lens[s] tokens long and its newest token (position seq_lens[s] - 1) is the query.
+ *   k_pages, v_pages   bf16 [num_pages, 64, H_kv, d_h]
+ *   k_idx_pages        bf16 [num_pages, 64, d_idx]
+ *   page_table         int32 [S, max_pages]  (entries past a sequence's last block are ignored)
+ *   seq_lens           int64 [S], 1 <= seq_lens[s] <= max_len <= 64 * max_pages
+ *   q, q_idx, o, lse, idx_out, ws: as msa_sparse_decode (ws of msa_sparse_decode_workspace()).
+ * page_table and seq_lens are read on the device only; a length outside [1, max_len] or a page id
+ * outside [0, num_pages) is a caller error that the kernels clamp rather than trust.  The results
+ * equal those of msa_sparse_decode on the same tokens stored packed, bit for bit.
+ * max_pages * 64 < max_len or num_pages < 1: MSA_ERR_INVALID_ARGUMENT; other errors as
+ * msa_sparse_decode. */
+msa_status_t msa_sparse_decode_paged(const void *q, const void *q_idx, const void *k_pages,
+                                     const void *v_pages, const void *k_idx_pages,
+                                     const int32_t *page_table, const int64_t *seq_lens, int S,
+                                     int64_t max_pages, int64_t num_pages, int64_t max_len,
+                                     int H_q, int H_kv, int d_h, int d_idx, int block_size, int k,
+                                     void *o, float *lse, int32_t *idx_out, void *ws,
+                                     size_t ws_bytes, void *stream);
+
 /* Size of the fixed device scratch used by msa_sparse_decode_noalloc (8 MiB). */
 #define MSA_DECODE_NOALLOC_SCRATCH_BYTES (8u << 20)
 

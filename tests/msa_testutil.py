@@ -57,3 +57,6 @@ def max_abs(a, b):
 
 def bf16_dev_to_f64(t):
     return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+from gen import to_pages  # noqa: E402,F401  (layout helper shared with the bench)

@@ -26,7 +26,8 @@ def test_header_declares_the_api():
     syms = declared_symbols()
     for name in ("msa_index_block_scores", "msa_select_blocks", "msa_index_select",
                  "msa_sparse_attn_fwd", "msa_sparse_attn_fwd_workspace", "msa_sparse_decode",
-                 "msa_sparse_decode_workspace", "msa_kl_loss_fwd", "msa_kl_loss_fwd_workspace",
+                 "msa_sparse_decode_workspace", "msa_sparse_decode_paged", "msa_kl_loss_fwd",
+                 "msa_kl_loss_fwd_workspace",
                  "msa_status_string", "msa_device_status"):
         assert name in syms
 
@@ -184,3 +185,26 @@ def test_kl_workspace(lib):
     assert floor <= need <= floor + 6 * 256
     assert lib.msa_kl_loss_fwd_workspace(i64(0), 4, 16) == 0
     assert kl(lib, N=1000, wsb=lib.msa_kl_loss_fwd_workspace(i64(1000), 4, 16) - 1) == WORKSPACE
+
+
+def paged(lib, pt=P, sl=ctypes.c_void_p(0x10008), S=4, max_pages=16, num_pages=64, max_len=1000,
+          H_q=32, H_kv=4, d_h=128, d_idx=64, B=64, k=16, ws=P, wsb=1 << 40, kp=P):
+    return lib.msa_sparse_decode_paged(P, P, kp, P, P, pt, sl, S, i64(max_pages), i64(num_pages),
+                                       i64(max_len), H_q, H_kv, d_h, d_idx, B, k, P, P, NUL, ws,
+                                       ctypes.c_size_t(wsb), NUL)
+
+
+@pytest.mark.parametrize("kw", [dict(pt=NUL), dict(pt=ctypes.c_void_p(0x10002)), dict(sl=NUL),
+                                dict(sl=ctypes.c_void_p(0x10004)), dict(kp=MIS), dict(S=0),
+                                dict(max_pages=15), dict(num_pages=0), dict(max_len=0),
+                                dict(k=0), dict(B=32), dict(ws=NUL)])
+def test_decode_paged_invalid(lib, kw):
+    assert paged(lib, **kw) == INVALID
+
+
+def test_decode_paged_unsupported_and_workspace(lib):
+    assert paged(lib, d_h=96) == UNSUPPORTED
+    assert paged(lib, d_idx=48) == UNSUPPORTED
+    lib.msa_sparse_decode_workspace.restype = ctypes.c_size_t
+    need = lib.msa_sparse_decode_workspace(4, i64(1000), 32, 4, 128, 64, 16)
+    assert paged(lib, wsb=need - 1) == WORKSPACE

@@ -9,7 +9,7 @@ import torch
 
 import gen
 import oracle
-from msa_testutil import LSE_TOL, O_TOL, selection_mismatches
+from msa_testutil import LSE_TOL, O_TOL, selection_mismatches, to_pages
 
 pytestmark = pytest.mark.gpu
 
@@ -129,3 +129,19 @@ def test_fullsize_decode():
         if np.array_equal(I_gpu, ref["I"]):
             assert np.abs(o[s].float().cpu().numpy() - ref["O64"][0]).max() <= O_TOL
             assert np.abs(lse[s].cpu().numpy() - ref["LSE"][0]).max() <= LSE_TOL
+
+
+def test_fullsize_decode_paged():
+    """The 32-sequence decode batch from a paged cache (shuffled 64-token pages) equals the packed
+    decode bit for bit."""
+    cfg = gen.CONFIGS["decode"]
+    d = gen.decode_inputs(cfg, seed=0, device="cuda")
+    o, lse, idx = msa.msa_sparse_decode(d["q"], d["q_idx"], d["k_cache"], d["v_cache"],
+                                        d["k_idx_cache"], d["cu_seqlens"], cfg.len_hi, cfg.k)
+    kp, vp, kip, pt, sl = to_pages(d, seed=1)
+    del d["k_cache"], d["v_cache"], d["k_idx_cache"]
+    o2, lse2, idx2 = msa.msa_sparse_decode_paged(d["q"], d["q_idx"], kp, vp, kip, pt, sl,
+                                                 min(cfg.len_hi, 64 * pt.shape[1]), cfg.k)
+    torch.cuda.synchronize()
+    msa.msa_device_status()
+    assert torch.equal(idx2, idx) and torch.equal(o2, o) and torch.equal(lse2, lse)

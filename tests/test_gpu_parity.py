@@ -13,7 +13,7 @@ import torch
 
 import gen
 import oracle
-from msa_testutil import (LSE_TOL, O_TOL, bits, cuda, max_abs, selection_mismatches)
+from msa_testutil import (LSE_TOL, O_TOL, bits, cuda, max_abs, selection_mismatches, to_pages)
 
 pytestmark = pytest.mark.gpu
 
@@ -370,6 +370,31 @@ def test_decode(name, lens, variant):
     dcfg = gen.DecodeConfig("t", len(lens), 1, 1, cfg.H_q, cfg.H_kv, cfg.d_h, cfg.d_idx, cfg.k)
     d = decode_case(dcfg, lens, seed=len(lens), variant=variant)
     check_decode(dcfg, d, max(lens) + 37, exact_idx=(variant == "int"))
+
+
+@pytest.mark.parametrize("name,lens,variant", [
+    ("p32k", [1, 2, 63, 64, 65, 128, 1000, 1025, 5000, 4097], "gauss"),
+    ("p32k", [70, 3000, 129, 64 * 17, 2049], "int"),
+    ("tiny", [1, 100, 900, 1024, 333], "gauss"),
+])
+def test_decode_paged_equals_packed(name, lens, variant):
+    """The paged cache holds the same tokens in shuffled 64-token pages: the results equal the
+    packed decode's bit for bit (same arithmetic in the same order), which the oracle pins."""
+    cfg = cfg_of(name)
+    dcfg = gen.DecodeConfig("t", len(lens), 1, 1, cfg.H_q, cfg.H_kv, cfg.d_h, cfg.d_idx, cfg.k)
+    d = decode_case(dcfg, lens, seed=len(lens) + 7, variant=variant)
+    max_len = max(lens) + 37
+    o, lse, idx = msa.msa_sparse_decode(d["q"], d["q_idx"], d["k_cache"], d["v_cache"],
+                                        d["k_idx_cache"], d["cu_seqlens"], max_len, dcfg.k)
+    kp, vp, kip, pt, sl = to_pages(d, seed=len(lens))
+    # max_len may exceed 64 * max_pages only up to the table's width
+    max_len_p = min(max_len, 64 * pt.shape[1])
+    o2, lse2, idx2 = msa.msa_sparse_decode_paged(d["q"], d["q_idx"], kp, vp, kip, pt, sl,
+                                                 max_len_p, dcfg.k)
+    sync_ok()
+    assert torch.equal(idx2, idx)
+    assert torch.equal(o2, o)
+    assert torch.equal(lse2, lse)
 
 
 def test_decode_equals_prefill_last_row():
