@@ -6,8 +6,9 @@ A step is one pass of the whole hot path over one batch of synthetic input:
   branch; H_q=32, H_kv=4, d_h=128, d_idx=64, block 64, k=16, 8 hot blocks), then
   decode of 32 sequences with cache lengths ~ U[65536, 262144] (same head layout).
 `value` is prefill tokens/s (N / prefill device time); decode tokens/s is reported beside it, and
-the forward of the KL alignment loss (on the step's selection and LSE) and the decode of the same
-batch from a paged KV cache are timed after the steps, outside `value`.
+the forward of the KL alignment loss (on the step's selection and LSE), the decode of the same
+batch from a paged KV cache, and a varlen prefill of the same tokens cut into sequences of mixed
+lengths are timed after the steps, outside `value`.
 Inputs stay resident in HBM; every timed input (M alone is 4.3 GB, the decode caches 11.5 GB)
 is larger than the 129 MB L2, so no flush is needed.
 
@@ -377,6 +378,8 @@ def run_msa(args, world, rank, local):
         line["kl_loss_fwd"] = time_kl(msa, pcfg, x, bufs, K, sizes, pk, world)
     if d is not None and not args.no_paged:
         line["decode_paged"] = time_decode_paged(msa, dcfg, d, dbufs, K, sizes, pk, world)
+    if not args.no_varlen and pcfg.k <= 32:
+        line["prefill_varlen"] = time_varlen(msa, pcfg, x, bufs, K, world)
     if not args.no_e2e:
         line["e2e"] = e2e_prefill(msa, pcfg, x, bufs, K, W, world)
     if not args.no_cpu_baseline and rank == 0 and world == 1:
@@ -448,6 +451,40 @@ def time_decode_paged(msa, dcfg, d, dbufs, K, sizes, pk, world):
             "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": pk["hbm"],
                          "unit": "GB/s", "frac": round(achieved / pk["hbm"], 4),
                          "algorithmic": sizes["decode_bytes"]}}
+
+
+VARLEN_LENS = (65536, 32768, 16384, 8192, 4096, 2048, 1024, 512, 256, 256)
+
+
+def time_varlen(msa, pcfg, x, bufs, K, world):
+    """Varlen prefill of the same N tokens cut into independent sequences of mixed lengths
+    (VARLEN_LENS scaled to N), timed apart from the step: K calls after 3 warm-up calls.  It
+    overwrites the step's output buffers, so it runs after every other use of them."""
+    N = pcfg.N
+    lens = [max(1, L * N // 131072) for L in VARLEN_LENS]
+    lens[0] += N - sum(lens)
+    cu = torch.zeros(len(lens) + 1, dtype=torch.int64)
+    cu[1:] = torch.cumsum(torch.tensor(lens), 0)
+
+    def call():
+        msa.msa_prefill_varlen(x["q"], x["k"], x["v"], x["q_idx"], x["k_idx"], cu, pcfg.k,
+                               o=bufs["o"], lse=bufs["lse"].view(-1), idx=bufs["idx"].view(-1),
+                               ws=bufs["ws"])
+
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(K + 1)]
+    evs[0].record(stream)
+    for s in range(K):
+        call()
+        evs[s + 1].record(stream)
+    torch.cuda.synchronize()
+    msa.msa_device_status()
+    ms = max_over_ranks(float(np.mean([evs[s].elapsed_time(evs[s + 1]) for s in range(K)])), world)
+    return {"ms": round(ms, 4), "value": round(world * N / (ms * 1e-3), 1), "unit": "tokens/s",
+            "sequences": lens}
 
 
 def e2e_prefill(msa, pcfg, x, bufs, K, W, world):
@@ -582,6 +619,8 @@ def main():
     ap.add_argument("--no-kl", action="store_true", help="skip the KL loss forward measurement")
     ap.add_argument("--no-paged", action="store_true",
                     help="skip the paged-cache decode measurement")
+    ap.add_argument("--no-varlen", action="store_true",
+                    help="skip the varlen (batched) prefill measurement")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--write-traffic", metavar="NCU_CSV",
                     help="write profiles/traffic.txt from an ncu CSV of whole steps and exit")

@@ -5,5 +5,6 @@ the C ABI of libmsa.so (include/msa.h)."""
 from .msa import (MSAError, msa_device_status, msa_index_block_scores,  # noqa: F401
                   msa_index_select, msa_select_blocks, msa_sparse_attn_fwd, msa_sparse_attn_fwd_workspace,
                   msa_sparse_decode, msa_sparse_decode_workspace, msa_sparse_decode_paged,
+                  msa_prefill_varlen,
                   msa_kl_loss_fwd,
                   msa_kl_loss_fwd_workspace)

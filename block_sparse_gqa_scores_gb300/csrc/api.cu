@@ -2,6 +2,7 @@
 // Nothing here allocates device memory or synchronises, except msa_device_status().
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "../../include/msa.h"
@@ -215,6 +216,71 @@ MSA_API msa_status_t msa_sparse_decode(const void* q, const void* q_idx, const v
   e = msa::launch_sparse_attn_decode(q, k_cache, v_cache, idx, cm, S, max_len, H_q, H_kv,
                                      d_h, k, w.nsplit, part_o, part_lse, o, lse, st);
   return from_cuda(e);
+}
+
+// Varlen prefill: the sequences of a packed batch, one after another on `stream`, each through the
+// fused index branch and the main branch (the kernels are the single-sequence ones; only the
+// pointers move).  cu_seqlens is host memory: the launch sizes depend on it.
+MSA_API size_t msa_prefill_varlen_workspace(const int64_t* cu_seqlens, int nseq, int H_q, int H_kv,
+                                            int d_h, int k) {
+  if (!cu_seqlens || nseq < 1 || H_kv < 1 || H_q < H_kv || H_q % H_kv != 0 || k < 1 || k > 64 ||
+      d_h < 1)
+    return 0;
+  int64_t longest = 0;
+  for (int s = 0; s < nseq; ++s) longest = std::max(longest, cu_seqlens[s + 1] - cu_seqlens[s]);
+  return longest < 1 ? 0 : msa::sparse_attn_ws_bytes(longest, H_q, H_kv, d_h, k);
+}
+
+MSA_API msa_status_t msa_prefill_varlen(const void* q, const void* k, const void* v,
+                                        const void* q_idx, const void* k_idx,
+                                        const int64_t* cu_seqlens, int nseq, int H_q, int H_kv,
+                                        int d_h, int d_idx, int block_size, int k_blocks,
+                                        int32_t* idx, void* o, float* lse, void* ws,
+                                        size_t ws_bytes, void* stream) {
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(q_idx) || !aligned16(k_idx) ||
+      !aligned4(idx) || !aligned16(o) || !aligned4(lse) || !aligned16(ws) || !cu_seqlens)
+    return MSA_ERR_INVALID_ARGUMENT;
+  if (nseq < 1 || H_q < 1 || H_kv < 1 || H_q % H_kv != 0 || d_h < 1 || d_idx < 1 ||
+      block_size != 64 || k_blocks < 1 || k_blocks > 64 || cu_seqlens[0] != 0)
+    return MSA_ERR_INVALID_ARGUMENT;
+  int64_t longest = 0;
+  for (int s = 0; s < nseq; ++s) {
+    const int64_t n = cu_seqlens[s + 1] - cu_seqlens[s];
+    if (n < 1) return MSA_ERR_INVALID_ARGUMENT;
+    longest = std::max(longest, n);
+  }
+  if (!pow2_upto(H_kv, 8) || !pow2_upto(H_q / H_kv, 8) || (d_h != 64 && d_h != 128) ||
+      (d_idx != 32 && d_idx != 64) || k_blocks > MSA_INDEX_SELECT_MAX_K)
+    return MSA_ERR_UNSUPPORTED;
+  if (longest * H_kv >= kMaxRows || longest > ((int64_t)1 << 21)) return MSA_ERR_UNSUPPORTED;
+  if (ws_bytes < msa::sparse_attn_ws_bytes(longest, H_q, H_kv, d_h, k_blocks))
+    return MSA_ERR_WORKSPACE;
+  cudaStream_t st = (cudaStream_t)stream;
+  const auto* qb = static_cast<const char*>(q);
+  const auto* kb = static_cast<const char*>(k);
+  const auto* vb = static_cast<const char*>(v);
+  const auto* qib = static_cast<const char*>(q_idx);
+  const auto* kib = static_cast<const char*>(k_idx);
+  auto* ob = static_cast<char*>(o);
+  for (int s = 0; s < nseq; ++s) {
+    const int64_t t0 = cu_seqlens[s], n = cu_seqlens[s + 1] - t0;
+    // a sequence's rows start t0 rows into each packed tensor; its selections and LSE are
+    // contiguous blocks [H_kv, n, k] and [H_q, n] starting at t0 * H_kv * k and t0 * H_q
+    const void* qs = qb + t0 * H_q * d_h * 2;
+    const void* ks = kb + t0 * H_kv * d_h * 2;
+    const void* vs = vb + t0 * H_kv * d_h * 2;
+    const void* qis = qib + t0 * H_kv * d_idx * 2;
+    const void* kis = kib + t0 * d_idx * 2;
+    int32_t* idxs = idx + t0 * H_kv * k_blocks;
+    void* os = ob + t0 * H_q * d_h * 2;
+    float* lses = lse + t0 * H_q;
+    cudaError_t e = msa::launch_index_select(qis, kis, idxs, n, H_kv, d_idx, k_blocks, 0, n, st);
+    if (e != cudaSuccess) return MSA_ERR_CUDA;
+    e = msa::launch_sparse_attn_fwd(qs, ks, vs, idxs, os, lses, n, H_q, H_kv, d_h, k_blocks, ws,
+                                    st);
+    if (e != cudaSuccess) return MSA_ERR_CUDA;
+  }
+  return MSA_OK;
 }
 
 MSA_API msa_status_t msa_sparse_decode_paged(

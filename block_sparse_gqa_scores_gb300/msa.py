@@ -48,11 +48,16 @@ def _load():
                                             i32, P, P, P, P]
     L.msa_sparse_decode_paged.argtypes = [P, P, P, P, P, P, P, i32, i64, i64, i64, i32, i32, i32,
                                           i32, i32, i32, P, P, P, P, sz, P]
+    L.msa_prefill_varlen_workspace.argtypes = [P, i32, i32, i32, i32, i32]
+    L.msa_prefill_varlen_workspace.restype = sz
+    L.msa_prefill_varlen.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32, P, P, P,
+                                     P, sz, P]
     L.msa_kl_loss_fwd_workspace.argtypes = [i64, i32, i32]
     L.msa_kl_loss_fwd_workspace.restype = sz
     L.msa_kl_loss_fwd.argtypes = [P, P, P, P, P, P, P, i64, i32, i32, i32, i32, i32, i32, P, sz, P]
     for fn in ("msa_index_block_scores", "msa_select_blocks", "msa_index_select", "msa_sparse_attn_fwd",
                "msa_sparse_decode", "msa_sparse_decode_noalloc", "msa_sparse_decode_paged",
+               "msa_prefill_varlen",
                "msa_kl_loss_fwd",
                "msa_device_status"):
         getattr(L, fn).restype = i32
@@ -210,6 +215,35 @@ def msa_sparse_decode_noalloc(q, q_idx, k_cache, v_cache, k_idx_cache, cu_seqlen
         S, max_len, H_q, H_kv, d_h, d_idx, block_size, k, _ptr(o), _ptr(lse), _ptr(idx_out),
         _stream(stream)))
     return o, lse, idx_out
+
+
+def msa_prefill_varlen(q, k, v, q_idx, k_idx, cu_seqlens, kk, o=None, lse=None, idx=None,
+                       ws=None, block_size=BLOCK, stream=None):
+    """Prefill of packed independent sequences (cu_seqlens: a CPU int64 tensor [nseq+1]) ->
+    (O [T,H_q,d_h], LSE flat fp32 (sequence s: [H_q, N_s] at H_q*cu[s]), idx flat int32
+    (sequence s: [H_kv, N_s, k] at H_kv*k*cu[s]))."""
+    for t, n, nd in ((q, "q", 3), (k, "k", 3), (v, "v", 3), (q_idx, "q_idx", 3)):
+        _req(t, torch.bfloat16, nd, n)
+    _req(k_idx, torch.bfloat16, 2, "k_idx")
+    if cu_seqlens.dtype != torch.int64 or cu_seqlens.is_cuda or not cu_seqlens.is_contiguous():
+        raise ValueError("cu_seqlens must be a contiguous int64 CPU tensor")
+    T, H_q, d_h = q.shape
+    H_kv, d_idx = k.shape[1], q_idx.shape[2]
+    nseq = cu_seqlens.numel() - 1
+    cu_ptr = ctypes.c_void_p(cu_seqlens.data_ptr())
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(T * H_q, dtype=torch.float32, device=q.device)
+    if idx is None:
+        idx = torch.empty(T * H_kv * kk, dtype=torch.int32, device=q.device)
+    nws = int(lib.msa_prefill_varlen_workspace(cu_ptr, nseq, H_q, H_kv, d_h, kk))
+    if ws is None:
+        ws = torch.empty(max(nws, 16), dtype=torch.uint8, device=q.device)
+    _check("msa_prefill_varlen", lib.msa_prefill_varlen(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(q_idx), _ptr(k_idx), cu_ptr, nseq, H_q, H_kv, d_h, d_idx,
+        block_size, kk, _ptr(idx), _ptr(o), _ptr(lse), _ptr(ws), ws.numel(), _stream(stream)))
+    return o, lse, idx
 
 
 def msa_sparse_decode_paged(q, q_idx, k_pages, v_pages, k_idx_pages, page_table, seq_lens,

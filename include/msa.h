@@ -124,6 +124,31 @@ msa_status_t msa_sparse_attn_fwd(const void *q, const void *k, const void *v, co
                                  int block_size, int k_blocks, void *ws, size_t ws_bytes,
                                  void *stream);
 
+/* Workspace bytes msa_prefill_varlen needs: that of msa_sparse_attn_fwd for the longest sequence
+ * (0 for invalid sizes).  cu_seqlens is host memory here. */
+size_t msa_prefill_varlen_workspace(const int64_t *cu_seqlens, int nseq, int H_q, int H_kv,
+                                    int d_h, int k);
+
+/* Batched / varlen prefill: the whole prefill path (msa_index_select, then msa_sparse_attn_fwd)
+ * for each of nseq independent sequences packed along the token axis.  Sequence s is rows
+ * cu_seqlens[s] .. cu_seqlens[s+1]-1 of every packed tensor, with causal attention inside the
+ * sequence only (positions restart at 0 for each sequence).
+ *   q      bf16 [T, H_q, d_h];  k, v bf16 [T, H_kv, d_h];  q_idx bf16 [T, H_kv, d_idx];
+ *   k_idx  bf16 [T, d_idx];  T = cu_seqlens[nseq]
+ *   o      bf16 [T, H_q, d_h]
+ *   idx    int32: sequence s's selections [H_kv, N_s, k] at element offset cu_seqlens[s] * H_kv * k
+ *   lse    fp32: sequence s's [H_q, N_s] at element offset cu_seqlens[s] * H_q
+ *   cu_seqlens  int64 [nseq + 1], HOST memory, cu_seqlens[0] = 0, every sequence >= 1 token
+ *   ws     device workspace of msa_prefill_varlen_workspace() bytes (reused by every sequence).
+ * Each sequence's results equal those of the single-sequence calls on its rows, bit for bit.
+ * The sequences run one after another on `stream` (launches per sequence as the two calls);
+ * k > MSA_INDEX_SELECT_MAX_K: MSA_ERR_UNSUPPORTED; other errors as the two calls. */
+msa_status_t msa_prefill_varlen(const void *q, const void *k, const void *v, const void *q_idx,
+                                const void *k_idx, const int64_t *cu_seqlens, int nseq, int H_q,
+                                int H_kv, int d_h, int d_idx, int block_size, int k_blocks,
+                                int32_t *idx, void *o, float *lse, void *ws, size_t ws_bytes,
+                                void *stream);
+
 /* Workspace bytes msa_sparse_decode needs (block scores, selections, split partials). */
 size_t msa_sparse_decode_workspace(int S, int64_t max_len, int H_q, int H_kv, int d_h, int d_idx,
                                    int k);

@@ -26,7 +26,8 @@ def test_header_declares_the_api():
     syms = declared_symbols()
     for name in ("msa_index_block_scores", "msa_select_blocks", "msa_index_select",
                  "msa_sparse_attn_fwd", "msa_sparse_attn_fwd_workspace", "msa_sparse_decode",
-                 "msa_sparse_decode_workspace", "msa_sparse_decode_paged", "msa_kl_loss_fwd",
+                 "msa_sparse_decode_workspace", "msa_sparse_decode_paged", "msa_prefill_varlen",
+                 "msa_prefill_varlen_workspace", "msa_kl_loss_fwd",
                  "msa_kl_loss_fwd_workspace",
                  "msa_status_string", "msa_device_status"):
         assert name in syms
@@ -208,3 +209,29 @@ def test_decode_paged_unsupported_and_workspace(lib):
     lib.msa_sparse_decode_workspace.restype = ctypes.c_size_t
     need = lib.msa_sparse_decode_workspace(4, i64(1000), 32, 4, 128, 64, 16)
     assert paged(lib, wsb=need - 1) == WORKSPACE
+
+
+def varlen(lib, cu=(0, 100, 1100), q=P, k=16, ws=P, wsb=1 << 40, H_q=32, H_kv=4, d_h=128,
+           d_idx=64, B=64, idx=P):
+    arr = None if cu is None else (ctypes.c_int64 * len(cu))(*cu)
+    n = 0 if cu is None else len(cu) - 1
+    return lib.msa_prefill_varlen(q, P, P, P, P, arr, n, H_q, H_kv, d_h, d_idx, B, k, idx, P, P,
+                                  ws, ctypes.c_size_t(wsb), NUL)
+
+
+@pytest.mark.parametrize("kw", [dict(cu=None), dict(cu=(1, 100)), dict(cu=(0, 100, 100)),
+                                dict(q=NUL), dict(idx=ctypes.c_void_p(0x10002)), dict(k=0),
+                                dict(B=32), dict(ws=NUL)])
+def test_prefill_varlen_invalid(lib, kw):
+    assert varlen(lib, **kw) == INVALID
+
+
+def test_prefill_varlen_unsupported_and_workspace(lib):
+    assert varlen(lib, k=33) == UNSUPPORTED
+    assert varlen(lib, d_h=96) == UNSUPPORTED
+    lib.msa_prefill_varlen_workspace.restype = ctypes.c_size_t
+    lib.msa_sparse_attn_fwd_workspace.restype = ctypes.c_size_t
+    cu = (ctypes.c_int64 * 4)(0, 100, 40100, 41000)
+    need = lib.msa_prefill_varlen_workspace(cu, 3, 32, 4, 128, 16)
+    assert need == lib.msa_sparse_attn_fwd_workspace(i64(40000), 32, 4, 128, 16)
+    assert varlen(lib, cu=(0, 100, 40100, 41000), wsb=need - 1) == WORKSPACE

@@ -308,6 +308,34 @@ def test_kl_loss_uniform_teacher():
     check_kl(kl, oracle.kl_loss(b["q"], b["k"], b["q_idx"], b["k_idx"], idx.cpu().numpy()))
 
 
+# -------------------------------------------------------------- varlen prefill --
+
+@pytest.mark.parametrize("name,lens", [("p32k", [1, 63, 64, 65, 1000, 3000, 4500]),
+                                       ("tiny", [700, 1, 1024, 129]),
+                                       ("p32k", [40000, 2000])])
+def test_prefill_varlen_equals_single_sequences(name, lens):
+    """A packed batch of independent sequences gives, per sequence, exactly the single-sequence
+    results (same kernels on the sequence's rows; positions restart at each sequence)."""
+    cfg = cfg_of(name)
+    T = sum(lens)
+    x, _ = fresh(cfg, T, seed=31)
+    cu = torch.zeros(len(lens) + 1, dtype=torch.int64)
+    cu[1:] = torch.cumsum(torch.tensor(lens), 0)
+    o, lse, idx = msa.msa_prefill_varlen(x["q"], x["k"], x["v"], x["q_idx"], x["k_idx"], cu, cfg.k)
+    sync_ok()
+    for s_, n in enumerate(lens):
+        t0 = int(cu[s_])
+        sl = slice(t0, t0 + n)
+        xs = {k_: x[k_][sl].contiguous() for k_ in ("q", "k", "v", "q_idx", "k_idx")}
+        idx1 = msa.msa_index_select(xs["q_idx"], xs["k_idx"], cfg.k)
+        o1, lse1 = msa.msa_sparse_attn_fwd(xs["q"], xs["k"], xs["v"], idx1)
+        sync_ok()
+        assert torch.equal(idx[t0 * cfg.H_kv * cfg.k:(t0 + n) * cfg.H_kv * cfg.k],
+                           idx1.reshape(-1))
+        assert torch.equal(o[sl], o1)
+        assert torch.equal(lse[t0 * cfg.H_q:(t0 + n) * cfg.H_q], lse1.reshape(-1))
+
+
 # ------------------------------------------------------------------------ decode --
 
 def decode_case(cfg, lens, seed, variant="gauss"):
