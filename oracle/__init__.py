@@ -18,6 +18,9 @@ Pins (what this oracle is checked against, in tests/test_oracle_pins.py):
                    torch.nn.functional.scaled_dot_product_attention (causal, fp64);
                    Q = 0 closed form (LSE = ln|T|, O = mean of V over T).
   decode        -- equals the prefill row L-1 on the same tokens.
+  KL gradient   -- torch.autograd (fp64) through a dense masked restatement of the loss; central
+                   finite differences of the oracle's own kl_loss; the uniform-teacher closed
+                   form; sum over the index keys of dK_idx . K_idx equals sum of dQ_idx . Q_idx.
   KL loss       -- k >= #blocks equals scipy.stats.entropy of torch.softmax distributions
                    (causal); sparse selections equal the same library routines on a mask
                    built by brute force; uniform-teacher and uniform-student closed forms;
@@ -65,6 +68,8 @@ def lib():
         L.msa_oracle_decode.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32, P,
                                         i32, P, P, i64, P, P, P]
         L.msa_oracle_kl_loss.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, i32, P, i64, P]
+        L.msa_oracle_kl_loss_grad.argtypes = [P, P, P, P, P, P, i64, i32, i32, i32, i32, i32,
+                                               i32, P, P, P, P]
         L.msa_oracle_set_threads.argtypes = [i32]
         L.msa_oracle_get_threads.restype = i32
         L.msa_oracle_f64_to_bf16.argtypes = [ctypes.c_double]
@@ -211,3 +216,19 @@ def kl_loss(q, k, q_idx, k_idx, I, block_size=64, rows=None, compact=False):
     lib().msa_oracle_kl_loss(_p(q), _p(k), _p(q_idx), _p(k_idx), _p(I_rows), H_q, H_kv, d_h,
                              d_idx, block_size, I_rows.shape[2], _p(rows_a), n, _p(KL))
     return KL
+
+
+def kl_loss_grad(q, k, q_idx, k_idx, I, g_kl, block_size=64):
+    """Index-branch gradient of sum(g_kl * KL) (teacher fixed) over all rows ->
+    dict(dq_idx [N,H_kv,d_idx], dk_idx [N,d_idx], lse_idx [H_kv,N], psum [H_kv,N]) float64."""
+    q, k, q_idx, k_idx = map(_u16, (q, k, q_idx, k_idx))
+    I = np.ascontiguousarray(I, dtype=np.int32)
+    g_kl = np.ascontiguousarray(g_kl, dtype=np.float64)
+    N, H_q, d_h = q.shape
+    H_kv, d_idx = k.shape[1], q_idx.shape[2]
+    out = dict(dq_idx=np.empty((N, H_kv, d_idx)), dk_idx=np.empty((N, d_idx)),
+               lse_idx=np.empty((H_kv, N)), psum=np.empty((H_kv, N)))
+    lib().msa_oracle_kl_loss_grad(_p(q), _p(k), _p(q_idx), _p(k_idx), _p(I), _p(g_kl), N, H_q,
+                                  H_kv, d_h, d_idx, block_size, I.shape[2], _p(out["dq_idx"]),
+                                  _p(out["dk_idx"]), _p(out["lse_idx"]), _p(out["psum"]))
+    return out

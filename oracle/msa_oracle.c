@@ -18,7 +18,8 @@
  *   - section Kernel: the forward also emits the per-row log-sum-exp (LSE).
  * and the section 训练：top-k 不可导怎么办 (training), eq. P^idx / P / L_KL: the KL alignment
  *   loss of a row and group over its selected token set, the main branch's group-averaged
- *   attention (teacher) against the index branch's softmax (student).
+ *   attention (teacher) against the index branch's softmax (student); and its gradient with
+ *   respect to the index branch's inputs with the teacher held fixed (gradient detach).
  *
  * Readings where the page is silent (each is listed with its reason in the design notes):
  *   - k counts the forced local block: I = {l} U top-(k-1) of the blocks b < l.
@@ -247,6 +248,71 @@ static double row_kl(const uint16_t *q_i, const uint16_t *qidx_ir, const uint16_
     return kl;
 }
 
+/* Gradient of L = sum over rows of g[r,i] * KL[r,i] with respect to the index branch's inputs
+ * for one (row i, group r), the teacher held fixed (the gradient detach of section 训练):
+ *   dKL/dS^idx_j = (sum_u P_u) P^idx_j - P_j      (the KL as defined above, differentiated)
+ *   dQ_idx[i,r] += g sum_j dS_j K_idx[j] / sqrt(d_idx),  dK_idx[j] += g dS_j Q_idx[i,r] / sqrt(d_idx)
+ * dq: [d_idx] for this row; dk: [N, d_idx] accumulated.  Also returns the student's LSE over T
+ * and the teacher's total mass sum_j P_j in *lse_idx_out, *psum_out. */
+static void row_kl_grad(const uint16_t *q_i, const uint16_t *qidx_ir, const uint16_t *K,
+                        const uint16_t *K_idx, int64_t i, int r, int H_q, int H_kv, int d_h,
+                        int d_idx, int B, const int32_t *sel, int kk, double g, double *dq,
+                        double *dk, double *lse_idx_out, double *psum_out, double *s_buf,
+                        double *p_buf, int64_t *j_buf)
+{
+    const int G = H_q / H_kv;
+    int64_t nt = 0;
+    for (int t = 0; t < kk; ++t) {
+        const int64_t b = sel[t];
+        if (b < 0) continue;
+        const int64_t j1 = imin64(b * B + B - 1, i);
+        for (int64_t j = b * B; j <= j1; ++j) j_buf[nt++] = j;
+    }
+    const double scale_h = 1.0 / sqrt((double)d_h);
+    for (int64_t t = 0; t < nt; ++t) p_buf[t] = 0.0;
+    for (int h = r * G; h < (r + 1) * G; ++h) {
+        const uint16_t *qh = q_i + (int64_t)h * d_h;
+        double m = -INFINITY;
+        for (int64_t t = 0; t < nt; ++t) {
+            const uint16_t *kj = K + (j_buf[t] * H_kv + r) * (int64_t)d_h;
+            double dot = 0.0;
+            for (int d = 0; d < d_h; ++d) dot += bf16_to_f64(qh[d]) * bf16_to_f64(kj[d]);
+            s_buf[t] = dot * scale_h;
+            if (s_buf[t] > m) m = s_buf[t];
+        }
+        double z = 0.0;
+        for (int64_t t = 0; t < nt; ++t) z += exp(s_buf[t] - m);
+        for (int64_t t = 0; t < nt; ++t) p_buf[t] += exp(s_buf[t] - m) / z / G;
+    }
+    const double scale_idx = 1.0 / sqrt((double)d_idx);
+    double m = -INFINITY;
+    for (int64_t t = 0; t < nt; ++t) {
+        const uint16_t *kj = K_idx + j_buf[t] * (int64_t)d_idx;
+        double dot = 0.0;
+        for (int d = 0; d < d_idx; ++d) dot += bf16_to_f64(qidx_ir[d]) * bf16_to_f64(kj[d]);
+        s_buf[t] = dot * scale_idx;
+        if (s_buf[t] > m) m = s_buf[t];
+    }
+    double z = 0.0, psum = 0.0;
+    for (int64_t t = 0; t < nt; ++t) {
+        z += exp(s_buf[t] - m);
+        psum += p_buf[t];
+    }
+    const double lse_idx = m + log(z);
+    *lse_idx_out = lse_idx;
+    *psum_out = psum;
+    for (int d = 0; d < d_idx; ++d) dq[d] = 0.0;
+    for (int64_t t = 0; t < nt; ++t) {
+        const double ds = g * (psum * exp(s_buf[t] - lse_idx) - p_buf[t]) * scale_idx;
+        const uint16_t *kj = K_idx + j_buf[t] * (int64_t)d_idx;
+        double *dkj = dk + j_buf[t] * (int64_t)d_idx;
+        for (int d = 0; d < d_idx; ++d) {
+            dq[d] += ds * bf16_to_f64(kj[d]);
+            dkj[d] += ds * bf16_to_f64(qidx_ir[d]);
+        }
+    }
+}
+
 /* ------------------------------------------------------------- exports ----- */
 
 void msa_oracle_set_threads(int n)
@@ -460,6 +526,31 @@ void msa_oracle_kl_loss(const uint16_t *q_rows, const uint16_t *k, const uint16_
         free(p_buf);
         free(j_buf);
     }
+}
+
+/* Index-branch gradient of L = sum_{r,i} G_KL[r,i] KL[r,i] over all N rows, teacher fixed.
+ * G_KL [H_kv, N] fp64; outputs dQ_idx [N, H_kv, d_idx], dK_idx [N, d_idx] (fp64, overwritten),
+ * LSE_idx [H_kv, N] (the student's LSE over T) and PSUM [H_kv, N] (the teacher's mass over T).
+ * Single-threaded over rows for dK_idx (a plain sum in row order). */
+void msa_oracle_kl_loss_grad(const uint16_t *q, const uint16_t *k, const uint16_t *q_idx,
+                             const uint16_t *k_idx, const int32_t *I, const double *G_KL,
+                             int64_t N, int H_q, int H_kv, int d_h, int d_idx, int B, int kk,
+                             double *dQ_idx, double *dK_idx, double *LSE_idx, double *PSUM)
+{
+    double *s_buf = (double *)malloc((size_t)kk * B * sizeof(double));
+    double *p_buf = (double *)malloc((size_t)kk * B * sizeof(double));
+    int64_t *j_buf = (int64_t *)malloc((size_t)kk * B * sizeof(int64_t));
+    for (int64_t e = 0; e < N * (int64_t)d_idx; ++e) dK_idx[e] = 0.0;
+    for (int64_t i = 0; i < N; ++i)
+        for (int r = 0; r < H_kv; ++r)
+            row_kl_grad(q + i * H_q * (int64_t)d_h, q_idx + (i * H_kv + r) * (int64_t)d_idx, k,
+                        k_idx, i, r, H_q, H_kv, d_h, d_idx, B, I + ((int64_t)r * N + i) * kk, kk,
+                        G_KL[(int64_t)r * N + i], dQ_idx + (i * H_kv + r) * (int64_t)d_idx, dK_idx,
+                        LSE_idx + (int64_t)r * N + i, PSUM + (int64_t)r * N + i, s_buf, p_buf,
+                        j_buf);
+    free(s_buf);
+    free(p_buf);
+    free(j_buf);
 }
 
 /* Exposed for the pins on the rounding step. */

@@ -431,3 +431,76 @@ def test_kl_nonnegative_and_group_specific():
     y["q"] = np.ascontiguousarray(x["q"][:, [3, 2, 1, 0, 7, 6, 5, 4]])  # within-group order
     KL_perm = oracle.kl_loss(y["q"], y["k"], y["q_idx"], y["k_idx"], I, block_size=B)
     np.testing.assert_allclose(KL_perm, KL, rtol=1e-12, atol=1e-14)
+
+
+# ------------------------------------------ KL gradient (index branch, teacher fixed) --
+
+def autograd_kl_grad(x, I, g, B):
+    """torch.autograd in fp64 through a dense masked restatement of the loss: teacher from
+    torch.softmax (no gradient), student log-probabilities from torch.log_softmax over T."""
+    N = x["q"].shape[0]
+    Q, K = torch.from_numpy(f64(x["q"])), torch.from_numpy(f64(x["k"]))
+    Qi = torch.from_numpy(f64(x["q_idx"])).requires_grad_(True)
+    Ki = torch.from_numpy(f64(x["k_idx"])).requires_grad_(True)
+    H_q, d_h = Q.shape[1], Q.shape[2]
+    H_kv, d_idx = K.shape[1], Qi.shape[2]
+    G = H_q // H_kv
+    mask = torch.from_numpy(np.array(selected_token_mask(I, N, B)))
+    loss = 0.0
+    for r in range(H_kv):
+        S = torch.einsum("nhd,md->hnm", Q[:, r * G:(r + 1) * G], K[:, r]) / math.sqrt(d_h)
+        teacher = torch.softmax(S.masked_fill(~mask[r], float("-inf")), dim=-1).mean(dim=0)
+        Si = (Qi[:, r] @ Ki.T) / math.sqrt(d_idx)
+        logp = torch.log_softmax(Si.masked_fill(~mask[r], float("-inf")), dim=-1)
+        term = torch.where(mask[r], teacher * (torch.log(teacher.clamp_min(1e-300)) - logp),
+                           torch.zeros((), dtype=torch.float64))
+        loss = loss + (torch.from_numpy(g[r]) * term.sum(dim=-1)).sum()
+    loss.backward()
+    return Qi.grad.numpy(), Ki.grad.numpy()
+
+
+@pytest.mark.parametrize("variant,seed", [("gauss", 21), ("int", 22)])
+def test_kl_grad_matches_autograd(variant, seed):
+    cfg = small_cfg(N=100, H_q=8, H_kv=2, d_h=16, d_idx=8, k=3)
+    x = bits(gen.prefill_inputs(cfg, seed=seed, variant=variant))
+    B = 8
+    _, M32 = oracle.block_scores(x["q_idx"], x["k_idx"], block_size=B)
+    I = oracle.select_blocks(M32, 100, 3, block_size=B)
+    g = np.random.default_rng(seed).uniform(0.5, 2.0, (2, 100))
+    out = oracle.kl_loss_grad(x["q"], x["k"], x["q_idx"], x["k_idx"], I, g, block_size=B)
+    dq_ref, dk_ref = autograd_kl_grad(x, I, g, B)
+    np.testing.assert_allclose(out["dq_idx"], dq_ref, rtol=1e-9, atol=1e-12)
+    np.testing.assert_allclose(out["dk_idx"], dk_ref, rtol=1e-9, atol=1e-12)
+    # by-products: the student's LSE over T and the teacher's mass (1 up to rounding)
+    assert np.abs(out["psum"] - 1).max() < 1e-12
+    Qi, Ki = f64(x["q_idx"]), f64(x["k_idx"])
+    from scipy.special import logsumexp
+    for r, i in [(0, 0), (1, 57), (0, 99)]:
+        toks = [j for b in I[r, i] if b >= 0 for j in range(b * B, min(b * B + B, i + 1))]
+        assert out["lse_idx"][r, i] == pytest.approx(logsumexp(Ki[toks] @ Qi[i, r] / math.sqrt(8)),
+                                                     abs=1e-12)
+
+
+def test_kl_grad_invariants():
+    """sum_j dK_idx[j].K_idx[j] = sum_{i,r} dQ_idx[i,r].Q_idx[i,r] (both are sum g dS S^idx), and
+    the gradient vanishes when the student's scores equal the teacher's."""
+    cfg = small_cfg(N=120, H_q=8, H_kv=2, d_h=16, d_idx=8, k=4)
+    x = bits(gen.prefill_inputs(cfg, seed=23))
+    B = 8
+    _, M32 = oracle.block_scores(x["q_idx"], x["k_idx"], block_size=B)
+    I = oracle.select_blocks(M32, 120, 4, block_size=B)
+    g = np.random.default_rng(5).uniform(0.5, 2.0, (2, 120))
+    out = oracle.kl_loss_grad(x["q"], x["k"], x["q_idx"], x["k_idx"], I, g, block_size=B)
+    lhs = (out["dk_idx"] * f64(x["k_idx"])).sum()
+    rhs = (out["dq_idx"] * f64(x["q_idx"])).sum()
+    assert lhs == pytest.approx(rhs, rel=1e-10, abs=1e-12) and abs(lhs) > 1e-3
+    # student == teacher
+    cfg = small_cfg(N=130, H_q=1, H_kv=1, d_h=16, d_idx=16, k=3)
+    y = bits(gen.prefill_inputs(cfg, seed=24))
+    y["q_idx"] = np.ascontiguousarray(y["q"])
+    y["k_idx"] = np.ascontiguousarray(y["k"][:, 0])
+    _, M32 = oracle.block_scores(y["q_idx"], y["k_idx"], block_size=B)
+    I = oracle.select_blocks(M32, 130, 3, block_size=B)
+    out = oracle.kl_loss_grad(y["q"], y["k"], y["q_idx"], y["k_idx"], I, np.ones((1, 130)),
+                              block_size=B)
+    assert np.abs(out["dq_idx"]).max() < 1e-12 and np.abs(out["dk_idx"]).max() < 1e-12
