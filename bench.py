@@ -412,7 +412,39 @@ def time_kl(msa, pcfg, x, bufs, K, sizes, pk, world):
     msa.msa_device_status()
     ms = max_over_ranks(float(np.mean([evs[s].elapsed_time(evs[s + 1]) for s in range(K)])), world)
     achieved = sizes["F_kl"] / (ms * 1e-3) / 1e12
+    # the index-branch gradient of the loss (teacher fixed), on the same inputs, g = 1 per row
+    lse_idx = torch.empty((pcfg.H_kv, N), dtype=torch.float32, device="cuda")
+    psum = torch.empty_like(lse_idx)
+    msa.msa_kl_loss_fwd(x["q"], x["k"], x["q_idx"], x["k_idx"], bufs["idx"], bufs["lse"], kl=kl,
+                        ws=ws, lse_idx=lse_idx, p_sum=psum)
+    del ws
+    g = torch.ones_like(lse_idx)
+    dq = torch.empty((N, pcfg.H_kv, pcfg.d_idx), dtype=torch.float32, device="cuda")
+    dk = torch.empty((N, pcfg.d_idx), dtype=torch.float32, device="cuda")
+    wsb = torch.empty(msa.msa_kl_loss_bwd_workspace(N, pcfg.H_kv, pcfg.d_idx, pcfg.k),
+                      dtype=torch.uint8, device="cuda")
+
+    def bwd():
+        msa.msa_kl_loss_bwd(x["q"], x["k"], x["q_idx"], x["k_idx"], bufs["idx"], bufs["lse"],
+                            lse_idx, psum, g, dq_idx=dq, dk_idx=dk, ws=wsb)
+
+    for _ in range(3):
+        bwd()
+    torch.cuda.synchronize()
+    evb = [torch.cuda.Event(enable_timing=True) for _ in range(K + 1)]
+    evb[0].record(stream)
+    for s in range(K):
+        bwd()
+        evb[s + 1].record(stream)
+    torch.cuda.synchronize()
+    msa.msa_device_status()
+    del wsb
+    ms_b = max_over_ranks(float(np.mean([evb[s].elapsed_time(evb[s + 1]) for s in range(K)])),
+                          world)
     return {"ms": round(ms, 4), "value": round(world * N / (ms * 1e-3), 1), "unit": "tokens/s",
+            "backward_index_branch": {"ms": round(ms_b, 4),
+                                      "value": round(world * N / (ms_b * 1e-3), 1),
+                                      "unit": "tokens/s", "gpu_launches_per_call": KL_LAUNCHES + 1},
             "mean_kl": round(float(kl.mean()), 6), "gpu_launches_per_call": KL_LAUNCHES,
             "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": pk["bf16_sust"],
                          "unit": "TFLOP/s", "frac": round(achieved / pk["bf16_sust"], 4),

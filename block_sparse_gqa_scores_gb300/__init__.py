@@ -6,5 +6,5 @@ from .msa import (MSAError, msa_device_status, msa_index_block_scores,  # noqa: 
                   msa_index_select, msa_select_blocks, msa_sparse_attn_fwd, msa_sparse_attn_fwd_workspace,
                   msa_sparse_decode, msa_sparse_decode_workspace, msa_sparse_decode_paged,
                   msa_prefill_varlen,
-                  msa_kl_loss_fwd,
+                  msa_kl_loss_fwd, msa_kl_loss_bwd, msa_kl_loss_bwd_workspace,
                   msa_kl_loss_fwd_workspace)

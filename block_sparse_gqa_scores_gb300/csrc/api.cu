@@ -328,11 +328,12 @@ MSA_API size_t msa_kl_loss_fwd_workspace(int64_t N, int H_kv, int k) {
 
 MSA_API msa_status_t msa_kl_loss_fwd(const void* q, const void* k, const void* q_idx,
                                      const void* k_idx, const int32_t* idx, const float* lse,
-                                     float* kl, int64_t N, int H_q, int H_kv, int d_h, int d_idx,
-                                     int block_size, int k_blocks, void* ws, size_t ws_bytes,
-                                     void* stream) {
+                                     float* kl, float* lse_idx, float* p_sum, int64_t N, int H_q,
+                                     int H_kv, int d_h, int d_idx, int block_size, int k_blocks,
+                                     void* ws, size_t ws_bytes, void* stream) {
   if (!aligned16(q) || !aligned16(k) || !aligned16(q_idx) || !aligned16(k_idx) ||
-      !aligned4(idx) || !aligned4(lse) || !aligned4(kl) || !aligned16(ws))
+      !aligned4(idx) || !aligned4(lse) || !aligned4(kl) || !aligned16(ws) ||
+      (lse_idx && !aligned4(lse_idx)) || (p_sum && !aligned4(p_sum)))
     return MSA_ERR_INVALID_ARGUMENT;
   if (N < 1 || H_q < 1 || H_kv < 1 || H_q % H_kv != 0 || d_h < 1 || d_idx < 1 ||
       block_size != 64 || k_blocks < 1 || k_blocks > 64)
@@ -342,8 +343,37 @@ MSA_API msa_status_t msa_kl_loss_fwd(const void* q, const void* k, const void* q
     return MSA_ERR_UNSUPPORTED;
   if (N > ((int64_t)1 << 21) || N * H_kv * k_blocks >= kMaxRows) return MSA_ERR_UNSUPPORTED;
   if (ws_bytes < msa::kl_ws_bytes(N, H_kv, k_blocks)) return MSA_ERR_WORKSPACE;
-  return from_cuda(msa::launch_kl_loss_fwd(q, k, q_idx, k_idx, idx, lse, kl, N, H_q, H_kv, d_h,
-                                           d_idx, k_blocks, ws, (cudaStream_t)stream));
+  return from_cuda(msa::launch_kl_loss_fwd(q, k, q_idx, k_idx, idx, lse, kl, lse_idx, p_sum, N,
+                                           H_q, H_kv, d_h, d_idx, k_blocks, ws,
+                                           (cudaStream_t)stream));
+}
+
+MSA_API size_t msa_kl_loss_bwd_workspace(int64_t N, int H_kv, int d_idx, int k) {
+  if (N < 1 || H_kv < 1 || k < 1 || k > 64 || d_idx < 1) return 0;
+  return msa::kl_bwd_ws_bytes(N, H_kv, d_idx, k);
+}
+
+MSA_API msa_status_t msa_kl_loss_bwd(const void* q, const void* k, const void* q_idx,
+                                     const void* k_idx, const int32_t* idx, const float* lse,
+                                     const float* lse_idx, const float* p_sum,
+                                     const float* grad_kl, float* dq_idx, float* dk_idx, int64_t N,
+                                     int H_q, int H_kv, int d_h, int d_idx, int block_size,
+                                     int k_blocks, void* ws, size_t ws_bytes, void* stream) {
+  if (!aligned16(q) || !aligned16(k) || !aligned16(q_idx) || !aligned16(k_idx) ||
+      !aligned4(idx) || !aligned4(lse) || !aligned4(lse_idx) || !aligned4(p_sum) ||
+      !aligned4(grad_kl) || !aligned16(dq_idx) || !aligned16(dk_idx) || !aligned16(ws))
+    return MSA_ERR_INVALID_ARGUMENT;
+  if (N < 1 || H_q < 1 || H_kv < 1 || H_q % H_kv != 0 || d_h < 1 || d_idx < 1 ||
+      block_size != 64 || k_blocks < 1 || k_blocks > 64)
+    return MSA_ERR_INVALID_ARGUMENT;
+  if (!pow2_upto(H_kv, 8) || H_q / H_kv != 8 || (d_h != 64 && d_h != 128) ||
+      (d_idx != 32 && d_idx != 64))
+    return MSA_ERR_UNSUPPORTED;
+  if (N > ((int64_t)1 << 21) || N * H_kv * k_blocks >= kMaxRows) return MSA_ERR_UNSUPPORTED;
+  if (ws_bytes < msa::kl_bwd_ws_bytes(N, H_kv, d_idx, k_blocks)) return MSA_ERR_WORKSPACE;
+  return from_cuda(msa::launch_kl_loss_bwd(q, k, q_idx, k_idx, idx, lse, lse_idx, p_sum, grad_kl,
+                                           dq_idx, dk_idx, N, H_q, H_kv, d_h, d_idx, k_blocks, ws,
+                                           (cudaStream_t)stream));
 }
 
 MSA_API msa_status_t msa_device_status(void) {

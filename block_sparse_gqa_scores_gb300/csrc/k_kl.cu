@@ -189,19 +189,36 @@ struct KlQMaps {
 // issues one box at a time, so several warps keep more of them in flight), warp 10 loads the
 // keys and index queries, warp 1 issues the MMAs, warps 2..9 are two epilogue groups of four
 // (one warp per TMEM lane quarter) that take alternate work tiles.
-constexpr int kKlQWarps = 4;
-constexpr int kKlWarps = 10 + 1 + (kKlQWarps - 1);
-constexpr int kKlWsThreads = 32 * kKlWarps;
+// The gradient pass keeps per-thread key-gradient accumulators, so it runs one query-row warp
+// (more registers per thread) where the loss pass runs four.
+template <bool BWD>
+struct KlWarps {
+  static constexpr int kQ = BWD ? 1 : 4;            // query-row warps
+  static constexpr int kAll = 10 + 1 + (kQ - 1);
+  static constexpr int kThreads = 32 * kAll;
+};
 
-template <int D_H, int G>
-__global__ void __launch_bounds__(kKlWsThreads, 1)
+// Gradient inputs and outputs (the BWD instantiation only): per row the upstream gradient, the
+// student's LSE over T and the teacher's mass, from the loss pass; per selection a partial of
+// dQ_idx (d_idx floats at its (group, row, slot) position); dK_idx accumulated in fp32.
+struct KlGrad {
+  const float* grad_kl;     // [H_kv, N]
+  const float* lse_idx;     // [H_kv, N], natural log
+  const float* psum;        // [H_kv, N]
+  float* part_dq;           // [H_kv, N, k, d_idx]
+  float* dk_idx;            // [N, d_idx], zeroed before the pass
+};
+
+template <int D_H, int G, bool BWD>
+__global__ void __launch_bounds__(KlWarps<BWD>::kThreads, 1)
     k_kl_kvouter(const __grid_constant__ KlQMaps tm_q, const __nv_bfloat16* __restrict__ q,
                  const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ q_idx,
                  const __nv_bfloat16* __restrict__ k_idx, const float* __restrict__ lse,
                  const int* __restrict__ entries, const int* __restrict__ offset,
                  const int* __restrict__ tile_off, int nbuckets, int64_t nblk, int64_t N,
                  int H_kv, int d_idx, int kk, float4* __restrict__ part, float scale_log2,
-                 float idx_scale) {
+                 float idx_scale, const KlGrad gr) {
+  constexpr int kKlQWarps = KlWarps<BWD>::kQ;
   using L = KlSmem<D_H, G>;
   constexpr int kEpt = L::kEpt;
   constexpr int kQStages = L::kQStages, kKStages = L::kKStages, kTStages = L::kTStages;
@@ -482,6 +499,11 @@ __global__ void __launch_bounds__(kKlWsThreads, 1)
         lse_raw = __ldg(lse + (int64_t)(r0 * G + h) * N + (ent >> 6));
       }
     }
+    // gradient pass: key-gradient accumulators of this thread's (token, dims) of the current
+    // bucket's block, flushed to dK_idx with fp32 atomics when the group's bucket changes
+    float dkacc[BWD ? 32 : 1];
+#pragma unroll
+    for (int d = 0; d < (BWD ? 32 : 1); ++d) dkacc[d] = 0.f;
     for (int j = grp; j < ntiles; j += 2) {
       const int r = (int)(c_bkt / nblk);
       const int64_t b = c_bkt - (int64_t)r * nblk;
@@ -577,8 +599,97 @@ __global__ void __launch_bounds__(kKlWsThreads, 1)
         l = l * ex2(mx - nm) + lo * ex2(mo - nm);
         mx = nm;
       }
-      if (rv && h == 0)
+      if (!BWD && rv && h == 0)
         part[((int64_t)r * N + (cur_ent >> 6)) * kk + (cur_ent & 63)] = make_float4(C, W, mx, l);
+      if constexpr (BWD) {
+        // dS of this lane's columns: g (W P^idx - P) / sqrt(d_idx), with the row's upstream
+        // gradient g, teacher mass W and student LSE from the loss pass; 0 where not visible
+        float g = 0.f, wsum = 0.f, lsei2 = 0.f;
+        if (rv) {
+          const int64_t row = (int64_t)r * N + (cur_ent >> 6);
+          g = __ldg(gr.grad_kl + row);
+          wsum = __ldg(gr.psum + row);
+          lsei2 = __ldg(gr.lse_idx + row) * kLog2e;
+        }
+#pragma unroll
+        for (int c = 0; c < kCpl; ++c) {
+          const float pidx = ex2(si[c] * idx_scale * kLog2e - lsei2);
+          const float ds = g * (wsum * pidx - a[c] * invG) * idx_scale;
+          s_si[e * 64 + cb + c] = cb + c <= cmax ? ds : 0.f;
+        }
+        kl_group_sync(1 + grp);                            // dS [entry][token] is complete
+        const int64_t tok0 = b * kBlock;
+        // dQ_idx of entry R / 8, dims (R % 8) * d_idx / 8 ..: sum over the block's tokens
+        {
+          const int eq = R >> 3, nd = d_idx >> 3, d0 = (R & 7) * nd;
+          if (eq < c_ne) {
+            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            for (int c = 0; c < kBlock; ++c) {
+              if (tok0 + c >= N) break;
+              const float ds = s_si[eq * 64 + c];
+              const __nv_bfloat16* kr = k_idx + (tok0 + c) * d_idx + d0;
+              if (nd == 8) {
+                const uint4 v = ldg_nc_v4(kr);
+                const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                  const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w4[u]));
+                  acc[2 * u] += ds * f.x;
+                  acc[2 * u + 1] += ds * f.y;
+                }
+              } else {
+                const uint2 v = *reinterpret_cast<const uint2*>(kr);
+                const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.x));
+                const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.y));
+                acc[0] += ds * f0.x;
+                acc[1] += ds * f0.y;
+                acc[2] += ds * f1.x;
+                acc[3] += ds * f1.y;
+              }
+            }
+            const int ent_q = __ldg(entries + c_e0 + eq);
+            float* dst = gr.part_dq +
+                         (((int64_t)r * N + (ent_q >> 6)) * kk + (ent_q & 63)) * d_idx + d0;
+#pragma unroll
+            for (int d = 0; d < 8; ++d)
+              if (d < nd) dst[d] = acc[d];
+          }
+        }
+        // dK_idx of token R / 2, dims (R % 2) * d_idx / 2 ..: sum over the tile's entries
+        {
+          const int ck = R >> 1, nd = d_idx >> 1, d0 = (R & 1) * nd;
+          for (int eq = 0; eq < c_ne; ++eq) {
+            const float ds = s_si[eq * 64 + ck];
+            if (ds == 0.f) continue;
+            const int ent_q = __ldg(entries + c_e0 + eq);
+            const __nv_bfloat16* qr = q_idx + ((int64_t)(ent_q >> 6) * H_kv + r) * d_idx + d0;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              if (8 * u >= nd) break;
+              const uint4 v = ldg_nc_v4(qr + 8 * u);
+              const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+              for (int t = 0; t < 4; ++t) {
+                const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w4[t]));
+                dkacc[8 * u + 2 * t] += ds * f.x;
+                dkacc[8 * u + 2 * t + 1] += ds * f.y;
+              }
+            }
+          }
+          kl_group_sync(1 + grp);                          // s_si may be overwritten
+          const bool flush = !has_next || (int64_t)(n_bkt % nblk) != b;
+          if (flush) {
+            if (tok0 + ck < N) {
+              float* dst = gr.dk_idx + (tok0 + ck) * d_idx + d0;
+#pragma unroll
+              for (int d = 0; d < 32; ++d)
+                if (d < nd) atomicAdd(dst + d, dkacc[d]);
+            }
+#pragma unroll
+            for (int d = 0; d < 32; ++d) dkacc[d] = 0.f;
+          }
+        }
+      }
       c_bkt = n_bkt;
       c_e0 = n_e0;
       c_ne = n_ne;
@@ -596,7 +707,7 @@ __global__ void __launch_bounds__(kKlWsThreads, 1)
 // the entries' (max, sum) pairs in slot order.
 __global__ void __launch_bounds__(256)
     k_kl_merge(const int32_t* __restrict__ idx, const float4* __restrict__ part, float* kl,
-               int64_t N, int H_kv, int kk) {
+               float* lse_idx, float* psum, int64_t N, int H_kv, int kk) {
   const int64_t x = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (x >= (int64_t)H_kv * N) return;
   const int64_t i = x % N;
@@ -613,7 +724,29 @@ __global__ void __launch_bounds__(256)
     l = l * ex2(mx - nm) + v.w * ex2(v.z - nm);
     mx = nm;
   }
-  kl[x] = C + W * (mx + __log2f(l)) * kLn2;
+  const float lsei = (mx + __log2f(l)) * kLn2;
+  kl[x] = C + W * lsei;
+  if (lse_idx) lse_idx[x] = lsei;                 // by-products for the gradient pass
+  if (psum) psum[x] = W;
+}
+
+// dQ_idx[i, r, :] = sum over the row's selections (slot order) of their partials.
+__global__ void __launch_bounds__(256)
+    k_kl_dq_merge(const int32_t* __restrict__ idx, const float* __restrict__ part_dq,
+                  float* __restrict__ dq_idx, int64_t N, int H_kv, int kk, int d_idx) {
+  const int64_t x = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;   // ((r * N + i) * d_idx + d)
+  if (x >= (int64_t)H_kv * N * d_idx) return;
+  const int64_t ri = x / d_idx;
+  const int d = (int)(x - ri * d_idx);
+  const int64_t r = ri / N, i = ri - r * N;
+  const int32_t* sel = idx + ri * kk;
+  float acc = 0.f;
+  for (int t = 0; t < kk; ++t) {
+    const int b = __ldg(sel + t);
+    if (b < 0 || (int64_t)b > (i >> 6)) continue;
+    acc += __ldg(part_dq + (ri * kk + t) * d_idx + d);
+  }
+  dq_idx[(i * H_kv + r) * d_idx + d] = acc;
 }
 
 }  // namespace
@@ -625,10 +758,18 @@ size_t kl_ws_bytes(int64_t N, int H_kv, int kk) {
   return 4 * a256(4 * (size_t)(nb + 1)) + a256(4 * sel) + a256(16 * sel);
 }
 
-cudaError_t launch_kl_loss_fwd(const void* q, const void* k, const void* q_idx, const void* k_idx,
-                               const int32_t* idx, const float* lse, float* kl, int64_t N, int H_q,
-                               int H_kv, int d_h, int d_idx, int kk, void* ws,
-                               cudaStream_t st) {
+size_t kl_bwd_ws_bytes(int64_t N, int H_kv, int d_idx, int kk) {
+  auto a256 = [](size_t x) { return (x + 255) & ~size_t(255); };
+  return kl_ws_bytes(N, H_kv, kk) + a256(4 * (size_t)H_kv * N * kk * d_idx);
+}
+
+namespace {
+
+// Plan (bucket every selection by (group, block)), then the block-major pass, forward or gradient.
+cudaError_t kl_pass(bool bwd, const void* q, const void* k, const void* q_idx, const void* k_idx,
+                    const int32_t* idx, const float* lse, int64_t N, int H_q, int H_kv, int d_h,
+                    int d_idx, int kk, void* ws, const KlGrad& gr, float4** part_out,
+                    cudaStream_t st) {
   const int G = H_q / H_kv;
   const int64_t nblk = (N + kBlock - 1) / kBlock;
   const int nb = (int)(H_kv * nblk);
@@ -641,6 +782,7 @@ cudaError_t launch_kl_loss_fwd(const void* q, const void* k, const void* q_idx, 
   int* cursor = reinterpret_cast<int*>(base + 3 * a256(4 * (size_t)(nb + 1)));
   int* entries = reinterpret_cast<int*>(base + 4 * a256(4 * (size_t)(nb + 1)));
   float4* part = reinterpret_cast<float4*>(base + 4 * a256(4 * (size_t)(nb + 1)) + a256(4 * sel));
+  *part_out = part;
 
   cudaError_t e = cudaMemsetAsync(count, 0, sizeof(int) * (size_t)nb, st);
   if (e != cudaSuccess) return e;
@@ -671,28 +813,61 @@ cudaError_t launch_kl_loss_fwd(const void* q, const void* k, const void* q_idx, 
   const auto* kp = static_cast<const __nv_bfloat16*>(k);
   const auto* qi = static_cast<const __nv_bfloat16*>(q_idx);
   const auto* ki = static_cast<const __nv_bfloat16*>(k_idx);
-  auto run = [&](auto kern, int smem) -> cudaError_t {
+  auto run = [&](auto kern, int smem, int threads) -> cudaError_t {
     cudaError_t x = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (x != cudaSuccess) return x;
     const int grid = sms;                                  // persistent: one CTA per SM
-    kern<<<grid, kKlWsThreads, smem, st>>>(tq, qq, kp, qi, ki, lse, entries, offset, tile_off, nb,
-                                         nblk, N, H_kv, d_idx, kk, part, scale_log2, idx_scale);
+    kern<<<grid, threads, smem, st>>>(tq, qq, kp, qi, ki, lse, entries, offset, tile_off, nb,
+                                      nblk, N, H_kv, d_idx, kk, part, scale_log2, idx_scale, gr);
     return cudaGetLastError();
   };
-  auto dispatch_g = [&](auto dh) -> cudaError_t {
+  auto dispatch = [&](auto dh) -> cudaError_t {
     constexpr int D = decltype(dh)::value;
+    if (bwd)   // the gradient pass exists for G = 8 (checked by the caller)
+      return run(k_kl_kvouter<D, 8, true>, KlSmem<D, 8>::kAlloc, KlWarps<true>::kThreads);
+    constexpr int T = KlWarps<false>::kThreads;
     switch (G) {
-      case 1: return run(k_kl_kvouter<D, 1>, KlSmem<D, 1>::kAlloc);
-      case 2: return run(k_kl_kvouter<D, 2>, KlSmem<D, 2>::kAlloc);
-      case 4: return run(k_kl_kvouter<D, 4>, KlSmem<D, 4>::kAlloc);
-      default: return run(k_kl_kvouter<D, 8>, KlSmem<D, 8>::kAlloc);
+      case 1: return run(k_kl_kvouter<D, 1, false>, KlSmem<D, 1>::kAlloc, T);
+      case 2: return run(k_kl_kvouter<D, 2, false>, KlSmem<D, 2>::kAlloc, T);
+      case 4: return run(k_kl_kvouter<D, 4, false>, KlSmem<D, 4>::kAlloc, T);
+      default: return run(k_kl_kvouter<D, 8, false>, KlSmem<D, 8>::kAlloc, T);
     }
   };
-  e = d_h == 128 ? dispatch_g(std::integral_constant<int, 128>())
-                 : dispatch_g(std::integral_constant<int, 64>());
+  return d_h == 128 ? dispatch(std::integral_constant<int, 128>())
+                    : dispatch(std::integral_constant<int, 64>());
+}
+
+}  // namespace
+
+cudaError_t launch_kl_loss_fwd(const void* q, const void* k, const void* q_idx, const void* k_idx,
+                               const int32_t* idx, const float* lse, float* kl, float* lse_idx,
+                               float* psum, int64_t N, int H_q, int H_kv, int d_h, int d_idx,
+                               int kk, void* ws, cudaStream_t st) {
+  float4* part = nullptr;
+  cudaError_t e = kl_pass(false, q, k, q_idx, k_idx, idx, lse, N, H_q, H_kv, d_h, d_idx, kk, ws,
+                          KlGrad{}, &part, st);
   if (e != cudaSuccess) return e;
   const int64_t n = (int64_t)H_kv * N;
-  k_kl_merge<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(idx, part, kl, N, H_kv, kk);
+  k_kl_merge<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(idx, part, kl, lse_idx, psum, N, H_kv,
+                                                          kk);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_kl_loss_bwd(const void* q, const void* k, const void* q_idx, const void* k_idx,
+                               const int32_t* idx, const float* lse, const float* lse_idx,
+                               const float* psum, const float* grad_kl, float* dq_idx,
+                               float* dk_idx, int64_t N, int H_q, int H_kv, int d_h, int d_idx,
+                               int kk, void* ws, cudaStream_t st) {
+  float* part_dq = reinterpret_cast<float*>(static_cast<char*>(ws) + kl_ws_bytes(N, H_kv, kk));
+  cudaError_t e = cudaMemsetAsync(dk_idx, 0, sizeof(float) * (size_t)N * d_idx, st);
+  if (e != cudaSuccess) return e;
+  const KlGrad gr{grad_kl, lse_idx, psum, part_dq, dk_idx};
+  float4* part = nullptr;
+  e = kl_pass(true, q, k, q_idx, k_idx, idx, lse, N, H_q, H_kv, d_h, d_idx, kk, ws, gr, &part, st);
+  if (e != cudaSuccess) return e;
+  const int64_t n = (int64_t)H_kv * N * d_idx;
+  k_kl_dq_merge<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(idx, part_dq, dq_idx, N, H_kv, kk,
+                                                             d_idx);
   return cudaGetLastError();
 }
 

@@ -62,9 +62,16 @@ cudaError_t read_reset_score_status(unsigned* out);
 // KL alignment loss forward: workspace bytes and the launch sequence (plan, scan, block-major
 // partials, merge).
 size_t kl_ws_bytes(int64_t N, int H_kv, int kk);
+size_t kl_bwd_ws_bytes(int64_t N, int H_kv, int d_idx, int kk);
 cudaError_t launch_kl_loss_fwd(const void* q, const void* k, const void* q_idx, const void* k_idx,
-                               const int32_t* idx, const float* lse, float* kl, int64_t N, int H_q,
-                               int H_kv, int d_h, int d_idx, int kk, void* ws, cudaStream_t st);
+                               const int32_t* idx, const float* lse, float* kl, float* lse_idx,
+                               float* psum, int64_t N, int H_q, int H_kv, int d_h, int d_idx,
+                               int kk, void* ws, cudaStream_t st);
+cudaError_t launch_kl_loss_bwd(const void* q, const void* k, const void* q_idx, const void* k_idx,
+                               const int32_t* idx, const float* lse, const float* lse_idx,
+                               const float* psum, const float* grad_kl, float* dq_idx,
+                               float* dk_idx, int64_t N, int H_q, int H_kv, int d_h, int d_idx,
+                               int kk, void* ws, cudaStream_t st);
 cudaError_t read_reset_kl_status(unsigned* out);
 
 cudaError_t launch_select_prefill(const float* M, int32_t* idx, int64_t N, int H_kv, int k,

@@ -54,11 +54,16 @@ def _load():
                                      P, sz, P]
     L.msa_kl_loss_fwd_workspace.argtypes = [i64, i32, i32]
     L.msa_kl_loss_fwd_workspace.restype = sz
-    L.msa_kl_loss_fwd.argtypes = [P, P, P, P, P, P, P, i64, i32, i32, i32, i32, i32, i32, P, sz, P]
+    L.msa_kl_loss_fwd.argtypes = [P, P, P, P, P, P, P, P, P, i64, i32, i32, i32, i32, i32, i32, P,
+                                  sz, P]
+    L.msa_kl_loss_bwd_workspace.argtypes = [i64, i32, i32, i32]
+    L.msa_kl_loss_bwd_workspace.restype = sz
+    L.msa_kl_loss_bwd.argtypes = [P, P, P, P, P, P, P, P, P, P, P, i64, i32, i32, i32, i32, i32,
+                                  i32, P, sz, P]
     for fn in ("msa_index_block_scores", "msa_select_blocks", "msa_index_select", "msa_sparse_attn_fwd",
                "msa_sparse_decode", "msa_sparse_decode_noalloc", "msa_sparse_decode_paged",
                "msa_prefill_varlen",
-               "msa_kl_loss_fwd",
+               "msa_kl_loss_fwd", "msa_kl_loss_bwd",
                "msa_device_status"):
         getattr(L, fn).restype = i32
     return L
@@ -281,8 +286,9 @@ def msa_kl_loss_fwd_workspace(N, H_kv, k):
 
 
 def msa_kl_loss_fwd(q, k, q_idx, k_idx, idx, lse, kl=None, ws=None, block_size=BLOCK,
-                    stream=None):
-    """KL alignment loss per (group, row): KL [H_kv, N] fp32, teacher from the forward's LSE."""
+                    stream=None, lse_idx=None, p_sum=None):
+    """KL alignment loss per (group, row): KL [H_kv, N] fp32, teacher from the forward's LSE.
+    lse_idx / p_sum ([H_kv, N] fp32, optional) receive what msa_kl_loss_bwd needs."""
     _req(q, torch.bfloat16, 3, "q")
     _req(k, torch.bfloat16, 3, "k")
     _req(q_idx, torch.bfloat16, 3, "q_idx")
@@ -298,9 +304,37 @@ def msa_kl_loss_fwd(q, k, q_idx, k_idx, idx, lse, kl=None, ws=None, block_size=B
     if ws is None and nws:
         ws = torch.empty(nws, dtype=torch.uint8, device=q.device)
     _check("msa_kl_loss_fwd", lib.msa_kl_loss_fwd(
-        _ptr(q), _ptr(k), _ptr(q_idx), _ptr(k_idx), _ptr(idx), _ptr(lse), _ptr(kl), N, H_q, H_kv,
-        d_h, d_idx, block_size, kk, _ptr(ws), 0 if ws is None else ws.numel(), _stream(stream)))
+        _ptr(q), _ptr(k), _ptr(q_idx), _ptr(k_idx), _ptr(idx), _ptr(lse), _ptr(kl), _ptr(lse_idx),
+        _ptr(p_sum), N, H_q, H_kv, d_h, d_idx, block_size, kk, _ptr(ws),
+        0 if ws is None else ws.numel(), _stream(stream)))
     return kl
+
+
+def msa_kl_loss_bwd_workspace(N, H_kv, d_idx, k):
+    return int(lib.msa_kl_loss_bwd_workspace(N, H_kv, d_idx, k))
+
+
+def msa_kl_loss_bwd(q, k, q_idx, k_idx, idx, lse, lse_idx, p_sum, grad_kl, dq_idx=None,
+                    dk_idx=None, ws=None, block_size=BLOCK, stream=None):
+    """Index-branch gradient of sum(grad_kl * KL), teacher fixed -> (dq_idx [N,H_kv,d_idx],
+    dk_idx [N,d_idx]) fp32."""
+    for t, n in ((lse_idx, "lse_idx"), (p_sum, "p_sum"), (grad_kl, "grad_kl")):
+        _req(t, torch.float32, 2, n)
+    N, H_q, d_h = q.shape
+    H_kv, d_idx = k.shape[1], q_idx.shape[2]
+    kk = idx.shape[2]
+    if dq_idx is None:
+        dq_idx = torch.empty((N, H_kv, d_idx), dtype=torch.float32, device=q.device)
+    if dk_idx is None:
+        dk_idx = torch.empty((N, d_idx), dtype=torch.float32, device=q.device)
+    if ws is None:
+        ws = torch.empty(msa_kl_loss_bwd_workspace(N, H_kv, d_idx, kk), dtype=torch.uint8,
+                         device=q.device)
+    _check("msa_kl_loss_bwd", lib.msa_kl_loss_bwd(
+        _ptr(q), _ptr(k), _ptr(q_idx), _ptr(k_idx), _ptr(idx), _ptr(lse), _ptr(lse_idx),
+        _ptr(p_sum), _ptr(grad_kl), _ptr(dq_idx), _ptr(dk_idx), N, H_q, H_kv, d_h, d_idx,
+        block_size, kk, _ptr(ws), ws.numel(), _stream(stream)))
+    return dq_idx, dk_idx
 
 
 def msa_device_status():

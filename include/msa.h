@@ -237,15 +237,42 @@ size_t msa_kl_loss_fwd_workspace(int64_t N, int H_kv, int k);
  *   lse  fp32 [H_q, N], the natural-log LSE msa_sparse_attn_fwd wrote for the same q, k, idx
  *        (with another lse the teacher rows do not sum to 1 and the result is not a KL);
  *   kl   fp32 [H_kv, N];
+ *   lse_idx, p_sum  fp32 [H_kv, N] or NULL: the student's LSE over T (natural log) and the
+ *        teacher's mass sum_j P_j, which msa_kl_loss_bwd takes;
  *   ws   device workspace of at least msa_kl_loss_fwd_workspace() bytes, 16-byte aligned
  *        (contents ignored on entry, unspecified on return; one call at a time per workspace).
  * fp32 arithmetic from bf16 inputs.  Each selection's contribution is computed independently
  * and a row's contributions are combined in slot order, with no atomic update of any result.
  * Errors as msa_sparse_attn_fwd; N > 2^21 or H_kv * N * k >= 2^31: MSA_ERR_UNSUPPORTED. */
 msa_status_t msa_kl_loss_fwd(const void *q, const void *k, const void *q_idx, const void *k_idx,
-                             const int32_t *idx, const float *lse, float *kl, int64_t N, int H_q,
-                             int H_kv, int d_h, int d_idx, int block_size, int k_blocks, void *ws,
-                             size_t ws_bytes, void *stream);
+                             const int32_t *idx, const float *lse, float *kl, float *lse_idx,
+                             float *p_sum, int64_t N, int H_q, int H_kv, int d_h, int d_idx,
+                             int block_size, int k_blocks, void *ws, size_t ws_bytes,
+                             void *stream);
+
+/* Workspace bytes msa_kl_loss_bwd needs: that of msa_kl_loss_fwd plus one d_idx-float partial of
+ * dQ_idx per selection (2.15 GB at N = 131072, H_kv = 4, k = 16, d_idx = 64). */
+size_t msa_kl_loss_bwd_workspace(int64_t N, int H_kv, int d_idx, int k);
+
+/* Gradient of the KL alignment loss with respect to the index branch (part of the training
+ * backward; the teacher is held fixed -- the gradient detach of section 训练).  For the scalar
+ * L = sum_{r,i} grad_kl[r,i] * kl[r,i], with kl as msa_kl_loss_fwd defines it:
+ *   dS_j = grad_kl[r,i] * (p_sum[r,i] * P^idx_j - P_j) / sqrt(d_idx)   for j in T (else 0)
+ *   dq_idx[i,r,:] = sum_j dS_j k_idx[j,:],   dk_idx[j,:] = sum over (r,i) with j in T of dS_j q_idx[i,r,:]
+ * where P^idx_j = exp(q_idx[i,r,:].k_idx[j,:]/sqrt(d_idx) - lse_idx[r,i]) and P_j the teacher.
+ *   lse_idx, p_sum  fp32 [H_kv, N] as msa_kl_loss_fwd wrote them for the same inputs
+ *   grad_kl         fp32 [H_kv, N]  the upstream gradient of each row's loss
+ *   dq_idx          fp32 [N, H_kv, d_idx] (written);  dk_idx fp32 [N, d_idx] (written)
+ *   other arguments as msa_kl_loss_fwd; ws of msa_kl_loss_bwd_workspace() bytes.
+ * dq_idx sums its row's selections in slot order; dk_idx is accumulated with fp32 atomic adds,
+ * so its last bits depend on the order blocks are processed in.  G = H_q/H_kv must be 8
+ * (otherwise MSA_ERR_UNSUPPORTED). */
+msa_status_t msa_kl_loss_bwd(const void *q, const void *k, const void *q_idx, const void *k_idx,
+                             const int32_t *idx, const float *lse, const float *lse_idx,
+                             const float *p_sum, const float *grad_kl, float *dq_idx,
+                             float *dk_idx, int64_t N, int H_q, int H_kv, int d_h, int d_idx,
+                             int block_size, int k_blocks, void *ws, size_t ws_bytes,
+                             void *stream);
 
 /* Reads and clears the device status words of the current device (synchronising call).
  * Returns MSA_ERR_TIMEOUT if any kernel since the last call gave up a bounded wait,

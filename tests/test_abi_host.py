@@ -27,7 +27,8 @@ def test_header_declares_the_api():
     for name in ("msa_index_block_scores", "msa_select_blocks", "msa_index_select",
                  "msa_sparse_attn_fwd", "msa_sparse_attn_fwd_workspace", "msa_sparse_decode",
                  "msa_sparse_decode_workspace", "msa_sparse_decode_paged", "msa_prefill_varlen",
-                 "msa_prefill_varlen_workspace", "msa_kl_loss_fwd",
+                 "msa_prefill_varlen_workspace", "msa_kl_loss_fwd", "msa_kl_loss_bwd",
+                 "msa_kl_loss_bwd_workspace",
                  "msa_kl_loss_fwd_workspace",
                  "msa_status_string", "msa_device_status"):
         assert name in syms
@@ -79,7 +80,8 @@ def decode(lib, q=P, S=4, max_len=1000, H_q=32, H_kv=4, d_h=128, d_idx=64, B=64,
 
 def kl(lib, q=P, k=P, qi=P, ki=P, idx=P, lse=P, out=P, N=1024, H_q=32, H_kv=4, d_h=128, d_idx=64,
        B=64, kk=16, ws=P, wsb=1 << 40):
-    return lib.msa_kl_loss_fwd(q, k, qi, ki, idx, lse, out, i64(N), H_q, H_kv, d_h, d_idx, B, kk,
+    return lib.msa_kl_loss_fwd(q, k, qi, ki, idx, lse, out, NUL, NUL, i64(N), H_q, H_kv, d_h, d_idx,
+                               B, kk,
                                ws, ctypes.c_size_t(wsb), NUL)
 
 
@@ -235,3 +237,25 @@ def test_prefill_varlen_unsupported_and_workspace(lib):
     need = lib.msa_prefill_varlen_workspace(cu, 3, 32, 4, 128, 16)
     assert need == lib.msa_sparse_attn_fwd_workspace(i64(40000), 32, 4, 128, 16)
     assert varlen(lib, cu=(0, 100, 40100, 41000), wsb=need - 1) == WORKSPACE
+
+
+def klb(lib, gk=P, dq=P, dk=P, N=1024, H_q=32, H_kv=4, d_h=128, d_idx=64, B=64, kk=16, ws=P,
+        wsb=1 << 40):
+    return lib.msa_kl_loss_bwd(P, P, P, P, P, P, P, P, gk, dq, dk, i64(N), H_q, H_kv, d_h, d_idx,
+                               B, kk, ws, ctypes.c_size_t(wsb), NUL)
+
+
+@pytest.mark.parametrize("kw", [dict(gk=NUL), dict(dq=MIS), dict(dk=NUL), dict(N=0), dict(kk=0),
+                                dict(B=32), dict(ws=NUL), dict(H_q=30)])
+def test_kl_bwd_invalid(lib, kw):
+    assert klb(lib, **kw) == INVALID
+
+
+def test_kl_bwd_unsupported_and_workspace(lib):
+    assert klb(lib, H_q=16) == UNSUPPORTED          # G = 4: the gradient pass is built for G = 8
+    assert klb(lib, d_idx=48) == UNSUPPORTED
+    lib.msa_kl_loss_bwd_workspace.restype = ctypes.c_size_t
+    lib.msa_kl_loss_fwd_workspace.restype = ctypes.c_size_t
+    need = lib.msa_kl_loss_bwd_workspace(i64(1024), 4, 64, 16)
+    assert need >= lib.msa_kl_loss_fwd_workspace(i64(1024), 4, 16) + 4 * 4 * 1024 * 16 * 64
+    assert klb(lib, wsb=need - 1) == WORKSPACE

@@ -308,6 +308,41 @@ def test_kl_loss_uniform_teacher():
     check_kl(kl, oracle.kl_loss(b["q"], b["k"], b["q_idx"], b["k_idx"], idx.cpu().numpy()))
 
 
+# ---------------------------------------- KL gradient (index branch, teacher fixed) --
+
+KLB_CASES = [("p32k", {}, 1000, 16), ("p32k", {}, 65, 16), ("p32k", {}, 3000, 16),
+             ("p32k", {}, 2500, 64), ("p32k", dict(d_idx=32), 900, 16),
+             ("p32k", dict(d_h=64), 900, 16), ("p32k", dict(H_q=8, H_kv=1), 700, 5)]
+
+
+@pytest.mark.parametrize("name,over,N,k", KLB_CASES)
+def test_kl_loss_grad(name, over, N, k):
+    """dQ_idx and dK_idx of sum(g * KL) against the oracle's fp64 gradient on the GPU's own
+    selection.  Bound: the same fp32 error sources as the loss (about 1e-5 relative in each
+    probability), plus fp32 atomic accumulation in dK_idx: 1e-3 of the largest magnitude."""
+    cfg = cfg_of(name, k=k, **over)
+    x, b = fresh(cfg, N, seed=41)
+    idx = gpu_index(x, cfg, N)
+    _, lse = msa.msa_sparse_attn_fwd(x["q"], x["k"], x["v"], idx)
+    lse_idx = torch.empty((cfg.H_kv, N), dtype=torch.float32, device="cuda")
+    psum = torch.empty_like(lse_idx)
+    msa.msa_kl_loss_fwd(x["q"], x["k"], x["q_idx"], x["k_idx"], idx, lse, lse_idx=lse_idx,
+                        p_sum=psum)
+    g = torch.rand((cfg.H_kv, N), generator=torch.Generator(device="cuda").manual_seed(3),
+                   device="cuda") * 1.5 + 0.5
+    dq, dk = msa.msa_kl_loss_bwd(x["q"], x["k"], x["q_idx"], x["k_idx"], idx, lse, lse_idx, psum, g)
+    sync_ok()
+    ref = oracle.kl_loss_grad(b["q"], b["k"], b["q_idx"], b["k_idx"], idx.cpu().numpy(),
+                              g.cpu().numpy().astype(np.float64))
+    for got, want in ((dq, ref["dq_idx"]), (dk, ref["dk_idx"])):
+        got = got.cpu().numpy().astype(np.float64)
+        assert np.isfinite(got).all()
+        assert np.abs(got - want).max() <= 1e-3 * np.abs(want).max() + 1e-6, \
+            float(np.abs(got - want).max())
+    assert np.abs(lse_idx.cpu().numpy() - ref["lse_idx"]).max() <= 1e-3
+    assert np.abs(psum.cpu().numpy() - ref["psum"]).max() <= 1e-4
+
+
 # -------------------------------------------------------------- varlen prefill --
 
 @pytest.mark.parametrize("name,lens", [("p32k", [1, 63, 64, 65, 1000, 3000, 4500]),
