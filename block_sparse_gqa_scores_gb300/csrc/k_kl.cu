@@ -40,6 +40,7 @@ constexpr float kLog2e = 1.442695040888963407f;
 // entry -- a ring of two key stages (K_b and K_idx_b of one bucket) and, per epilogue group, the
 // tile's student scores transposed to (entry, token).  TMEM holds kTStages accumulator stages:
 // S (128 rows x 64 tokens) and the student scores (64 tokens on the lanes x the tile's entries).
+constexpr int kSiStride = 68;
 template <int D_H, int G>
 struct KlSmem {
   static constexpr int kEpt = kKlRows / G;        // entries per work tile
@@ -58,8 +59,13 @@ struct KlSmem {
   // the student MMA reads 128 rows of K_idx_b, the last 64 of them past the stage (ignored
   // lanes): the transposed-score buffers (>= 8 KB) follow the key stages
   static constexpr int kOffSi = kOffK + kKStages * kKStage;
-  static constexpr int kSiBytes = kEpt * 64 * 4;  // per epilogue group
-  static constexpr int kOffBar = kOffSi + 2 * kSiBytes;
+  // per epilogue group: [entry][token] at a row stride of kSiStride floats (68: rows of different
+  // entries fall in different banks, and each row stays 16-byte aligned)
+  static constexpr int kSiBytes = kEpt * kSiStride * 4;
+  // gradient pass, per epilogue group: the tile's index queries (one 128-byte row per entry)
+  static constexpr int kOffQg = kOffSi + 2 * kSiBytes;
+  static constexpr int kQgBytes = G == 8 ? kEpt * 128 : 0;   // the gradient pass is G = 8 only
+  static constexpr int kOffBar = kOffQg + 2 * kQgBytes;
   static constexpr int kNumBars = 2 * kQStages + 2 * kKStages + 2 * kTStages;
   static constexpr int kOffMisc = kOffBar + 8 * kNumBars;
   static constexpr int kOffPEnt = kOffMisc + 16;  // each producer warp's copy of a tile's entries
@@ -485,6 +491,7 @@ __global__ void __launch_bounds__(KlWarps<BWD>::kThreads, 1)
     const int R = 32 * qd + lane;                          // row (TMEM lane) of this thread
     const int e = R / G, h = R - e * G;
     float* s_si = reinterpret_cast<float*>(smem + L::kOffSi + grp * L::kSiBytes);
+    const uint32_t s_qg = sb + L::kOffQg + grp * L::kQgBytes;   // gradient pass only
     int bkt = bucket0, nxt = next0;
     // this row's entry and forward LSE, fetched one group-tile ahead
     int c_e0 = 0, c_ne = 0, c_bkt = 0;
@@ -519,6 +526,15 @@ __global__ void __launch_bounds__(KlWarps<BWD>::kThreads, 1)
         ent = R < n_ne * G ? __ldg(entries + n_e0 + e) : 0;
       }
       const int t = j % kTStages;
+      if constexpr (BWD) {
+        // this tile's index queries -> s_qg[entry] (thread R copies 16 bytes of row R / 8; G = 8,
+        // so R / 8 is this thread's own entry), landing under the MMA wait and the loss part
+        const int qc = R & 7;
+        if (rv && qc < (d_idx >> 3))
+          kl_cp_async16(s_qg + (R >> 3) * 128 + qc * 16,
+                        q_idx + ((int64_t)(cur_ent >> 6) * H_kv + r) * d_idx + qc * 8);
+        asm volatile("cp.async.commit_group;" ::: "memory");
+      }
       const bool okw = *s_abort == 0 && mbar_wait(t_full(t), (j / kTStages) & 1, &g_kl_status);
       if (!kl_group_and(1 + grp, okw)) { fail(); break; }
       tc_fence_after();
@@ -531,7 +547,7 @@ __global__ void __launch_bounds__(KlWarps<BWD>::kThreads, 1)
           KL_TMEM_LD16(tbase + 64 + cc, v);
           tmem_ld_wait();
 #pragma unroll
-          for (int c = 0; c < 16; ++c) s_si[(cc + c) * 64 + R] = __uint_as_float(v[c]);
+          for (int c = 0; c < 16; ++c) s_si[(cc + c) * kSiStride + R] = __uint_as_float(v[c]);
         }
       }
       int cmax = -1;                                       // last visible column, -1: none
@@ -562,7 +578,7 @@ __global__ void __launch_bounds__(KlWarps<BWD>::kThreads, 1)
       float si[kCpl];
 #pragma unroll
       for (int c = 0; c < kCpl; c += 4) {
-        const float4 v = *reinterpret_cast<const float4*>(s_si + e * 64 + cb + c);
+        const float4 v = *reinterpret_cast<const float4*>(s_si + e * kSiStride + cb + c);
         si[c] = v.x;
         si[c + 1] = v.y;
         si[c + 2] = v.z;
@@ -615,19 +631,22 @@ __global__ void __launch_bounds__(KlWarps<BWD>::kThreads, 1)
         for (int c = 0; c < kCpl; ++c) {
           const float pidx = ex2(si[c] * idx_scale * kLog2e - lsei2);
           const float ds = g * (wsum * pidx - a[c] * invG) * idx_scale;
-          s_si[e * 64 + cb + c] = cb + c <= cmax ? ds : 0.f;
+          s_si[e * kSiStride + cb + c] = cb + c <= cmax ? ds : 0.f;
         }
-        kl_group_sync(1 + grp);                            // dS [entry][token] is complete
+        asm volatile("cp.async.wait_all;" ::: "memory");   // this thread's index-query copy
+        kl_group_sync(1 + grp);                            // dS and the index queries are complete
         const int64_t tok0 = b * kBlock;
         // dQ_idx of entry R / 8, dims (R % 8) * d_idx / 8 ..: sum over the block's tokens
         {
           const int eq = R >> 3, nd = d_idx >> 3, d0 = (R & 7) * nd;
           if (eq < c_ne) {
             float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            // tokens past the sequence have dS = 0; their loads read the last row instead
+#pragma unroll 8
             for (int c = 0; c < kBlock; ++c) {
-              if (tok0 + c >= N) break;
-              const float ds = s_si[eq * 64 + c];
-              const __nv_bfloat16* kr = k_idx + (tok0 + c) * d_idx + d0;
+              const float ds = s_si[eq * kSiStride + c];
+              const int64_t tok = tok0 + c < N ? tok0 + c : N - 1;
+              const __nv_bfloat16* kr = k_idx + tok * d_idx + d0;
               if (nd == 8) {
                 const uint4 v = ldg_nc_v4(kr);
                 const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
@@ -658,15 +677,14 @@ __global__ void __launch_bounds__(KlWarps<BWD>::kThreads, 1)
         // dK_idx of token R / 2, dims (R % 2) * d_idx / 2 ..: sum over the tile's entries
         {
           const int ck = R >> 1, nd = d_idx >> 1, d0 = (R & 1) * nd;
+#pragma unroll 4
           for (int eq = 0; eq < c_ne; ++eq) {
-            const float ds = s_si[eq * 64 + ck];
-            if (ds == 0.f) continue;
-            const int ent_q = __ldg(entries + c_e0 + eq);
-            const __nv_bfloat16* qr = q_idx + ((int64_t)(ent_q >> 6) * H_kv + r) * d_idx + d0;
+            const float ds = s_si[eq * kSiStride + ck];
+            const uint8_t* qr = smem + L::kOffQg + grp * L::kQgBytes + eq * 128 + d0 * 2;
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
               if (8 * u >= nd) break;
-              const uint4 v = ldg_nc_v4(qr + 8 * u);
+              const uint4 v = *reinterpret_cast<const uint4*>(qr + 16 * u);
               const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
               for (int t = 0; t < 4; ++t) {
