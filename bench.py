@@ -48,7 +48,8 @@ KERNEL_FILES = {"index_branch": ["k_score.cu"],
                 "main_branch": ["attn_fwd.cu", "k_attn_shared.cu", "k_attn_kvouter.cu",
                                 "k_attn_plan.cu", "attn_tile.cuh"],
                 "decode": ["k_decode.cu", "k_select.cu", "k_attn.cu"],
-                "kl_loss_fwd": ["k_kl.cu", "k_attn_plan.cu", "attn_tile.cuh"]}
+                "kl_loss_fwd": ["k_kl.cu", "k_attn_plan.cu", "attn_tile.cuh"],
+                "kl_loss_bwd": ["k_kl.cu", "k_attn_plan.cu", "attn_tile.cuh"]}
 # the KL alignment loss forward, timed apart from the step: plan, scan, plan, block-major pass,
 # merge (+ one memset)
 KL_LAUNCHES = 5
@@ -109,7 +110,8 @@ NCU_ROWS = {"k_index_block_scores": "index_branch",
             "k_attn_kvouter": "main_branch", "k_attn_shared": "main_branch",
             "k_decode_block_scores": "decode", "k_select_decode": "decode",
             "k_sparse_attn": "decode", "k_decode_merge": "decode",
-            "k_kl_plan": "kl_loss_fwd", "k_kl_kvouter": "kl_loss_fwd", "k_kl_merge": "kl_loss_fwd"}
+            "k_kl_plan": "kl_loss_fwd", "k_kl_kvouter": "kl_loss_fwd", "k_kl_merge": "kl_loss_fwd",
+            "k_kl_dq_merge": "kl_loss_bwd"}
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.txt")
 
 
@@ -140,23 +142,31 @@ def write_traffic(csv_path, command):
                                               "Metric Unit"))
     scale = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9}
     tot = collections.defaultdict(float)
+    calls = collections.Counter()      # KL rows: calls counted by their block-major launches
     steps = 0
     for r in rows[1:]:
-        name = r[ki].split("(")[0].split("<")[0].split("::")[-1].strip()
+        raw = r[ki].split("(")[0]
+        name = raw.split("<")[0].split("::")[-1].strip()
         if name not in NCU_ROWS:
             continue
-        if r[mi] == "gpu__time_duration.sum" and name == "k_index_block_scores":   # 1 per step
-            steps += 1
+        row = NCU_ROWS[name]
+        if name == "k_kl_kvouter" and raw.replace(" ", "").endswith(",1>"):
+            row = "kl_loss_bwd"                  # the gradient instantiation
+        if r[mi] == "gpu__time_duration.sum":
+            if name == "k_index_block_scores":   # 1 per step
+                steps += 1
+            if name == "k_kl_kvouter":
+                calls[row] += 1
         if r[mi] in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
-            tot[NCU_ROWS[name]] += float(r[vi].replace(",", "")) * scale[r[ui]]
+            tot[row] += float(r[vi].replace(",", "")) * scale[r[ui]]
     with open(TRAFFIC_FILE, "w") as f:
         f.write("# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per call of each bench\n"
                 "# row, averaged over %d whole steps of one ncu capture (1 pass, cold cache):\n"
                 "#   %s\n# row  bytes_per_call  source_sha\n" % (steps, command))
-        for k in ("index_branch", "main_branch", "decode", "kl_loss_fwd"):
+        for k in ("index_branch", "main_branch", "decode", "kl_loss_fwd", "kl_loss_bwd"):
             if k in tot:
-                f.write("%s %d %s\n" % (k, tot[k] / max(steps, 1),
-                                         kernel_source_hash(KERNEL_FILES[k])))
+                n = calls[k] if k.startswith("kl_") else steps
+                f.write("%s %d %s\n" % (k, tot[k] / max(n, 1), kernel_source_hash(KERNEL_FILES[k])))
 
 
 class Clocks:
@@ -444,7 +454,8 @@ def time_kl(msa, pcfg, x, bufs, K, sizes, pk, world):
     return {"ms": round(ms, 4), "value": round(world * N / (ms * 1e-3), 1), "unit": "tokens/s",
             "backward_index_branch": {"ms": round(ms_b, 4),
                                       "value": round(world * N / (ms_b * 1e-3), 1),
-                                      "unit": "tokens/s", "gpu_launches_per_call": KL_LAUNCHES + 1},
+                                      "unit": "tokens/s", "gpu_launches_per_call": KL_LAUNCHES + 1,
+                                      "traffic": ncu_traffic("kl_loss_bwd")},
             "mean_kl": round(float(kl.mean()), 6), "gpu_launches_per_call": KL_LAUNCHES,
             "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": pk["bf16_sust"],
                          "unit": "TFLOP/s", "frac": round(achieved / pk["bf16_sust"], 4),

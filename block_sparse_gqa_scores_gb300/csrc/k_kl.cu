@@ -669,9 +669,10 @@ __global__ void __launch_bounds__(KlWarps<BWD>::kThreads, 1)
             const int ent_q = __ldg(entries + c_e0 + eq);
             float* dst = gr.part_dq +
                          (((int64_t)r * N + (ent_q >> 6)) * kk + (ent_q & 63)) * d_idx + d0;
-#pragma unroll
-            for (int d = 0; d < 8; ++d)
-              if (d < nd) dst[d] = acc[d];
+            // 16-byte stores: a thread's nd floats are contiguous and 16-byte aligned
+            reinterpret_cast<float4*>(dst)[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+            if (nd == 8)
+              reinterpret_cast<float4*>(dst)[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
           }
         }
         // dK_idx of token R / 2, dims (R % 2) * d_idx / 2 ..: sum over the tile's entries
