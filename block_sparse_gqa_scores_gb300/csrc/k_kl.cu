@@ -651,11 +651,9 @@ __global__ void __launch_bounds__(KlWarps<BWD>::kThreads, 1)
                 const uint4 v = ldg_nc_v4(kr);
                 const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                  const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w4[u]));
-                  acc[2 * u] += ds * f.x;
-                  acc[2 * u + 1] += ds * f.y;
-                }
+                for (int u = 0; u < 4; ++u)   // bf16 pair -> fp32 pair is exact (a shift), then one packed FMA
+                  ffma2(acc[2 * u], acc[2 * u + 1], ds, ds, __uint_as_float(w4[u] << 16),
+                        __uint_as_float(w4[u] & 0xffff0000u), acc[2 * u], acc[2 * u + 1]);
               } else {
                 const uint2 v = *reinterpret_cast<const uint2*>(kr);
                 const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.x));
@@ -688,11 +686,10 @@ __global__ void __launch_bounds__(KlWarps<BWD>::kThreads, 1)
               const uint4 v = *reinterpret_cast<const uint4*>(qr + 16 * u);
               const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-              for (int t = 0; t < 4; ++t) {
-                const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w4[t]));
-                dkacc[8 * u + 2 * t] += ds * f.x;
-                dkacc[8 * u + 2 * t + 1] += ds * f.y;
-              }
+              for (int t = 0; t < 4; ++t)
+                ffma2(dkacc[8 * u + 2 * t], dkacc[8 * u + 2 * t + 1], ds, ds,
+                      __uint_as_float(w4[t] << 16), __uint_as_float(w4[t] & 0xffff0000u),
+                      dkacc[8 * u + 2 * t], dkacc[8 * u + 2 * t + 1]);
             }
           }
           kl_group_sync(1 + grp);                          // s_si may be overwritten
