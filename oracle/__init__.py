@@ -18,6 +18,8 @@ Pins (what this oracle is checked against, in tests/test_oracle_pins.py):
                    torch.nn.functional.scaled_dot_product_attention (causal, fp64);
                    Q = 0 closed form (LSE = ln|T|, O = mean of V over T).
   decode        -- equals the prefill row L-1 on the same tokens.
+  main-branch gradient -- torch.autograd (fp64) through a dense masked attention; k >= #blocks
+                   equals torch.autograd through scaled_dot_product_attention (causal).
   KL gradient   -- torch.autograd (fp64) through a dense masked restatement of the loss; central
                    finite differences of the oracle's own kl_loss; the uniform-teacher closed
                    form; sum over the index keys of dK_idx . K_idx equals sum of dQ_idx . Q_idx.
@@ -70,6 +72,8 @@ def lib():
         L.msa_oracle_kl_loss.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, i32, P, i64, P]
         L.msa_oracle_kl_loss_grad.argtypes = [P, P, P, P, P, P, i64, i32, i32, i32, i32, i32,
                                                i32, P, P, P, P]
+        L.msa_oracle_sparse_attn_grad.argtypes = [P, P, P, P, P, i64, i32, i32, i32, i32, i32, P,
+                                                   P, P]
         L.msa_oracle_set_threads.argtypes = [i32]
         L.msa_oracle_get_threads.restype = i32
         L.msa_oracle_f64_to_bf16.argtypes = [ctypes.c_double]
@@ -231,4 +235,19 @@ def kl_loss_grad(q, k, q_idx, k_idx, I, g_kl, block_size=64):
     lib().msa_oracle_kl_loss_grad(_p(q), _p(k), _p(q_idx), _p(k_idx), _p(I), _p(g_kl), N, H_q,
                                   H_kv, d_h, d_idx, block_size, I.shape[2], _p(out["dq_idx"]),
                                   _p(out["dk_idx"]), _p(out["lse_idx"]), _p(out["psum"]))
+    return out
+
+
+def sparse_attn_grad(q, k, v, dO, I, block_size=64):
+    """Main-branch gradient for upstream dO [N,H_q,d_h] (bf16 bits) over a given selection ->
+    dict(dq [N,H_q,d_h], dk [N,H_kv,d_h], dv [N,H_kv,d_h]) float64."""
+    q, k, v, dO = map(_u16, (q, k, v, dO))
+    I = np.ascontiguousarray(I, dtype=np.int32)
+    N, H_q, d_h = q.shape
+    H_kv = k.shape[1]
+    out = dict(dq=np.empty((N, H_q, d_h)), dk=np.empty((N, H_kv, d_h)),
+               dv=np.empty((N, H_kv, d_h)))
+    lib().msa_oracle_sparse_attn_grad(_p(q), _p(k), _p(v), _p(dO), _p(I), N, H_q, H_kv, d_h,
+                                      block_size, I.shape[2], _p(out["dq"]), _p(out["dk"]),
+                                      _p(out["dv"]))
     return out

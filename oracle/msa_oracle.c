@@ -313,6 +313,67 @@ static void row_kl_grad(const uint16_t *q_i, const uint16_t *qidx_ir, const uint
     }
 }
 
+/* ------------------------------------------- main branch backward (L3) ---- */
+
+/* Gradient of the main branch for row i given dO [H_q, d_h] (bf16 bits) of that row, for every
+ * head h (group r = h / G), over the same T as row_attend:
+ *   p_j = exp(s_j - LSE),  dP_j = dO[i,h] . V[j,r],  D = sum_j p_j dP_j,  dS_j = p_j (dP_j - D)
+ *   dQ[i,h] = sum_j dS_j K[j,r] / sqrt(d_h),  dK[j,r] += dS_j Q[i,h] / sqrt(d_h),
+ *   dV[j,r] += p_j dO[i,h]
+ * (the softmax attention of eq. O^(h)_i differentiated).  dq: [H_q, d_h] for this row; dk, dv:
+ * [N, H_kv, d_h] accumulated. */
+static void row_attend_grad(const uint16_t *q_i, const uint16_t *do_i, const uint16_t *K,
+                            const uint16_t *V, int64_t i, int H_q, int H_kv, int d_h, int B,
+                            const int32_t *sel, int kk, double *dq, double *dk, double *dv,
+                            double *s_buf, double *p_buf, int64_t *j_buf)
+{
+    const int G = H_q / H_kv;
+    const double scale = 1.0 / sqrt((double)d_h);
+    for (int h = 0; h < H_q; ++h) {
+        const int r = h / G;
+        const uint16_t *qh = q_i + (int64_t)h * d_h, *doh = do_i + (int64_t)h * d_h;
+        int64_t nt = 0;
+        for (int t = 0; t < kk; ++t) {
+            const int64_t b = sel[r * kk + t];
+            if (b < 0) continue;
+            const int64_t j1 = imin64(b * B + B - 1, i);
+            for (int64_t j = b * B; j <= j1; ++j) {
+                const uint16_t *kj = K + (j * H_kv + r) * (int64_t)d_h;
+                double dot = 0.0;
+                for (int d = 0; d < d_h; ++d) dot += bf16_to_f64(qh[d]) * bf16_to_f64(kj[d]);
+                s_buf[nt] = dot * scale;
+                j_buf[nt] = j;
+                ++nt;
+            }
+        }
+        double m = -INFINITY;
+        for (int64_t t = 0; t < nt; ++t) if (s_buf[t] > m) m = s_buf[t];
+        double z = 0.0;
+        for (int64_t t = 0; t < nt; ++t) z += exp(s_buf[t] - m);
+        const double L = m + log(z);
+        double D = 0.0;
+        for (int64_t t = 0; t < nt; ++t) {
+            const uint16_t *vj = V + (j_buf[t] * H_kv + r) * (int64_t)d_h;
+            double dp = 0.0;
+            for (int d = 0; d < d_h; ++d) dp += bf16_to_f64(doh[d]) * bf16_to_f64(vj[d]);
+            p_buf[t] = exp(s_buf[t] - L);
+            s_buf[t] = dp;                                    /* dP_j from here on */
+            D += p_buf[t] * dp;
+        }
+        double *dqh = dq + (int64_t)h * d_h;
+        for (int d = 0; d < d_h; ++d) dqh[d] = 0.0;
+        for (int64_t t = 0; t < nt; ++t) {
+            const double ds = p_buf[t] * (s_buf[t] - D) * scale;
+            const int64_t row = (j_buf[t] * H_kv + r) * (int64_t)d_h;
+            for (int d = 0; d < d_h; ++d) {
+                dqh[d] += ds * bf16_to_f64(K[row + d]);
+                dk[row + d] += ds * bf16_to_f64(qh[d]);
+                dv[row + d] += p_buf[t] * bf16_to_f64(doh[d]);
+            }
+        }
+    }
+}
+
 /* ------------------------------------------------------------- exports ----- */
 
 void msa_oracle_set_threads(int n)
@@ -551,6 +612,32 @@ void msa_oracle_kl_loss_grad(const uint16_t *q, const uint16_t *k, const uint16_
     free(s_buf);
     free(p_buf);
     free(j_buf);
+}
+
+/* Main-branch gradient over all N rows with a given selection I [H_kv, N, kk] and upstream dO
+ * [N, H_q, d_h] (bf16 bits): dQ [N, H_q, d_h], dK, dV [N, H_kv, d_h] (fp64, overwritten).
+ * Single-threaded: dK and dV are plain sums in row order. */
+void msa_oracle_sparse_attn_grad(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                                 const uint16_t *dO, const int32_t *I, int64_t N, int H_q,
+                                 int H_kv, int d_h, int B, int kk, double *dQ, double *dK,
+                                 double *dV)
+{
+    double *s_buf = (double *)malloc((size_t)kk * B * sizeof(double));
+    double *p_buf = (double *)malloc((size_t)kk * B * sizeof(double));
+    int64_t *j_buf = (int64_t *)malloc((size_t)kk * B * sizeof(int64_t));
+    int32_t *sel = (int32_t *)malloc((size_t)H_kv * kk * sizeof(int32_t));
+    for (int64_t e = 0; e < N * (int64_t)H_kv * d_h; ++e) dK[e] = dV[e] = 0.0;
+    for (int64_t i = 0; i < N; ++i) {
+        for (int r = 0; r < H_kv; ++r)
+            for (int u = 0; u < kk; ++u) sel[r * kk + u] = I[((int64_t)r * N + i) * kk + u];
+        row_attend_grad(q + i * H_q * (int64_t)d_h, dO + i * H_q * (int64_t)d_h, k, v, i, H_q,
+                        H_kv, d_h, B, sel, kk, dQ + i * H_q * (int64_t)d_h, dK, dV, s_buf, p_buf,
+                        j_buf);
+    }
+    free(s_buf);
+    free(p_buf);
+    free(j_buf);
+    free(sel);
 }
 
 /* Exposed for the pins on the rounding step. */

@@ -504,3 +504,63 @@ def test_kl_grad_invariants():
     out = oracle.kl_loss_grad(y["q"], y["k"], y["q_idx"], y["k_idx"], I, np.ones((1, 130)),
                               block_size=B)
     assert np.abs(out["dq_idx"]).max() < 1e-12 and np.abs(out["dk_idx"]).max() < 1e-12
+
+
+# --------------------------------------------------------- main-branch gradient --
+
+def autograd_attn_grad(x, dO, mask_fn):
+    """torch.autograd in fp64 through attention whose score mask mask_fn(r) gives -> (dQ, dK, dV)."""
+    Q = torch.from_numpy(f64(x["q"])).requires_grad_(True)
+    K = torch.from_numpy(f64(x["k"])).requires_grad_(True)
+    V = torch.from_numpy(f64(x["v"])).requires_grad_(True)
+    N, H_q, d = Q.shape
+    H_kv = K.shape[1]
+    G = H_q // H_kv
+    out = []
+    for h in range(H_q):
+        r = h // G
+        S = (Q[:, h] @ K[:, r].T) / math.sqrt(d)
+        P = torch.softmax(S.masked_fill(~mask_fn(r), float("-inf")), dim=-1)
+        out.append(P @ V[:, r])
+    O = torch.stack(out, dim=1)
+    (O * torch.from_numpy(f64(dO))).sum().backward()
+    return Q.grad.numpy(), K.grad.numpy(), V.grad.numpy()
+
+
+@pytest.mark.parametrize("variant,seed", [("gauss", 31), ("int", 32)])
+def test_attn_grad_matches_autograd(variant, seed):
+    cfg = small_cfg(N=96, H_q=8, H_kv=2, d_h=16, d_idx=8, k=3)
+    x = bits(gen.prefill_inputs(cfg, seed=seed, variant=variant))
+    B = 8
+    _, M32 = oracle.block_scores(x["q_idx"], x["k_idx"], block_size=B)
+    I = oracle.select_blocks(M32, 96, 3, block_size=B)
+    dO = gen.to_bits(torch.randn(96, 8, 16, generator=torch.Generator().manual_seed(seed)).to(
+        torch.bfloat16))
+    out = oracle.sparse_attn_grad(x["q"], x["k"], x["v"], dO, I, block_size=B)
+    mask = torch.from_numpy(np.array(selected_token_mask(I, 96, B)))
+    dq, dk, dv = autograd_attn_grad(x, dO, lambda r: mask[r])
+    np.testing.assert_allclose(out["dq"], dq, rtol=1e-9, atol=1e-12)
+    np.testing.assert_allclose(out["dk"], dk, rtol=1e-9, atol=1e-12)
+    np.testing.assert_allclose(out["dv"], dv, rtol=1e-9, atol=1e-12)
+
+
+def test_attn_grad_full_k_equals_sdpa_autograd():
+    """k >= number of blocks: plain causal GQA attention, so the gradient equals torch.autograd
+    through scaled_dot_product_attention(is_causal=True) in fp64 (a library routine)."""
+    cfg = small_cfg(N=64, H_q=8, H_kv=2, d_h=16, k=8)
+    x = bits(gen.prefill_inputs(cfg, seed=33))
+    B = 8
+    _, M32 = oracle.block_scores(x["q_idx"], x["k_idx"], block_size=B)
+    I = oracle.select_blocks(M32, 64, 8, block_size=B)
+    dO = gen.to_bits(torch.randn(64, 8, 16, generator=torch.Generator().manual_seed(4)).to(
+        torch.bfloat16))
+    out = oracle.sparse_attn_grad(x["q"], x["k"], x["v"], dO, I, block_size=B)
+    Q = torch.from_numpy(f64(x["q"])).permute(1, 0, 2)[None].requires_grad_(True)
+    K = torch.from_numpy(f64(x["k"])).permute(1, 0, 2)[None].requires_grad_(True)
+    V = torch.from_numpy(f64(x["v"])).permute(1, 0, 2)[None].requires_grad_(True)
+    O = torch.nn.functional.scaled_dot_product_attention(
+        Q, K.repeat_interleave(4, dim=1), V.repeat_interleave(4, dim=1), is_causal=True)
+    (O * torch.from_numpy(f64(dO)).permute(1, 0, 2)[None]).sum().backward()
+    np.testing.assert_allclose(out["dq"], Q.grad[0].permute(1, 0, 2).numpy(), rtol=1e-9, atol=1e-12)
+    np.testing.assert_allclose(out["dk"], K.grad[0].permute(1, 0, 2).numpy(), rtol=1e-9, atol=1e-12)
+    np.testing.assert_allclose(out["dv"], V.grad[0].permute(1, 0, 2).numpy(), rtol=1e-9, atol=1e-12)
