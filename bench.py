@@ -146,7 +146,7 @@ def write_traffic(csv_path, command):
     steps = 0
     for r in rows[1:]:
         raw = r[ki].split("(")[0]
-        name = raw.split("<")[0].split("::")[-1].strip()
+        name = raw.split("<")[0].split("::")[-1].split()[-1]   # bare kernel name
         if name not in NCU_ROWS:
             continue
         row = NCU_ROWS[name]

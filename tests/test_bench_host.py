@@ -1,0 +1,49 @@
+"""Host-side logic of the benchmark (no GPU): the per-row DRAM traffic attribution that feeds the
+roofline's `traffic` figure."""
+import importlib.util
+import os
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def load_bench():
+    spec = importlib.util.spec_from_file_location("bench_under_test", os.path.join(ROOT, "bench.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod
+
+
+def test_write_traffic_rows(tmp_path, monkeypatch):
+    bench = load_bench()
+    out = tmp_path / "traffic.txt"
+    monkeypatch.setattr(bench, "TRAFFIC_FILE", str(out))
+    hdr = '"ID","Kernel Name","Metric Name","Metric Unit","Metric Value"\n'
+    lines = [hdr]
+
+    def launch(i, name, mb_read, mb_write):
+        lines.append('"%d","%s","gpu__time_duration.sum","us","10"\n' % (i, name))
+        lines.append('"%d","%s","dram__bytes_read.sum","Mbyte","%s"\n' % (i, name, mb_read))
+        lines.append('"%d","%s","dram__bytes_write.sum","Mbyte","%s"\n' % (i, name, mb_write))
+
+    n = 0
+    for step in range(2):                                   # two steps
+        launch(n, "void k_index_block_scores<64, 2, 32>(const CUtensorMap_st)", 80, 8); n += 1
+        for _ in range(4):
+            launch(n, "k_attn_plan(const int *, long)", 1, 0); n += 1
+            launch(n, "void k_attn_kvouter<128>(CUtensorMap_st)", 1000, 1000); n += 1
+        launch(n, "void k_decode_merge<128>(const float *)", 2, 0); n += 1
+    for _ in range(3):                                      # three loss calls, two gradient calls
+        launch(n, "void k_kl_kvouter<128, 8, 0>(KlQMaps)", 19000, 200); n += 1
+    for _ in range(2):
+        launch(n, "void k_kl_kvouter<128, 8, 1>(KlQMaps)", 20000, 2000); n += 1
+        launch(n, "k_kl_dq_merge(const int *)", 2000, 100); n += 1
+    csv = tmp_path / "t.csv"
+    csv.write_text("".join(lines))
+    bench.write_traffic(str(csv), "test command")
+    rows = {l.split()[0]: int(l.split()[1]) for l in out.read_text().splitlines()
+            if l and not l.startswith("#")}
+    assert rows["index_branch"] == 88_000_000
+    assert rows["main_branch"] == 4 * (1_000_000 + 2_000_000_000)
+    assert rows["decode"] == 2_000_000
+    assert rows["kl_loss_fwd"] == 19_200_000_000              # per loss call (3 calls)
+    assert rows["kl_loss_bwd"] == 22_000_000_000 + 2_100_000_000   # gradient pass + dQ merge
