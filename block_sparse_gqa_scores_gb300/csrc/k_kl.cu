@@ -10,15 +10,21 @@
 //
 // Organisation: the same KV-outer scheme as the main branch's block-major pass.  Every
 // selection (row, slot) is bucketed by (group, block); a work tile stacks up to 128/G entries of
-// one bucket, G rows each, into one 128-row UMMA tile:
-//   S   = Q_stack  [128 x d_h]   . K_b^T     [d_h x 64]     tcgen05 -> TMEM columns [0, 64)
-//   S^i = Qi_stack [128 x d_idx] . K_idx_b^T [d_idx x 64]   tcgen05 -> TMEM columns [64, 128)
-// (an entry's index query is repeated on its G rows, so every TMEM lane holds the student
-// scores of its own entry).  The teacher's head mean is a reduce-scatter over the entry's G
-// lanes by shuffles, after which each lane owns 64/G of the block's tokens; each entry leaves
-// one partial (sum P (ln P - S^idx), sum P, and the student's max and sum of exponentials in the
-// log2 domain) at the fixed position of its (group, row, slot).  A merge kernel combines a row's
+// one bucket, G rows each, into one 128-row UMMA tile, per TMEM stage:
+//   S     = Q_stack [128 x d_h] . K_b^T [d_h x 64]              columns [0, 64)
+//   S^i^T = K_idx_b [64 tokens on M] . Qi^T [d_idx x entries]    columns [64, 64 + 128/G)
+// (the student scores transposed, one index-query row per entry, moved to (entry, token) order
+// through shared memory).  The teacher's head mean is a reduce-scatter over the entry's G lanes
+// by shuffles, after which each lane owns 64/G of the block's tokens; each entry leaves one
+// partial (sum P (ln P - S^idx), sum P, and the student's max and sum of exponentials in the log2
+// domain) at the fixed position of its (group, row, slot).  A merge kernel combines a row's
 // partials in slot order: no atomic update of any result.
+// One persistent, warp-specialized CTA per SM: producer warps (query rows by TMA, keys and index
+// queries by cp.async), an MMA warp, and two epilogue groups taking alternate tiles.
+//
+// Gradient (the BWD instantiation, G = 8): the same pass recomputes teacher and student per
+// tile and turns them into dS = g (W P^idx - P) / sqrt(d_idx); dQ_idx per selection (partials,
+// merged in slot order) and dK_idx per block (fp32 atomics per run of tiles of one block).
 #include <cmath>
 
 #include "attn_tile.cuh"
