@@ -346,20 +346,15 @@ def run_msa(args, world, rank, local):
     pk = peaks()
     kern = []
 
-    def add(name, ms, bound, work, unit, peak, traffic=None):
-        achieved = work / (ms * 1e-3) / (1e12 if unit == "TFLOP/s" else 1e9)
-        kern.append({"kernel": name, "ms": round(ms, 4), "bound": bound,
-                     "achieved": round(achieved, 2), "peak": peak, "unit": unit,
-                     "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "algorithmic": work})
+    def add(name, ms, bound, work, unit, traffic=None):
+        kern.append(roofline_row(name, ms, bound, work, unit, pk, traffic))
 
-    add("index_branch", t_index, "tensor", sizes["F_idx"], "TFLOP/s", pk["bf16_sust"],
+    add("index_branch", t_index, "tensor", sizes["F_idx"], "TFLOP/s",
         ncu_traffic("index_branch"))
-    add("main_branch", t_attn, "tensor", sizes["F_main"], "TFLOP/s", pk["bf16_sust"],
-        ncu_traffic("main_branch"))
+    add("main_branch", t_attn, "tensor", sizes["F_main"], "TFLOP/s", ncu_traffic("main_branch"))
     if d is not None:
-        add("decode (4 kernels)", t_decode, "hbm", sizes["decode_bytes"], "GB/s", pk["hbm"],
-            ncu_traffic("decode"))
+        add("decode (%d kernels)" % DECODE_LAUNCHES, t_decode, "hbm", sizes["decode_bytes"],
+            "GB/s", ncu_traffic("decode"))
     dom = max(kern, key=lambda r: r["ms"])
 
     value = world * N * K / (t_prefill_total * 1e-3)
@@ -375,17 +370,21 @@ def run_msa(args, world, rank, local):
                    "ms": round(t_decode_total / K, 4),
                    "mean_len": float(np.mean(d["meta"]["lens"]))} if d is not None else None,
         "kernels": kern,
-        "roofline": {"kernel": dom["kernel"], "bound": dom["bound"], "achieved": dom["achieved"],
-                     "peak": dom["peak"], "unit": dom["unit"], "frac": dom["frac"],
-                     "traffic": dom["traffic"],
-                     "peak_source": "%s (%s)" % (pk["src"], "bf16 sustained" if dom["unit"] ==
-                                                 "TFLOP/s" else "HBM copy")},
+        "roofline": {k_: dom[k_] for k_ in ("kernel", "bound", "achieved", "peak", "unit", "frac",
+                                             "traffic", "peak_source")
+                     if k_ in dom} | ({"frac_of_sustained": dom["frac_of_sustained"]}
+                                      if "frac_of_sustained" in dom else {}),
         "clocks": clk,
         "gpu_launches": (1 + ATTN_LAUNCHES_PER_CHUNK * (-(-N // ATTN_CHUNK_ROWS)) +
                          (DECODE_LAUNCHES if d is not None else 0)) * K,
     }
     if not args.no_kl:
         line["kl_loss_fwd"] = time_kl(msa, pcfg, x, bufs, K, sizes, pk, world)
+    if DEFAULT_WORKLOAD and not args.no_extra_prefill:
+        # the other two prefill lengths of the workload set, each on its own inputs
+        for key, name in (("prefill_32k", "p32k"), ("prefill_1m", "p1m")):
+            line[key] = time_prefill_only(msa, gen.CONFIGS[name], bufs, K, pk, world,
+                                          seed=args.seed + rank)
     if d is not None and not args.no_paged:
         line["decode_paged"] = time_decode_paged(msa, dcfg, d, dbufs, K, sizes, pk, world)
     if not args.no_varlen and pcfg.k <= 32:
@@ -395,6 +394,65 @@ def run_msa(args, world, rank, local):
     if not args.no_cpu_baseline and rank == 0 and world == 1:
         line["cpu_baseline"] = cpu_baseline(pcfg, x, args.cpu_seconds, args.seed)
     return line
+
+
+def roofline_row(name, ms, bound, work, unit, pk, traffic=None):
+    """One kernel row: achieved = algorithmic work / measured time.  Tensor-bound rows are
+    divided by the burst bf16 peak (these rows run in sub-second loops at full clocks); the
+    fraction of the sustained (power-capped) figure is given beside it."""
+    achieved = work / (ms * 1e-3) / (1e12 if unit == "TFLOP/s" else 1e9)
+    row = {"kernel": name, "ms": round(ms, 4), "bound": bound, "achieved": round(achieved, 2),
+           "unit": unit, "traffic": traffic, "algorithmic": work}
+    if unit == "TFLOP/s":
+        row.update(peak=pk["bf16"], frac=round(achieved / pk["bf16"], 4),
+                   frac_of_sustained=round(achieved / pk["bf16_sust"], 4),
+                   peak_source="%s (bf16 burst)" % pk["src"])
+    else:
+        row.update(peak=pk["hbm"], frac=round(achieved / pk["hbm"], 4),
+                   peak_source="%s (HBM copy)" % pk["src"])
+    return row
+
+
+def time_prefill_only(msa, pcfg, bufs, K, pk, world, seed=0):
+    """Prefill alone (fused index branch, then the main branch) on a workload of its own, timed
+    apart from the step: K calls after 3 warm-up calls, per-call CUDA events around each of the
+    two calls.  The main branch reuses the step's workspace (sized for any N > 32768)."""
+    x = gen.prefill_inputs(pcfg, seed=seed, device="cuda")
+    N = pcfg.N
+    idx = torch.empty((pcfg.H_kv, N, pcfg.k), dtype=torch.int32, device="cuda")
+    o = torch.empty_like(x["q"])
+    lse = torch.empty((pcfg.H_q, N), dtype=torch.float32, device="cuda")
+    need = msa.msa_sparse_attn_fwd_workspace(N, pcfg.H_q, pcfg.H_kv, pcfg.d_h, pcfg.k)
+    ws = bufs["ws"] if bufs["ws"].numel() >= need else torch.empty(need, dtype=torch.uint8,
+                                                                   device="cuda")
+    stream = torch.cuda.current_stream()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+
+    def call(e=None):
+        if e is not None:
+            e[0].record(stream)
+        msa.msa_index_select(x["q_idx"], x["k_idx"], pcfg.k, idx=idx)
+        if e is not None:
+            e[1].record(stream)
+        msa.msa_sparse_attn_fwd(x["q"], x["k"], x["v"], idx, o=o, lse=lse, ws=ws)
+        if e is not None:
+            e[2].record(stream)
+
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize()
+    for s in range(K):
+        call(ev[s])
+    torch.cuda.synchronize()
+    msa.msa_device_status()
+    t_i = max_over_ranks(float(np.mean([e[0].elapsed_time(e[1]) for e in ev])), world)
+    t_a = max_over_ranks(float(np.mean([e[1].elapsed_time(e[2]) for e in ev])), world)
+    sz = workload_sizes(pcfg, None, [])
+    del x, o, idx, lse
+    return {"N": N, "value": round(world * N / ((t_i + t_a) * 1e-3), 1), "unit": "tokens/s",
+            "ms": round(t_i + t_a, 4),
+            "kernels": [roofline_row("index_branch", t_i, "tensor", sz["F_idx"], "TFLOP/s", pk),
+                        roofline_row("main_branch", t_a, "tensor", sz["F_main"], "TFLOP/s", pk)]}
 
 
 def time_kl(msa, pcfg, x, bufs, K, sizes, pk, world):
@@ -421,7 +479,6 @@ def time_kl(msa, pcfg, x, bufs, K, sizes, pk, world):
     torch.cuda.synchronize()
     msa.msa_device_status()
     ms = max_over_ranks(float(np.mean([evs[s].elapsed_time(evs[s + 1]) for s in range(K)])), world)
-    achieved = sizes["F_kl"] / (ms * 1e-3) / 1e12
     # the index-branch gradient of the loss (teacher fixed), on the same inputs, g = 1 per row
     lse_idx = torch.empty((pcfg.H_kv, N), dtype=torch.float32, device="cuda")
     psum = torch.empty_like(lse_idx)
@@ -457,9 +514,8 @@ def time_kl(msa, pcfg, x, bufs, K, sizes, pk, world):
                                       "unit": "tokens/s", "gpu_launches_per_call": KL_LAUNCHES + 1,
                                       "traffic": ncu_traffic("kl_loss_bwd")},
             "mean_kl": round(float(kl.mean()), 6), "gpu_launches_per_call": KL_LAUNCHES,
-            "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": pk["bf16_sust"],
-                         "unit": "TFLOP/s", "frac": round(achieved / pk["bf16_sust"], 4),
-                         "traffic": ncu_traffic("kl_loss_fwd"), "algorithmic": sizes["F_kl"]}}
+            "roofline": roofline_row("kl_loss_fwd", ms, "tensor", sizes["F_kl"], "TFLOP/s", pk,
+                                     ncu_traffic("kl_loss_fwd"))}
 
 
 def time_decode_paged(msa, dcfg, d, dbufs, K, sizes, pk, world):
@@ -664,6 +720,8 @@ def main():
                     help="skip the paged-cache decode measurement")
     ap.add_argument("--no-varlen", action="store_true",
                     help="skip the varlen (batched) prefill measurement")
+    ap.add_argument("--no-extra-prefill", action="store_true",
+                    help="skip the 32K and 1M prefill measurements")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--write-traffic", metavar="NCU_CSV",
                     help="write profiles/traffic.txt from an ncu CSV of whole steps and exit")

@@ -384,3 +384,7 @@ MSA_API msa_status_t msa_device_status(void) {
   if (msa::read_reset_kl_status(&y) != cudaSuccess) return MSA_ERR_CUDA;
   return (v | w | x | y) ? MSA_ERR_TIMEOUT : MSA_OK;
 }
+
+MSA_API msa_status_t msa_set_wait_limit_ns(uint64_t ns) {
+  return from_cuda(msa::set_score_wait_limit((unsigned long long)ns));
+}

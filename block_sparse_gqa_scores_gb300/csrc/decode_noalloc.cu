@@ -11,7 +11,9 @@
 // The array is part of the library image: every GPU that loads libmsa.so holds these bytes
 // until the process exits.  Its device address is looked up once per device, on the first call
 // made with that device current (cudaGetSymbolAddress); make that first call before capturing
-// any stream.  All calls share the array and it keeps the last call's contents; nothing in it
+// any stream.  The cached address belongs to the device's primary context: a device reset
+// (cudaDeviceReset) re-creates that context and may load the library elsewhere, after which the
+// cached address is stale, so this entry point must not be used on that device again.  All calls share the array and it keeps the last call's contents; nothing in it
 // has to start at zero, because every entry a kernel reads was written earlier in the same
 // call.  Two calls whose work overlaps on the GPU (different streams, or different host threads
 // on one device) race on the array: serialise them.

@@ -40,6 +40,10 @@ namespace msa {
 namespace {
 
 __device__ unsigned g_score_status = 0;
+// Bound on the pipeline waits of this kernel (ring slots, accumulators); the waits that drain
+// copies and MMAs still in flight before the CTA exits keep the fixed kWaitNs bound.  Set from
+// the host by set_score_wait_limit (msa_set_wait_limit_ns).
+__device__ unsigned long long g_score_wait_ns = kWaitNs;
 
 constexpr int kRows = 128;     // UMMA M: rows per sub-tile
 constexpr int kKeys = 128;     // UMMA N: keys per tile
@@ -214,6 +218,7 @@ __global__ void __launch_bounds__(ScoreSmem<D_IDX, SUB, CAP>::kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  const unsigned long long lim = g_score_wait_ns;          // pipeline waits only
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -227,7 +232,7 @@ __global__ void __launch_bounds__(ScoreSmem<D_IDX, SUB, CAP>::kThreads, 1)
       for (int s = 0; s < kStages; ++s) last_round[s] = -1;
       for (int kt = 0; kt < nkt; ++kt) {
         const int stg = kt % kStages, round = kt / kStages;
-        if (!mbar_wait(empty_b(stg), (round & 1) ^ 1, &g_score_status)) break;
+        if (!mbar_wait(empty_b(stg), (round & 1) ^ 1, &g_score_status, lim)) break;
         mbar_expect_tx(full_b(stg), L::kBBytes);
         tma_load_2d(sbase + L::kOffB + stg * L::kBBytes, &tm_k, full_b(stg), 0, kt * kKeys);
         last_round[stg] = round;
@@ -243,13 +248,13 @@ __global__ void __launch_bounds__(ScoreSmem<D_IDX, SUB, CAP>::kThreads, 1)
       constexpr uint32_t idesc = umma_idesc_bf16(kRows, kKeys);
       constexpr uint32_t sbo = 8 * D_IDX * 2;            // 8 rows of one swizzle atom
       constexpr int swz = D_IDX * 2;                     // 128-B or 64-B swizzle rows
-      if (mbar_wait(full_a, 0, &g_score_status)) {
+      if (mbar_wait(full_a, 0, &g_score_status, lim)) {
         tc_fence_after();
         for (int kt = 0; kt < nkt; ++kt) {
           const int stg = kt % kStages, round = kt / kStages;
           const int acc = kt & 1, use = kt >> 1;
-          if (!mbar_wait(tempty(acc), (use & 1) ^ 1, &g_score_status)) break;
-          if (!mbar_wait(full_b(stg), round & 1, &g_score_status)) break;
+          if (!mbar_wait(tempty(acc), (use & 1) ^ 1, &g_score_status, lim)) break;
+          if (!mbar_wait(full_b(stg), round & 1, &g_score_status, lim)) break;
           tc_fence_after();
           const uint32_t b_addr = sbase + L::kOffB + stg * L::kBBytes;
 #pragma unroll
@@ -286,7 +291,9 @@ __global__ void __launch_bounds__(ScoreSmem<D_IDX, SUB, CAP>::kThreads, 1)
       bool ok = true;
       for (int kt = 0; kt < nkt; ++kt) {
         const int acc = kt & 1, use = kt >> 1;
-        if (!mbar_wait(tfull(acc), use & 1, &g_score_status)) {
+        // every lane waits; the warp leaves together if any lane gave up (the loop body has
+        // warp-wide operations)
+        if (!__all_sync(0xffffffffu, mbar_wait(tfull(acc), use & 1, &g_score_status, lim))) {
           ok = false;
           break;
         }
@@ -352,7 +359,9 @@ __global__ void __launch_bounds__(ScoreSmem<D_IDX, SUB, CAP>::kThreads, 1)
       bool ok = true;
       for (int kt = 0; kt < nkt; ++kt) {
         const int acc = kt & 1, use = kt >> 1;
-        if (!mbar_wait(tfull(acc), use & 1, &g_score_status)) {
+        // every lane waits; the warp leaves together if any lane gave up (the loop body has
+        // warp-wide operations)
+        if (!__all_sync(0xffffffffu, mbar_wait(tfull(acc), use & 1, &g_score_status, lim))) {
           ok = false;
           break;
         }
@@ -454,6 +463,10 @@ cudaError_t launch_index_select(const void* q_idx, const void* k_idx, int32_t* i
                                 int H_kv, int d_idx, int k, int64_t q_start, int64_t q_count,
                                 cudaStream_t stream) {
   return launch_index(q_idx, k_idx, nullptr, idx, k, N, H_kv, d_idx, q_start, q_count, stream);
+}
+
+cudaError_t set_score_wait_limit(unsigned long long ns) {
+  return cudaMemcpyToSymbol(g_score_wait_ns, &ns, sizeof(ns));
 }
 
 cudaError_t read_reset_score_status(unsigned* out) {

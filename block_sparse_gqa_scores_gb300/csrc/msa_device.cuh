@@ -75,18 +75,21 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parit
   return ok != 0;
 }
 
-// Waits until the phase with the given parity has completed.  Gives up after kWaitNs,
-// records kErrTimeout in *err and returns false; the caller then stops its loop.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned* err) {
+// Waits until the phase with the given parity has completed.  Gives up once `limit_ns` has
+// passed since the first unsuccessful test (kWaitNs unless the caller passes another bound;
+// 0 gives up at once if the phase is not already complete), records kErrTimeout in *err and
+// returns false; the caller then stops its loop.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned* err,
+                                          unsigned long long limit_ns = kWaitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer_ns();
   while (true) {
-    for (int it = 0; it < 16; ++it)
-      if (mbar_try_wait_sleep(bar, parity, 100000u)) return true;
-    if (globaltimer_ns() - t0 > kWaitNs) {
+    if (globaltimer_ns() - t0 >= limit_ns) {
       atomicOr(err, kErrTimeout);
       return false;
     }
+    for (int it = 0; it < 16; ++it)
+      if (mbar_try_wait_sleep(bar, parity, 100000u)) return true;
   }
 }
 

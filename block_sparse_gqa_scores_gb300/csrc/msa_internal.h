@@ -58,6 +58,7 @@ cudaError_t launch_index_select(const void* q_idx, const void* k_idx, int32_t* i
                                 int H_kv, int d_idx, int k, int64_t q_start, int64_t q_count,
                                 cudaStream_t stream);
 cudaError_t read_reset_score_status(unsigned* out);
+cudaError_t set_score_wait_limit(unsigned long long ns);
 
 // KL alignment loss forward: workspace bytes and the launch sequence (plan, scan, block-major
 // partials, merge).
@@ -79,8 +80,9 @@ cudaError_t launch_select_prefill(const float* M, int32_t* idx, int64_t N, int H
 // Where a decode sequence's cache rows live.  Packed: sequence s is rows cu[s] .. cu[s+1]-1 of the
 // cache.  Paged: the cache is 64-token pages (one page per MSA block); token j of sequence s is
 // row j % 64 of page pages[s * max_pages + j / 64], and the sequence is lens[s] tokens long.
-// Lengths are clamped to [1, max_len] and page ids to [0, num_pages): a caller's bad value gives
-// wrong results, never an access outside the cache.
+// Lengths are clamped to [1, max_len] and page ids to [0, num_pages), so a bad length or page id
+// gives wrong results, never an access outside the cache.  The packed layout trusts cu itself:
+// its rows start at cu[s], so a cu[s] that is not a row of the cache addresses memory outside it.
 struct CacheMap {
   const int64_t* cu;        // packed (nullptr when paged)
   const int32_t* pages;     // paged: [S, max_pages]

@@ -56,6 +56,7 @@ def _load():
     L.msa_kl_loss_fwd_workspace.restype = sz
     L.msa_kl_loss_fwd.argtypes = [P, P, P, P, P, P, P, P, P, i64, i32, i32, i32, i32, i32, i32, P,
                                   sz, P]
+    L.msa_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
     L.msa_kl_loss_bwd_workspace.argtypes = [i64, i32, i32, i32]
     L.msa_kl_loss_bwd_workspace.restype = sz
     L.msa_kl_loss_bwd.argtypes = [P, P, P, P, P, P, P, P, P, P, P, i64, i32, i32, i32, i32, i32,
@@ -64,7 +65,7 @@ def _load():
                "msa_sparse_decode", "msa_sparse_decode_noalloc", "msa_sparse_decode_paged",
                "msa_prefill_varlen",
                "msa_kl_loss_fwd", "msa_kl_loss_bwd",
-               "msa_device_status"):
+               "msa_device_status", "msa_set_wait_limit_ns"):
         getattr(L, fn).restype = i32
     return L
 
@@ -88,12 +89,35 @@ def _check(fn, code):
         raise MSAError(fn, code)
 
 
-def _req(t, dtype, ndim, name):
+def _req(t, dtype, ndim, name, shape=None, device=None):
     if not isinstance(t, torch.Tensor):
         raise TypeError("%s must be a torch.Tensor" % name)
     if t.dtype != dtype or t.dim() != ndim or not t.is_contiguous() or not t.is_cuda:
         raise ValueError("%s must be a contiguous %dD %s CUDA tensor, got %s %s %s" % (
             name, ndim, dtype, tuple(t.shape), t.dtype, t.device))
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError("%s must have shape %s, got %s" % (name, tuple(shape), tuple(t.shape)))
+    if device is not None and t.device != device:
+        raise ValueError("%s must be on %s, got %s" % (name, device, t.device))
+
+
+def _decode_outputs(q, q_idx, k, o, lse, idx_out, alloc):
+    """Checks (or, with alloc, creates) the decode outputs: o like q, lse [S, H_q] fp32 and
+    idx_out [S, H_kv, k] int32, all on q's device (a smaller buffer would be written past its
+    end by the kernels)."""
+    S, H_q, _ = q.shape
+    H_kv = q_idx.shape[1]
+    if alloc and o is None:
+        o = torch.empty_like(q)
+    if alloc and lse is None:
+        lse = torch.empty((S, H_q), dtype=torch.float32, device=q.device)
+    if alloc and idx_out is None:
+        idx_out = torch.empty((S, H_kv, k), dtype=torch.int32, device=q.device)
+    _req(o, torch.bfloat16, 3, "o", q.shape, q.device)
+    _req(lse, torch.float32, 2, "lse", (S, H_q), q.device)
+    if idx_out is not None:
+        _req(idx_out, torch.int32, 3, "idx_out", (S, H_kv, k), q.device)
+    return o, lse, idx_out
 
 
 def msa_index_block_scores(q_idx, k_idx, M=None, q_start=0, q_count=None, block_size=BLOCK,
@@ -183,12 +207,10 @@ def msa_sparse_decode(q, q_idx, k_cache, v_cache, k_idx_cache, cu_seqlens, max_l
     _req(cu_seqlens, torch.int64, 1, "cu_seqlens")
     S, H_q, d_h = q.shape
     H_kv, d_idx = q_idx.shape[1], q_idx.shape[2]
-    if o is None:
-        o = torch.empty_like(q)
-    if lse is None:
-        lse = torch.empty((S, H_q), dtype=torch.float32, device=q.device)
-    if idx_out is None:
-        idx_out = torch.empty((S, H_kv, k), dtype=torch.int32, device=q.device)
+    for t, n in ((q_idx, "q_idx"), (k_cache, "k_cache"), (v_cache, "v_cache"),
+                 (k_idx_cache, "k_idx_cache"), (cu_seqlens, "cu_seqlens")):
+        _req(t, t.dtype, t.dim(), n, device=q.device)
+    o, lse, idx_out = _decode_outputs(q, q_idx, k, o, lse, idx_out, alloc=True)
     nws = msa_sparse_decode_workspace(S, max_len, H_q, H_kv, d_h, d_idx, k)
     if ws is None:
         ws = torch.empty(max(nws, 16), dtype=torch.uint8, device=q.device)
@@ -211,10 +233,12 @@ def msa_sparse_decode_noalloc(q, q_idx, k_cache, v_cache, k_idx_cache, cu_seqlen
     _req(v_cache, torch.bfloat16, 3, "v_cache")
     _req(k_idx_cache, torch.bfloat16, 2, "k_idx_cache")
     _req(cu_seqlens, torch.int64, 1, "cu_seqlens")
-    _req(o, torch.bfloat16, 3, "o")
-    _req(lse, torch.float32, 2, "lse")
     S, H_q, d_h = q.shape
     H_kv, d_idx = q_idx.shape[1], q_idx.shape[2]
+    for t, n in ((q_idx, "q_idx"), (k_cache, "k_cache"), (v_cache, "v_cache"),
+                 (k_idx_cache, "k_idx_cache"), (cu_seqlens, "cu_seqlens")):
+        _req(t, t.dtype, t.dim(), n, device=q.device)
+    o, lse, idx_out = _decode_outputs(q, q_idx, k, o, lse, idx_out, alloc=False)
     _check("msa_sparse_decode_noalloc", lib.msa_sparse_decode_noalloc(
         _ptr(q), _ptr(q_idx), _ptr(k_cache), _ptr(v_cache), _ptr(k_idx_cache), _ptr(cu_seqlens),
         S, max_len, H_q, H_kv, d_h, d_idx, block_size, k, _ptr(o), _ptr(lse), _ptr(idx_out),
@@ -265,12 +289,9 @@ def msa_sparse_decode_paged(q, q_idx, k_pages, v_pages, k_idx_pages, page_table,
     S, H_q, d_h = q.shape
     H_kv, d_idx = q_idx.shape[1], q_idx.shape[2]
     num_pages, max_pages = k_pages.shape[0], page_table.shape[1]
-    if o is None:
-        o = torch.empty_like(q)
-    if lse is None:
-        lse = torch.empty((S, H_q), dtype=torch.float32, device=q.device)
-    if idx_out is None:
-        idx_out = torch.empty((S, H_kv, k), dtype=torch.int32, device=q.device)
+    if page_table.shape[0] != S or seq_lens.shape[0] != S:
+        raise ValueError("page_table must be [S, max_pages] and seq_lens [S], S = %d" % S)
+    o, lse, idx_out = _decode_outputs(q, q_idx, k, o, lse, idx_out, alloc=True)
     nws = msa_sparse_decode_workspace(S, max_len, H_q, H_kv, d_h, d_idx, k)
     if ws is None:
         ws = torch.empty(max(nws, 16), dtype=torch.uint8, device=q.device)
@@ -340,3 +361,9 @@ def msa_kl_loss_bwd(q, k, q_idx, k_idx, idx, lse, lse_idx, p_sum, grad_kl, dq_id
 def msa_device_status():
     """Reads and clears the device status words; raises on a recorded timeout."""
     _check("msa_device_status", lib.msa_device_status())
+
+
+def msa_set_wait_limit_ns(ns):
+    """Time limit of the index-branch kernel's pipeline waits on the current device (default
+    2e9 ns; 0 makes a wait that is not already satisfied give up at once)."""
+    _check("msa_set_wait_limit_ns", lib.msa_set_wait_limit_ns(int(ns)))

@@ -165,7 +165,8 @@ size_t msa_sparse_decode_workspace(int S, int64_t max_len, int H_q, int H_kv, in
  *   idx_out      int32 [S, H_kv, k] or NULL (selected blocks, as msa_select_blocks)
  *   ws           device workspace of msa_sparse_decode_workspace() bytes.
  * cu_seqlens is read on the device only (the call never synchronises); lengths outside
- * [1, max_len] are a caller error that the kernels clamp rather than trust. */
+ * [1, max_len] are a caller error that the kernels clamp rather than trust.  The offsets
+ * themselves are trusted: every cu_seqlens[s] must be a row of the caches. */
 msa_status_t msa_sparse_decode(const void *q, const void *q_idx, const void *k_cache,
                                const void *v_cache, const void *k_idx_cache,
                                const int64_t *cu_seqlens, int S, int64_t max_len, int H_q,
@@ -209,7 +210,10 @@ msa_status_t msa_sparse_decode_paged(const void *q, const void *q_idx, const voi
  *     until the process exits.  Sizes whose msa_sparse_decode_workspace() exceeds it return
  *     MSA_ERR_WORKSPACE before any launch.
  *   - The first call on each device looks up the array's device address (cudaGetSymbolAddress)
- *     with that device current; make that first call before capturing any stream.
+ *     with that device current; make that first call before capturing any stream.  The address
+ *     is kept for the life of the process: after a device reset (cudaDeviceReset, or anything
+ *     else that destroys and re-creates the device's primary context) the library may load at
+ *     another address, so do not call this entry point on that device again in that process.
  *   - All calls share the array and it keeps the last call's contents (nothing in it needs to
  *     start at zero).  Calls whose GPU work overlaps -- on different streams or from different
  *     host threads on one device -- race on it and must be serialised by the caller. */
@@ -276,8 +280,23 @@ msa_status_t msa_kl_loss_bwd(const void *q, const void *k, const void *q_idx, co
 
 /* Reads and clears the device status words of the current device (synchronising call).
  * Returns MSA_ERR_TIMEOUT if any kernel since the last call gave up a bounded wait,
- * MSA_ERR_CUDA if the read itself failed, MSA_OK otherwise. */
+ * MSA_ERR_CUDA if the read itself failed, MSA_OK otherwise.
+ * The status words are per device and per library, not per call: several calls may share one
+ * stream or workspace-free entry points (msa_index_block_scores, msa_select_blocks,
+ * msa_index_select) have no workspace to hold a status word, so a timeout is reported for
+ * the device since the last read; read it after synchronising the calls you want covered. */
 msa_status_t msa_device_status(void);
+
+/* Time limit, in nanoseconds, of the pipeline waits (ring slots and accumulator hand-offs)
+ * inside the index-branch kernel -- the kernel of msa_index_block_scores and msa_index_select,
+ * also run by msa_prefill_varlen -- on the current device; the default is 2e9 (2 s).  A wait
+ * that reaches the limit gives up: the kernel stops its loops, waits for the copies and MMAs it
+ * has in flight (those waits keep the fixed 2 s bound), frees its tensor memory and records
+ * MSA_ERR_TIMEOUT for msa_device_status(); that call's outputs are unspecified.  ns = 0 makes
+ * every pipeline wait that is not already satisfied give up at once, which exercises the
+ * timeout path without any fault.  Every other kernel keeps the fixed 2 s bound.
+ * Synchronising call (it writes a device variable); MSA_ERR_CUDA if that write failed. */
+msa_status_t msa_set_wait_limit_ns(uint64_t ns);
 
 #ifdef __cplusplus
 }

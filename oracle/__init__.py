@@ -65,6 +65,8 @@ def lib():
         L.msa_oracle_select_blocks.argtypes = [P, i64, i32, i32, i32, i64, i64, P]
         L.msa_oracle_sparse_attn.argtypes = [P, P, P, P, i64, i32, i32, i32, i32, i32, P, i64,
                                              P, P, P]
+        L.msa_oracle_sparse_attn_rows.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, P, i64,
+                                                  P, P, P]
         L.msa_oracle_prefill_rows.argtypes = [P, P, P, P, P, i64, i32, i32, i32, i32, i32, i32,
                                               P, i64, P, P, P, P, P]
         L.msa_oracle_decode.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32, P,
@@ -131,10 +133,25 @@ def select_blocks(M32, N, k, block_size=64, q_start=0, I=None):
     return I
 
 
-def sparse_attn(q, k, v, I, block_size=64, rows=None):
-    """Main branch over a given selection I [H_kv, N, kk] -> (O64, O16 bits, LSE64)."""
+def sparse_attn(q, k, v, I, block_size=64, rows=None, compact=False):
+    """Main branch over a given selection I [H_kv, N, kk] -> (O64, O16 bits, LSE64).
+    compact=True: q and I hold only the listed rows ([n,H_q,d_h] and [H_kv,n,kk], row t is
+    query position rows[t]); k and v are the whole sequence."""
     q, k, v = _u16(q), _u16(k), _u16(v)
     I = np.ascontiguousarray(I, dtype=np.int32)
+    if compact:
+        rows_a = np.ascontiguousarray(rows, dtype=np.int64)
+        n, H_q, d_h = q.shape
+        H_kv = k.shape[1]
+        assert I.shape[:2] == (H_kv, n) and len(rows_a) == n
+        I_rows = np.ascontiguousarray(I.transpose(1, 0, 2))
+        O64 = np.empty((n, H_q, d_h), np.float64)
+        O16 = np.empty((n, H_q, d_h), np.uint16)
+        LSE = np.empty((n, H_q), np.float64)
+        lib().msa_oracle_sparse_attn_rows(_p(q), _p(k), _p(v), _p(I_rows), H_q, H_kv, d_h,
+                                          block_size, I.shape[2], _p(rows_a), n, _p(O64),
+                                          _p(O16), _p(LSE))
+        return O64, O16, LSE
     N, H_q, d_h = q.shape
     H_kv = k.shape[1]
     kk = I.shape[2]

@@ -469,6 +469,32 @@ void msa_oracle_sparse_attn(const uint16_t *q, const uint16_t *k, const uint16_t
     }
 }
 
+/* Main branch for the listed rows only, with their projections and selections given compactly:
+ * row t is query position rows[t]; q_rows [n_rows,H_q,d_h] and I_rows [n_rows,H_kv,kk] hold that
+ * row's queries and selection; K, V are the full sequence.  Outputs as msa_oracle_sparse_attn. */
+void msa_oracle_sparse_attn_rows(const uint16_t *q_rows, const uint16_t *k, const uint16_t *v,
+                                 const int32_t *I_rows, int H_q, int H_kv, int d_h, int B, int kk,
+                                 const int64_t *rows, int64_t n_rows, double *O64, uint16_t *O16,
+                                 double *LSE)
+{
+#pragma omp parallel
+    {
+        double *s_buf = (double *)malloc((size_t)kk * B * sizeof(double));
+        int64_t *j_buf = (int64_t *)malloc((size_t)kk * B * sizeof(int64_t));
+#pragma omp for schedule(dynamic, 8)
+        for (int64_t t = 0; t < n_rows; ++t) {
+            double *o = O64 + t * H_q * (int64_t)d_h;
+            row_attend(q_rows + t * H_q * (int64_t)d_h, k, v, rows[t], H_q, H_kv, d_h, B,
+                       I_rows + t * H_kv * (int64_t)kk, kk, o, LSE + t * H_q, s_buf, j_buf);
+            if (O16)
+                for (int64_t e = 0; e < (int64_t)H_q * d_h; ++e)
+                    O16[t * H_q * (int64_t)d_h + e] = f64_to_bf16(o[e]);
+        }
+        free(s_buf);
+        free(j_buf);
+    }
+}
+
 /* The whole prefill path (scores -> selection -> main branch) for the given rows only.
  * q_rows [n_rows,H_q,d_h] and q_idx_rows [n_rows,H_kv,d_idx] hold the projections of the
  * listed rows only (row t is query position rows[t]); K, V, K_idx are the full sequence.

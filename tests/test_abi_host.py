@@ -259,3 +259,14 @@ def test_kl_bwd_unsupported_and_workspace(lib):
     need = lib.msa_kl_loss_bwd_workspace(i64(1024), 4, 64, 16)
     assert need >= lib.msa_kl_loss_fwd_workspace(i64(1024), 4, 16) + 4 * 4 * 1024 * 16 * 64
     assert klb(lib, wsb=need - 1) == WORKSPACE
+
+
+def test_device_status_and_wait_limit_without_a_device(lib):
+    """The status word and the wait-limit knob live in device memory of the current device; with
+    no usable device both calls report MSA_ERR_CUDA instead of failing in another way."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a CUDA device is present")
+    assert lib.msa_device_status() == 4
+    lib.msa_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+    assert lib.msa_set_wait_limit_ns(ctypes.c_uint64(0)) == 4

@@ -47,3 +47,15 @@ def test_write_traffic_rows(tmp_path, monkeypatch):
     assert rows["decode"] == 2_000_000
     assert rows["kl_loss_fwd"] == 19_200_000_000              # per loss call (3 calls)
     assert rows["kl_loss_bwd"] == 22_000_000_000 + 2_100_000_000   # gradient pass + dQ merge
+
+
+def test_roofline_row_peaks():
+    """Tensor-bound rows divide by the burst bf16 figure and give the sustained fraction beside
+    it; HBM-bound rows divide by the measured copy bandwidth."""
+    bench = load_bench()
+    pk = dict(hbm=6000.0, bf16=2000.0, bf16_sust=1600.0, src="measured")
+    t = bench.roofline_row("main_branch", 2.0, "tensor", 2.0e12, "TFLOP/s", pk)
+    assert t["achieved"] == 1000.0 and t["peak"] == 2000.0 and t["frac"] == 0.5
+    assert t["frac_of_sustained"] == 0.625 and "burst" in t["peak_source"]
+    h = bench.roofline_row("decode", 0.1, "hbm", 3.0e8, "GB/s", pk)
+    assert h["achieved"] == 3000.0 and h["frac"] == 0.5 and "frac_of_sustained" not in h

@@ -1,15 +1,20 @@
 """Full-size parity on the benchmark's own workloads, in the benchmark's launch configuration
 (the same C-ABI calls on the full tensors), checked on sampled query rows / sequences that the
-oracle recomputes one by one: 32K and 128K prefill, the 32-sequence decode batch, and 1M prefill
-(query-chunked index scores).  Selections must match the oracle up to near-ties; O and LSE are
-compared on rows whose selection matches exactly."""
+oracle recomputes one by one: 32K and 128K prefill, the 32-sequence decode batch (packed and
+paged), 1M prefill (query-chunked index scores) and the packed varlen batch.
+
+Every sampled row is checked twice: its selection against the oracle's (exact up to near-ties,
+1e-3 relative), and its O and LSE against the oracle's main branch evaluated on the GPU's own
+selection (O max-abs <= 2e-2, LSE <= 1e-3), so rows inside the near-tie band are covered too.
+Row counts: 512 at 32K, 1024 at 128K, 4096 random rows at 1M (plus edge rows), every decode
+sequence."""
 import numpy as np
 import pytest
 import torch
 
 import gen
 import oracle
-from msa_testutil import LSE_TOL, O_TOL, selection_mismatches, to_pages
+from msa_testutil import check_decode_seqs, check_prefill_rows, to_pages, unpage
 
 pytestmark = pytest.mark.gpu
 
@@ -19,7 +24,8 @@ msa = pytest.importorskip("block_sparse_gqa_scores_gb300")
 def sample_rows(N, n, seed):
     rng = np.random.default_rng(seed)
     edge = [0, 1, 63, 64, 65, N // 2, N - 65, N - 64, N - 1]
-    rows = np.unique(np.concatenate([rng.choice(N, n, replace=False), [e for e in edge if e < N]]))
+    rows = np.unique(np.concatenate([rng.choice(N, min(n, N), replace=False),
+                                     [e for e in edge if 0 <= e < N]]))
     return rows.astype(np.int64)
 
 
@@ -47,35 +53,14 @@ def run_prefill(x, cfg):
     return idx, o, lse
 
 
-def check_rows(x, cfg, idx, o, lse, rows, M_last=None, chunk_start=None):
-    b = {n: gen.to_bits(x[n]) for n in ("k", "v", "k_idx")}
-    rows_t = torch.from_numpy(rows).cuda()
-    qr = gen.to_bits(x["q"][rows_t])
-    qir = gen.to_bits(x["q_idx"][rows_t])
-    ref = oracle.prefill(qr, b["k"], b["v"], qir, b["k_idx"], cfg.k, rows=rows, want_m=True,
-                         compact=True)
-    I_gpu = idx[:, rows_t].cpu().numpy()                       # [H_kv, n, k]
-    I_ref = ref["I"].transpose(1, 0, 2)
-    differ, bad = selection_mismatches(I_gpu, I_ref, ref["M32"].transpose(1, 0, 2), cfg.k, rows=rows)
-    assert not bad, bad[:5]
-    same = (I_gpu == I_ref).all(axis=(0, 2))                   # rows with all groups identical
-    assert same.mean() >= 0.9
-    o_s = o[rows_t].float().cpu().numpy()
-    l_s = lse[:, rows_t].cpu().numpy().T
-    err_o = np.abs(o_s - ref["O64"]).max(axis=(1, 2))[same]
-    err_l = np.abs(l_s - ref["LSE"]).max(axis=1)[same]
-    assert err_o.max() <= O_TOL and err_l.max() <= LSE_TOL
-    return differ
-
-
-@pytest.mark.parametrize("name,n_rows", [("p32k", 48), ("p128k", 40)])
+@pytest.mark.parametrize("name,n_rows", [("p32k", 512), ("p128k", 1024)])
 def test_fullsize_prefill(name, n_rows):
     cfg = gen.CONFIGS[name]
     x = gen.prefill_inputs(cfg, seed=0, device="cuda")
     idx, o, lse = run_prefill(x, cfg)
     # the fused index branch selects exactly what block scores + selection select
     assert torch.equal(idx, unfused_index(x, cfg))
-    check_rows(x, cfg, idx, o, lse, sample_rows(cfg.N, n_rows, seed=1))
+    check_prefill_rows(x, cfg.k, idx, o, lse, sample_rows(cfg.N, n_rows, seed=1))
 
 
 def test_fullsize_kl_loss():
@@ -87,7 +72,7 @@ def test_fullsize_kl_loss():
     kl = msa.msa_kl_loss_fwd(x["q"], x["k"], x["q_idx"], x["k_idx"], idx, lse)
     torch.cuda.synchronize()
     msa.msa_device_status()
-    rows = sample_rows(cfg.N, 40, seed=3)
+    rows = sample_rows(cfg.N, 256, seed=3)
     rows_t = torch.from_numpy(rows).cuda()
     ref = oracle.kl_loss(gen.to_bits(x["q"][rows_t]), gen.to_bits(x["k"]),
                          gen.to_bits(x["q_idx"][rows_t]), gen.to_bits(x["k_idx"]),
@@ -98,42 +83,31 @@ def test_fullsize_kl_loss():
 
 
 def test_fullsize_prefill_1m():
+    """1M tokens: the whole index array against the unfused path, and 4096 random query rows
+    (plus edge rows) against the oracle."""
     cfg = gen.CONFIGS["p1m"]
     x = gen.prefill_inputs(cfg, seed=0, device="cuda")
     idx, o, lse = run_prefill(x, cfg)
     ref = unfused_index(x, cfg, chunk=16384)
     assert torch.equal(idx, ref)
     del ref
-    check_rows(x, cfg, idx, o, lse, sample_rows(cfg.N, 8, seed=2))
+    check_prefill_rows(x, cfg.k, idx, o, lse, sample_rows(cfg.N, 4096, seed=2))
 
 
 def test_fullsize_decode():
+    """Every sequence of the 32-sequence batch against the oracle."""
     cfg = gen.CONFIGS["decode"]
     d = gen.decode_inputs(cfg, seed=0, device="cuda")
     o, lse, idx = msa.msa_sparse_decode(d["q"], d["q_idx"], d["k_cache"], d["v_cache"],
                                         d["k_idx_cache"], d["cu_seqlens"], cfg.len_hi, cfg.k)
     torch.cuda.synchronize()
     msa.msa_device_status()
-    cu = d["cu_seqlens"].cpu().numpy()
-    for s in (0, 13, 31):
-        sl = slice(int(cu[s]), int(cu[s + 1]))
-        L = int(cu[s + 1] - cu[s])
-        sub = lambda n: gen.to_bits(d[n][sl])
-        ref = oracle.decode(gen.to_bits(d["q"][s:s + 1]), gen.to_bits(d["q_idx"][s:s + 1]),
-                            sub("k_cache"), sub("v_cache"), sub("k_idx_cache"),
-                            np.array([0, L], np.int64), cfg.k, want_m=True)
-        I_gpu = idx[s:s + 1].cpu().numpy()
-        differ, bad = selection_mismatches(I_gpu.transpose(1, 0, 2), ref["I"].transpose(1, 0, 2),
-                                           ref["M32"].transpose(1, 0, 2), cfg.k, rows=[L - 1])
-        assert not bad
-        if np.array_equal(I_gpu, ref["I"]):
-            assert np.abs(o[s].float().cpu().numpy() - ref["O64"][0]).max() <= O_TOL
-            assert np.abs(lse[s].cpu().numpy() - ref["LSE"][0]).max() <= LSE_TOL
+    check_decode_seqs(d, cfg.k, o, lse, idx)
 
 
 def test_fullsize_decode_paged():
-    """The 32-sequence decode batch from a paged cache (shuffled 64-token pages) equals the packed
-    decode bit for bit."""
+    """The 32-sequence batch from a paged cache (shuffled 64-token pages): bit-equal to the packed
+    decode, and every sequence against the oracle on the tokens gathered back from the pages."""
     cfg = gen.CONFIGS["decode"]
     d = gen.decode_inputs(cfg, seed=0, device="cuda")
     o, lse, idx = msa.msa_sparse_decode(d["q"], d["q_idx"], d["k_cache"], d["v_cache"],
@@ -145,3 +119,29 @@ def test_fullsize_decode_paged():
     torch.cuda.synchronize()
     msa.msa_device_status()
     assert torch.equal(idx2, idx) and torch.equal(o2, o) and torch.equal(lse2, lse)
+    del o, lse, idx
+    kc, vc, kic, cu = unpage((kp, vp, kip), pt, sl)
+    del kp, vp, kip
+    dd = dict(q=d["q"], q_idx=d["q_idx"], k_cache=kc, v_cache=vc, k_idx_cache=kic, cu_seqlens=cu)
+    check_decode_seqs(dd, cfg.k, o2, lse2, idx2)
+
+
+def test_fullsize_prefill_varlen():
+    """The benchmark's varlen batch (the 128K workload cut into 10 independent sequences) on
+    sampled rows of every sequence against the oracle on that sequence alone."""
+    cfg = gen.CONFIGS["p128k"]
+    x = gen.prefill_inputs(cfg, seed=0, device="cuda")
+    lens = [65536, 32768, 16384, 8192, 4096, 2048, 1024, 512, 256, 256]
+    cu = torch.zeros(len(lens) + 1, dtype=torch.int64)
+    cu[1:] = torch.cumsum(torch.tensor(lens), 0)
+    o, lse, idx = msa.msa_prefill_varlen(x["q"], x["k"], x["v"], x["q_idx"], x["k_idx"], cu,
+                                         cfg.k)
+    torch.cuda.synchronize()
+    msa.msa_device_status()
+    for s, n in enumerate(lens):
+        t0 = int(cu[s])
+        sl = slice(t0, t0 + n)
+        xs = {k_: x[k_][sl] for k_ in ("q", "k", "v", "q_idx", "k_idx")}
+        idx_s = idx[t0 * cfg.H_kv * cfg.k:(t0 + n) * cfg.H_kv * cfg.k].view(cfg.H_kv, n, cfg.k)
+        lse_s = lse[t0 * cfg.H_q:(t0 + n) * cfg.H_q].view(cfg.H_q, n)
+        check_prefill_rows(xs, cfg.k, idx_s, o[sl], lse_s, sample_rows(n, 96, seed=10 + s))

@@ -13,7 +13,8 @@ import torch
 
 import gen
 import oracle
-from msa_testutil import (LSE_TOL, O_TOL, bits, cuda, max_abs, selection_mismatches, to_pages)
+from msa_testutil import (LSE_TOL, O_TOL, bits, check_decode_seqs, check_prefill_rows, cuda,
+                          max_abs, selection_mismatches, to_pages, unpage)
 
 pytestmark = pytest.mark.gpu
 
@@ -369,6 +370,12 @@ def test_prefill_varlen_equals_single_sequences(name, lens):
                            idx1.reshape(-1))
         assert torch.equal(o[sl], o1)
         assert torch.equal(lse[t0 * cfg.H_q:(t0 + n) * cfg.H_q], lse1.reshape(-1))
+        # and against the oracle on the sequence alone (positions restart at 0)
+        rows = np.unique(np.concatenate([np.arange(min(n, 70)), np.arange(max(0, n - 70), n),
+                                         np.random.default_rng(s_).choice(n, min(n, 200),
+                                                                          replace=False)]))
+        check_prefill_rows(xs, cfg.k, idx1, o[sl], lse[t0 * cfg.H_q:(t0 + n) * cfg.H_q]
+                           .view(cfg.H_q, n), rows, min_same=0.0 if n < 200 else 0.9)
 
 
 # ------------------------------------------------------------------------ decode --
@@ -458,6 +465,10 @@ def test_decode_paged_equals_packed(name, lens, variant):
     assert torch.equal(idx2, idx)
     assert torch.equal(o2, o)
     assert torch.equal(lse2, lse)
+    # and against the oracle on the tokens gathered back from the pages
+    kc, vc, kic, cu = unpage((kp, vp, kip), pt, sl)
+    dd = dict(q=d["q"], q_idx=d["q_idx"], k_cache=kc, v_cache=vc, k_idx_cache=kic, cu_seqlens=cu)
+    check_decode_seqs(dd, dcfg.k, o2, lse2, idx2, exact_idx=(variant == "int"))
 
 
 def test_decode_equals_prefill_last_row():

@@ -178,6 +178,12 @@ def test_attention_matches_dense_masked(variant):
     # the stored bf16 output is the RNE rounding of the fp64 result
     torch_round = gen.to_bits(torch.from_numpy(O64).to(torch.float32).to(torch.bfloat16))
     assert (O16 == torch_round).mean() > 0.999   # fp64->fp32->bf16 double rounding differs rarely
+    # the compact form (only some rows' queries and selections passed) on the same rows
+    rows = np.array([0, 7, 8, 63, 64, 119, 33])
+    Oc, _, Lc = oracle.sparse_attn(x["q"][rows], x["k"], x["v"], I[:, rows], block_size=B,
+                                   rows=rows, compact=True)
+    np.testing.assert_allclose(Oc, Oref[rows], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(Lc, Lref[rows], rtol=0, atol=1e-12)
 
 
 def test_full_k_equals_causal_sdpa():
