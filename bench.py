@@ -49,7 +49,8 @@ KERNEL_FILES = {"index_branch": ["k_score.cu"],
                                 "k_attn_plan.cu", "attn_tile.cuh"],
                 "decode": ["k_decode.cu", "k_select.cu", "k_attn.cu"],
                 "kl_loss_fwd": ["k_kl.cu", "k_attn_plan.cu", "attn_tile.cuh"],
-                "kl_loss_bwd": ["k_kl.cu", "k_attn_plan.cu", "attn_tile.cuh"]}
+                "kl_loss_bwd": ["k_kl.cu", "k_attn_plan.cu", "attn_tile.cuh"],
+                "sparse_attn_bwd": ["k_attn_bwd.cu", "k_kl.cu", "k_attn_plan.cu", "attn_tile.cuh"]}
 # the KL alignment loss forward, timed apart from the step: plan, scan, plan, block-major pass,
 # merge (+ one memset)
 KL_LAUNCHES = 5
@@ -111,7 +112,9 @@ NCU_ROWS = {"k_index_block_scores": "index_branch",
             "k_decode_block_scores": "decode", "k_select_decode": "decode",
             "k_sparse_attn": "decode", "k_decode_merge": "decode",
             "k_kl_plan": "kl_loss_fwd", "k_kl_kvouter": "kl_loss_fwd", "k_kl_merge": "kl_loss_fwd",
-            "k_kl_dq_merge": "kl_loss_bwd"}
+            "k_kl_dq_merge": "kl_loss_bwd",
+            "k_attn_bwd_kvouter": "sparse_attn_bwd", "k_attn_bwd_dq_merge": "sparse_attn_bwd",
+            "k_attn_bwd_dkv_merge": "sparse_attn_bwd", "k_attn_bwd_delta": "sparse_attn_bwd"}
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.txt")
 
 
@@ -155,7 +158,7 @@ def write_traffic(csv_path, command):
         if r[mi] == "gpu__time_duration.sum":
             if name == "k_index_block_scores":   # 1 per step
                 steps += 1
-            if name == "k_kl_kvouter":
+            if name in ("k_kl_kvouter", "k_attn_bwd_kvouter"):
                 calls[row] += 1
         if r[mi] in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
             tot[row] += float(r[vi].replace(",", "")) * scale[r[ui]]
@@ -163,9 +166,10 @@ def write_traffic(csv_path, command):
         f.write("# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per call of each bench\n"
                 "# row, averaged over %d whole steps of one ncu capture (1 pass, cold cache):\n"
                 "#   %s\n# row  bytes_per_call  source_sha\n" % (steps, command))
-        for k in ("index_branch", "main_branch", "decode", "kl_loss_fwd", "kl_loss_bwd"):
+        for k in ("index_branch", "main_branch", "decode", "kl_loss_fwd", "kl_loss_bwd",
+                  "sparse_attn_bwd"):
             if k in tot:
-                n = calls[k] if k.startswith("kl_") else steps
+                n = calls[k] if k.startswith("kl_") or k == "sparse_attn_bwd" else steps
                 f.write("%s %d %s\n" % (k, tot[k] / max(n, 1), kernel_source_hash(KERNEL_FILES[k])))
 
 
@@ -380,6 +384,8 @@ def run_msa(args, world, rank, local):
     }
     if not args.no_kl:
         line["kl_loss_fwd"] = time_kl(msa, pcfg, x, bufs, K, sizes, pk, world)
+    if not args.no_bwd:
+        line["sparse_attn_bwd"] = time_bwd(msa, pcfg, x, bufs, K, sizes, pk, world)
     if DEFAULT_WORKLOAD and not args.no_extra_prefill:
         # the other two prefill lengths of the workload set, each on its own inputs
         for key, name in (("prefill_32k", "p32k"), ("prefill_1m", "p1m")):
@@ -453,6 +459,50 @@ def time_prefill_only(msa, pcfg, bufs, K, pk, world, seed=0):
             "ms": round(t_i + t_a, 4),
             "kernels": [roofline_row("index_branch", t_i, "tensor", sz["F_idx"], "TFLOP/s", pk),
                         roofline_row("main_branch", t_a, "tensor", sz["F_main"], "TFLOP/s", pk)]}
+
+
+# the main-branch backward: ordered bucketing (2 memsets, count, scan, bases, scatter), piece
+# offsets, delta, the block-major gradient pass, the dQ merge and the dK/dV merge
+BWD_LAUNCHES = 9
+
+
+def time_bwd(msa, pcfg, x, bufs, K, sizes, pk, world):
+    """The main-branch backward (dQ, dK, dV) on the last step's selection, O and LSE with a seeded
+    upstream gradient, timed apart from the step: K calls after 3 warm-up calls.  Work counted:
+    per visible selected token and head the five d_h-long products S, dP, dV, dK and dQ, i.e.
+    2.5 times the forward's."""
+    N = pcfg.N
+    g = torch.Generator(device="cuda")
+    g.manual_seed(7)
+    d_o = torch.randn(x["q"].shape, generator=g, device="cuda").to(torch.bfloat16)
+    dq = torch.empty(x["q"].shape, dtype=torch.float32, device="cuda")
+    dk = torch.empty(x["k"].shape, dtype=torch.float32, device="cuda")
+    dv = torch.empty(x["v"].shape, dtype=torch.float32, device="cuda")
+    ws = torch.empty(msa.msa_sparse_attn_bwd_workspace(N, pcfg.H_q, pcfg.H_kv, pcfg.d_h, pcfg.k),
+                     dtype=torch.uint8, device="cuda")
+
+    def call():
+        msa.msa_sparse_attn_bwd(x["q"], x["k"], x["v"], bufs["idx"], bufs["o"], bufs["lse"], d_o,
+                                dq=dq, dk=dk, dv=dv, ws=ws)
+
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(K + 1)]
+    evs[0].record(stream)
+    for s in range(K):
+        call()
+        evs[s + 1].record(stream)
+    torch.cuda.synchronize()
+    msa.msa_device_status()
+    ms = max_over_ranks(float(np.mean([evs[s].elapsed_time(evs[s + 1]) for s in range(K)])), world)
+    finite = bool(torch.isfinite(dq).all() and torch.isfinite(dk).all() and torch.isfinite(dv).all())
+    del ws, dq, dk, dv, d_o
+    return {"ms": round(ms, 4), "value": round(world * N / (ms * 1e-3), 1), "unit": "tokens/s",
+            "gpu_launches_per_call": BWD_LAUNCHES, "finite": finite,
+            "roofline": roofline_row("sparse_attn_bwd", ms, "tensor", 2.5 * sizes["F_main"],
+                                     "TFLOP/s", pk, ncu_traffic("sparse_attn_bwd"))}
 
 
 def time_kl(msa, pcfg, x, bufs, K, sizes, pk, world):
@@ -720,6 +770,8 @@ def main():
                     help="skip the paged-cache decode measurement")
     ap.add_argument("--no-varlen", action="store_true",
                     help="skip the varlen (batched) prefill measurement")
+    ap.add_argument("--no-bwd", action="store_true",
+                    help="skip the main-branch backward measurement")
     ap.add_argument("--no-extra-prefill", action="store_true",
                     help="skip the 32K and 1M prefill measurements")
     ap.add_argument("--no-cpu-baseline", action="store_true")

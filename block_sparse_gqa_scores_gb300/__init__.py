@@ -8,4 +8,4 @@ from .msa import (MSAError, msa_device_status, msa_index_block_scores,  # noqa: 
                   msa_prefill_varlen,
                   msa_kl_loss_fwd, msa_kl_loss_bwd, msa_kl_loss_bwd_workspace,
                   msa_kl_loss_fwd_workspace, msa_sparse_decode_noalloc,
-                  msa_set_wait_limit_ns)
+                  msa_set_wait_limit_ns, msa_sparse_attn_bwd, msa_sparse_attn_bwd_workspace)

@@ -175,6 +175,32 @@ MSA_API msa_status_t msa_sparse_attn_fwd(const void* q, const void* k, const voi
                                                ws, (cudaStream_t)stream));
 }
 
+MSA_API size_t msa_sparse_attn_bwd_workspace(int64_t N, int H_q, int H_kv, int d_h, int k) {
+  if (N < 1 || H_kv < 1 || H_q < H_kv || H_q % H_kv != 0 || k < 1 || k > 64 || d_h < 1) return 0;
+  return msa::sparse_attn_bwd_ws_bytes(N, H_q, H_kv, d_h, k);
+}
+
+MSA_API msa_status_t msa_sparse_attn_bwd(const void* q, const void* k, const void* v,
+                                         const int32_t* idx, const void* o, const float* lse,
+                                         const void* d_o, float* dq, float* dk, float* dv,
+                                         int64_t N, int H_q, int H_kv, int d_h, int block_size,
+                                         int k_blocks, void* ws, size_t ws_bytes, void* stream) {
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned4(idx) || !aligned16(o) ||
+      !aligned4(lse) || !aligned16(d_o) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv) ||
+      !aligned16(ws))
+    return MSA_ERR_INVALID_ARGUMENT;
+  if (N < 1 || H_q < 1 || H_kv < 1 || H_q % H_kv != 0 || d_h < 1 || block_size != 64 ||
+      k_blocks < 1 || k_blocks > 64)
+    return MSA_ERR_INVALID_ARGUMENT;
+  if (!pow2_upto(H_kv, 8) || !pow2_upto(H_q / H_kv, 8) || (d_h != 64 && d_h != 128))
+    return MSA_ERR_UNSUPPORTED;
+  if (N > ((int64_t)1 << 21) || N * H_kv * k_blocks >= kMaxRows) return MSA_ERR_UNSUPPORTED;
+  if (ws_bytes < msa::sparse_attn_bwd_ws_bytes(N, H_q, H_kv, d_h, k_blocks))
+    return MSA_ERR_WORKSPACE;
+  return from_cuda(msa::launch_sparse_attn_bwd(q, k, v, idx, o, lse, d_o, dq, dk, dv, N, H_q,
+                                               H_kv, d_h, k_blocks, ws, (cudaStream_t)stream));
+}
+
 MSA_API size_t msa_sparse_decode_workspace(int S, int64_t max_len, int H_q, int H_kv, int d_h,
                                            int d_idx, int k) {
   (void)d_idx;
@@ -377,12 +403,13 @@ MSA_API msa_status_t msa_kl_loss_bwd(const void* q, const void* k, const void* q
 }
 
 MSA_API msa_status_t msa_device_status(void) {
-  unsigned v = 0, w = 0, x = 0, y = 0;
+  unsigned v = 0, w = 0, x = 0, y = 0, z = 0;
   if (msa::read_reset_score_status(&v) != cudaSuccess) return MSA_ERR_CUDA;
   if (msa::read_reset_shared_status(&w) != cudaSuccess) return MSA_ERR_CUDA;
   if (msa::read_reset_kvo_status(&x) != cudaSuccess) return MSA_ERR_CUDA;
   if (msa::read_reset_kl_status(&y) != cudaSuccess) return MSA_ERR_CUDA;
-  return (v | w | x | y) ? MSA_ERR_TIMEOUT : MSA_OK;
+  if (msa::read_reset_bwd_status(&z) != cudaSuccess) return MSA_ERR_CUDA;
+  return (v | w | x | y | z) ? MSA_ERR_TIMEOUT : MSA_OK;
 }
 
 MSA_API msa_status_t msa_set_wait_limit_ns(uint64_t ns) {

@@ -29,7 +29,7 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 // query rows per pass: bounds the workspace; larger chunks fill the (group, block) buckets of
 // the block-major pass better (32768 rows: 9.59 ms at 128K against 10.01 ms with 16384)
 constexpr int64_t kChunkRows = 32768;
-constexpr int kKvoCtasPerSm = 3;         // block-major pass: resident CTAs per SM (shared memory)
+constexpr int kKvoCtasPerSm = 1;         // block-major pass: persistent, one CTA per SM (TMEM)
 
 struct AttnWs {
   size_t count, offset, tile_off, cursor, entries, tile_list, tile_priv, part_o, part_lse,

@@ -139,6 +139,108 @@ __global__ void __launch_bounds__(32 * kKlPlanWarps)
   });
 }
 
+// ------------------------------------------------- row-ordered bucketing --
+// The same buckets with every bucket's selections in row order, whatever order the hardware
+// runs the warps in: counts per bucket and per (bucket, range of kRangeTiles tiles), bases from
+// an exclusive scan over a bucket's ranges, then one warp per range that walks its tiles in order
+// and alone advances that range's cursors.
+constexpr int kRangeTiles = 64;
+
+template <int EPL>
+__device__ __forceinline__ void order_count_tile(const int32_t* __restrict__ idx, int r, int64_t i0,
+                                                 int64_t N, int kk, int64_t nblk, int R, int range,
+                                                 int* s_U, unsigned* s_mask, int* count,
+                                                 int* cnt_mat) {
+  const int lane = threadIdx.x & 31;
+  int x[EPL], rank[EPL];
+  const int nU = tile_union<EPL>(idx, r, i0, N, N, kk, x, rank, s_U, s_mask);
+  for (int u = lane; u < nU; u += 32) {
+    const int64_t bucket = (int64_t)r * nblk + s_U[u];
+    const int n = __popc(s_mask[u]);
+    atomicAdd(count + bucket, n);
+    atomicAdd(cnt_mat + bucket * R + range, n);
+  }
+}
+
+__global__ void __launch_bounds__(32 * kKlPlanWarps)
+    k_order_count(const int32_t* __restrict__ idx, int64_t N, int kk, int64_t nblk, int R,
+                  int* count, int* cnt_mat) {
+  __shared__ int s_U[kKlPlanWarps][kMaxKeys];
+  __shared__ unsigned s_mask[kKlPlanWarps][kMaxKeys];
+  const int warp = threadIdx.x >> 5;
+  const int r = blockIdx.y;
+  const int64_t t = (int64_t)blockIdx.x * kKlPlanWarps + warp;
+  const int64_t i0 = t * kTileQ;
+  if (i0 >= N) return;
+  with_epl(kk, [&](auto e) {
+    order_count_tile<decltype(e)::value>(idx, r, i0, N, kk, nblk, R, (int)(t / kRangeTiles),
+                                         s_U[warp], s_mask[warp], count, cnt_mat);
+    return 0;
+  });
+}
+
+// cnt_mat[b][range] := offset[b] + sum of the bucket's counts in earlier ranges
+__global__ void __launch_bounds__(256)
+    k_order_bases(const int* __restrict__ offset, int* cnt_mat, int nb, int R) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= nb) return;
+  int run = offset[b];
+  int* row = cnt_mat + (int64_t)b * R;
+  for (int g = 0; g < R; ++g) {
+    const int c = row[g];
+    row[g] = run;
+    run += c;
+  }
+}
+
+template <int EPL>
+__device__ __forceinline__ void order_scatter_range(const int32_t* __restrict__ idx, int r,
+                                                    int range, int64_t N, int kk, int64_t nblk,
+                                                    int R, int* s_U, unsigned* s_mask,
+                                                    int* cnt_mat, int* entries) {
+  const int lane = threadIdx.x & 31;
+  const int64_t t_end = (N + kTileQ - 1) / kTileQ;
+  for (int64_t t = (int64_t)range * kRangeTiles; t < t_end && t < (int64_t)(range + 1) * kRangeTiles;
+       ++t) {
+    const int64_t i0 = t * kTileQ;
+    int x[EPL], rank[EPL];
+    const int nU = tile_union<EPL>(idx, r, i0, N, N, kk, x, rank, s_U, s_mask);
+    // each union block is a different bucket: its lane alone moves that bucket's cursor
+    for (int u = lane; u < nU; u += 32) {
+      int* cur = cnt_mat + ((int64_t)r * nblk + s_U[u]) * R + range;
+      const int pos = *cur;
+      *cur = pos + __popc(s_mask[u]);
+      s_U[u] = pos;
+    }
+    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < EPL; ++j) {
+      const int key = x[j];
+      if (key == INT_MAX) continue;
+      const int w = TileKeys::query(key);
+      const int pos = s_U[rank[j]] + __popc(s_mask[rank[j]] & ((1u << w) - 1u));
+      entries[pos] = (int)(((i0 + w) << 6) | TileKeys::slot(key));
+    }
+    __syncwarp();
+  }
+}
+
+__global__ void __launch_bounds__(32 * kKlPlanWarps)
+    k_order_scatter(const int32_t* __restrict__ idx, int64_t N, int kk, int64_t nblk, int R,
+                    int* cnt_mat, int* entries) {
+  __shared__ int s_U[kKlPlanWarps][kMaxKeys];
+  __shared__ unsigned s_mask[kKlPlanWarps][kMaxKeys];
+  const int warp = threadIdx.x >> 5;
+  const int r = blockIdx.y;
+  const int range = blockIdx.x * kKlPlanWarps + warp;
+  if (range >= R) return;
+  with_epl(kk, [&](auto e) {
+    order_scatter_range<decltype(e)::value>(idx, r, range, N, kk, nblk, R, s_U[warp],
+                                            s_mask[warp], cnt_mat, entries);
+    return 0;
+  });
+}
+
 // ------------------------------------------------------- block-major partials --
 // Reduce-scatter over the G lanes of an entry (lanes e*G .. e*G+G-1 of one warp, h = lane's
 // head): afterwards lane h holds, in a[0 .. 64/G), the sums over the G lanes of columns
@@ -773,6 +875,52 @@ __global__ void __launch_bounds__(256)
 
 }  // namespace
 
+// Every selection of idx bucketed by (group, block): count -> scan -> scatter, with each bucket's
+// selections in (16-query tile, query) order and ept entries per work tile.
+cudaError_t launch_bucket_selections(const int32_t* idx, int64_t N, int H_kv, int kk, int ept,
+                                     int* count, int* offset, int* tile_off, int* cursor,
+                                     int* entries, cudaStream_t st) {
+  const int64_t nblk = (N + kBlock - 1) / kBlock;
+  const int nb = (int)(H_kv * nblk);
+  cudaError_t e = cudaMemsetAsync(count, 0, sizeof(int) * (size_t)nb, st);
+  if (e != cudaSuccess) return e;
+  const int64_t tiles = (N + kTileQ - 1) / kTileQ;
+  const dim3 pgrid((unsigned)((tiles + kKlPlanWarps - 1) / kKlPlanWarps), (unsigned)H_kv);
+  k_kl_plan<<<pgrid, 32 * kKlPlanWarps, 0, st>>>(idx, N, kk, nblk, 0, count, offset, cursor,
+                                                 entries);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if ((e = launch_attn_scan(count, offset, tile_off, cursor, nb, ept, st)) != cudaSuccess) return e;
+  k_kl_plan<<<pgrid, 32 * kKlPlanWarps, 0, st>>>(idx, N, kk, nblk, 1, count, offset, cursor,
+                                                 entries);
+  return cudaGetLastError();
+}
+
+int ordered_bucket_ranges(int64_t N) {
+  return (int)(((N + kTileQ - 1) / kTileQ + kRangeTiles - 1) / kRangeTiles);
+}
+
+cudaError_t launch_bucket_selections_ordered(const int32_t* idx, int64_t N, int H_kv, int kk,
+                                             int ept, int* count, int* offset, int* tile_off,
+                                             int* cursor, int* cnt_mat, int* entries,
+                                             cudaStream_t st) {
+  const int64_t nblk = (N + kBlock - 1) / kBlock;
+  const int nb = (int)(H_kv * nblk);
+  const int R = ordered_bucket_ranges(N);
+  cudaError_t e = cudaMemsetAsync(count, 0, sizeof(int) * (size_t)nb, st);
+  if (e != cudaSuccess) return e;
+  if ((e = cudaMemsetAsync(cnt_mat, 0, sizeof(int) * (size_t)nb * R, st)) != cudaSuccess) return e;
+  const int64_t tiles = (N + kTileQ - 1) / kTileQ;
+  const dim3 cgrid((unsigned)((tiles + kKlPlanWarps - 1) / kKlPlanWarps), (unsigned)H_kv);
+  k_order_count<<<cgrid, 32 * kKlPlanWarps, 0, st>>>(idx, N, kk, nblk, R, count, cnt_mat);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if ((e = launch_attn_scan(count, offset, tile_off, cursor, nb, ept, st)) != cudaSuccess) return e;
+  k_order_bases<<<(nb + 255) / 256, 256, 0, st>>>(offset, cnt_mat, nb, R);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  const dim3 sgrid((unsigned)((R + kKlPlanWarps - 1) / kKlPlanWarps), (unsigned)H_kv);
+  k_order_scatter<<<sgrid, 32 * kKlPlanWarps, 0, st>>>(idx, N, kk, nblk, R, cnt_mat, entries);
+  return cudaGetLastError();
+}
+
 size_t kl_ws_bytes(int64_t N, int H_kv, int kk) {
   const int64_t nb = (int64_t)H_kv * ((N + kBlock - 1) / kBlock);
   auto a256 = [](size_t x) { return (x + 255) & ~size_t(255); };
@@ -806,18 +954,9 @@ cudaError_t kl_pass(bool bwd, const void* q, const void* k, const void* q_idx, c
   float4* part = reinterpret_cast<float4*>(base + 4 * a256(4 * (size_t)(nb + 1)) + a256(4 * sel));
   *part_out = part;
 
-  cudaError_t e = cudaMemsetAsync(count, 0, sizeof(int) * (size_t)nb, st);
+  cudaError_t e = launch_bucket_selections(idx, N, H_kv, kk, kKlRows / G, count, offset,
+                                           tile_off, cursor, entries, st);
   if (e != cudaSuccess) return e;
-  const int64_t tiles = (N + kTileQ - 1) / kTileQ;
-  const dim3 pgrid((unsigned)((tiles + kKlPlanWarps - 1) / kKlPlanWarps), (unsigned)H_kv);
-  k_kl_plan<<<pgrid, 32 * kKlPlanWarps, 0, st>>>(idx, N, kk, nblk, 0, count, offset, cursor,
-                                                 entries);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  if ((e = launch_attn_scan(count, offset, tile_off, cursor, nb, kKlRows / G, st)) != cudaSuccess)
-    return e;
-  k_kl_plan<<<pgrid, 32 * kKlPlanWarps, 0, st>>>(idx, N, kk, nblk, 1, count, offset, cursor,
-                                                 entries);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
   KlQMaps tq;
   for (int m = 0; m < 5; ++m) {

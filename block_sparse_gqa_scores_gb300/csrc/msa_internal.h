@@ -74,6 +74,27 @@ cudaError_t launch_kl_loss_bwd(const void* q, const void* k, const void* q_idx, 
                                float* dk_idx, int64_t N, int H_q, int H_kv, int d_h, int d_idx,
                                int kk, void* ws, cudaStream_t st);
 cudaError_t read_reset_kl_status(unsigned* out);
+// Every selection of idx [H_kv, N, k] bucketed by (group, block) (entries (row << 6 | slot) in
+// (16-query tile, query) order within a bucket; offsets and work-tile offsets of ept entries per
+// tile, totals at index H_kv * ceil(N/64)).
+cudaError_t launch_bucket_selections(const int32_t* idx, int64_t N, int H_kv, int kk, int ept,
+                                     int* count, int* offset, int* tile_off, int* cursor,
+                                     int* entries, cudaStream_t st);
+// The same buckets with every bucket's entries in row order, independent of execution order;
+// cnt_mat holds H_kv * ceil(N/64) * ordered_bucket_ranges(N) ints of scratch.
+int ordered_bucket_ranges(int64_t N);
+cudaError_t launch_bucket_selections_ordered(const int32_t* idx, int64_t N, int H_kv, int kk,
+                                             int ept, int* count, int* offset, int* tile_off,
+                                             int* cursor, int* cnt_mat, int* entries,
+                                             cudaStream_t st);
+
+// Backward of the main branch: workspace bytes and the launch sequence.
+size_t sparse_attn_bwd_ws_bytes(int64_t N, int H_q, int H_kv, int d_h, int kk);
+cudaError_t launch_sparse_attn_bwd(const void* q, const void* k, const void* v, const int32_t* idx,
+                                   const void* o, const float* lse, const void* d_o, float* dq,
+                                   float* dk, float* dv, int64_t N, int H_q, int H_kv, int d_h,
+                                   int kk, void* ws, cudaStream_t st);
+cudaError_t read_reset_bwd_status(unsigned* out);
 
 cudaError_t launch_select_prefill(const float* M, int32_t* idx, int64_t N, int H_kv, int k,
                                   int64_t q_start, int64_t q_count, cudaStream_t stream);

@@ -40,6 +40,10 @@ def _load():
     L.msa_sparse_attn_fwd_workspace.argtypes = [i64, i32, i32, i32, i32]
     L.msa_sparse_attn_fwd_workspace.restype = sz
     L.msa_sparse_attn_fwd.argtypes = [P, P, P, P, P, P, i64, i32, i32, i32, i32, i32, P, sz, P]
+    L.msa_sparse_attn_bwd_workspace.argtypes = [i64, i32, i32, i32, i32]
+    L.msa_sparse_attn_bwd_workspace.restype = sz
+    L.msa_sparse_attn_bwd.argtypes = [P, P, P, P, P, P, P, P, P, P, i64, i32, i32, i32, i32, i32,
+                                      P, sz, P]
     L.msa_sparse_decode_workspace.argtypes = [i32, i64, i32, i32, i32, i32, i32]
     L.msa_sparse_decode_workspace.restype = sz
     L.msa_sparse_decode.argtypes = [P, P, P, P, P, P, i32, i64, i32, i32, i32, i32, i32, i32, P, P,
@@ -62,6 +66,7 @@ def _load():
     L.msa_kl_loss_bwd.argtypes = [P, P, P, P, P, P, P, P, P, P, P, i64, i32, i32, i32, i32, i32,
                                   i32, P, sz, P]
     for fn in ("msa_index_block_scores", "msa_select_blocks", "msa_index_select", "msa_sparse_attn_fwd",
+               "msa_sparse_attn_bwd",
                "msa_sparse_decode", "msa_sparse_decode_noalloc", "msa_sparse_decode_paged",
                "msa_prefill_varlen",
                "msa_kl_loss_fwd", "msa_kl_loss_bwd",
@@ -190,6 +195,41 @@ def msa_sparse_attn_fwd(q, k, v, idx, o=None, lse=None, ws=None, block_size=BLOC
         _ptr(q), _ptr(k), _ptr(v), _ptr(idx), _ptr(o), _ptr(lse), N, H_q, H_kv, d_h, block_size,
         kk, _ptr(ws), 0 if ws is None else ws.numel(), _stream(stream)))
     return o, lse
+
+
+def msa_sparse_attn_bwd_workspace(N, H_q, H_kv, d_h, k):
+    return int(lib.msa_sparse_attn_bwd_workspace(N, H_q, H_kv, d_h, k))
+
+
+def msa_sparse_attn_bwd(q, k, v, idx, o, lse, d_o, dq=None, dk=None, dv=None, ws=None,
+                        block_size=BLOCK, stream=None):
+    """Main-branch gradients for upstream d_o: (dq [N,H_q,d_h], dk, dv [N,H_kv,d_h]) fp32, from
+    the forward's o and lse on the same q, k, v, idx."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (d_o, "d_o")):
+        _req(t, torch.bfloat16, 3, n, device=q.device)
+    _req(idx, torch.int32, 3, "idx", device=q.device)
+    N, H_q, d_h = q.shape
+    H_kv = k.shape[1]
+    kk = idx.shape[2]
+    _req(o, torch.bfloat16, 3, "o", q.shape)
+    _req(d_o, torch.bfloat16, 3, "d_o", q.shape)
+    _req(lse, torch.float32, 2, "lse", (H_q, N), q.device)
+    if dq is None:
+        dq = torch.empty(q.shape, dtype=torch.float32, device=q.device)
+    if dk is None:
+        dk = torch.empty(k.shape, dtype=torch.float32, device=q.device)
+    if dv is None:
+        dv = torch.empty(v.shape, dtype=torch.float32, device=q.device)
+    _req(dq, torch.float32, 3, "dq", q.shape, q.device)
+    _req(dk, torch.float32, 3, "dk", k.shape, q.device)
+    _req(dv, torch.float32, 3, "dv", v.shape, q.device)
+    if ws is None:
+        ws = torch.empty(max(16, msa_sparse_attn_bwd_workspace(N, H_q, H_kv, d_h, kk)),
+                         dtype=torch.uint8, device=q.device)
+    _check("msa_sparse_attn_bwd", lib.msa_sparse_attn_bwd(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(idx), _ptr(o), _ptr(lse), _ptr(d_o), _ptr(dq), _ptr(dk),
+        _ptr(dv), N, H_q, H_kv, d_h, block_size, kk, _ptr(ws), ws.numel(), _stream(stream)))
+    return dq, dk, dv
 
 
 def msa_sparse_decode_workspace(S, max_len, H_q, H_kv, d_h, d_idx, k):

@@ -124,6 +124,37 @@ msa_status_t msa_sparse_attn_fwd(const void *q, const void *k, const void *v, co
                                  int block_size, int k_blocks, void *ws, size_t ws_bytes,
                                  void *stream);
 
+/* Workspace bytes msa_sparse_attn_bwd needs (0 for invalid sizes): per (group, block) bucket
+ * counts and offsets, per selection an entry and a fp32 dQ partial of G*d_h values (the bulk:
+ * 4*H_kv*N*k*G*d_h bytes, 34.4 GB at N = 131072, H_q = 32, H_kv = 4, k = 16, d_h = 128), per
+ * (row, head) the delta dO . O, and one fp32 dK/dV partial of 2*64*d_h values per piece of at
+ * most 64 work tiles of a bucket. */
+size_t msa_sparse_attn_bwd_workspace(int64_t N, int H_q, int H_kv, int d_h, int k);
+
+/* Backward of the sparse main branch (eq. O^(h)_i of section 主分支 differentiated; the
+ * persistent, load-balanced backward of section Kernel).  With the forward's o and lse for the
+ * same q, k, v, idx and the upstream gradient d_o, for every row i, head h (group r) and selected
+ * visible token j (the forward's T_i):
+ *   P_j = exp(q[i,h].k[j,r]/sqrt(d_h) - lse[h,i]),  D = d_o[i,h] . o[i,h],
+ *   dS_j = P_j (d_o[i,h] . v[j,r] - D)
+ *   dq[i,h,:] = sum_j dS_j k[j,r,:] / sqrt(d_h)
+ *   dk[j,r,:] = sum_{(i,h): j in T_i} dS_j q[i,h,:] / sqrt(d_h),  dv[j,r,:] = sum_{(i,h)} P_j d_o[i,h,:]
+ *   q, d_o, o  bf16 [N, H_q, d_h];  k, v bf16 [N, H_kv, d_h];  idx int32 [H_kv, N, k] (as the
+ *              forward requires it);  lse fp32 [H_q, N] (the forward's, natural log)
+ *   dq         fp32 [N, H_q, d_h];  dk, dv fp32 [N, H_kv, d_h] (written in full; tokens no query
+ *              selected get 0)
+ *   ws         device workspace of msa_sparse_attn_bwd_workspace() bytes, 16-byte aligned.
+ * P and dS enter the tensor-core products as bf16, accumulation is fp32.  Every selection is
+ * bucketed by (group, block) and each bucket cut into pieces of at most 64 work tiles; dq sums a
+ * row's partials in slot order and dk/dv a bucket's pieces in piece order, with no atomic update
+ * of any result, so the outputs are deterministic.  Errors as msa_sparse_attn_fwd; N > 2^21 or
+ * H_kv * N * k >= 2^31: MSA_ERR_UNSUPPORTED. */
+msa_status_t msa_sparse_attn_bwd(const void *q, const void *k, const void *v, const int32_t *idx,
+                                 const void *o, const float *lse, const void *d_o, float *dq,
+                                 float *dk, float *dv, int64_t N, int H_q, int H_kv, int d_h,
+                                 int block_size, int k_blocks, void *ws, size_t ws_bytes,
+                                 void *stream);
+
 /* Workspace bytes msa_prefill_varlen needs: that of msa_sparse_attn_fwd for the longest sequence
  * (0 for invalid sizes).  cu_seqlens is host memory here. */
 size_t msa_prefill_varlen_workspace(const int64_t *cu_seqlens, int nseq, int H_q, int H_kv,

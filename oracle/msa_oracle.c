@@ -324,12 +324,12 @@ static void row_kl_grad(const uint16_t *q_i, const uint16_t *qidx_ir, const uint
  * [N, H_kv, d_h] accumulated. */
 static void row_attend_grad(const uint16_t *q_i, const uint16_t *do_i, const uint16_t *K,
                             const uint16_t *V, int64_t i, int H_q, int H_kv, int d_h, int B,
-                            const int32_t *sel, int kk, double *dq, double *dk, double *dv,
-                            double *s_buf, double *p_buf, int64_t *j_buf)
+                            const int32_t *sel, int kk, int h_begin, int h_end, double *dq,
+                            double *dk, double *dv, double *s_buf, double *p_buf, int64_t *j_buf)
 {
     const int G = H_q / H_kv;
     const double scale = 1.0 / sqrt((double)d_h);
-    for (int h = 0; h < H_q; ++h) {
+    for (int h = h_begin; h < h_end; ++h) {
         const int r = h / G;
         const uint16_t *qh = q_i + (int64_t)h * d_h, *doh = do_i + (int64_t)h * d_h;
         int64_t nt = 0;
@@ -642,28 +642,32 @@ void msa_oracle_kl_loss_grad(const uint16_t *q, const uint16_t *k, const uint16_
 
 /* Main-branch gradient over all N rows with a given selection I [H_kv, N, kk] and upstream dO
  * [N, H_q, d_h] (bf16 bits): dQ [N, H_q, d_h], dK, dV [N, H_kv, d_h] (fp64, overwritten).
- * Single-threaded: dK and dV are plain sums in row order. */
+ * One thread per KV group r (only the heads of group r touch dK[:, r] and dV[:, r]); within a
+ * group, dK and dV are plain sums in row order, then head order. */
 void msa_oracle_sparse_attn_grad(const uint16_t *q, const uint16_t *k, const uint16_t *v,
                                  const uint16_t *dO, const int32_t *I, int64_t N, int H_q,
                                  int H_kv, int d_h, int B, int kk, double *dQ, double *dK,
                                  double *dV)
 {
-    double *s_buf = (double *)malloc((size_t)kk * B * sizeof(double));
-    double *p_buf = (double *)malloc((size_t)kk * B * sizeof(double));
-    int64_t *j_buf = (int64_t *)malloc((size_t)kk * B * sizeof(int64_t));
-    int32_t *sel = (int32_t *)malloc((size_t)H_kv * kk * sizeof(int32_t));
+    const int G = H_q / H_kv;
     for (int64_t e = 0; e < N * (int64_t)H_kv * d_h; ++e) dK[e] = dV[e] = 0.0;
-    for (int64_t i = 0; i < N; ++i) {
-        for (int r = 0; r < H_kv; ++r)
+#pragma omp parallel for schedule(static, 1)
+    for (int r = 0; r < H_kv; ++r) {
+        double *s_buf = (double *)malloc((size_t)kk * B * sizeof(double));
+        double *p_buf = (double *)malloc((size_t)kk * B * sizeof(double));
+        int64_t *j_buf = (int64_t *)malloc((size_t)kk * B * sizeof(int64_t));
+        int32_t *sel = (int32_t *)malloc((size_t)H_kv * kk * sizeof(int32_t));
+        for (int64_t i = 0; i < N; ++i) {
             for (int u = 0; u < kk; ++u) sel[r * kk + u] = I[((int64_t)r * N + i) * kk + u];
-        row_attend_grad(q + i * H_q * (int64_t)d_h, dO + i * H_q * (int64_t)d_h, k, v, i, H_q,
-                        H_kv, d_h, B, sel, kk, dQ + i * H_q * (int64_t)d_h, dK, dV, s_buf, p_buf,
-                        j_buf);
+            row_attend_grad(q + i * H_q * (int64_t)d_h, dO + i * H_q * (int64_t)d_h, k, v, i,
+                            H_q, H_kv, d_h, B, sel, kk, r * G, (r + 1) * G,
+                            dQ + i * H_q * (int64_t)d_h, dK, dV, s_buf, p_buf, j_buf);
+        }
+        free(s_buf);
+        free(p_buf);
+        free(j_buf);
+        free(sel);
     }
-    free(s_buf);
-    free(p_buf);
-    free(j_buf);
-    free(sel);
 }
 
 /* Exposed for the pins on the rounding step. */

@@ -29,7 +29,7 @@ def test_header_declares_the_api():
                  "msa_sparse_decode_workspace", "msa_sparse_decode_paged", "msa_prefill_varlen",
                  "msa_prefill_varlen_workspace", "msa_kl_loss_fwd", "msa_kl_loss_bwd",
                  "msa_kl_loss_bwd_workspace",
-                 "msa_kl_loss_fwd_workspace",
+                 "msa_kl_loss_fwd_workspace", "msa_sparse_attn_bwd", "msa_sparse_attn_bwd_workspace",
                  "msa_status_string", "msa_device_status"):
         assert name in syms
 

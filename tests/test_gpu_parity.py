@@ -344,6 +344,50 @@ def test_kl_loss_grad(name, over, N, k):
     assert np.abs(psum.cpu().numpy() - ref["psum"]).max() <= 1e-4
 
 
+# ------------------------------------------------------- main-branch backward --
+# dQ, dK, dV of the main branch against the oracle's fp64 gradient (which recomputes P and
+# D = sum_j P_j dP_j itself) on the GPU's own selection.  Bound: P and dS enter the tensor-core
+# products rounded to bf16 (2^-9 relative each), D comes from the bf16-rounded forward output,
+# and the sums run in fp32 over at most 1024 tokens (dQ) or every selecting row (dK, dV): errors
+# of a few 1e-3 of each tensor's largest magnitude, so 1e-2 of it leaves a wide margin.  Where a
+# gradient vanishes exactly (a row with one visible token has dS = dP - D = 0), what remains is
+# the fp32 rounding of the d_h-term dot products dP and D that cancel (|dP| ~ sqrt(d_h)): a floor
+# of 1e-4 covers it with margin.
+BWD_RTOL = 1e-2
+BWD_ATOL = 1e-4
+
+BWD_CASES = [
+    ("tiny", {}, 1024, 4), ("tiny", {}, 4500, 4), ("tiny", {}, 1024, 64),
+    ("p32k", {}, 1, 16), ("p32k", {}, 65, 16), ("p32k", {}, 1000, 16), ("p32k", {}, 2500, 16),
+    ("p32k", dict(H_q=4, H_kv=4), 700, 8), ("p32k", dict(H_q=8, H_kv=4), 700, 8),
+    ("p32k", dict(H_q=16, H_kv=4), 700, 8), ("p32k", dict(H_q=8, H_kv=1), 700, 5),
+    ("p32k", dict(d_h=64), 900, 16), ("tiny", dict(d_h=128), 900, 4),
+]
+
+
+@pytest.mark.parametrize("name,over,N,k", BWD_CASES)
+def test_sparse_attn_bwd(name, over, N, k):
+    cfg = cfg_of(name, k=k, **over)
+    x, b = fresh(cfg, N, seed=51)
+    idx = gpu_index(x, cfg, N)
+    o, lse = msa.msa_sparse_attn_fwd(x["q"], x["k"], x["v"], idx)
+    g = torch.Generator(device="cuda").manual_seed(5)
+    d_o = torch.randn(x["q"].shape, generator=g, device="cuda").to(torch.bfloat16)
+    dq, dk, dv = msa.msa_sparse_attn_bwd(x["q"], x["k"], x["v"], idx, o, lse, d_o)
+    sync_ok()
+    ref = oracle.sparse_attn_grad(b["q"], b["k"], b["v"], gen.to_bits(d_o), idx.cpu().numpy())
+    for got, nm in ((dq, "dq"), (dk, "dk"), (dv, "dv")):
+        got = got.cpu().numpy().astype(np.float64)
+        want = ref[nm]
+        assert np.isfinite(got).all(), nm
+        err, scale = float(np.abs(got - want).max()), float(np.abs(want).max())
+        assert err <= BWD_RTOL * scale + BWD_ATOL, (nm, err, scale)
+    # deterministic: no atomic updates, so a second call gives the same bits
+    dq2, dk2, dv2 = msa.msa_sparse_attn_bwd(x["q"], x["k"], x["v"], idx, o, lse, d_o)
+    sync_ok()
+    assert torch.equal(dq, dq2) and torch.equal(dk, dk2) and torch.equal(dv, dv2)
+
+
 # -------------------------------------------------------------- varlen prefill --
 
 @pytest.mark.parametrize("name,lens", [("p32k", [1, 63, 64, 65, 1000, 3000, 4500]),
