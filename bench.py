@@ -603,6 +603,7 @@ def time_decode_paged(msa, dcfg, d, dbufs, K, sizes, pk, world):
 
 
 VARLEN_LENS = (65536, 32768, 16384, 8192, 4096, 2048, 1024, 512, 256, 256)
+VARLEN_UNIFORM = (64, 2048)       # a batch of many equal short sequences (count, length)
 
 
 def time_varlen(msa, pcfg, x, bufs, K, world):
@@ -632,8 +633,35 @@ def time_varlen(msa, pcfg, x, bufs, K, world):
     torch.cuda.synchronize()
     msa.msa_device_status()
     ms = max_over_ranks(float(np.mean([evs[s].elapsed_time(evs[s + 1]) for s in range(K)])), world)
-    return {"ms": round(ms, 4), "value": round(world * N / (ms * 1e-3), 1), "unit": "tokens/s",
-            "sequences": lens}
+    out = {"ms": round(ms, 4), "value": round(world * N / (ms * 1e-3), 1), "unit": "tokens/s",
+           "sequences": lens}
+    # many equal short sequences: launch count per sequence matters most here
+    cnt, ln = VARLEN_UNIFORM
+    if cnt * ln <= N:
+        cu2 = torch.arange(cnt + 1, dtype=torch.int64) * ln
+        T = cnt * ln
+
+        def call2():
+            msa.msa_prefill_varlen(x["q"][:T], x["k"][:T], x["v"][:T], x["q_idx"][:T],
+                                   x["k_idx"][:T], cu2, pcfg.k, o=bufs["o"][:T],
+                                   lse=bufs["lse"].view(-1)[:T * pcfg.H_q],
+                                   idx=bufs["idx"].view(-1)[:T * pcfg.H_kv * pcfg.k], ws=bufs["ws"])
+
+        for _ in range(3):
+            call2()
+        torch.cuda.synchronize()
+        ev2 = [torch.cuda.Event(enable_timing=True) for _ in range(K + 1)]
+        ev2[0].record(stream)
+        for s in range(K):
+            call2()
+            ev2[s + 1].record(stream)
+        torch.cuda.synchronize()
+        msa.msa_device_status()
+        ms2 = max_over_ranks(float(np.mean([ev2[s].elapsed_time(ev2[s + 1]) for s in range(K)])),
+                             world)
+        out["uniform"] = {"sequences": cnt, "length": ln, "ms": round(ms2, 4),
+                          "value": round(world * T / (ms2 * 1e-3), 1), "unit": "tokens/s"}
+    return out
 
 
 def e2e_prefill(msa, pcfg, x, bufs, K, W, world):

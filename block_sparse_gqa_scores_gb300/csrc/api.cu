@@ -82,7 +82,7 @@ DecodeWs decode_layout(int S, int64_t max_len, int H_q, int H_kv, int d_h, int k
   DecodeWs w{};
   const int64_t nblk = (max_len + 63) / 64;
   const int G = H_q / H_kv;
-  w.nsplit = k < 4 ? k : 4;
+  w.nsplit = k < 8 ? k : 8;            // splits per (sequence, group): 2 blocks each at k = 16
   size_t off = 0;
   w.off_m = off;
   off = align256(off + sizeof(float) * (size_t)S * H_kv * nblk);
