@@ -53,6 +53,7 @@ __global__ void __launch_bounds__(32 * kWarps) k_sparse_attn(const AttnParams p)
   constexpr int KCH = D_H / 32;            // 16-B K chunks per thread per key row
   constexpr int VCH = D_H / 64;            // 16-B V chunks per thread per key
   __shared__ AttnSmem<D_H> sm;
+  pdl_launch_dependents();                  // the merge may be scheduled under this grid's tail
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int c = lane & 3, r4 = lane >> 2;
@@ -100,6 +101,7 @@ __global__ void __launch_bounds__(32 * kWarps) k_sparse_attn(const AttnParams p)
   float l_run[2] = {0.f, 0.f};
 
 
+  pdl_wait();                               // the selection is written
   for (int t = t0; t < t1; ++t) {
     const int b = __ldg(sel + t);
     if (b < 0) continue;
@@ -268,6 +270,7 @@ __global__ void __launch_bounds__(128) k_decode_merge(const float* __restrict__ 
                                                       __nv_bfloat16* __restrict__ o,
                                                       float* __restrict__ lse, int H_q, int H_kv,
                                                       int G, int nsplit) {
+  pdl_wait();                                    // the split partials are written
   const int64_t sr = blockIdx.x;                 // (s, r)
   const int64_t s = sr / H_kv;
   const int r = (int)(sr - s * H_kv);
@@ -320,24 +323,21 @@ cudaError_t launch_sparse_attn_decode(const void* q, const void* k_cache, const 
   p.kk = kk;
   p.nsplit = nsplit;
   p.scale_log2 = (float)(1.4426950408889634 / sqrt((double)d_h));
-  const int64_t grid = (int64_t)S * H_kv * nsplit;
-  const int64_t mgrid = (int64_t)S * H_kv;
-  if (d_h == 128) {
-    if (cm.pages)
-      k_sparse_attn<128, true><<<(unsigned)grid, 32 * kWarps, 0, stream>>>(p);
-    else
-      k_sparse_attn<128, false><<<(unsigned)grid, 32 * kWarps, 0, stream>>>(p);
-    k_decode_merge<128><<<(unsigned)mgrid, 128, 0, stream>>>(
-        part_o, part_lse, static_cast<__nv_bfloat16*>(o), lse, H_q, H_kv, p.G, nsplit);
-  } else {
-    if (cm.pages)
-      k_sparse_attn<64, true><<<(unsigned)grid, 32 * kWarps, 0, stream>>>(p);
-    else
-      k_sparse_attn<64, false><<<(unsigned)grid, 32 * kWarps, 0, stream>>>(p);
-    k_decode_merge<64><<<(unsigned)mgrid, 128, 0, stream>>>(
-        part_o, part_lse, static_cast<__nv_bfloat16*>(o), lse, H_q, H_kv, p.G, nsplit);
-  }
-  return cudaGetLastError();
+  const dim3 grid((unsigned)((int64_t)S * H_kv * nsplit));
+  const dim3 mgrid((unsigned)((int64_t)S * H_kv));
+  auto* ob = static_cast<__nv_bfloat16*>(o);
+  // both launches may start under the previous kernel's tail (they wait for its results)
+  auto run = [&](auto attn, auto merge) -> cudaError_t {
+    cudaError_t e = launch_pdl(attn, grid, dim3(32 * kWarps), 0, stream, p);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(merge, mgrid, dim3(128), 0, stream, (const float*)part_o,
+                      (const float*)part_lse, ob, lse, H_q, H_kv, p.G, nsplit);
+  };
+  if (d_h == 128)
+    return cm.pages ? run(k_sparse_attn<128, true>, k_decode_merge<128>)
+                    : run(k_sparse_attn<128, false>, k_decode_merge<128>);
+  return cm.pages ? run(k_sparse_attn<64, true>, k_decode_merge<64>)
+                  : run(k_sparse_attn<64, false>, k_decode_merge<64>);
 }
 
 }  // namespace msa

@@ -30,6 +30,7 @@ __global__ void __launch_bounds__(32 * kDecWarps)
                           float scale) {
   constexpr int KS = D_IDX / 16;           // k-steps
   constexpr int KCH = D_IDX / 32;          // 16-B chunks per thread per token row
+  pdl_launch_dependents();                 // the selection may be scheduled under this grid's tail
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int c = lane & 3, r4 = lane >> 2;
   const int64_t s = blockIdx.y;

@@ -216,6 +216,8 @@ __global__ void __launch_bounds__(32 * kSelWarps)
                     int64_t nblk_max) {
   __shared__ SelScratch sc[kSelWarps];
   __shared__ int s_cnt[kSelWarps];
+  pdl_launch_dependents();
+  pdl_wait();                                                   // the block scores are written
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t row = blockIdx.x;                               // row = s*H_kv + r
   const int64_t s = row / H_kv;
@@ -277,9 +279,8 @@ cudaError_t launch_select_decode(const float* Mdec, int32_t* idx, const CacheMap
                                  int H_kv, int k, int64_t max_len, int64_t nblk_max,
                                  cudaStream_t stream) {
   const int64_t nrows = (int64_t)S * H_kv;
-  k_select_decode<<<(unsigned)nrows, 32 * kSelWarps, 0, stream>>>(Mdec, idx, cm, S, H_kv, k,
-                                                                  max_len, nblk_max);
-  return cudaGetLastError();
+  return launch_pdl(k_select_decode, dim3((unsigned)nrows), dim3(32 * kSelWarps), 0, stream, Mdec,
+                    idx, cm, S, H_kv, k, max_len, nblk_max);
 }
 
 }  // namespace msa

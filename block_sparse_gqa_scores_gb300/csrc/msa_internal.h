@@ -7,6 +7,25 @@
 
 namespace msa {
 
+// Launches kernel<<<grid, block, smem, stream>>>(args...) with programmatic stream serialization:
+// it may start while the previous kernel on the stream finishes, and must call pdl_wait() before
+// reading that kernel's results.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // Byte offsets of the decode workspace: block scores [S, H_kv, ceil(max_len/64)] fp32,
 // selections [S, H_kv, k] int32, split partials O [S*H_kv*nsplit, G, d_h] and LSE
 // [S*H_kv*nsplit, G] fp32, each 256-byte aligned.
