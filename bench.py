@@ -40,14 +40,14 @@ import gen  # noqa: E402
 METRIC = ("MSA prefill tokens/s and decode tokens/s at 128K ctx; % of bf16 TC / HBM roofline")
 # kernels per step: the fused index branch (block scores + top-k); attention per 32768-row chunk:
 # plan, scan, plan, block-major pass, shared-block pass with the merge (+ one memset); decode:
-# scores, select, attention, merge
+# the index-key scan and the tail (selection + attention + merge in one kernel)
 ATTN_LAUNCHES_PER_CHUNK = 5
 ATTN_CHUNK_ROWS = 32768
-DECODE_LAUNCHES = 4
+DECODE_LAUNCHES = 2
 KERNEL_FILES = {"index_branch": ["k_score.cu"],
                 "main_branch": ["attn_fwd.cu", "k_attn_shared.cu", "k_attn_kvouter.cu",
                                 "k_attn_plan.cu", "attn_tile.cuh"],
-                "decode": ["k_decode.cu", "k_select.cu", "k_attn.cu"],
+                "decode": ["k_decode.cu", "select_core.cuh", "k_attn.cu"],
                 "kl_loss_fwd": ["k_kl.cu", "k_attn_plan.cu", "attn_tile.cuh"],
                 "kl_loss_bwd": ["k_kl.cu", "k_attn_plan.cu", "attn_tile.cuh"],
                 "sparse_attn_bwd": ["k_attn_bwd.cu", "k_kl.cu", "k_attn_plan.cu", "attn_tile.cuh"]}
@@ -109,8 +109,7 @@ def kernel_source_hash(fnames):
 NCU_ROWS = {"k_index_block_scores": "index_branch",
             "k_attn_plan": "main_branch", "k_attn_scan": "main_branch",
             "k_attn_kvouter": "main_branch", "k_attn_shared": "main_branch",
-            "k_decode_block_scores": "decode", "k_select_decode": "decode",
-            "k_sparse_attn": "decode", "k_decode_merge": "decode",
+            "k_decode_block_scores": "decode", "k_decode_tail": "decode",
             "k_kl_plan": "kl_loss_fwd", "k_kl_kvouter": "kl_loss_fwd", "k_kl_merge": "kl_loss_fwd",
             "k_kl_dq_merge": "kl_loss_bwd",
             "k_attn_bwd_kvouter": "sparse_attn_bwd", "k_attn_bwd_dq_merge": "sparse_attn_bwd",

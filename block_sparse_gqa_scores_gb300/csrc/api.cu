@@ -79,19 +79,15 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 namespace msa {
 
 DecodeWs decode_layout(int S, int64_t max_len, int H_q, int H_kv, int d_h, int k) {
+  (void)H_q;
+  (void)d_h;
   DecodeWs w{};
   const int64_t nblk = (max_len + 63) / 64;
-  const int G = H_q / H_kv;
-  w.nsplit = k < 8 ? k : 8;            // splits per (sequence, group): 2 blocks each at k = 16
   size_t off = 0;
   w.off_m = off;
   off = align256(off + sizeof(float) * (size_t)S * H_kv * nblk);
   w.off_idx = off;
   off = align256(off + sizeof(int32_t) * (size_t)S * H_kv * k);
-  w.off_po = off;
-  off = align256(off + sizeof(float) * (size_t)S * H_kv * w.nsplit * G * d_h);
-  w.off_pl = off;
-  off = align256(off + sizeof(float) * (size_t)S * H_kv * w.nsplit * G);
   w.total = off;
   return w;
 }
@@ -230,17 +226,13 @@ MSA_API msa_status_t msa_sparse_decode(const void* q, const void* q_idx, const v
   char* base = static_cast<char*>(ws);
   float* Mdec = reinterpret_cast<float*>(base + w.off_m);
   int32_t* idx = idx_out ? idx_out : reinterpret_cast<int32_t*>(base + w.off_idx);
-  float* part_o = reinterpret_cast<float*>(base + w.off_po);
-  float* part_lse = reinterpret_cast<float*>(base + w.off_pl);
   const int64_t nblk = (max_len + 63) / 64;
   const msa::CacheMap cm{cu_seqlens, nullptr, nullptr, 0, 0};
   cudaError_t e = msa::launch_decode_block_scores(q_idx, k_idx_cache, cm, Mdec, S, H_kv,
                                                   d_idx, max_len, nblk, st);
   if (e != cudaSuccess) return MSA_ERR_CUDA;
-  e = msa::launch_select_decode(Mdec, idx, cm, S, H_kv, k, max_len, nblk, st);
-  if (e != cudaSuccess) return MSA_ERR_CUDA;
-  e = msa::launch_sparse_attn_decode(q, k_cache, v_cache, idx, cm, S, max_len, H_q, H_kv,
-                                     d_h, k, w.nsplit, part_o, part_lse, o, lse, st);
+  e = msa::launch_decode_tail(q, k_cache, v_cache, Mdec, nblk, cm, S, max_len, H_q, H_kv, d_h, k,
+                              idx, o, lse, st);
   return from_cuda(e);
 }
 
@@ -333,17 +325,13 @@ MSA_API msa_status_t msa_sparse_decode_paged(
   char* base = static_cast<char*>(ws);
   float* Mdec = reinterpret_cast<float*>(base + w.off_m);
   int32_t* idx = idx_out ? idx_out : reinterpret_cast<int32_t*>(base + w.off_idx);
-  float* part_o = reinterpret_cast<float*>(base + w.off_po);
-  float* part_lse = reinterpret_cast<float*>(base + w.off_pl);
   const int64_t nblk = (max_len + 63) / 64;
   const msa::CacheMap cm{nullptr, page_table, seq_lens, max_pages, num_pages};
   cudaError_t e = msa::launch_decode_block_scores(q_idx, k_idx_pages, cm, Mdec, S, H_kv, d_idx,
                                                   max_len, nblk, st);
   if (e != cudaSuccess) return MSA_ERR_CUDA;
-  e = msa::launch_select_decode(Mdec, idx, cm, S, H_kv, k, max_len, nblk, st);
-  if (e != cudaSuccess) return MSA_ERR_CUDA;
-  e = msa::launch_sparse_attn_decode(q, k_pages, v_pages, idx, cm, S, max_len, H_q, H_kv, d_h, k,
-                                     w.nsplit, part_o, part_lse, o, lse, st);
+  e = msa::launch_decode_tail(q, k_pages, v_pages, Mdec, nblk, cm, S, max_len, H_q, H_kv, d_h, k,
+                              idx, o, lse, st);
   return from_cuda(e);
 }
 

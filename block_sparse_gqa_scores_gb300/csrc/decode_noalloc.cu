@@ -5,7 +5,7 @@
 // for example a serving runtime that reserved all device memory for its own pool up front, or
 // a latency-critical decode loop that must not call cudaMalloc/cudaFree because those calls can
 // block on other work or synchronise the device.  Such a caller still owns and passes every
-// input and output; only the temporary block scores, selections and split partials live in
+// input and output; only the temporary block scores and selections live in
 // the array below.
 //
 // The array is part of the library image: every GPU that loads libmsa.so holds these bytes
@@ -77,16 +77,12 @@ extern "C" __attribute__((visibility("default"))) msa_status_t msa_sparse_decode
   char* base = static_cast<char*>(scratch);
   float* Mdec = reinterpret_cast<float*>(base + w.off_m);
   int32_t* idx = idx_out ? idx_out : reinterpret_cast<int32_t*>(base + w.off_idx);
-  float* part_o = reinterpret_cast<float*>(base + w.off_po);
-  float* part_lse = reinterpret_cast<float*>(base + w.off_pl);
   const int64_t nblk = (max_len + 63) / 64;
   const msa::CacheMap cm{cu_seqlens, nullptr, nullptr, 0, 0};
   cudaError_t e = msa::launch_decode_block_scores(q_idx, k_idx_cache, cm, Mdec, S, H_kv,
                                                   d_idx, max_len, nblk, st);
   if (e != cudaSuccess) return MSA_ERR_CUDA;
-  e = msa::launch_select_decode(Mdec, idx, cm, S, H_kv, k, max_len, nblk, st);
-  if (e != cudaSuccess) return MSA_ERR_CUDA;
-  e = msa::launch_sparse_attn_decode(q, k_cache, v_cache, idx, cm, S, max_len, H_q, H_kv,
-                                     d_h, k, w.nsplit, part_o, part_lse, o, lse, st);
+  e = msa::launch_decode_tail(q, k_cache, v_cache, Mdec, nblk, cm, S, max_len, H_q, H_kv, d_h,
+                              k, idx, o, lse, st);
   return e == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
 }

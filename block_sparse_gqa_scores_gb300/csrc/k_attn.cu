@@ -1,67 +1,77 @@
-// Decode attention of MSA («MiniMax-M3：MSA 技术报告速读», section 主分支, eq. O^(h)_i, and
-// the LSE of section Kernel): exact softmax attention of the G query heads of group r of one new
-// token over the visible tokens of its selected blocks, split into block ranges whose partials
-// are merged in a fixed order (the kernel section's pre-scheduled splits with a two-stage merge
-// and no atomics).
+// Decode tail of MSA («MiniMax-M3：MSA 技术报告速读», section 索引分支 eq. I^(r)_i and section
+// 主分支 eq. O^(h)_i with the LSE of section Kernel): for one new token per sequence, the per-group
+// top-k selection over the block scores the index-key scan wrote, then exact softmax attention of
+// the group's G query heads over the visible tokens of the selected blocks, in one CTA per
+// (sequence, group) -- no selection array, split partials or merge kernel between the stages.
 //
-// Layout of the work: one CTA = 4 warps per (sequence, group, split).  Warp w owns keys
-// [16w, 16w+16) of every selected block, so a block is read by the 4 warps side by side.  The
-// G <= 8 heads of the group are the N=8 side of the m16n8k16 MMA with the keys (S^T = K Q^T) or
-// the head dims (O^T += V^T P^T) as its M side, which wastes no MMA lane on the single query; P
-// goes from the S^T accumulator to the P^T operand with one movmatrix transpose per 8x8 tile.
-// K and V rows are loaded from global memory directly into MMA fragments as 16-byte vectors:
-//   * S^T: the contracted head dim is permuted identically in K (A operand) and Q^T (B), so a
-//     thread's A fragment words are whole 16-byte chunks of a K row;
-//   * O^T: a thread owns 8 (d_h=64) or 16 (d_h=128) head dims of V for 4 keys and pairs keys
-//     with byte permutes; the output rows are un-permuted when stored.
-// Online softmax per warp in the log2 domain (scale*log2 e folded into the scores), then the
-// four warps' (max, sum, O) states are merged in shared memory in a fixed order.
+//   selection   the row's candidate blocks are cut into segments, one per warp; each warp keeps
+//               its segment's k-1 best (select_core.cuh), then warp 0 keeps the k-1 best of those
+//               (exactly the single-warp selection) and appends the local block
+//   attention   warps form quads; quad g takes the selected blocks g, g + kQuads, ...; warp w of a
+//               quad owns keys [16w, 16w+16) of each of them.  The G <= 8 heads are the N=8 side of
+//               the m16n8k16 MMA with the keys (S^T = K Q^T) or the head dims (O^T += V^T P^T) as
+//               its M side; P goes from the S^T accumulator to the P^T operand with one movmatrix
+//               transpose per 8x8 tile.  K and V rows are loaded from global memory straight into
+//               MMA fragments as 16-byte vectors (the contracted head dim is permuted identically
+//               in K and Q^T; V keys are paired with byte permutes, output rows un-permuted).
+//               Online softmax per warp in the log2 domain
+//   merge       the warps' (max, sum, O) states combined in shared memory in warp order, then O
+//               (bf16) and the natural-log LSE written directly
+// Results do not depend on timing: the selection is exact, and every sum runs in a fixed order.
 #include <math.h>
 
-#include "msa_device.cuh"
 #include "msa_internal.h"
+#include "select_core.cuh"
 
 namespace msa {
 namespace {
 
-constexpr int kWarps = 4;
+constexpr int kTailWarps = 16;                 // 4 quads of 4 warps
+constexpr int kQuads = kTailWarps / 4;
 constexpr unsigned kFull = 0xffffffffu;
 
 template <int D_H>
-struct AttnSmem {
-  float m[kWarps][8];
-  float l[kWarps][8];
-  float o[kWarps][8][D_H];
+struct TailSmem {
+  int cnt[kTailWarps];
+  int blocks[64];                               // the row's selection (ascending, -1 padded)
+  float m[kTailWarps][8];
+  float l[kTailWarps][8];
+  union {                                       // selection scratch, then the warps' O states
+    sel::SelScratch sc[kTailWarps];
+    float o[kTailWarps][8][D_H];
+  } u;
 };
 
 struct AttnParams {
   const __nv_bfloat16* q;
   const __nv_bfloat16* k;
   const __nv_bfloat16* v;
-  const int32_t* idx;
-  float* part_o;      // decode split partials [S*H_kv*nsplit, G, D_H] (normalised)
-  float* part_lse;    // decode split partials [S*H_kv*nsplit, G] (log2 units)
+  const float* Mdec;  // block scores [S * H_kv, nblk_max]
+  int32_t* idx_out;   // [S, H_kv, k] or null
+  __nv_bfloat16* o;   // [S, H_q, D_H]
+  float* lse;         // [S, H_q], natural log
   CacheMap cm;        // where each sequence's cache rows are (packed or paged)
   int64_t max_len;    // length bound
-  int H_q, H_kv, G, kk, nsplit, S;
+  int64_t nblk_max;
+  int H_q, H_kv, G, kk, S;
   float scale_log2;   // log2(e) / sqrt(d_h)
 };
 
 template <int D_H, bool PAGED>
-__global__ void __launch_bounds__(32 * kWarps) k_sparse_attn(const AttnParams p) {
+__global__ void __launch_bounds__(32 * kTailWarps) k_decode_tail(const AttnParams p) {
   constexpr int KS = D_H / 16;             // k-steps of S^T, m-tiles of O^T
   constexpr int KCH = D_H / 32;            // 16-B K chunks per thread per key row
   constexpr int VCH = D_H / 64;            // 16-B V chunks per thread per key
-  __shared__ AttnSmem<D_H> sm;
-  pdl_launch_dependents();                  // the merge may be scheduled under this grid's tail
+  extern __shared__ __align__(16) uint8_t tail_raw[];
+  TailSmem<D_H>& sm = *reinterpret_cast<TailSmem<D_H>*>(tail_raw);
+  pdl_launch_dependents();
+  pdl_wait();                               // the block scores are written
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int c = lane & 3, r4 = lane >> 2;
 
   // ---------------------------------------------------------------- the problem
-  const int64_t unit = blockIdx.x;          // (sequence, group, split)
-  const int split = (int)(unit % p.nsplit);
-  const int64_t sr = unit / p.nsplit;
+  const int64_t sr = blockIdx.x;            // (sequence, group)
   const int64_t s = sr / p.H_kv;
   const int r = (int)(sr - s * p.H_kv);
   const int64_t L = p.cm.len<PAGED>(s, p.max_len);
@@ -70,11 +80,51 @@ __global__ void __launch_bounds__(32 * kWarps) k_sparse_attn(const AttnParams p)
   const __nv_bfloat16* kseq = p.k + (srow * p.H_kv + r) * D_H;   // packed: the sequence's rows
   const __nv_bfloat16* vseq = p.v + (srow * p.H_kv + r) * D_H;
   const int64_t i = L - 1;                  // the new token's position
-  const int32_t* sel = p.idx + sr * p.kk;
   const __nv_bfloat16* qrow = p.q + s * (int64_t)p.H_q * D_H;
-  const int per = (p.kk + p.nsplit - 1) / p.nsplit;
-  const int t0 = split * per;
-  const int t1 = min(p.kk, t0 + per);
+  const int kk = p.kk;
+
+  // ---------------------------------------------------------------- selection
+  {
+    const int64_t l = i >> 6;
+    const float* Mrow = p.Mdec + sr * p.nblk_max;
+    if (l + 1 <= kk) {
+      for (int x = threadIdx.x; x < kk; x += 32 * kTailWarps) sm.blocks[x] = x <= l ? x : -1;
+    } else {
+      const int K1 = kk - 1, n = (int)l;
+      int nseg = sel::kBuf / K1;
+      nseg = nseg > kTailWarps ? kTailWarps : (nseg < 1 ? 1 : nseg);
+      const int seg = (n + nseg - 1) / nseg;
+      if (warp < nseg) {
+        const int b0 = min(n, warp * seg), b1 = min(n, b0 + seg);
+        const int cnt = b1 > b0 ? sel::select_segment(Mrow, b0, b1, K1, sm.u.sc[warp]) : 0;
+        if (lane == 0) sm.cnt[warp] = cnt;
+      }
+      __syncthreads();
+      if (warp == 0) {
+        // the segments' survivors after warp 0's own, in segment (= block) order
+        int cnt = sm.cnt[0];
+        for (int w = 1; w < nseg; ++w) {
+          const int cw = sm.cnt[w];
+          for (int x = lane; x < cw; x += 32) {
+            sm.u.sc[0].v[cnt + x] = sm.u.sc[w].v[x];
+            sm.u.sc[0].b[cnt + x] = sm.u.sc[w].b[x];
+          }
+          cnt += cw;
+        }
+        __syncwarp();
+        if (cnt > K1) {
+          sel::compact(sm.u.sc[0], cnt, K1);
+          cnt = K1;
+        }
+        for (int x = lane; x < K1; x += 32) sm.blocks[x] = x < cnt ? sm.u.sc[0].b[x] : -1;
+        if (lane == 0) sm.blocks[K1] = (int32_t)l;
+      }
+    }
+    __syncthreads();
+    if (p.idx_out != nullptr)
+      for (int x = threadIdx.x; x < kk; x += 32 * kTailWarps) p.idx_out[sr * kk + x] = sm.blocks[x];
+  }
+  const int quad = warp >> 2, wq = warp & 3;   // this warp: keys [16 wq, 16 wq + 16) of its blocks
 
   // Q^T fragments (B operand of S^T = K Q^T): head n = r4, dims permuted as the K loads.
   uint32_t qf[KS][2];
@@ -101,9 +151,8 @@ __global__ void __launch_bounds__(32 * kWarps) k_sparse_attn(const AttnParams p)
   float l_run[2] = {0.f, 0.f};
 
 
-  pdl_wait();                               // the selection is written
-  for (int t = t0; t < t1; ++t) {
-    const int b = __ldg(sel + t);
+  for (int t = quad; t < kk; t += kQuads) {
+    const int b = sm.blocks[t];
     if (b < 0) continue;
     // keys are indexed by position; a paged block's rows are shifted to its page
     const __nv_bfloat16* kbase = kseq;
@@ -113,7 +162,7 @@ __global__ void __launch_bounds__(32 * kWarps) k_sparse_attn(const AttnParams p)
       kbase = p.k + shift + r * D_H;
       vbase = p.v + shift + r * D_H;
     }
-    const int64_t j0 = (int64_t)b * kBlock + 16 * warp;     // first key of this warp's slice
+    const int64_t j0 = (int64_t)b * kBlock + 16 * wq;       // first key of this warp's slice
     const int64_t jlo = j0 + r4, jhi = j0 + r4 + 8;
     const bool vlo = jlo <= i, vhi = jhi <= i;
 
@@ -226,118 +275,77 @@ __global__ void __launch_bounds__(32 * kWarps) k_sparse_attn(const AttnParams p)
   const int base_hi = (D_H == 128) ? 64 + 8 * r4 : 8 * r4 + 4;
 #pragma unroll
   for (int mt = 0; mt < KS; ++mt) {
-    sm.o[warp][2 * c][base_lo + mt] = oacc[mt][0];
-    sm.o[warp][2 * c + 1][base_lo + mt] = oacc[mt][1];
-    sm.o[warp][2 * c][base_hi + mt] = oacc[mt][2];
-    sm.o[warp][2 * c + 1][base_hi + mt] = oacc[mt][3];
+    sm.u.o[warp][2 * c][base_lo + mt] = oacc[mt][0];
+    sm.u.o[warp][2 * c + 1][base_lo + mt] = oacc[mt][1];
+    sm.u.o[warp][2 * c][base_hi + mt] = oacc[mt][2];
+    sm.u.o[warp][2 * c + 1][base_hi + mt] = oacc[mt][3];
   }
   __syncthreads();
 
-  // ---- merge the 4 warps: thread -> (head, 8-dim chunk)
+  // ---- merge the warps in warp order: thread -> (head, 8-dim chunk); O and LSE written
   constexpr int kChunks = D_H / 8;
-  for (int wi = threadIdx.x; wi < p.G * kChunks; wi += 32 * kWarps) {
+  for (int wi = threadIdx.x; wi < p.G * kChunks; wi += 32 * kTailWarps) {
     const int h = wi / kChunks, d0 = (wi - h * kChunks) * 8;
     float mx = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) mx = fmaxf(mx, sm.m[w][h]);
-    float wgt[kWarps], L = 0.f;
+    for (int w = 0; w < kTailWarps; ++w) mx = fmaxf(mx, sm.m[w][h]);
+    float L2 = 0.f, acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
-      wgt[w] = mx == -INFINITY ? 0.f : ex2(sm.m[w][h] - mx);
-      L += wgt[w] * sm.l[w][h];
+    for (int w = 0; w < kTailWarps; ++w) {
+      const float wgt = mx == -INFINITY ? 0.f : ex2(sm.m[w][h] - mx);
+      L2 += wgt * sm.l[w][h];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[e] += wgt * sm.u.o[w][h][d0 + e];
     }
-    const float inv = L > 0.f ? 1.f / L : 0.f;
-    float ov[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      float acc = 0.f;
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) acc += wgt[w] * sm.o[w][h][d0 + e];
-      ov[e] = acc * inv;
-    }
-    const float lse2 = L > 0.f ? mx + __log2f(L) : -INFINITY;
-    float* po = p.part_o + (unit * p.G + h) * D_H + d0;
-#pragma unroll
-    for (int e = 0; e < 8; ++e) po[e] = ov[e];
-    if (d0 == 0) p.part_lse[unit * p.G + h] = lse2;
-  }
-}
-
-// Decode: combine the split partials of each (sequence, head) in split order.
-template <int D_H>
-__global__ void __launch_bounds__(128) k_decode_merge(const float* __restrict__ part_o,
-                                                      const float* __restrict__ part_lse,
-                                                      __nv_bfloat16* __restrict__ o,
-                                                      float* __restrict__ lse, int H_q, int H_kv,
-                                                      int G, int nsplit) {
-  pdl_wait();                                    // the split partials are written
-  const int64_t sr = blockIdx.x;                 // (s, r)
-  const int64_t s = sr / H_kv;
-  const int r = (int)(sr - s * H_kv);
-  constexpr int kChunks = D_H / 8;
-  for (int wi = threadIdx.x; wi < G * kChunks; wi += blockDim.x) {
-    const int h = wi / kChunks, d0 = (wi - h * kChunks) * 8;
-    float mx = -INFINITY;
-    for (int sp = 0; sp < nsplit; ++sp) mx = fmaxf(mx, part_lse[(sr * nsplit + sp) * G + h]);
-    float L = 0.f, acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int sp = 0; sp < nsplit; ++sp) {
-      const int64_t u = sr * nsplit + sp;
-      const float w = mx == -INFINITY ? 0.f : ex2(part_lse[u * G + h] - mx);
-      L += w;
-      const float* po = part_o + (u * G + h) * D_H + d0;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) acc[e] += w * po[e];
-    }
-    const float inv = L > 0.f ? 1.f / L : 0.f;
-    const int hq = r * G + h;
+    const float inv = L2 > 0.f ? 1.f / L2 : 0.f;
+    const int hq = r * p.G + h;
     uint4 pk;
     pk.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
     pk.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
     pk.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
     pk.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
-    *reinterpret_cast<uint4*>(o + (s * H_q + hq) * D_H + d0) = pk;
-    if (d0 == 0) lse[s * H_q + hq] = (mx + __log2f(L)) * 0.69314718055994531f;
+    *reinterpret_cast<uint4*>(p.o + (s * p.H_q + hq) * D_H + d0) = pk;
+    if (d0 == 0) p.lse[s * p.H_q + hq] = (mx + __log2f(L2)) * 0.69314718055994531f;
   }
 }
 
 }  // namespace
 
-cudaError_t launch_sparse_attn_decode(const void* q, const void* k_cache, const void* v_cache,
-                                      const int32_t* idx, const CacheMap& cm, int S,
-                                      int64_t max_len, int H_q, int H_kv, int d_h, int kk,
-                                      int nsplit, float* part_o, float* part_lse, void* o,
-                                      float* lse, cudaStream_t stream) {
+cudaError_t launch_decode_tail(const void* q, const void* k_cache, const void* v_cache,
+                               const float* Mdec, int64_t nblk_max, const CacheMap& cm, int S,
+                               int64_t max_len, int H_q, int H_kv, int d_h, int kk,
+                               int32_t* idx_out, void* o, float* lse, cudaStream_t stream) {
   AttnParams p{};
   p.q = static_cast<const __nv_bfloat16*>(q);
   p.k = static_cast<const __nv_bfloat16*>(k_cache);
   p.v = static_cast<const __nv_bfloat16*>(v_cache);
-  p.idx = idx;
+  p.Mdec = Mdec;
+  p.idx_out = idx_out;
+  p.o = static_cast<__nv_bfloat16*>(o);
+  p.lse = lse;
   p.cm = cm;
-  p.part_o = part_o;
-  p.part_lse = part_lse;
   p.max_len = max_len;
+  p.nblk_max = nblk_max;
   p.S = S;
   p.H_q = H_q;
   p.H_kv = H_kv;
   p.G = H_q / H_kv;
   p.kk = kk;
-  p.nsplit = nsplit;
   p.scale_log2 = (float)(1.4426950408889634 / sqrt((double)d_h));
-  const dim3 grid((unsigned)((int64_t)S * H_kv * nsplit));
-  const dim3 mgrid((unsigned)((int64_t)S * H_kv));
-  auto* ob = static_cast<__nv_bfloat16*>(o);
-  // both launches may start under the previous kernel's tail (they wait for its results)
-  auto run = [&](auto attn, auto merge) -> cudaError_t {
-    cudaError_t e = launch_pdl(attn, grid, dim3(32 * kWarps), 0, stream, p);
+  const dim3 grid((unsigned)((int64_t)S * H_kv));
+  // may start under the index-key scan's tail (it waits for the block scores)
+  auto run = [&](auto kern, size_t smem) -> cudaError_t {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
     if (e != cudaSuccess) return e;
-    return launch_pdl(merge, mgrid, dim3(128), 0, stream, (const float*)part_o,
-                      (const float*)part_lse, ob, lse, H_q, H_kv, p.G, nsplit);
+    return launch_pdl(kern, grid, dim3(32 * kTailWarps), smem, stream, p);
   };
-  if (d_h == 128)
-    return cm.pages ? run(k_sparse_attn<128, true>, k_decode_merge<128>)
-                    : run(k_sparse_attn<128, false>, k_decode_merge<128>);
-  return cm.pages ? run(k_sparse_attn<64, true>, k_decode_merge<64>)
-                  : run(k_sparse_attn<64, false>, k_decode_merge<64>);
+  if (d_h == 128) {
+    constexpr size_t S128 = sizeof(TailSmem<128>);
+    return cm.pages ? run(k_decode_tail<128, true>, S128) : run(k_decode_tail<128, false>, S128);
+  }
+  constexpr size_t S64 = sizeof(TailSmem<64>);
+  return cm.pages ? run(k_decode_tail<64, true>, S64) : run(k_decode_tail<64, false>, S64);
 }
 
 }  // namespace msa

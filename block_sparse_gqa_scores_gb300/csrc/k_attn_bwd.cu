@@ -19,7 +19,8 @@
 //   dV^T += dO_stack^T P             M=d_h dims, N=64 keys, K=128 rows  (both operands MN-major)
 //   dK^T += Q_stack^T dS             M=d_h dims, N=64 keys, K=128 rows
 //   dQp  = dS K_b                    M=128 rows, N=d_h, K=64 keys       (K_b MN-major)
-// and each row writes its dQ partial (fp32) at the fixed position of its (group, row, slot).
+// and each row writes its dQ partial (bf16; staged in shared memory and stored by TMA at G = 8)
+// at the fixed position of its (group, row, slot).
 // Merges: dQ of a row sums its slots in slot order; dK, dV of a block sum the bucket's pieces in
 // piece order.  The buckets list their selections in row order (row-ordered planning), so the
 // work tiles and every sum's order are fixed: no atomic update of any result, and every output
@@ -139,7 +140,7 @@ struct BwdArgs {
   const int* offset;
   const int* tile_off;
   const int* piece_off;
-  float* part_dq;            // [H_kv, N, k, G, d_h]
+  __nv_bfloat16* part_dq;    // [H_kv, N, k, G, d_h]
   float* part_dkv;           // [pieces, 2, d_h, 64]: dK^T then dV^T
   int64_t N;
   int nb, nblk, H_kv, kk;
@@ -151,7 +152,8 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     k_attn_bwd_kvouter(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_do,
                        const __grid_constant__ CUtensorMap tm_k,
-                       const __grid_constant__ CUtensorMap tm_v, const BwdArgs a) {
+                       const __grid_constant__ CUtensorMap tm_v,
+                       const __grid_constant__ CUtensorMap tm_dq, const BwdArgs a) {
   using L = BwdSmem<D_H>;
   constexpr int kEpt = kRowsB / G;
   constexpr int kChunks = D_H / 8;
@@ -276,6 +278,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       }
       // ---- S = Q K_b^T and dP = dO V_b^T
       if (tid == 0) {
+        bulk_wait_read_all();           // the previous tile's dQ stores have read the staging
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < D_H / 16; ++ks) {
@@ -356,25 +359,46 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       }
       if (!(ok = wait_all(mma_bar, mma_ph))) break;
       tc_fence_after();
-      // ---- this row's dQ partial (unscaled; the merge applies 1/sqrt(d_h))
+      // ---- this row's dQ partial (bf16, unscaled; the merge applies 1/sqrt(d_h)).  At G = 8 the
+      //      rows are staged over P and dS (free once the MMAs above completed) in the layout of a
+      //      query box and stored by TMA, one 1-KB box per entry and half; otherwise row by row.
       {
-        float* dst = a.part_dq + ((((int64_t)rb * a.N + i) * a.kk + (ent & 63)) * G + h) * D_H;
+        const int64_t slot = ((int64_t)rb * a.N + i) * a.kk + (ent & 63);
 #pragma unroll
         for (int half = 0; half < D_H / 64; ++half) {
           uint32_t v[64];
           MSA_TMEM_LD64(tmem + lanes + 64 * half, v);
           tmem_ld_wait();
-          if (rv) {
-            float4* d4 = reinterpret_cast<float4*>(dst + 64 * half);
 #pragma unroll
-            for (int c = 0; c < 16; ++c)
-              d4[c] = make_float4(__uint_as_float(v[4 * c]), __uint_as_float(v[4 * c + 1]),
-                                  __uint_as_float(v[4 * c + 2]), __uint_as_float(v[4 * c + 3]));
+          for (int c = 0; c < 8; ++c) {
+            const uint32_t w0 = pack_bf16x2(__uint_as_float(v[8 * c]), __uint_as_float(v[8 * c + 1]));
+            const uint32_t w1 = pack_bf16x2(__uint_as_float(v[8 * c + 2]), __uint_as_float(v[8 * c + 3]));
+            const uint32_t w2 = pack_bf16x2(__uint_as_float(v[8 * c + 4]), __uint_as_float(v[8 * c + 5]));
+            const uint32_t w3 = pack_bf16x2(__uint_as_float(v[8 * c + 6]), __uint_as_float(v[8 * c + 7]));
+            if (G == 8) {
+              st_shared_v4(sb + L::kOffP + half * (kRowsB * 128) + R * 128 + ((c ^ (R & 7)) << 4),
+                           w0, w1, w2, w3);
+            } else if (rv) {
+              reinterpret_cast<uint4*>(a.part_dq + (slot * G + h) * D_H + 64 * half)[c] =
+                  make_uint4(w0, w1, w2, w3);
+            }
           }
         }
       }
       tc_fence_before();
-      __syncthreads();                                        // TMEM and s_ent are reused
+      if (G == 8) bwd_fence_async_smem();
+      __syncthreads();                                        // TMEM, s_ent and staging reused
+      if (G == 8 && tid == 0) {
+        for (int x = 0; x < n_e; ++x) {
+          const int ex = s_ent[x];
+          const int z = (int)(((int64_t)rb * a.N + (ex >> 6)) * a.kk + (ex & 63));
+#pragma unroll
+          for (int half = 0; half < D_H / 64; ++half)
+            tma_store_3d(&tm_dq, sb + L::kOffP + half * (kRowsB * 128) + x * 1024, 64 * half, 0, z);
+        }
+        bulk_commit();
+      }
+      __syncthreads();                                        // s_ent read before it is reused
     }
     if (!ok) break;
     // ---- the piece's dK^T and dV^T (lane = dim): its partial
@@ -406,6 +430,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     __syncthreads();
   }
 
+  if (tid == 0) bulk_wait_all();                            // the dQ stores have completed
   if (!ok && tid == 0) {
     // a wait gave up: let whatever it waited for land (bounded) and every MMA issued complete
     // before the tensor memory is released
@@ -424,7 +449,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
 // dq[i, h, :] = (1/sqrt(d_h)) sum over the row's selections (slot order) of their partials; one
 // thread per (row, head, 4 dims).
 __global__ void __launch_bounds__(256)
-    k_attn_bwd_dq_merge(const int32_t* __restrict__ idx, const float* __restrict__ part_dq,
+    k_attn_bwd_dq_merge(const int32_t* __restrict__ idx, const __nv_bfloat16* __restrict__ part_dq,
                         float* __restrict__ dq, int64_t N, int H_kv, int G, int d_h, int kk,
                         float scale) {
   const int64_t x = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -441,12 +466,14 @@ __global__ void __launch_bounds__(256)
   for (int t = 0; t < kk; ++t) {
     const int b = __ldg(sel + t);
     if (b < 0 || (int64_t)b > (i >> 6)) continue;
-    const float4 v = __ldg(reinterpret_cast<const float4*>(
-                         part_dq + ((((int64_t)r * N + i) * kk + t) * G + hg) * d_h) + d4);
-    acc.x += v.x;
-    acc.y += v.y;
-    acc.z += v.z;
-    acc.w += v.w;
+    const uint2 v = __ldg(reinterpret_cast<const uint2*>(
+                        part_dq + ((((int64_t)r * N + i) * kk + t) * G + hg) * d_h) + d4);
+    const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.x));
+    const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.y));
+    acc.x += f0.x;
+    acc.y += f0.y;
+    acc.z += f1.x;
+    acc.w += f1.y;
   }
   reinterpret_cast<float4*>(dq + ih * d_h)[d4] =
       make_float4(acc.x * scale, acc.y * scale, acc.z * scale, acc.w * scale);
@@ -512,7 +539,7 @@ BwdWs bwd_layout(int64_t N, int H_q, int H_kv, int d_h, int kk) {
   w.cnt_mat = take(4 * (size_t)w.nb * ordered_bucket_ranges(N));
   w.entries = take(4 * sel);
   w.delta = take(4 * (size_t)H_q * N);
-  w.part_dq = take(4 * sel * G * d_h);
+  w.part_dq = take(2 * sel * G * d_h);
   w.part_dkv = take(4 * pieces * 2 * d_h * 64);
   w.total = off;
   return w;
@@ -540,7 +567,7 @@ cudaError_t launch_sparse_attn_bwd(const void* q, const void* k, const void* v, 
   int* cnt_mat = reinterpret_cast<int*>(base + w.cnt_mat);
   int* entries = reinterpret_cast<int*>(base + w.entries);
   float* delta = reinterpret_cast<float*>(base + w.delta);
-  float* part_dq = reinterpret_cast<float*>(base + w.part_dq);
+  auto* part_dq = reinterpret_cast<__nv_bfloat16*>(base + w.part_dq);
   float* part_dkv = reinterpret_cast<float*>(base + w.part_dkv);
   const auto* qq = static_cast<const __nv_bfloat16*>(q);
   const auto* dd = static_cast<const __nv_bfloat16*>(d_o);
@@ -571,6 +598,11 @@ cudaError_t launch_sparse_attn_bwd(const void* q, const void* k, const void* v, 
   if ((e = make_tma_3d_bf16(&tv, v, (uint64_t)d_h, (uint64_t)H_kv, (uint64_t)N, 64, 1, 64, 128)) !=
       cudaSuccess)
     return e;
+  // the dQ partials as [H_kv * N * k slots, G, d_h]: one box = one selection's G heads x 64 dims
+  CUtensorMap tdq;
+  if ((e = make_tma_3d_bf16(&tdq, part_dq, (uint64_t)d_h, (uint64_t)G, (uint64_t)H_kv * N * kk, 64,
+                            G, 1, 128)) != cudaSuccess)
+    return e;
   int dev = 0, sms = 0;
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
@@ -581,7 +613,7 @@ cudaError_t launch_sparse_attn_bwd(const void* q, const void* k, const void* v, 
   auto run = [&](auto kern, int smem) -> cudaError_t {
     cudaError_t x = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (x != cudaSuccess) return x;
-    kern<<<sms, kThreadsB, smem, st>>>(tq, tdo, tk, tv, args);
+    kern<<<sms, kThreadsB, smem, st>>>(tq, tdo, tk, tv, tdq, args);
     return cudaGetLastError();
   };
   auto dispatch = [&](auto dh) -> cudaError_t {

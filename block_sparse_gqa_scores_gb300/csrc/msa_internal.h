@@ -26,12 +26,10 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
-// Byte offsets of the decode workspace: block scores [S, H_kv, ceil(max_len/64)] fp32,
-// selections [S, H_kv, k] int32, split partials O [S*H_kv*nsplit, G, d_h] and LSE
-// [S*H_kv*nsplit, G] fp32, each 256-byte aligned.
+// Byte offsets of the decode workspace: block scores [S, H_kv, ceil(max_len/64)] fp32 and
+// selections [S, H_kv, k] int32 (when the caller passes no idx_out), each 256-byte aligned.
 struct DecodeWs {
-  size_t off_m, off_idx, off_po, off_pl, total;
-  int nsplit;
+  size_t off_m, off_idx, total;
 };
 DecodeWs decode_layout(int S, int64_t max_len, int H_q, int H_kv, int d_h, int k);
 
@@ -150,15 +148,13 @@ struct CacheMap {
 #endif
 };
 
-cudaError_t launch_select_decode(const float* Mdec, int32_t* idx, const CacheMap& cm, int S,
-                                 int H_kv, int k, int64_t max_len, int64_t nblk_max,
-                                 cudaStream_t stream);
-
-cudaError_t launch_sparse_attn_decode(const void* q, const void* k_cache, const void* v_cache,
-                                      const int32_t* idx, const CacheMap& cm, int S,
-                                      int64_t max_len, int H_q, int H_kv, int d_h, int kk,
-                                      int nsplit, float* part_o, float* part_lse, void* o,
-                                      float* lse, cudaStream_t stream);
+// The decode tail: per (sequence, group), the selection over the block scores Mdec and the
+// attention of the group's heads over the selected blocks, writing o, lse and (if not null)
+// idx_out.
+cudaError_t launch_decode_tail(const void* q, const void* k_cache, const void* v_cache,
+                               const float* Mdec, int64_t nblk_max, const CacheMap& cm, int S,
+                               int64_t max_len, int H_q, int H_kv, int d_h, int kk,
+                               int32_t* idx_out, void* o, float* lse, cudaStream_t stream);
 
 cudaError_t launch_decode_block_scores(const void* q_idx, const void* k_idx_cache,
                                        const CacheMap& cm, float* Mdec, int S, int H_kv, int d_idx,

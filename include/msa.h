@@ -125,8 +125,8 @@ msa_status_t msa_sparse_attn_fwd(const void *q, const void *k, const void *v, co
                                  void *stream);
 
 /* Workspace bytes msa_sparse_attn_bwd needs (0 for invalid sizes): per (group, block) bucket
- * counts and offsets, per selection an entry and a fp32 dQ partial of G*d_h values (the bulk:
- * 4*H_kv*N*k*G*d_h bytes, 34.4 GB at N = 131072, H_q = 32, H_kv = 4, k = 16, d_h = 128), per
+ * counts and offsets, per selection an entry and a bf16 dQ partial of G*d_h values (the bulk:
+ * 2*H_kv*N*k*G*d_h bytes, 17.2 GB at N = 131072, H_q = 32, H_kv = 4, k = 16, d_h = 128), per
  * (row, head) the delta dO . O, and one fp32 dK/dV partial of 2*64*d_h values per piece of at
  * most 64 work tiles of a bucket. */
 size_t msa_sparse_attn_bwd_workspace(int64_t N, int H_q, int H_kv, int d_h, int k);
@@ -144,7 +144,8 @@ size_t msa_sparse_attn_bwd_workspace(int64_t N, int H_q, int H_kv, int d_h, int 
  *   dq         fp32 [N, H_q, d_h];  dk, dv fp32 [N, H_kv, d_h] (written in full; tokens no query
  *              selected get 0)
  *   ws         device workspace of msa_sparse_attn_bwd_workspace() bytes, 16-byte aligned.
- * P and dS enter the tensor-core products as bf16, accumulation is fp32.  Every selection is
+ * P and dS enter the tensor-core products as bf16, each selection's dQ contribution is kept in
+ * bf16 until the merge, accumulation is fp32.  Every selection is
  * bucketed by (group, block) and each bucket cut into pieces of at most 64 work tiles; dq sums a
  * row's partials in slot order and dk/dv a bucket's pieces in piece order, with no atomic update
  * of any result, so the outputs are deterministic.  Errors as msa_sparse_attn_fwd; N > 2^21 or
@@ -180,7 +181,8 @@ msa_status_t msa_prefill_varlen(const void *q, const void *k, const void *v, con
                                 int32_t *idx, void *o, float *lse, void *ws, size_t ws_bytes,
                                 void *stream);
 
-/* Workspace bytes msa_sparse_decode needs (block scores, selections, split partials). */
+/* Workspace bytes msa_sparse_decode needs (block scores, and the selections when idx_out is
+ * NULL). */
 size_t msa_sparse_decode_workspace(int S, int64_t max_len, int H_q, int H_kv, int d_h, int d_idx,
                                    int k);
 
@@ -236,7 +238,7 @@ msa_status_t msa_sparse_decode_paged(const void *q, const void *q_idx, const voi
  * counterpart to this entry point; it changes where the scratch lives, not what is computed.
  *   - Arguments and results are those of msa_sparse_decode without ws/ws_bytes; the caller still
  *     owns and passes every input and output.  Nothing is allocated by the call.
- *   - The temporaries (block scores, selections, split partials) live in a fixed device array of
+ *   - The temporaries (block scores, selections) live in a fixed device array of
  *     MSA_DECODE_NOALLOC_SCRATCH_BYTES inside libmsa.so, held by every GPU that loads the library
  *     until the process exits.  Sizes whose msa_sparse_decode_workspace() exceeds it return
  *     MSA_ERR_WORKSPACE before any launch.

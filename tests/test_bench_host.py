@@ -31,7 +31,7 @@ def test_write_traffic_rows(tmp_path, monkeypatch):
         for _ in range(4):
             launch(n, "k_attn_plan(const int *, long)", 1, 0); n += 1
             launch(n, "void k_attn_kvouter<128>(CUtensorMap_st)", 1000, 1000); n += 1
-        launch(n, "void k_decode_merge<128>(const float *)", 2, 0); n += 1
+        launch(n, "void k_decode_tail<128, 0>(AttnParams)", 2, 0); n += 1
     for _ in range(3):                                      # three loss calls, two gradient calls
         launch(n, "void k_kl_kvouter<128, 8, 0>(KlQMaps)", 19000, 200); n += 1
     for _ in range(2):
