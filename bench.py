@@ -133,19 +133,22 @@ def ncu_traffic(kernel):
     return None
 
 
-def write_traffic(csv_path, command):
-    """profiles/traffic.txt from an ncu CSV of gpu__time_duration.sum, dram__bytes_read.sum and
-    dram__bytes_write.sum over whole bench steps: bytes per step of each row (one call each)."""
+def write_traffic(csv_path, command, scale=1.0, only=None, tag="A"):
+    """Updates profiles/traffic.txt from an ncu CSV of gpu__time_duration.sum,
+    dram__bytes_read.sum and dram__bytes_write.sum over whole bench steps: DRAM bytes per call of
+    each row (one call per step; the KL and backward rows per call of their block-major pass),
+    times `scale` (a capture of a smaller case scaled to the bench workload by the units it
+    processes).  Rows not in `only` keep their previous lines."""
     import csv
     import collections
     rows = list(csv.reader(l for l in open(csv_path) if not l.startswith("==")))
     hdr = rows[0]
     ki, mi, vi, ui = (hdr.index(c) for c in ("Kernel Name", "Metric Name", "Metric Value",
                                               "Metric Unit"))
-    scale = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9}
+    unit = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9}
     tot = collections.defaultdict(float)
-    calls = collections.Counter()      # KL rows: calls counted by their block-major launches
-    steps = 0
+    calls = collections.Counter()      # KL / backward rows: calls counted by their main launch
+    firsts = collections.Counter()     # launches of the first kernel of a step
     for r in rows[1:]:
         raw = r[ki].split("(")[0]
         name = raw.split("<")[0].split("::")[-1].split()[-1]   # bare kernel name
@@ -155,21 +158,42 @@ def write_traffic(csv_path, command):
         if name == "k_kl_kvouter" and raw.replace(" ", "").endswith(",1>"):
             row = "kl_loss_bwd"                  # the gradient instantiation
         if r[mi] == "gpu__time_duration.sum":
-            if name == "k_index_block_scores":   # 1 per step
-                steps += 1
+            firsts[name] += 1
             if name in ("k_kl_kvouter", "k_attn_bwd_kvouter"):
                 calls[row] += 1
         if r[mi] in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
-            tot[row] += float(r[vi].replace(",", "")) * scale[r[ui]]
+            tot[row] += float(r[vi].replace(",", "")) * unit[r[ui]]
+    # one index-branch launch per step (one decode scan when the capture has no prefill)
+    steps = firsts["k_index_block_scores"] or firsts["k_decode_block_scores"]
+    keep, notes = {}, []
+    if os.path.exists(TRAFFIC_FILE):
+        for line in open(TRAFFIC_FILE):
+            if line.startswith("# capture "):
+                notes.append(line.rstrip("\n"))
+            elif line.strip() and not line.startswith("#"):
+                keep[line.split()[0]] = line.rstrip("\n")
+    wrote = []
+    for k in ("index_branch", "main_branch", "decode", "kl_loss_fwd", "kl_loss_bwd",
+              "sparse_attn_bwd"):
+        if k in tot and (only is None or k in only):
+            n = calls[k] if k.startswith("kl_") or k == "sparse_attn_bwd" else steps
+            keep[k] = "%s %d %s %s" % (k, scale * tot[k] / max(n, 1),
+                                       kernel_source_hash(KERNEL_FILES[k]), tag)
+            wrote.append(k)
+    notes = [x for x in notes if not x.startswith("# capture %s:" % tag)]
+    notes.append("# capture %s: %s (rows %s, %d steps, bytes x %g)" % (
+        tag, command, ",".join(wrote), steps, scale))
     with open(TRAFFIC_FILE, "w") as f:
         f.write("# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per call of each bench\n"
-                "# row, averaged over %d whole steps of one ncu capture (1 pass, cold cache):\n"
-                "#   %s\n# row  bytes_per_call  source_sha\n" % (steps, command))
+                "# row, from ncu captures of whole bench steps (one pass, cold cache); a capture of\n"
+                "# a smaller case is scaled to the bench workload by the query rows it processes.\n")
+        for n_ in sorted(notes):
+            f.write(n_ + "\n")
+        f.write("# row  bytes_per_call  source_sha  capture\n")
         for k in ("index_branch", "main_branch", "decode", "kl_loss_fwd", "kl_loss_bwd",
                   "sparse_attn_bwd"):
-            if k in tot:
-                n = calls[k] if k.startswith("kl_") or k == "sparse_attn_bwd" else steps
-                f.write("%s %d %s\n" % (k, tot[k] / max(n, 1), kernel_source_hash(KERNEL_FILES[k])))
+            if k in keep:
+                f.write(keep[k] + "\n")
 
 
 class Clocks:
@@ -288,6 +312,9 @@ def run_msa(args, world, rank, local):
     if args.prefill_n:
         pcfg = gen.PrefillConfig(**{**pcfg.__dict__, "N": args.prefill_n})
     dcfg = None if args.decode == "none" else gen.CONFIGS[args.decode]
+    if dcfg is not None and args.decode_seqs:
+        dcfg = gen.DecodeConfig(**{**dcfg.__dict__, "S": args.decode_seqs})
+    DEFAULT_WORKLOAD = DEFAULT_WORKLOAD and not args.decode_seqs
     msa, x, bufs, d, dbufs = setup(pcfg, dcfg, seed=args.seed + rank)
     stream = torch.cuda.current_stream()
     N = pcfg.N
@@ -789,6 +816,8 @@ def main():
     ap.add_argument("--prefill-n", type=int, default=None,
                     help="override the prefill length (same head layout and structure)")
     ap.add_argument("--decode", default="decode", help="decode workload, or 'none'")
+    ap.add_argument("--decode-seqs", type=int, default=None,
+                    help="override the decode batch size (same length range)")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-e2e", action="store_true")
@@ -806,9 +835,16 @@ def main():
                     help="write profiles/traffic.txt from an ncu CSV of whole steps and exit")
     ap.add_argument("--traffic-command", default="",
                     help="the command the ncu CSV was captured on (recorded in the file)")
+    ap.add_argument("--traffic-scale", type=float, default=1.0,
+                    help="factor from the captured case to the bench workload (query rows)")
+    ap.add_argument("--traffic-rows", default="",
+                    help="comma-separated rows to update (default: every row in the capture)")
+    ap.add_argument("--traffic-tag", default="A", help="capture label recorded per row")
     args = ap.parse_args()
     if args.write_traffic:
-        write_traffic(args.write_traffic, args.traffic_command)
+        write_traffic(args.write_traffic, args.traffic_command, args.traffic_scale,
+                      set(args.traffic_rows.split(",")) if args.traffic_rows else None,
+                      args.traffic_tag)
         return
     if args.warmup < 3 and args.impl == "msa":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)

@@ -47,6 +47,13 @@ def test_write_traffic_rows(tmp_path, monkeypatch):
     assert rows["decode"] == 2_000_000
     assert rows["kl_loss_fwd"] == 19_200_000_000              # per loss call (3 calls)
     assert rows["kl_loss_bwd"] == 22_000_000_000 + 2_100_000_000   # gradient pass + dQ merge
+    # a capture of a smaller case scaled by 4 updates only the rows asked for
+    bench.write_traffic(str(csv), "smaller case", scale=4.0, only={"main_branch"}, tag="B")
+    text = out.read_text()
+    rows2 = {l.split()[0]: l.split() for l in text.splitlines() if l and not l.startswith("#")}
+    assert int(rows2["main_branch"][1]) == 4 * rows["main_branch"] and rows2["main_branch"][3] == "B"
+    assert int(rows2["decode"][1]) == rows["decode"] and rows2["decode"][3] == "A"
+    assert "# capture A: test command" in text and "# capture B: smaller case" in text
 
 
 def test_roofline_row_peaks():
