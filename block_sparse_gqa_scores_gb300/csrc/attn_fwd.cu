@@ -2,7 +2,7 @@
 // launch sequence over query chunks and its workspace.
 //
 // Per chunk of at most 32768 query rows:
-//   plan (count) -> scan -> plan (scatter)   bucket the private selections (attn_tile.cuh) and
+//   plan -> scan -> scatter                  bucket the private selections (attn_tile.cuh) and
 //                                            record each tile's shared blocks
 //   k_attn_kvouter                           block-major tcgen05 pass over private selections
 //   k_attn_shared                            16-query tiles over their shared blocks; its
@@ -32,7 +32,7 @@ constexpr int64_t kChunkRows = 32768;
 constexpr int kKvoCtasPerSm = 1;         // block-major pass: persistent, one CTA per SM (TMEM)
 
 struct AttnWs {
-  size_t count, offset, tile_off, cursor, entries, tile_list, tile_priv, part_o, part_lse,
+  size_t count, offset, tile_off, sc, sc_n, entries, tile_list, tile_priv, part_o, part_lse,
       set_bytes;
   int64_t qc;
   int nb, sets;
@@ -51,9 +51,10 @@ AttnWs attn_layout(int64_t N, int H_q, int H_kv, int d_h, int kk) {
   w.count = take(4 * (size_t)(w.nb + 1));
   w.offset = take(4 * (size_t)(w.nb + 1));
   w.tile_off = take(4 * (size_t)(w.nb + 1));
-  w.cursor = take(4 * (size_t)(w.nb + 1));
   w.entries = take(4 * sel);
   const size_t tiles = (size_t)H_kv * (w.qc / kTileQ);            // 16-query tiles of a chunk
+  w.sc = take(12 * sel);                 // per tile: (bucket, rank, entry) of its private selections
+  w.sc_n = take(4 * tiles);
   w.tile_list = take(4 * tiles * (kMaxShared + 1));
   w.tile_priv = take(8 * tiles * kTileQ);
   w.part_o = take(2 * sel * G * d_h);
@@ -106,7 +107,7 @@ size_t sparse_attn_ws_bytes(int64_t N, int H_q, int H_kv, int d_h, int kk) {
   return w.set_bytes * w.sets;
 }
 
-// The main branch over query chunks: plan (count) -> scan -> plan (scatter) -> block-major pass
+// The main branch over query chunks: plan -> scan -> scatter -> block-major pass
 // over private selections, then the shared-block pass (which also merges), pipelined as above.
 cudaError_t launch_sparse_attn_fwd(const void* q, const void* k, const void* v, const int32_t* idx,
                                    void* o, float* lse, int64_t N, int H_q, int H_kv, int d_h,
@@ -142,7 +143,8 @@ cudaError_t launch_sparse_attn_fwd(const void* q, const void* k, const void* v, 
     int* count = reinterpret_cast<int*>(base + w.count);
     int* offset = reinterpret_cast<int*>(base + w.offset);
     int* tile_off = reinterpret_cast<int*>(base + w.tile_off);
-    int* cursor = reinterpret_cast<int*>(base + w.cursor);
+    int* sc = reinterpret_cast<int*>(base + w.sc);
+    int* sc_n = reinterpret_cast<int*>(base + w.sc_n);
     int* entries = reinterpret_cast<int*>(base + w.entries);
     int* tile_list = reinterpret_cast<int*>(base + w.tile_list);
     auto* tile_priv = reinterpret_cast<unsigned long long*>(base + w.tile_priv);
@@ -152,12 +154,13 @@ cudaError_t launch_sparse_attn_fwd(const void* q, const void* k, const void* v, 
     if (w.sets == 2 && c >= 2 && (e = cudaStreamWaitEvent(side, ev.freed[s], 0)) != cudaSuccess)
       return e;
     if ((e = cudaMemsetAsync(count, 0, 4 * (size_t)w.nb, side)) != cudaSuccess) return e;
-    if ((e = launch_attn_plan(idx, N, H_kv, kk, q0, q1, nblk, 0, count, offset, cursor, entries,
-                              tile_list, tile_priv, side)) != cudaSuccess) return e;
-    if ((e = launch_attn_scan(count, offset, tile_off, cursor, w.nb, 128 / G, side)) != cudaSuccess)
+    if ((e = launch_attn_plan(idx, N, H_kv, kk, q0, q1, nblk, count, tile_list, tile_priv, sc,
+                              sc_n, side)) != cudaSuccess) return e;
+    if ((e = launch_attn_scan(count, offset, tile_off, w.nb, 128 / G, side)) != cudaSuccess)
       return e;
-    if ((e = launch_attn_plan(idx, N, H_kv, kk, q0, q1, nblk, 1, count, offset, cursor, entries,
-                              tile_list, tile_priv, side)) != cudaSuccess) return e;
+    if ((e = launch_attn_scatter(sc, sc_n, offset, entries,
+                                 (int64_t)H_kv * ((q1 - q0 + kTileQ - 1) / kTileQ), kk, side)) != cudaSuccess)
+      return e;
     if ((e = launch_attn_kvouter(q, k, v, entries, offset, tile_off, w.nb, nblk, N, q0, q1, H_q,
                                  H_kv, d_h, kk, kKvoCtasPerSm * sms, part_o, part_lse, side)) != cudaSuccess)
       return e;

@@ -889,7 +889,8 @@ cudaError_t launch_bucket_selections(const int32_t* idx, int64_t N, int H_kv, in
   k_kl_plan<<<pgrid, 32 * kKlPlanWarps, 0, st>>>(idx, N, kk, nblk, 0, count, offset, cursor,
                                                  entries);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  if ((e = launch_attn_scan(count, offset, tile_off, cursor, nb, ept, st)) != cudaSuccess) return e;
+  if ((e = launch_attn_scan(count, offset, tile_off, nb, ept, st)) != cudaSuccess) return e;
+  if ((e = cudaMemsetAsync(cursor, 0, sizeof(int) * (size_t)nb, st)) != cudaSuccess) return e;
   k_kl_plan<<<pgrid, 32 * kKlPlanWarps, 0, st>>>(idx, N, kk, nblk, 1, count, offset, cursor,
                                                  entries);
   return cudaGetLastError();
@@ -913,7 +914,7 @@ cudaError_t launch_bucket_selections_ordered(const int32_t* idx, int64_t N, int 
   const dim3 cgrid((unsigned)((tiles + kKlPlanWarps - 1) / kKlPlanWarps), (unsigned)H_kv);
   k_order_count<<<cgrid, 32 * kKlPlanWarps, 0, st>>>(idx, N, kk, nblk, R, count, cnt_mat);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  if ((e = launch_attn_scan(count, offset, tile_off, cursor, nb, ept, st)) != cudaSuccess) return e;
+  if ((e = launch_attn_scan(count, offset, tile_off, nb, ept, st)) != cudaSuccess) return e;
   k_order_bases<<<(nb + 255) / 256, 256, 0, st>>>(offset, cnt_mat, nb, R);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const dim3 sgrid((unsigned)((R + kKlPlanWarps - 1) / kKlPlanWarps), (unsigned)H_kv);

@@ -58,11 +58,12 @@ cudaError_t launch_attn_shared(const CUtensorMap& tq, const CUtensorMap& tk, con
                                int64_t q1, int H_q, int H_kv, int d_h, int kk, cudaStream_t st);
 
 cudaError_t launch_attn_plan(const int32_t* idx, int64_t N, int H_kv, int kk, int64_t q0,
-                             int64_t q1, int64_t nblk, int pass, int* count, const int* offset,
-                             int* cursor, int* entries, int* tile_list,
-                             unsigned long long* tile_priv, cudaStream_t st);
-cudaError_t launch_attn_scan(const int* count, int* offset, int* tile_off, int* cursor, int nb,
-                             int ept, cudaStream_t st);
+                             int64_t q1, int64_t nblk, int* count, int* tile_list,
+                             unsigned long long* tile_priv, int* sc, int* sc_n, cudaStream_t st);
+cudaError_t launch_attn_scan(const int* count, int* offset, int* tile_off, int nb, int ept,
+                             cudaStream_t st);
+cudaError_t launch_attn_scatter(const int* sc, const int* sc_n, const int* offset, int* entries,
+                                int64_t ntiles, int kk, cudaStream_t st);
 cudaError_t launch_attn_kvouter(const void* q, const void* k, const void* v, const int* entries,
                                 const int* offset, const int* tile_off, int nbuckets, int64_t nblk,
                                 int64_t N, int64_t q0, int64_t q1, int H_q, int H_kv, int d_h,

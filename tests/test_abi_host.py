@@ -154,15 +154,16 @@ def test_workspace_sizes(lib):
     nblk = L // 64
     floor = 4 * S * H_kv * nblk + 4 * S * H_kv * k
     assert floor <= need <= floor + 2 * 256
-    # main branch: per query chunk (<= 32768 rows) the bucket arrays, the entries, each tile's
-    # shared-block list and private-slot masks, and the private partials (bf16 O + fp32 LSE per
-    # selection, at fixed (row, slot) positions)
+    # main branch: per query chunk (<= 32768 rows) the bucket arrays, the entries, the plan's
+    # (bucket, rank, entry) scratch and its per-tile counts, each tile's shared-block list and
+    # private-slot masks, and the private partials (bf16 O + fp32 LSE per selection, at fixed
+    # (row, slot) positions)
     need = lib.msa_sparse_attn_fwd_workspace(i64(1024), 8, 2, 64, 4)
     sel = 2 * 1024 * 4
     tiles = 2 * 1024 // 16                       # 16-query tiles: shared-block lists, masks
-    floor = (4 * sel + sel * 4 * (64 * 2 + 4) + 4 * 4 * (2 * 16 + 1) + 4 * tiles * (512 + 1) +
-             8 * tiles * 16)
-    assert floor <= need <= floor + 8 * 256
+    floor = (4 * sel + 12 * sel + 4 * tiles + sel * 4 * (64 * 2 + 4) + 3 * 4 * (2 * 16 + 1) +
+             4 * tiles * (512 + 1) + 8 * tiles * 16)
+    assert floor <= need <= floor + 10 * 256
     assert attn(lib, N=1024, H_q=8, H_kv=2, d_h=64, kk=4, wsb=need - 1) == WORKSPACE
 
 
