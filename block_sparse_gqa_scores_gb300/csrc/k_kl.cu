@@ -123,21 +123,38 @@ __device__ __forceinline__ void kl_plan_tile(const int32_t* __restrict__ idx, in
   }
 }
 
+// The planning kernels are instantiated per keys-per-lane EPL (32 EPL >= 16 k), so their
+// registers and shared memory fit the k in use.
+template <int EPL>
 __global__ void __launch_bounds__(32 * kKlPlanWarps)
     k_kl_plan(const int32_t* __restrict__ idx, int64_t N, int kk, int64_t nblk, int pass,
               int* count, const int* offset, int* cursor, int* entries) {
-  __shared__ int s_U[kKlPlanWarps][kMaxKeys];
-  __shared__ unsigned s_mask[kKlPlanWarps][kMaxKeys];
+  __shared__ int s_U[kKlPlanWarps][32 * EPL];
+  __shared__ unsigned s_mask[kKlPlanWarps][32 * EPL];
   const int warp = threadIdx.x >> 5;
   const int r = blockIdx.y;
   const int64_t i0 = ((int64_t)blockIdx.x * kKlPlanWarps + warp) * kTileQ;
   if (i0 >= N) return;
-  with_epl(kk, [&](auto e) {
-    kl_plan_tile<decltype(e)::value>(idx, r, i0, N, kk, nblk, pass, s_U[warp], s_mask[warp],
-                                     count, offset, cursor, entries);
-    return 0;
-  });
+  kl_plan_tile<EPL>(idx, r, i0, N, kk, nblk, pass, s_U[warp], s_mask[warp], count, offset,
+                    cursor, entries);
 }
+
+// Launches kern<EPL> for the EPL that k needs.
+template <template <int> class K, typename... A>
+cudaError_t launch_epl(int kk, dim3 grid, dim3 block, cudaStream_t st, A... args) {
+  if (kk <= 2) K<1>::launch(grid, block, st, args...);
+  else if (kk <= 4) K<2>::launch(grid, block, st, args...);
+  else if (kk <= 8) K<4>::launch(grid, block, st, args...);
+  else if (kk <= 16) K<8>::launch(grid, block, st, args...);
+  else if (kk <= 32) K<16>::launch(grid, block, st, args...);
+  else K<32>::launch(grid, block, st, args...);
+  return cudaGetLastError();
+}
+template <int EPL>
+struct KlPlanK {
+  template <typename... A>
+  static void launch(dim3 g, dim3 b, cudaStream_t st, A... a) { k_kl_plan<EPL><<<g, b, 0, st>>>(a...); }
+};
 
 // ------------------------------------------------- row-ordered bucketing --
 // The same buckets with every bucket's selections in row order, whatever order the hardware
@@ -162,22 +179,25 @@ __device__ __forceinline__ void order_count_tile(const int32_t* __restrict__ idx
   }
 }
 
+template <int EPL>
 __global__ void __launch_bounds__(32 * kKlPlanWarps)
     k_order_count(const int32_t* __restrict__ idx, int64_t N, int kk, int64_t nblk, int R,
                   int* count, int* cnt_mat) {
-  __shared__ int s_U[kKlPlanWarps][kMaxKeys];
-  __shared__ unsigned s_mask[kKlPlanWarps][kMaxKeys];
+  __shared__ int s_U[kKlPlanWarps][32 * EPL];
+  __shared__ unsigned s_mask[kKlPlanWarps][32 * EPL];
   const int warp = threadIdx.x >> 5;
   const int r = blockIdx.y;
   const int64_t t = (int64_t)blockIdx.x * kKlPlanWarps + warp;
   const int64_t i0 = t * kTileQ;
   if (i0 >= N) return;
-  with_epl(kk, [&](auto e) {
-    order_count_tile<decltype(e)::value>(idx, r, i0, N, kk, nblk, R, (int)(t / kRangeTiles),
-                                         s_U[warp], s_mask[warp], count, cnt_mat);
-    return 0;
-  });
+  order_count_tile<EPL>(idx, r, i0, N, kk, nblk, R, (int)(t / kRangeTiles), s_U[warp],
+                        s_mask[warp], count, cnt_mat);
 }
+template <int EPL>
+struct OrderCountK {
+  template <typename... A>
+  static void launch(dim3 g, dim3 b, cudaStream_t st, A... a) { k_order_count<EPL><<<g, b, 0, st>>>(a...); }
+};
 
 // cnt_mat[b][range] := offset[b] + sum of the bucket's counts in earlier ranges
 __global__ void __launch_bounds__(256)
@@ -225,21 +245,24 @@ __device__ __forceinline__ void order_scatter_range(const int32_t* __restrict__ 
   }
 }
 
+template <int EPL>
 __global__ void __launch_bounds__(32 * kKlPlanWarps)
     k_order_scatter(const int32_t* __restrict__ idx, int64_t N, int kk, int64_t nblk, int R,
                     int* cnt_mat, int* entries) {
-  __shared__ int s_U[kKlPlanWarps][kMaxKeys];
-  __shared__ unsigned s_mask[kKlPlanWarps][kMaxKeys];
+  __shared__ int s_U[kKlPlanWarps][32 * EPL];
+  __shared__ unsigned s_mask[kKlPlanWarps][32 * EPL];
   const int warp = threadIdx.x >> 5;
   const int r = blockIdx.y;
   const int range = blockIdx.x * kKlPlanWarps + warp;
   if (range >= R) return;
-  with_epl(kk, [&](auto e) {
-    order_scatter_range<decltype(e)::value>(idx, r, range, N, kk, nblk, R, s_U[warp],
-                                            s_mask[warp], cnt_mat, entries);
-    return 0;
-  });
+  order_scatter_range<EPL>(idx, r, range, N, kk, nblk, R, s_U[warp], s_mask[warp], cnt_mat,
+                           entries);
 }
+template <int EPL>
+struct OrderScatterK {
+  template <typename... A>
+  static void launch(dim3 g, dim3 b, cudaStream_t st, A... a) { k_order_scatter<EPL><<<g, b, 0, st>>>(a...); }
+};
 
 // ------------------------------------------------------- block-major partials --
 // Reduce-scatter over the G lanes of an entry (lanes e*G .. e*G+G-1 of one warp, h = lane's
@@ -886,14 +909,13 @@ cudaError_t launch_bucket_selections(const int32_t* idx, int64_t N, int H_kv, in
   if (e != cudaSuccess) return e;
   const int64_t tiles = (N + kTileQ - 1) / kTileQ;
   const dim3 pgrid((unsigned)((tiles + kKlPlanWarps - 1) / kKlPlanWarps), (unsigned)H_kv);
-  k_kl_plan<<<pgrid, 32 * kKlPlanWarps, 0, st>>>(idx, N, kk, nblk, 0, count, offset, cursor,
-                                                 entries);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if ((e = launch_epl<KlPlanK>(kk, pgrid, dim3(32 * kKlPlanWarps), st, idx, N, kk, nblk, 0, count,
+                               (const int*)offset, cursor, entries)) != cudaSuccess)
+    return e;
   if ((e = launch_attn_scan(count, offset, tile_off, nb, ept, st)) != cudaSuccess) return e;
   if ((e = cudaMemsetAsync(cursor, 0, sizeof(int) * (size_t)nb, st)) != cudaSuccess) return e;
-  k_kl_plan<<<pgrid, 32 * kKlPlanWarps, 0, st>>>(idx, N, kk, nblk, 1, count, offset, cursor,
-                                                 entries);
-  return cudaGetLastError();
+  return launch_epl<KlPlanK>(kk, pgrid, dim3(32 * kKlPlanWarps), st, idx, N, kk, nblk, 1, count,
+                             (const int*)offset, cursor, entries);
 }
 
 int ordered_bucket_ranges(int64_t N) {
@@ -912,14 +934,15 @@ cudaError_t launch_bucket_selections_ordered(const int32_t* idx, int64_t N, int 
   if ((e = cudaMemsetAsync(cnt_mat, 0, sizeof(int) * (size_t)nb * R, st)) != cudaSuccess) return e;
   const int64_t tiles = (N + kTileQ - 1) / kTileQ;
   const dim3 cgrid((unsigned)((tiles + kKlPlanWarps - 1) / kKlPlanWarps), (unsigned)H_kv);
-  k_order_count<<<cgrid, 32 * kKlPlanWarps, 0, st>>>(idx, N, kk, nblk, R, count, cnt_mat);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if ((e = launch_epl<OrderCountK>(kk, cgrid, dim3(32 * kKlPlanWarps), st, idx, N, kk, nblk, R,
+                                   count, cnt_mat)) != cudaSuccess)
+    return e;
   if ((e = launch_attn_scan(count, offset, tile_off, nb, ept, st)) != cudaSuccess) return e;
   k_order_bases<<<(nb + 255) / 256, 256, 0, st>>>(offset, cnt_mat, nb, R);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const dim3 sgrid((unsigned)((R + kKlPlanWarps - 1) / kKlPlanWarps), (unsigned)H_kv);
-  k_order_scatter<<<sgrid, 32 * kKlPlanWarps, 0, st>>>(idx, N, kk, nblk, R, cnt_mat, entries);
-  return cudaGetLastError();
+  return launch_epl<OrderScatterK>(kk, sgrid, dim3(32 * kKlPlanWarps), st, idx, N, kk, nblk, R,
+                                   cnt_mat, entries);
 }
 
 size_t kl_ws_bytes(int64_t N, int H_kv, int kk) {
