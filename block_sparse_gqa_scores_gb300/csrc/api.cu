@@ -380,7 +380,7 @@ MSA_API msa_status_t msa_kl_loss_bwd(const void* q, const void* k, const void* q
   if (N < 1 || H_q < 1 || H_kv < 1 || H_q % H_kv != 0 || d_h < 1 || d_idx < 1 ||
       block_size != 64 || k_blocks < 1 || k_blocks > 64)
     return MSA_ERR_INVALID_ARGUMENT;
-  if (!pow2_upto(H_kv, 8) || H_q / H_kv != 8 || (d_h != 64 && d_h != 128) ||
+  if (!pow2_upto(H_kv, 8) || !pow2_upto(H_q / H_kv, 8) || (d_h != 64 && d_h != 128) ||
       (d_idx != 32 && d_idx != 64))
     return MSA_ERR_UNSUPPORTED;
   if (N > ((int64_t)1 << 21) || N * H_kv * k_blocks >= kMaxRows) return MSA_ERR_UNSUPPORTED;

@@ -47,14 +47,17 @@ constexpr float kLog2e = 1.442695040888963407f;
 // tile's student scores transposed to (entry, token).  TMEM holds kTStages accumulator stages:
 // S (128 rows x 64 tokens) and the student scores (64 tokens on the lanes x the tile's entries).
 constexpr int kSiStride = 68;
-template <int D_H, int G>
+template <int D_H, int G, bool BWD = false>
 struct KlSmem {
   static constexpr int kEpt = kKlRows / G;        // entries per work tile
   static constexpr int kHalves = D_H / 64;
   static constexpr int kQHalf = kKlRows * 128;    // 128 rows x 64 dims, bf16, SW128
   static constexpr int kKHalf = 64 * 128;         // 64 keys x 64 dims
   static constexpr int kQiBytes = kEpt * 128 < 1024 ? 1024 : kEpt * 128;
-  static constexpr int kQStages = G == 8 ? 4 : (G == 4 ? 3 : 2);
+  // (the gradient pass at G = 1, d_h = 128 keeps one query stage: two do not fit with its
+  // per-group index-query copies)
+  static constexpr int kQStages =
+      G == 8 ? 4 : (G == 4 ? 3 : (BWD && G == 1 && D_H == 128 ? 1 : 2));
   static constexpr int kKStages = 2;
   static constexpr int kTCols = 64 + kEpt <= 128 ? 128 : 256;
   static constexpr int kTStages = 512 / kTCols;
@@ -70,7 +73,7 @@ struct KlSmem {
   static constexpr int kSiBytes = kEpt * kSiStride * 4;
   // gradient pass, per epilogue group: the tile's index queries (one 128-byte row per entry)
   static constexpr int kOffQg = kOffSi + 2 * kSiBytes;
-  static constexpr int kQgBytes = G == 8 ? kEpt * 128 : 0;   // the gradient pass is G = 8 only
+  static constexpr int kQgBytes = BWD ? kEpt * 128 : 0;
   static constexpr int kOffBar = kOffQg + 2 * kQgBytes;
   static constexpr int kNumBars = 2 * kQStages + 2 * kKStages + 2 * kTStages;
   static constexpr int kOffMisc = kOffBar + 8 * kNumBars;
@@ -343,8 +346,16 @@ struct KlGrad {
   const float* lse_idx;     // [H_kv, N], natural log
   const float* psum;        // [H_kv, N]
   float* part_dq;           // [H_kv, N, k, d_idx]
-  float* dk_idx;            // [N, d_idx], zeroed before the pass
+  float* part_dk;           // [(buckets + CTAs) * 2, 64, d_idx]: see kl_dk_slot
 };
+
+// Slot of the dK_idx partial that epilogue group `grp` of CTA `cta` writes for bucket `bkt`.
+// The CTAs take contiguous ranges of the bucket-ordered work tiles, so a bucket's CTAs are
+// consecutive and bkt + cta is unique over the (CTA, bucket) pairs that occur.
+__host__ __device__ __forceinline__ int64_t kl_dk_slot(int bkt, int cta, int grp) {
+  return ((int64_t)bkt + cta) * 2 + grp;
+}
+constexpr int kKlMaxGrid = 1024;          // CTAs of the block-major pass at most (workspace bound)
 
 template <int D_H, int G, bool BWD>
 __global__ void __launch_bounds__(KlWarps<BWD>::kThreads, 1)
@@ -356,7 +367,7 @@ __global__ void __launch_bounds__(KlWarps<BWD>::kThreads, 1)
                  int H_kv, int d_idx, int kk, float4* __restrict__ part, float scale_log2,
                  float idx_scale, const KlGrad gr) {
   constexpr int kKlQWarps = KlWarps<BWD>::kQ;
-  using L = KlSmem<D_H, G>;
+  using L = KlSmem<D_H, G, BWD>;
   constexpr int kEpt = L::kEpt;
   constexpr int kQStages = L::kQStages, kKStages = L::kKStages, kTStages = L::kTStages;
   constexpr int kCpl = 64 / G;               // columns a lane owns after the reduce-scatter
@@ -638,7 +649,8 @@ __global__ void __launch_bounds__(KlWarps<BWD>::kThreads, 1)
       }
     }
     // gradient pass: key-gradient accumulators of this thread's (token, dims) of the current
-    // bucket's block, flushed to dK_idx with fp32 atomics when the group's bucket changes
+    // bucket's block, written to the group's partial slot of the bucket when the group moves
+    // to another bucket (no atomics: k_kl_dk_merge sums the slots in a fixed order)
     float dkacc[BWD ? 32 : 1];
 #pragma unroll
     for (int d = 0; d < (BWD ? 32 : 1); ++d) dkacc[d] = 0.f;
@@ -658,12 +670,17 @@ __global__ void __launch_bounds__(KlWarps<BWD>::kThreads, 1)
       }
       const int t = j % kTStages;
       if constexpr (BWD) {
-        // this tile's index queries -> s_qg[entry] (thread R copies 16 bytes of row R / 8; G = 8,
-        // so R / 8 is this thread's own entry), landing under the MMA wait and the loss part
-        const int qc = R & 7;
-        if (rv && qc < (d_idx >> 3))
-          kl_cp_async16(s_qg + (R >> 3) * 128 + qc * 16,
-                        q_idx + ((int64_t)(cur_ent >> 6) * H_kv + r) * d_idx + qc * 8);
+        // this tile's index queries -> s_qg[entry], 16 bytes per (entry, chunk) item, landing
+        // under the MMA wait and the loss part (at G = 8 item R is a chunk of this thread's own
+        // entry R / 8)
+        for (int item = R; item < kEpt * 8; item += kKlRows) {
+          const int eq = item >> 3, qc = item & 7;
+          if (eq < c_ne && qc < (d_idx >> 3)) {
+            const int eg = G == 8 ? cur_ent : __ldg(entries + c_e0 + eq);
+            kl_cp_async16(s_qg + eq * 128 + qc * 16,
+                          q_idx + ((int64_t)(eg >> 6) * H_kv + r) * d_idx + qc * 8);
+          }
+        }
         asm volatile("cp.async.commit_group;" ::: "memory");
       }
       const bool okw = *s_abort == 0 && mbar_wait(t_full(t), (j / kTStages) & 1, &g_kl_status);
@@ -767,9 +784,10 @@ __global__ void __launch_bounds__(KlWarps<BWD>::kThreads, 1)
         asm volatile("cp.async.wait_all;" ::: "memory");   // this thread's index-query copy
         kl_group_sync(1 + grp);                            // dS and the index queries are complete
         const int64_t tok0 = b * kBlock;
-        // dQ_idx of entry R / 8, dims (R % 8) * d_idx / 8 ..: sum over the block's tokens
-        {
-          const int eq = R >> 3, nd = d_idx >> 3, d0 = (R & 7) * nd;
+        // dQ_idx of (entry, dims chunk) items: entry item / 8, dims (item % 8) * d_idx / 8 ..,
+        // summed over the block's tokens
+        for (int item = R; item < kEpt * 8; item += kKlRows) {
+          const int eq = item >> 3, nd = d_idx >> 3, d0 = (item & 7) * nd;
           if (eq < c_ne) {
             float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
             // tokens past the sequence have dS = 0; their loads read the last row instead
@@ -824,14 +842,13 @@ __global__ void __launch_bounds__(KlWarps<BWD>::kThreads, 1)
             }
           }
           kl_group_sync(1 + grp);                          // s_si may be overwritten
-          const bool flush = !has_next || (int64_t)(n_bkt % nblk) != b;
+          const bool flush = !has_next || n_bkt != c_bkt;
           if (flush) {
-            if (tok0 + ck < N) {
-              float* dst = gr.dk_idx + (tok0 + ck) * d_idx + d0;
+            float4* dst = reinterpret_cast<float4*>(
+                gr.part_dk + (kl_dk_slot(c_bkt, blockIdx.x, grp) * kBlock + ck) * d_idx + d0);
 #pragma unroll
-              for (int d = 0; d < 32; ++d)
-                if (d < nd) atomicAdd(dst + d, dkacc[d]);
-            }
+            for (int d = 0; d < 32; d += 4)
+              if (d < nd) dst[d / 4] = make_float4(dkacc[d], dkacc[d + 1], dkacc[d + 2], dkacc[d + 3]);
 #pragma unroll
             for (int d = 0; d < 32; ++d) dkacc[d] = 0.f;
           }
@@ -896,6 +913,38 @@ __global__ void __launch_bounds__(256)
   dq_idx[(i * H_kv + r) * d_idx + d] = acc;
 }
 
+// dK_idx[j, d] = sum over the groups r, then the CTAs that processed bucket (r, floor(j/64)) in
+// CTA order, then their two epilogue groups, of the slots' partials: a fixed order, so the
+// result does not depend on the hardware's schedule.  `grid` and the tile ranges are those of
+// the block-major pass.
+__global__ void __launch_bounds__(256)
+    k_kl_dk_merge(const int* __restrict__ tile_off, const float* __restrict__ part_dk,
+                  float* dk_idx, int64_t N, int64_t nblk, int H_kv, int d_idx, int grid) {
+  const int64_t x = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (x >= N * d_idx) return;
+  const int64_t j = x / d_idx;
+  const int d = (int)(x - j * d_idx);
+  const int64_t b = j >> 6;
+  const int c = (int)(j & 63);
+  const int total = __ldg(tile_off + H_kv * nblk);
+  const int per = (total + grid - 1) / grid;
+  float acc = 0.f;
+  for (int r = 0; r < H_kv; ++r) {
+    const int bkt = (int)(r * nblk + b);
+    const int t0 = __ldg(tile_off + bkt), t1 = __ldg(tile_off + bkt + 1);
+    if (t0 == t1) continue;
+    for (int cta = t0 / per; cta <= (t1 - 1) / per; ++cta) {
+      const int tb = cta * per;
+      const int lo = max(t0, tb) - tb, hi = min(t1, tb + per) - tb;   // local tiles [lo, hi)
+#pragma unroll
+      for (int g = 0; g < 2; ++g)
+        if (hi - lo >= 2 || (lo & 1) == g)
+          acc += __ldg(part_dk + (kl_dk_slot(bkt, cta, g) * kBlock + c) * d_idx + d);
+    }
+  }
+  dk_idx[x] = acc;
+}
+
 }  // namespace
 
 // Every selection of idx bucketed by (group, block): count -> scan -> scatter, with each bucket's
@@ -954,7 +1003,10 @@ size_t kl_ws_bytes(int64_t N, int H_kv, int kk) {
 
 size_t kl_bwd_ws_bytes(int64_t N, int H_kv, int d_idx, int kk) {
   auto a256 = [](size_t x) { return (x + 255) & ~size_t(255); };
-  return kl_ws_bytes(N, H_kv, kk) + a256(4 * (size_t)H_kv * N * kk * d_idx);
+  const int64_t nb = (int64_t)H_kv * ((N + kBlock - 1) / kBlock);
+  return kl_ws_bytes(N, H_kv, kk) + a256(4 * (size_t)H_kv * N * kk * d_idx) +
+         a256(4 * (size_t)kl_dk_slot((int)nb, kKlMaxGrid, 0) * kBlock * d_idx) +
+         a256(4 * (size_t)nb * ordered_bucket_ranges(N));
 }
 
 namespace {
@@ -962,8 +1014,8 @@ namespace {
 // Plan (bucket every selection by (group, block)), then the block-major pass, forward or gradient.
 cudaError_t kl_pass(bool bwd, const void* q, const void* k, const void* q_idx, const void* k_idx,
                     const int32_t* idx, const float* lse, int64_t N, int H_q, int H_kv, int d_h,
-                    int d_idx, int kk, void* ws, const KlGrad& gr, float4** part_out,
-                    cudaStream_t st) {
+                    int d_idx, int kk, void* ws, const KlGrad& gr, int* cnt_mat,
+                    float4** part_out, int* grid_out, cudaStream_t st) {
   const int G = H_q / H_kv;
   const int64_t nblk = (N + kBlock - 1) / kBlock;
   const int nb = (int)(H_kv * nblk);
@@ -978,8 +1030,13 @@ cudaError_t kl_pass(bool bwd, const void* q, const void* k, const void* q_idx, c
   float4* part = reinterpret_cast<float4*>(base + 4 * a256(4 * (size_t)(nb + 1)) + a256(4 * sel));
   *part_out = part;
 
-  cudaError_t e = launch_bucket_selections(idx, N, H_kv, kk, kKlRows / G, count, offset,
-                                           tile_off, cursor, entries, st);
+  // the gradient pass sums dK_idx over a bucket's work tiles: it takes the buckets in row order,
+  // so that the tiles, and with them the sums, are the same on every call
+  cudaError_t e =
+      bwd ? launch_bucket_selections_ordered(idx, N, H_kv, kk, kKlRows / G, count, offset,
+                                             tile_off, cursor, cnt_mat, entries, st)
+          : launch_bucket_selections(idx, N, H_kv, kk, kKlRows / G, count, offset, tile_off,
+                                     cursor, entries, st);
   if (e != cudaSuccess) return e;
 
   KlQMaps tq;
@@ -998,18 +1055,26 @@ cudaError_t kl_pass(bool bwd, const void* q, const void* k, const void* q_idx, c
   const auto* kp = static_cast<const __nv_bfloat16*>(k);
   const auto* qi = static_cast<const __nv_bfloat16*>(q_idx);
   const auto* ki = static_cast<const __nv_bfloat16*>(k_idx);
+  const int grid = sms < kKlMaxGrid ? sms : kKlMaxGrid;    // persistent: one CTA per SM
+  if (grid_out) *grid_out = grid;
   auto run = [&](auto kern, int smem, int threads) -> cudaError_t {
     cudaError_t x = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (x != cudaSuccess) return x;
-    const int grid = sms;                                  // persistent: one CTA per SM
     kern<<<grid, threads, smem, st>>>(tq, qq, kp, qi, ki, lse, entries, offset, tile_off, nb,
                                       nblk, N, H_kv, d_idx, kk, part, scale_log2, idx_scale, gr);
     return cudaGetLastError();
   };
   auto dispatch = [&](auto dh) -> cudaError_t {
     constexpr int D = decltype(dh)::value;
-    if (bwd)   // the gradient pass exists for G = 8 (checked by the caller)
-      return run(k_kl_kvouter<D, 8, true>, KlSmem<D, 8>::kAlloc, KlWarps<true>::kThreads);
+    if (bwd) {
+      constexpr int TB = KlWarps<true>::kThreads;
+      switch (G) {
+        case 1: return run(k_kl_kvouter<D, 1, true>, KlSmem<D, 1, true>::kAlloc, TB);
+        case 2: return run(k_kl_kvouter<D, 2, true>, KlSmem<D, 2, true>::kAlloc, TB);
+        case 4: return run(k_kl_kvouter<D, 4, true>, KlSmem<D, 4, true>::kAlloc, TB);
+        default: return run(k_kl_kvouter<D, 8, true>, KlSmem<D, 8, true>::kAlloc, TB);
+      }
+    }
     constexpr int T = KlWarps<false>::kThreads;
     switch (G) {
       case 1: return run(k_kl_kvouter<D, 1, false>, KlSmem<D, 1>::kAlloc, T);
@@ -1030,7 +1095,7 @@ cudaError_t launch_kl_loss_fwd(const void* q, const void* k, const void* q_idx, 
                                int kk, void* ws, cudaStream_t st) {
   float4* part = nullptr;
   cudaError_t e = kl_pass(false, q, k, q_idx, k_idx, idx, lse, N, H_q, H_kv, d_h, d_idx, kk, ws,
-                          KlGrad{}, &part, st);
+                          KlGrad{}, nullptr, &part, nullptr, st);
   if (e != cudaSuccess) return e;
   const int64_t n = (int64_t)H_kv * N;
   k_kl_merge<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(idx, part, kl, lse_idx, psum, N, H_kv,
@@ -1043,16 +1108,30 @@ cudaError_t launch_kl_loss_bwd(const void* q, const void* k, const void* q_idx, 
                                const float* psum, const float* grad_kl, float* dq_idx,
                                float* dk_idx, int64_t N, int H_q, int H_kv, int d_h, int d_idx,
                                int kk, void* ws, cudaStream_t st) {
-  float* part_dq = reinterpret_cast<float*>(static_cast<char*>(ws) + kl_ws_bytes(N, H_kv, kk));
-  cudaError_t e = cudaMemsetAsync(dk_idx, 0, sizeof(float) * (size_t)N * d_idx, st);
-  if (e != cudaSuccess) return e;
-  const KlGrad gr{grad_kl, lse_idx, psum, part_dq, dk_idx};
+  auto a256 = [](size_t x) { return (x + 255) & ~size_t(255); };
+  char* base = static_cast<char*>(ws) + kl_ws_bytes(N, H_kv, kk);
+  float* part_dq = reinterpret_cast<float*>(base);
+  const size_t dq_bytes = a256(4 * (size_t)H_kv * N * kk * d_idx);
+  float* part_dk = reinterpret_cast<float*>(base + dq_bytes);
+  const int64_t nb = (int64_t)H_kv * ((N + kBlock - 1) / kBlock);
+  int* cnt_mat = reinterpret_cast<int*>(
+      base + dq_bytes + a256(4 * (size_t)kl_dk_slot((int)nb, kKlMaxGrid, 0) * kBlock * d_idx));
+  const KlGrad gr{grad_kl, lse_idx, psum, part_dq, part_dk};
   float4* part = nullptr;
-  e = kl_pass(true, q, k, q_idx, k_idx, idx, lse, N, H_q, H_kv, d_h, d_idx, kk, ws, gr, &part, st);
+  int grid = 0;
+  cudaError_t e = kl_pass(true, q, k, q_idx, k_idx, idx, lse, N, H_q, H_kv, d_h, d_idx, kk, ws, gr,
+                          cnt_mat, &part, &grid, st);
   if (e != cudaSuccess) return e;
   const int64_t n = (int64_t)H_kv * N * d_idx;
   k_kl_dq_merge<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(idx, part_dq, dq_idx, N, H_kv, kk,
                                                              d_idx);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  const int64_t nblk = (N + kBlock - 1) / kBlock;
+  const int* tile_off = reinterpret_cast<const int*>(static_cast<char*>(ws) +
+                                                     2 * a256(4 * (size_t)(H_kv * nblk + 1)));
+  const int64_t nk = N * d_idx;
+  k_kl_dk_merge<<<(unsigned)((nk + 255) / 256), 256, 0, st>>>(tile_off, part_dk, dk_idx, N, nblk,
+                                                              H_kv, d_idx, grid);
   return cudaGetLastError();
 }
 

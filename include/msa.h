@@ -288,7 +288,9 @@ msa_status_t msa_kl_loss_fwd(const void *q, const void *k, const void *q_idx, co
                              void *stream);
 
 /* Workspace bytes msa_kl_loss_bwd needs: that of msa_kl_loss_fwd plus one d_idx-float partial of
- * dQ_idx per selection (2.15 GB at N = 131072, H_kv = 4, k = 16, d_idx = 64). */
+ * dQ_idx per selection, 64 x d_idx floats of dK_idx partial per (bucket, CTA, epilogue group)
+ * slot for 2 (H_kv * ceil(N/64) + 1024) slots, and the row-ordered bucketing's counters (one
+ * int per bucket and range of 1024 rows): 2.62 GB at N = 131072, H_kv = 4, k = 16, d_idx = 64. */
 size_t msa_kl_loss_bwd_workspace(int64_t N, int H_kv, int d_idx, int k);
 
 /* Gradient of the KL alignment loss with respect to the index branch (part of the training
@@ -301,9 +303,10 @@ size_t msa_kl_loss_bwd_workspace(int64_t N, int H_kv, int d_idx, int k);
  *   grad_kl         fp32 [H_kv, N]  the upstream gradient of each row's loss
  *   dq_idx          fp32 [N, H_kv, d_idx] (written);  dk_idx fp32 [N, d_idx] (written)
  *   other arguments as msa_kl_loss_fwd; ws of msa_kl_loss_bwd_workspace() bytes.
- * dq_idx sums its row's selections in slot order; dk_idx is accumulated with fp32 atomic adds,
- * so its last bits depend on the order blocks are processed in.  G = H_q/H_kv must be 8
- * (otherwise MSA_ERR_UNSUPPORTED). */
+ * dq_idx sums its row's selections in slot order; dk_idx sums, per token, one partial per
+ * (group, CTA of the block-major pass, epilogue group) in that order, with no atomic update of
+ * any result, so repeated calls on one device give identical bits.  G = H_q/H_kv in
+ * {1, 2, 4, 8} (otherwise MSA_ERR_UNSUPPORTED). */
 msa_status_t msa_kl_loss_bwd(const void *q, const void *k, const void *q_idx, const void *k_idx,
                              const int32_t *idx, const float *lse, const float *lse_idx,
                              const float *p_sum, const float *grad_kl, float *dq_idx,

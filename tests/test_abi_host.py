@@ -253,7 +253,7 @@ def test_kl_bwd_invalid(lib, kw):
 
 
 def test_kl_bwd_unsupported_and_workspace(lib):
-    assert klb(lib, H_q=16) == UNSUPPORTED          # G = 4: the gradient pass is built for G = 8
+    assert klb(lib, H_q=48) == UNSUPPORTED          # G = 12: the pass is built for G in {1,2,4,8}
     assert klb(lib, d_idx=48) == UNSUPPORTED
     lib.msa_kl_loss_bwd_workspace.restype = ctypes.c_size_t
     lib.msa_kl_loss_fwd_workspace.restype = ctypes.c_size_t

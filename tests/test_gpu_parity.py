@@ -313,14 +313,22 @@ def test_kl_loss_uniform_teacher():
 
 KLB_CASES = [("p32k", {}, 1000, 16), ("p32k", {}, 65, 16), ("p32k", {}, 3000, 16),
              ("p32k", {}, 2500, 64), ("p32k", dict(d_idx=32), 900, 16),
-             ("p32k", dict(d_h=64), 900, 16), ("p32k", dict(H_q=8, H_kv=1), 700, 5)]
+             ("p32k", dict(d_h=64), 900, 16), ("p32k", dict(H_q=8, H_kv=1), 700, 5),
+             # G = 1, 2, 4 (more entries per work tile), at both head sizes
+             ("p32k", dict(H_q=4, H_kv=4), 700, 8), ("p32k", dict(H_q=8, H_kv=4), 1500, 16),
+             ("p32k", dict(H_q=16, H_kv=4), 2000, 16), ("tiny", {}, 1024, 4),
+             ("p32k", dict(H_q=4, H_kv=4, d_h=64), 900, 16),
+             ("p32k", dict(H_q=8, H_kv=4, d_h=64, d_idx=32), 700, 8),
+             ("tiny", dict(d_h=128), 1000, 64)]
 
 
 @pytest.mark.parametrize("name,over,N,k", KLB_CASES)
 def test_kl_loss_grad(name, over, N, k):
     """dQ_idx and dK_idx of sum(g * KL) against the oracle's fp64 gradient on the GPU's own
     selection.  Bound: the same fp32 error sources as the loss (about 1e-5 relative in each
-    probability), plus fp32 atomic accumulation in dK_idx: 1e-3 of the largest magnitude."""
+    probability), plus the fp32 sums over every selecting row in dK_idx: 1e-3 of the largest
+    magnitude.  Both are combined in a fixed order (no atomics), so a second call gives the
+    same bits."""
     cfg = cfg_of(name, k=k, **over)
     x, b = fresh(cfg, N, seed=41)
     idx = gpu_index(x, cfg, N)
@@ -342,6 +350,10 @@ def test_kl_loss_grad(name, over, N, k):
             float(np.abs(got - want).max())
     assert np.abs(lse_idx.cpu().numpy() - ref["lse_idx"]).max() <= 1e-3
     assert np.abs(psum.cpu().numpy() - ref["psum"]).max() <= 1e-4
+    dq2, dk2 = msa.msa_kl_loss_bwd(x["q"], x["k"], x["q_idx"], x["k_idx"], idx, lse, lse_idx, psum,
+                                   g)
+    sync_ok()
+    assert torch.equal(dq, dq2) and torch.equal(dk, dk2)
 
 
 # ------------------------------------------------------- main-branch backward --
