@@ -641,11 +641,18 @@ def time_varlen(msa, pcfg, x, bufs, K, world):
     lens[0] += N - sum(lens)
     cu = torch.zeros(len(lens) + 1, dtype=torch.int64)
     cu[1:] = torch.cumsum(torch.tensor(lens), 0)
+    # one workspace for both batches (the virtual rows of a batch can outnumber its tokens)
+    cnt, ln = VARLEN_UNIFORM
+    cu2 = torch.arange(cnt + 1, dtype=torch.int64) * ln
+    nws = max(msa.msa_prefill_varlen_workspace(c, pcfg.H_q, pcfg.H_kv, pcfg.d_h, pcfg.k)
+              for c in (cu, cu2))
+    ws = bufs["ws"] if nws <= bufs["ws"].numel() else torch.empty(nws, dtype=torch.uint8,
+                                                                     device="cuda")
 
     def call():
         msa.msa_prefill_varlen(x["q"], x["k"], x["v"], x["q_idx"], x["k_idx"], cu, pcfg.k,
                                o=bufs["o"], lse=bufs["lse"].view(-1), idx=bufs["idx"].view(-1),
-                               ws=bufs["ws"])
+                               ws=ws)
 
     for _ in range(3):
         call()
@@ -662,16 +669,14 @@ def time_varlen(msa, pcfg, x, bufs, K, world):
     out = {"ms": round(ms, 4), "value": round(world * N / (ms * 1e-3), 1), "unit": "tokens/s",
            "sequences": lens}
     # many equal short sequences: launch count per sequence matters most here
-    cnt, ln = VARLEN_UNIFORM
     if cnt * ln <= N:
-        cu2 = torch.arange(cnt + 1, dtype=torch.int64) * ln
         T = cnt * ln
 
         def call2():
             msa.msa_prefill_varlen(x["q"][:T], x["k"][:T], x["v"][:T], x["q_idx"][:T],
                                    x["k_idx"][:T], cu2, pcfg.k, o=bufs["o"][:T],
                                    lse=bufs["lse"].view(-1)[:T * pcfg.H_q],
-                                   idx=bufs["idx"].view(-1)[:T * pcfg.H_kv * pcfg.k], ws=bufs["ws"])
+                                   idx=bufs["idx"].view(-1)[:T * pcfg.H_kv * pcfg.k], ws=ws)
 
         for _ in range(3):
             call2()

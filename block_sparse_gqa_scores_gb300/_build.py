@@ -14,7 +14,7 @@ OBJ = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmsa.so")
 SOURCES = ["api.cu", "k_score.cu", "k_select.cu", "k_attn.cu", "attn_fwd.cu", "k_attn_shared.cu",
            "k_attn_kvouter.cu", "k_attn_plan.cu", "k_decode.cu", "decode_noalloc.cu",
-           "k_kl.cu", "k_attn_bwd.cu"]
+           "k_kl.cu", "k_attn_bwd.cu", "varlen.cu"]
 HEADERS = ["msa_device.cuh", "msa_internal.h", "attn_tile.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -236,17 +236,32 @@ MSA_API msa_status_t msa_sparse_decode(const void* q, const void* q_idx, const v
   return from_cuda(e);
 }
 
-// Varlen prefill: the sequences of a packed batch, one after another on `stream`, each through the
-// fused index branch and the main branch (the kernels are the single-sequence ones; only the
-// pointers move).  cu_seqlens is host memory: the launch sizes depend on it.
+// Varlen prefill: the whole packed batch in one launch per stage over a virtual row space in which
+// each sequence starts on an aligned row (varlen.cu).  cu_seqlens is host memory: the launch
+// sizes and the workspace layout depend on it.
+namespace {
+// the virtual row count of a valid batch, or -1
+int64_t varlen_rows(const int64_t* cu_seqlens, int nseq, int H_kv) {
+  if (!cu_seqlens || nseq < 1 || H_kv < 1 || cu_seqlens[0] != 0) return -1;
+  const int64_t align = std::max<int64_t>(128, msa::index_rows_per_cta(H_kv));
+  int64_t tv = 0;
+  for (int s = 0; s < nseq; ++s) {
+    const int64_t n = cu_seqlens[s + 1] - cu_seqlens[s];
+    if (n < 1) return -1;
+    tv += (n + align - 1) / align * align;
+  }
+  return tv;
+}
+}  // namespace
+
 MSA_API size_t msa_prefill_varlen_workspace(const int64_t* cu_seqlens, int nseq, int H_q, int H_kv,
                                             int d_h, int k) {
   if (!cu_seqlens || nseq < 1 || H_kv < 1 || H_q < H_kv || H_q % H_kv != 0 || k < 1 || k > 64 ||
       d_h < 1)
     return 0;
-  int64_t longest = 0;
-  for (int s = 0; s < nseq; ++s) longest = std::max(longest, cu_seqlens[s + 1] - cu_seqlens[s]);
-  return longest < 1 ? 0 : msa::sparse_attn_ws_bytes(longest, H_q, H_kv, d_h, k);
+  if (varlen_rows(cu_seqlens, nseq, H_kv) < 1) return 0;
+  // d_idx is not an argument: the layout is sized for the largest supported index dim (64)
+  return msa::varlen_layout(cu_seqlens, nseq, H_q, H_kv, d_h, 64, k).total;
 }
 
 MSA_API msa_status_t msa_prefill_varlen(const void* q, const void* k, const void* v,
@@ -261,44 +276,19 @@ MSA_API msa_status_t msa_prefill_varlen(const void* q, const void* k, const void
   if (nseq < 1 || H_q < 1 || H_kv < 1 || H_q % H_kv != 0 || d_h < 1 || d_idx < 1 ||
       block_size != 64 || k_blocks < 1 || k_blocks > 64 || cu_seqlens[0] != 0)
     return MSA_ERR_INVALID_ARGUMENT;
-  int64_t longest = 0;
-  for (int s = 0; s < nseq; ++s) {
-    const int64_t n = cu_seqlens[s + 1] - cu_seqlens[s];
-    if (n < 1) return MSA_ERR_INVALID_ARGUMENT;
-    longest = std::max(longest, n);
-  }
+  for (int s = 0; s < nseq; ++s)
+    if (cu_seqlens[s + 1] - cu_seqlens[s] < 1) return MSA_ERR_INVALID_ARGUMENT;
   if (!pow2_upto(H_kv, 8) || !pow2_upto(H_q / H_kv, 8) || (d_h != 64 && d_h != 128) ||
       (d_idx != 32 && d_idx != 64) || k_blocks > MSA_INDEX_SELECT_MAX_K)
     return MSA_ERR_UNSUPPORTED;
-  if (longest * H_kv >= kMaxRows || longest > ((int64_t)1 << 21)) return MSA_ERR_UNSUPPORTED;
-  if (ws_bytes < msa::sparse_attn_ws_bytes(longest, H_q, H_kv, d_h, k_blocks))
+  const int64_t tv = varlen_rows(cu_seqlens, nseq, H_kv);
+  if (tv * H_kv >= kMaxRows || tv > ((int64_t)1 << 21) || (int64_t)H_kv * tv * k_blocks >= kMaxRows)
+    return MSA_ERR_UNSUPPORTED;
+  if (ws_bytes < msa::varlen_layout(cu_seqlens, nseq, H_q, H_kv, d_h, 64, k_blocks).total)
     return MSA_ERR_WORKSPACE;
-  cudaStream_t st = (cudaStream_t)stream;
-  const auto* qb = static_cast<const char*>(q);
-  const auto* kb = static_cast<const char*>(k);
-  const auto* vb = static_cast<const char*>(v);
-  const auto* qib = static_cast<const char*>(q_idx);
-  const auto* kib = static_cast<const char*>(k_idx);
-  auto* ob = static_cast<char*>(o);
-  for (int s = 0; s < nseq; ++s) {
-    const int64_t t0 = cu_seqlens[s], n = cu_seqlens[s + 1] - t0;
-    // a sequence's rows start t0 rows into each packed tensor; its selections and LSE are
-    // contiguous blocks [H_kv, n, k] and [H_q, n] starting at t0 * H_kv * k and t0 * H_q
-    const void* qs = qb + t0 * H_q * d_h * 2;
-    const void* ks = kb + t0 * H_kv * d_h * 2;
-    const void* vs = vb + t0 * H_kv * d_h * 2;
-    const void* qis = qib + t0 * H_kv * d_idx * 2;
-    const void* kis = kib + t0 * d_idx * 2;
-    int32_t* idxs = idx + t0 * H_kv * k_blocks;
-    void* os = ob + t0 * H_q * d_h * 2;
-    float* lses = lse + t0 * H_q;
-    cudaError_t e = msa::launch_index_select(qis, kis, idxs, n, H_kv, d_idx, k_blocks, 0, n, st);
-    if (e != cudaSuccess) return MSA_ERR_CUDA;
-    e = msa::launch_sparse_attn_fwd(qs, ks, vs, idxs, os, lses, n, H_q, H_kv, d_h, k_blocks, ws,
-                                    st);
-    if (e != cudaSuccess) return MSA_ERR_CUDA;
-  }
-  return MSA_OK;
+  return from_cuda(msa::launch_prefill_varlen(q, k, v, q_idx, k_idx, cu_seqlens, nseq, H_q, H_kv,
+                                              d_h, d_idx, k_blocks, idx, o, lse, ws,
+                                              (cudaStream_t)stream));
 }
 
 MSA_API msa_status_t msa_sparse_decode_paged(

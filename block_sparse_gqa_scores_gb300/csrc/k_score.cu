@@ -174,7 +174,8 @@ __global__ void __launch_bounds__(ScoreSmem<D_IDX, SUB, CAP>::kThreads, 1)
     k_index_block_scores(const __grid_constant__ CUtensorMap tm_q,
                          const __grid_constant__ CUtensorMap tm_k, float* __restrict__ M,
                          int32_t* __restrict__ idx, int kk, int64_t N, int log2_hkv,
-                         int64_t q_start, int64_t q_count, int64_t nblk, float scale) {
+                         int64_t q_start, int64_t q_count, int64_t nblk, float scale,
+                         const int* __restrict__ ktab) {
   using L = ScoreSmem<D_IDX, SUB, CAP>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -190,6 +191,9 @@ __global__ void __launch_bounds__(ScoreSmem<D_IDX, SUB, CAP>::kThreads, 1)
   const int64_t i0 = q_start + st * per_cta;
   const int64_t i_end = min(i0 + per_cta, q_start + q_count);
   const int nkt = (int)((i_end - 1) / kKeys) + 1;         // key tiles covering [0, i_end)
+  // first key tile: 0, or (packed variable-length batches) the first tile of the sequence that
+  // holds this CTA's rows -- sequences start on 128-row boundaries and no CTA spans two of them
+  const int kt0 = ktab != nullptr ? __ldg(ktab + (i0 >> 7)) : 0;
   const int64_t R0 = i0 << log2_hkv;                      // first (query, group) row
 
   const uint32_t bar0 = sbase + L::kOffBar;
@@ -230,8 +234,9 @@ __global__ void __launch_bounds__(ScoreSmem<D_IDX, SUB, CAP>::kThreads, 1)
         tma_load_2d(sbase + L::kOffA + s * L::kABytes, &tm_q, full_a, 0, (int)(R0 + s * kRows));
       int last_round[kStages];
       for (int s = 0; s < kStages; ++s) last_round[s] = -1;
-      for (int kt = 0; kt < nkt; ++kt) {
-        const int stg = kt % kStages, round = kt / kStages;
+      for (int kt = kt0; kt < nkt; ++kt) {
+        const int u = kt - kt0;
+        const int stg = u % kStages, round = u / kStages;
         if (!mbar_wait(empty_b(stg), (round & 1) ^ 1, &g_score_status, lim)) break;
         mbar_expect_tx(full_b(stg), L::kBBytes);
         tma_load_2d(sbase + L::kOffB + stg * L::kBBytes, &tm_k, full_b(stg), 0, kt * kKeys);
@@ -250,9 +255,10 @@ __global__ void __launch_bounds__(ScoreSmem<D_IDX, SUB, CAP>::kThreads, 1)
       constexpr int swz = D_IDX * 2;                     // 128-B or 64-B swizzle rows
       if (mbar_wait(full_a, 0, &g_score_status, lim)) {
         tc_fence_after();
-        for (int kt = 0; kt < nkt; ++kt) {
-          const int stg = kt % kStages, round = kt / kStages;
-          const int acc = kt & 1, use = kt >> 1;
+        for (int kt = kt0; kt < nkt; ++kt) {
+          const int u = kt - kt0;
+          const int stg = u % kStages, round = u / kStages;
+          const int acc = u & 1, use = u >> 1;
           if (!mbar_wait(tempty(acc), (use & 1) ^ 1, &g_score_status, lim)) break;
           if (!mbar_wait(full_b(stg), round & 1, &g_score_status, lim)) break;
           tc_fence_after();
@@ -289,8 +295,8 @@ __global__ void __launch_bounds__(ScoreSmem<D_IDX, SUB, CAP>::kThreads, 1)
       int cnt = 0;
       float tau = km1 > 0 ? -INFINITY : INFINITY;
       bool ok = true;
-      for (int kt = 0; kt < nkt; ++kt) {
-        const int acc = kt & 1, use = kt >> 1;
+      for (int kt = kt0; kt < nkt; ++kt) {
+        const int acc = (kt - kt0) & 1, use = (kt - kt0) >> 1;
         // every lane waits; the warp leaves together if any lane gave up (the loop body has
         // warp-wide operations)
         if (!__all_sync(0xffffffffu, mbar_wait(tfull(acc), use & 1, &g_score_status, lim))) {
@@ -418,7 +424,7 @@ __global__ void __launch_bounds__(ScoreSmem<D_IDX, SUB, CAP>::kThreads, 1)
 template <int D_IDX, int SUB, int CAP>
 cudaError_t launch_scores(const CUtensorMap& tq, const CUtensorMap& tk, float* M, int32_t* idx,
                           int kk, int64_t N, int H_kv, int64_t q_start, int64_t q_count,
-                          int64_t nblk, cudaStream_t stream) {
+                          int64_t nblk, const int* ktab, cudaStream_t stream) {
   using L = ScoreSmem<D_IDX, SUB, CAP>;
   auto kern = k_index_block_scores<D_IDX, SUB, CAP>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
@@ -429,7 +435,7 @@ cudaError_t launch_scores(const CUtensorMap& tq, const CUtensorMap& tk, float* M
   const int64_t grid = (q_count + per_cta - 1) / per_cta;
   const float scale = (float)(1.0 / std::sqrt((double)D_IDX));
   kern<<<(unsigned)grid, L::kThreads, L::kAlloc, stream>>>(tq, tk, M, idx, kk, N, log2_hkv,
-                                                           q_start, q_count, nblk, scale);
+                                                           q_start, q_count, nblk, scale, ktab);
   return cudaGetLastError();
 }
 
@@ -437,7 +443,7 @@ cudaError_t launch_scores(const CUtensorMap& tq, const CUtensorMap& tk, float* M
 
 static cudaError_t launch_index(const void* q_idx, const void* k_idx, float* M, int32_t* idx,
                                int kk, int64_t N, int H_kv, int d_idx, int64_t q_start,
-                               int64_t q_count, cudaStream_t stream) {
+                               int64_t q_count, const int* ktab, cudaStream_t stream) {
   CUtensorMap tq, tk;
   const int swz = d_idx * 2;   // one swizzle row per index vector
   cudaError_t e = make_tma_2d_bf16(&tq, q_idx, (uint64_t)d_idx, (uint64_t)N * H_kv, d_idx, kRows, swz);
@@ -446,7 +452,7 @@ static cudaError_t launch_index(const void* q_idx, const void* k_idx, float* M, 
   if (e != cudaSuccess) return e;
   const int64_t nblk = (N + kBlock - 1) / kBlock;
 #define MSA_SCORES(D, CAP) \
-  launch_scores<D, 2, CAP>(tq, tk, M, idx, kk, N, H_kv, q_start, q_count, nblk, stream)
+  launch_scores<D, 2, CAP>(tq, tk, M, idx, kk, N, H_kv, q_start, q_count, nblk, ktab, stream)
   if (idx != nullptr && kk <= 16) return d_idx == 64 ? MSA_SCORES(64, 32) : MSA_SCORES(32, 32);
   if (idx != nullptr) return d_idx == 64 ? MSA_SCORES(64, 56) : MSA_SCORES(32, 56);
   return d_idx == 64 ? MSA_SCORES(64, 0) : MSA_SCORES(32, 0);
@@ -456,14 +462,18 @@ static cudaError_t launch_index(const void* q_idx, const void* k_idx, float* M, 
 cudaError_t launch_index_block_scores(const void* q_idx, const void* k_idx, float* M, int64_t N,
                                       int H_kv, int d_idx, int64_t q_start, int64_t q_count,
                                       cudaStream_t stream) {
-  return launch_index(q_idx, k_idx, M, nullptr, 0, N, H_kv, d_idx, q_start, q_count, stream);
+  return launch_index(q_idx, k_idx, M, nullptr, 0, N, H_kv, d_idx, q_start, q_count, nullptr,
+                      stream);
 }
 
 cudaError_t launch_index_select(const void* q_idx, const void* k_idx, int32_t* idx, int64_t N,
                                 int H_kv, int d_idx, int k, int64_t q_start, int64_t q_count,
-                                cudaStream_t stream) {
-  return launch_index(q_idx, k_idx, nullptr, idx, k, N, H_kv, d_idx, q_start, q_count, stream);
+                                cudaStream_t stream, const int* ktab) {
+  return launch_index(q_idx, k_idx, nullptr, idx, k, N, H_kv, d_idx, q_start, q_count, ktab,
+                      stream);
 }
+
+int index_rows_per_cta(int H_kv) { return 2 * (kRows / H_kv); }
 
 cudaError_t set_score_wait_limit(unsigned long long ns) {
   return cudaMemcpyToSymbol(g_score_wait_ns, &ns, sizeof(ns));

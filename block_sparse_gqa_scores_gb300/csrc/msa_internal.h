@@ -1,6 +1,9 @@
 // Internal launchers shared between the kernel translation units and the C ABI layer.
 #pragma once
 
+#include <algorithm>
+#include <vector>
+
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -72,9 +75,27 @@ cudaError_t launch_attn_kvouter(const void* q, const void* k, const void* v, con
 cudaError_t launch_index_block_scores(const void* q_idx, const void* k_idx, float* M, int64_t N,
                                       int H_kv, int d_idx, int64_t q_start, int64_t q_count,
                                       cudaStream_t stream);
+// ktab (variable-length batches): per 128 rows, the first 128-key tile of the sequence that
+// holds them; sequences then start on 128-row boundaries and no CTA's rows (index_rows_per_cta)
+// span two of them.  Null: every row starts at key 0.
 cudaError_t launch_index_select(const void* q_idx, const void* k_idx, int32_t* idx, int64_t N,
                                 int H_kv, int d_idx, int k, int64_t q_start, int64_t q_count,
-                                cudaStream_t stream);
+                                cudaStream_t stream, const int* ktab = nullptr);
+int index_rows_per_cta(int H_kv);
+
+// Variable-length prefill in one launch per stage (varlen.cu): the workspace layout over the
+// virtual rows (each sequence padded to a multiple of `align` rows) and the launch sequence.
+struct VarlenLayout {
+  int64_t align, Tv;
+  bool in_place;                       // virtual rows = packed rows: Q, K, V, O used in place
+  size_t main, starts, ktab, idx, lse, q, k, v, qi, ki, o, total;
+};
+VarlenLayout varlen_layout(const int64_t* cu_seqlens, int nseq, int H_q, int H_kv, int d_h,
+                           int d_idx, int k);
+cudaError_t launch_prefill_varlen(const void* q, const void* k, const void* v, const void* q_idx,
+                                  const void* k_idx, const int64_t* cu_seqlens, int nseq,
+                                  int H_q, int H_kv, int d_h, int d_idx, int kk, int32_t* idx,
+                                  void* o, float* lse, void* ws, cudaStream_t st);
 cudaError_t read_reset_score_status(unsigned* out);
 cudaError_t set_score_wait_limit(unsigned long long ns);
 

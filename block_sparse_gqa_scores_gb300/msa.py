@@ -286,6 +286,14 @@ def msa_sparse_decode_noalloc(q, q_idx, k_cache, v_cache, k_idx_cache, cu_seqlen
     return o, lse, idx_out
 
 
+def msa_prefill_varlen_workspace(cu_seqlens, H_q, H_kv, d_h, kk):
+    """Workspace bytes of msa_prefill_varlen for this batch (cu_seqlens: CPU int64 [nseq+1])."""
+    if cu_seqlens.dtype != torch.int64 or cu_seqlens.is_cuda or not cu_seqlens.is_contiguous():
+        raise ValueError("cu_seqlens must be a contiguous int64 CPU tensor")
+    return int(lib.msa_prefill_varlen_workspace(ctypes.c_void_p(cu_seqlens.data_ptr()),
+                                                cu_seqlens.numel() - 1, H_q, H_kv, d_h, kk))
+
+
 def msa_prefill_varlen(q, k, v, q_idx, k_idx, cu_seqlens, kk, o=None, lse=None, idx=None,
                        ws=None, block_size=BLOCK, stream=None):
     """Prefill of packed independent sequences (cu_seqlens: a CPU int64 tensor [nseq+1]) ->

@@ -156,8 +156,11 @@ msa_status_t msa_sparse_attn_bwd(const void *q, const void *k, const void *v, co
                                  int block_size, int k_blocks, void *ws, size_t ws_bytes,
                                  void *stream);
 
-/* Workspace bytes msa_prefill_varlen needs: that of msa_sparse_attn_fwd for the longest sequence
- * (0 for invalid sizes).  cu_seqlens is host memory here. */
+/* Workspace bytes msa_prefill_varlen needs (0 for invalid sizes); cu_seqlens is host memory
+ * here.  The batch runs over Tv virtual rows, each sequence padded to a multiple of
+ * max(128, 256 / H_kv) rows: the main-branch workspace of msa_sparse_attn_fwd for Tv rows, the
+ * selections and LSEs over the virtual rows and, unless every length is such a multiple,
+ * virtual copies of q, k, v, q_idx, k_idx and o (sized for d_idx = 64). */
 size_t msa_prefill_varlen_workspace(const int64_t *cu_seqlens, int nseq, int H_q, int H_kv,
                                     int d_h, int k);
 
@@ -171,9 +174,12 @@ size_t msa_prefill_varlen_workspace(const int64_t *cu_seqlens, int nseq, int H_q
  *   idx    int32: sequence s's selections [H_kv, N_s, k] at element offset cu_seqlens[s] * H_kv * k
  *   lse    fp32: sequence s's [H_q, N_s] at element offset cu_seqlens[s] * H_q
  *   cu_seqlens  int64 [nseq + 1], HOST memory, cu_seqlens[0] = 0, every sequence >= 1 token
- *   ws     device workspace of msa_prefill_varlen_workspace() bytes (reused by every sequence).
+ *   ws     device workspace of msa_prefill_varlen_workspace() bytes.
  * Each sequence's results equal those of the single-sequence calls on its rows, bit for bit.
- * The sequences run one after another on `stream` (launches per sequence as the two calls);
+ * The whole batch runs in one launch per stage: every sequence starts on an aligned row of a
+ * virtual row space (see msa_prefill_varlen_workspace), where the index branch starts each
+ * row's key range at its sequence's first block and the main branch runs unchanged; rows are
+ * gathered into and scattered out of that space only when a length is not aligned.
  * k > MSA_INDEX_SELECT_MAX_K: MSA_ERR_UNSUPPORTED; other errors as the two calls. */
 msa_status_t msa_prefill_varlen(const void *q, const void *k, const void *v, const void *q_idx,
                                 const void *k_idx, const int64_t *cu_seqlens, int nseq, int H_q,

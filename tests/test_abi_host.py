@@ -234,10 +234,23 @@ def test_prefill_varlen_unsupported_and_workspace(lib):
     assert varlen(lib, d_h=96) == UNSUPPORTED
     lib.msa_prefill_varlen_workspace.restype = ctypes.c_size_t
     lib.msa_sparse_attn_fwd_workspace.restype = ctypes.c_size_t
+    # one launch per stage over a virtual row space where each sequence starts on a multiple of
+    # 128 rows: 100, 40000, 900 -> 128 + 40064 + 1024 = 41216 rows.  Workspace: the main
+    # branch's for 41216 rows, the selections and LSEs over the virtual rows, and (lengths not
+    # multiples of 128) virtual copies of q, k, v, q_idx, k_idx and o; d_idx is sized at 64.
     cu = (ctypes.c_int64 * 4)(0, 100, 40100, 41000)
     need = lib.msa_prefill_varlen_workspace(cu, 3, 32, 4, 128, 16)
-    assert need == lib.msa_sparse_attn_fwd_workspace(i64(40000), 32, 4, 128, 16)
+    tv = 41216
+    floor = (lib.msa_sparse_attn_fwd_workspace(i64(tv), 32, 4, 128, 16) + 4 * 4 * tv * 16 +
+             4 * 32 * tv + 2 * tv * (32 * 128 + 2 * 4 * 128 + 4 * 64 + 64 + 32 * 128))
+    assert floor <= need <= floor + 12 * 256 + 2 * 8 * 4 + 4 * tv // 128
     assert varlen(lib, cu=(0, 100, 40100, 41000), wsb=need - 1) == WORKSPACE
+    # lengths that are multiples of 128: the packed rows are the virtual rows, nothing is copied
+    cu2 = (ctypes.c_int64 * 3)(0, 2048, 4096)
+    need2 = lib.msa_prefill_varlen_workspace(cu2, 2, 32, 4, 128, 16)
+    floor2 = (lib.msa_sparse_attn_fwd_workspace(i64(4096), 32, 4, 128, 16) + 4 * 4 * 4096 * 16 +
+              4 * 32 * 4096)
+    assert floor2 <= need2 <= floor2 + 6 * 256 + 2 * 8 * 3 + 4 * 32
 
 
 def klb(lib, gk=P, dq=P, dk=P, N=1024, H_q=32, H_kv=4, d_h=128, d_idx=64, B=64, kk=16, ws=P,

@@ -402,13 +402,19 @@ def test_sparse_attn_bwd(name, over, N, k):
 
 # -------------------------------------------------------------- varlen prefill --
 
-@pytest.mark.parametrize("name,lens", [("p32k", [1, 63, 64, 65, 1000, 3000, 4500]),
-                                       ("tiny", [700, 1, 1024, 129]),
-                                       ("p32k", [40000, 2000])])
-def test_prefill_varlen_equals_single_sequences(name, lens):
+@pytest.mark.parametrize("name,over,lens", [("p32k", {}, [1, 63, 64, 65, 1000, 3000, 4500]),
+                                            ("tiny", {}, [700, 1, 1024, 129]),
+                                            ("p32k", {}, [40000, 2000]),
+                                            # lengths on the 128-row alignment: rows used in place
+                                            ("p32k", {}, [2048, 128, 4096, 2048]),
+                                            # H_kv = 1: 256-row alignment
+                                            ("p32k", dict(H_q=8, H_kv=1), [300, 1500, 256]),
+                                            ("tiny", dict(d_h=128, k=8), [5000, 77])])
+def test_prefill_varlen_equals_single_sequences(name, over, lens):
     """A packed batch of independent sequences gives, per sequence, exactly the single-sequence
-    results (same kernels on the sequence's rows; positions restart at each sequence)."""
-    cfg = cfg_of(name)
+    results (positions restart at each sequence), whether the batch's rows are used in place or
+    gathered into the aligned virtual rows."""
+    cfg = cfg_of(name, **over)
     T = sum(lens)
     x, _ = fresh(cfg, T, seed=31)
     cu = torch.zeros(len(lens) + 1, dtype=torch.int64)
