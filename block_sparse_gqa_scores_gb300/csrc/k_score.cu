@@ -47,7 +47,6 @@ __device__ unsigned long long g_score_wait_ns = kWaitNs;
 
 constexpr int kRows = 128;     // UMMA M: rows per sub-tile
 constexpr int kKeys = 128;     // UMMA N: keys per tile
-constexpr int kStages = 4;     // K_idx ring depth
 constexpr int kGroupBlocks = 32;   // blocks staged per row before a store
 constexpr int kTilesPerGroup = kGroupBlocks / (kKeys / kBlock);
 // SELECT: candidate slots per row, CAP = 32 for k <= 16 and 56 for k <= 32 (k - 1 kept after
@@ -58,6 +57,9 @@ struct ScoreSmem {
   static constexpr int kCapStride = CAP + 1;
   static constexpr int kABytes = kRows * D_IDX * 2;
   static constexpr int kBBytes = kKeys * D_IDX * 2;
+  // K_idx ring depth: six stages keep about two microseconds of key tiles in flight; the
+  // k <= 32 candidate buffers (CAP = 56) leave room for four
+  static constexpr int kStages = SELECT && CAP > 32 ? 4 : 6;
   static constexpr int kEpiWarps = 4 * SUB;
   static constexpr int kStageFloats = 32 * 33;        // 32 rows x 32 blocks, padded
   static constexpr int kOffA = 0;
@@ -199,15 +201,15 @@ __global__ void __launch_bounds__(ScoreSmem<D_IDX, SUB, CAP>::kThreads, 1)
   const uint32_t bar0 = sbase + L::kOffBar;
   const uint32_t full_a = bar0;
   auto full_b = [&](int s) { return bar0 + 8u * (1 + s); };
-  auto empty_b = [&](int s) { return bar0 + 8u * (1 + kStages + s); };
-  auto tfull = [&](int a) { return bar0 + 8u * (1 + 2 * kStages + a); };
-  auto tempty = [&](int a) { return bar0 + 8u * (3 + 2 * kStages + a); };
-  const uint32_t done_bar = bar0 + 8u * (5 + 2 * kStages);
+  auto empty_b = [&](int s) { return bar0 + 8u * (1 + L::kStages + s); };
+  auto tfull = [&](int a) { return bar0 + 8u * (1 + 2 * L::kStages + a); };
+  auto tempty = [&](int a) { return bar0 + 8u * (3 + 2 * L::kStages + a); };
+  const uint32_t done_bar = bar0 + 8u * (5 + 2 * L::kStages);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffTmem);
 
   if (threadIdx.x == 0) {
     mbar_init(full_a, 1);
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < L::kStages; ++s) {
       mbar_init(full_b(s), 1);
       mbar_init(empty_b(s), 1);
     }
@@ -232,11 +234,11 @@ __global__ void __launch_bounds__(ScoreSmem<D_IDX, SUB, CAP>::kThreads, 1)
       mbar_expect_tx(full_a, SUB * L::kABytes);
       for (int s = 0; s < SUB; ++s)
         tma_load_2d(sbase + L::kOffA + s * L::kABytes, &tm_q, full_a, 0, (int)(R0 + s * kRows));
-      int last_round[kStages];
-      for (int s = 0; s < kStages; ++s) last_round[s] = -1;
+      int last_round[L::kStages];
+      for (int s = 0; s < L::kStages; ++s) last_round[s] = -1;
       for (int kt = kt0; kt < nkt; ++kt) {
         const int u = kt - kt0;
-        const int stg = u % kStages, round = u / kStages;
+        const int stg = u % L::kStages, round = u / L::kStages;
         if (!mbar_wait(empty_b(stg), (round & 1) ^ 1, &g_score_status, lim)) break;
         mbar_expect_tx(full_b(stg), L::kBBytes);
         tma_load_2d(sbase + L::kOffB + stg * L::kBBytes, &tm_k, full_b(stg), 0, kt * kKeys);
@@ -244,7 +246,7 @@ __global__ void __launch_bounds__(ScoreSmem<D_IDX, SUB, CAP>::kThreads, 1)
       }
       // never leave the CTA with a copy in flight
       mbar_wait(full_a, 0, &g_score_status);
-      for (int s = 0; s < kStages; ++s)
+      for (int s = 0; s < L::kStages; ++s)
         if (last_round[s] >= 0) mbar_wait(full_b(s), last_round[s] & 1, &g_score_status);
     }
   } else if (warp == 1) {
@@ -257,7 +259,7 @@ __global__ void __launch_bounds__(ScoreSmem<D_IDX, SUB, CAP>::kThreads, 1)
         tc_fence_after();
         for (int kt = kt0; kt < nkt; ++kt) {
           const int u = kt - kt0;
-          const int stg = u % kStages, round = u / kStages;
+          const int stg = u % L::kStages, round = u / L::kStages;
           const int acc = u & 1, use = u >> 1;
           if (!mbar_wait(tempty(acc), (use & 1) ^ 1, &g_score_status, lim)) break;
           if (!mbar_wait(full_b(stg), round & 1, &g_score_status, lim)) break;
