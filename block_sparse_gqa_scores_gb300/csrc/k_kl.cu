@@ -47,7 +47,12 @@ constexpr float kLog2e = 1.442695040888963407f;
 // tile's student scores transposed to (entry, token).  TMEM holds kTStages accumulator stages:
 // S (128 rows x 64 tokens) and the student scores (64 tokens on the lanes x the tile's entries).
 constexpr int kSiStride = 68;
-template <int D_H, int G, bool BWD = false>
+// TCG (gradient pass; d_idx = 64 and G = 4, 8, or 2 at d_h = 64): the gradient products run on
+// the tensor core.  Per
+// epilogue group: dS in bf16 split into hi + lo (so the products keep about fp32 accuracy) as
+// [entry][64 tokens] rows of 128 bytes, and a copy of the bucket's K_idx block [64 tokens][64
+// dims], both in the 128-byte swizzle; the tile's index queries are stored swizzled as well.
+template <int D_H, int G, bool BWD = false, bool TCG = false>
 struct KlSmem {
   static constexpr int kEpt = kKlRows / G;        // entries per work tile
   static constexpr int kHalves = D_H / 64;
@@ -60,7 +65,10 @@ struct KlSmem {
       G == 8 ? 4 : (G == 4 ? 3 : (BWD && G == 1 && D_H == 128 ? 1 : 2));
   static constexpr int kKStages = 2;
   static constexpr int kTCols = 64 + kEpt <= 128 ? 128 : 256;
-  static constexpr int kTStages = 512 / kTCols;
+  // TCG: two score stages; the other half of TMEM holds each group's dQ_idx^T (kEpt columns)
+  // and dK_idx (64 columns) accumulators at kColGrad + 128 grp
+  static constexpr int kTStages = TCG ? 2 : 512 / kTCols;
+  static constexpr uint32_t kColGrad = 2u * kTCols;
   static constexpr int kQStage = kHalves * kQHalf + kQiBytes;
   static constexpr int kKStage = kHalves * kKHalf + kKHalf;
   static constexpr int kOffQ = 0;
@@ -72,10 +80,19 @@ struct KlSmem {
   // entries fall in different banks, and each row stays 16-byte aligned)
   static constexpr int kSiBytes = kEpt * kSiStride * 4;
   // gradient pass, per epilogue group: the tile's index queries (one 128-byte row per entry)
-  static constexpr int kOffQg = kOffSi + 2 * kSiBytes;
+  static constexpr int kOffQg =
+      TCG ? (kOffSi + 2 * kSiBytes + 1023) / 1024 * 1024 : kOffSi + 2 * kSiBytes;
   static constexpr int kQgBytes = BWD ? kEpt * 128 : 0;
-  static constexpr int kOffBar = kOffQg + 2 * kQgBytes;
-  static constexpr int kNumBars = 2 * kQStages + 2 * kKStages + 2 * kTStages;
+  static constexpr int kDsBytes = TCG ? kEpt * 128 : 0;      // per group and half (hi, lo)
+  static constexpr int kKgBytes = TCG ? 64 * 128 : 0;        // per group
+  static constexpr int kOffKg = kOffQg + 2 * kQgBytes;
+  static constexpr int kOffDs = kOffKg + 2 * kKgBytes;
+  // the MN-major operands of the gradient MMAs span M = 128 of which rows 64..127 are unused:
+  // those reads land up to 1 KB past a tile, inside the next tile or this zeroed pad
+  static constexpr int kPad = TCG ? 1024 : 0;
+  static constexpr int kOffBar = kOffDs + 4 * kDsBytes + kPad;
+  // + per group the completion of its gradient MMAs (TCG)
+  static constexpr int kNumBars = 2 * kQStages + 2 * kKStages + 2 * kTStages + (TCG ? 2 : 0);
   static constexpr int kOffMisc = kOffBar + 8 * kNumBars;
   static constexpr int kOffPEnt = kOffMisc + 16;  // each producer warp's copy of a tile's entries
   static constexpr int kBytes = kOffPEnt + 2 * 4 * kKlRows;
@@ -84,6 +101,10 @@ struct KlSmem {
   static_assert(kQStage % 1024 == 0 && kKStage % 1024 == 0, "swizzle atoms");
   static_assert(2 * kSiBytes >= 8 * 1024, "rows 64..127 of the student A operand stay in bounds");
   static_assert(kAlloc <= 227 * 1024, "shared memory");
+  static_assert(!TCG || (G >= 2 && kEpt <= 64 && kTCols == 128 && kColGrad + 256 <= 512),
+                "TCG layout");
+  static_assert(!TCG || (kOffQg % 1024 == 0 && kQgBytes % 1024 == 0 && kDsBytes % 1024 == 0),
+                "swizzle atoms");
 };
 
 __device__ __forceinline__ void kl_cp_async16(uint32_t dst, const void* src) {
@@ -357,7 +378,7 @@ __host__ __device__ __forceinline__ int64_t kl_dk_slot(int bkt, int cta, int grp
 }
 constexpr int kKlMaxGrid = 1024;          // CTAs of the block-major pass at most (workspace bound)
 
-template <int D_H, int G, bool BWD>
+template <int D_H, int G, bool BWD, bool TCG = false>
 __global__ void __launch_bounds__(KlWarps<BWD>::kThreads, 1)
     k_kl_kvouter(const __grid_constant__ KlQMaps tm_q, const __nv_bfloat16* __restrict__ q,
                  const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ q_idx,
@@ -367,7 +388,7 @@ __global__ void __launch_bounds__(KlWarps<BWD>::kThreads, 1)
                  int H_kv, int d_idx, int kk, float4* __restrict__ part, float scale_log2,
                  float idx_scale, const KlGrad gr) {
   constexpr int kKlQWarps = KlWarps<BWD>::kQ;
-  using L = KlSmem<D_H, G, BWD>;
+  using L = KlSmem<D_H, G, BWD, TCG>;
   constexpr int kEpt = L::kEpt;
   constexpr int kQStages = L::kQStages, kKStages = L::kKStages, kTStages = L::kTStages;
   constexpr int kCpl = 64 / G;               // columns a lane owns after the reduce-scatter
@@ -383,6 +404,7 @@ __global__ void __launch_bounds__(KlWarps<BWD>::kThreads, 1)
   auto k_empty = [&](int s) { return bar0 + 8u * (2 * kQStages + kKStages + s); };
   auto t_full = [&](int s) { return bar0 + 8u * (2 * kQStages + 2 * kKStages + s); };
   auto t_empty = [&](int s) { return bar0 + 8u * (2 * kQStages + 2 * kKStages + kTStages + s); };
+  auto g_done = [&](int g) { return bar0 + 8u * (2 * kQStages + 2 * kKStages + 2 * kTStages + g); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffMisc);
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + L::kOffMisc + 4);
   int* s_pent = reinterpret_cast<int*>(smem + L::kOffPEnt);
@@ -406,8 +428,19 @@ __global__ void __launch_bounds__(KlWarps<BWD>::kThreads, 1)
       mbar_init(t_full(s), 1);
       mbar_init(t_empty(s), 4 * 32);         // the 128 threads of one epilogue group
     }
+    if (TCG) {
+      mbar_init(g_done(0), 1);
+      mbar_init(g_done(1), 1);
+    }
     *s_abort = 0;
     fence_barrier_init();
+  }
+  if (TCG) {
+    // index queries, dS and K_idx copies start as zeros: rows a tile leaves unwritten are
+    // multiplied by zero dS, and must not hold NaN bit patterns
+    for (int x = threadIdx.x; x < (L::kOffBar - L::kOffQg) / 16; x += blockDim.x)
+      kl_zero16(sb + L::kOffQg + 16 * x);
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), 512);
@@ -634,6 +667,10 @@ __global__ void __launch_bounds__(KlWarps<BWD>::kThreads, 1)
     const int e = R / G, h = R - e * G;
     float* s_si = reinterpret_cast<float*>(smem + L::kOffSi + grp * L::kSiBytes);
     const uint32_t s_qg = sb + L::kOffQg + grp * L::kQgBytes;   // gradient pass only
+    const uint32_t s_ds = sb + L::kOffDs + grp * 2 * L::kDsBytes;   // TCG: dS hi, then lo
+    const uint32_t s_kg = sb + L::kOffKg + grp * L::kKgBytes;       // TCG: K_idx block
+    int kg_bkt = -1, gcount = 0;                                     // TCG state
+    bool dk_fresh = true;
     int bkt = bucket0, nxt = next0;
     // this row's entry and forward LSE, fetched one group-tile ahead
     int c_e0 = 0, c_ne = 0, c_bkt = 0;
@@ -677,9 +714,22 @@ __global__ void __launch_bounds__(KlWarps<BWD>::kThreads, 1)
           const int eq = item >> 3, qc = item & 7;
           if (eq < c_ne && qc < (d_idx >> 3)) {
             const int eg = G == 8 ? cur_ent : __ldg(entries + c_e0 + eq);
-            kl_cp_async16(s_qg + eq * 128 + qc * 16,
+            kl_cp_async16(s_qg + eq * 128 + ((TCG ? qc ^ (eq & 7) : qc) << 4),
                           q_idx + ((int64_t)(eg >> 6) * H_kv + r) * d_idx + qc * 8);
           }
+        }
+        if (TCG && c_bkt != kg_bkt) {
+          // the bucket's K_idx block for the gradient MMAs (the previous tile's have completed)
+          const __nv_bfloat16* kib = k_idx + b * kBlock * (int64_t)d_idx;
+          for (int x = R; x < kBlock * 8; x += kKlRows) {
+            const int jj = x >> 3, c = x & 7;
+            const uint32_t dst = s_kg + jj * 128 + ((c ^ (jj & 7)) << 4);
+            if (b * kBlock + jj < N)
+              kl_cp_async16(dst, kib + (int64_t)jj * d_idx + c * 8);
+            else
+              kl_zero16(dst);
+          }
+          kg_bkt = c_bkt;
         }
         asm volatile("cp.async.commit_group;" ::: "memory");
       }
@@ -775,85 +825,180 @@ __global__ void __launch_bounds__(KlWarps<BWD>::kThreads, 1)
           wsum = __ldg(gr.psum + row);
           lsei2 = __ldg(gr.lse_idx + row) * kLog2e;
         }
+        if constexpr (TCG) {
+          // dS of this lane's columns, split into bf16 hi + lo, into row e of the group's dS
+          // tiles (column c of row e: 16-byte chunk c / 8 at position (c / 8) ^ (e & 7))
 #pragma unroll
-        for (int c = 0; c < kCpl; ++c) {
-          const float pidx = ex2(si[c] * idx_scale * kLog2e - lsei2);
-          const float ds = g * (wsum * pidx - a[c] * invG) * idx_scale;
-          s_si[e * kSiStride + cb + c] = cb + c <= cmax ? ds : 0.f;
-        }
-        asm volatile("cp.async.wait_all;" ::: "memory");   // this thread's index-query copy
-        kl_group_sync(1 + grp);                            // dS and the index queries are complete
-        const int64_t tok0 = b * kBlock;
-        // dQ_idx of (entry, dims chunk) items: entry item / 8, dims (item % 8) * d_idx / 8 ..,
-        // summed over the block's tokens
-        for (int item = R; item < kEpt * 8; item += kKlRows) {
-          const int eq = item >> 3, nd = d_idx >> 3, d0 = (item & 7) * nd;
-          if (eq < c_ne) {
-            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-            // tokens past the sequence have dS = 0; their loads read the last row instead
-#pragma unroll 8
-            for (int c = 0; c < kBlock; ++c) {
-              const float ds = s_si[eq * kSiStride + c];
-              const int64_t tok = tok0 + c < N ? tok0 + c : N - 1;
-              const __nv_bfloat16* kr = k_idx + tok * d_idx + d0;
-              if (nd == 8) {
-                const uint4 v = ldg_nc_v4(kr);
-                const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                for (int u = 0; u < 4; ++u)   // bf16 pair -> fp32 pair is exact (a shift), then one packed FMA
-                  ffma2(acc[2 * u], acc[2 * u + 1], ds, ds, __uint_as_float(w4[u] << 16),
-                        __uint_as_float(w4[u] & 0xffff0000u), acc[2 * u], acc[2 * u + 1]);
-              } else {
-                const uint2 v = *reinterpret_cast<const uint2*>(kr);
-                const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.x));
-                const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.y));
-                acc[0] += ds * f0.x;
-                acc[1] += ds * f0.y;
-                acc[2] += ds * f1.x;
-                acc[3] += ds * f1.y;
-              }
-            }
-            const int ent_q = __ldg(entries + c_e0 + eq);
-            float* dst = gr.part_dq +
-                         (((int64_t)r * N + (ent_q >> 6)) * kk + (ent_q & 63)) * d_idx + d0;
-            // 16-byte stores: a thread's nd floats are contiguous and 16-byte aligned
-            reinterpret_cast<float4*>(dst)[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-            if (nd == 8)
-              reinterpret_cast<float4*>(dst)[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
-          }
-        }
-        // dK_idx of token R / 2, dims (R % 2) * d_idx / 2 ..: sum over the tile's entries
-        {
-          const int ck = R >> 1, nd = d_idx >> 1, d0 = (R & 1) * nd;
-#pragma unroll 4
-          for (int eq = 0; eq < c_ne; ++eq) {
-            const float ds = s_si[eq * kSiStride + ck];
-            const uint8_t* qr = smem + L::kOffQg + grp * L::kQgBytes + eq * 128 + d0 * 2;
+          for (int c8 = 0; c8 < kCpl; c8 += 8) {
+            uint32_t hw[4], lw[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-              if (8 * u >= nd) break;
-              const uint4 v = *reinterpret_cast<const uint4*>(qr + 16 * u);
-              const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+              float dv[2];
 #pragma unroll
-              for (int t = 0; t < 4; ++t)
-                ffma2(dkacc[8 * u + 2 * t], dkacc[8 * u + 2 * t + 1], ds, ds,
-                      __uint_as_float(w4[t] << 16), __uint_as_float(w4[t] & 0xffff0000u),
-                      dkacc[8 * u + 2 * t], dkacc[8 * u + 2 * t + 1]);
+              for (int q2 = 0; q2 < 2; ++q2) {
+                const int c = c8 + 2 * u + q2;
+                const float pidx = ex2(si[c] * idx_scale * kLog2e - lsei2);
+                dv[q2] = cb + c <= cmax ? g * (wsum * pidx - a[c] * invG) * idx_scale : 0.f;
+              }
+              hw[u] = pack_bf16x2(dv[0], dv[1]);
+              lw[u] = pack_bf16x2(dv[0] - __uint_as_float(hw[u] << 16),
+                                  dv[1] - __uint_as_float(hw[u] & 0xffff0000u));
+            }
+            const int chunk = (cb + c8) >> 3;
+            const uint32_t off = (uint32_t)((e >> 3) * 1024 + (e & 7) * 128 + ((chunk ^ (e & 7)) << 4));
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(s_ds + off), "r"(hw[0]),
+                         "r"(hw[1]), "r"(hw[2]), "r"(hw[3]) : "memory");
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(s_ds + L::kDsBytes + off),
+                         "r"(lw[0]), "r"(lw[1]), "r"(lw[2]), "r"(lw[3]) : "memory");
+          }
+          asm volatile("cp.async.wait_all;" ::: "memory");   // index queries, K_idx block
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          tc_fence_before();
+          kl_group_sync(1 + grp);                            // dS, Q_idx, K_idx are complete
+          const uint32_t col_dq = L::kColGrad + 128u * grp, col_dk = col_dq + 64u;
+          if (R == 0) {
+            tc_fence_after();
+            constexpr uint32_t idesc_dq = umma_idesc_bf16(128, kEpt) | (1u << 15);
+            constexpr uint32_t idesc_dk = umma_idesc_bf16(128, 64) | (1u << 15) | (1u << 16);
+            // dQ_idx^T [dims][entries] = K_idx_b^T [dims][tokens] . dS^T [tokens][entries]
+            // (A: K_idx rows read MN-major; rows 64..127 of M are unused lanes)
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+#pragma unroll
+              for (int part = 0; part < 2; ++part)
+                umma_bf16(tmem + col_dq, desc_mn_sw128(s_kg + ks * 2048, 1024, 1024),
+                          umma_desc_kmajor(s_ds + part * L::kDsBytes + ks * 32, 1024, 128),
+                          idesc_dq, (ks | part) ? 1u : 0u);
+            // dK_idx [tokens][dims] += dS^T [tokens][entries] . Q_idx [entries][dims], over the
+            // group's tiles of this bucket
+#pragma unroll
+            for (int ks = 0; ks < kEpt / 16; ++ks)
+#pragma unroll
+              for (int part = 0; part < 2; ++part)
+                umma_bf16(tmem + col_dk,
+                          desc_mn_sw128(s_ds + part * L::kDsBytes + ks * 2048, 1024, 1024),
+                          desc_mn_sw128(s_qg + ks * 2048, 8192, 1024), idesc_dk,
+                          (!dk_fresh || ks || part) ? 1u : 0u);
+            umma_commit(g_done(grp));
+          }
+          const bool okg = mbar_wait(g_done(grp), gcount & 1, &g_kl_status);
+          ++gcount;
+          if (!kl_group_and(1 + grp, okg)) { fail(); break; }
+          tc_fence_after();
+          const bool flush = !has_next || n_bkt != c_bkt;
+          if (qd < 2) {
+            // lanes 0..63: this thread's dims row R of dQ_idx^T over the tile's entries
+            const uint32_t lanes = (uint32_t)(32 * qd) << 16;
+#pragma unroll
+            for (int cc = 0; cc < kEpt; cc += 16) {
+              uint32_t v[16];
+              KL_TMEM_LD16(tmem + lanes + col_dq + cc, v);
+              tmem_ld_wait();
+#pragma unroll
+              for (int c = 0; c < 16; ++c)
+                if (cc + c < c_ne) {
+                  const int ent_q = __ldg(entries + c_e0 + cc + c);
+                  gr.part_dq[(((int64_t)r * N + (ent_q >> 6)) * kk + (ent_q & 63)) * d_idx + R] =
+                      __uint_as_float(v[c]);
+                }
+            }
+            if (flush) {
+              // token row R of the bucket's dK_idx, to the group's slot
+              uint32_t v[64];
+              MSA_TMEM_LD64(tmem + lanes + col_dk, v);
+              tmem_ld_wait();
+              float4* dst = reinterpret_cast<float4*>(
+                  gr.part_dk + (kl_dk_slot(c_bkt, blockIdx.x, grp) * kBlock + R) * d_idx);
+#pragma unroll
+              for (int d = 0; d < 64; d += 4)
+                dst[d / 4] = make_float4(__uint_as_float(v[d]), __uint_as_float(v[d + 1]),
+                                         __uint_as_float(v[d + 2]), __uint_as_float(v[d + 3]));
             }
           }
-          kl_group_sync(1 + grp);                          // s_si may be overwritten
-          const bool flush = !has_next || n_bkt != c_bkt;
-          if (flush) {
-            float4* dst = reinterpret_cast<float4*>(
-                gr.part_dk + (kl_dk_slot(c_bkt, blockIdx.x, grp) * kBlock + ck) * d_idx + d0);
+          dk_fresh = flush;
+          tc_fence_before();
+          kl_group_sync(1 + grp);                          // TMEM and dS may be overwritten
+        } else {
 #pragma unroll
-            for (int d = 0; d < 32; d += 4)
-              if (d < nd) dst[d / 4] = make_float4(dkacc[d], dkacc[d + 1], dkacc[d + 2], dkacc[d + 3]);
-#pragma unroll
-            for (int d = 0; d < 32; ++d) dkacc[d] = 0.f;
+          for (int c = 0; c < kCpl; ++c) {
+            const float pidx = ex2(si[c] * idx_scale * kLog2e - lsei2);
+            const float ds = g * (wsum * pidx - a[c] * invG) * idx_scale;
+            s_si[e * kSiStride + cb + c] = cb + c <= cmax ? ds : 0.f;
+          }
+          asm volatile("cp.async.wait_all;" ::: "memory");   // this thread's index-query copy
+          kl_group_sync(1 + grp);                            // dS and the index queries are complete
+          const int64_t tok0 = b * kBlock;
+          // dQ_idx of (entry, dims chunk) items: entry item / 8, dims (item % 8) * d_idx / 8 ..,
+          // summed over the block's tokens
+          for (int item = R; item < kEpt * 8; item += kKlRows) {
+            const int eq = item >> 3, nd = d_idx >> 3, d0 = (item & 7) * nd;
+            if (eq < c_ne) {
+              float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+              // tokens past the sequence have dS = 0; their loads read the last row instead
+  #pragma unroll 8
+              for (int c = 0; c < kBlock; ++c) {
+                const float ds = s_si[eq * kSiStride + c];
+                const int64_t tok = tok0 + c < N ? tok0 + c : N - 1;
+                const __nv_bfloat16* kr = k_idx + tok * d_idx + d0;
+                if (nd == 8) {
+                  const uint4 v = ldg_nc_v4(kr);
+                  const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+  #pragma unroll
+                  for (int u = 0; u < 4; ++u)   // bf16 pair -> fp32 pair is exact (a shift), then one packed FMA
+                    ffma2(acc[2 * u], acc[2 * u + 1], ds, ds, __uint_as_float(w4[u] << 16),
+                          __uint_as_float(w4[u] & 0xffff0000u), acc[2 * u], acc[2 * u + 1]);
+                } else {
+                  const uint2 v = *reinterpret_cast<const uint2*>(kr);
+                  const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.x));
+                  const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.y));
+                  acc[0] += ds * f0.x;
+                  acc[1] += ds * f0.y;
+                  acc[2] += ds * f1.x;
+                  acc[3] += ds * f1.y;
+                }
+              }
+              const int ent_q = __ldg(entries + c_e0 + eq);
+              float* dst = gr.part_dq +
+                           (((int64_t)r * N + (ent_q >> 6)) * kk + (ent_q & 63)) * d_idx + d0;
+              // 16-byte stores: a thread's nd floats are contiguous and 16-byte aligned
+              reinterpret_cast<float4*>(dst)[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+              if (nd == 8)
+                reinterpret_cast<float4*>(dst)[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+            }
+          }
+          // dK_idx of token R / 2, dims (R % 2) * d_idx / 2 ..: sum over the tile's entries
+          {
+            const int ck = R >> 1, nd = d_idx >> 1, d0 = (R & 1) * nd;
+  #pragma unroll 4
+            for (int eq = 0; eq < c_ne; ++eq) {
+              const float ds = s_si[eq * kSiStride + ck];
+              const uint8_t* qr = smem + L::kOffQg + grp * L::kQgBytes + eq * 128 + d0 * 2;
+  #pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                if (8 * u >= nd) break;
+                const uint4 v = *reinterpret_cast<const uint4*>(qr + 16 * u);
+                const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+  #pragma unroll
+                for (int t = 0; t < 4; ++t)
+                  ffma2(dkacc[8 * u + 2 * t], dkacc[8 * u + 2 * t + 1], ds, ds,
+                        __uint_as_float(w4[t] << 16), __uint_as_float(w4[t] & 0xffff0000u),
+                        dkacc[8 * u + 2 * t], dkacc[8 * u + 2 * t + 1]);
+              }
+            }
+            kl_group_sync(1 + grp);                          // s_si may be overwritten
+            const bool flush = !has_next || n_bkt != c_bkt;
+            if (flush) {
+              float4* dst = reinterpret_cast<float4*>(
+                  gr.part_dk + (kl_dk_slot(c_bkt, blockIdx.x, grp) * kBlock + ck) * d_idx + d0);
+  #pragma unroll
+              for (int d = 0; d < 32; d += 4)
+                if (d < nd) dst[d / 4] = make_float4(dkacc[d], dkacc[d + 1], dkacc[d + 2], dkacc[d + 3]);
+  #pragma unroll
+              for (int d = 0; d < 32; ++d) dkacc[d] = 0.f;
+            }
           }
         }
-      }
+        }
       c_bkt = n_bkt;
       c_e0 = n_e0;
       c_ne = n_ne;
@@ -1068,6 +1213,14 @@ cudaError_t kl_pass(bool bwd, const void* q, const void* k, const void* q_idx, c
     constexpr int D = decltype(dh)::value;
     if (bwd) {
       constexpr int TB = KlWarps<true>::kThreads;
+      // the gradient products on the tensor core where the layout allows (d_idx = 64, G = 4 or 8,
+      // or G = 2 at d_h = 64: at d_h = 128 its buffers do not fit), on the CUDA cores otherwise
+      if (d_idx == 64) {
+        if (G == 8) return run(k_kl_kvouter<D, 8, true, true>, KlSmem<D, 8, true, true>::kAlloc, TB);
+        if (G == 4) return run(k_kl_kvouter<D, 4, true, true>, KlSmem<D, 4, true, true>::kAlloc, TB);
+        if constexpr (D == 64)
+          if (G == 2) return run(k_kl_kvouter<D, 2, true, true>, KlSmem<D, 2, true, true>::kAlloc, TB);
+      }
       switch (G) {
         case 1: return run(k_kl_kvouter<D, 1, true>, KlSmem<D, 1, true>::kAlloc, TB);
         case 2: return run(k_kl_kvouter<D, 2, true>, KlSmem<D, 2, true>::kAlloc, TB);

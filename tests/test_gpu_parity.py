@@ -319,6 +319,7 @@ KLB_CASES = [("p32k", {}, 1000, 16), ("p32k", {}, 65, 16), ("p32k", {}, 3000, 16
              ("p32k", dict(H_q=16, H_kv=4), 2000, 16), ("tiny", {}, 1024, 4),
              ("p32k", dict(H_q=4, H_kv=4, d_h=64), 900, 16),
              ("p32k", dict(H_q=8, H_kv=4, d_h=64, d_idx=32), 700, 8),
+             ("p32k", dict(H_q=8, H_kv=4, d_h=64), 1200, 16), ("p32k", dict(H_q=16, H_kv=2), 1100, 64),
              ("tiny", dict(d_h=128), 1000, 64)]
 
 
