@@ -39,7 +39,7 @@ import gen  # noqa: E402
 
 METRIC = ("MSA prefill tokens/s and decode tokens/s at 128K ctx; % of bf16 TC / HBM roofline")
 # kernels per step: the fused index branch (block scores + top-k); attention per 32768-row chunk:
-# plan, scan, plan, block-major pass, shared-block pass with the merge (+ one memset); decode:
+# plan, scan, scatter, block-major pass, shared-block pass with the merge (+ one memset); decode:
 # the index-key scan and the tail (selection + attention + merge in one kernel)
 ATTN_LAUNCHES_PER_CHUNK = 5
 ATTN_CHUNK_ROWS = 32768
@@ -52,8 +52,10 @@ KERNEL_FILES = {"index_branch": ["k_score.cu"],
                 "kl_loss_bwd": ["k_kl.cu", "k_attn_plan.cu", "attn_tile.cuh"],
                 "sparse_attn_bwd": ["k_attn_bwd.cu", "k_kl.cu", "k_attn_plan.cu", "attn_tile.cuh"]}
 # the KL alignment loss forward, timed apart from the step: plan, scan, plan, block-major pass,
-# merge (+ one memset)
+# merge (+ two memsets); its gradient: row-ordered bucketing (count, scan, bases, scatter),
+# block-major pass, dQ_idx merge, dK_idx merge (+ two memsets)
 KL_LAUNCHES = 5
+KLB_LAUNCHES = 7
 
 
 # ------------------------------------------------------------------------ helpers --
@@ -108,10 +110,11 @@ def kernel_source_hash(fnames):
 # ncu kernel name -> the bench row it belongs to (a row is one call of the C ABI per step)
 NCU_ROWS = {"k_index_block_scores": "index_branch",
             "k_attn_plan": "main_branch", "k_attn_scan": "main_branch",
+            "k_attn_scatter": "main_branch",
             "k_attn_kvouter": "main_branch", "k_attn_shared": "main_branch",
             "k_decode_block_scores": "decode", "k_decode_tail": "decode",
             "k_kl_plan": "kl_loss_fwd", "k_kl_kvouter": "kl_loss_fwd", "k_kl_merge": "kl_loss_fwd",
-            "k_kl_dq_merge": "kl_loss_bwd",
+            "k_kl_dq_merge": "kl_loss_bwd", "k_kl_dk_merge": "kl_loss_bwd",
             "k_attn_bwd_kvouter": "sparse_attn_bwd", "k_attn_bwd_dq_merge": "sparse_attn_bwd",
             "k_attn_bwd_dkv_merge": "sparse_attn_bwd", "k_attn_bwd_delta": "sparse_attn_bwd"}
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.txt")
@@ -155,8 +158,10 @@ def write_traffic(csv_path, command, scale=1.0, only=None, tag="A"):
         if name not in NCU_ROWS:
             continue
         row = NCU_ROWS[name]
-        if name == "k_kl_kvouter" and raw.replace(" ", "").endswith(",1>"):
-            row = "kl_loss_bwd"                  # the gradient instantiation
+        if name == "k_kl_kvouter" and "<" in raw:
+            targs = raw[raw.index("<") + 1:raw.rindex(">")].replace(" ", "").split(",")
+            if len(targs) >= 3 and targs[2] in ("1", "true"):
+                row = "kl_loss_bwd"              # the gradient instantiation (third argument)
         if r[mi] == "gpu__time_duration.sum":
             firsts[name] += 1
             if name in ("k_kl_kvouter", "k_attn_bwd_kvouter"):
@@ -587,7 +592,7 @@ def time_kl(msa, pcfg, x, bufs, K, sizes, pk, world):
     return {"ms": round(ms, 4), "value": round(world * N / (ms * 1e-3), 1), "unit": "tokens/s",
             "backward_index_branch": {"ms": round(ms_b, 4),
                                       "value": round(world * N / (ms_b * 1e-3), 1),
-                                      "unit": "tokens/s", "gpu_launches_per_call": KL_LAUNCHES + 1,
+                                      "unit": "tokens/s", "gpu_launches_per_call": KLB_LAUNCHES,
                                       "traffic": ncu_traffic("kl_loss_bwd")},
             "mean_kl": round(float(kl.mean()), 6), "gpu_launches_per_call": KL_LAUNCHES,
             "roofline": roofline_row("kl_loss_fwd", ms, "tensor", sizes["F_kl"], "TFLOP/s", pk,
