@@ -701,43 +701,78 @@ def time_varlen(msa, pcfg, x, bufs, K, world):
 
 
 def e2e_prefill(msa, pcfg, x, bufs, K, W, world):
-    """Prefill through the public calls with host (pinned) inputs and outputs: H2D of
-    Q, K, V, Q_idx, K_idx, the two calls, D2H of O and LSE -- all inside the timed region."""
+    """Prefill through the public calls with host (pinned) inputs and outputs: every step copies
+    its Q, K, V, Q_idx, K_idx host -> device, runs the two calls, and reads O and LSE back to the
+    host, all inside the timed region.  The steps are pipelined as a serving loop would run
+    them: two device buffer sets, the host -> device copies on one stream and the device -> host
+    reads on another, so step s+1's inputs and step s-1's results move while step s computes
+    (each stream's order and the events keep every copy after the step it belongs to)."""
     names = ["q", "k", "v", "q_idx", "k_idx"]
     host = {n: torch.empty(x[n].shape, dtype=x[n].dtype, pin_memory=True) for n in names}
     for n in names:
         host[n].copy_(x[n])
-    dev = {n: torch.empty_like(x[n]) for n in names}
+    dev = [{n: torch.empty_like(x[n]) for n in names} for _ in range(2)]
+    outs = [(torch.empty_like(bufs["o"]), torch.empty_like(bufs["lse"])) for _ in range(2)]
     o_h = torch.empty(bufs["o"].shape, dtype=bufs["o"].dtype, pin_memory=True)
     l_h = torch.empty(bufs["lse"].shape, dtype=bufs["lse"].dtype, pin_memory=True)
     N = pcfg.N
+    comp = torch.cuda.current_stream()
+    h2d_s, d2h_s = torch.cuda.Stream(), torch.cuda.Stream()
+    ev = lambda: torch.cuda.Event()
+    in_ready = [ev(), ev()]      # inputs of the buffer set copied
+    in_free = [ev(), ev()]       # the step that read the buffer set's inputs is done
+    out_ready = [ev(), ev()]     # the step's outputs written
+    out_free = [ev(), ev()]      # the outputs read back to the host
+    started = [False, False]
 
-    def step():
-        for n in names:
-            dev[n].copy_(host[n], non_blocking=True)
-        idx = msa.msa_index_select(dev["q_idx"], dev["k_idx"], pcfg.k, idx=bufs["idx"])
-        msa.msa_sparse_attn_fwd(dev["q"], dev["k"], dev["v"], idx, o=bufs["o"], lse=bufs["lse"],
-                                ws=bufs["ws"])
-        o_h.copy_(bufs["o"], non_blocking=True)
-        l_h.copy_(bufs["lse"], non_blocking=True)
+    def step(i):
+        j = i & 1
+        with torch.cuda.stream(h2d_s):
+            if started[j]:
+                h2d_s.wait_event(in_free[j])
+            for n in names:
+                dev[j][n].copy_(host[n], non_blocking=True)
+            in_ready[j].record(h2d_s)
+        comp.wait_event(in_ready[j])
+        if started[j]:
+            comp.wait_event(out_free[j])
+        idx = msa.msa_index_select(dev[j]["q_idx"], dev[j]["k_idx"], pcfg.k, idx=bufs["idx"])
+        msa.msa_sparse_attn_fwd(dev[j]["q"], dev[j]["k"], dev[j]["v"], idx, o=outs[j][0],
+                                lse=outs[j][1], ws=bufs["ws"])
+        in_free[j].record(comp)
+        out_ready[j].record(comp)
+        with torch.cuda.stream(d2h_s):
+            d2h_s.wait_event(out_ready[j])
+            o_h.copy_(outs[j][0], non_blocking=True)
+            l_h.copy_(outs[j][1], non_blocking=True)
+            out_free[j].record(d2h_s)
+        started[j] = True
 
-    for _ in range(W):
-        step()
+    def run(n0, n):
+        for i in range(n0, n0 + n):
+            step(i)
+        # the step sequence ends once the last reads are on the host
+        for j in range(2):
+            if started[j]:
+                comp.wait_event(out_free[j])
+
+    run(0, W)
     torch.cuda.synchronize()
     barrier(world)
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record()
-    for _ in range(K):
-        step()
-    b.record()
+    a.record(comp)
+    h2d_s.wait_event(a)
+    d2h_s.wait_event(a)
+    run(W, K)
+    b.record(comp)
     torch.cuda.synchronize()
     t = max_over_ranks(a.elapsed_time(b), world)
     h2d = sum(host[n].numel() * host[n].element_size() for n in names)
     d2h = o_h.numel() * o_h.element_size() + l_h.numel() * l_h.element_size()
-    del dev, host
+    del dev, host, outs
     return {"value": round(world * N * K / (t * 1e-3), 1), "unit": "tokens/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "ms_per_step": round(t / K, 4)}
+            "ms_per_step": round(t / K, 4), "copies": "pipelined over steps"}
 
 
 def cpu_sample_rows(N, n, seed):
