@@ -14,7 +14,8 @@
 //     in shared memory before one coalesced 128-byte store per row.
 //   * blocks after a row's own block are written as -inf.
 // Warp roles: warp 0 = TMA producer, warp 1 = TMEM allocator + MMA issuer,
-// warps 2.. = 4*SUB epilogue warps (warp w reads TMEM lanes 32*(w%4) .. +31).
+// warps 2.. = 4*SUB epilogue warps (warp w reads TMEM lanes 32*(w%4) .. +31); with the select
+// epilogue at k <= 16, 4*SUB more warps, one selection warp per epilogue warp (below).
 //
 // The SELECT variant fuses the per-group top-k of the same section (eq. I^(r)_i) into the
 // epilogue and never writes M: the thread that owns a (query, group) row sees the row's block
@@ -25,7 +26,11 @@
 // to tau ranks below the k-1 earlier (lower-indexed) blocks that hold tau or more, so the
 // strict test loses nothing.  Compaction is stable, so the buffer stays in ascending block
 // order; at the end each row writes its kept blocks, then l(i), then -1 padding: exactly what
-// msa_select_blocks writes from the same fp32 block scores.
+// msa_select_blocks writes from the same fp32 block scores.  At k <= 16 the epilogue warps only
+// reduce each key tile to its two block maxima per row and pass them through a shared-memory
+// ring to a selection warp that owns the same rows and does the bookkeeping: a compaction then
+// delays nothing but its own warp, where it used to hold a TMEM accumulator (and with it the
+// MMA pipeline, two accumulators deep) until it finished.
 #include <cudaTypedefs.h>
 
 #include <algorithm>
@@ -68,13 +73,21 @@ struct ScoreSmem {
   // SELECT: candidate scores of every epilogue row (row stride kCapStride), then their blocks
   static constexpr int kStageBytes =
       SELECT ? kEpiWarps * 32 * kCapStride * 8 : kEpiWarps * kStageFloats * 4;
-  static constexpr int kOffBar = kOffStage + kStageBytes;
-  // barriers: full_a, full_b[kStages], empty_b[kStages], tfull[2], tempty[2], done
-  static constexpr int kNumBars = 1 + 2 * kStages + 4 + 1;
+  // SELECT with CAP = 32: each epilogue warp hands its rows' block maxima to a selection warp of
+  // its own through a ring of kRing key tiles (32 rows x 2 blocks, 8 bytes per row), so the
+  // candidate bookkeeping never holds a TMEM accumulator.  CAP = 56 keeps the bookkeeping in the
+  // epilogue warps (its compaction needs more registers than twice the threads leave).
+  static constexpr int kRing = SELECT && CAP <= 32 ? 8 : 0;
+  static constexpr int kSelWarps = kRing > 0 ? kEpiWarps : 0;
+  static constexpr int kOffRing = kOffStage + kStageBytes;
+  static constexpr int kOffBar = kOffRing + kSelWarps * kRing * 32 * 8;
+  // barriers: full_a, full_b[kStages], empty_b[kStages], tfull[2], tempty[2], done,
+  // ring_full[kSelWarps][kRing], ring_empty[kSelWarps][kRing]
+  static constexpr int kNumBars = 1 + 2 * kStages + 4 + 1 + 2 * kSelWarps * kRing;
   static constexpr int kOffTmem = kOffBar + kNumBars * 8;
   static constexpr int kBytes = kOffTmem + 16;
   static constexpr int kAlloc = kBytes + 1024;
-  static constexpr int kThreads = 64 + 32 * kEpiWarps;
+  static constexpr int kThreads = 64 + 32 * (kEpiWarps + kSelWarps);
   static constexpr uint32_t kTmemCols = 2 * SUB * kKeys;
   static_assert(kTmemCols <= 512, "TMEM has 512 columns");
   static_assert(kAlloc <= 227 * 1024, "shared memory per CTA");
@@ -171,6 +184,34 @@ __device__ __forceinline__ float compact_row(float* sc, int* bl, int& cnt, int k
   return kept == km1 ? th : -INFINITY;
 }
 
+// SELECT: offer block b's score m to a row's candidate buffer (blocks before the row's local
+// block l only, strictly above the running threshold tau).
+template <int CAP>
+__device__ __forceinline__ void offer_block(float* sc, int* bl, int& cnt, float tau, int64_t b,
+                                            int64_t l, float m) {
+  if (b < l && m > tau) {
+    sc[cnt] = m;
+    bl[cnt] = (int)b;
+    ++cnt;
+  }
+}
+
+// SELECT: the row's final selection -- its best k-1 kept blocks (already ascending), then l,
+// then -1 padding.  The whole warp calls it (the compaction is unrolled).
+template <int CAP>
+__device__ __forceinline__ void write_selection(float* sc, int* bl, int cnt, int km1, int kk,
+                                                int64_t R, int log2_hkv, int64_t N, int64_t i,
+                                                int64_t i_end, int64_t l, int32_t* idx) {
+  compact_row<CAP>(sc, bl, cnt, km1);
+  if (i < i_end) {
+    const int rr = (int)(R & ((1 << log2_hkv) - 1));
+    int32_t* out = idx + ((int64_t)rr * N + i) * kk;
+    for (int j = 0; j < cnt; ++j) out[j] = bl[j];
+    out[cnt] = (int32_t)l;
+    for (int j = cnt + 1; j < kk; ++j) out[j] = -1;
+  }
+}
+
 template <int D_IDX, int SUB, int CAP>
 __global__ void __launch_bounds__(ScoreSmem<D_IDX, SUB, CAP>::kThreads, 1)
     k_index_block_scores(const __grid_constant__ CUtensorMap tm_q,
@@ -205,6 +246,12 @@ __global__ void __launch_bounds__(ScoreSmem<D_IDX, SUB, CAP>::kThreads, 1)
   auto tfull = [&](int a) { return bar0 + 8u * (1 + 2 * L::kStages + a); };
   auto tempty = [&](int a) { return bar0 + 8u * (3 + 2 * L::kStages + a); };
   const uint32_t done_bar = bar0 + 8u * (5 + 2 * L::kStages);
+  auto ring_full = [&](int e, int slot) {
+    return bar0 + 8u * (6 + 2 * L::kStages + e * L::kRing + slot);
+  };
+  auto ring_empty = [&](int e, int slot) {
+    return bar0 + 8u * (6 + 2 * L::kStages + (L::kSelWarps + e) * L::kRing + slot);
+  };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffTmem);
 
   if (threadIdx.x == 0) {
@@ -218,6 +265,10 @@ __global__ void __launch_bounds__(ScoreSmem<D_IDX, SUB, CAP>::kThreads, 1)
       mbar_init(tempty(a), L::kEpiWarps);
     }
     mbar_init(done_bar, 1);
+    for (int x = 0; x < L::kSelWarps * L::kRing; ++x) {
+      mbar_init(bar0 + 8u * (6 + 2 * L::kStages + x), 32);
+      mbar_init(bar0 + 8u * (6 + 2 * L::kStages + L::kSelWarps * L::kRing + x), 32);
+    }
     fence_barrier_init();
   }
   if (warp == 1) tmem_alloc(smem_u32(tmem_slot), L::kTmemCols);
@@ -281,12 +332,75 @@ __global__ void __launch_bounds__(ScoreSmem<D_IDX, SUB, CAP>::kThreads, 1)
       umma_commit(done_bar);                           // every MMA issued has completed
       mbar_wait(done_bar, 0, &g_score_status);
     }
+  } else if (warp >= 2 + L::kEpiWarps) {
+    // ------------------------------------------------- selection (SELECT, CAP = 32)
+    // selection warp e takes the rows of epilogue warp e (warp 2 + e) from the ring
+    if constexpr (L::kRing > 0) {
+      const int e = warp - 2 - L::kEpiWarps;
+      const int s = e >> 2, q = (e + 2) & 3;
+      const int64_t R = R0 + (int64_t)s * kRows + 32 * q + lane;
+      const int64_t i = R >> log2_hkv;
+      const int64_t l = i >> 6;
+      float* sc = reinterpret_cast<float*>(smem + L::kOffStage) + (e * 32 + lane) * L::kCapStride;
+      int* bl = reinterpret_cast<int*>(smem + L::kOffStage) +
+                (L::kEpiWarps + e) * 32 * L::kCapStride + lane * L::kCapStride;
+      const float2* ring = reinterpret_cast<const float2*>(smem + L::kOffRing) + e * L::kRing * 32;
+      const int km1 = kk - 1;
+      int cnt = 0;
+      float tau = km1 > 0 ? -INFINITY : INFINITY;
+      bool ok = true;
+      for (int kt = kt0; kt < nkt; ++kt) {
+        const int u = kt - kt0, slot = u % L::kRing, round = u / L::kRing;
+        if (!__all_sync(0xffffffffu,
+                        mbar_wait(ring_full(e, slot), round & 1, &g_score_status, lim))) {
+          ok = false;
+          break;
+        }
+        const float2 m = ring[slot * 32 + lane];
+        mbar_arrive(ring_empty(e, slot));
+        offer_block<CAP>(sc, bl, cnt, tau, 2 * (int64_t)kt, l, m.x);
+        offer_block<CAP>(sc, bl, cnt, tau, 2 * (int64_t)kt + 1, l, m.y);
+        if (__any_sync(0xffffffffu, cnt > CAP - 2)) tau = compact_row<CAP>(sc, bl, cnt, km1);
+      }
+      if (ok) write_selection<CAP>(sc, bl, cnt, km1, kk, R, log2_hkv, N, i, i_end, l, idx);
+    }
   } else {
     // --------------------------------------------------------------- epilogue
     const int e = warp - 2;
     const int s = e >> 2;                                 // sub-tile
     const int q = warp & 3;                               // TMEM lane quarter
-    if constexpr (L::SELECT) {
+    if constexpr (L::kRing > 0) {
+      // block maxima of each key tile into the ring of this warp's selection warp
+      const int64_t R = R0 + (int64_t)s * kRows + 32 * q + lane;
+      const int64_t l = (R >> log2_hkv) >> 6;             // local block of this row
+      float2* ring = reinterpret_cast<float2*>(smem + L::kOffRing) + e * L::kRing * 32;
+      for (int kt = kt0; kt < nkt; ++kt) {
+        const int u = kt - kt0, acc = u & 1, use = u >> 1;
+        const int slot = u % L::kRing, round = u / L::kRing;
+        if (!__all_sync(0xffffffffu, mbar_wait(tfull(acc), use & 1, &g_score_status, lim))) break;
+        tc_fence_after();
+        float m[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int64_t b = 2 * (int64_t)kt + h;
+          if (!__any_sync(0xffffffffu, b < l)) continue;   // no row of the warp needs it
+          uint32_t v[64];
+          const uint32_t taddr = tmem_base + ((uint32_t)(32 * q) << 16) +
+                                 (uint32_t)((acc * SUB + s) * kKeys + 64 * h);
+          MSA_TMEM_LD64(taddr, v);
+          tmem_ld_wait();
+          if (b < l) m[h] = max64(v) * scale;
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tempty(acc));
+        if (!__all_sync(0xffffffffu,
+                        mbar_wait(ring_empty(e, slot), (round & 1) ^ 1, &g_score_status, lim)))
+          break;
+        ring[slot * 32 + lane] = make_float2(m[0], m[1]);
+        mbar_arrive(ring_full(e, slot));
+      }
+    } else if constexpr (L::SELECT) {
       const int64_t R = R0 + (int64_t)s * kRows + 32 * q + lane;
       const int64_t i = R >> log2_hkv;
       const int64_t l = i >> 6;                           // local block of this row
@@ -315,31 +429,14 @@ __global__ void __launch_bounds__(ScoreSmem<D_IDX, SUB, CAP>::kThreads, 1)
                                  (uint32_t)((acc * SUB + s) * kKeys + 64 * h);
           MSA_TMEM_LD64(taddr, v);
           tmem_ld_wait();
-          if (b < l) {
-            const float m = max64(v) * scale;
-            if (m > tau) {
-              sc[cnt] = m;
-              bl[cnt] = (int)b;
-              ++cnt;
-            }
-          }
+          if (b < l) offer_block<CAP>(sc, bl, cnt, tau, b, l, max64(v) * scale);
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(tempty(acc));
         if (__any_sync(0xffffffffu, cnt > CAP - 2)) tau = compact_row<CAP>(sc, bl, cnt, km1);
       }
-      if (ok) {
-        compact_row<CAP>(sc, bl, cnt, km1);      // whole warp: the compaction is unrolled
-        if (i < i_end) {
-          // kept blocks (already ascending), then l, then -1
-          const int rr = (int)(R & ((1 << log2_hkv) - 1));
-          int32_t* out = idx + ((int64_t)rr * N + i) * kk;
-          for (int j = 0; j < cnt; ++j) out[j] = bl[j];
-          out[cnt] = (int32_t)l;
-          for (int j = cnt + 1; j < kk; ++j) out[j] = -1;
-        }
-      }
+      if (ok) write_selection<CAP>(sc, bl, cnt, km1, kk, R, log2_hkv, N, i, i_end, l, idx);
     } else {
       float* stage = reinterpret_cast<float*>(smem + L::kOffStage) + e * L::kStageFloats;
       const int64_t Rw = R0 + (int64_t)s * kRows + 32 * q;  // first row of this warp
