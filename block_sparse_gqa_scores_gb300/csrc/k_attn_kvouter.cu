@@ -14,8 +14,8 @@
 // merge in the shared-block pass (k_attn_shared.cu) reads them in slot order without an index.
 //
 // One persistent, warp-specialised CTA per SM:
-//   warp 0      query rows of each tile into a ring of Q stages (TMA, one box of G heads per
-//               entry and 64-dim half, at G = 8; cp.async otherwise)
+//   warp 0      query rows of each tile into a ring of Q stages (TMA at G = 8: one 4-D box per
+//               entry, its 8 head rows of every 64-dim half; cp.async otherwise)
 //   warp 10     K_b and V_b of each new bucket into one of two K/V stages (TMA, 64-token boxes;
 //               rows past the sequence read as zeros)
 //   warp 1      the MMA issuer: S of tile j, then O of tile j-1, so the tensor pipe computes the
@@ -77,6 +77,16 @@ struct KvoSmem {
 
 __device__ __forceinline__ void kvo_cp_async16(uint32_t dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
+// Byte offset of row R's 128-byte line of 64-dim half `half` in a Q stage (and in the partials'
+// staging, which has the same layout).  At G = 8 an entry's 8 head rows of both halves are two
+// adjacent 1-KB swizzle atoms, so one TMA box moves the entry; otherwise each half is a
+// [128 rows x 64 dims] block.  q_line(8, 0) is the stride between 8-row atoms (the UMMA SBO).
+template <int G, int D_H>
+__device__ __forceinline__ constexpr uint32_t q_line(int R, int half) {
+  return G == 8 ? (uint32_t)((R >> 3) * 1024 * (D_H / 64) + half * 1024 + (R & 7) * 128)
+                : (uint32_t)(half * kRowsT * 128 + R * 128);
 }
 
 __device__ __forceinline__ float rowmax64(const uint32_t* v) {
@@ -245,10 +255,8 @@ __global__ void __launch_bounds__(kThreadsKvo, 1)
         __syncwarp();
         if (lane < n_e) {
           const int i = (int)(q0 + (my_ent >> 6));
-#pragma unroll
-          for (int bx = 0; bx < L::kHalves; ++bx)
-            tma_load_3d(qbase + bx * L::kQHalf + lane * 1024, &tm_q, q_full(s), 64 * bx,
-                        rb * 8, i);
+          // one box: the entry's 8 head rows of both 64-dim halves, as two adjacent atoms
+          tma_load_4d(qbase + lane * 1024 * L::kHalves, &tm_q, q_full(s), 0, rb * 8, 0, i);
         }
       } else {
         __syncwarp();                                       // the previous tile's reads are done
@@ -258,7 +266,7 @@ __global__ void __launch_bounds__(kThreadsKvo, 1)
           const int R = x / kChunks, c = x - R * kChunks;
           const int e = R / G, h = R - e * G;
           const int64_t i = q0 + (s_pent[e] >> 6);
-          const uint32_t off = (c >> 3) * L::kQHalf + R * 128 + (((c & 7) ^ (R & 7)) << 4);
+          const uint32_t off = q_line<G, D_H>(R, c >> 3) + (((c & 7) ^ (R & 7)) << 4);
           kvo_cp_async16(qbase + off, q + (i * H_q + (int64_t)rb * G + h) * D_H + c * 8);
         }
         asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(q_full(s))
@@ -344,10 +352,10 @@ __global__ void __launch_bounds__(kThreadsKvo, 1)
         const uint32_t d = tmem + (uint32_t)(kColS * t);
 #pragma unroll
         for (int ks = 0; ks < D_H / 16; ++ks) {
-          const uint32_t a = qbase + (ks >> 2) * L::kQHalf + (ks & 3) * 32;
+          const uint32_t a = qbase + q_line<G, D_H>(0, ks >> 2) + (ks & 3) * 32;
           const uint32_t bk = kbase + (ks >> 2) * L::kKHalf + (ks & 3) * 32;
-          umma_bf16(d, umma_desc_kmajor(a, 1024, 128), umma_desc_kmajor(bk, 1024, 128), idesc_s,
-                    ks > 0 ? 1u : 0u);
+          umma_bf16(d, umma_desc_kmajor(a, q_line<G, D_H>(8, 0), 128),
+                    umma_desc_kmajor(bk, 1024, 128), idesc_s, ks > 0 ? 1u : 0u);
         }
         umma_commit(s_full(t));
         umma_commit(q_empty(s));                 // P goes to TMEM: the Q stage is free after S
@@ -462,7 +470,7 @@ __global__ void __launch_bounds__(kThreadsKvo, 1)
           if (G == 8) {
             // row R's 16-byte chunk c of this half, at its place in the 128-byte swizzle
             asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(
-                             out + half * L::kQHalf + R * 128 + ((c ^ (R & 7)) << 4)),
+                             out + q_line<G, D_H>(R, half) + ((c ^ (R & 7)) << 4)),
                          "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
                          : "memory");
           } else if (rv) {
@@ -472,16 +480,14 @@ __global__ void __launch_bounds__(kThreadsKvo, 1)
       }
       if (rv) part_lse[slot_pos * G + h] = mx + __log2f(l);
       if (G == 8) {
-        // the group's rows are staged: one thread stores each entry's two halves by TMA
+        // the group's rows are staged: one thread stores each entry (all its halves) by TMA
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         asm volatile("bar.sync %0, 128;" ::"r"(3 + grp) : "memory");
         if (qd == 2 && lane == 0) {
           for (int x = 0; x < n_cur; ++x) {
             const int ex = __ldg(entries + e0_cur + x);
             const int zs = (int)(((int64_t)r * nq + (ex >> 6)) * kk + (ex & 63));
-#pragma unroll
-            for (int half = 0; half < D_H / 64; ++half)
-              tma_store_3d(&tm_p, out + half * L::kQHalf + x * 1024, 64 * half, 0, zs);
+            tma_store_4d(&tm_p, out + x * 1024 * L::kHalves, 0, 0, 0, zs);
           }
           bulk_commit();
           bulk_wait_read_all();                  // the staging buffer is free for the next tile
@@ -510,17 +516,29 @@ cudaError_t launch_attn_kvouter(const void* q, const void* k, const void* v, con
   const float scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)d_h));
   // Q as [N, H_q, d_h]: one box = one query's G heads x 64 dims; K, V as [N, H_kv, d_h]: one box
   // = one group's 64 tokens x 64 dims; 128-byte swizzle
+  // At G = 8 the query box is 4-D, [64 dims, 8 heads, d_h/64 halves, 1 token]: its two halves
+  // land as two adjacent 1-KB atoms (the heads' stride is d_h elements, the halves' 64).
   CUtensorMap tq, tk, tv;
-  cudaError_t e = make_tma_3d_bf16(&tq, q, (uint64_t)d_h, (uint64_t)H_q, (uint64_t)N, 64, G, 1, 128);
+  const uint64_t qdims[4] = {64, (uint64_t)H_q, (uint64_t)d_h / 64, (uint64_t)N};
+  const uint64_t qstr[3] = {(uint64_t)d_h * 2, 128, (uint64_t)H_q * d_h * 2};
+  const int qbox[4] = {64, 8, d_h / 64, 1};
+  cudaError_t e = G == 8 ? make_tma_4d_bf16(&tq, q, qdims, qstr, qbox, 128)
+                         : make_tma_3d_bf16(&tq, q, (uint64_t)d_h, (uint64_t)H_q, (uint64_t)N, 64,
+                                            G, 1, 128);
   if (e != cudaSuccess) return e;
   e = make_tma_3d_bf16(&tk, k, (uint64_t)d_h, (uint64_t)H_kv, (uint64_t)N, 64, 1, 64, 128);
   if (e != cudaSuccess) return e;
   e = make_tma_3d_bf16(&tv, v, (uint64_t)d_h, (uint64_t)H_kv, (uint64_t)N, 64, 1, 64, 128);
   if (e != cudaSuccess) return e;
   // the partials as [H_kv * chunk rows * k slots, G, d_h]: one box = one entry's G heads x 64 dims
+  // (at G = 8 a 4-D box over [64 dims, 8 heads, d_h/64 halves, rows], one store per entry)
   CUtensorMap tp;
-  e = make_tma_3d_bf16(&tp, part_o, (uint64_t)d_h, (uint64_t)G,
-                       (uint64_t)H_kv * (uint64_t)(q1 - q0) * (uint64_t)kk, 64, G, 1, 128);
+  const uint64_t prows = (uint64_t)H_kv * (uint64_t)(q1 - q0) * (uint64_t)kk;
+  const uint64_t pdims[4] = {64, 8, (uint64_t)d_h / 64, prows};
+  const uint64_t pstr[3] = {(uint64_t)d_h * 2, 128, (uint64_t)8 * d_h * 2};
+  const int pbox[4] = {64, 8, d_h / 64, 1};
+  e = G == 8 ? make_tma_4d_bf16(&tp, part_o, pdims, pstr, pbox, 128)
+             : make_tma_3d_bf16(&tp, part_o, (uint64_t)d_h, (uint64_t)G, prows, 64, G, 1, 128);
   if (e != cudaSuccess) return e;
   const auto* qq = static_cast<const __nv_bfloat16*>(q);
   auto* po = static_cast<__nv_bfloat16*>(part_o);

@@ -45,6 +45,10 @@ cudaError_t make_tma_2d_bf16(CUtensorMap* map, const void* base, uint64_t inner,
 // box0 x box1 x box2, swizzle_bytes in {0, 64, 128}.
 cudaError_t make_tma_3d_bf16(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1,
                              uint64_t d2, int box0, int box1, int box2, int swizzle_bytes);
+// 4-D map with explicit byte strides of dims 1..3 (in any order: a box may gather dims whose
+// strides are not increasing, e.g. the two 64-dim halves of G head rows)
+cudaError_t make_tma_4d_bf16(CUtensorMap* map, const void* base, const uint64_t dims[4],
+                             const uint64_t strides[3], const int box[4], int swizzle_bytes);
 
 // Main branch of prefill: workspace bytes and the chunked launch sequence.
 size_t sparse_attn_ws_bytes(int64_t N, int H_q, int H_kv, int d_h, int kk);
