@@ -413,7 +413,8 @@ __global__ void __launch_bounds__(kThreadsKvo, 1)
       float mx = 0.f, l = 0.f;
       {
         uint32_t sv[64];
-        MSA_TMEM_LD64(ts, sv);
+        float lmx;                               // the load's maximum over the 64 keys
+        MSA_TMEM_LDMAX64(ts, sv, lmx);
         tmem_ld_wait();
         if (rv) {
           if (blk == (i >> 6)) {                 // local block: keys j <= i only
@@ -421,8 +422,9 @@ __global__ void __launch_bounds__(kThreadsKvo, 1)
 #pragma unroll
             for (int c = 0; c < 64; ++c)
               if (c > lim) sv[c] = __float_as_uint(-INFINITY);
+            lmx = rowmax64(sv);
           }
-          mx = rowmax64(sv) * scale_log2;
+          mx = lmx * scale_log2;
         }
         uint32_t pk[32];
         float l0 = 0.f, l1 = 0.f;

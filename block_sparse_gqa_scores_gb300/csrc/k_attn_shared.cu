@@ -270,10 +270,10 @@ __global__ void __launch_bounds__(kShThreads, 2)
       const bool okw =
           ok && __all_sync(kAllLanes, mbar_wait(s_full(sbuf), (hb / kSBufs) & 1, &g_shared_status));
       uint32_t sv[16];
-      float pmx = -INFINITY;
+      float pmx = -INFINITY, lmx;
       if (okw) {
         tc_fence_after();
-        MSA_TMEM_LD16(tmem + lanes + 32 * sbuf + 16 * ch, sv);
+        MSA_TMEM_LDMAX16(tmem + lanes + 32 * sbuf + 16 * ch, sv, lmx);
         tmem_ld_wait();
         tc_fence_before();
         __syncwarp();
@@ -284,12 +284,14 @@ __global__ void __launch_bounds__(kShThreads, 2)
 #pragma unroll
             for (int c = 0; c < 16; ++c)
               if (c > lim) sv[c] = __float_as_uint(-INFINITY);
-          }
-          pmx = fmax3(__uint_as_float(sv[0]), __uint_as_float(sv[1]), __uint_as_float(sv[2]));
+            pmx = fmax3(__uint_as_float(sv[0]), __uint_as_float(sv[1]), __uint_as_float(sv[2]));
 #pragma unroll
-          for (int c = 3; c < 15; c += 2)
-            pmx = fmax3(pmx, __uint_as_float(sv[c]), __uint_as_float(sv[c + 1]));
-          pmx = fmaxf(pmx, __uint_as_float(sv[15]));
+            for (int c = 3; c < 15; c += 2)
+              pmx = fmax3(pmx, __uint_as_float(sv[c]), __uint_as_float(sv[c + 1]));
+            pmx = fmaxf(pmx, __uint_as_float(sv[15]));
+          } else {
+            pmx = lmx;                                // every key visible: the load's maximum
+          }
         }
       }
       s_xm[((hb & 1) * 2 + ch) * 128 + R] = pmx;

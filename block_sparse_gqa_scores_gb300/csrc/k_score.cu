@@ -9,9 +9,10 @@
 //   * K_idx tiles of 128 keys (two 64-token blocks) stream through a 4-deep TMA ring.
 //   * one thread issues tcgen05.mma (bf16 x bf16 -> fp32) into a double-buffered TMEM
 //     accumulator; the next tile's MMA overlaps the epilogue of the previous one.
-//   * epilogue warps tcgen05.ld 64 columns (= one block) per row, mask j > i on the
-//     diagonal block, max-reduce with 3-input max, scale once, and stage 32 blocks per row
-//     in shared memory before one coalesced 128-byte store per row.
+//   * epilogue warps read 64 columns (= one block) per row with tcgen05.ld.red, which also
+//     returns the row's maximum over them (the diagonal block masks j > i and reduces in
+//     registers), scale once, and stage 32 blocks per row in shared memory before one
+//     coalesced 128-byte store per row.
 //   * blocks after a row's own block are written as -inf.
 // Warp roles: warp 0 = TMA producer, warp 1 = TMEM allocator + MMA issuer,
 // warps 2.. = 4*SUB epilogue warps (warp w reads TMEM lanes 32*(w%4) .. +31); with the select
@@ -385,11 +386,12 @@ __global__ void __launch_bounds__(ScoreSmem<D_IDX, SUB, CAP>::kThreads, 1)
           const int64_t b = 2 * (int64_t)kt + h;
           if (!__any_sync(0xffffffffu, b < l)) continue;   // no row of the warp needs it
           uint32_t v[64];
+          float mx;
           const uint32_t taddr = tmem_base + ((uint32_t)(32 * q) << 16) +
                                  (uint32_t)((acc * SUB + s) * kKeys + 64 * h);
-          MSA_TMEM_LD64(taddr, v);
+          MSA_TMEM_LDMAX64(taddr, v, mx);
           tmem_ld_wait();
-          if (b < l) m[h] = max64(v) * scale;
+          if (b < l) m[h] = mx * scale;
         }
         tc_fence_before();
         __syncwarp();
@@ -425,11 +427,12 @@ __global__ void __launch_bounds__(ScoreSmem<D_IDX, SUB, CAP>::kThreads, 1)
           const int64_t b = 2 * (int64_t)kt + h;
           if (!__any_sync(0xffffffffu, b < l)) continue;   // no row of the warp needs it
           uint32_t v[64];
+          float mx;
           const uint32_t taddr = tmem_base + ((uint32_t)(32 * q) << 16) +
                                  (uint32_t)((acc * SUB + s) * kKeys + 64 * h);
-          MSA_TMEM_LD64(taddr, v);
+          MSA_TMEM_LDMAX64(taddr, v, mx);
           tmem_ld_wait();
-          if (b < l) offer_block<CAP>(sc, bl, cnt, tau, b, l, max64(v) * scale);
+          if (b < l) offer_block<CAP>(sc, bl, cnt, tau, b, l, mx * scale);
         }
         tc_fence_before();
         __syncwarp();
@@ -475,13 +478,14 @@ __global__ void __launch_bounds__(ScoreSmem<D_IDX, SUB, CAP>::kThreads, 1)
         for (int h = 0; h < 2; ++h) {
           const int64_t b = 2 * (int64_t)kt + h;
           uint32_t v[64];
+          float mx;
           const uint32_t taddr = tmem_base + ((uint32_t)(32 * q) << 16) +
                                  (uint32_t)((acc * SUB + s) * kKeys + 64 * h);
-          MSA_TMEM_LD64(taddr, v);
+          MSA_TMEM_LDMAX64(taddr, v, mx);
           tmem_ld_wait();
           float m = ninf;
           if (b < l) {
-            m = max64(v) * scale;
+            m = mx * scale;
           } else if (b == l) {                              // diagonal block: keys j <= i only
             const int lim = (int)(i - 64 * b);
   #pragma unroll
