@@ -381,17 +381,21 @@ __global__ void __launch_bounds__(ScoreSmem<D_IDX, SUB, CAP>::kThreads, 1)
         if (!__all_sync(0xffffffffu, mbar_wait(tfull(acc), use & 1, &g_score_status, lim))) break;
         tc_fence_after();
         float m[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int64_t b = 2 * (int64_t)kt + h;
-          if (!__any_sync(0xffffffffu, b < l)) continue;   // no row of the warp needs it
+        {
+          // both blocks' loads in flight at once; only their maxima are used, so the two share
+          // one (dead) destination vector
+          const int64_t b0 = 2 * (int64_t)kt;
+          const bool need0 = __any_sync(0xffffffffu, b0 < l);
+          const bool need1 = __any_sync(0xffffffffu, b0 + 1 < l);
           uint32_t v[64];
-          float mx;
+          float mx0 = -INFINITY, mx1 = -INFINITY;
           const uint32_t taddr = tmem_base + ((uint32_t)(32 * q) << 16) +
-                                 (uint32_t)((acc * SUB + s) * kKeys + 64 * h);
-          MSA_TMEM_LDMAX64(taddr, v, mx);
+                                 (uint32_t)((acc * SUB + s) * kKeys);
+          if (need0) MSA_TMEM_LDMAX64(taddr, v, mx0);
+          if (need1) MSA_TMEM_LDMAX64(taddr + 64, v, mx1);
           tmem_ld_wait();
-          if (b < l) m[h] = mx * scale;
+          if (b0 < l) m[0] = mx0 * scale;
+          if (b0 + 1 < l) m[1] = mx1 * scale;
         }
         tc_fence_before();
         __syncwarp();
