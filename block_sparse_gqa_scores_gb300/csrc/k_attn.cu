@@ -27,6 +27,9 @@ namespace msa {
 namespace {
 
 constexpr int kTailWarps = 16;                 // 4 quads of 4 warps
+// rows of at most this many candidate blocks (a 512K-token cache) are copied to shared memory
+// before the selection, with every load in flight at once
+constexpr int kRowCap = 8192;
 constexpr int kQuads = kTailWarps / 4;
 constexpr unsigned kFull = 0xffffffffu;
 
@@ -37,7 +40,10 @@ struct TailSmem {
   float m[kTailWarps][8];
   float l[kTailWarps][8];
   union {                                       // selection scratch, then the warps' O states
-    sel::SelScratch sc[kTailWarps];
+    struct {
+      sel::SelScratch sc[kTailWarps];
+      float row[kRowCap];                       // the row's block scores
+    } s;
     float o[kTailWarps][8][D_H];
   } u;
 };
@@ -94,9 +100,30 @@ __global__ void __launch_bounds__(32 * kTailWarps) k_decode_tail(const AttnParam
       int nseg = sel::kBuf / K1;
       nseg = nseg > kTailWarps ? kTailWarps : (nseg < 1 ? 1 : nseg);
       const int seg = (n + nseg - 1) / nseg;
+      // the row's scores into shared memory, all loads of a thread issued together (the
+      // segment passes below then read shared memory instead of one L2 round trip per step)
+      const bool staged = n <= kRowCap;
+      if (staged) {
+        constexpr int kPer = kRowCap / (32 * kTailWarps);
+        float v[kPer];
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {
+          const int x = threadIdx.x + u * 32 * kTailWarps;
+          v[u] = x < n ? __ldg(Mrow + x) : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {
+          const int x = threadIdx.x + u * 32 * kTailWarps;
+          if (x < n) sm.u.s.row[x] = v[u];
+        }
+        __syncthreads();
+      }
       if (warp < nseg) {
         const int b0 = min(n, warp * seg), b1 = min(n, b0 + seg);
-        const int cnt = b1 > b0 ? sel::select_segment(Mrow, b0, b1, K1, sm.u.sc[warp]) : 0;
+        int cnt = 0;
+        if (b1 > b0)
+          cnt = staged ? sel::select_segment<true>(sm.u.s.row, b0, b1, K1, sm.u.s.sc[warp])
+                       : sel::select_segment(Mrow, b0, b1, K1, sm.u.s.sc[warp]);
         if (lane == 0) sm.cnt[warp] = cnt;
       }
       __syncthreads();
@@ -106,17 +133,17 @@ __global__ void __launch_bounds__(32 * kTailWarps) k_decode_tail(const AttnParam
         for (int w = 1; w < nseg; ++w) {
           const int cw = sm.cnt[w];
           for (int x = lane; x < cw; x += 32) {
-            sm.u.sc[0].v[cnt + x] = sm.u.sc[w].v[x];
-            sm.u.sc[0].b[cnt + x] = sm.u.sc[w].b[x];
+            sm.u.s.sc[0].v[cnt + x] = sm.u.s.sc[w].v[x];
+            sm.u.s.sc[0].b[cnt + x] = sm.u.s.sc[w].b[x];
           }
           cnt += cw;
         }
         __syncwarp();
         if (cnt > K1) {
-          sel::compact(sm.u.sc[0], cnt, K1);
+          sel::compact(sm.u.s.sc[0], cnt, K1);
           cnt = K1;
         }
-        for (int x = lane; x < K1; x += 32) sm.blocks[x] = x < cnt ? sm.u.sc[0].b[x] : -1;
+        for (int x = lane; x < K1; x += 32) sm.blocks[x] = x < cnt ? sm.u.s.sc[0].b[x] : -1;
         if (lane == 0) sm.blocks[K1] = (int32_t)l;
       }
     }

@@ -87,13 +87,16 @@ __device__ __forceinline__ float compact(SelScratch& sc, int cnt, int K1) {
 }
 
 // The K1 best of blocks [b0, b1) of a row (score desc, block asc), left in sc.v / sc.b in block
-// order; returns how many (min(K1, b1 - b0)).  Whole warp.
+// order; returns how many (min(K1, b1 - b0)).  Whole warp.  SMEM: the row is a copy in shared
+// memory (plain loads), else in global memory (read-only loads).
+template <bool SMEM = false>
 static __device__ int select_segment(const float* __restrict__ Mrow, int b0, int b1, int K1,
                               SelScratch& sc) {
   const int lane = threadIdx.x & 31;
+  auto at = [&](int b) -> float { return SMEM ? Mrow[b] : __ldg(Mrow + b); };
   float a1 = -INFINITY, a2 = -INFINITY;
   for (int b = b0 + lane; b < b1; b += 32) {
-    const float v = __ldg(Mrow + b);
+    const float v = at(b);
     if (v > a1) {
       a2 = a1;
       a1 = v;
@@ -107,7 +110,7 @@ static __device__ int select_segment(const float* __restrict__ Mrow, int b0, int
   int cnt = 0;
   for (int base = b0; base < b1; base += 32) {
     const int b = base + lane;
-    const float v = b < b1 ? __ldg(Mrow + b) : -INFINITY;
+    const float v = b < b1 ? at(b) : -INFINITY;
     bool pred = b < b1 && (strict ? v > tau : v >= tau);
     unsigned m = __ballot_sync(kFull, pred);
     if (cnt + __popc(m) > kBuf) {
