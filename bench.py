@@ -144,15 +144,20 @@ def write_traffic(csv_path, command, scale=1.0, only=None, tag="A"):
     processes).  Rows not in `only` keep their previous lines."""
     import csv
     import collections
-    rows = list(csv.reader(l for l in open(csv_path) if not l.startswith("==")))
-    hdr = rows[0]
-    ki, mi, vi, ui = (hdr.index(c) for c in ("Kernel Name", "Metric Name", "Metric Value",
-                                              "Metric Unit"))
     unit = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9}
     tot = collections.defaultdict(float)
     calls = collections.Counter()      # KL / backward rows: calls counted by their main launch
     firsts = collections.Counter()     # launches of the first kernel of a step
-    for r in rows[1:]:
+    # several CSVs (comma-separated paths) add up: e.g. one capture per kernel of the same step
+    recs = []
+    for path in csv_path.split(","):
+        rows = list(csv.reader(l for l in open(path) if not l.startswith("==")))
+        hdr = rows[0]
+        ki, mi, vi, ui = (hdr.index(c) for c in ("Kernel Name", "Metric Name", "Metric Value",
+                                                  "Metric Unit"))
+        recs += [(r[ki], r[mi], r[vi], r[ui]) for r in rows[1:]]
+    ki, mi, vi, ui = 0, 1, 2, 3
+    for r in recs:
         raw = r[ki].split("(")[0]
         name = raw.split("<")[0].split("::")[-1].split()[-1]   # bare kernel name
         if name not in NCU_ROWS:
@@ -877,7 +882,8 @@ def main():
                     help="skip the 32K and 1M prefill measurements")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--write-traffic", metavar="NCU_CSV",
-                    help="write profiles/traffic.txt from an ncu CSV of whole steps and exit")
+                    help="write profiles/traffic.txt from ncu CSVs (comma-separated) that "
+                         "together cover whole steps, and exit")
     ap.add_argument("--traffic-command", default="",
                     help="the command the ncu CSV was captured on (recorded in the file)")
     ap.add_argument("--traffic-scale", type=float, default=1.0,
