@@ -151,7 +151,9 @@ def write_traffic(csv_path, command, scale=1.0, only=None, tag="A"):
     # several CSVs (comma-separated paths) add up: e.g. one capture per kernel of the same step
     recs = []
     for path in csv_path.split(","):
-        rows = list(csv.reader(l for l in open(path) if not l.startswith("==")))
+        # ncu's CSV rows all start with a quote; its "==" messages and the program's own output
+        # (when ncu writes to stdout) are skipped
+        rows = list(csv.reader(l for l in open(path) if l.startswith('"')))
         hdr = rows[0]
         ki, mi, vi, ui = (hdr.index(c) for c in ("Kernel Name", "Metric Name", "Metric Value",
                                                   "Metric Unit"))
@@ -191,12 +193,15 @@ def write_traffic(csv_path, command, scale=1.0, only=None, tag="A"):
                                        kernel_source_hash(KERNEL_FILES[k]), tag)
             wrote.append(k)
     notes = [x for x in notes if not x.startswith("# capture %s:" % tag)]
+    used = {line.split()[3] for line in keep.values() if len(line.split()) >= 4} | {tag}
+    notes = [x for x in notes if x.split(":")[0].split()[-1] in used]
     notes.append("# capture %s: %s (rows %s, %d steps, bytes x %g)" % (
         tag, command, ",".join(wrote), steps, scale))
     with open(TRAFFIC_FILE, "w") as f:
         f.write("# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per call of each bench\n"
-                "# row, from ncu captures of whole bench steps (one pass, cold cache); a capture of\n"
-                "# a smaller case is scaled to the bench workload by the query rows it processes.\n")
+                "# row, from ncu captures (cold cache) of whole bench steps or of each kernel of one\n"
+                "# step; a capture of a smaller case is scaled to the bench workload by the units it\n"
+                "# processes (query rows, or the decode batch's algorithmic bytes).\n")
         for n_ in sorted(notes):
             f.write(n_ + "\n")
         f.write("# row  bytes_per_call  source_sha  capture\n")
