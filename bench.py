@@ -716,8 +716,11 @@ def e2e_prefill(msa, pcfg, x, bufs, K, W, world):
     host, all inside the timed region.  The steps are pipelined as a serving loop would run
     them: two device buffer sets, the host -> device copies on one stream and the device -> host
     reads on another, so step s+1's inputs and step s-1's results move while step s computes
-    (each stream's order and the events keep every copy after the step it belongs to)."""
-    names = ["q", "k", "v", "q_idx", "k_idx"]
+    (each stream's order and the events keep every copy after the step it belongs to).  Q_idx
+    and K_idx are copied first and the index branch waits only for them, so in the first step
+    the Q, K and V copies run under the index branch."""
+    # the index branch's inputs first: it starts on them while Q, K and V are still copying
+    names = ["q_idx", "k_idx", "q", "k", "v"]
     host = {n: torch.empty(x[n].shape, dtype=x[n].dtype, pin_memory=True) for n in names}
     for n in names:
         host[n].copy_(x[n])
@@ -729,7 +732,8 @@ def e2e_prefill(msa, pcfg, x, bufs, K, W, world):
     comp = torch.cuda.current_stream()
     h2d_s, d2h_s = torch.cuda.Stream(), torch.cuda.Stream()
     ev = lambda: torch.cuda.Event()
-    in_ready = [ev(), ev()]      # inputs of the buffer set copied
+    idx_ready = [ev(), ev()]     # Q_idx and K_idx of the buffer set copied
+    in_ready = [ev(), ev()]      # Q, K and V of the buffer set copied
     in_free = [ev(), ev()]       # the step that read the buffer set's inputs is done
     out_ready = [ev(), ev()]     # the step's outputs written
     out_free = [ev(), ev()]      # the outputs read back to the host
@@ -742,11 +746,14 @@ def e2e_prefill(msa, pcfg, x, bufs, K, W, world):
                 h2d_s.wait_event(in_free[j])
             for n in names:
                 dev[j][n].copy_(host[n], non_blocking=True)
+                if n == "k_idx":
+                    idx_ready[j].record(h2d_s)
             in_ready[j].record(h2d_s)
-        comp.wait_event(in_ready[j])
+        comp.wait_event(idx_ready[j])
         if started[j]:
             comp.wait_event(out_free[j])
         idx = msa.msa_index_select(dev[j]["q_idx"], dev[j]["k_idx"], pcfg.k, idx=bufs["idx"])
+        comp.wait_event(in_ready[j])
         msa.msa_sparse_attn_fwd(dev[j]["q"], dev[j]["k"], dev[j]["v"], idx, o=outs[j][0],
                                 lse=outs[j][1], ws=bufs["ws"])
         in_free[j].record(comp)
