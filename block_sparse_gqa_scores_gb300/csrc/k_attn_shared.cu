@@ -52,10 +52,9 @@ struct ShSmem {
   static constexpr int kNumBars = 2 * kRing + 2 * kSBufs + 6;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kOffPriv = kOffMisc + 16;    // per query: its private slots (bit t)
-  // the two softmax warps of a lane quarter exchange per-row values: half-block maxima
-  // (double-buffered by half-block parity), the halves of the row sum, the O weight
-  static constexpr int kOffXm = kOffPriv + kTileQ * 8;
-  static constexpr int kOffLh = kOffXm + 2 * 2 * 128 * 4;
+  // the two softmax warps of a lane quarter exchange per-row values: the halves of the row
+  // sum, the O weight
+  static constexpr int kOffLh = kOffPriv + kTileQ * 8;
   static constexpr int kOffCo = kOffLh + 2 * 128 * 4;
   static constexpr int kBytes = kOffCo + 128 * 4;
   static constexpr int kAlloc = kBytes + 1024;
@@ -245,8 +244,10 @@ __global__ void __launch_bounds__(kShThreads, 2)
   } else {
     // ------------------------------------------------------ softmax and epilogue
     // warps 2..9, two per TMEM lane quarter: half ch takes keys [16 ch, 16 ch + 16) of every
-    // half block and columns [ch d_h / 2, (ch + 1) d_h / 2) of O; the pair exchanges row maxima
-    // and sums through shared memory at its own named barrier
+    // half block and columns [ch d_h / 2, (ch + 1) d_h / 2) of O.  Both warps of a pair read
+    // all 32 keys' maximum from TMEM (tcgen05.ld.red on each half), so they take the same
+    // reference-max decisions without exchanging anything; they add their halves of the row sum
+    // through shared memory at the end
     const int qd = warp & 3;                          // TMEM lane quarter
     const int ch = (warp - 2) >> 2;
     const int pair = 1 + qd;                          // named barrier id of the quarter's pair
@@ -255,13 +256,12 @@ __global__ void __launch_bounds__(kShThreads, 2)
     const int64_t i = i0 + w;
     const bool valid = R < rows && i < q1;
     const uint32_t lanes = (uint32_t)(32 * qd) << 16;
-    float* s_xm = reinterpret_cast<float*>(smem + L::kOffXm);
     float* s_lh = reinterpret_cast<float*>(smem + L::kOffLh);
     float* s_co = reinterpret_cast<float*>(smem + L::kOffCo);
     float m_ref = -INFINITY, l = 0.f;                 // l: this half's share of the row sum
     bool ok = true;
-    // No warp leaves the loop except at the pair barrier, which both reach every half block:
-    // a failed wait is carried in `ok` to the next one, where both see it.
+    // A warp leaves the loop at its own failed (bounded) wait; its partner then fails at one of
+    // its next waits, and the pair agrees again at the epilogue's reducing barrier.
     for (int hb = 0; hb < nH; ++hb) {
       const int ent = s_list[hb >> 1];
       const int64_t b = ent >> 16;
@@ -269,39 +269,40 @@ __global__ void __launch_bounds__(kShThreads, 2)
       const int buf = hb & 1, sbuf = hb % kSBufs;          // P buffer, S buffer
       const bool okw =
           ok && __all_sync(kAllLanes, mbar_wait(s_full(sbuf), (hb / kSBufs) & 1, &g_shared_status));
-      uint32_t sv[16];
-      float pmx = -INFINITY, lmx;
+      uint32_t sv[16], so[16];                        // this half's keys; the other half's
+      float pmx = -INFINITY, lmx, omx;                // pmx: the row max over all 32 keys
       if (okw) {
         tc_fence_after();
         MSA_TMEM_LDMAX16(tmem + lanes + 32 * sbuf + 16 * ch, sv, lmx);
+        MSA_TMEM_LDMAX16(tmem + lanes + 32 * sbuf + 16 * (ch ^ 1), so, omx);
         tmem_ld_wait();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(s_free(sbuf));
         if (sel) {
           if (b == (i >> 6)) {                        // local block: keys j <= i only
-            const int lim = (int)(i - (b * kBlock + (hb & 1) * kHalfTok)) - 16 * ch;
+            const int lim = (int)(i - (b * kBlock + (hb & 1) * kHalfTok));
 #pragma unroll
-            for (int c = 0; c < 16; ++c)
-              if (c > lim) sv[c] = __float_as_uint(-INFINITY);
-            pmx = fmax3(__uint_as_float(sv[0]), __uint_as_float(sv[1]), __uint_as_float(sv[2]));
+            for (int c = 0; c < 16; ++c) {
+              if (16 * ch + c > lim) sv[c] = __float_as_uint(-INFINITY);
+              if (16 * (ch ^ 1) + c > lim) so[c] = __float_as_uint(-INFINITY);
+            }
+            pmx = fmax3(__uint_as_float(sv[0]), __uint_as_float(so[0]), __uint_as_float(sv[1]));
 #pragma unroll
-            for (int c = 3; c < 15; c += 2)
-              pmx = fmax3(pmx, __uint_as_float(sv[c]), __uint_as_float(sv[c + 1]));
-            pmx = fmaxf(pmx, __uint_as_float(sv[15]));
+            for (int c = 1; c < 15; ++c)
+              pmx = fmax3(pmx, __uint_as_float(so[c]), __uint_as_float(sv[c + 1]));
+            pmx = fmaxf(pmx, __uint_as_float(so[15]));
           } else {
-            pmx = lmx;                                // every key visible: the load's maximum
+            pmx = fmaxf(lmx, omx);                    // every key visible: the loads' maxima
           }
         }
       }
-      s_xm[((hb & 1) * 2 + ch) * 128 + R] = pmx;
-      ok = pair_and(pair, okw);
+      ok = okw;
       if (!ok) break;
       float alpha = 1.f;
       uint32_t pk[8];
       if (sel) {
-        const float bm =
-            fmaxf(s_xm[(hb & 1) * 256 + R], s_xm[(hb & 1) * 256 + 128 + R]) * scale_log2;
+        const float bm = pmx * scale_log2;
         if (m_ref == -INFINITY) {
           m_ref = bm;                                 // this row's O and l are still zero
         } else if (bm > m_ref + 8.f) {
