@@ -10,8 +10,11 @@
 //   warp 1   allocates TMEM and issues  S[b] = Q K^T  (M=128, N=32) and  O += P V  (M=128,
 //            N=d_h, P read from TMEM, V as an MN-major operand); S is triple- and P
 //            double-buffered, so QK^T runs two half blocks ahead of the softmax;
-//   warps 2-5 own one row each (TMEM lane): they load Q, read S rows, mask queries that did not
-//            select the block and keys after the query, and write P (bf16) back to TMEM.
+//   warps 2-9 two per TMEM lane quarter, one row per thread: warp half ch takes keys
+//            [16 ch, 16 ch + 16) of every half block and columns [ch d_h/2, (ch+1) d_h/2) of O;
+//            they read S (each warp its own 16 keys and the other half's maximum, so the pair
+//            needs no exchange), mask queries that did not select the block and keys after the
+//            query, and write P (bf16) back to TMEM; then all ten warps run the epilogue.
 // Online softmax with a lazily moved reference max: a row's reference m moves only when a block
 // max exceeds it by more than 2^8, so P <= 2^8 and O (in TMEM) is rescaled only then.  The
 // result is exact either way -- O/l and m + log2 l use the same reference.
