@@ -36,6 +36,7 @@ constexpr unsigned kFull = 0xffffffffu;
 template <int D_H>
 struct TailSmem {
   int cnt[kTailWarps];
+  float tau[kTailWarps];                        // the segments' bounds on the (k-1)-th best
   int blocks[64];                               // the row's selection (ascending, -1 padded)
   float m[kTailWarps][8];
   float l[kTailWarps][8];
@@ -118,12 +119,25 @@ __global__ void __launch_bounds__(32 * kTailWarps) k_decode_tail(const AttnParam
         }
         __syncthreads();
       }
+      // every segment's bound is a bound for the whole row: the largest of them lets each
+      // segment keep only the blocks that can still be among the row's k-1 best, so warp 0
+      // merges a few dozen candidates instead of k-1 per segment
+      const int b0 = min(n, warp * seg), b1 = min(n, b0 + seg);
       if (warp < nseg) {
-        const int b0 = min(n, warp * seg), b1 = min(n, b0 + seg);
+        const float t = b1 > b0 ? (staged ? sel::segment_bound<true>(sm.u.s.row, b0, b1, K1)
+                                          : sel::segment_bound(Mrow, b0, b1, K1))
+                                : -INFINITY;
+        if (lane == 0) sm.tau[warp] = t;
+      }
+      __syncthreads();
+      float tg = -INFINITY;
+      for (int x = 0; x < nseg; ++x) tg = fmaxf(tg, sm.tau[x]);
+      if (warp < nseg) {
         int cnt = 0;
         if (b1 > b0)
-          cnt = staged ? sel::select_segment<true>(sm.u.s.row, b0, b1, K1, sm.u.s.sc[warp])
-                       : sel::select_segment(Mrow, b0, b1, K1, sm.u.s.sc[warp]);
+          cnt = staged
+                    ? sel::select_segment_from<true>(sm.u.s.row, b0, b1, K1, tg, sm.u.s.sc[warp])
+                    : sel::select_segment_from(Mrow, b0, b1, K1, tg, sm.u.s.sc[warp]);
         if (lane == 0) sm.cnt[warp] = cnt;
       }
       __syncthreads();

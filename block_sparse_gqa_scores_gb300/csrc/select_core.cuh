@@ -86,17 +86,16 @@ __device__ __forceinline__ float compact(SelScratch& sc, int cnt, int K1) {
   return tau;
 }
 
-// The K1 best of blocks [b0, b1) of a row (score desc, block asc), left in sc.v / sc.b in block
-// order; returns how many (min(K1, b1 - b0)).  Whole warp.  SMEM: the row is a copy in shared
-// memory (plain loads), else in global memory (read-only loads).
+// A lower bound on the K1-th best score of blocks [b0, b1) of a row: the K1-th largest of every
+// lane's two best, all of them scores of the segment; -inf when the segment has at most K1
+// blocks.  Whole warp.  SMEM: the row is a copy in shared memory (plain loads), else in global
+// memory (read-only loads).
 template <bool SMEM = false>
-static __device__ int select_segment(const float* __restrict__ Mrow, int b0, int b1, int K1,
-                              SelScratch& sc) {
+static __device__ float segment_bound(const float* __restrict__ Mrow, int b0, int b1, int K1) {
   const int lane = threadIdx.x & 31;
-  auto at = [&](int b) -> float { return SMEM ? Mrow[b] : __ldg(Mrow + b); };
   float a1 = -INFINITY, a2 = -INFINITY;
   for (int b = b0 + lane; b < b1; b += 32) {
-    const float v = at(b);
+    const float v = SMEM ? Mrow[b] : __ldg(Mrow + b);
     if (v > a1) {
       a2 = a1;
       a1 = v;
@@ -104,13 +103,22 @@ static __device__ int select_segment(const float* __restrict__ Mrow, int b0, int
       a2 = v;
     }
   }
-  // fewer than K1 candidates: the bound is -inf and every block is kept
-  float tau = b1 - b0 > K1 ? kth_largest64(a1, a2, K1) : -INFINITY;
+  return b1 - b0 > K1 ? kth_largest64(a1, a2, K1) : -INFINITY;
+}
+
+// The K1 best (score desc, block asc) of the blocks of [b0, b1) that score at least tau0, left
+// in sc.v / sc.b in block order; returns how many.  tau0 must not exceed the K1-th best score of
+// the whole row, so that the row's K1 best blocks in this segment all pass.  Whole warp.
+template <bool SMEM = false>
+static __device__ int select_segment_from(const float* __restrict__ Mrow, int b0, int b1, int K1,
+                                          float tau0, SelScratch& sc) {
+  const int lane = threadIdx.x & 31;
+  float tau = tau0;
   bool strict = false;
   int cnt = 0;
   for (int base = b0; base < b1; base += 32) {
     const int b = base + lane;
-    const float v = b < b1 ? at(b) : -INFINITY;
+    const float v = b < b1 ? (SMEM ? Mrow[b] : __ldg(Mrow + b)) : -INFINITY;
     bool pred = b < b1 && (strict ? v > tau : v >= tau);
     unsigned m = __ballot_sync(kFull, pred);
     if (cnt + __popc(m) > kBuf) {
@@ -133,6 +141,14 @@ static __device__ int select_segment(const float* __restrict__ Mrow, int b0, int
     cnt = K1;
   }
   return cnt;
+}
+
+// The K1 best of blocks [b0, b1) of a row (score desc, block asc), left in sc.v / sc.b in block
+// order; returns how many (min(K1, b1 - b0)).  Whole warp.
+template <bool SMEM = false>
+static __device__ int select_segment(const float* __restrict__ Mrow, int b0, int b1, int K1,
+                              SelScratch& sc) {
+  return select_segment_from<SMEM>(Mrow, b0, b1, K1, segment_bound<SMEM>(Mrow, b0, b1, K1), sc);
 }
 
 }  // namespace sel
