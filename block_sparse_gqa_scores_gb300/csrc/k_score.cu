@@ -5,8 +5,11 @@
 // One dense GEMM  [N*H_kv x d_idx] . [d_idx x N]  restricted to the causal triangle:
 //   * rows are (query i, group r) pairs, i.e. Q_idx viewed as [N*H_kv, d_idx]; 128 consecutive
 //     rows (128/H_kv queries x H_kv groups) form one UMMA M=128 sub-tile, and SUB sub-tiles
-//     share every K_idx tile, so the shared index key is read once for all groups.
-//   * K_idx tiles of 128 keys (two 64-token blocks) stream through a 4-deep TMA ring.
+//     share every K_idx tile, so the shared index key is read once for all groups.  The select
+//     epilogue at k <= 16 runs one sub-tile per CTA and two CTAs per SM, so one CTA's MMAs run
+//     while the other's epilogue drains its accumulators; the other variants run two sub-tiles
+//     in one CTA per SM.
+//   * K_idx tiles of 128 keys (two 64-token blocks) stream through a TMA ring (3 to 6 stages).
 //   * one thread issues tcgen05.mma (bf16 x bf16 -> fp32) into a double-buffered TMEM
 //     accumulator; the next tile's MMA overlaps the epilogue of the previous one.
 //   * epilogue warps read 64 columns (= one block) per row with tcgen05.ld.red, which also
@@ -64,8 +67,11 @@ struct ScoreSmem {
   static constexpr int kABytes = kRows * D_IDX * 2;
   static constexpr int kBBytes = kKeys * D_IDX * 2;
   // K_idx ring depth: six stages keep about two microseconds of key tiles in flight; the
-  // k <= 32 candidate buffers (CAP = 56) leave room for four
-  static constexpr int kStages = SELECT && CAP > 32 ? 4 : 6;
+  // k <= 32 candidate buffers (CAP = 56) leave room for four.  One sub-tile (SUB = 1: 128 rows,
+  // 256 TMEM columns, about 107 KB) runs two CTAs per SM with three stages each: one CTA's MMAs
+  // run while the other's epilogue drains its accumulators.
+  static constexpr int kStages = SUB == 1 ? 3 : (SELECT && CAP > 32 ? 4 : 6);
+  static constexpr int kCtasPerSm = SUB == 1 ? 2 : 1;
   static constexpr int kEpiWarps = 4 * SUB;
   static constexpr int kStageFloats = 32 * 33;        // 32 rows x 32 blocks, padded
   static constexpr int kOffA = 0;
@@ -214,7 +220,8 @@ __device__ __forceinline__ void write_selection(float* sc, int* bl, int cnt, int
 }
 
 template <int D_IDX, int SUB, int CAP>
-__global__ void __launch_bounds__(ScoreSmem<D_IDX, SUB, CAP>::kThreads, 1)
+__global__ void __launch_bounds__(ScoreSmem<D_IDX, SUB, CAP>::kThreads,
+                                  ScoreSmem<D_IDX, SUB, CAP>::kCtasPerSm)
     k_index_block_scores(const __grid_constant__ CUtensorMap tm_q,
                          const __grid_constant__ CUtensorMap tm_k, float* __restrict__ M,
                          int32_t* __restrict__ idx, int kk, int64_t N, int log2_hkv,
@@ -558,11 +565,13 @@ static cudaError_t launch_index(const void* q_idx, const void* k_idx, float* M, 
   e = make_tma_2d_bf16(&tk, k_idx, (uint64_t)d_idx, (uint64_t)N, d_idx, kKeys, swz);
   if (e != cudaSuccess) return e;
   const int64_t nblk = (N + kBlock - 1) / kBlock;
-#define MSA_SCORES(D, CAP) \
-  launch_scores<D, 2, CAP>(tq, tk, M, idx, kk, N, H_kv, q_start, q_count, nblk, ktab, stream)
-  if (idx != nullptr && kk <= 16) return d_idx == 64 ? MSA_SCORES(64, 32) : MSA_SCORES(32, 32);
-  if (idx != nullptr) return d_idx == 64 ? MSA_SCORES(64, 56) : MSA_SCORES(32, 56);
-  return d_idx == 64 ? MSA_SCORES(64, 0) : MSA_SCORES(32, 0);
+#define MSA_SCORES(D, SUB, CAP) \
+  launch_scores<D, SUB, CAP>(tq, tk, M, idx, kk, N, H_kv, q_start, q_count, nblk, ktab, stream)
+  // k <= 16: one sub-tile per CTA, two CTAs per SM (3.53 -> 3.11 ms at 128K); k <= 32 keeps two
+  // sub-tiles per CTA (its compaction takes 168 registers, too many for two CTAs per SM)
+  if (idx != nullptr && kk <= 16) return d_idx == 64 ? MSA_SCORES(64, 1, 32) : MSA_SCORES(32, 1, 32);
+  if (idx != nullptr) return d_idx == 64 ? MSA_SCORES(64, 2, 56) : MSA_SCORES(32, 2, 56);
+  return d_idx == 64 ? MSA_SCORES(64, 2, 0) : MSA_SCORES(32, 2, 0);
 #undef MSA_SCORES
 }
 
@@ -580,6 +589,7 @@ cudaError_t launch_index_select(const void* q_idx, const void* k_idx, int32_t* i
                       stream);
 }
 
+// the most query rows one CTA covers, over every instantiation above (two sub-tiles)
 int index_rows_per_cta(int H_kv) { return 2 * (kRows / H_kv); }
 
 cudaError_t set_score_wait_limit(unsigned long long ns) {
