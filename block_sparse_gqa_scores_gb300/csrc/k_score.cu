@@ -5,10 +5,10 @@
 // One dense GEMM  [N*H_kv x d_idx] . [d_idx x N]  restricted to the causal triangle:
 //   * rows are (query i, group r) pairs, i.e. Q_idx viewed as [N*H_kv, d_idx]; 128 consecutive
 //     rows (128/H_kv queries x H_kv groups) form one UMMA M=128 sub-tile, and SUB sub-tiles
-//     share every K_idx tile, so the shared index key is read once for all groups.  The select
-//     epilogue at k <= 16 runs one sub-tile per CTA and two CTAs per SM, so one CTA's MMAs run
-//     while the other's epilogue drains its accumulators; the other variants run two sub-tiles
-//     in one CTA per SM.
+//     share every K_idx tile, so the shared index key is read once for all groups.  The plain
+//     block scores and the select epilogue at k <= 16 run one sub-tile per CTA and two CTAs per
+//     SM, so one CTA's MMAs run while the other's epilogue drains its accumulators; the k <= 32
+//     select epilogue runs two sub-tiles in one CTA per SM.
 //   * K_idx tiles of 128 keys (two 64-token blocks) stream through a TMA ring (3 to 6 stages).
 //   * one thread issues tcgen05.mma (bf16 x bf16 -> fp32) into a double-buffered TMEM
 //     accumulator; the next tile's MMA overlaps the epilogue of the previous one.
@@ -567,11 +567,12 @@ static cudaError_t launch_index(const void* q_idx, const void* k_idx, float* M, 
   const int64_t nblk = (N + kBlock - 1) / kBlock;
 #define MSA_SCORES(D, SUB, CAP) \
   launch_scores<D, SUB, CAP>(tq, tk, M, idx, kk, N, H_kv, q_start, q_count, nblk, ktab, stream)
-  // k <= 16: one sub-tile per CTA, two CTAs per SM (3.53 -> 3.11 ms at 128K); k <= 32 keeps two
-  // sub-tiles per CTA (its compaction takes 168 registers, too many for two CTAs per SM)
+  // k <= 16 and the block scores alone: one sub-tile per CTA, two CTAs per SM (3.53 -> 3.11 ms
+  // for the fused branch at 128K); k <= 32 keeps two sub-tiles per CTA (its compaction takes 168
+  // registers, too many for two CTAs per SM)
   if (idx != nullptr && kk <= 16) return d_idx == 64 ? MSA_SCORES(64, 1, 32) : MSA_SCORES(32, 1, 32);
   if (idx != nullptr) return d_idx == 64 ? MSA_SCORES(64, 2, 56) : MSA_SCORES(32, 2, 56);
-  return d_idx == 64 ? MSA_SCORES(64, 2, 0) : MSA_SCORES(32, 2, 0);
+  return d_idx == 64 ? MSA_SCORES(64, 1, 0) : MSA_SCORES(32, 1, 0);
 #undef MSA_SCORES
 }
 
