@@ -775,6 +775,16 @@ def e2e_prefill(msa, pcfg, x, bufs, K, W, world):
 
     run(0, W)
     torch.cuda.synchronize()
+    # the host link on its own (outside the timed region): one input copy each way, for reading
+    # the e2e figure against the device time
+    link = {}
+    for name, dst, src in (("h2d_gbs", dev[0]["k"], host["k"]), ("d2h_gbs", o_h, outs[0][0])):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(comp)
+        dst.copy_(src, non_blocking=True)
+        e1.record(comp)
+        torch.cuda.synchronize()
+        link[name] = round(src.numel() * src.element_size() / (e0.elapsed_time(e1) * 1e-3) / 1e9, 1)
     barrier(world)
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record(comp)
@@ -789,7 +799,7 @@ def e2e_prefill(msa, pcfg, x, bufs, K, W, world):
     del dev, host, outs
     return {"value": round(world * N * K / (t * 1e-3), 1), "unit": "tokens/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "ms_per_step": round(t / K, 4), "copies": "pipelined over steps"}
+            "ms_per_step": round(t / K, 4), "copies": "pipelined over steps", **link}
 
 
 def cpu_sample_rows(N, n, seed):
