@@ -20,8 +20,9 @@ constexpr int kMaxSel = 64;        // largest k supported
 constexpr int kMaxKeys = kTileQ * kMaxSel;
 // A block is processed once for the tile ("shared") when at least kSharedMin of the tile's
 // queries selected it; otherwise each of its selections goes to the block-major pass, which
-// packs full 128-row tiles (at 128K: 9.17 ms with 3, 9.60 ms with 2, 9.20 ms with 4).
-constexpr int kSharedMin = 3;
+// packs full 128-row tiles (main branch at 128K: 7.10 ms with 3, 8.00 ms with 2, 6.94-6.95 ms
+// with 4, 5, 6 or 8).
+constexpr int kSharedMin = 4;
 constexpr int kMaxShared = kMaxKeys / 2;   // a shared block holds at least two selections
 
 // Keys per lane for a tile's 16*k selections (a power of two, 32*EPL >= 16*k).

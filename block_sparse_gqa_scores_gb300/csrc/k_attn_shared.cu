@@ -1,5 +1,5 @@
 // Shared-block pass of the sparse main branch («MiniMax-M3：MSA 技术报告速读», section 主分支,
-// eq. O^(h)_i; LSE from section Kernel): the KV blocks that at least kSharedMin (3) queries of a
+// eq. O^(h)_i; LSE from section Kernel): the KV blocks that at least kSharedMin (4) queries of a
 // 16-query tile selected, processed once for the tile on the 5th-generation tensor cores.
 //
 // One CTA = one tile (16 consecutive queries of KV group r).  Its 16*G <= 128 (query, head)
