@@ -38,11 +38,11 @@ sys.path.insert(0, ROOT)
 import gen  # noqa: E402
 
 METRIC = ("MSA prefill tokens/s and decode tokens/s at 128K ctx; % of bf16 TC / HBM roofline")
-# kernels per step: the fused index branch (block scores + top-k); attention per 32768-row chunk:
+# kernels per step: the fused index branch (block scores + top-k); attention per 65536-row chunk:
 # plan, scan, scatter, block-major pass, shared-block pass with the merge (+ one memset); decode:
 # the index-key scan and the tail (selection + attention + merge in one kernel)
 ATTN_LAUNCHES_PER_CHUNK = 5
-ATTN_CHUNK_ROWS = 32768
+ATTN_CHUNK_ROWS = 65536
 DECODE_LAUNCHES = 2
 KERNEL_FILES = {"index_branch": ["k_score.cu"],
                 "main_branch": ["attn_fwd.cu", "k_attn_shared.cu", "k_attn_kvouter.cu",
@@ -463,7 +463,7 @@ def roofline_row(name, ms, bound, work, unit, pk, traffic=None):
 def time_prefill_only(msa, pcfg, bufs, K, pk, world, seed=0):
     """Prefill alone (fused index branch, then the main branch) on a workload of its own, timed
     apart from the step: K calls after 3 warm-up calls, per-call CUDA events around each of the
-    two calls.  The main branch reuses the step's workspace (sized for any N > 32768)."""
+    two calls.  The main branch reuses the step's workspace (sized for any N > 65536)."""
     x = gen.prefill_inputs(pcfg, seed=seed, device="cuda")
     N = pcfg.N
     idx = torch.empty((pcfg.H_kv, N, pcfg.k), dtype=torch.int32, device="cuda")

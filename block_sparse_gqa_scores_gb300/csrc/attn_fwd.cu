@@ -1,7 +1,7 @@
 // Main branch of prefill («MiniMax-M3：MSA 技术报告速读», section 主分支, eq. O^(h)_i): the
 // launch sequence over query chunks and its workspace.
 //
-// Per chunk of at most 32768 query rows:
+// Per chunk of at most 65536 query rows:
 //   plan -> scan -> scatter                  bucket the private selections (attn_tile.cuh) and
 //                                            record each tile's shared blocks
 //   k_attn_kvouter                           block-major tcgen05 pass over private selections
@@ -26,9 +26,11 @@ namespace {
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-// query rows per pass: bounds the workspace; larger chunks fill the (group, block) buckets of
-// the block-major pass better (32768 rows: 9.59 ms at 128K against 10.01 ms with 16384)
-constexpr int64_t kChunkRows = 32768;
+// query rows per pass: bounds the workspace (about 8.8 GB per set at the 128K shape); larger
+// chunks fill the (group, block) buckets of the block-major pass better and leave fewer passes
+// (main branch at 128K: 6.66 ms with 65536 rows, 6.94 ms with 32768, 6.74 ms with one chunk of
+// 131072)
+constexpr int64_t kChunkRows = 65536;
 constexpr int kKvoCtasPerSm = 1;         // block-major pass: persistent, one CTA per SM (TMEM)
 
 struct AttnWs {

@@ -97,9 +97,9 @@ msa_status_t msa_index_select(const void *q_idx, const void *k_idx, int32_t *idx
                               int64_t q_count, void *stream);
 
 /* Workspace bytes msa_sparse_attn_fwd needs for these sizes (0 for invalid sizes).  It grows
- * with min(N, 32768) * H_q * k * d_h (the private-block partials of one 32768-row query chunk),
- * twice over when N > 32768 (two chunks in flight): 4.39 GB at H_q=32, k=16, d_h=128 for
- * N = 32768, 8.78 GB for any larger N. */
+ * with min(N, 65536) * H_q * k * d_h (the private-block partials of one 65536-row query chunk),
+ * twice over when N > 65536 (two chunks in flight): 4.41 GB at H_q=32, k=16, d_h=128 for
+ * N = 32768, 8.83 GB for N = 65536, 17.65 GB for any larger N. */
 size_t msa_sparse_attn_fwd_workspace(int64_t N, int H_q, int H_kv, int d_h, int k);
 
 /* Sparse main branch (eq. O^(h)_i of section 主分支, LSE of section Kernel).  For every row i
@@ -116,7 +116,7 @@ size_t msa_sparse_attn_fwd_workspace(int64_t N, int H_q, int H_kv, int d_h, int 
  *        per workspace).  Smaller: MSA_ERR_WORKSPACE.  N > 2^21: MSA_ERR_UNSUPPORTED.
  * Results do not depend on the launch order of work inside the call: the private-block
  * partials are merged per row in slot order, with no atomic updates of results.
- * With more than one 32768-row chunk, part of the work runs on a stream the library creates
+ * With more than one 65536-row chunk, part of the work runs on a stream the library creates
  * once per device, ordered against `stream` by events; all of it has completed when `stream`
  * has passed the call. */
 msa_status_t msa_sparse_attn_fwd(const void *q, const void *k, const void *v, const int32_t *idx,
