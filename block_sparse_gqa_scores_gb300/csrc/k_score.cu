@@ -5,10 +5,9 @@
 // One dense GEMM  [N*H_kv x d_idx] . [d_idx x N]  restricted to the causal triangle:
 //   * rows are (query i, group r) pairs, i.e. Q_idx viewed as [N*H_kv, d_idx]; 128 consecutive
 //     rows (128/H_kv queries x H_kv groups) form one UMMA M=128 sub-tile, and SUB sub-tiles
-//     share every K_idx tile, so the shared index key is read once for all groups.  The plain
-//     block scores and the select epilogue at k <= 16 run one sub-tile per CTA and two CTAs per
-//     SM, so one CTA's MMAs run while the other's epilogue drains its accumulators; the k <= 32
-//     select epilogue runs two sub-tiles in one CTA per SM.
+//     share every K_idx tile, so the shared index key is read once for all groups.  Every
+//     variant dispatched runs one sub-tile per CTA and two CTAs per SM, so one CTA's MMAs run
+//     while the other's epilogue drains its accumulators.
 //   * K_idx tiles of 128 keys (two 64-token blocks) stream through a TMA ring (3 to 6 stages).
 //   * one thread issues tcgen05.mma (bf16 x bf16 -> fp32) into a double-buffered TMEM
 //     accumulator; the next tile's MMA overlaps the epilogue of the previous one.
@@ -66,11 +65,12 @@ struct ScoreSmem {
   static constexpr int kCapStride = CAP + 1;
   static constexpr int kABytes = kRows * D_IDX * 2;
   static constexpr int kBBytes = kKeys * D_IDX * 2;
-  // K_idx ring depth: six stages keep about two microseconds of key tiles in flight; the
-  // k <= 32 candidate buffers (CAP = 56) leave room for four.  One sub-tile (SUB = 1: 128 rows,
-  // 256 TMEM columns, about 107 KB) runs two CTAs per SM with three stages each: one CTA's MMAs
-  // run while the other's epilogue drains its accumulators.
-  static constexpr int kStages = SUB == 1 ? 3 : (SELECT && CAP > 32 ? 4 : 6);
+  // K_idx ring depth: six stages keep about two microseconds of key tiles in flight with two
+  // sub-tiles per CTA (four beside the k <= 32 candidate buffers).  One sub-tile (SUB = 1: 128
+  // rows, 256 TMEM columns, about 107 KB) runs two CTAs per SM with three stages each (two beside
+  // the k <= 32 candidate buffers): one CTA's MMAs run while the other's epilogue drains its
+  // accumulators.
+  static constexpr int kStages = SUB == 1 ? (CAP > 32 ? 2 : 3) : (SELECT && CAP > 32 ? 4 : 6);
   static constexpr int kCtasPerSm = SUB == 1 ? 2 : 1;
   static constexpr int kEpiWarps = 4 * SUB;
   static constexpr int kStageFloats = 32 * 33;        // 32 rows x 32 blocks, padded
@@ -567,11 +567,11 @@ static cudaError_t launch_index(const void* q_idx, const void* k_idx, float* M, 
   const int64_t nblk = (N + kBlock - 1) / kBlock;
 #define MSA_SCORES(D, SUB, CAP) \
   launch_scores<D, SUB, CAP>(tq, tk, M, idx, kk, N, H_kv, q_start, q_count, nblk, ktab, stream)
-  // k <= 16 and the block scores alone: one sub-tile per CTA, two CTAs per SM (3.53 -> 3.11 ms
-  // for the fused branch at 128K); k <= 32 keeps two sub-tiles per CTA (its compaction takes 168
-  // registers, too many for two CTAs per SM)
+  // one sub-tile per CTA, two CTAs per SM (fused branch at 128K: 3.53 -> 3.11 ms at k = 16,
+  // 4.51 -> 3.63 ms at k = 32, whose 168-register compaction fits two 192-thread CTAs with a
+  // two-stage key ring)
   if (idx != nullptr && kk <= 16) return d_idx == 64 ? MSA_SCORES(64, 1, 32) : MSA_SCORES(32, 1, 32);
-  if (idx != nullptr) return d_idx == 64 ? MSA_SCORES(64, 2, 56) : MSA_SCORES(32, 2, 56);
+  if (idx != nullptr) return d_idx == 64 ? MSA_SCORES(64, 1, 56) : MSA_SCORES(32, 1, 56);
   return d_idx == 64 ? MSA_SCORES(64, 1, 0) : MSA_SCORES(32, 1, 0);
 #undef MSA_SCORES
 }
