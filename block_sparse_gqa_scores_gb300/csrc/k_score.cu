@@ -590,7 +590,8 @@ cudaError_t launch_index_select(const void* q_idx, const void* k_idx, int32_t* i
                       stream);
 }
 
-// the most query rows one CTA covers, over every instantiation above (two sub-tiles)
+// a bound on the query rows one CTA covers (two sub-tiles' worth; every variant dispatched
+// above runs one), used to align variable-length sequences
 int index_rows_per_cta(int H_kv) { return 2 * (kRows / H_kv); }
 
 cudaError_t set_score_wait_limit(unsigned long long ns) {
