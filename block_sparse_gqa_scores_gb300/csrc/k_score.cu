@@ -57,7 +57,7 @@ constexpr int kRows = 128;     // UMMA M: rows per sub-tile
 constexpr int kKeys = 128;     // UMMA N: keys per tile
 constexpr int kGroupBlocks = 32;   // blocks staged per row before a store
 constexpr int kTilesPerGroup = kGroupBlocks / (kKeys / kBlock);
-// SELECT: candidate slots per row, CAP = 32 for k <= 16 and 56 for k <= 32 (k - 1 kept after
+// SELECT: candidate slots per row, CAP = 24 for k <= 16 and 56 for k <= 32 (k - 1 kept after
 // each compaction); the row stride CAP + 1 is odd, so the 32 lanes' rows fall in distinct banks.
 template <int D_IDX, int SUB, int CAP = 0>
 struct ScoreSmem {
@@ -67,10 +67,13 @@ struct ScoreSmem {
   static constexpr int kBBytes = kKeys * D_IDX * 2;
   // K_idx ring depth: six stages keep about two microseconds of key tiles in flight with two
   // sub-tiles per CTA (four beside the k <= 32 candidate buffers).  One sub-tile (SUB = 1: 128
-  // rows, 256 TMEM columns, about 107 KB) runs two CTAs per SM with three stages each (two beside
-  // the k <= 32 candidate buffers): one CTA's MMAs run while the other's epilogue drains its
-  // accumulators.
-  static constexpr int kStages = SUB == 1 ? (CAP > 32 ? 2 : 3) : (SELECT && CAP > 32 ? 4 : 6);
+  // rows, 256 TMEM columns, about 110 KB) runs two CTAs per SM: one CTA's MMAs run while the
+  // other's epilogue drains its accumulators.  There the ring has four stages beside the k <= 16
+  // buffers of 24 candidates and a 4-tile maxima ring (3.108 -> 3.088 ms at 128K against three
+  // stages with 32 candidates), three beside the plain block scores' staging, two beside the
+  // k <= 32 buffers.
+  static constexpr int kStages =
+      SUB == 1 ? (CAP > 32 ? 2 : (CAP > 24 ? 3 : 4)) : (SELECT && CAP > 32 ? 4 : 6);
   static constexpr int kCtasPerSm = SUB == 1 ? 2 : 1;
   static constexpr int kEpiWarps = 4 * SUB;
   static constexpr int kStageFloats = 32 * 33;        // 32 rows x 32 blocks, padded
@@ -80,11 +83,11 @@ struct ScoreSmem {
   // SELECT: candidate scores of every epilogue row (row stride kCapStride), then their blocks
   static constexpr int kStageBytes =
       SELECT ? kEpiWarps * 32 * kCapStride * 8 : kEpiWarps * kStageFloats * 4;
-  // SELECT with CAP = 32: each epilogue warp hands its rows' block maxima to a selection warp of
+  // SELECT with CAP <= 32: each epilogue warp hands its rows' block maxima to a selection warp of
   // its own through a ring of kRing key tiles (32 rows x 2 blocks, 8 bytes per row), so the
   // candidate bookkeeping never holds a TMEM accumulator.  CAP = 56 keeps the bookkeeping in the
   // epilogue warps (its compaction needs more registers than twice the threads leave).
-  static constexpr int kRing = SELECT && CAP <= 32 ? 8 : 0;
+  static constexpr int kRing = SELECT && CAP <= 32 ? (CAP <= 24 ? 4 : 8) : 0;
   static constexpr int kSelWarps = kRing > 0 ? kEpiWarps : 0;
   static constexpr int kOffRing = kOffStage + kStageBytes;
   static constexpr int kOffBar = kOffRing + kSelWarps * kRing * 32 * 8;
@@ -341,7 +344,7 @@ __global__ void __launch_bounds__(ScoreSmem<D_IDX, SUB, CAP>::kThreads,
       mbar_wait(done_bar, 0, &g_score_status);
     }
   } else if (warp >= 2 + L::kEpiWarps) {
-    // ------------------------------------------------- selection (SELECT, CAP = 32)
+    // ----------------------------------------------- selection (SELECT, CAP <= 32)
     // selection warp e takes the rows of epilogue warp e (warp 2 + e) from the ring
     if constexpr (L::kRing > 0) {
       const int e = warp - 2 - L::kEpiWarps;
@@ -570,7 +573,7 @@ static cudaError_t launch_index(const void* q_idx, const void* k_idx, float* M, 
   // one sub-tile per CTA, two CTAs per SM (fused branch at 128K: 3.53 -> 3.11 ms at k = 16,
   // 4.51 -> 3.63 ms at k = 32, whose 168-register compaction fits two 192-thread CTAs with a
   // two-stage key ring)
-  if (idx != nullptr && kk <= 16) return d_idx == 64 ? MSA_SCORES(64, 1, 32) : MSA_SCORES(32, 1, 32);
+  if (idx != nullptr && kk <= 16) return d_idx == 64 ? MSA_SCORES(64, 1, 24) : MSA_SCORES(32, 1, 24);
   if (idx != nullptr) return d_idx == 64 ? MSA_SCORES(64, 1, 56) : MSA_SCORES(32, 1, 56);
   return d_idx == 64 ? MSA_SCORES(64, 1, 0) : MSA_SCORES(32, 1, 0);
 #undef MSA_SCORES
