@@ -66,3 +66,38 @@ def test_roofline_row_peaks():
     assert t["frac_of_sustained"] == 0.625 and "burst" in t["peak_source"]
     h = bench.roofline_row("decode", 0.1, "hbm", 3.0e8, "GB/s", pk)
     assert h["achieved"] == 3000.0 and h["frac"] == 0.5 and "frac_of_sustained" not in h
+
+
+def test_write_traffic_adds_per_kernel_captures(tmp_path, monkeypatch):
+    """One capture per kernel of the same step add up to the step's figure; ncu's own messages
+    and the program's output in an ncu stdout CSV are skipped; a capture label that no row uses
+    any more is dropped from the notes."""
+    bench = load_bench()
+    out = tmp_path / "traffic.txt"
+    monkeypatch.setattr(bench, "TRAFFIC_FILE", str(out))
+    hdr = '"ID","Kernel Name","Metric Name","Metric Unit","Metric Value"\n'
+
+    def capture(path, name, mb_read, mb_write):
+        path.write_text(
+            '{"metric": "program output on stdout"}\n==PROF== Connected to process 1\n' + hdr +
+            '"0","%s","gpu__time_duration.sum","us","10"\n' % name +
+            '"0","%s","dram__bytes_read.sum","Mbyte","%s"\n' % (name, mb_read) +
+            '"0","%s","dram__bytes_write.sum","Mbyte","%s"\n' % (name, mb_write))
+
+    paths = []
+    for n, (name, r, w) in enumerate([("void k_index_block_scores<64, 1, 24>(CUtensorMap_st)", 20, 1),
+                                      ("void k_attn_kvouter<128, 8>(CUtensorMap_st)", 900, 1500),
+                                      ("void k_attn_shared<128>(CUtensorMap_st)", 2000, 300),
+                                      ("k_attn_plan(const int *, long)", 10, 5)]):
+        p = tmp_path / ("c%d.csv" % n)
+        capture(p, name, r, w)
+        paths.append(str(p))
+    bench.write_traffic(",".join(paths), "per-kernel captures", scale=4.0, tag="C")
+    rows = {l.split()[0]: l.split() for l in out.read_text().splitlines()
+            if l and not l.startswith("#")}
+    assert int(rows["index_branch"][1]) == 4 * 21_000_000
+    assert int(rows["main_branch"][1]) == 4 * (2_400_000_000 + 2_300_000_000 + 15_000_000)
+    # a second capture of the same rows under another label replaces the first label's note
+    bench.write_traffic(",".join(paths), "again", scale=4.0, tag="E")
+    text = out.read_text()
+    assert "# capture E: again" in text and "# capture C:" not in text
